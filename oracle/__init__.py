@@ -1,0 +1,233 @@
+"""fp64 CPU oracle for isolated sequence packing -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does; the two
+share no code.  ``oracle.c`` holds the segment-by-segment fp64 definitions
+(cu_seqlens validation, positions, labels, work lists, RoPE, attention forward
+and backward); ``brute.py`` is an independent whole-pack numpy restatement used
+to pin it.  Every function cites the page and section it follows in its C
+source.
+
+Pins (see tests/test_oracle_pins.py): the pages' nine-token example, the
+pre-shifted label example, the 10-versus-3.25 contamination counterexample,
+closed forms at Q = 0, packed == per-sample, change-A-keeps-B, brute force
+(numpy, full T x T mask), torch CPU fp64 SDPA with a boolean block mask, RoPE
+shift invariance and closed-form angles, and finite differences for the
+backward pass.  No oracle function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERR_CU_FIRST, ERR_CU_ORDER, ERR_CU_TOTAL, ERR_MAXLEN, ERR_ARG = 1, 2, 4, 8, 16
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (-O2, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.run(
+            ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", tmp, _SRC, "-lm"],
+            check=True,
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            lib.orc_validate_cu.argtypes = [P, i32, i32, i32]
+            lib.orc_validate_cu.restype = ctypes.c_int
+            lib.orc_positions_labels.argtypes = [P, i32, P, P, P, P]
+            lib.orc_positions_labels.restype = None
+            for f in (lib.orc_worklist_fwd, lib.orc_worklist_bwd):
+                f.argtypes = [P, i32, i32, i32, P, i64]
+                f.restype = i64
+            lib.orc_rope_rows.argtypes = [P, P, i64, i32, f64, P]
+            lib.orc_rope_rows.restype = None
+            lib.orc_attn_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int, P, P]
+            lib.orc_attn_fwd.restype = None
+            lib.orc_attn_fwd_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int,
+                                              P, P, i64, P, P]
+            lib.orc_attn_fwd_rows.restype = None
+            lib.orc_attn_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int,
+                                         P, P, P]
+            lib.orc_attn_bwd.restype = None
+            lib.orc_attn_bwd_seg_heads.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, f64,
+                                                   ctypes.c_int, P, P, i64, P, P, P]
+            lib.orc_attn_bwd_seg_heads.restype = None
+            lib.orc_num_threads.argtypes = []
+            lib.orc_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def bf16_bits(x) -> np.ndarray:
+    """Raw uint16 bit patterns of a bf16 torch tensor (or pass-through for uint16 arrays)."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return np.ascontiguousarray(x)
+    import torch
+
+    assert x.dtype == torch.bfloat16
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float64 (exact)."""
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def num_threads() -> int:
+    return int(_load().orc_num_threads())
+
+
+def validate_cu(cu, total: int, max_seqlen: int) -> int:
+    cu = _c(cu, np.int32)
+    return int(_load().orc_validate_cu(_ptr(cu), len(cu) - 1, int(total), int(max_seqlen)))
+
+
+def positions_labels(cu, tokens, seg_ignore=None):
+    cu = _c(cu, np.int32)
+    tokens = _c(tokens, np.int64)
+    nseg = len(cu) - 1
+    total = int(cu[-1])
+    assert tokens.shape[0] == total
+    ign = _c(seg_ignore, np.uint8) if seg_ignore is not None else None
+    pos = np.zeros(total, np.int32)
+    lab = np.zeros(total, np.int64)
+    _load().orc_positions_labels(_ptr(cu), nseg, _ptr(tokens), _ptr(ign), _ptr(pos), _ptr(lab))
+    return pos, lab
+
+
+def _worklist(fn, cu, BM, BN):
+    cu = _c(cu, np.int32)
+    nseg = len(cu) - 1
+    lens = np.diff(cu.astype(np.int64))
+    cap = int(np.sum((lens + min(BM, BN) - 1) // min(BM, BN))) + 1
+    items = np.zeros((cap, 4), np.int32)
+    n = fn(_ptr(cu), nseg, int(BM), int(BN), _ptr(items), cap)
+    assert n >= 0
+    return items[:n].copy()
+
+
+def worklist_fwd(cu, BM: int = 128, BN: int = 128) -> np.ndarray:
+    """Forward items [n, 4] = {seg, q_tile, kv_lo, kv_hi} (oracle.c: orc_worklist_fwd)."""
+    return _worklist(_load().orc_worklist_fwd, cu, BM, BN)
+
+
+def worklist_bwd(cu, BM: int = 128, BN: int = 128) -> np.ndarray:
+    """Backward items [n, 4] = {seg, kv_tile, q_lo, q_hi} (oracle.c: orc_worklist_bwd)."""
+    return _worklist(_load().orc_worklist_bwd, cu, BM, BN)
+
+
+def rope_rows(x, pos, theta: float = 10000.0) -> np.ndarray:
+    x = _c(x, np.float64)
+    n, d = x.shape
+    pos = _c(pos, np.int64)
+    out = np.zeros_like(x)
+    _load().orc_rope_rows(_ptr(x), _ptr(pos), n, d, float(theta), _ptr(out))
+    return out
+
+
+def attn_fwd(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True):
+    """Exact per-segment causal attention in fp64.  q/k/v: bf16 tensors or uint16 bit arrays
+    [total, H, d].  Returns (o [total, H, d] f64, lse [H, total] f64, natural log)."""
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    total, H, d = qb.shape
+    cu = _c(cu, np.int32)
+    o = np.zeros((total, H, d), np.float64)
+    lse = np.zeros((H, total), np.float64)
+    _load().orc_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, d,
+                         float(scale), float(theta), int(bool(contract)), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def attn_fwd_rows(q, k, v, cu, rows, heads, scale: float = 0.0, theta: float = 10000.0,
+                  contract: bool = True):
+    """Forward for selected (token row, head) pairs: returns (o [n, d], lse [n])."""
+    qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    total, H, d = qb.shape
+    cu = _c(cu, np.int32)
+    rows = _c(rows, np.int64)
+    heads = _c(heads, np.int32)
+    n = rows.shape[0]
+    o = np.zeros((n, d), np.float64)
+    lse = np.zeros(n, np.float64)
+    _load().orc_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, d,
+                              float(scale), float(theta), int(bool(contract)), _ptr(rows),
+                              _ptr(heads), n, _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def attn_fwd_f64(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0):
+    """Exact-mode forward on float64 inputs [total, H, d] (finite-difference tests)."""
+    q, k, v = (_c(x, np.float64) for x in (q, k, v))
+    total, H, d = q.shape
+    cu = _c(cu, np.int32)
+    o = np.zeros((total, H, d), np.float64)
+    lse = np.zeros((H, total), np.float64)
+    _load().orc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, d,
+                         float(scale), float(theta), -1, _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def attn_bwd_f64(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0):
+    """Exact-mode gradients on float64 inputs (finite-difference tests)."""
+    g, q, k, v = (_c(x, np.float64) for x in (dout, q, k, v))
+    total, H, d = q.shape
+    cu = _c(cu, np.int32)
+    dq = np.zeros((total, H, d), np.float64)
+    dk = np.zeros_like(dq)
+    dv = np.zeros_like(dq)
+    _load().orc_attn_bwd(_ptr(g), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, d,
+                         float(scale), float(theta), -1, _ptr(dq), _ptr(dk), _ptr(dv))
+    return dq, dk, dv
+
+
+def attn_bwd(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
+             seg_heads=None):
+    """Gradients (dq, dk, dv) [total, H, d] f64 of sum(O * dO).  With ``seg_heads`` (a list of
+    (segment, head) pairs) only those segment-heads are computed; other entries stay 0."""
+    gb, qb, kb, vb = bf16_bits(dout), bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    total, H, d = qb.shape
+    cu = _c(cu, np.int32)
+    dq = np.zeros((total, H, d), np.float64)
+    dk = np.zeros_like(dq)
+    dv = np.zeros_like(dq)
+    lib = _load()
+    if seg_heads is None:
+        lib.orc_attn_bwd(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, d,
+                         float(scale), float(theta), int(bool(contract)), _ptr(dq), _ptr(dk), _ptr(dv))
+    else:
+        sh = np.asarray(seg_heads, np.int32).reshape(-1, 2)
+        segs = np.ascontiguousarray(sh[:, 0])
+        heads = np.ascontiguousarray(sh[:, 1])
+        lib.orc_attn_bwd_seg_heads(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1,
+                                   total, H, d, float(scale), float(theta), int(bool(contract)),
+                                   _ptr(segs), _ptr(heads), sh.shape[0], _ptr(dq), _ptr(dk), _ptr(dv))
+    return dq, dk, dv

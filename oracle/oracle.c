@@ -1,0 +1,491 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU oracle for isolated sequence packing.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it.  It shares no code, header, table or helper with the
+ * CUDA library; it is written from the pages' statement of the method.
+ *
+ * Sources (page title, section):
+ *  [CSTAR] "Sequence packing and variable-length attention" (charlestar.github.io)
+ *      - "Nine tokens together keep three sample identities": cu_seqlens as a
+ *        prefix sum, segment r = [cu_r, cu_{r+1}), local position p_i = i - cu_r,
+ *        and the validity contract (cu[0]==0, strictly increasing,
+ *        cu[-1]==total, max_seqlen == largest difference, int32 range).
+ *      - "EOS is content; isolation happens before softmax":
+ *        allow(i,j) = (s_i == s_j) and (p_j <= p_i); additive mask M (0 / -inf)
+ *        added to QK^T/sqrt(d) before the softmax, O = softmax(QK^T/sqrt(d)+M) V.
+ *      - "Positions are reset per segment; the pure-RoPE argument": fixed-frequency
+ *        RoPE rotation R(p) with (R(m+c)q)^T (R(n+c)k) = q^T R(n-m) k.
+ *      - "After isolation one cross-boundary prediction pair remains": the
+ *        pre-shifted label contract (ignore index -100 on each segment's last logit).
+ *  [M020] "Length grouping, de-padding and packing" (xuujii ai-infra-kb M020),
+ *      section 06 "positions and labels": targets [12,13,ignore,22,ignore].
+ *  [COMPASS] "Sequence Packing" (brenchcc llm-compass), "Implementation notes":
+ *      padding tail as its own segment whose labels are all -100.
+ *
+ * Everything is computed one segment at a time; there is no tiling, fusion or
+ * reordering beyond the definitions above.  Inputs are the raw bf16 bit
+ * patterns of q/k/v/dO (exactly representable in fp64); all arithmetic is fp64.
+ *
+ * "Contract" mode (contract == 1) rounds the RoPE-rotated q', k' to bf16
+ * (round to nearest, ties to even) before the contraction, because the tensor
+ * cores consume bf16 operands; the pages fix no precision for this step, and
+ * exact mode (contract == 0) keeps them in fp64.  Gradients pass through that
+ * rounding unchanged (straight-through).  contract == -1 selects exact mode
+ * with fp64 input arrays instead of bf16 bit patterns (finite-difference tests).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_ERR_CU_FIRST 1     /* cu[0] != 0 */
+#define ORC_ERR_CU_ORDER 2     /* some segment has length <= 0 */
+#define ORC_ERR_CU_TOTAL 4     /* cu[nseg] != total */
+#define ORC_ERR_MAXLEN 8       /* max_seqlen != largest segment length */
+#define ORC_ERR_ARG 16         /* nseg < 1 or total < 1 */
+
+/* ---------------------------------------------------------------- helpers */
+
+/* bf16 bit pattern -> double.  A bf16 value is the upper 16 bits of an IEEE
+ * binary32 value, so widening is exact. */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16 value (8 significant bits, ties to even),
+ * returned as a double.  Written from the definition: scale the significand to
+ * [128, 256), round to an integer with ties to even, scale back.  Values in
+ * the bf16 subnormal range are rounded at the fixed 2^-133 quantum. */
+static double round_to_bf16(double x) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    double m = frexp(x, &e);          /* x = m * 2^e, 0.5 <= |m| < 1 */
+    int shift = 8;
+    if (e - 1 < -126) shift = 8 - ((-126) - (e - 1));   /* subnormal quantum */
+    if (shift < 0) return 0.0 * x;
+    double s = ldexp(m, shift);
+    double r = floor(s);
+    double frac = s - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    return ldexp(r, e - shift);
+}
+
+/* RoPE angle for local position p and rotation pair j of a head of size d:
+ * phi = p * theta^(-2j/d)  (fixed frequencies, rotate-half pairing). */
+static double rope_angle(int64_t p, int j, int d, double theta) {
+    return (double)p * pow(theta, -2.0 * (double)j / (double)d);
+}
+
+/* Rotate one head vector x[0..d) by R(p), rotate-half pairing
+ * (x_j, x_{j+d/2}):  x'_j = x_j cos - x_{j+d/2} sin,
+ *                    x'_{j+d/2} = x_{j+d/2} cos + x_j sin. */
+static void rope_rotate(const double* x, double* out, int64_t p, int d, double theta) {
+    int half = d / 2;
+    for (int j = 0; j < half; ++j) {
+        double phi = rope_angle(p, j, d, theta);
+        double c = cos(phi), s = sin(phi);
+        double a = x[j], b = x[j + half];
+        out[j] = a * c - b * s;
+        out[j + half] = b * c + a * s;
+    }
+}
+
+/* Transpose rotation R(p)^T = R(-p), used to carry gradients back through RoPE. */
+static void rope_rotate_transpose(const double* g, double* out, int64_t p, int d, double theta) {
+    int half = d / 2;
+    for (int j = 0; j < half; ++j) {
+        double phi = rope_angle(p, j, d, theta);
+        double c = cos(phi), s = sin(phi);
+        double a = g[j], b = g[j + half];
+        out[j] = a * c + b * s;
+        out[j + half] = b * c - a * s;
+    }
+}
+
+/* ---------------------------------------------------------------- cu_seqlens */
+
+/* Validity contract for cu_seqlens ([CSTAR], "Nine tokens together ..."). */
+int orc_validate_cu(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen) {
+    if (nseg < 1 || total < 1) return ORC_ERR_ARG;
+    int err = 0;
+    if (cu[0] != 0) err |= ORC_ERR_CU_FIRST;
+    int64_t longest = 0;
+    for (int32_t r = 0; r < nseg; ++r) {
+        int64_t len = (int64_t)cu[r + 1] - (int64_t)cu[r];
+        if (len <= 0) err |= ORC_ERR_CU_ORDER;
+        if (len > longest) longest = len;
+    }
+    if (cu[nseg] != total) err |= ORC_ERR_CU_TOTAL;
+    if (longest != max_seqlen) err |= ORC_ERR_MAXLEN;
+    return err;
+}
+
+/* Segment index of token i: the r with cu[r] <= i < cu[r+1], found by a
+ * plain linear scan (the pages use searchsorted; the answer is the same). */
+static int32_t segment_of(const int32_t* cu, int32_t nseg, int64_t i) {
+    for (int32_t r = 0; r < nseg; ++r)
+        if (i >= cu[r] && i < cu[r + 1]) return r;
+    return -1;
+}
+
+/* Local positions p_i = i - cu_r and pre-shifted next-token labels:
+ * label_i = token_{i+1} when i+1 is still inside segment r, else -100; every
+ * label of an ignored segment (a padding tail) is -100. */
+void orc_positions_labels(const int32_t* cu, int32_t nseg, const int64_t* tokens,
+                          const uint8_t* seg_ignore, int32_t* pos, int64_t* labels) {
+    int64_t total = cu[nseg];
+    for (int64_t i = 0; i < total; ++i) {
+        int32_t r = segment_of(cu, nseg, i);
+        if (r < 0) { pos[i] = -1; labels[i] = -100; continue; }   /* invalid cu */
+        pos[i] = (int32_t)(i - cu[r]);
+        int ignored = seg_ignore != NULL && seg_ignore[r] != 0;
+        if (!ignored && i + 1 < cu[r + 1])
+            labels[i] = tokens[i + 1];
+        else
+            labels[i] = -100;
+    }
+}
+
+/* ---------------------------------------------------------------- work lists */
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+/* Stable order of segments by descending tile count n_r = ceil(L_r / tile).
+ * Plain insertion sort: O(nseg^2) worst case, fine for an oracle. */
+static void order_segments(const int32_t* cu, int32_t nseg, int32_t tile, int32_t* order) {
+    for (int32_t r = 0; r < nseg; ++r) order[r] = r;
+    for (int32_t a = 1; a < nseg; ++a) {
+        int32_t x = order[a];
+        int64_t nx = ceil_div((int64_t)cu[x + 1] - cu[x], tile);
+        int32_t b = a - 1;
+        while (b >= 0) {
+            int32_t y = order[b];
+            int64_t ny = ceil_div((int64_t)cu[y + 1] - cu[y], tile);
+            if (ny >= nx) break;        /* keep equal keys in index order */
+            order[b + 1] = y;
+            --b;
+        }
+        order[b + 1] = x;
+    }
+}
+
+/* Forward work list: one item {seg, q_tile, kv_lo, kv_hi} per q tile of BM
+ * rows of every segment.  Query row p (local) may see key rows 0..p of its own
+ * segment only, so q tile t needs key tiles [0, ceil(min(L, (t+1)BM) / BN)).
+ * No item refers to another segment, and no key tile lies wholly above the
+ * diagonal.  Order: segments by descending q-tile count (ties by index), and
+ * inside a segment q tiles from last to first (longest key range first).
+ * Returns the item count, or -1 if cap is too small. */
+int64_t orc_worklist_fwd(const int32_t* cu, int32_t nseg, int32_t BM, int32_t BN,
+                         int32_t* items, int64_t cap) {
+    int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)nseg);
+    order_segments(cu, nseg, BM, order);
+    int64_t n = 0;
+    for (int32_t k = 0; k < nseg; ++k) {
+        int32_t r = order[k];
+        int64_t L = (int64_t)cu[r + 1] - cu[r];
+        int64_t nq = ceil_div(L, BM);
+        for (int64_t t = nq - 1; t >= 0; --t) {
+            if (n >= cap) { free(order); return -1; }
+            int64_t last_row = (t + 1) * BM < L ? (t + 1) * BM : L;
+            items[4 * n + 0] = r;
+            items[4 * n + 1] = (int32_t)t;
+            items[4 * n + 2] = 0;
+            items[4 * n + 3] = (int32_t)ceil_div(last_row, BN);
+            ++n;
+        }
+    }
+    free(order);
+    return n;
+}
+
+/* Backward work list: one item {seg, kv_tile, q_lo, q_hi} per key tile of BN
+ * rows.  Key row j (local) is seen by query rows j..L-1, so key tile t is
+ * needed by q tiles [floor(t*BN / BM), ceil(L / BM)).  Order: segments by
+ * descending key-tile count (ties by index), key tiles first to last. */
+int64_t orc_worklist_bwd(const int32_t* cu, int32_t nseg, int32_t BM, int32_t BN,
+                         int32_t* items, int64_t cap) {
+    int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)nseg);
+    order_segments(cu, nseg, BN, order);
+    int64_t n = 0;
+    for (int32_t k = 0; k < nseg; ++k) {
+        int32_t r = order[k];
+        int64_t L = (int64_t)cu[r + 1] - cu[r];
+        int64_t nk = ceil_div(L, BN);
+        for (int64_t t = 0; t < nk; ++t) {
+            if (n >= cap) { free(order); return -1; }
+            items[4 * n + 0] = r;
+            items[4 * n + 1] = (int32_t)t;
+            items[4 * n + 2] = (int32_t)((t * BN) / BM);
+            items[4 * n + 3] = (int32_t)ceil_div(L, BM);
+            ++n;
+        }
+    }
+    free(order);
+    return n;
+}
+
+/* ---------------------------------------------------------------- RoPE */
+
+/* Apply R(pos[n]) to rows of x ([n][d] fp64).  Exposed so tests can probe the
+ * rotation at arbitrary positions (shift invariance, R(0) = I, ...). */
+void orc_rope_rows(const double* x, const int64_t* pos, int64_t n, int32_t d,
+                   double theta, double* out) {
+    for (int64_t i = 0; i < n; ++i) rope_rotate(x + i * d, out + i * d, pos[i], d, theta);
+}
+
+/* ---------------------------------------------------------------- attention */
+
+typedef struct {
+    const void *q, *k, *v, *dout;       /* [total][H][d]: bf16 bits, or fp64 when f64_inputs */
+    int f64_inputs;
+    const int32_t* cu;
+    int32_t nseg, total, H, d;
+    double scale, theta;                 /* theta == 0: no RoPE */
+    int contract;
+} orc_problem;
+
+/* q' (or k') for token row i of head h: widen, rotate by its local position,
+ * and round to bf16 in contract mode. */
+/* Element c of token row i, head h of an input tensor, widened to fp64. */
+static double input_elem(const orc_problem* P, const void* x, int64_t i, int32_t h, int c) {
+    size_t off = ((size_t)i * P->H + h) * P->d + c;
+    if (P->f64_inputs) return ((const double*)x)[off];
+    return bf16_bits_to_double(((const uint16_t*)x)[off]);
+}
+
+static void load_rotated(const orc_problem* P, const void* x, int64_t i, int32_t h,
+                         int64_t p, double* out) {
+    int d = P->d;
+    double* tmp = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int c = 0; c < d; ++c) tmp[c] = input_elem(P, x, i, h, c);
+    if (P->theta != 0.0) {
+        rope_rotate(tmp, out, p, d, P->theta);
+        if (P->contract)
+            for (int c = 0; c < d; ++c) out[c] = round_to_bf16(out[c]);
+    } else {
+        memcpy(out, tmp, sizeof(double) * (size_t)d);
+    }
+    free(tmp);
+}
+
+static void load_plain(const orc_problem* P, const void* x, int64_t i, int32_t h, double* out) {
+    for (int c = 0; c < P->d; ++c) out[c] = input_elem(P, x, i, h, c);
+}
+
+/* One segment r, one head h: Q', K', V (and dO) of the segment in fp64. */
+typedef struct {
+    int64_t L, base;
+    double *q, *k, *v, *g;  /* [L][d] each */
+} seg_head;
+
+static void seg_head_load(const orc_problem* P, int32_t r, int32_t h, int want_grad, seg_head* S) {
+    int d = P->d;
+    S->base = P->cu[r];
+    S->L = (int64_t)P->cu[r + 1] - P->cu[r];
+    size_t n = (size_t)S->L * d;
+    S->q = (double*)malloc(sizeof(double) * n);
+    S->k = (double*)malloc(sizeof(double) * n);
+    S->v = (double*)malloc(sizeof(double) * n);
+    S->g = want_grad ? (double*)malloc(sizeof(double) * n) : NULL;
+    for (int64_t p = 0; p < S->L; ++p) {
+        int64_t i = S->base + p;
+        load_rotated(P, P->q, i, h, p, S->q + p * d);
+        load_rotated(P, P->k, i, h, p, S->k + p * d);
+        load_plain(P, P->v, i, h, S->v + p * d);
+        if (want_grad) load_plain(P, P->dout, i, h, S->g + p * d);
+    }
+}
+
+static void seg_head_free(seg_head* S) {
+    free(S->q); free(S->k); free(S->v); free(S->g);
+}
+
+static double dot(const double* a, const double* b, int d) {
+    double s = 0.0;
+    for (int c = 0; c < d; ++c) s += a[c] * b[c];
+    return s;
+}
+
+/* Masked softmax row p of one segment-head: scores s_j = q'_p . k'_j * scale
+ * for the allowed keys j <= p (the -inf entries of the additive mask
+ * contribute exp(-inf) = 0 to the normaliser), LSE_p = ln sum_j exp(s_j). */
+static double softmax_row(const seg_head* S, int64_t p, int d, double scale, double* s) {
+    double m = -INFINITY;
+    for (int64_t j = 0; j <= p; ++j) {
+        s[j] = dot(S->q + p * d, S->k + j * d, d) * scale;
+        if (s[j] > m) m = s[j];
+    }
+    double z = 0.0;
+    for (int64_t j = 0; j <= p; ++j) z += exp(s[j] - m);
+    return m + log(z);
+}
+
+/* Forward for one row: o[d] = sum_{j<=p} exp(s_j - LSE) v_j, returns LSE. */
+static double fwd_row(const seg_head* S, int64_t p, int d, double scale, double* s, double* o) {
+    double lse = softmax_row(S, p, d, scale, s);
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t j = 0; j <= p; ++j) {
+        double w = exp(s[j] - lse);
+        for (int c = 0; c < d; ++c) o[c] += w * S->v[j * d + c];
+    }
+    return lse;
+}
+
+static orc_problem make_problem(const void* q, const void* k, const void* v,
+                                const void* dout, const int32_t* cu, int32_t nseg,
+                                int32_t total, int32_t H, int32_t d, double scale,
+                                double theta, int contract) {
+    orc_problem P;
+    P.q = q; P.k = k; P.v = v; P.dout = dout; P.cu = cu;
+    P.f64_inputs = contract < 0;   /* contract == -1 selects fp64 inputs, exact mode */
+    if (contract < 0) contract = 0;
+    P.nseg = nseg; P.total = total; P.H = H; P.d = d;
+    P.scale = scale > 0.0 ? scale : 1.0 / sqrt((double)d);
+    P.theta = theta; P.contract = contract;
+    return P;
+}
+
+/* Full forward: o [total][H][d], lse [H][total] (natural log). */
+void orc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
+                  int32_t nseg, int32_t total, int32_t H, int32_t d, double scale, double theta,
+                  int contract, double* o, double* lse) {
+    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, d, scale, theta, contract);
+    int64_t nwork = (int64_t)nseg * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t w = 0; w < nwork; ++w) {
+        int32_t r = (int32_t)(w / H), h = (int32_t)(w % H);
+        seg_head S;
+        seg_head_load(&P, r, h, 0, &S);
+        double* s = (double*)malloc(sizeof(double) * (size_t)S.L);
+        for (int64_t p = 0; p < S.L; ++p) {
+            int64_t i = S.base + p;
+            lse[(size_t)h * total + i] =
+                fwd_row(&S, p, d, P.scale, s, o + ((size_t)i * H + h) * d);
+        }
+        free(s);
+        seg_head_free(&S);
+    }
+}
+
+/* Sampled forward: the same result for selected (token, head) pairs only,
+ * so that full-size problems can be checked row by row. */
+void orc_attn_fwd_rows(const void* q, const void* k, const void* v, const int32_t* cu,
+                       int32_t nseg, int32_t total, int32_t H, int32_t d, double scale,
+                       double theta, int contract, const int64_t* rows, const int32_t* heads,
+                       int64_t n, double* o, double* lse) {
+    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, d, scale, theta, contract);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t i = rows[t];
+        int32_t h = heads[t];
+        int32_t r = segment_of(cu, nseg, i);
+        int64_t p = i - cu[r];
+        /* only the prefix 0..p of the segment is needed */
+        seg_head S;
+        S.base = cu[r];
+        S.L = p + 1;
+        S.q = (double*)malloc(sizeof(double) * (size_t)(p + 1) * d);
+        S.k = (double*)malloc(sizeof(double) * (size_t)(p + 1) * d);
+        S.v = (double*)malloc(sizeof(double) * (size_t)(p + 1) * d);
+        S.g = NULL;
+        load_rotated(&P, q, i, h, p, S.q + p * d);
+        for (int64_t j = 0; j <= p; ++j) {
+            load_rotated(&P, k, S.base + j, h, j, S.k + j * d);
+            load_plain(&P, v, S.base + j, h, S.v + j * d);
+        }
+        double* s = (double*)malloc(sizeof(double) * (size_t)(p + 1));
+        lse[t] = fwd_row(&S, p, d, P.scale, s, o + t * d);
+        free(s);
+        seg_head_free(&S);
+    }
+}
+
+/* Backward of one segment-head (the standard softmax-attention derivatives):
+ *   P = exp(S - LSE) on allowed entries, dV = P^T dO, dP = dO V^T,
+ *   D_p = sum_j P_pj dP_pj, dS = P o (dP - D), dQ' = scale dS K', dK' = scale dS^T Q',
+ * then dQ = R(p)^T dQ', dK = R(p)^T dK'.
+ * dq/dk/dv are written at the segment's rows (layout [total][H][d]). */
+static void bwd_seg_head(const orc_problem* P, int32_t r, int32_t h, double* dq, double* dk,
+                         double* dv) {
+    int d = P->d;
+    seg_head S;
+    seg_head_load(P, r, h, 1, &S);
+    int64_t L = S.L;
+    double* lse = (double*)malloc(sizeof(double) * (size_t)L);
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    for (int64_t p = 0; p < L; ++p) lse[p] = softmax_row(&S, p, d, P->scale, s);
+    double* gq = (double*)calloc((size_t)L * d, sizeof(double));
+    double* gk = (double*)calloc((size_t)L * d, sizeof(double));
+    double* gv = (double*)calloc((size_t)L * d, sizeof(double));
+    double* pr = (double*)malloc(sizeof(double) * (size_t)L);
+    double* dp = (double*)malloc(sizeof(double) * (size_t)L);
+    for (int64_t p = 0; p < L; ++p) {
+        double D = 0.0;
+        for (int64_t j = 0; j <= p; ++j) {
+            pr[j] = exp(dot(S.q + p * d, S.k + j * d, d) * P->scale - lse[p]);
+            dp[j] = dot(S.g + p * d, S.v + j * d, d);
+            D += pr[j] * dp[j];
+        }
+        for (int64_t j = 0; j <= p; ++j) {
+            double ds = pr[j] * (dp[j] - D);
+            for (int c = 0; c < d; ++c) {
+                gv[j * d + c] += pr[j] * S.g[p * d + c];
+                gq[p * d + c] += P->scale * ds * S.k[j * d + c];
+                gk[j * d + c] += P->scale * ds * S.q[p * d + c];
+            }
+        }
+    }
+    for (int64_t p = 0; p < L; ++p) {
+        size_t off = ((size_t)(S.base + p) * P->H + h) * d;
+        if (P->theta != 0.0) {
+            rope_rotate_transpose(gq + p * d, dq + off, p, d, P->theta);
+            rope_rotate_transpose(gk + p * d, dk + off, p, d, P->theta);
+        } else {
+            memcpy(dq + off, gq + p * d, sizeof(double) * (size_t)d);
+            memcpy(dk + off, gk + p * d, sizeof(double) * (size_t)d);
+        }
+        memcpy(dv + off, gv + p * d, sizeof(double) * (size_t)d);
+    }
+    free(lse); free(s); free(gq); free(gk); free(gv); free(pr); free(dp);
+    seg_head_free(&S);
+}
+
+void orc_attn_bwd(const void* dout, const void* q, const void* k, const void* v,
+                  const int32_t* cu, int32_t nseg, int32_t total, int32_t H, int32_t d,
+                  double scale, double theta, int contract, double* dq, double* dk, double* dv) {
+    orc_problem P = make_problem(q, k, v, dout, cu, nseg, total, H, d, scale, theta, contract);
+    int64_t nwork = (int64_t)nseg * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t w = 0; w < nwork; ++w)
+        bwd_seg_head(&P, (int32_t)(w / H), (int32_t)(w % H), dq, dk, dv);
+}
+
+/* Backward restricted to a set of (segment, head) pairs; the other rows of
+ * dq/dk/dv are left untouched.  Used for sampled checks at full size. */
+void orc_attn_bwd_seg_heads(const void* dout, const void* q, const void* k,
+                            const void* v, const int32_t* cu, int32_t nseg, int32_t total,
+                            int32_t H, int32_t d, double scale, double theta, int contract,
+                            const int32_t* segs, const int32_t* heads, int64_t n, double* dq,
+                            double* dk, double* dv) {
+    orc_problem P = make_problem(q, k, v, dout, cu, nseg, total, H, d, scale, theta, contract);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n; ++t) bwd_seg_head(&P, segs[t], heads[t], dq, dk, dv);
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,425 @@
+"""Pins of the fp64 oracle against what the pages and mathematics fix (CPU only).
+
+Each test names the page and section whose value or property it checks.  A
+plausible slip in the oracle (a dropped term, a wrong sign or index, a
+transposed operand, a mask applied after the softmax, a position that does
+not reset) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import brute
+from tests.conftest import GOLDEN
+from variable_length_causal_gb300 import synth
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _bf16(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _rand_qkv(lengths, H, d, seed, with_grad=False):
+    w = synth.custom_workload(lengths, H, d)
+    return w, synth.make_tensors(w, seed=seed, with_grad=with_grad)
+
+
+def _f64(t):
+    return t.float().double().numpy()
+
+
+# ------------------------------------------------------------------ cu_seqlens, positions, labels
+
+def test_nine_token_example_positions():
+    """charlestar, 'Nine tokens together keep three sample identities'."""
+    g = _golden("nine_token_example.json")
+    tokens = np.arange(g["total"]) + 1
+    pos, _ = oracle.positions_labels(g["cu_seqlens"], tokens)
+    assert pos.tolist() == g["position"]
+    assert oracle.validate_cu(g["cu_seqlens"], g["total"], g["max_seqlen"]) == 0
+    # max_seqlen is the largest segment, not the total nor a bin capacity
+    assert oracle.validate_cu(g["cu_seqlens"], g["total"], g["total"]) == oracle.ERR_MAXLEN
+    assert oracle.validate_cu(g["cu_seqlens"], g["total"], 3) == oracle.ERR_MAXLEN
+    # segment ids agree with numpy's searchsorted (brute)
+    assert brute.segment_ids(np.array(g["cu_seqlens"])).tolist() == g["segment"]
+
+
+@pytest.mark.parametrize("cu,total,maxlen,err", [
+    ([1, 3, 5, 9], 9, 4, oracle.ERR_CU_FIRST),
+    ([0, 3, 3, 9], 9, 6, oracle.ERR_CU_ORDER),
+    ([0, 5, 3, 9], 9, 6, oracle.ERR_CU_ORDER),
+    ([0, 3, 5, 9], 10, 4, oracle.ERR_CU_TOTAL),
+    ([0, 3, 5, 9], 9, 5, oracle.ERR_MAXLEN),
+])
+def test_validity_contract(cu, total, maxlen, err):
+    """charlestar: cu[0]==0, strictly increasing, cu[-1]==total, max_seqlen == max diff."""
+    got = oracle.validate_cu(cu, total, maxlen)
+    assert got & err == err
+    if err == oracle.ERR_CU_FIRST:
+        assert got == oracle.ERR_CU_FIRST | (0 if maxlen == 4 else oracle.ERR_MAXLEN)
+
+
+def test_preshifted_labels_example():
+    """M020 section 06: A=[11,12,13], B=[21,22] -> [12, 13, ignore, 22, ignore], 3 targets."""
+    g = _golden("labels_example.json")
+    pos, lab = oracle.positions_labels(g["cu_seqlens"], g["tokens"])
+    assert pos.tolist() == g["positions"]
+    assert lab.tolist() == g["labels_preshifted"]
+    assert int(np.sum(lab != -100)) == g["valid_targets"]
+
+
+def test_internal_shift_gives_same_prediction_pairs():
+    """charlestar, 'one cross-boundary prediction pair remains': the internal-shift
+    labels (-100 at segment starts, logits[:-1] vs labels[1:]) and the pre-shifted labels
+    (-100 at segment ends) supervise the same (input position -> target) pairs, and the
+    count is sum (L_r - 1) = 6 for nine tokens."""
+    g = _golden("internal_shift_labels.json")
+    tok = np.array(g["tokens"])
+    cu = np.array(g["cu_seqlens"])
+    internal = tok.copy()
+    internal[cu[:-1]] = -100
+    assert internal.tolist() == g["labels_internal_shift"]
+    pairs_internal = {(i, int(internal[i + 1])) for i in range(len(tok) - 1) if internal[i + 1] != -100}
+    _, pre = oracle.positions_labels(cu, tok)
+    pairs_pre = {(i, int(pre[i])) for i in range(len(tok)) if pre[i] != -100}
+    assert pairs_internal == pairs_pre
+    assert len(pairs_pre) == g["valid_targets"] == int(np.sum(np.diff(cu) - 1))
+    names = g["tokens_symbolic"]
+    sym = sorted((names[i], names[i + 1]) for i, _ in pairs_pre)
+    assert sym == sorted(tuple(p) for p in g["prediction_pairs_symbolic"])
+
+
+def test_ignored_segment_labels_all_ignored():
+    """llm-compass 'Implementation notes': the padding tail's labels are all -100."""
+    cu = [0, 3, 5, 9]
+    tok = np.arange(9) + 7
+    _, lab = oracle.positions_labels(cu, tok, seg_ignore=[0, 1, 0])
+    assert lab[3:5].tolist() == [-100, -100]
+    assert lab[:3].tolist() == [8, 9, -100]
+    assert lab[5:].tolist() == [13, 14, 15, -100]
+
+
+def test_positions_labels_random_against_searchsorted():
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 40, size=30)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    tok = rng.integers(0, 1000, size=cu[-1])
+    ign = (rng.random(30) < 0.2).astype(np.uint8)
+    pos, lab = oracle.positions_labels(cu, tok, ign)
+    seg = brute.segment_ids(cu)
+    assert np.array_equal(pos, brute.local_positions(cu))
+    nxt_same = np.append(seg[1:] == seg[:-1], False)
+    want = np.where(nxt_same & (ign[seg] == 0), np.append(tok[1:], -100), -100)
+    assert np.array_equal(lab, want)
+
+
+# ------------------------------------------------------------------ attention forward
+
+def test_contamination_counterexample():
+    """charlestar, 'EOS is content; isolation happens before softmax': scores all 0,
+    V(A)=1, V(b0)=10 -> isolated b0 output 10, whole-pack causal 3.25."""
+    g = _golden("contamination_counterexample.json")
+    d = 4
+    T = 9
+    q = torch.zeros(T, 1, d, dtype=torch.bfloat16)
+    k = _bf16(np.random.default_rng(0).standard_normal((T, 1, d)))
+    v = torch.full((T, 1, d), 5.0, dtype=torch.bfloat16)
+    v[0:3] = g["v_values"]["A"]
+    v[3] = g["v_values"]["b0"]
+    r = g["query_row"]
+    o_iso, _ = oracle.attn_fwd(q, k, v, g["cu_seqlens_isolated"])
+    o_all, _ = oracle.attn_fwd(q, k, v, g["cu_seqlens_whole_pack"], theta=0.0)
+    assert np.allclose(o_iso[r, 0], g["output_isolated"], atol=1e-12)
+    assert np.allclose(o_all[r, 0], g["output_whole_pack"], atol=1e-12)
+
+
+def test_closed_form_zero_queries():
+    """With Q = 0 every allowed score is 0: LSE_i = ln(p_i + 1) and O_i is the mean of the
+    segment's V rows 0..p_i (uniform softmax over the allowed keys only)."""
+    lens = [1, 7, 3, 12, 2]
+    w, (q, k, v) = _rand_qkv(lens, 2, 8, seed=3)
+    q = torch.zeros_like(q)
+    o, lse = oracle.attn_fwd(q, k, v, w.cu)
+    pos = brute.local_positions(w.cu)
+    assert np.allclose(lse, np.log(pos + 1.0)[None, :], atol=1e-13)
+    vf = _f64(v)
+    for r in range(len(lens)):
+        a, b = w.cu[r], w.cu[r + 1]
+        mean = np.cumsum(vf[a:b], axis=0) / np.arange(1, b - a + 1)[:, None, None]
+        assert np.allclose(o[a:b], mean, atol=1e-13)
+
+
+@pytest.mark.parametrize("theta,contract", [(0.0, True), (10000.0, False), (10000.0, True), (500.0, False)])
+@pytest.mark.parametrize("d", [8, 16])
+def test_against_whole_pack_brute_force(theta, contract, d):
+    """Segment-by-segment oracle == full T x T masked softmax (numpy, complex-form RoPE)."""
+    lens = [1, 5, 17, 3, 9]
+    w, (q, k, v) = _rand_qkv(lens, 3, d, seed=11)
+    o, lse = oracle.attn_fwd(q, k, v, w.cu, theta=theta, contract=contract)
+    ob, lseb = brute.attention(_f64(q), _f64(k), _f64(v), w.cu, theta=theta, contract=contract)
+    tol = 1e-12 if not contract else 1e-9
+    assert np.max(np.abs(o - ob)) < tol
+    assert np.max(np.abs(lse - lseb)) < tol
+
+
+def test_against_torch_sdpa_bool_mask():
+    """torch CPU fp64 scaled_dot_product_attention with a boolean mask, True = attend
+    (charlestar notes PyTorch SDPA's boolean semantics)."""
+    lens = [4, 1, 11, 6]
+    w, (q, k, v) = _rand_qkv(lens, 2, 16, seed=21)
+    pos = brute.local_positions(w.cu)
+    qr = brute.rope_complex(_f64(q), pos, 10000.0)
+    kr = brute.rope_complex(_f64(k), pos, 10000.0)
+    mask = torch.from_numpy(brute.block_causal_allow(w.cu))
+    qt = torch.from_numpy(qr).permute(1, 0, 2)
+    kt = torch.from_numpy(kr).permute(1, 0, 2)
+    vt = torch.from_numpy(_f64(v)).permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask)
+    o, _ = oracle.attn_fwd(q, k, v, w.cu, contract=False)
+    assert np.max(np.abs(o - ref.permute(1, 0, 2).numpy())) < 1e-12
+
+
+def test_packed_equals_per_sample_and_isolation():
+    """charlestar, 'change A, B must not change'; M020 section 08: packed run equals the
+    per-sample runs, and replacing A's tokens leaves B and C bit-identical."""
+    lens = [3, 2, 4]
+    w, (q, k, v) = _rand_qkv(lens, 2, 8, seed=2)
+    o, lse = oracle.attn_fwd(q, k, v, w.cu)
+    for r, L in enumerate(lens):
+        a, b = w.cu[r], w.cu[r + 1]
+        o1, l1 = oracle.attn_fwd(q[a:b].contiguous(), k[a:b].contiguous(), v[a:b].contiguous(), [0, L])
+        assert np.array_equal(o1, o[a:b])
+        assert np.array_equal(l1, lse[:, a:b])
+    q2, k2, v2 = q.clone(), k.clone(), v.clone()
+    g = torch.Generator().manual_seed(99)
+    q2[:3] = torch.randn(3, 2, 8, generator=g).bfloat16()
+    k2[:3] = torch.randn(3, 2, 8, generator=g).bfloat16()
+    v2[:3] = torch.randn(3, 2, 8, generator=g).bfloat16()
+    o2, lse2 = oracle.attn_fwd(q2, k2, v2, w.cu)
+    assert np.array_equal(o2[3:], o[3:]) and np.array_equal(lse2[:, 3:], lse[:, 3:])
+    assert not np.array_equal(o2[:3], o[:3])
+
+
+def test_wrong_cu_changes_a_and_b0():
+    """charlestar: writing [0,4,5,9] instead of [0,3,5,9] puts b0 into A's context."""
+    g = _golden("nine_token_example.json")
+    w, (q, k, v) = _rand_qkv(g["lengths"], 1, 8, seed=4)
+    o_ok, _ = oracle.attn_fwd(q, k, v, g["cu_seqlens"])
+    o_bad, _ = oracle.attn_fwd(q, k, v, g["wrong_cu_seqlens"])
+    assert not np.allclose(o_ok[3], o_bad[3])           # b0 now sees A
+    assert not np.allclose(o_ok[4], o_bad[4])           # B's EOS lost b0 from its context
+    assert np.array_equal(o_ok[:3], o_bad[:3])          # A's own rows keep their prefix
+    assert np.array_equal(o_ok[5:], o_bad[5:])          # C untouched
+
+
+def test_rows_api_matches_full():
+    lens = [130, 7, 260]
+    w, (q, k, v) = _rand_qkv(lens, 2, 16, seed=8)
+    o, lse = oracle.attn_fwd(q, k, v, w.cu)
+    rows = np.array([0, 129, 130, 136, 137, 300, 396])
+    heads = np.array([0, 1, 1, 0, 1, 0, 1])
+    o_r, l_r = oracle.attn_fwd_rows(q, k, v, w.cu, rows, heads)
+    assert np.array_equal(o_r, o[rows, heads])
+    assert np.array_equal(l_r, lse[heads, rows])
+
+
+# ------------------------------------------------------------------ RoPE
+
+def test_rope_closed_forms():
+    """R(0) = I; d=2 rotates by angle p; d=4's second pair turns at theta^(-1/2) per step
+    (rotate-half pairing (x_j, x_{j+d/2}), fixed frequencies theta^(-2j/d))."""
+    x = np.random.default_rng(0).standard_normal((5, 8))
+    assert np.array_equal(oracle.rope_rows(x, np.zeros(5)), x)
+    p = 3
+    out = oracle.rope_rows(np.array([[1.0, 0.0]]), [p])[0]
+    assert np.allclose(out, [math.cos(p), math.sin(p)], atol=1e-15)
+    out = oracle.rope_rows(np.array([[0.0, 1.0, 0.0, 0.0]]), [p], theta=10000.0)[0]
+    ang = p * 10000.0 ** (-0.5)
+    assert np.allclose(out, [0.0, math.cos(ang), 0.0, math.sin(ang)], atol=1e-15)
+
+
+def test_rope_shift_invariance_and_norm():
+    """charlestar, 'the pure-RoPE argument': (R(m+c)q)^T (R(n+c)k) = q^T R(n-m) k."""
+    rng = np.random.default_rng(1)
+    d = 64
+    for _ in range(20):
+        q, k = rng.standard_normal((2, d))
+        m, n, c = rng.integers(0, 4000, size=3)
+        a = oracle.rope_rows(q[None], [m + c])[0] @ oracle.rope_rows(k[None], [n + c])[0]
+        b = oracle.rope_rows(q[None], [m])[0] @ oracle.rope_rows(k[None], [n])[0]
+        assert abs(a - b) < 1e-9 * (1 + abs(b))
+        assert abs(np.linalg.norm(oracle.rope_rows(q[None], [m])[0]) - np.linalg.norm(q)) < 1e-12
+    x = rng.standard_normal((7, 32))
+    pos = rng.integers(0, 30000, size=7)
+    assert np.allclose(oracle.rope_rows(x, pos), brute.rope_complex(x, pos, 10000.0), atol=1e-9)
+
+
+def test_rope_exact_mode_reset_invariance():
+    """In exact mode, resetting positions per segment or counting them across the pack gives
+    the same attention output (the shift cancels inside each segment's scores)."""
+    lens = [6, 9]
+    w, (q, k, v) = _rand_qkv(lens, 1, 16, seed=6)
+    o, _ = oracle.attn_fwd(q, k, v, w.cu, contract=False)
+    # second segment alone, but with its q/k pre-rotated by the pack offset c = 6
+    a, b = w.cu[1], w.cu[2]
+    qf, kf = _f64(q[a:b]), _f64(k[a:b])
+    c = np.full(b - a, a)
+    qs = brute.rope_complex(qf, c, 10000.0)
+    ks = brute.rope_complex(kf, c, 10000.0)
+    o2, _ = oracle.attn_fwd_f64(qs, ks, _f64(v[a:b]), [0, b - a])
+    assert np.max(np.abs(o2 - o[a:b])) < 1e-12
+
+
+def test_round_bf16_against_torch():
+    """brute.round_bf16 (integer RNE on binary64) agrees with torch's float32->bf16 rounding on
+    float32-representable values, where a single rounding happens."""
+    x = np.random.default_rng(3).standard_normal(100000).astype(np.float32)
+    x = np.concatenate([x, (np.arange(-512, 512) / 256.0 + 1.0 / 512).astype(np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(brute.round_bf16(x.astype(np.float64)), ref)
+
+
+# ------------------------------------------------------------------ attention backward
+
+def _fd_check(lens, H, d, theta, seed):
+    rng = np.random.default_rng(seed)
+    w = synth.custom_workload(lens, H, d)
+    T = w.total
+    q, k, v, g = (rng.standard_normal((T, H, d)) for _ in range(4))
+    dq, dk, dv = oracle.attn_bwd_f64(g, q, k, v, w.cu, theta=theta)
+    eps = 1e-6
+
+    def f(qq, kk, vv):
+        o, _ = oracle.attn_fwd_f64(qq, kk, vv, w.cu, theta=theta)
+        return float(np.sum(o * g))
+
+    for name, x, gx in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        idx = [tuple(rng.integers(0, s) for s in x.shape) for _ in range(12)]
+        for ix in idx:
+            xp, xm = x.copy(), x.copy()
+            xp[ix] += eps
+            xm[ix] -= eps
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num = (f(*args_p) - f(*args_m)) / (2 * eps)
+            assert abs(num - gx[ix]) < 1e-6 * (1 + abs(num)), (name, ix, num, gx[ix])
+
+
+@pytest.mark.parametrize("theta", [0.0, 10000.0])
+def test_backward_finite_differences(theta):
+    """charlestar, 'change A, B must not change' (its CPU recheck uses finite differences
+    for the Q/K/V gradients)."""
+    _fd_check([3, 1, 5], 2, 8, theta, seed=7)
+
+
+def test_backward_against_torch_autograd():
+    """Whole-pack torch fp64 autograd (complex-form RoPE, boolean-mask SDPA) vs the oracle."""
+    lens = [5, 2, 9]
+    w, (q, k, v, g) = _rand_qkv(lens, 2, 16, seed=12, with_grad=True)
+    pos = torch.from_numpy(brute.local_positions(w.cu)).double()
+    qt = torch.from_numpy(_f64(q)).requires_grad_()
+    kt = torch.from_numpy(_f64(k)).requires_grad_()
+    vt = torch.from_numpy(_f64(v)).requires_grad_()
+    half = 8
+    wfreq = 10000.0 ** (-2.0 * torch.arange(half, dtype=torch.float64) / 16)
+    rot = torch.polar(torch.ones(len(pos), half, dtype=torch.float64), pos[:, None] * wfreq[None])
+
+    def rope(x):
+        z = torch.complex(x[..., :half], x[..., half:]) * rot[:, None, :]
+        return torch.cat([z.real, z.imag], dim=-1)
+
+    mask = torch.from_numpy(brute.block_causal_allow(w.cu))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        rope(qt).permute(1, 0, 2), rope(kt).permute(1, 0, 2), vt.permute(1, 0, 2), attn_mask=mask
+    ).permute(1, 0, 2)
+    (o * torch.from_numpy(_f64(g))).sum().backward()
+    dq, dk, dv = oracle.attn_bwd(g, q, k, v, w.cu, contract=False)
+    assert np.max(np.abs(dq - qt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dk - kt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dv - vt.grad.numpy())) < 1e-11
+
+
+def test_backward_seg_heads_subset_matches_full():
+    lens = [4, 9, 3]
+    w, (q, k, v, g) = _rand_qkv(lens, 2, 8, seed=13, with_grad=True)
+    full = oracle.attn_bwd(g, q, k, v, w.cu)
+    part = oracle.attn_bwd(g, q, k, v, w.cu, seg_heads=[(1, 1), (2, 0)])
+    for a, b in zip(full, part):
+        assert np.array_equal(a[4:13, 1], b[4:13, 1])
+        assert np.array_equal(a[13:16, 0], b[13:16, 0])
+        assert not b[:4].any()
+
+
+def test_backward_isolation():
+    """Gradients of one segment do not depend on another segment's inputs."""
+    lens = [3, 2, 4]
+    w, (q, k, v, g) = _rand_qkv(lens, 1, 8, seed=14, with_grad=True)
+    base = oracle.attn_bwd(g, q, k, v, w.cu)
+    q2 = q.clone()
+    q2[:3] = -q2[:3]
+    alt = oracle.attn_bwd(g, q2, k, v, w.cu)
+    for a, b in zip(base, alt):
+        assert np.array_equal(a[3:], b[3:])
+
+
+# ------------------------------------------------------------------ work lists
+
+def _allowed_tiles(cu, BM, BN):
+    """Brute force: every (seg, q_tile, kv_tile) holding at least one allowed pair."""
+    tiles = set()
+    for r in range(len(cu) - 1):
+        L = cu[r + 1] - cu[r]
+        for i in range(L):
+            for j in range(i + 1):
+                tiles.add((r, i // BM, j // BN))
+    return tiles
+
+
+@pytest.mark.parametrize("BM,BN", [(128, 128), (64, 128), (128, 64), (16, 16), (16, 32)])
+def test_worklists_cover_exactly_the_allowed_tiles(BM, BN):
+    """No item touches another segment or a tile wholly above the diagonal, and every
+    allowed (query, key) pair lies in exactly one forward and one backward tile."""
+    rng = np.random.default_rng(BM * 7 + BN)
+    lens = np.concatenate([rng.integers(1, 300, size=12), [1, BM, BM + 1, BN - 1 if BN > 1 else 1]])
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    want = _allowed_tiles(cu, BM, BN)
+    fwd = oracle.worklist_fwd(cu, BM, BN)
+    got_f = []
+    for s, qt, lo, hi in fwd:
+        got_f += [(s, qt, kt) for kt in range(lo, hi)]
+    assert len(got_f) == len(set(got_f)) and set(got_f) == want
+    bwd = oracle.worklist_bwd(cu, BM, BN)
+    got_b = []
+    for s, kt, lo, hi in bwd:
+        got_b += [(s, qt, kt) for qt in range(lo, hi)]
+    assert len(got_b) == len(set(got_b)) and set(got_b) == want
+    # one forward item per q tile, one backward item per kv tile
+    assert len(fwd) == int(np.sum(-(-lens // BM)))
+    assert len(bwd) == int(np.sum(-(-lens // BN)))
+
+
+def test_worklist_order():
+    """Longest segments first (stable on ties), longest key range first inside a segment."""
+    lens = np.array([100, 300, 129, 256, 300, 1, 257])
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    fwd = oracle.worklist_fwd(cu, 128, 128)
+    nq = -(-lens // 128)
+    seg_seq = [s for s, *_ in fwd]
+    firsts = list(dict.fromkeys(seg_seq))
+    assert firsts == sorted(range(len(lens)), key=lambda r: (-nq[r], r))
+    for r in range(len(lens)):
+        qts = [qt for s, qt, _, _ in fwd if s == r]
+        assert qts == list(range(nq[r] - 1, -1, -1))
+    bwd = oracle.worklist_bwd(cu, 128, 128)
+    for r in range(len(lens)):
+        kts = [kt for s, kt, _, _ in bwd if s == r]
+        assert kts == list(range(nq[r]))
