@@ -1,0 +1,162 @@
+/*
+ * vlc.h -- C ABI of the varlen block-diagonal causal attention library for
+ * isolated sequence packing (NVIDIA GB300, sm_103a).
+ *
+ * The problem (sources are cited by page title and section):
+ *
+ *  - Packed THD layout.  Several independent samples are concatenated into one
+ *    token buffer with no batch dimension; q, k, v are [total, H, d]
+ *    ("Long-context training: remove padding", vllbc, section on cu_seqlens and
+ *    the THD format).
+ *  - cu_seqlens.  int32 prefix sums [0, L_1, L_1+L_2, ..., total]; segment r is
+ *    the half-open range [cu_r, cu_{r+1}).  Valid only if cu[0] == 0, the
+ *    entries strictly increase, cu[nseg] == total and max_seqlen equals the
+ *    largest difference ("Sequence packing and variable-length attention",
+ *    charlestar, section "Nine tokens together keep three sample identities").
+ *  - Isolation.  Token i attends to token j iff both lie in the same segment
+ *    and p_j <= p_i; the mask is applied before the softmax normalisation:
+ *    O = softmax(Q K^T / sqrt(d) + M) V with M in {0, -inf} (same page, section
+ *    "EOS is content; isolation happens before softmax").  No work is issued
+ *    for key tiles of another segment or wholly above the diagonal.
+ *  - Positions.  p_i = i - cu_r (per-segment reset); RoPE rotates q and k by
+ *    R(p_i) with fixed frequencies theta^(-2j/d), rotate-half pairing
+ *    (x_j, x_{j+d/2}) (same page, "Positions are reset per segment"; "Packing
+ *    document boundary", operatorworld, pitfall 2).
+ *  - Labels.  Pre-shifted next-token labels, -100 at each segment's last token
+ *    ("Length grouping, de-padding and packing", ai-infra-kb M020, section 06).
+ *
+ * Conventions for every call:
+ *  - All data pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no device memory; scratch lives in the caller's workspace
+ *    (size from vlc_workspace_bytes).
+ *  - Work is enqueued asynchronously on the caller's stream (a cudaStream_t,
+ *    passed as void*; NULL is the legacy default stream).
+ *  - A non-zero return is a host-side error detected before anything was
+ *    enqueued (bad argument, unsupported shape, workspace too small, CUDA launch
+ *    failure).  Content errors in cu_seqlens are found on the device: they set
+ *    bits in the workspace's device error word, every later kernel of that call
+ *    becomes a no-op, and vlc_get_error() reports them.  Nothing traps.
+ *  - bf16 tensors are contiguous [total, H, d] row-major (last dim stride 1),
+ *    d in {64, 128}, H >= 1.  lse is fp32 [H, total], natural log.
+ */
+#ifndef VLC_H
+#define VLC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VLC_OK = 0,
+    VLC_ERR_ARG = 1,           /* null pointer, non-positive size, bad enum */
+    VLC_ERR_CU_SEQLENS = 2,    /* device found cu_seqlens / max_seqlen invalid */
+    VLC_ERR_UNSUPPORTED = 3,   /* head_dim not 64/128, sizes beyond the limits below */
+    VLC_ERR_WORKSPACE = 4,     /* workspace pointer null / too small / misaligned */
+    VLC_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    VLC_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up */
+} vlc_status;
+
+/* Device error word bits (vlc_get_error folds them into a vlc_status). */
+#define VLC_DEVERR_CU_FIRST 0x1    /* cu[0] != 0 */
+#define VLC_DEVERR_CU_ORDER 0x2    /* some cu[r+1] <= cu[r] */
+#define VLC_DEVERR_CU_TOTAL 0x4    /* cu[nseg] != total */
+#define VLC_DEVERR_MAXLEN 0x8      /* max_seqlen != largest segment length */
+#define VLC_DEVERR_TIMEOUT 0x100   /* a bounded mbarrier wait expired */
+
+/* Limits checked on the host. */
+#define VLC_MAX_SEQLEN (1 << 20)   /* longest segment */
+#define VLC_WORKLIST_FWD 0
+#define VLC_WORKLIST_BWD 1
+
+/* Human-readable name of a vlc_status value. */
+const char* vlc_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int vlc_version(void);
+
+/* Bytes of workspace needed by vlc_attn_fwd (is_bwd = 0) or vlc_attn_bwd
+ * (is_bwd = 1) for these sizes.  Returns 0 for invalid sizes.  The workspace
+ * must be 256-byte aligned; its contents need no initialisation. */
+size_t vlc_workspace_bytes(int32_t nseg, int32_t total, int32_t H, int32_t d,
+                           int32_t max_seqlen, int is_bwd);
+
+/* Capacity (in items) that vlc_build_worklist may write for these sizes:
+ * an upper bound of sum_r ceil(L_r / tile) = nseg + total / tile. */
+int64_t vlc_worklist_capacity(int32_t nseg, int32_t total, int32_t tile);
+
+/* Local positions and pre-shifted labels (one kernel, HBM-bound).
+ *   cu         int32 [nseg+1]   segment boundaries (see above)
+ *   tokens     int64 [total]    token ids
+ *   seg_ignore uint8 [nseg] or NULL; segments with a non-zero byte (padding
+ *              tails) get labels -100 everywhere ("Sequence Packing",
+ *              llm-compass, implementation notes)
+ *   pos_out    int32 [total]    p_i = i - cu_r
+ *   labels_out int64 [total]    tokens[i+1] if i+1 < cu_{r+1} and r is not
+ *              ignored, else -100
+ *   err_out    int32 [1] or NULL; if given, cu validity bits (VLC_DEVERR_*
+ *              except MAXLEN) are OR-ed into it.  With invalid cu the outputs
+ *              are unspecified but every access stays in bounds. */
+int vlc_build_positions_labels(const int32_t* cu, int32_t nseg, const int64_t* tokens,
+                               int32_t total, const uint8_t* seg_ignore, int32_t* pos_out,
+                               int64_t* labels_out, int32_t* err_out, void* stream);
+
+/* Work list (the first kernel of both attention calls, exposed for checking).
+ * Validates cu against total/max_seqlen, then writes
+ *   kind == VLC_WORKLIST_FWD: items {seg, q_tile, kv_lo, kv_hi}, one per q tile
+ *       of BM rows; key tiles [kv_lo, kv_hi) = [0, ceil(min(L, (q_tile+1)BM)/BN));
+ *       segments by descending q-tile count (ties by index), q tiles last to first.
+ *   kind == VLC_WORKLIST_BWD: items {seg, kv_tile, q_lo, q_hi}, one per key tile
+ *       of BN rows; q tiles [floor(kv_tile*BN/BM), ceil(L/BM)); segments by
+ *       descending key-tile count (ties by index), key tiles first to last.
+ * No item refers to another segment's rows and no tile lies wholly above the
+ * diagonal ("Packing document boundary", operatorworld, pitfall 1: the varlen
+ * kernel does not spend FLOPs on cross-document blocks).
+ *   items_out     int32 [capacity][4], 16-byte aligned
+ *   seg_order_out int32 [2*nseg+1]: the sorted segment order, then the item
+ *                 offset of each sorted segment (prefix sums, last = count)
+ *   count_out     int32 [1]: number of items (0 on error)
+ *   err_out       int32 [1]: VLC_DEVERR_* bits are OR-ed in (caller zeroes it)
+ *   capacity must be >= vlc_worklist_capacity(nseg, total, tile) where tile is
+ *   BM (forward) or BN (backward); BM, BN powers of two in [16, 256];
+ *   ceil(max_seqlen / tile) must stay below 16384. */
+int vlc_build_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
+                       int32_t BM, int32_t BN, int kind, int32_t* items_out, int64_t capacity,
+                       int32_t* seg_order_out, int32_t* count_out, int32_t* err_out,
+                       void* stream);
+
+/* Forward varlen attention with per-segment RoPE reset.
+ *   q, k, v   bf16 [total, H, d]
+ *   softmax_scale <= 0 selects 1/sqrt(d)
+ *   rope_theta == 0 disables RoPE; otherwise q and k are rotated by R(p_i)
+ *              inside the kernel (the rotated values are rounded to bf16 before
+ *              the tensor-core contraction)
+ *   o         bf16 [total, H, d]  (written for every token)
+ *   lse       fp32 [H, total]     ln sum_j exp(s_ij) over the allowed keys
+ *   ws        workspace of at least vlc_workspace_bytes(..., 0) bytes. */
+int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                 int32_t total, int32_t H, int32_t d, int32_t max_seqlen, float softmax_scale,
+                 float rope_theta, void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of vlc_attn_fwd: gradients of sum(O * dO) with respect to q, k, v
+ * (through the RoPE rotation).  o and lse are the forward outputs.
+ *   dout, q, k, v, o  bf16 [total, H, d];  lse fp32 [H, total]
+ *   dq, dk, dv        bf16 [total, H, d]
+ *   ws                workspace of at least vlc_workspace_bytes(..., 1) bytes. */
+int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
+                 int32_t d, int32_t max_seqlen, float softmax_scale, float rope_theta, void* dq,
+                 void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream` and read the workspace's device error word.
+ * Returns VLC_OK, VLC_ERR_CU_SEQLENS or VLC_ERR_TIMEOUT; *bits_out (if not
+ * NULL) receives the raw VLC_DEVERR_* bits. */
+int vlc_get_error(const void* ws, int32_t* bits_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VLC_H */

@@ -1,0 +1,61 @@
+"""The C-ABI library builds, loads, and exports every function include/vlc.h declares (CPU)."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "vlc.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(vlc_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+
+    g.build()
+    import variable_length_causal_gb300 as vlc
+
+    return vlc.load_library()
+
+
+def test_header_declares_the_path():
+    names = _declared()
+    for n in ("vlc_build_positions_labels", "vlc_attn_fwd", "vlc_attn_bwd", "vlc_build_worklist",
+              "vlc_get_error", "vlc_workspace_bytes"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from variable_length_causal_gb300 import binding
+
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert sorted(binding.EXPORTED) == _declared()
+
+
+def test_host_side_queries(lib):
+    assert lib.vlc_version() >= 100
+    assert lib.vlc_status_string(0) == b"ok"
+    assert lib.vlc_workspace_bytes(3, 9, 2, 128, 4, 0) > 0
+    assert lib.vlc_workspace_bytes(3, 9, 2, 96, 4, 0) == 0        # unsupported head dim
+    assert lib.vlc_workspace_bytes(3, 9, 2, 128, 4, 1) > lib.vlc_workspace_bytes(3, 9, 2, 128, 4, 0)
+    assert lib.vlc_worklist_capacity(3, 9, 128) == 3 + 0 + 1
+
+
+def test_host_argument_checks_need_no_gpu(lib):
+    import ctypes
+
+    # null pointers are rejected before anything touches a device
+    assert lib.vlc_attn_fwd(None, None, None, None, 3, 9, 2, 128, 4, 0.0, 0.0, None, None, None, 0, None) == 1
+    assert lib.vlc_build_positions_labels(None, 3, None, 9, None, None, None, None, None) == 1
+    dummy = ctypes.c_void_p(256)
+    # unsupported head dim / missing workspace
+    assert lib.vlc_attn_fwd(dummy, dummy, dummy, dummy, 3, 9, 2, 96, 4, 0.0, 0.0, dummy, dummy,
+                            dummy, 1 << 20, None) == 3
+    assert lib.vlc_attn_fwd(dummy, dummy, dummy, dummy, 3, 9, 2, 128, 4, 0.0, 0.0, dummy, dummy,
+                            None, 0, None) == 4

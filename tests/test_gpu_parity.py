@@ -1,0 +1,252 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Integer outputs (positions, labels, work lists, error bits) must match
+bit-exactly.  Attention is compared on the same bf16 inputs against the
+oracle's contract mode (rotated q/k rounded to bf16), with the stated bounds:
+O max |err| <= 2e-2 and mean |err| <= 2e-3, LSE max |err| <= 1e-3, gradients
+max |err| <= 5e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from variable_length_causal_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX, G_MAX = 2e-2, 2e-3, 1e-3, 5e-2
+
+
+@pytest.fixture(scope="module")
+def vlc():
+    import __graft_entry__ as g
+
+    g.build()
+    import variable_length_causal_gb300 as m
+
+    m.load_library()
+    return m
+
+
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+def _cu(w):
+    return torch.from_numpy(w.cu).to(DEV)
+
+
+def _cmp_fwd(o, lse, o_ref, lse_ref, rows=None):
+    og = o.float().cpu().numpy()
+    lg = lse.cpu().numpy()
+    if rows is not None:
+        r, h = rows
+        og = og[r, h]
+        lg = lg[h, r]
+    eo = np.abs(og - o_ref)
+    el = np.abs(lg - lse_ref)
+    assert np.isfinite(og).all() and np.isfinite(lg).all()
+    assert eo.max() <= O_MAX, f"O max err {eo.max()}"
+    assert eo.mean() <= O_MEAN, f"O mean err {eo.mean()}"
+    assert el.max() <= LSE_MAX, f"LSE max err {el.max()}"
+    return eo.max(), eo.mean(), el.max()
+
+
+# ------------------------------------------------------------------ positions and labels
+
+@pytest.mark.parametrize("idx", range(5))
+def test_positions_labels_configs(vlc, idx):
+    w = synth.workload(idx)
+    tok = synth.make_tokens(w)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pos, lab = vlc.build_positions_labels(_cu(w), torch.from_numpy(tok).to(DEV),
+                                          torch.from_numpy(w.seg_ignore).to(DEV), err=err)
+    pr, lr = oracle.positions_labels(w.cu, tok, w.seg_ignore)
+    assert np.array_equal(pos.cpu().numpy(), pr)
+    assert np.array_equal(lab.cpu().numpy(), lr)
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("lens", [[1], [9], [3, 2, 4], [1, 1, 1, 1, 1], [5, 1, 7, 1, 2, 3, 8, 1, 1]])
+def test_positions_labels_edges(vlc, lens):
+    w = synth.custom_workload(lens, 1, 64)
+    tok = np.arange(w.total, dtype=np.int64) * 7 + 3
+    pos, lab = vlc.build_positions_labels(_cu(w), torch.from_numpy(tok).to(DEV))
+    pr, lr = oracle.positions_labels(w.cu, tok)
+    assert np.array_equal(pos.cpu().numpy(), pr) and np.array_equal(lab.cpu().numpy(), lr)
+
+
+def test_positions_labels_random_many_segments(vlc):
+    rng = np.random.default_rng(17)
+    lens = rng.integers(1, 50, size=3000)
+    w = synth.custom_workload(lens, 1, 64)
+    tok = rng.integers(0, 50000, size=w.total)
+    ign = (rng.random(len(lens)) < 0.1).astype(np.uint8)
+    pos, lab = vlc.build_positions_labels(_cu(w), torch.from_numpy(tok).to(DEV),
+                                          torch.from_numpy(ign).to(DEV))
+    pr, lr = oracle.positions_labels(w.cu, tok, ign)
+    assert np.array_equal(pos.cpu().numpy(), pr) and np.array_equal(lab.cpu().numpy(), lr)
+
+
+@pytest.mark.parametrize("cu,total", [([1, 3, 5, 9], 9), ([0, 3, 3, 9], 9), ([0, 5, 3, 9], 9),
+                                      ([0, 3, 5, 9], 10)])
+def test_positions_labels_error_bits(vlc, cu, total):
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    tok = torch.arange(total, dtype=torch.int64, device=DEV)
+    vlc.build_positions_labels(cu_t, tok, err=err)
+    want = oracle.validate_cu(cu, total, max(np.diff(cu))) & ~oracle.ERR_MAXLEN
+    assert int(err.item()) == want
+
+
+# ------------------------------------------------------------------ work lists
+
+def _wl_cases():
+    out = [synth.workload(i).cu for i in range(4)]
+    rng = np.random.default_rng(3)
+    for _ in range(3):
+        lens = rng.integers(1, 600, size=int(rng.integers(1, 400)))
+        out.append(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+    out.append(np.array([0, 1], np.int32))
+    out.append(np.concatenate([[0], np.cumsum([128, 128, 127, 129, 1, 256, 255])]).astype(np.int32))
+    return out
+
+
+@pytest.mark.parametrize("ci", range(9))
+@pytest.mark.parametrize("kind,BM,BN", [(0, 128, 128), (1, 64, 128), (0, 64, 64), (1, 128, 64)])
+def test_worklist_bit_exact(vlc, ci, kind, BM, BN):
+    cu = _wl_cases()[ci]
+    lens = np.diff(cu)
+    items, order, bits = vlc.build_worklist(torch.from_numpy(cu).to(DEV), int(cu[-1]), int(lens.max()),
+                                            kind, BM, BN)
+    assert bits == 0
+    ref = oracle.worklist_fwd(cu, BM, BN) if kind == 0 else oracle.worklist_bwd(cu, BM, BN)
+    assert np.array_equal(items.cpu().numpy(), ref)
+    nseg = len(lens)
+    o = order.cpu().numpy()
+    seg_seq = list(dict.fromkeys(ref[:, 0].tolist()))
+    assert o[:nseg].tolist() == seg_seq
+    tile = BM if kind == 0 else BN
+    n_sorted = -(-lens[o[:nseg]] // tile)
+    assert o[nseg:].tolist() == np.concatenate([[0], np.cumsum(n_sorted)]).tolist()
+
+
+@pytest.mark.parametrize("cu,total,maxlen", [([1, 3, 5, 9], 9, 4), ([0, 3, 3, 9], 9, 6),
+                                             ([0, 5, 3, 9], 9, 6), ([0, 3, 5, 9], 10, 4),
+                                             ([0, 3, 5, 9], 9, 5), ([0, 3, 5, 9], 9, 3)])
+def test_worklist_validation_bits(vlc, cu, total, maxlen):
+    items, _, bits = vlc.build_worklist(torch.tensor(cu, dtype=torch.int32, device=DEV), total, maxlen)
+    assert bits == oracle.validate_cu(cu, total, maxlen)
+    assert items.shape[0] == 0
+
+
+# ------------------------------------------------------------------ forward attention
+
+TINY_CASES = [
+    ([3, 2, 4], 2, 64, 10000.0),
+    ([1], 1, 128, 10000.0),
+    ([1, 1, 1], 3, 128, 10000.0),
+    ([127, 128, 129], 2, 128, 10000.0),
+    ([255, 256, 257, 1, 2], 2, 128, 10000.0),
+    ([300, 17, 513], 3, 64, 10000.0),
+    ([200, 55, 140], 2, 128, 0.0),
+    ([640], 1, 128, 500.0),
+]
+
+
+@pytest.mark.parametrize("lens,H,d,theta", TINY_CASES)
+def test_fwd_small(vlc, lens, H, d, theta):
+    w = synth.custom_workload(lens, H, d)
+    q, k, v = synth.make_tensors(w, seed=sum(lens) + H + d)
+    o, lse = vlc.varlen_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), _cu(w), w.max_seqlen, rope_theta=theta)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.cu, theta=theta)
+    _cmp_fwd(o, lse, o_ref, lse_ref)
+
+
+def test_fwd_tiny_config_full(vlc):
+    w = synth.workload(0)
+    q, k, v = synth.make_tensors(w)
+    o, lse = vlc.varlen_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), _cu(w), w.max_seqlen)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.cu)
+    _cmp_fwd(o, lse, o_ref, lse_ref)
+
+
+def test_fwd_zero_queries_closed_form(vlc):
+    """Q = 0: LSE_i = ln(p_i + 1) and O_i = mean of the segment's V rows 0..p_i."""
+    w = synth.custom_workload([1, 7, 130, 3], 2, 128)
+    _, k, v = synth.make_tensors(w, seed=5)
+    q = torch.zeros_like(k)
+    o, lse = vlc.varlen_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), _cu(w), w.max_seqlen)
+    pos = np.concatenate([np.arange(L) for L in w.lengths])
+    assert np.abs(lse.cpu().numpy() - np.log(pos + 1.0)[None]).max() <= LSE_MAX
+    o_ref, _ = oracle.attn_fwd(q, k, v, w.cu)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_MAX
+
+
+def test_fwd_isolation_bitwise(vlc):
+    """Change A's q/k/v: every other segment's O and LSE stay bit-identical
+    (charlestar, 'change A, B must not change')."""
+    w = synth.custom_workload([200, 3, 129, 60], 2, 128)
+    q, k, v = (t.to(DEV) for t in synth.make_tensors(w, seed=9))
+    o1, l1 = vlc.varlen_attn_fwd(q, k, v, _cu(w), w.max_seqlen)
+    q2, k2, v2 = q.clone(), k.clone(), v.clone()
+    for t in (q2, k2, v2):
+        t[:200] = torch.randn_like(t[:200].float()).bfloat16()
+    o2, l2 = vlc.varlen_attn_fwd(q2, k2, v2, _cu(w), w.max_seqlen)
+    assert torch.equal(o1[200:], o2[200:]) and torch.equal(l1[:, 200:], l2[:, 200:])
+    assert not torch.equal(o1[:200], o2[:200])
+
+
+def test_fwd_packed_equals_per_sample_bitwise(vlc):
+    """Tiles are segment-local, so a segment computes the same bits alone or packed."""
+    lens = [131, 5, 300]
+    w = synth.custom_workload(lens, 2, 128)
+    q, k, v = (t.to(DEV) for t in synth.make_tensors(w, seed=10))
+    o, lse = vlc.varlen_attn_fwd(q, k, v, _cu(w), w.max_seqlen)
+    for r, L in enumerate(lens):
+        a, b = int(w.cu[r]), int(w.cu[r + 1])
+        cu1 = torch.tensor([0, L], dtype=torch.int32, device=DEV)
+        o1, l1 = vlc.varlen_attn_fwd(q[a:b].contiguous(), k[a:b].contiguous(), v[a:b].contiguous(), cu1, L)
+        assert torch.equal(o1, o[a:b]) and torch.equal(l1, lse[:, a:b])
+
+
+def test_fwd_bad_cu_is_reported_and_noop(vlc):
+    w = synth.custom_workload([3, 2, 4], 1, 64)
+    q, k, v = (t.to(DEV) for t in synth.make_tensors(w, seed=1))
+    bad = torch.tensor([0, 4, 3, 9], dtype=torch.int32, device=DEV)
+    o = torch.full_like(q, 7.0)
+    with pytest.raises(vlc.VlcError) as ei:
+        vlc.varlen_attn_fwd(q, k, v, bad, 4, out=o)
+    assert ei.value.bits & 0x2
+    assert torch.all(o == 7.0)
+
+
+def _sample_rows(w, n, rng):
+    """Rows near segment starts/ends and tile edges, plus random ones (real segments)."""
+    rows = []
+    real = np.nonzero(w.seg_ignore == 0)[0]
+    for r in rng.choice(real, size=min(len(real), n // 2), replace=False):
+        a, b = int(w.cu[r]), int(w.cu[r + 1])
+        cand = [a, b - 1, a + min(127, b - a - 1), a + min(128, b - a - 1), (a + b) // 2]
+        rows.append(cand[rng.integers(len(cand))])
+    rows += list(rng.integers(0, w.total, size=n - len(rows)))
+    heads = rng.integers(0, w.H, size=len(rows))
+    return np.asarray(rows, np.int64), heads
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3])
+def test_fwd_full_size_sampled(vlc, idx):
+    """Full-size workloads in the bench's launch configuration; sampled rows against the oracle."""
+    w = synth.workload(idx)
+    q, k, v = synth.make_tensors(w, device=DEV)
+    o, lse = vlc.varlen_attn_fwd(q, k, v, _cu(w), w.max_seqlen)
+    rng = np.random.default_rng(100 + idx)
+    rows, heads = _sample_rows(w, 48, rng)
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    o_ref, lse_ref = oracle.attn_fwd_rows(qc, kc, vc, w.cu, rows, heads)
+    _cmp_fwd(o, lse, o_ref, lse_ref, rows=(rows, heads))
+    # properties that hold at any size: finite everywhere, LSE >= max score bound ln(1) for row 0
+    assert torch.isfinite(lse).all()
+    starts = torch.from_numpy(w.cu[:-1].astype(np.int64)).to(DEV)
+    # a segment's first row attends only to itself: O equals V there
+    assert torch.allclose(o[starts].float(), v[starts].float(), atol=1e-2)

@@ -1,0 +1,233 @@
+"""Python binding of libvlc.so: argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; PyTorch supplies
+device memory (outputs and workspace) and the current stream.  There is no
+CPU or PyTorch fallback: if the library is missing or no CUDA device is
+present, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libvlc.so")
+
+VLC_OK, VLC_ERR_ARG, VLC_ERR_CU_SEQLENS, VLC_ERR_UNSUPPORTED = 0, 1, 2, 3
+VLC_ERR_WORKSPACE, VLC_ERR_CUDA, VLC_ERR_TIMEOUT = 4, 5, 6
+DEVERR_CU_FIRST, DEVERR_CU_ORDER, DEVERR_CU_TOTAL, DEVERR_MAXLEN = 0x1, 0x2, 0x4, 0x8
+DEVERR_TIMEOUT = 0x100
+WORKLIST_FWD, WORKLIST_BWD = 0, 1
+
+EXPORTED = [
+    "vlc_status_string", "vlc_version", "vlc_workspace_bytes", "vlc_worklist_capacity",
+    "vlc_build_positions_labels", "vlc_build_worklist", "vlc_attn_fwd", "vlc_attn_bwd",
+    "vlc_get_error",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class VlcError(RuntimeError):
+    def __init__(self, status: int, where: str, bits: int = 0):
+        self.status = status
+        self.bits = bits
+        msg = f"{where}: {load_library().vlc_status_string(status).decode()} (status {status}"
+        msg += f", device bits 0x{bits:x})" if bits else ")"
+        super().__init__(msg)
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libvlc.so and declare its signatures (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`"
+            )
+        lib = ctypes.CDLL(path)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        f32, sz, cint = ctypes.c_float, ctypes.c_size_t, ctypes.c_int
+        lib.vlc_status_string.argtypes = [cint]
+        lib.vlc_status_string.restype = ctypes.c_char_p
+        lib.vlc_version.argtypes = []
+        lib.vlc_version.restype = cint
+        lib.vlc_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, cint]
+        lib.vlc_workspace_bytes.restype = sz
+        lib.vlc_worklist_capacity.argtypes = [i32, i32, i32]
+        lib.vlc_worklist_capacity.restype = i64
+        lib.vlc_build_positions_labels.argtypes = [P, i32, P, i32, P, P, P, P, P]
+        lib.vlc_build_positions_labels.restype = cint
+        lib.vlc_build_worklist.argtypes = [P, i32, i32, i32, i32, i32, cint, P, i64, P, P, P, P]
+        lib.vlc_build_worklist.restype = cint
+        lib.vlc_attn_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, f32, P, P, P, sz, P]
+        lib.vlc_attn_fwd.restype = cint
+        lib.vlc_attn_bwd.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, f32,
+                                     P, P, P, P, sz, P]
+        lib.vlc_attn_bwd.restype = cint
+        lib.vlc_get_error.argtypes = [P, P, P]
+        lib.vlc_get_error.restype = cint
+        _lib = lib
+        return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != VLC_OK:
+        raise VlcError(status, where)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (the library has no CPU path)")
+
+
+def _cu_info(cu_seqlens: torch.Tensor):
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor")
+    return cu_seqlens.numel() - 1
+
+
+def workspace_bytes(nseg: int, total: int, H: int, d: int, max_seqlen: int, backward: bool) -> int:
+    return int(load_library().vlc_workspace_bytes(nseg, total, H, d, max_seqlen, int(backward)))
+
+
+def new_workspace(nseg, total, H, d, max_seqlen, backward, device) -> torch.Tensor:
+    n = workspace_bytes(nseg, total, H, d, max_seqlen, backward)
+    if n == 0:
+        raise VlcError(VLC_ERR_UNSUPPORTED, "workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def get_error(ws: torch.Tensor) -> Tuple[int, int]:
+    """Synchronise the current stream and return (status, device error bits)."""
+    bits = ctypes.c_int32(0)
+    st = load_library().vlc_get_error(_ptr(ws), ctypes.byref(bits), _stream(ws.device))
+    return int(st), int(bits.value)
+
+
+def _raise_device_error(ws, where):
+    st, bits = get_error(ws)
+    if st != VLC_OK:
+        raise VlcError(st, where, bits)
+
+
+def build_positions_labels(cu_seqlens: torch.Tensor, tokens: torch.Tensor,
+                           seg_ignore: Optional[torch.Tensor] = None,
+                           err: Optional[torch.Tensor] = None):
+    """Per-segment positions (int32) and pre-shifted labels (int64, -100 at segment ends)."""
+    lib = load_library()
+    _require_cuda(cu_seqlens, tokens, seg_ignore, err)
+    nseg = _cu_info(cu_seqlens)
+    if tokens.dtype != torch.int64 or not tokens.is_contiguous():
+        raise ValueError("tokens must be contiguous int64")
+    total = tokens.numel()
+    if seg_ignore is not None and (seg_ignore.dtype != torch.uint8 or seg_ignore.numel() != nseg):
+        raise ValueError("seg_ignore must be uint8 with one entry per segment")
+    pos = torch.empty(total, dtype=torch.int32, device=tokens.device)
+    lab = torch.empty(total, dtype=torch.int64, device=tokens.device)
+    st = lib.vlc_build_positions_labels(_ptr(cu_seqlens), nseg, _ptr(tokens), total,
+                                        _ptr(seg_ignore), _ptr(pos), _ptr(lab), _ptr(err),
+                                        _stream(tokens.device))
+    _check(st, "vlc_build_positions_labels")
+    return pos, lab
+
+
+def build_worklist(cu_seqlens: torch.Tensor, total: int, max_seqlen: int, kind: int = WORKLIST_FWD,
+                   BM: int = 128, BN: int = 128):
+    """Device work list: returns (items [n, 4] int32, seg_order [2*nseg+1] int32, err bits)."""
+    lib = load_library()
+    _require_cuda(cu_seqlens)
+    nseg = _cu_info(cu_seqlens)
+    tile = BM if kind == WORKLIST_FWD else BN
+    cap = int(lib.vlc_worklist_capacity(nseg, total, tile))
+    dev = cu_seqlens.device
+    items = torch.zeros((max(cap, 1), 4), dtype=torch.int32, device=dev)
+    order = torch.zeros(2 * nseg + 1, dtype=torch.int32, device=dev)
+    meta = torch.zeros(2, dtype=torch.int32, device=dev)    # count, err
+    st = lib.vlc_build_worklist(_ptr(cu_seqlens), nseg, total, max_seqlen, BM, BN, kind, _ptr(items),
+                                cap, _ptr(order), ctypes.c_void_p(meta.data_ptr()),
+                                ctypes.c_void_p(meta.data_ptr() + 4), _stream(dev))
+    _check(st, "vlc_build_worklist")
+    count, bits = (int(x) for x in meta.cpu())
+    return items[:count], order, bits
+
+
+def _scale(softmax_scale, d):
+    return float(softmax_scale) if softmax_scale else 1.0 / math.sqrt(d)
+
+
+def _check_qkv(*ts):
+    ref = ts[0]
+    for t in ts:
+        if t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+            raise ValueError("q/k/v/o tensors must be contiguous bf16 [total, H, d]")
+        if t.shape != ref.shape or t.device != ref.device:
+            raise ValueError("q/k/v/o tensors must share shape and device")
+
+
+def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                    max_seqlen: int, softmax_scale: Optional[float] = None,
+                    rope_theta: float = 10000.0, out: Optional[torch.Tensor] = None,
+                    lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    check: bool = True):
+    """Segment-local causal attention with per-segment RoPE reset.  Returns (O, LSE[H, total])."""
+    lib = load_library()
+    _require_cuda(q, k, v, cu_seqlens)
+    _check_qkv(q, k, v)
+    total, H, d = q.shape
+    nseg = _cu_info(cu_seqlens)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = new_workspace(nseg, total, H, d, max_seqlen, False, q.device) if workspace is None else workspace
+    st = lib.vlc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseg, total, H, d,
+                          int(max_seqlen), _scale(softmax_scale, d), float(rope_theta), _ptr(out),
+                          _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device))
+    _check(st, "vlc_attn_fwd")
+    if check:
+        _raise_device_error(ws, "vlc_attn_fwd")
+    return out, lse
+
+
+def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                    o: torch.Tensor, lse: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,
+                    softmax_scale: Optional[float] = None, rope_theta: float = 10000.0,
+                    dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+                    dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    check: bool = True):
+    """Gradients (dQ, dK, dV) of sum(O * dO) for the forward above."""
+    lib = load_library()
+    _require_cuda(dout, q, k, v, o, lse, cu_seqlens)
+    _check_qkv(dout, q, k, v, o)
+    total, H, d = q.shape
+    nseg = _cu_info(cu_seqlens)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [H, total]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = new_workspace(nseg, total, H, d, max_seqlen, True, q.device) if workspace is None else workspace
+    st = lib.vlc_attn_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                          _ptr(cu_seqlens), nseg, total, H, d, int(max_seqlen),
+                          _scale(softmax_scale, d), float(rope_theta), _ptr(dq), _ptr(dk), _ptr(dv),
+                          _ptr(ws), ws.numel(), _stream(q.device))
+    _check(st, "vlc_attn_bwd")
+    if check:
+        _raise_device_error(ws, "vlc_attn_bwd")
+    return dq, dk, dv

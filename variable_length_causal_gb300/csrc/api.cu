@@ -1,0 +1,286 @@
+// api.cu -- the extern "C" boundary declared in include/vlc.h: host-side
+// argument checks, workspace layout, TMA descriptor encoding and the launch
+// sequence of each call.  No device memory is allocated here.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/vlc.h"
+#include "internal.h"
+
+namespace vlc {
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+static int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t max_seqlen,
+                   int is_bwd) {
+    WsLayout L{};
+    const int min_tile = is_bwd ? (kBwdBM < kFwdBM ? kBwdBM : kFwdBM) : kFwdBM;
+    L.item_cap = static_cast<int64_t>(nseg) + static_cast<int64_t>(total) / min_tile + 1;
+    L.table_rows = static_cast<int32_t>(ceil_div64(max_seqlen, kTablePad) * kTablePad);
+    size_t off = 0;
+    L.header = off;
+    off = align256(off + sizeof(WsHeader));
+    L.items = off;
+    off = align256(off + sizeof(int4) * static_cast<size_t>(L.item_cap) * (is_bwd ? 2 : 1));
+    L.order = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(nseg) * (is_bwd ? 2 : 1));
+    L.seg_base = off;
+    off = align256(off + sizeof(int32_t) * static_cast<size_t>(nseg + 1) * (is_bwd ? 2 : 1));
+    L.table = off;
+    off = align256(off + sizeof(float2) * static_cast<size_t>(L.table_rows) * (d / 2));
+    L.delta = off;
+    if (is_bwd) {
+        L.delta = off;
+        off = align256(off + sizeof(float) * static_cast<size_t>(H) * total);
+    }
+    L.total = off;
+    return L;
+}
+
+static int num_sms_cached() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [total, H, d] bf16, boxes of 64 (d) x 1 (head) x box_rows (tokens), 128-byte swizzle.
+// Rows past `total` read as zeros.
+bool make_tmap_thd(CUtensorMap* map, const void* base, int32_t total, int32_t H, int32_t d,
+                   int box_rows) {
+    auto enc = get_encode();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(total)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace vlc
+
+using namespace vlc;
+
+static bool aligned(const void* p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+extern "C" {
+
+const char* vlc_status_string(int status) {
+    switch (status) {
+        case VLC_OK: return "ok";
+        case VLC_ERR_ARG: return "invalid argument";
+        case VLC_ERR_CU_SEQLENS: return "invalid cu_seqlens / max_seqlen";
+        case VLC_ERR_UNSUPPORTED: return "unsupported shape";
+        case VLC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case VLC_ERR_CUDA: return "CUDA error";
+        case VLC_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int vlc_version(void) { return 100; }
+
+size_t vlc_workspace_bytes(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t max_seqlen,
+                           int is_bwd) {
+    if (nseg < 1 || total < 1 || H < 1 || (d != 64 && d != 128) || max_seqlen < 1 ||
+        max_seqlen > VLC_MAX_SEQLEN)
+        return 0;
+    return ws_layout(nseg, total, H, d, max_seqlen, is_bwd ? 1 : 0).total;
+}
+
+int64_t vlc_worklist_capacity(int32_t nseg, int32_t total, int32_t tile) {
+    if (nseg < 1 || total < 1 || tile < 1) return 0;
+    return static_cast<int64_t>(nseg) + static_cast<int64_t>(total) / tile + 1;
+}
+
+int vlc_build_positions_labels(const int32_t* cu, int32_t nseg, const int64_t* tokens,
+                               int32_t total, const uint8_t* seg_ignore, int32_t* pos_out,
+                               int64_t* labels_out, int32_t* err_out, void* stream) {
+    if (cu == nullptr || tokens == nullptr || pos_out == nullptr || labels_out == nullptr)
+        return VLC_ERR_ARG;
+    if (nseg < 1 || total < 1) return VLC_ERR_ARG;
+    if (!aligned(tokens, 8) || !aligned(pos_out, 4) || !aligned(labels_out, 8)) return VLC_ERR_ARG;
+    cudaError_t e = launch_positions_labels(cu, nseg, tokens, total, seg_ignore, pos_out,
+                                            labels_out, err_out,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VLC_OK : VLC_ERR_CUDA;
+}
+
+int vlc_build_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
+                       int32_t BM, int32_t BN, int kind, int32_t* items_out, int64_t capacity,
+                       int32_t* seg_order_out, int32_t* count_out, int32_t* err_out,
+                       void* stream) {
+    if (cu == nullptr || items_out == nullptr || seg_order_out == nullptr ||
+        count_out == nullptr || err_out == nullptr)
+        return VLC_ERR_ARG;
+    if (nseg < 1 || total < 1 || max_seqlen < 1) return VLC_ERR_ARG;
+    if (kind != VLC_WORKLIST_FWD && kind != VLC_WORKLIST_BWD) return VLC_ERR_ARG;
+    auto pow2ok = [](int32_t t) { return t >= 16 && t <= 256 && (t & (t - 1)) == 0; };
+    if (!pow2ok(BM) || !pow2ok(BN)) return VLC_ERR_ARG;
+    if (max_seqlen > VLC_MAX_SEQLEN) return VLC_ERR_UNSUPPORTED;
+    const int32_t tile = (kind == VLC_WORKLIST_FWD) ? BM : BN;
+    if (ceil_div64(max_seqlen, tile) + 1 > 16384) return VLC_ERR_UNSUPPORTED;
+    if (capacity < vlc_worklist_capacity(nseg, total, tile)) return VLC_ERR_WORKSPACE;
+    if (!aligned(items_out, 16)) return VLC_ERR_ARG;
+    cudaError_t e = launch_worklist(cu, nseg, total, max_seqlen, BM, BN, kind,
+                                    reinterpret_cast<int4*>(items_out), capacity, seg_order_out,
+                                    seg_order_out + nseg, count_out, err_out,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VLC_OK : VLC_ERR_CUDA;
+}
+
+static int check_attn_args(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t max_seqlen,
+                           void* ws, size_t ws_bytes, int is_bwd) {
+    if (nseg < 1 || total < 1 || H < 1 || max_seqlen < 1) return VLC_ERR_ARG;
+    if (d != 64 && d != 128) return VLC_ERR_UNSUPPORTED;
+    if (max_seqlen > VLC_MAX_SEQLEN) return VLC_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(total) * H * d > (int64_t(1) << 40)) return VLC_ERR_UNSUPPORTED;
+    if (ws == nullptr || !aligned(ws, 256)) return VLC_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(nseg, total, H, d, max_seqlen, is_bwd).total) return VLC_ERR_WORKSPACE;
+    return VLC_OK;
+}
+
+int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                 int32_t total, int32_t H, int32_t d, int32_t max_seqlen, float softmax_scale,
+                 float rope_theta, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    if (q == nullptr || k == nullptr || v == nullptr || cu == nullptr || o == nullptr ||
+        lse == nullptr)
+        return VLC_ERR_ARG;
+    int st = check_attn_args(nseg, total, H, d, max_seqlen, ws, ws_bytes, 0);
+    if (st != VLC_OK) return st;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4))
+        return VLC_ERR_ARG;
+    if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return VLC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(nseg, total, H, d, max_seqlen, 0);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
+    int4* items = reinterpret_cast<int4*>(w + L.items);
+    int32_t* order = reinterpret_cast<int32_t*>(w + L.order);
+    int32_t* seg_base = reinterpret_cast<int32_t*>(w + L.seg_base);
+    float2* table = reinterpret_cast<float2*>(w + L.table);
+
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
+    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items,
+                        L.item_cap, order, seg_base, &hdr->count, &hdr->err, s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    const bool rope = rope_theta != 0.f;
+    if (rope && launch_rope_table(table, L.table_rows, d, static_cast<double>(rope_theta),
+                                  &hdr->err, s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    FwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu = cu;
+    p.items = items; p.seg_base = seg_base; p.count = &hdr->count; p.err = &hdr->err;
+    p.table = rope ? table : nullptr;
+    p.nseg = nseg; p.total = total; p.H = H; p.d = d;
+    const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.use_rope = rope ? 1 : 0;
+    if (launch_attn_fwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
+    return VLC_OK;
+}
+
+int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
+                 int32_t d, int32_t max_seqlen, float softmax_scale, float rope_theta, void* dq,
+                 void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+    if (dout == nullptr || q == nullptr || k == nullptr || v == nullptr || o == nullptr ||
+        lse == nullptr || cu == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+        return VLC_ERR_ARG;
+    int st = check_attn_args(nseg, total, H, d, max_seqlen, ws, ws_bytes, 1);
+    if (st != VLC_OK) return st;
+    for (const void* ptr : {dout, q, k, v, o, static_cast<const void*>(dq),
+                            static_cast<const void*>(dk), static_cast<const void*>(dv)})
+        if (!aligned(ptr, 16)) return VLC_ERR_ARG;
+    if (!aligned(lse, 4)) return VLC_ERR_ARG;
+    if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return VLC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(nseg, total, H, d, max_seqlen, 1);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
+    int4* items_q = reinterpret_cast<int4*>(w + L.items);
+    int4* items_k = items_q + L.item_cap;
+    int32_t* order = reinterpret_cast<int32_t*>(w + L.order);
+    int32_t* seg_base_q = reinterpret_cast<int32_t*>(w + L.seg_base);
+    int32_t* seg_base_k = seg_base_q + (nseg + 1);
+    float2* table = reinterpret_cast<float2*>(w + L.table);
+
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
+    // q-tile items (dQ pass) and key-tile items (dK/dV pass)
+    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items_q,
+                        L.item_cap, order, seg_base_q, &hdr->count, &hdr->err, s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    if (launch_worklist(cu, nseg, total, max_seqlen, kBwdBM, kFwdBN, VLC_WORKLIST_BWD, items_k,
+                        L.item_cap, order + nseg, seg_base_k, &hdr->pad[0], &hdr->err, s) !=
+        cudaSuccess)
+        return VLC_ERR_CUDA;
+    const bool rope = rope_theta != 0.f;
+    if (rope && launch_rope_table(table, L.table_rows, d, static_cast<double>(rope_theta),
+                                  &hdr->err, s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    BwdParams p{};
+    p.dout = dout; p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.cu = cu;
+    p.items = items_q; p.seg_base = seg_base_q; p.count = &hdr->count; p.err = &hdr->err;
+    p.items_k = items_k; p.seg_base_k = seg_base_k; p.count_k = &hdr->pad[0];
+    p.table = rope ? table : nullptr;
+    p.delta = reinterpret_cast<float*>(w + L.delta);
+    p.nseg = nseg; p.total = total; p.H = H; p.d = d;
+    p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
+    p.use_rope = rope ? 1 : 0;
+    if (launch_attn_bwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
+    return VLC_OK;
+}
+
+int vlc_get_error(const void* ws, int32_t* bits_out, void* stream) {
+    if (ws == nullptr) return VLC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t bits = 0;
+    if (cudaMemcpyAsync(&bits, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return VLC_ERR_CUDA;
+    if (bits_out != nullptr) *bits_out = bits;
+    if (bits & VLC_DEVERR_TIMEOUT) return VLC_ERR_TIMEOUT;
+    if (bits != 0) return VLC_ERR_CU_SEQLENS;
+    return VLC_OK;
+}
+
+}  // extern "C"

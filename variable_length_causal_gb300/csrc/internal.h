@@ -1,0 +1,91 @@
+// internal.h -- declarations shared by the C-ABI layer and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace vlc {
+
+constexpr int kFwdBM = 128;   // query rows per forward tile
+constexpr int kFwdBN = 128;   // key rows per forward tile
+constexpr int kBwdBM = 64;    // query rows per backward step
+constexpr int kBwdBN = 64;    // key rows per backward tile
+constexpr int kTablePad = 128;  // RoPE table rows are padded to a multiple of this
+
+// Workspace header (first 256 bytes).
+struct WsHeader {
+    int32_t err;          // VLC_DEVERR_* bits
+    int32_t count;        // work items written by the work-list kernel
+    int32_t pad[62];
+};
+
+// Byte offsets of the workspace regions for one problem size.
+struct WsLayout {
+    size_t header, items, order, seg_base, table, delta, total;
+    int64_t item_cap;
+    int32_t table_rows;
+};
+
+WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t max_seqlen,
+                   int is_bwd);
+
+// Kernel launchers (return cudaGetLastError()).
+cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64_t* tokens,
+                                    int32_t total, const uint8_t* seg_ignore, int32_t* pos,
+                                    int64_t* labels, int32_t* err, cudaStream_t s);
+
+cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
+                            int32_t BM, int32_t BN, int kind, int4* items, int64_t cap,
+                            int32_t* order, int32_t* seg_base, int32_t* count, int32_t* err,
+                            cudaStream_t s);
+
+cudaError_t launch_rope_table(float2* table, int32_t rows, int32_t d, double theta,
+                              const int32_t* err, cudaStream_t s);
+
+struct FwdParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    const int32_t* cu;
+    const int4* items;
+    const int32_t* seg_base;   // [nseg+1] item offsets of the sorted segments
+    const int32_t* count;
+    int32_t* err;
+    const float2* table;       // RoPE cos/sin [rows][d/2], null if no RoPE
+    int32_t nseg, total, H, d;
+    float scale_log2;          // softmax_scale * log2(e)
+    int use_rope;
+};
+
+cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s);
+
+struct BwdParams {
+    const void* dout;
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;
+    const float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+    const int32_t* cu;
+    const int4* items;         // q-tile items (dQ pass), as in the forward
+    const int32_t* seg_base;
+    const int32_t* count;
+    const int4* items_k;       // key-tile items (dK/dV pass)
+    const int32_t* seg_base_k;
+    const int32_t* count_k;
+    int32_t* err;
+    const float2* table;
+    float* delta;              // [H, total]: rowsum(dO * O)
+    int32_t nseg, total, H, d;
+    float scale;
+    int use_rope;
+};
+
+cudaError_t launch_attn_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
+
+}  // namespace vlc

@@ -1,0 +1,344 @@
+// prep.cu -- the integer/metadata kernels of the path:
+//   * work-list builder: validates cu_seqlens and emits only in-segment,
+//     at-or-below-diagonal tiles ("Sequence packing and variable-length
+//     attention", charlestar: validity contract and allow(i,j); "Packing document
+//     boundary", operatorworld, pitfall 1: the varlen kernel skips cross-document
+//     blocks);
+//   * positions and labels: p_i = i - cu_r and pre-shifted labels with -100 at
+//     segment ends ("Length grouping, de-padding and packing", M020 section 06);
+//   * RoPE cos/sin table for fixed frequencies theta^(-2j/d).
+#include <cstdint>
+
+#include "../../include/vlc.h"
+#include "internal.h"
+
+namespace vlc {
+
+// ============================================================== work list
+//
+// One CTA of 1024 threads.  Segments are ordered by descending tile count with
+// a stable counting sort (histogram over tile counts, exclusive scan from the
+// largest count down, then in-order placement warp by warp so that equal
+// counts keep their segment order).
+
+constexpr int kWlThreads = 1024;
+
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int* total_out) {
+    // Exclusive scan of one int per thread across the CTA (1024 threads).
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+        int s = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s - w;   // exclusive prefix of warp totals
+        if (lane == 31) warp_sums[32] = s;
+    }
+    __syncthreads();
+    int r = x - v + warp_sums[warp];
+    *total_out = warp_sums[32];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kWlThreads, 1)
+worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int32_t max_seqlen,
+                int32_t BM, int32_t BN, int kind, int4* __restrict__ items, int64_t cap,
+                int32_t* __restrict__ order, int32_t* __restrict__ seg_base,
+                int32_t* __restrict__ count, int32_t* __restrict__ err) {
+    extern __shared__ int wl_smem[];
+    int* hist = wl_smem;                    // [nbins] counts, then running positions
+    __shared__ int warp_sums[33];
+    __shared__ int s_err, s_maxlen;
+    const int tid = threadIdx.x;
+    const int tile = (kind == VLC_WORKLIST_FWD) ? BM : BN;
+    const int nbins = (max_seqlen + tile - 1) / tile + 1;
+
+    if (tid == 0) {
+        s_err = 0;
+        s_maxlen = 0;
+    }
+    for (int b = tid; b < nbins; b += kWlThreads) hist[b] = 0;
+    __syncthreads();
+
+    // ---- 1. validate cu_seqlens
+    int local_err = 0, local_max = 0;
+    for (int r = tid; r < nseg; r += kWlThreads) {
+        int a = cu[r], b = cu[r + 1];
+        if (r == 0 && a != 0) local_err |= VLC_DEVERR_CU_FIRST;
+        if (b <= a) local_err |= VLC_DEVERR_CU_ORDER;
+        local_max = max(local_max, b - a);
+    }
+    if (tid == 0 && cu[nseg] != total) local_err |= VLC_DEVERR_CU_TOTAL;
+    if (local_err) atomicOr(&s_err, local_err);
+    atomicMax(&s_maxlen, local_max);
+    __syncthreads();
+    if (tid == 0 && s_maxlen != max_seqlen) s_err |= VLC_DEVERR_MAXLEN;
+    __syncthreads();
+    if (s_err != 0) {
+        if (tid == 0) {
+            atomicOr(err, s_err);
+            *count = 0;
+        }
+        return;
+    }
+
+    // ---- 2. histogram of tile counts
+    for (int r = tid; r < nseg; r += kWlThreads) {
+        int n = (cu[r + 1] - cu[r] + tile - 1) / tile;
+        atomicAdd(&hist[n], 1);
+    }
+    __syncthreads();
+
+    // ---- 3. start position of each bin in descending-count order:
+    //         start[b] = number of segments with count > b.
+    //         Thread t owns bins [t*per, (t+1)*per) counted from the top.
+    {
+        const int per = (nbins + kWlThreads - 1) / kWlThreads;
+        int vals[16];
+        int sum = 0;
+        for (int i = 0; i < per; ++i) {
+            int rb = tid * per + i;          // rank from the top
+            int b = nbins - 1 - rb;
+            int c = (rb < nbins) ? hist[b] : 0;
+            if (i < 16) vals[i] = c;
+            sum += c;
+        }
+        int tot;
+        int base = block_excl_scan(sum, warp_sums, &tot);
+        for (int i = 0; i < per; ++i) {
+            int rb = tid * per + i;
+            if (rb < nbins) {
+                int b = nbins - 1 - rb;
+                hist[b] = base;             // becomes the running position of bin b
+                base += vals[i];
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- 4. stable placement, one warp at a time inside each chunk of 1024
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int c0 = 0; c0 < nseg; c0 += kWlThreads) {
+        const int r = c0 + tid;
+        const bool valid = r < nseg;
+        const int n = valid ? (cu[r + 1] - cu[r] + tile - 1) / tile : -1;
+        for (int w = 0; w < kWlThreads / 32; ++w) {
+            if (warp == w) {
+                unsigned peers = __match_any_sync(0xffffffffu, n);
+                int leader = __ffs(peers) - 1;
+                int rank = __popc(peers & ((1u << lane) - 1u));
+                int base = 0;
+                if (valid && lane == leader) {
+                    base = hist[n];
+                    hist[n] = base + __popc(peers);
+                }
+                base = __shfl_sync(peers, base, leader);
+                if (valid) order[base + rank] = r;
+            }
+            __syncthreads();
+        }
+    }
+    __syncthreads();
+
+    // ---- 5. item offset of each sorted segment (exclusive scan of tile counts)
+    int carry = 0;
+    for (int c0 = 0; c0 < nseg; c0 += kWlThreads) {
+        const int k = c0 + tid;
+        int n = 0;
+        if (k < nseg) {
+            int r = order[k];
+            n = (cu[r + 1] - cu[r] + tile - 1) / tile;
+        }
+        int tot;
+        int ex = block_excl_scan(n, warp_sums, &tot);
+        if (k < nseg) seg_base[k] = carry + ex;
+        carry += tot;
+    }
+    if (tid == 0) seg_base[nseg] = carry;
+    __syncthreads();
+
+    // ---- 6. items (host guarantees cap >= nseg + total / tile >= carry)
+    for (int k = tid; k < nseg; k += kWlThreads) {
+        const int r = order[k];
+        const int L = cu[r + 1] - cu[r];
+        const int base = seg_base[k];
+        const int n = seg_base[k + 1] - base;
+        for (int j = 0; j < n; ++j) {
+            int4 it;
+            it.x = r;
+            if (kind == VLC_WORKLIST_FWD) {
+                const int qt = n - 1 - j;
+                const int last = min(L, (qt + 1) * BM);
+                it.y = qt;
+                it.z = 0;
+                it.w = (last + BN - 1) / BN;
+            } else {
+                const int kt = j;
+                it.y = kt;
+                it.z = (kt * BN) / BM;
+                it.w = (L + BM - 1) / BM;
+            }
+            if (base + j < cap) items[base + j] = it;
+        }
+    }
+    if (tid == 0) *count = carry;
+}
+
+cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
+                            int32_t BM, int32_t BN, int kind, int4* items, int64_t cap,
+                            int32_t* order, int32_t* seg_base, int32_t* count, int32_t* err,
+                            cudaStream_t s) {
+    const int tile = (kind == VLC_WORKLIST_FWD) ? BM : BN;
+    const int nbins = (max_seqlen + tile - 1) / tile + 1;
+    const size_t smem = sizeof(int) * static_cast<size_t>(nbins);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(worklist_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    worklist_kernel<<<1, kWlThreads, smem, s>>>(cu, nseg, total, max_seqlen, BM, BN, kind, items,
+                                                cap, order, seg_base, count, err);
+    return cudaGetLastError();
+}
+
+// ============================================================== positions + labels
+//
+// Each thread handles 4 consecutive tokens: one binary search over cu for the
+// first, then forward steps.  Loads and stores are vectorised (16 B).
+
+constexpr int kPlThreads = 256;
+constexpr int kPlVec = 4;
+
+__global__ void __launch_bounds__(kPlThreads)
+positions_labels_kernel(const int32_t* __restrict__ cu, int32_t nseg,
+                        const int64_t* __restrict__ tokens, int32_t total,
+                        const uint8_t* __restrict__ seg_ignore, int32_t* __restrict__ pos,
+                        int64_t* __restrict__ labels, int32_t* __restrict__ err) {
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+
+    if (err != nullptr) {   // validity bits (cheap: nseg reads in total)
+        int e = 0;
+        for (int64_t r = gtid; r < nseg; r += nthreads) {
+            if (r == 0 && cu[0] != 0) e |= VLC_DEVERR_CU_FIRST;
+            if (cu[r + 1] <= cu[r]) e |= VLC_DEVERR_CU_ORDER;
+        }
+        if (gtid == 0 && cu[nseg] != total) e |= VLC_DEVERR_CU_TOTAL;
+        if (e) atomicOr(err, e);
+    }
+
+    const bool vec_ok = ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(labels)) & 15) == 0;
+    const int64_t ngroups = (static_cast<int64_t>(total) + kPlVec - 1) / kPlVec;
+    for (int64_t g = gtid; g < ngroups; g += nthreads) {
+        const int64_t i0 = g * kPlVec;
+        // largest r in [0, nseg-1] with cu[r] <= i0 (clamped; in bounds even for bad cu)
+        int lo = 0, hi = nseg - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (__ldg(cu + mid) <= i0) lo = mid; else hi = mid - 1;
+        }
+        int r = lo;
+        int32_t p[kPlVec];
+        int64_t lab[kPlVec];
+        int32_t seg_start = __ldg(cu + r), seg_end = __ldg(cu + r + 1);
+        bool full = (i0 + kPlVec <= total);
+        int64_t tk[kPlVec + 1];
+#pragma unroll
+        for (int t = 0; t <= kPlVec; ++t)
+            tk[t] = (i0 + t < total) ? __ldg(tokens + i0 + t) : 0;
+#pragma unroll
+        for (int t = 0; t < kPlVec; ++t) {
+            const int64_t i = i0 + t;
+            while (r < nseg - 1 && i >= seg_end) {
+                ++r;
+                seg_start = seg_end;
+                seg_end = __ldg(cu + r + 1);
+            }
+            const bool ign = seg_ignore != nullptr && __ldg(seg_ignore + r) != 0;
+            p[t] = static_cast<int32_t>(i - seg_start);
+            lab[t] = (!ign && i + 1 < seg_end) ? tk[t + 1] : -100;
+        }
+        if (full && vec_ok) {
+            *reinterpret_cast<int4*>(pos + i0) = make_int4(p[0], p[1], p[2], p[3]);
+            reinterpret_cast<longlong2*>(labels + i0)[0] = make_longlong2(lab[0], lab[1]);
+            reinterpret_cast<longlong2*>(labels + i0)[1] = make_longlong2(lab[2], lab[3]);
+        } else {
+            for (int t = 0; t < kPlVec; ++t)
+                if (i0 + t < total) {
+                    pos[i0 + t] = p[t];
+                    labels[i0 + t] = lab[t];
+                }
+        }
+    }
+}
+
+cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64_t* tokens,
+                                    int32_t total, const uint8_t* seg_ignore, int32_t* pos,
+                                    int64_t* labels, int32_t* err, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t groups = (static_cast<int64_t>(total) + kPlVec - 1) / kPlVec;
+    int64_t blocks = (groups + kPlThreads - 1) / kPlThreads;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;   // 8 resident CTAs per SM, grid-stride beyond
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    positions_labels_kernel<<<static_cast<int>(blocks), kPlThreads, 0, s>>>(
+        cu, nseg, tokens, total, seg_ignore, pos, labels, err);
+    return cudaGetLastError();
+}
+
+// ============================================================== RoPE table
+//
+// table[p][j] = (cos(p w_j), sin(p w_j)), w_j = theta^(-2j/d).  The angle is
+// formed in fp64 and reduced to [-pi, pi] in fp64 (one fused multiply-add
+// against 2*pi in double), so the fp32 sincos that follows sees a small
+// argument; the result is accurate to a few 1e-7 even at p ~ 1e6.
+
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+
+__global__ void rope_table_kernel(float2* __restrict__ table, int32_t rows, int32_t half,
+                                  double log2_theta, const int32_t* __restrict__ err) {
+    if (err != nullptr && *err != 0) return;
+    __shared__ double w[256];
+    for (int j = threadIdx.x; j < half; j += blockDim.x)
+        w[j] = exp2(-2.0 * static_cast<double>(j) / static_cast<double>(2 * half) * log2_theta);
+    __syncthreads();
+    const int64_t n = static_cast<int64_t>(rows) * half;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t p = idx / half;
+        const int j = static_cast<int>(idx - p * half);
+        const double x = static_cast<double>(p) * w[j];
+        const double k = rint(x * (1.0 / kTwoPi));
+        const double red = fma(-k, kTwoPi, x);
+        float sn, cs;
+        sincosf(static_cast<float>(red), &sn, &cs);
+        table[idx] = make_float2(cs, sn);
+    }
+}
+
+cudaError_t launch_rope_table(float2* table, int32_t rows, int32_t d, double theta,
+                              const int32_t* err, cudaStream_t s) {
+    const int half = d / 2;
+    const int64_t n = static_cast<int64_t>(rows) * half;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    rope_table_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(table, rows, half, log2(theta), err);
+    return cudaGetLastError();
+}
+
+}  // namespace vlc
