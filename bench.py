@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of the packed varlen causal attention path on GB300.
+
+One step = the whole hot path over one synthetic packed batch:
+  positions + labels  ->  forward attention (work list, RoPE table, tcgen05 kernel)
+  ->  backward attention (work lists, delta, dQ pass, dK/dV pass).
+Metric: effective TFLOP/s counting only in-segment causal FLOPs of real (non-pad)
+segments, 4*d*H*pairs (forward) + 10*d*H*pairs (backward); packed real tokens/s
+is reported beside it.  Default workload: the SFT pack (16 x 4096 tokens,
+lognormal(300, 1.0) lengths packed first-fit-decreasing, H=32, d=128).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+
+With --impl reference the fp64 CPU oracle is timed on the host cores instead (a
+bounded sample of the same workload per step).  Under torchrun each rank runs its
+own independently seeded pack on its own GPU (weak scaling, no collective on the
+data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from variable_length_causal_gb300 import synth  # noqa: E402
+
+METRIC = "varlen causal attn effective TFLOP/s (in-segment FLOPs only); packed tokens/s"
+UNIT = "TFLOP/s"
+WORKLOAD_BY_NAME = {n: i for i, n in enumerate(synth.WORKLOAD_NAMES)}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+def make_inputs(w: synth.Workload, device, rank: int):
+    seed = 1000 + max(w.index, 0) + 7919 * rank
+    q, k, v, g = synth.make_tensors(w, device=device, seed=seed, with_grad=True)
+    tokens = torch.from_numpy(synth.make_tokens(w, seed=2000 + w.index + rank)).to(device)
+    cu = torch.from_numpy(w.cu).to(device)
+    ign = torch.from_numpy(w.seg_ignore).to(device)
+    return q, k, v, g, tokens, cu, ign
+
+
+class Step:
+    """Pre-allocated buffers and one call per path step (no allocation inside the step)."""
+
+    def __init__(self, vlc, w, q, k, v, g, tokens, cu, ign):
+        self.vlc, self.w = vlc, w
+        self.q, self.k, self.v, self.g, self.tokens, self.cu, self.ign = q, k, v, g, tokens, cu, ign
+        dev = q.device
+        self.o = torch.empty_like(q)
+        self.lse = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        self.ws_f = vlc.new_workspace(w.nseg, w.total, w.H, w.d, w.max_seqlen, False, dev)
+        self.ws_b = vlc.new_workspace(w.nseg, w.total, w.H, w.d, w.max_seqlen, True, dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def __call__(self, ev=None):
+        vlc, w = self.vlc, self.w
+        if ev is not None:
+            ev[0].record()
+        self.pos, self.lab = vlc.build_positions_labels(self.cu, self.tokens, self.ign, err=self.err)
+        if ev is not None:
+            ev[1].record()
+        vlc.varlen_attn_fwd(self.q, self.k, self.v, self.cu, w.max_seqlen, out=self.o, lse=self.lse,
+                            workspace=self.ws_f, check=False)
+        if ev is not None:
+            ev[2].record()
+        vlc.varlen_attn_bwd(self.g, self.q, self.k, self.v, self.o, self.lse, self.cu, w.max_seqlen,
+                            dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws_b, check=False)
+        if ev is not None:
+            ev[3].record()
+
+    def check_errors(self):
+        for ws in (self.ws_f, self.ws_b):
+            st, bits = self.vlc.get_error(ws)
+            if st != 0:
+                raise RuntimeError(f"device error status {st} bits 0x{bits:x}")
+        if int(self.err.item()) != 0:
+            raise RuntimeError("positions/labels reported invalid cu_seqlens")
+
+
+LAUNCHES_PER_STEP = 1 + 3 + 6   # posl; worklist+table+fwd; 2 worklists+table+delta+dq+dkdv
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_sample(w: synth.Workload, q, k, v, g, budget_s: float):
+    """Pick (segment, head) pairs of real segments in a seeded order until the oracle's
+    estimated fwd+bwd time on all host threads fills ``budget_s``; returns the pairs and
+    their legal-pair count.  q/k/v/g are uint16 bf16 bit arrays (converted once)."""
+    import oracle
+
+    rng = np.random.default_rng(12345)
+    real = np.nonzero(w.seg_ignore == 0)[0]
+    order = rng.permutation(len(real))
+    threads = max(oracle.num_threads(), 1)
+    r0 = int(real[order[0]])
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, w.cu, seg_heads=[(r0, 0)])
+    oracle.attn_bwd(g, q, k, v, w.cu, seg_heads=[(r0, 0)])
+    dt = max(time.perf_counter() - t0, 1e-4)
+    L0 = int(w.lengths[r0])
+    per_pair = dt / max(L0 * (L0 + 1) // 2, 1)          # single-thread seconds per legal pair
+    pairs, total_pairs, work = [], 0, 0.0
+    for n, i in enumerate(order):
+        r = int(real[i])
+        L = int(w.lengths[r])
+        pc = L * (L + 1) // 2
+        pairs.append((r, int(rng.integers(0, w.H))))
+        total_pairs += pc
+        work += pc * per_pair
+        if work >= budget_s * threads and n + 1 >= threads:
+            break
+    return pairs, total_pairs
+
+
+def run_oracle_step(w, q, k, v, g, tokens_np, pairs):
+    import oracle
+
+    oracle.positions_labels(w.cu, tokens_np, w.seg_ignore)
+    oracle.attn_fwd(q, k, v, w.cu, seg_heads=pairs)
+    oracle.attn_bwd(g, q, k, v, w.cu, seg_heads=pairs)
+
+
+def reference_arm(args, w, world, rank):
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    q, k, v, g = (oracle.bf16_bits(t) for t in synth.make_tensors(w, seed=1000 + w.index, with_grad=True))
+    tokens_np = synth.make_tokens(w)
+    pairs, npairs = oracle_sample(w, q, k, v, g, budget_s=args.ref_step_seconds)
+    for _ in range(args.warmup):
+        run_oracle_step(w, q, k, v, g, tokens_np, pairs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_step(w, q, k, v, g, tokens_np, pairs)
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = 14.0 * w.d * npairs
+    value = flops / dt / 1e12
+    tok = sum(int(w.lengths[r]) for r, _ in pairs) / w.H
+    sample = (f"{len(pairs)} (segment, head) pairs of the {w.name} pack ({npairs} legal pairs), "
+              f"fwd + bwd + positions/labels of the whole pack, fp64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w, world, "oracle sample"),
+        "tokens_per_s": tok / dt,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w, world, flush):
+    return {"workload": f"{w.name}: {w.description}", "nseg": w.nseg, "real_segments": int((w.seg_ignore == 0).sum()),
+            "total_tokens": w.total, "real_tokens": int(w.real_lengths.sum()), "H": w.H, "head_dim": w.d,
+            "max_seqlen": w.max_seqlen, "rope_theta": w.theta, "legal_pairs": synth.causal_pairs(w.real_lengths),
+            "tile_efficiency_128": round(synth.tile_efficiency(w), 4),
+            "slot_efficiency": round(float(w.real_lengths.sum()) / w.total, 4),
+            "parallelism": f"dp{world} (independent packs per GPU)", "l2": flush}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def gpu_arm(args, w, world, rank, local):
+    import variable_length_causal_gb300 as vlc
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    vlc.load_library()
+    peaks = _peaks()
+    q, k, v, g, tokens, cu, ign = make_inputs(w, dev, rank)
+    step = Step(vlc, w, q, k, v, g, tokens, cu, ign)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    step.check_errors()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    step.check_errors()
+    ms_local = start.elapsed_time(stop) / args.steps
+    ms = max_over_ranks(ms_local, world, dev)
+    t_pos = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    t_fwd = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    t_bwd = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+    fl_f, fl_b = synth.fwd_flops(w), synth.bwd_flops(w)
+    flops_all = sum_over_ranks(fl_f + fl_b, world, dev)
+    real_tok = sum_over_ranks(float(w.real_lengths.sum()), world, dev)
+    value = flops_all / (ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API, pinned host buffers in and out
+    e2e = e2e_measure(vlc, w, step, args.steps, world, dev)
+
+    if rank != 0:
+        return
+    tb = w.total * w.H
+    fwd_tflops = fl_f / (t_fwd * 1e-3) / 1e12
+    bwd_tflops = fl_b / (t_bwd * 1e-3) / 1e12
+    pos_bytes = 20.0 * w.total
+    kernels = {
+        "positions_labels": {"ms": t_pos, "GB/s": pos_bytes / (t_pos * 1e-3) / 1e9},
+        "attn_fwd_call": {"ms": t_fwd, "eff_TFLOP/s": fwd_tflops,
+                          "kernels": "worklist + rope_table + attn_fwd_kernel"},
+        "attn_bwd_call": {"ms": t_bwd, "eff_TFLOP/s": bwd_tflops,
+                          "kernels": "2 worklists + rope_table + delta + dq_kernel + dkdv_kernel"},
+    }
+    dominant = "attn_bwd_call" if t_bwd >= t_fwd else "attn_fwd_call"
+    ach = bwd_tflops if dominant == "attn_bwd_call" else fwd_tflops
+    traffic = _traffic_from_profiles(dominant)
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_source": f"{peaks['source']} bf16 burst",
+                "algorithmic": ("10*d*H*pairs" if dominant == "attn_bwd_call" else "4*d*H*pairs")
+                + " FLOP per call, real segments only"}
+    roofline_fwd = {"bound": "tensor", "achieved": fwd_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": fwd_tflops / peaks["bf16_tflops"]}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _config(w, world, f"inputs larger than L2 ({4 * tb * w.d * 2 / 2**30:.1f} GiB q/k/v/dO vs 129 MB)"),
+        "tokens_per_s": real_tok / (ms * 1e-3),
+        "fwd_eff_tflops": fwd_tflops, "bwd_eff_tflops": bwd_tflops,
+        "kernels": kernels, "roofline": roofline, "roofline_fwd": roofline_fwd,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, q, k, v, g, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def e2e_measure(vlc, w, step, steps, world, dev):
+    """Same metric through the public API with pinned host buffers: every step copies this
+    step's inputs host->device and reads back every output device->host."""
+    host_in = [t.cpu().pin_memory() for t in (step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign)]
+    outs = (step.o, step.lse, step.dq, step.dk, step.dv)
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    host_pos = torch.empty(w.total, dtype=torch.int32).pin_memory()
+    host_lab = torch.empty(w.total, dtype=torch.int64).pin_memory()
+    dev_in = [step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out) + w.total * 12
+
+    def one():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+        host_pos.copy_(step.pos, non_blocking=True)
+        host_lab.copy_(step.lab, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    dt = max_over_ranks(dt, world, dev)
+    flops = sum_over_ranks(synth.fwd_flops(w) + synth.bwd_flops(w), world, dev)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3}
+
+
+def cpu_baseline(w, q, k, v, g, seconds):
+    import oracle
+
+    oracle.build()
+    qc, kc, vc, gc = (oracle.bf16_bits(t) for t in (q, k, v, g))
+    pairs, npairs = oracle_sample(w, qc, kc, vc, gc, budget_s=seconds)
+    tokens_np = synth.make_tokens(w)
+    t0 = time.perf_counter()
+    run_oracle_step(w, qc, kc, vc, gc, tokens_np, pairs)
+    dt = time.perf_counter() - t0
+    return {"value": 14.0 * w.d * npairs / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{len(pairs)} (segment, head) pairs of the {w.name} pack ({npairs} legal pairs): "
+                      f"fwd + bwd in fp64, plus positions/labels of the whole pack; {dt:.1f} s"}
+
+
+def _traffic_from_profiles(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if one matches this build."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(kernel)
+    except Exception:
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="vlc", choices=["vlc", "reference"])
+    ap.add_argument("--workload", default="sft", choices=synth.WORKLOAD_NAMES)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "vlc" else args.warmup
+    world, rank, local = dist_setup()
+    w = synth.workload(WORKLOAD_BY_NAME[args.workload])
+    if args.impl == "reference":
+        reference_arm(args, w, world, rank)
+    else:
+        gpu_arm(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -66,6 +66,9 @@ def _load():
             lib.orc_attn_fwd_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int,
                                               P, P, i64, P, P]
             lib.orc_attn_fwd_rows.restype = None
+            lib.orc_attn_fwd_seg_heads.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int,
+                                                   P, P, i64, P, P]
+            lib.orc_attn_fwd_seg_heads.restype = None
             lib.orc_attn_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int,
                                          P, P, P]
             lib.orc_attn_bwd.restype = None
@@ -154,16 +157,25 @@ def rope_rows(x, pos, theta: float = 10000.0) -> np.ndarray:
     return out
 
 
-def attn_fwd(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True):
+def attn_fwd(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
+             seg_heads=None):
     """Exact per-segment causal attention in fp64.  q/k/v: bf16 tensors or uint16 bit arrays
-    [total, H, d].  Returns (o [total, H, d] f64, lse [H, total] f64, natural log)."""
+    [total, H, d].  Returns (o [total, H, d] f64, lse [H, total] f64, natural log).  With
+    ``seg_heads`` (a list of (segment, head) pairs) only those are computed; the rest stay 0."""
     qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
     total, H, d = qb.shape
     cu = _c(cu, np.int32)
     o = np.zeros((total, H, d), np.float64)
     lse = np.zeros((H, total), np.float64)
-    _load().orc_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, d,
-                         float(scale), float(theta), int(bool(contract)), _ptr(o), _ptr(lse))
+    if seg_heads is None:
+        _load().orc_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, d,
+                             float(scale), float(theta), int(bool(contract)), _ptr(o), _ptr(lse))
+    else:
+        sh = np.asarray(seg_heads, np.int32).reshape(-1, 2)
+        segs, heads = np.ascontiguousarray(sh[:, 0]), np.ascontiguousarray(sh[:, 1])
+        _load().orc_attn_fwd_seg_heads(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H,
+                                       d, float(scale), float(theta), int(bool(contract)), _ptr(segs),
+                                       _ptr(heads), sh.shape[0], _ptr(o), _ptr(lse))
     return o, lse
 
 

@@ -355,6 +355,8 @@ static orc_problem make_problem(const void* q, const void* k, const void* v,
     return P;
 }
 
+static void fwd_seg_head(const orc_problem* P, int32_t r, int32_t h, double* o, double* lse);
+
 /* Full forward: o [total][H][d], lse [H][total] (natural log). */
 void orc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
                   int32_t nseg, int32_t total, int32_t H, int32_t d, double scale, double theta,
@@ -362,19 +364,30 @@ void orc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu
     orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, d, scale, theta, contract);
     int64_t nwork = (int64_t)nseg * H;
 #pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t w = 0; w < nwork; ++w) {
-        int32_t r = (int32_t)(w / H), h = (int32_t)(w % H);
-        seg_head S;
-        seg_head_load(&P, r, h, 0, &S);
-        double* s = (double*)malloc(sizeof(double) * (size_t)S.L);
-        for (int64_t p = 0; p < S.L; ++p) {
-            int64_t i = S.base + p;
-            lse[(size_t)h * total + i] =
-                fwd_row(&S, p, d, P.scale, s, o + ((size_t)i * H + h) * d);
-        }
-        free(s);
-        seg_head_free(&S);
+    for (int64_t w = 0; w < nwork; ++w) fwd_seg_head(&P, (int32_t)(w / H), (int32_t)(w % H), o, lse);
+}
+
+/* One segment-head of the forward: rows of segment r, head h. */
+static void fwd_seg_head(const orc_problem* P, int32_t r, int32_t h, double* o, double* lse) {
+    seg_head S;
+    seg_head_load(P, r, h, 0, &S);
+    double* s = (double*)malloc(sizeof(double) * (size_t)S.L);
+    for (int64_t p = 0; p < S.L; ++p) {
+        int64_t i = S.base + p;
+        lse[(size_t)h * P->total + i] = fwd_row(&S, p, P->d, P->scale, s, o + ((size_t)i * P->H + h) * P->d);
     }
+    free(s);
+    seg_head_free(&S);
+}
+
+/* Forward restricted to a set of (segment, head) pairs; other entries untouched. */
+void orc_attn_fwd_seg_heads(const void* q, const void* k, const void* v, const int32_t* cu,
+                            int32_t nseg, int32_t total, int32_t H, int32_t d, double scale,
+                            double theta, int contract, const int32_t* segs, const int32_t* heads,
+                            int64_t n, double* o, double* lse) {
+    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, d, scale, theta, contract);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n; ++t) fwd_seg_head(&P, segs[t], heads[t], o, lse);
 }
 
 /* Sampled forward: the same result for selected (token, head) pairs only,

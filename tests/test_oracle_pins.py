@@ -423,3 +423,12 @@ def test_worklist_order():
     for r in range(len(lens)):
         kts = [kt for s, kt, _, _ in bwd if s == r]
         assert kts == list(range(nq[r]))
+
+
+def test_forward_seg_heads_subset_matches_full():
+    lens = [4, 9, 3]
+    w, (q, k, v) = _rand_qkv(lens, 2, 8, seed=15)
+    o, lse = oracle.attn_fwd(q, k, v, w.cu)
+    o2, lse2 = oracle.attn_fwd(q, k, v, w.cu, seg_heads=[(1, 1), (2, 0)])
+    assert np.array_equal(o2[4:13, 1], o[4:13, 1]) and np.array_equal(lse2[1, 4:13], lse[1, 4:13])
+    assert np.array_equal(o2[13:16, 0], o[13:16, 0]) and not o2[:4].any()

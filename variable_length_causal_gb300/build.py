@@ -17,7 +17,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libvlc.so")
 SOURCES = ["api.cu", "prep.cu", "attn_fwd.cu", "attn_bwd.cu"]
-HEADERS = ["ptx.cuh", "internal.h"]
+HEADERS = ["ptx.cuh", "internal.h", "attn_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

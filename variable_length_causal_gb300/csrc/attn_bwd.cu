@@ -1,8 +1,777 @@
-// attn_bwd.cu -- backward pass (placeholder until the kernels land).
+// attn_bwd.cu -- backward of the varlen block-diagonal causal attention, sm_103a.
+//
+// Gradients of sum(O * dO) with the standard softmax-attention derivatives,
+// restricted (like the forward) to each segment's allowed pairs
+// ("Sequence packing and variable-length attention", charlestar: allow(i,j)
+// and the mask applied before the softmax; the page checks Q/K/V gradients by
+// finite differences):
+//   P = exp(S - LSE),  dV = P^T dO,  dP = dO V^T,  D_i = rowsum(dO_i * O_i),
+//   dS = P o (dP - D),  dQ' = scale dS K',  dK' = scale dS^T Q',
+//   dQ = R(p)^T dQ',  dK = R(p)^T dK'   (RoPE is orthogonal: its inverse is R(-p)).
+//
+// Three kernels, no atomics (results are bitwise reproducible):
+//   delta_kernel   D = rowsum(dO * O) in fp32, layout [H, total].
+//   dq_kernel      q-major, one unit = (q tile of 128 rows, head): for every key
+//                  tile, tcgen05 computes S = Q'K'^T and dP = dO V^T into TMEM,
+//                  128 threads form dS (bf16, shared memory), tcgen05 adds
+//                  dS K' into a TMEM dQ accumulator; epilogue applies scale and
+//                  R(p)^T and stores bf16.
+//   dkdv_kernel    key-major, one unit = (key tile of 128 rows, head): for every
+//                  q step of 64 rows from the diagonal to the segment end,
+//                  S^T = K'Q'^T and dP^T = V dO^T into TMEM (double buffered),
+//                  threads form P^T and dS^T, tcgen05 accumulates dV += P^T dO
+//                  and dK += dS^T Q' in TMEM; epilogue stores dV and R(p)^T dK.
+// Both attention kernels are persistent (one CTA per SM), warp-specialised
+// like the forward (TMA warp, MMA warp, TMEM warp, 4 math warps, 4 RoPE
+// warps), and use only bounded waits.
+#include <cuda.h>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/vlc.h"
+#include "attn_common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace vlc {
 
-cudaError_t launch_attn_bwd(const BwdParams&, int, cudaStream_t) { return cudaErrorNotSupported; }
+bool make_tmap_thd(CUtensorMap* map, const void* base, int32_t total, int32_t H, int32_t d,
+                   int box_rows);
+
+namespace bwd {
+
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kDrainNs = 200000000ull;
+
+// ====================================================================== delta
+// One (token, head) row per D/8 threads; each thread reads 16 B of dO and O.
+template <int D>
+__global__ void __launch_bounds__(256)
+delta_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, float* __restrict__ delta,
+             int32_t total, int32_t H, const int32_t* __restrict__ err) {
+    if (*err != 0) return;
+    constexpr int TPR = D / 8;   // threads per row
+    const int64_t rows = static_cast<int64_t>(total) * H;
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int sub = threadIdx.x % TPR;
+    const int64_t per_iter = nthreads / TPR;
+    // uniform trip count across the grid, so every lane joins the shuffles
+    for (int64_t first = 0; first < rows; first += per_iter) {
+        const int64_t row = first + gtid / TPR;
+        const bool in = row < rows;
+        float acc = 0.f;
+        if (in) {
+            const uint4 a = __ldg(dout + row * TPR + sub);
+            const uint4 b = __ldg(o + row * TPR + sub);
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                acc += bf16_lo(av[q]) * bf16_lo(bv[q]) + bf16_hi(av[q]) * bf16_hi(bv[q]);
+        }
+#pragma unroll
+        for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+        if (in && sub == 0) {
+            const int64_t tok = row / H, h = row - tok * H;
+            delta[h * total + tok] = acc;
+        }
+    }
+}
+
+// Apply scale and R(p)^T to one row of fp32 gradients held in TMEM columns
+// [col0, col0 + D) of this thread's lane, and store it as bf16.
+template <int D>
+__device__ __forceinline__ void store_unrotated(uint32_t taddr, const float2* __restrict__ table,
+                                                int pos, float scale, bool rope, bool valid,
+                                                uint8_t* __restrict__ row_out) {
+    constexpr int half = D / 2;
+#pragma unroll
+    for (int a = 0; a < half / 32; ++a) {
+        uint32_t lo[32], hi[32];
+        tmem_ld32(taddr + a * 32, lo);
+        tmem_ld32(taddr + half + a * 32, hi);
+        tmem_wait_ld();
+        uint32_t plo[16], phi[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            float g0 = __uint_as_float(lo[e]) * scale, g1 = __uint_as_float(lo[e + 1]) * scale;
+            float h0 = __uint_as_float(hi[e]) * scale, h1 = __uint_as_float(hi[e + 1]) * scale;
+            if (rope) {
+                const float4 cs = __ldg(reinterpret_cast<const float4*>(
+                    table + static_cast<int64_t>(pos) * half + a * 32 + e));
+                const float x0 = g0 * cs.x + h0 * cs.y, y0 = h0 * cs.x - g0 * cs.y;
+                const float x1 = g1 * cs.z + h1 * cs.w, y1 = h1 * cs.z - g1 * cs.w;
+                g0 = x0; h0 = y0; g1 = x1; h1 = y1;
+            }
+            plo[e / 2] = pack_bf16x2(g0, g1);
+            phi[e / 2] = pack_bf16x2(h0, h1);
+        }
+        if (valid) {
+            uint4* dlo = reinterpret_cast<uint4*>(row_out + (a * 32) * 2);
+            uint4* dhi = reinterpret_cast<uint4*>(row_out + (half + a * 32) * 2);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                dlo[q] = make_uint4(plo[4 * q], plo[4 * q + 1], plo[4 * q + 2], plo[4 * q + 3]);
+                dhi[q] = make_uint4(phi[4 * q], phi[4 * q + 1], phi[4 * q + 2], phi[4 * q + 3]);
+            }
+        }
+    }
+}
+
+// ====================================================================== dQ pass
+namespace dq {
+
+enum : int {
+    QD_FULL = 0, Q_READY = 1, QD_EMPTY = 2,
+    K_FULL = 3, K_READY = 5, V_FULL = 7, KV_EMPTY = 9,
+    SD_FULL = 11, SD_EMPTY = 12, DS_FULL = 13, DQ_DONE = 14, ACC_EMPTY = 15, DRAIN = 16,
+    NUM_BARS = 17
+};
+
+template <int D>
+struct Layout {
+    static constexpr int KB = D / 64;
+    static constexpr uint32_t BLK = 128u * 128u;
+    static constexpr uint32_t TILE = 128u * D * 2u;
+    static constexpr uint32_t Q0 = 0;
+    static constexpr uint32_t DO0 = TILE;
+    static constexpr uint32_t K0 = 2 * TILE;
+    static constexpr uint32_t V0 = 4 * TILE;
+    static constexpr uint32_t DS0 = 6 * TILE;
+    static constexpr uint32_t BAR0 = DS0 + 128u * 128u * 2u;
+    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;
+    static constexpr uint32_t BYTES = MISC + 16;
+    static constexpr uint32_t ALLOC = BYTES + 1024;
+    static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+          const BwdParams p) {
+    using LY = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
+    auto bar = [&](int i) -> uint32_t { return sbase + LY::BAR0 + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
+    volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    __shared__ int s_skip, s_nunits;
+    if (threadIdx.x == 0) {
+        s_skip = *reinterpret_cast<volatile int32_t*>(p.err);
+        s_nunits = *reinterpret_cast<const volatile int32_t*>(p.count) * p.H;
+    }
+    __syncthreads();
+    if (s_skip != 0) return;
+    const int nunits = s_nunits;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(QD_FULL), 1);
+        mbar_init(bar(Q_READY), 128);
+        mbar_init(bar(QD_EMPTY), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(K_FULL + i), 1);
+            mbar_init(bar(K_READY + i), 128);
+            mbar_init(bar(V_FULL + i), 1);
+            mbar_init(bar(KV_EMPTY + i), 1);
+        }
+        mbar_init(bar(SD_FULL), 1);
+        mbar_init(bar(SD_EMPTY), 128);
+        mbar_init(bar(DS_FULL), 128);
+        mbar_init(bar(DQ_DONE), 1);
+        mbar_init(bar(ACC_EMPTY), 128);
+        mbar_init(bar(DRAIN), 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    uint32_t q_issued = 0, kv_issued = 0, k_only = 0;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------------------------------- TMA producer
+            uint32_t unit_it = 0, kv_it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+                if (!(ok = mbar_wait(bar(QD_EMPTY), (unit_it & 1) ^ 1, abort))) break;
+                mbar_expect_tx(bar(QD_FULL), 2 * LY::TILE);
+                const int qrow = w.row0 + w.tile * 128;
+#pragma unroll
+                for (int kb = 0; kb < LY::KB; ++kb) {
+                    tma_load_3d(sbase + LY::Q0 + kb * LY::BLK, &tmQ, kb * 64, w.h, qrow, bar(QD_FULL));
+                    tma_load_3d(sbase + LY::DO0 + kb * LY::BLK, &tmDO, kb * 64, w.h, qrow, bar(QD_FULL));
+                }
+                q_issued = unit_it + 1;
+                for (int j = 0; j < w.hi; ++j) {
+                    const int ks = kv_it & 1;
+                    if (!(ok = mbar_wait(bar(KV_EMPTY + ks), ((kv_it >> 1) & 1) ^ 1, abort))) break;
+                    const int row = w.row0 + j * 128;
+                    mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
+                    mbar_expect_tx(bar(V_FULL + ks), LY::TILE);
+#pragma unroll
+                    for (int kb = 0; kb < LY::KB; ++kb) {
+                        tma_load_3d(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64, w.h,
+                                    row, bar(K_FULL + ks));
+                        tma_load_3d(sbase + LY::V0 + ks * LY::TILE + kb * LY::BLK, &tmV, kb * 64, w.h,
+                                    row, bar(V_FULL + ks));
+                    }
+                    kv_issued = ++kv_it;
+                }
+            }
+            (void)k_only;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---------------------------------------- MMA issuer
+            constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, D, true);
+            uint32_t unit_it = 0, kv_it = 0, sd_it = 0, ds_it = 0;
+            bool ok = true;
+            auto issue_dq = [&](bool first) -> bool {
+                const int ks = ds_it & 1;   // key stage of the tile this dS belongs to
+                if (first && !mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort)) return false;
+                if (!mbar_wait(bar(DS_FULL), ds_it & 1, abort)) return false;
+                tc_fence_after();
+                const uint32_t kbase = sbase + LY::K0 + ks * LY::TILE;
+#pragma unroll
+                for (int k = 0; k < 128 / 16; ++k) {
+                    const uint64_t a = smem_desc_sw128(sbase + LY::DS0 + (k >> 2) * LY::BLK + (k & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(kbase + k * 16 * 128, LY::BLK, 1024);
+                    mma_bf16_ss(tmem + LY::DQ_COL, a, b, IDESC_DQ, (!first || k > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(DQ_DONE));
+                mma_commit(bar(KV_EMPTY + ks));
+                ++ds_it;
+                return true;
+            };
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+                if (!(ok = mbar_wait(bar(QD_FULL), unit_it & 1, abort))) break;
+                if (!(ok = mbar_wait(bar(Q_READY), unit_it & 1, abort))) break;
+                for (int j = 0; j < w.hi; ++j) {
+                    const int ks = kv_it & 1;
+                    const uint32_t ph = (kv_it >> 1) & 1;
+                    if (!(ok = mbar_wait(bar(K_READY + ks), ph, abort))) break;
+                    if (!(ok = mbar_wait(bar(V_FULL + ks), ph, abort))) break;
+                    if (!(ok = mbar_wait(bar(SD_EMPTY), (sd_it & 1) ^ 1, abort))) break;
+                    tc_fence_after();
+                    const uint32_t kbase = sbase + LY::K0 + ks * LY::TILE;
+                    const uint32_t vbase = sbase + LY::V0 + ks * LY::TILE;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
+                        mma_bf16_ss(tmem + LY::S_COL, smem_desc_sw128(sbase + LY::Q0 + off, 16, 1024),
+                                    smem_desc_sw128(kbase + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
+                        mma_bf16_ss(tmem + LY::DP_COL, smem_desc_sw128(sbase + LY::DO0 + off, 16, 1024),
+                                    smem_desc_sw128(vbase + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(SD_FULL));
+                    if (j == w.hi - 1) mma_commit(bar(QD_EMPTY));
+                    ++sd_it;
+                    ++kv_it;
+                    if (j > 0 && !(ok = issue_dq(j == 1))) break;
+                }
+                if (!ok) break;
+                if (!(ok = issue_dq(w.hi == 1))) break;
+            }
+            mma_commit(bar(DRAIN));
+            mbar_wait_limit(bar(DRAIN), 0, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ dS + epilogue
+        const int wq = warp - 4;
+        const int r = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const float scale_log2 = p.scale * kLog2e;
+        uint32_t sd_it = 0, ds_it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+            const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+            const int qpos = w.tile * 128 + r;
+            const bool valid = qpos < w.L;
+            const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? qpos : 0);
+            const float lse2 = valid ? __ldg(p.lse + static_cast<int64_t>(w.h) * p.total + tok) * kLog2e : 0.f;
+            const float dlt = valid ? __ldg(p.delta + static_cast<int64_t>(w.h) * p.total + tok) : 0.f;
+            for (int j = 0; j < w.hi; ++j) {
+                if (!(ok = wait_warp(bar(SD_FULL), sd_it & 1, abort))) break;
+                tc_fence_after();
+                // allowed key columns of this tile: c <= lim
+                const int lim = !valid ? -1 : (j == w.hi - 1 ? min(qpos, w.L - 1) - j * 128 : 127);
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(tmem + lane_off + LY::S_COL + c * 32, sr);
+                    tmem_ld32(tmem + lane_off + LY::DP_COL + c * 32, dr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int col = c * 32 + e;
+                        const float p0 = (col <= lim) ? ex2_approx(__uint_as_float(sr[e]) * scale_log2 - lse2) : 0.f;
+                        const float p1 = (col + 1 <= lim) ? ex2_approx(__uint_as_float(sr[e + 1]) * scale_log2 - lse2) : 0.f;
+                        pk[(col >> 1)] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) - dlt),
+                                                     p1 * (__uint_as_float(dr[e + 1]) - dlt));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(SD_EMPTY));
+                ++sd_it;
+                if (ds_it > 0 && !(ok = wait_warp(bar(DQ_DONE), (ds_it - 1) & 1, abort))) break;
+#pragma unroll
+                for (int ci = 0; ci < 16; ++ci) {
+                    const uint32_t addr = sw128(sbase + LY::DS0 + (ci >> 3) * LY::BLK, r, ci & 7);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 ::"r"(addr), "r"(pk[4 * ci]), "r"(pk[4 * ci + 1]), "r"(pk[4 * ci + 2]),
+                                 "r"(pk[4 * ci + 3]) : "memory");
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(DS_FULL));
+                ++ds_it;
+            }
+            if (!ok) break;
+            if (!(ok = wait_warp(bar(DQ_DONE), (ds_it - 1) & 1, abort))) break;
+            tc_fence_after();
+            uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dq) + (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
+            store_unrotated<D>(tmem + lane_off + LY::DQ_COL, p.table, qpos, p.scale, p.use_rope != 0,
+                               valid, row_out);
+            tc_fence_before();
+            mbar_arrive(bar(ACC_EMPTY));
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ RoPE on staged Q / K
+        const int wr = warp - 8;
+        uint32_t unit_it = 0, kv_it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+            const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+            if (!(ok = wait_warp(bar(QD_FULL), unit_it & 1, abort))) break;
+            if (p.use_rope) rope_tile<D, 128>(sbase + LY::Q0, w.tile * 128, p.table, wr, lane);
+            fence_proxy_async_smem();
+            mbar_arrive(bar(Q_READY));
+            for (int j = 0; j < w.hi; ++j) {
+                const int ks = kv_it & 1;
+                if (!(ok = wait_warp(bar(K_FULL + ks), (kv_it >> 1) & 1, abort))) break;
+                if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * 128, p.table, wr, lane);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(K_READY + ks));
+                ++kv_it;
+            }
+        }
+    }
+
+    __syncthreads();
+    if (*abort) {
+        if (warp == 0 && lane == 0) {
+            if (q_issued > 0) mbar_wait_limit(bar(QD_FULL), (q_issued - 1) & 1, kDrainNs);
+            for (int s = 0; s < 2; ++s)
+                if (kv_issued > static_cast<uint32_t>(s)) {
+                    const uint32_t n = ((kv_issued - 1 - s) & ~1u) + s;
+                    mbar_wait_limit(bar(K_FULL + s), (n >> 1) & 1, kDrainNs);
+                    mbar_wait_limit(bar(V_FULL + s), (n >> 1) & 1, kDrainNs);
+                }
+        }
+        if (threadIdx.x == 0) atomicOr(p.err, VLC_DEVERR_TIMEOUT);
+        __syncthreads();
+    }
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace dq
+
+// ====================================================================== dK/dV pass
+namespace dkdv {
+
+enum : int {
+    KV_FULL = 0, K_READY = 1, KV_EMPTY = 2,
+    QO_FULL = 3, Q_READY = 5, QO_EMPTY = 7,
+    ST_FULL = 9, ST_EMPTY = 11, PDS_FULL = 13, PDS_EMPTY = 15,
+    ACC_FULL = 17, ACC_EMPTY = 18, DRAIN = 19, LSED_FULL = 20,
+    NUM_BARS = 22
+};
+
+constexpr int BQ = kBwdBM;    // q rows per step
+static_assert(BQ == 64, "the P^T / dS^T tiles are one 128-byte swizzle block wide");
+
+template <int D>
+struct Layout {
+    static constexpr int KB = D / 64;
+    static constexpr uint32_t BLKK = 128u * 128u;       // key-side block: 128 rows x 128 B
+    static constexpr uint32_t TILEK = 128u * D * 2u;
+    static constexpr uint32_t BLKQ = BQ * 128u;          // q-side block: 64 rows x 128 B
+    static constexpr uint32_t TILEQ = BQ * D * 2u;
+    static constexpr uint32_t PT = 128u * BQ * 2u;       // one P^T or dS^T tile (16 KB)
+    static constexpr uint32_t K0 = 0;
+    static constexpr uint32_t V0 = TILEK;
+    static constexpr uint32_t Q0 = 2 * TILEK;                 // 2 stages
+    static constexpr uint32_t DO0 = Q0 + 2 * TILEQ;           // 2 stages
+    static constexpr uint32_t P0 = DO0 + 2 * TILEQ;           // 2 buffers
+    static constexpr uint32_t DS0 = P0 + 2 * PT;              // 2 buffers
+    static constexpr uint32_t LSED = DS0 + 2 * PT;            // 2 x (64 lse2 + 64 delta) floats
+    static constexpr uint32_t BAR0 = LSED + 2 * 128 * 4;
+    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;
+    static constexpr uint32_t BYTES = MISC + 16;
+    static constexpr uint32_t ALLOC = BYTES + 1024;
+    static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+            const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+            const BwdParams p) {
+    using LY = Layout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
+    auto bar = [&](int i) -> uint32_t { return sbase + LY::BAR0 + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
+    volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
+    float* lsed = reinterpret_cast<float*>(sgen + LY::LSED);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    __shared__ int s_skip, s_nunits;
+    if (threadIdx.x == 0) {
+        s_skip = *reinterpret_cast<volatile int32_t*>(p.err);
+        s_nunits = *reinterpret_cast<const volatile int32_t*>(p.count_k) * p.H;
+    }
+    __syncthreads();
+    if (s_skip != 0) return;
+    const int nunits = s_nunits;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(KV_FULL), 1);
+        mbar_init(bar(K_READY), 128);
+        mbar_init(bar(KV_EMPTY), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(QO_FULL + i), 1);
+            mbar_init(bar(Q_READY + i), 128);
+            mbar_init(bar(QO_EMPTY + i), 1);
+            mbar_init(bar(ST_FULL + i), 1);
+            mbar_init(bar(ST_EMPTY + i), 128);
+            mbar_init(bar(PDS_FULL + i), 128);
+            mbar_init(bar(PDS_EMPTY + i), 1);
+        }
+        mbar_init(bar(ACC_FULL), 1);
+        mbar_init(bar(ACC_EMPTY), 128);
+        mbar_init(bar(DRAIN), 1);
+        mbar_init(bar(LSED_FULL), 128);
+        mbar_init(bar(LSED_FULL + 1), 128);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    uint32_t kv_issued = 0, q_issued = 0;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------------------------------- TMA producer
+            uint32_t unit_it = 0, st_it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
+                if (!(ok = mbar_wait(bar(KV_EMPTY), (unit_it & 1) ^ 1, abort))) break;
+                mbar_expect_tx(bar(KV_FULL), 2 * LY::TILEK);
+                const int krow = w.row0 + w.tile * 128;
+#pragma unroll
+                for (int kb = 0; kb < LY::KB; ++kb) {
+                    tma_load_3d(sbase + LY::K0 + kb * LY::BLKK, &tmK, kb * 64, w.h, krow, bar(KV_FULL));
+                    tma_load_3d(sbase + LY::V0 + kb * LY::BLKK, &tmV, kb * 64, w.h, krow, bar(KV_FULL));
+                }
+                kv_issued = unit_it + 1;
+                for (int i = w.lo; i < w.hi; ++i) {
+                    const int s = st_it & 1;
+                    if (!(ok = mbar_wait(bar(QO_EMPTY + s), ((st_it >> 1) & 1) ^ 1, abort))) break;
+                    mbar_expect_tx(bar(QO_FULL + s), 2 * LY::TILEQ);
+                    const int qrow = w.row0 + i * BQ;
+#pragma unroll
+                    for (int kb = 0; kb < LY::KB; ++kb) {
+                        tma_load_3d(sbase + LY::Q0 + s * LY::TILEQ + kb * LY::BLKQ, &tmQ, kb * 64, w.h,
+                                    qrow, bar(QO_FULL + s));
+                        tma_load_3d(sbase + LY::DO0 + s * LY::TILEQ + kb * LY::BLKQ, &tmDO, kb * 64, w.h,
+                                    qrow, bar(QO_FULL + s));
+                    }
+                    q_issued = ++st_it;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---------------------------------------- MMA issuer
+            constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, BQ, false);
+            constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, true);
+            uint32_t unit_it = 0, st_it = 0, acc_it = 0;
+            bool ok = true;
+            auto issue_acc = [&](bool first) -> bool {
+                const int b = acc_it & 1;   // P^T/dS^T buffer == Q/dO stage of that step
+                if (first && !mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort)) return false;
+                if (!mbar_wait(bar(PDS_FULL + b), (acc_it >> 1) & 1, abort)) return false;
+                tc_fence_after();
+                const uint32_t qb = sbase + LY::Q0 + b * LY::TILEQ;
+                const uint32_t ob = sbase + LY::DO0 + b * LY::TILEQ;
+#pragma unroll
+                for (int k = 0; k < BQ / 16; ++k) {
+                    const uint64_t a = smem_desc_sw128(sbase + LY::P0 + b * LY::PT + k * 32, 16, 1024);
+                    const uint64_t bb = smem_desc_sw128(ob + k * 16 * 128, LY::BLKQ, 1024);
+                    mma_bf16_ss(tmem + LY::DV_COL, a, bb, IDESC_ACC, (!first || k > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int k = 0; k < BQ / 16; ++k) {
+                    const uint64_t a = smem_desc_sw128(sbase + LY::DS0 + b * LY::PT + k * 32, 16, 1024);
+                    const uint64_t bb = smem_desc_sw128(qb + k * 16 * 128, LY::BLKQ, 1024);
+                    mma_bf16_ss(tmem + LY::DK_COL, a, bb, IDESC_ACC, (!first || k > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(PDS_EMPTY + b));
+                mma_commit(bar(QO_EMPTY + b));
+                ++acc_it;
+                return true;
+            };
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
+                if (!(ok = mbar_wait(bar(KV_FULL), unit_it & 1, abort))) break;
+                if (!(ok = mbar_wait(bar(K_READY), unit_it & 1, abort))) break;
+                for (int i = w.lo; i < w.hi; ++i) {
+                    const int s = st_it & 1;
+                    const uint32_t ph = (st_it >> 1) & 1;
+                    if (!(ok = mbar_wait(bar(QO_FULL + s), ph, abort))) break;
+                    if (!(ok = mbar_wait(bar(Q_READY + s), ph, abort))) break;
+                    if (!(ok = mbar_wait(bar(ST_EMPTY + s), ph ^ 1, abort))) break;
+                    tc_fence_after();
+                    const uint32_t qb = sbase + LY::Q0 + s * LY::TILEQ;
+                    const uint32_t ob = sbase + LY::DO0 + s * LY::TILEQ;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
+                        const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
+                        mma_bf16_ss(tmem + s * 128, smem_desc_sw128(sbase + LY::K0 + offk, 16, 1024),
+                                    smem_desc_sw128(qb + offq, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
+                        const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
+                        mma_bf16_ss(tmem + s * 128 + 64, smem_desc_sw128(sbase + LY::V0 + offk, 16, 1024),
+                                    smem_desc_sw128(ob + offq, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(ST_FULL + s));
+                    ++st_it;
+                    if (i > w.lo && !(ok = issue_acc(i == w.lo + 1))) break;
+                }
+                if (!ok) break;
+                if (!(ok = issue_acc(w.hi - w.lo == 1))) break;
+                mma_commit(bar(ACC_FULL));
+                mma_commit(bar(KV_EMPTY));
+            }
+            mma_commit(bar(DRAIN));
+            mbar_wait_limit(bar(DRAIN), 0, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ P^T, dS^T + epilogue
+        const int t = threadIdx.x - 128;          // 0..127
+        const int wq = warp - 4;
+        const int r = wq * 32 + lane;              // key row = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const float scale_log2 = p.scale * kLog2e;
+        uint32_t unit_it = 0, st_it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
+            const int kvpos = w.tile * 128 + r;
+            for (int i = w.lo; i < w.hi; ++i) {
+                const int b = st_it & 1;
+                {   // stage LSE (log2 units) and delta of this step's 64 q rows
+                    const int qq = i * BQ + (t & 63);
+                    float val = 0.f;
+                    if (qq < w.L) {
+                        const int64_t idx = static_cast<int64_t>(w.h) * p.total + w.row0 + qq;
+                        val = (t < 64) ? __ldg(p.lse + idx) * kLog2e : __ldg(p.delta + idx);
+                    }
+                    lsed[b * 128 + t] = val;
+                    mbar_arrive(bar(LSED_FULL + b));
+                    if (!(ok = wait_warp(bar(LSED_FULL + b), (st_it >> 1) & 1, abort))) break;
+                }
+                const float* l2 = lsed + b * 128;
+                const float* dl = l2 + 64;
+                if (!(ok = wait_warp(bar(ST_FULL + b), (st_it >> 1) & 1, abort))) break;
+                tc_fence_after();
+                const bool edge = (i * BQ < w.tile * 128 + 128) || ((i + 1) * BQ > w.L);
+                // allowed q columns c: kvpos <= i*BQ + c and i*BQ + c < L
+                const int c_lo = kvpos - i * BQ;
+                const int c_hi = w.L - 1 - i * BQ;
+                uint32_t pp[32], pd[32];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(tmem + lane_off + b * 128 + c * 32, sr);
+                    tmem_ld32(tmem + lane_off + b * 128 + 64 + c * 32, dr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int col = c * 32 + e;
+                        float p0 = ex2_approx(__uint_as_float(sr[e]) * scale_log2 - l2[col]);
+                        float p1 = ex2_approx(__uint_as_float(sr[e + 1]) * scale_log2 - l2[col + 1]);
+                        if (edge) {
+                            if (col < c_lo || col > c_hi) p0 = 0.f;
+                            if (col + 1 < c_lo || col + 1 > c_hi) p1 = 0.f;
+                        }
+                        pp[col >> 1] = pack_bf16x2(p0, p1);
+                        pd[col >> 1] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) - dl[col]),
+                                                   p1 * (__uint_as_float(dr[e + 1]) - dl[col + 1]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(ST_EMPTY + b));
+                if (!(ok = wait_warp(bar(PDS_EMPTY + b), ((st_it >> 1) & 1) ^ 1, abort))) break;
+#pragma unroll
+                for (int ci = 0; ci < 8; ++ci) {
+                    const uint32_t pa = sw128(sbase + LY::P0 + b * LY::PT, r, ci);
+                    const uint32_t da = sw128(sbase + LY::DS0 + b * LY::PT, r, ci);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 ::"r"(pa), "r"(pp[4 * ci]), "r"(pp[4 * ci + 1]), "r"(pp[4 * ci + 2]),
+                                 "r"(pp[4 * ci + 3]) : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 ::"r"(da), "r"(pd[4 * ci]), "r"(pd[4 * ci + 1]), "r"(pd[4 * ci + 2]),
+                                 "r"(pd[4 * ci + 3]) : "memory");
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(PDS_FULL + b));
+                ++st_it;
+            }
+            if (!ok) break;
+            if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
+            tc_fence_after();
+            const bool valid = kvpos < w.L;
+            const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? kvpos : 0);
+            const int64_t roff = (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
+            // dV: plain copy out
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_off + LY::DV_COL + c * 32, rr);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dv) + roff + c * 64);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            store_unrotated<D>(tmem + lane_off + LY::DK_COL, p.table, kvpos, p.scale, p.use_rope != 0,
+                               valid, reinterpret_cast<uint8_t*>(p.dk) + roff);
+            tc_fence_before();
+            mbar_arrive(bar(ACC_EMPTY));
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ RoPE on staged K / Q
+        const int wr = warp - 8;
+        uint32_t unit_it = 0, st_it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
+            if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
+            if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0, w.tile * 128, p.table, wr, lane);
+            fence_proxy_async_smem();
+            mbar_arrive(bar(K_READY));
+            for (int i = w.lo; i < w.hi; ++i) {
+                const int s = st_it & 1;
+                if (!(ok = wait_warp(bar(QO_FULL + s), (st_it >> 1) & 1, abort))) break;
+                if (p.use_rope) rope_tile<D, BQ>(sbase + LY::Q0 + s * LY::TILEQ, i * BQ, p.table, wr, lane);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(Q_READY + s));
+                ++st_it;
+            }
+        }
+    }
+
+    __syncthreads();
+    if (*abort) {
+        if (warp == 0 && lane == 0) {
+            if (kv_issued > 0) mbar_wait_limit(bar(KV_FULL), (kv_issued - 1) & 1, kDrainNs);
+            for (int s = 0; s < 2; ++s)
+                if (q_issued > static_cast<uint32_t>(s)) {
+                    const uint32_t n = ((q_issued - 1 - s) & ~1u) + s;
+                    mbar_wait_limit(bar(QO_FULL + s), (n >> 1) & 1, kDrainNs);
+                }
+        }
+        if (threadIdx.x == 0) atomicOr(p.err, VLC_DEVERR_TIMEOUT);
+        __syncthreads();
+    }
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace dkdv
+}  // namespace bwd
+
+template <int D>
+static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s) {
+    {
+        const int64_t rows = static_cast<int64_t>(p.total) * p.H;
+        int64_t blocks = (rows * (D / 8) + 255) / 256;
+        if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
+        bwd::delta_kernel<D><<<static_cast<int>(blocks), 256, 0, s>>>(
+            static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.o), p.delta, p.total,
+            p.H, p.err);
+    }
+    CUtensorMap q128, do128, k128, v128, q64, do64;
+    if (!make_tmap_thd(&q128, p.q, p.total, p.H, D, 128) ||
+        !make_tmap_thd(&do128, p.dout, p.total, p.H, D, 128) ||
+        !make_tmap_thd(&k128, p.k, p.total, p.H, D, 128) ||
+        !make_tmap_thd(&v128, p.v, p.total, p.H, D, 128) ||
+        !make_tmap_thd(&q64, p.q, p.total, p.H, D, bwd::dkdv::BQ) ||
+        !make_tmap_thd(&do64, p.dout, p.total, p.H, D, bwd::dkdv::BQ))
+        return cudaErrorInvalidValue;
+    {
+        constexpr uint32_t smem = bwd::dq::Layout<D>::ALLOC;
+        cudaError_t e = cudaFuncSetAttribute(bwd::dq::dq_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        bwd::dq::dq_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
+    }
+    {
+        constexpr uint32_t smem = bwd::dkdv::Layout<D>::ALLOC;
+        cudaError_t e = cudaFuncSetAttribute(bwd::dkdv::dkdv_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        bwd::dkdv::dkdv_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q64, do64, k128, v128, p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(const BwdParams& p, int num_sms, cudaStream_t s) {
+    return p.d == 128 ? launch_bwd_d<128>(p, num_sms, s) : launch_bwd_d<64>(p, num_sms, s);
+}
 
 }  // namespace vlc

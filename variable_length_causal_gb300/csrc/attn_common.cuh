@@ -1,0 +1,127 @@
+// attn_common.cuh -- device helpers shared by the forward and backward
+// attention kernels: work-unit decoding, warp-collective bounded waits, the
+// 128-byte swizzle address map, and RoPE applied to a staged tile.
+#pragma once
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace vlc {
+
+struct Unit {
+    int seg, tile, lo, hi, h, L, row0;   // tile = q tile (forward items) or key tile (backward items)
+};
+
+// Unit u -> (item, head).  Units run over the sorted segments; inside a
+// segment head-major, then the segment's items in work-list order.
+__device__ __forceinline__ Unit decode_unit(const int4* __restrict__ items,
+                                            const int32_t* __restrict__ seg_base,
+                                            const int32_t* __restrict__ cu, int nseg, int H, int u) {
+    const int64_t HH = H;
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (HH * __ldg(seg_base + mid) <= u) lo = mid; else hi = mid - 1;
+    }
+    const int base = __ldg(seg_base + lo);
+    const int n = __ldg(seg_base + lo + 1) - base;
+    const int64_t local = u - HH * base;
+    Unit w;
+    w.h = static_cast<int>(local / n);
+    const int4 it = __ldg(items + base + static_cast<int>(local - static_cast<int64_t>(w.h) * n));
+    w.seg = it.x;
+    w.tile = it.y;
+    w.lo = it.z;
+    w.hi = it.w;
+    w.row0 = __ldg(cu + it.x);
+    w.L = __ldg(cu + it.x + 1) - w.row0;
+    return w;
+}
+
+// All 32 lanes poll; succeed together or give up together.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
+    uint64_t t0 = 0;
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int it = 0;; ++it) {
+        const bool done = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        int give_up = 0;
+        if (lane == 0 && it >= 64) {
+            if (t0 == 0) t0 = globaltimer_ns();
+            if (*abort) give_up = 1;
+            else if (globaltimer_ns() - t0 > kWaitLimitNs) { *abort = 1; give_up = 1; }
+        }
+        if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+}
+
+// 16-byte chunk `ci` (0..7) of row `r` inside a block of rows x 128 bytes with
+// the 128-byte swizzle used by both TMA and the MMA descriptors.
+__device__ __forceinline__ uint32_t sw128(uint32_t block_base, int r, int ci) {
+    return block_base + static_cast<uint32_t>(r) * 128u +
+           static_cast<uint32_t>(((ci ^ (r & 7)) & 7) << 4);
+}
+
+// Named barrier among `nthreads` threads (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Rotate a staged tile of ROWS rows (segment-local positions pos0 + row) in
+// place: rotate-half pairs (c, c + D/2), x' = x cos - y sin, y' = y cos + x sin,
+// computed in fp32 from the cos/sin table and rounded to bf16.  Executed by
+// 128 threads (4 warps, wr = 0..3); each 64-column block holds ROWS x 128 B.
+template <int D, int ROWS>
+__device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2* __restrict__ table,
+                                          int wr, int lane) {
+    constexpr int half = D / 2;
+    constexpr uint32_t BLK = ROWS * 128u;
+    constexpr int PAIRS_PER_ROW = half / 8;            // 16-byte chunk pairs per row
+    constexpr int ROWS_PER_IT = 32 / PAIRS_PER_ROW;
+    constexpr int ROWS_PER_WARP = ROWS / 4;
+    const int rsub = lane / PAIRS_PER_ROW;
+    const int ci = lane % PAIRS_PER_ROW;
+#pragma unroll 2
+    for (int it = 0; it < ROWS_PER_WARP / ROWS_PER_IT; ++it) {
+        const int r = wr * ROWS_PER_WARP + it * ROWS_PER_IT + rsub;
+        uint32_t lo_addr, hi_addr;
+        if constexpr (D == 128) {
+            lo_addr = sw128(tile, r, ci);
+            hi_addr = sw128(tile + BLK, r, ci);
+        } else {
+            lo_addr = sw128(tile, r, ci);
+            hi_addr = sw128(tile, r, ci + 4);
+        }
+        uint32_t a[4], b[4];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(lo_addr));
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]) : "r"(hi_addr));
+        const float4* t4 = reinterpret_cast<const float4*>(
+            table + static_cast<int64_t>(pos0 + r) * half + ci * 8);
+        float cs[8], sn[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 f = __ldg(t4 + q);
+            cs[2 * q] = f.x; sn[2 * q] = f.y;
+            cs[2 * q + 1] = f.z; sn[2 * q + 1] = f.w;
+        }
+        uint32_t na[4], nb[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float x0 = bf16_lo(a[q]), x1 = bf16_hi(a[q]);
+            const float y0 = bf16_lo(b[q]), y1 = bf16_hi(b[q]);
+            const float c0 = cs[2 * q], s0 = sn[2 * q], c1 = cs[2 * q + 1], s1 = sn[2 * q + 1];
+            na[q] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
+            nb[q] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     ::"r"(lo_addr), "r"(na[0]), "r"(na[1]), "r"(na[2]), "r"(na[3]) : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     ::"r"(hi_addr), "r"(nb[0]), "r"(nb[1]), "r"(nb[2]), "r"(nb[3]) : "memory");
+    }
+}
+
+}  // namespace vlc

@@ -28,6 +28,7 @@
 #include <cstdint>
 
 #include "../../include/vlc.h"
+#include "attn_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -69,108 +70,6 @@ struct Layout {
     static constexpr uint32_t S_COL = 0;               // S buffers at columns 0 and 128
     static constexpr uint32_t O_COL = 256;             // O at columns 256 .. 256+D
 };
-
-struct Unit {
-    int seg, qt, kv_hi, h, L, row0;
-};
-
-// Unit u -> (item, head).  Units run over sorted segments; inside a segment
-// head-major, then the segment's items (q tiles, last first).
-__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
-    const int64_t H = p.H;
-    int lo = 0, hi = p.nseg - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (H * __ldg(p.seg_base + mid) <= u) lo = mid; else hi = mid - 1;
-    }
-    const int base = __ldg(p.seg_base + lo);
-    const int n = __ldg(p.seg_base + lo + 1) - base;
-    const int64_t local = u - H * base;
-    Unit w;
-    w.h = static_cast<int>(local / n);
-    const int4 it = __ldg(p.items + base + static_cast<int>(local - static_cast<int64_t>(w.h) * n));
-    w.seg = it.x;
-    w.qt = it.y;
-    w.kv_hi = it.w;
-    w.row0 = __ldg(p.cu + it.x);
-    w.L = __ldg(p.cu + it.x + 1) - w.row0;
-    return w;
-}
-
-// All 32 lanes poll; succeed together or give up together.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
-    uint64_t t0 = 0;
-    const int lane = threadIdx.x & 31;
-#pragma unroll 1
-    for (int it = 0;; ++it) {
-        const bool done = mbar_try_wait(bar, parity);
-        if (__all_sync(0xffffffffu, done)) return true;
-        int give_up = 0;
-        if (lane == 0 && it >= 64) {
-            if (t0 == 0) t0 = globaltimer_ns();
-            if (*abort) give_up = 1;
-            else if (globaltimer_ns() - t0 > kWaitLimitNs) { *abort = 1; give_up = 1; }
-        }
-        if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
-    }
-}
-
-// 16-byte chunk `ci` (0..7) of row `r` inside a 128-row x 128-byte block with
-// the 128-byte swizzle used by both TMA and the MMA descriptors.
-__device__ __forceinline__ uint32_t sw128(uint32_t block_base, int r, int ci) {
-    return block_base + static_cast<uint32_t>(r) * 128u +
-           static_cast<uint32_t>(((ci ^ (r & 7)) & 7) << 4);
-}
-
-// Rotate a staged tile (rows at segment-local positions pos0 + row) in place.
-template <int D>
-__device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2* __restrict__ table,
-                                          int wr, int lane) {
-    constexpr int half = D / 2;
-    constexpr int PAIRS_PER_ROW = half / 8;            // 16-byte chunk pairs per row
-    constexpr int ROWS_PER_IT = 32 / PAIRS_PER_ROW;
-    const int rsub = lane / PAIRS_PER_ROW;
-    const int ci = lane % PAIRS_PER_ROW;
-#pragma unroll 2
-    for (int it = 0; it < 32 / ROWS_PER_IT; ++it) {
-        const int r = wr * 32 + it * ROWS_PER_IT + rsub;
-        uint32_t lo_addr, hi_addr;
-        if constexpr (D == 128) {
-            lo_addr = sw128(tile, r, ci);
-            hi_addr = sw128(tile + Layout<D>::BLK, r, ci);
-        } else {
-            lo_addr = sw128(tile, r, ci);
-            hi_addr = sw128(tile, r, ci + 4);
-        }
-        uint32_t a[4], b[4];
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(lo_addr));
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]) : "r"(hi_addr));
-        const float4* t4 = reinterpret_cast<const float4*>(
-            table + static_cast<int64_t>(pos0 + r) * half + ci * 8);
-        float cs[8], sn[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 f = __ldg(t4 + q);
-            cs[2 * q] = f.x; sn[2 * q] = f.y;
-            cs[2 * q + 1] = f.z; sn[2 * q + 1] = f.w;
-        }
-        uint32_t na[4], nb[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float x0 = bf16_lo(a[q]), x1 = bf16_hi(a[q]);
-            const float y0 = bf16_lo(b[q]), y1 = bf16_hi(b[q]);
-            const float c0 = cs[2 * q], s0 = sn[2 * q], c1 = cs[2 * q + 1], s1 = sn[2 * q + 1];
-            na[q] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
-            nb[q] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
-        }
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                     ::"r"(lo_addr), "r"(na[0]), "r"(na[1]), "r"(na[2]), "r"(na[3]) : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                     ::"r"(hi_addr), "r"(nb[0]), "r"(nb[1]), "r"(nb[2]), "r"(nb[3]) : "memory");
-    }
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -236,18 +135,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (lane == 0) {
             uint32_t q_it = 0, kv_it = 0;
             for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-                const Unit w = decode_unit(p, u);
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
                 const int qs = q_it & 1;
                 if (!mbar_wait(bar(Q_EMPTY + qs), ((q_it >> 1) & 1) ^ 1, abort)) break;
                 mbar_expect_tx(bar(Q_FULL + qs), LY::TILE);
                 const uint32_t qdst = sbase + LY::Q0 + qs * LY::TILE;
 #pragma unroll
                 for (int kb = 0; kb < LY::KB; ++kb)
-                    tma_load_3d(qdst + kb * LY::BLK, &tmQ, kb * 64, w.h, w.row0 + w.qt * BM,
+                    tma_load_3d(qdst + kb * LY::BLK, &tmQ, kb * 64, w.h, w.row0 + w.tile * BM,
                                 bar(Q_FULL + qs));
                 q_issued = ++q_it;
                 bool ok = true;
-                for (int j = 0; j < w.kv_hi && ok; ++j) {
+                for (int j = 0; j < w.hi && ok; ++j) {
                     const int ks = kv_it & 1;
                     const uint32_t ph = ((kv_it >> 1) & 1) ^ 1;
                     const int row = w.row0 + j * BN;
@@ -299,11 +198,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 return true;
             };
             for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-                const Unit w = decode_unit(p, u);
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
                 const int qs = q_it & 1;
                 if (!(ok = mbar_wait(bar(Q_READY + qs), (q_it >> 1) & 1, abort))) break;
                 const uint32_t qbase = sbase + LY::Q0 + qs * LY::TILE;
-                for (int j = 0; j < w.kv_hi; ++j) {
+                for (int j = 0; j < w.hi; ++j) {
                     const int ks = kv_it & 1;
                     if (!(ok = mbar_wait(bar(K_READY + ks), (kv_it >> 1) & 1, abort))) break;
                     const int sb = s_it & 1;
@@ -320,13 +219,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                     mma_commit(bar(S_FULL + sb));
                     mma_commit(bar(K_EMPTY + ks));
-                    if (j == w.kv_hi - 1) mma_commit(bar(Q_EMPTY + qs));
+                    if (j == w.hi - 1) mma_commit(bar(Q_EMPTY + qs));
                     ++s_it;
                     ++kv_it;
                     if (j > 0 && !(ok = issue_pv(j == 1))) break;
                 }
                 if (!ok) break;
-                if (!(ok = issue_pv(w.kv_hi == 1))) break;
+                if (!(ok = issue_pv(w.hi == 1))) break;
                 ++q_it;
                 ++unit_it;
             }
@@ -344,10 +243,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint32_t s_it = 0, pv_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-            const Unit w = decode_unit(p, u);
-            const int qpos = w.qt * BM + r;
+            const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+            const int qpos = w.tile * BM + r;
             float m_run = 0.f, l_run = 0.f;
-            for (int j = 0; j < w.kv_hi; ++j) {
+            for (int j = 0; j < w.hi; ++j) {
                 const int sb = s_it & 1;
                 if (!(ok = wait_warp(bar(S_FULL + sb), (s_it >> 1) & 1, abort))) break;
                 tc_fence_after();
@@ -366,7 +265,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
                 // scale to the log2 domain; mask only on the last (diagonal / tail) tile
                 float mt = -INFINITY;
-                if (j == w.kv_hi - 1) {
+                if (j == w.hi - 1) {
                     const int lim = min(qpos, w.L - 1) - j * BN;   // allowed key columns: c <= lim
 #pragma unroll
                     for (int c = 0; c < BN; ++c) {
@@ -469,17 +368,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint32_t q_it = 0, kv_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-            const Unit w = decode_unit(p, u);
+            const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
             const int qs = q_it & 1;
             if (!(ok = wait_warp(bar(Q_FULL + qs), (q_it >> 1) & 1, abort))) break;
-            if (p.use_rope) rope_tile<D>(sbase + LY::Q0 + qs * LY::TILE, w.qt * BM, p.table, wr, lane);
+            if (p.use_rope) rope_tile<D, 128>(sbase + LY::Q0 + qs * LY::TILE, w.tile * BM, p.table, wr, lane);
             fence_proxy_async_smem();
             mbar_arrive(bar(Q_READY + qs));
             ++q_it;
-            for (int j = 0; j < w.kv_hi; ++j) {
+            for (int j = 0; j < w.hi; ++j) {
                 const int ks = kv_it & 1;
                 if (!(ok = wait_warp(bar(K_FULL + ks), (kv_it >> 1) & 1, abort))) break;
-                if (p.use_rope) rope_tile<D>(sbase + LY::K0 + ks * LY::TILE, j * BN, p.table, wr, lane);
+                if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * BN, p.table, wr, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(K_READY + ks));
                 ++kv_it;
