@@ -150,6 +150,29 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
                  int32_t d, int32_t max_seqlen, float softmax_scale, float rope_theta, void* dq,
                  void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
+/* Forward attention for callers that cannot allocate device memory.  No
+ * counterpart on the pages: it exists for callers that may not obtain memory
+ * per call, such as code running inside another runtime's execution hook (a
+ * plugin's enqueue function, a host callback) where allocating is forbidden,
+ * or services whose device-memory budget is fixed at start-up, and so cannot
+ * supply the workspace vlc_attn_fwd takes.
+ * Same arguments and result as vlc_attn_fwd, without ws/ws_bytes; the scratch
+ * lives in one file-scope device array of VLC_NOALLOC_SCRATCH_BYTES per GPU,
+ * held until the process exits.
+ *   err_out  int32 [1] device word or NULL: receives this call's VLC_DEVERR_*
+ *            bits in stream order (the caller zeroes it if it wants OR-free bits).
+ * Returns VLC_ERR_WORKSPACE, before enqueuing anything, when the problem's
+ * forward workspace (vlc_workspace_bytes(..., 0)) exceeds the array.
+ * The first call on a device looks up the array's address (do it before any
+ * stream capture begins).  All calls share the array: calls whose GPU work can
+ * overlap race on it, so order them on one stream or with events.  Calls no
+ * cudaMalloc, cudaFree or other allocating routine. */
+#define VLC_NOALLOC_SCRATCH_BYTES (8u << 20)
+int vlc_attn_fwd_noalloc(const void* q, const void* k, const void* v, const int32_t* cu,
+                         int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t max_seqlen,
+                         float softmax_scale, float rope_theta, void* o, float* lse,
+                         int32_t* err_out, void* stream);
+
 /* Synchronise `stream` and read the workspace's device error word.
  * Returns VLC_OK, VLC_ERR_CU_SEQLENS or VLC_ERR_TIMEOUT; *bits_out (if not
  * NULL) receives the raw VLC_DEVERR_* bits. */

@@ -27,7 +27,7 @@ WORKLIST_FWD, WORKLIST_BWD = 0, 1
 EXPORTED = [
     "vlc_status_string", "vlc_version", "vlc_workspace_bytes", "vlc_worklist_capacity",
     "vlc_build_positions_labels", "vlc_build_worklist", "vlc_attn_fwd", "vlc_attn_bwd",
-    "vlc_get_error",
+    "vlc_get_error", "vlc_attn_fwd_noalloc",
 ]
 
 _lock = threading.Lock()
@@ -75,6 +75,8 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_attn_bwd.restype = cint
         lib.vlc_get_error.argtypes = [P, P, P]
         lib.vlc_get_error.restype = cint
+        lib.vlc_attn_fwd_noalloc.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, f32, P, P, P, P]
+        lib.vlc_attn_fwd_noalloc.restype = cint
         _lib = lib
         return lib
 
