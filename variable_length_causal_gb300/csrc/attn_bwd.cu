@@ -357,18 +357,20 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     } else if (warp >= 8) {
         // ------------------------------------------------------------ RoPE on staged Q / K
         const int wr = warp - 8;
+        RopeStep<D> step{};
+        if (p.use_rope) step = rope_step<D>(p.table, lane);
         uint32_t unit_it = 0, kv_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
             const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
             if (!(ok = wait_warp(bar(QD_FULL), unit_it & 1, abort))) break;
-            if (p.use_rope) rope_tile<D, 128>(sbase + LY::Q0, w.tile * 128, p.table, wr, lane);
+            if (p.use_rope) rope_tile<D, 128>(sbase + LY::Q0, w.tile * 128, p.table, step, wr, lane);
             fence_proxy_async_smem();
             mbar_arrive(bar(Q_READY));
             for (int j = 0; j < w.hi; ++j) {
                 const int ks = kv_it & 1;
                 if (!(ok = wait_warp(bar(K_FULL + ks), (kv_it >> 1) & 1, abort))) break;
-                if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * 128, p.table, wr, lane);
+                if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * 128, p.table, step, wr, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(K_READY + ks));
                 ++kv_it;
@@ -694,18 +696,21 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     } else if (warp >= 8) {
         // ------------------------------------------------------------ RoPE on staged K / Q
         const int wr = warp - 8;
+        RopeStep<D> step128{};
+        RopeStep<D> step64{};
+        if (p.use_rope) step128 = step64 = rope_step<D>(p.table, lane);
         uint32_t unit_it = 0, st_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
             const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
             if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
-            if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0, w.tile * 128, p.table, wr, lane);
+            if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0, w.tile * 128, p.table, step128, wr, lane);
             fence_proxy_async_smem();
             mbar_arrive(bar(K_READY));
             for (int i = w.lo; i < w.hi; ++i) {
                 const int s = st_it & 1;
                 if (!(ok = wait_warp(bar(QO_FULL + s), (st_it >> 1) & 1, abort))) break;
-                if (p.use_rope) rope_tile<D, BQ>(sbase + LY::Q0 + s * LY::TILEQ, i * BQ, p.table, wr, lane);
+                if (p.use_rope) rope_tile<D, BQ>(sbase + LY::Q0 + s * LY::TILEQ, i * BQ, p.table, step64, wr, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(Q_READY + s));
                 ++st_it;

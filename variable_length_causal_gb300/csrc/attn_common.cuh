@@ -69,13 +69,41 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Per-thread RoPE state for rope_tile: this thread always handles the same
+// 8 rotation pairs j = 8*ci .. 8*ci+7 of rows spaced ROWS_PER_IT apart, so the
+// angle steps by the constant rotation e^{i * ROWS_PER_IT * w_j}, which is the
+// RoPE table's row ROWS_PER_IT.  Loaded once per kernel.
+template <int D>
+struct RopeStep {
+    float c[8], s[8];
+};
+
+template <int D>
+__device__ __forceinline__ RopeStep<D> rope_step(const float2* __restrict__ table, int lane) {
+    constexpr int half = D / 2;
+    constexpr int PAIRS_PER_ROW = half / 8;
+    constexpr int ROWS_PER_IT = 32 / PAIRS_PER_ROW;
+    const int ci = lane % PAIRS_PER_ROW;
+    RopeStep<D> st;
+    const float4* t4 = reinterpret_cast<const float4*>(table + ROWS_PER_IT * half + ci * 8);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 f = __ldg(t4 + q);
+        st.c[2 * q] = f.x; st.s[2 * q] = f.y;
+        st.c[2 * q + 1] = f.z; st.s[2 * q + 1] = f.w;
+    }
+    return st;
+}
+
 // Rotate a staged tile of ROWS rows (segment-local positions pos0 + row) in
 // place: rotate-half pairs (c, c + D/2), x' = x cos - y sin, y' = y cos + x sin,
-// computed in fp32 from the cos/sin table and rounded to bf16.  Executed by
-// 128 threads (4 warps, wr = 0..3); each 64-column block holds ROWS x 128 B.
+// computed in fp32 and rounded to bf16.  Executed by 128 threads (4 warps,
+// wr = 0..3); each 64-column block holds ROWS x 128 B.  A thread reads the
+// cos/sin of its first row from the table and advances the angle by complex
+// multiplication with its RopeStep (a few 1e-7 of drift over the tile).
 template <int D, int ROWS>
 __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2* __restrict__ table,
-                                          int wr, int lane) {
+                                          const RopeStep<D>& step, int wr, int lane) {
     constexpr int half = D / 2;
     constexpr uint32_t BLK = ROWS * 128u;
     constexpr int PAIRS_PER_ROW = half / 8;            // 16-byte chunk pairs per row
@@ -83,9 +111,21 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2*
     constexpr int ROWS_PER_WARP = ROWS / 4;
     const int rsub = lane / PAIRS_PER_ROW;
     const int ci = lane % PAIRS_PER_ROW;
+    const int r0 = wr * ROWS_PER_WARP + rsub;
+    float cs[8], sn[8];
+    {
+        const float4* t4 = reinterpret_cast<const float4*>(
+            table + static_cast<int64_t>(pos0 + r0) * half + ci * 8);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 f = __ldg(t4 + q);
+            cs[2 * q] = f.x; sn[2 * q] = f.y;
+            cs[2 * q + 1] = f.z; sn[2 * q + 1] = f.w;
+        }
+    }
 #pragma unroll 2
     for (int it = 0; it < ROWS_PER_WARP / ROWS_PER_IT; ++it) {
-        const int r = wr * ROWS_PER_WARP + it * ROWS_PER_IT + rsub;
+        const int r = r0 + it * ROWS_PER_IT;
         uint32_t lo_addr, hi_addr;
         if constexpr (D == 128) {
             lo_addr = sw128(tile, r, ci);
@@ -99,15 +139,6 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2*
                      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(lo_addr));
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]) : "r"(hi_addr));
-        const float4* t4 = reinterpret_cast<const float4*>(
-            table + static_cast<int64_t>(pos0 + r) * half + ci * 8);
-        float cs[8], sn[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 f = __ldg(t4 + q);
-            cs[2 * q] = f.x; sn[2 * q] = f.y;
-            cs[2 * q + 1] = f.z; sn[2 * q + 1] = f.w;
-        }
         uint32_t na[4], nb[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -121,6 +152,12 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2*
                      ::"r"(lo_addr), "r"(na[0]), "r"(na[1]), "r"(na[2]), "r"(na[3]) : "memory");
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                      ::"r"(hi_addr), "r"(nb[0]), "r"(nb[1]), "r"(nb[2]), "r"(nb[3]) : "memory");
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {   // advance the angle by ROWS_PER_IT rows
+            const float c = cs[q], sv = sn[q];
+            cs[q] = fmaf(c, step.c[q], -sv * step.s[q]);
+            sn[q] = fmaf(sv, step.c[q], c * step.s[q]);
+        }
     }
 }
 

@@ -264,21 +264,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ++s_it;
 
                 // scale to the log2 domain; mask only on the last (diagonal / tail) tile
+                // raw scores; the mask only on the last (diagonal / tail) tile.  The max of
+                // the raw scores times scale_log2 (> 0) is the max in the log2 domain.
                 float mt = -INFINITY;
                 if (j == w.hi - 1) {
                     const int lim = min(qpos, w.L - 1) - j * BN;   // allowed key columns: c <= lim
 #pragma unroll
                     for (int c = 0; c < BN; ++c) {
-                        x[c] = (c <= lim) ? x[c] * p.scale_log2 : -INFINITY;
+                        x[c] = (c <= lim) ? x[c] : -INFINITY;
                         mt = fmaxf(mt, x[c]);
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) {
-                        x[c] *= p.scale_log2;
-                        mt = fmaxf(mt, x[c]);
-                    }
+                    for (int c = 0; c < BN; ++c) mt = fmaxf(mt, x[c]);
                 }
+                mt *= p.scale_log2;
                 float m_use = m_run, alpha = 1.f;
                 bool rescale = false;
                 if (j == 0) {
@@ -295,8 +295,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 uint32_t pk[BN / 2];
 #pragma unroll
                 for (int c = 0; c < BN / 2; ++c) {
-                    const float p0 = ex2_approx(x[2 * c] - m_use);
-                    const float p1 = ex2_approx(x[2 * c + 1] - m_use);
+                    const float p0 = ex2_approx(fmaf(x[2 * c], p.scale_log2, -m_use));
+                    const float p1 = ex2_approx(fmaf(x[2 * c + 1], p.scale_log2, -m_use));
                     rs += p0 + p1;
                     pk[c] = pack_bf16x2(p0, p1);
                 }
@@ -365,20 +365,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else if (warp >= 8) {
         // ------------------------------------------------------------ RoPE on staged Q/K
         const int wr = warp - 8;
+        RopeStep<D> step{};
+        if (p.use_rope) step = rope_step<D>(p.table, lane);
         uint32_t q_it = 0, kv_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
             const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
             const int qs = q_it & 1;
             if (!(ok = wait_warp(bar(Q_FULL + qs), (q_it >> 1) & 1, abort))) break;
-            if (p.use_rope) rope_tile<D, 128>(sbase + LY::Q0 + qs * LY::TILE, w.tile * BM, p.table, wr, lane);
+            if (p.use_rope) rope_tile<D, 128>(sbase + LY::Q0 + qs * LY::TILE, w.tile * BM, p.table, step, wr, lane);
             fence_proxy_async_smem();
             mbar_arrive(bar(Q_READY + qs));
             ++q_it;
             for (int j = 0; j < w.hi; ++j) {
                 const int ks = kv_it & 1;
                 if (!(ok = wait_warp(bar(K_FULL + ks), (kv_it >> 1) & 1, abort))) break;
-                if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * BN, p.table, wr, lane);
+                if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * BN, p.table, step, wr, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(K_READY + ks));
                 ++kv_it;
