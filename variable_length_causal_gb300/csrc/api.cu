@@ -199,7 +199,7 @@ int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
     float2* table = reinterpret_cast<float2*>(w + L.table);
 
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
-    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items,
+    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD, items,
                         L.item_cap, order, seg_base, &hdr->count, &hdr->err, s) != cudaSuccess)
         return VLC_ERR_CUDA;
     const bool rope = rope_theta != 0.f;

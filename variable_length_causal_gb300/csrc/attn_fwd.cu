@@ -7,20 +7,25 @@
 // are q, k rotated by RoPE at the per-segment positions p = i - cu_r
 // (section "Positions are reset per segment").  LSE = ln sum exp(scores).
 //
-// Design (one persistent CTA per SM, 384 threads, warp-specialised):
-//   warp 0      TMA producer: Q tile (128 rows) per work unit, K/V tiles
-//               (128 rows) per key tile, 128-byte swizzle, 2 stages each.
-//   warp 1      MMA issuer (one thread): S = Q'K'^T into TMEM (double buffer),
-//               O += P V into TMEM (tcgen05.mma kind::f16, fp32 accumulate).
-//   warp 2      TMEM allocator (512 columns).
-//   warps 4-7   softmax + epilogue: one thread per query row (= TMEM lane):
-//               fp32 online softmax in the exp2 domain, the causal / segment-
-//               tail mask only on the last key tile of an item, P (bf16) to
-//               shared memory, lazy O rescale, final O / l and LSE.
-//   warps 8-11  RoPE: rotate the staged Q and K tiles in shared memory at the
-//               segment-local positions, round to bf16, hand them to the MMA.
-// A work unit is one (work item, head) pair; the work list (built on the
-// device beforehand) only holds in-segment, at-or-below-diagonal tiles.
+// Design: one persistent CTA per SM, 512 threads, warp-specialised.  A work
+// unit is (segment, head, block of 256 query rows) = two 128-row q tiles that
+// share every K/V tile; the work list holds only in-segment, at-or-below-
+// diagonal key tiles, and a q tile stops at its own diagonal key tile.
+//   warp 0       TMA producer: q tiles into a 3-slot ring, K/V tiles into 2
+//                stages, 128-byte swizzle.
+//   warp 1       MMA issuer (one thread), tcgen05.mma kind::f16, fp32 in TMEM:
+//                S_t = Q'_t K'^T (shared-memory operands) and O_t += P_t V with
+//                P_t read from TMEM; issue order S0 S1 | PV0(j) S0(j+1)
+//                PV1(j) S1(j+1) | ..., so each q tile's softmax overlaps the
+//                other tile's MMAs.
+//   warp 2       TMEM allocator (512 columns: S/P 0, S/P 1, O 0, O 1).
+//   warps 4-7    softmax + epilogue of q tile 0, one thread per query row:
+//   warps 8-11   the same for q tile 1.  Two passes over the S row in TMEM
+//                (row max, then exp2 and bf16 P written back over the consumed
+//                S columns); the causal / segment-tail mask only on a tile's
+//                last key tile; lazy O rescale when the row max grows by more
+//                than 2^8; epilogue O / l -> bf16 and LSE.
+//   warps 12-15  RoPE on the staged q and K tiles (segment-local positions).
 // Every wait is bounded; on expiry the kernel sets VLC_DEVERR_TIMEOUT, drains
 // its own in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -35,41 +40,56 @@
 namespace vlc {
 namespace fwd {
 
-constexpr int BM = kFwdBM;
-constexpr int BN = kFwdBN;
-static_assert(BM == 128 && BN == 128, "tile shape fixed by the TMEM lane mapping");
-constexpr int kThreads = 384;
+constexpr int BQ = 128;                 // rows per q tile
+constexpr int QB = kFwdQB;              // rows per work unit (two q tiles)
+constexpr int BN = kFwdBN;              // rows per key tile
+static_assert(QB == 2 * BQ && BN == 128, "two 128-row q tiles per unit, 128-row key tiles");
+constexpr int kThreads = 512;
+constexpr int kQSlots = 3;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when max grows > 2^8
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// barrier slots
 enum : int {
-    Q_FULL = 0, Q_READY = 2, Q_EMPTY = 4,
-    K_FULL = 6, K_READY = 8, K_EMPTY = 10,
-    V_FULL = 12, V_EMPTY = 14,
-    S_FULL = 16, S_EMPTY = 18,
-    P_FULL = 20, PV_DONE = 21, O_EMPTY = 22, DRAIN = 23,
-    NUM_BARS = 24
+    Q_FULL = 0, Q_READY = 3, Q_EMPTY = 6,
+    K_FULL = 9, K_READY = 11, V_FULL = 13, KV_EMPTY = 15,
+    S_FULL = 17, P_FULL = 19, O_FULL = 21, O_EMPTY = 23,
+    DRAIN = 25, NUM_BARS = 26
 };
 
 template <int D>
 struct Layout {
-    static constexpr int KB = D / 64;                  // 64-column (128-byte) blocks per row
-    static constexpr uint32_t BLK = 128u * 128u;       // one block of 128 rows: 16 KB
-    static constexpr uint32_t TILE = 128u * D * 2u;    // a Q/K/V tile
-    static constexpr uint32_t Q0 = 0;
-    static constexpr uint32_t K0 = Q0 + 2 * TILE;
-    static constexpr uint32_t V0 = K0 + 2 * TILE;
-    static constexpr uint32_t P0 = V0 + 2 * TILE;
-    static constexpr uint32_t PBYTES = 128u * BN * 2u;
-    static constexpr uint32_t BAR0 = P0 + PBYTES;
+    static constexpr int KB = D / 64;
+    static constexpr uint32_t BLK = 128u * 128u;       // 128 rows x 128 bytes
+    static constexpr uint32_t TILE = 128u * D * 2u;
+    static constexpr uint32_t Q0 = 0;                  // kQSlots tiles
+    static constexpr uint32_t K0 = kQSlots * TILE;     // 2 stages
+    static constexpr uint32_t V0 = K0 + 2 * TILE;      // 2 stages
+    static constexpr uint32_t BAR0 = V0 + 2 * TILE;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;
     static constexpr uint32_t BYTES = MISC + 16;
-    static constexpr uint32_t ALLOC = BYTES + 1024;    // room to align the base to 1024
-    static constexpr uint32_t S_COL = 0;               // S buffers at columns 0 and 128
-    static constexpr uint32_t O_COL = 256;             // O at columns 256 .. 256+D
+    static constexpr uint32_t ALLOC = BYTES + 1024;
+    __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }   // P_t shares these columns
+    __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + 128u * t; }
 };
+
+// One work unit: q tile t (t = 0, 1) covers rows qb*256 + t*128 + [0, 128) of
+// the segment and needs key tiles [0, n_t): n_0 = 2qb + 1 (up to its diagonal),
+// n_1 = 2qb + 2 when the second tile holds any row of the segment, else absent.
+struct FUnit {
+    Unit w;
+    bool has1;
+    int n0, n1;
+};
+
+__device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
+    FUnit f;
+    f.w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+    f.has1 = f.w.L > f.w.tile * QB + BQ;
+    f.n0 = 2 * f.w.tile + 1;
+    f.n1 = f.has1 ? f.w.hi : 0;
+    return f;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -82,7 +102,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     auto bar = [&](int i) -> uint32_t { return sbase + LY::BAR0 + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
-
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -96,21 +115,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int nunits = s_nunits;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQSlots; ++i) {
             mbar_init(bar(Q_FULL + i), 1);
             mbar_init(bar(Q_READY + i), 128);
             mbar_init(bar(Q_EMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(K_FULL + i), 1);
             mbar_init(bar(K_READY + i), 128);
-            mbar_init(bar(K_EMPTY + i), 1);
             mbar_init(bar(V_FULL + i), 1);
-            mbar_init(bar(V_EMPTY + i), 1);
+            mbar_init(bar(KV_EMPTY + i), 1);
             mbar_init(bar(S_FULL + i), 1);
-            mbar_init(bar(S_EMPTY + i), 128);
+            mbar_init(bar(P_FULL + i), 128);
+            mbar_init(bar(O_FULL + i), 1);
+            mbar_init(bar(O_EMPTY + i), 128);
         }
-        mbar_init(bar(P_FULL), 128);
-        mbar_init(bar(PV_DONE), 1);
-        mbar_init(bar(O_EMPTY), 128);
         mbar_init(bar(DRAIN), 1);
         *abort = 0;
         fence_mbar_init();
@@ -127,47 +146,41 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // per-role counters kept for the teardown drain
-    uint32_t q_issued = 0, kv_issued = 0;
+    uint32_t q_issued = 0, kv_issued = 0;   // for the teardown drain
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t q_it = 0, kv_it = 0;
-            for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-                const int qs = q_it & 1;
-                if (!mbar_wait(bar(Q_EMPTY + qs), ((q_it >> 1) & 1) ^ 1, abort)) break;
-                mbar_expect_tx(bar(Q_FULL + qs), LY::TILE);
-                const uint32_t qdst = sbase + LY::Q0 + qs * LY::TILE;
-#pragma unroll
-                for (int kb = 0; kb < LY::KB; ++kb)
-                    tma_load_3d(qdst + kb * LY::BLK, &tmQ, kb * 64, w.h, w.row0 + w.tile * BM,
-                                bar(Q_FULL + qs));
-                q_issued = ++q_it;
-                bool ok = true;
-                for (int j = 0; j < w.hi && ok; ++j) {
-                    const int ks = kv_it & 1;
-                    const uint32_t ph = ((kv_it >> 1) & 1) ^ 1;
-                    const int row = w.row0 + j * BN;
-                    if (!(ok = mbar_wait(bar(K_EMPTY + ks), ph, abort))) break;
-                    mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
+            uint32_t qm = 0, kvn = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+                const FUnit f = decode_funit(p, u);
+                for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
+                    const int slot = qm % kQSlots;
+                    if (!(ok = mbar_wait(bar(Q_EMPTY + slot), ((qm / kQSlots) & 1) ^ 1, abort))) break;
+                    mbar_expect_tx(bar(Q_FULL + slot), LY::TILE);
+                    const int row = f.w.row0 + f.w.tile * QB + t * BQ;
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
-                        tma_load_3d(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
-                                    w.h, row, bar(K_FULL + ks));
-                    if (!(ok = mbar_wait(bar(V_EMPTY + ks), ph, abort))) {
-                        kv_issued = kv_it + 1;   // the K half of this stage is in flight
-                        break;
-                    }
+                        tma_load_3d(sbase + LY::Q0 + slot * LY::TILE + kb * LY::BLK, &tmQ, kb * 64,
+                                    f.w.h, row, bar(Q_FULL + slot));
+                    q_issued = ++qm;
+                }
+                for (int j = 0; j < f.w.hi && ok; ++j) {
+                    const int ks = kvn & 1;
+                    if (!(ok = mbar_wait(bar(KV_EMPTY + ks), ((kvn >> 1) & 1) ^ 1, abort))) break;
+                    const int row = f.w.row0 + j * BN;
+                    mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
                     mbar_expect_tx(bar(V_FULL + ks), LY::TILE);
 #pragma unroll
-                    for (int kb = 0; kb < LY::KB; ++kb)
+                    for (int kb = 0; kb < LY::KB; ++kb) {
+                        tma_load_3d(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
+                                    f.w.h, row, bar(K_FULL + ks));
                         tma_load_3d(sbase + LY::V0 + ks * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
-                                    w.h, row, bar(V_FULL + ks));
-                    kv_issued = ++kv_it;
+                                    f.w.h, row, bar(V_FULL + ks));
+                    }
+                    kv_issued = ++kvn;
                 }
-                if (!ok) break;
             }
         }
         __syncwarp();
@@ -176,175 +189,177 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false);
             constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
-            uint32_t q_it = 0, kv_it = 0, s_it = 0, pv_it = 0, unit_it = 0;
+            uint32_t qm = 0, kvn = 0, cnt_p[2] = {0, 0}, cnt_u[2] = {0, 0};
             bool ok = true;
-            auto issue_pv = [&](bool first) -> bool {
-                const int vs = pv_it & 1;
-                if (first && !mbar_wait(bar(O_EMPTY), (unit_it & 1) ^ 1, abort)) return false;
-                if (!mbar_wait(bar(V_FULL + vs), (pv_it >> 1) & 1, abort)) return false;
-                if (!mbar_wait(bar(P_FULL), pv_it & 1, abort)) return false;
-                tc_fence_after();
-                const uint32_t vbase = sbase + LY::V0 + vs * LY::TILE;
-                const uint32_t pbase = sbase + LY::P0;
+            auto issue_s = [&](int t, int slot, int ks) {
+                const uint32_t qb = sbase + LY::Q0 + slot * LY::TILE;
+                const uint32_t kb = sbase + LY::K0 + ks * LY::TILE;
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint64_t a = smem_desc_sw128(pbase + (k >> 2) * LY::BLK + (k & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(vbase + k * 16 * 128, LY::BLK, 1024);
-                    mma_bf16_ss(tmem + LY::O_COL, a, b, IDESC_O, (!first || k > 0) ? 1u : 0u);
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
+                    mma_bf16_ss(tmem + LY::S_COL(t), smem_desc_sw128(qb + off, 16, 1024),
+                                smem_desc_sw128(kb + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(PV_DONE));
-                mma_commit(bar(V_EMPTY + vs));
-                ++pv_it;
-                return true;
+                mma_commit(bar(S_FULL + t));
             };
             for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-                const int qs = q_it & 1;
-                if (!(ok = mbar_wait(bar(Q_READY + qs), (q_it >> 1) & 1, abort))) break;
-                const uint32_t qbase = sbase + LY::Q0 + qs * LY::TILE;
-                for (int j = 0; j < w.hi; ++j) {
-                    const int ks = kv_it & 1;
-                    if (!(ok = mbar_wait(bar(K_READY + ks), (kv_it >> 1) & 1, abort))) break;
-                    const int sb = s_it & 1;
-                    if (!(ok = mbar_wait(bar(S_EMPTY + sb), ((s_it >> 1) & 1) ^ 1, abort))) break;
+                const FUnit f = decode_funit(p, u);
+                const int n[2] = {f.n0, f.n1};
+                const int slot[2] = {static_cast<int>(qm % kQSlots), static_cast<int>((qm + 1) % kQSlots)};
+                if (!(ok = mbar_wait(bar(Q_READY + slot[0]), (qm / kQSlots) & 1, abort))) break;
+                if (f.has1 && !(ok = mbar_wait(bar(Q_READY + slot[1]), ((qm + 1) / kQSlots) & 1, abort)))
+                    break;
+                {
+                    const int ks = kvn & 1;
+                    if (!(ok = mbar_wait(bar(K_READY + ks), (kvn >> 1) & 1, abort))) break;
                     tc_fence_after();
-                    const uint32_t kbase = sbase + LY::K0 + ks * LY::TILE;
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
-                        mma_bf16_ss(tmem + LY::S_COL + sb * 128,
-                                    smem_desc_sw128(qbase + off, 16, 1024),
-                                    smem_desc_sw128(kbase + off, 16, 1024), IDESC_S,
-                                    k > 0 ? 1u : 0u);
+                    for (int t = 0; t < 2; ++t) {
+                        if (n[t] == 0) continue;
+                        issue_s(t, slot[t], ks);
+                        if (n[t] == 1) mma_commit(bar(Q_EMPTY + slot[t]));
                     }
-                    mma_commit(bar(S_FULL + sb));
-                    mma_commit(bar(K_EMPTY + ks));
-                    if (j == w.hi - 1) mma_commit(bar(Q_EMPTY + qs));
-                    ++s_it;
-                    ++kv_it;
-                    if (j > 0 && !(ok = issue_pv(j == 1))) break;
+                }
+                for (int j = 0; j < f.w.hi && ok; ++j) {
+                    const uint32_t kvj = kvn + j;
+                    const int vs = kvj & 1;
+                    if (!(ok = mbar_wait(bar(V_FULL + vs), (kvj >> 1) & 1, abort))) break;
+                    bool k_next = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= n[t]) continue;
+                        if (!(ok = mbar_wait(bar(P_FULL + t), cnt_p[t] & 1, abort))) break;
+                        ++cnt_p[t];
+                        if (j == 0 && !(ok = mbar_wait(bar(O_EMPTY + t), (cnt_u[t] & 1) ^ 1, abort))) break;
+                        tc_fence_after();
+                        const uint32_t vb = sbase + LY::V0 + vs * LY::TILE;
+#pragma unroll
+                        for (int k = 0; k < BN / 16; ++k)
+                            mma_bf16_ts(tmem + LY::O_COL(t), tmem + LY::S_COL(t) + 8 * k,
+                                        smem_desc_sw128(vb + k * 16 * 128, LY::BLK, 1024), IDESC_O,
+                                        (j > 0 || k > 0) ? 1u : 0u);
+                        if (j == n[t] - 1) mma_commit(bar(O_FULL + t));
+                        if (j + 1 < n[t]) {
+                            const uint32_t kvn1 = kvj + 1;
+                            if (!k_next) {
+                                if (!(ok = mbar_wait(bar(K_READY + (kvn1 & 1)), (kvn1 >> 1) & 1, abort))) break;
+                                tc_fence_after();
+                                k_next = true;
+                            }
+                            issue_s(t, slot[t], kvn1 & 1);
+                            if (j + 1 == n[t] - 1) mma_commit(bar(Q_EMPTY + slot[t]));
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(KV_EMPTY + vs));
                 }
                 if (!ok) break;
-                if (!(ok = issue_pv(w.hi == 1))) break;
-                ++q_it;
-                ++unit_it;
+                kvn += f.w.hi;
+                qm += f.has1 ? 2 : 1;
+                ++cnt_u[0];
+                if (f.has1) ++cnt_u[1];
             }
-            // let every issued MMA finish before TMEM can be released
             mma_commit(bar(DRAIN));
             mbar_wait_limit(bar(DRAIN), 0, 200000000ull);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ softmax + epilogue
-        const int wq = warp - 4;
-        const int r = wq * 32 + lane;                  // query row in the tile = TMEM lane
+        const int t = (warp - 4) >> 2;             // q tile slot handled by this warpgroup
+        const int wq = warp & 3;                   // TMEM lane quadrant
+        const int r = wq * 32 + lane;              // query row in the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t sP = sbase + LY::P0;
-        uint32_t s_it = 0, pv_it = 0;
+        const uint32_t sadr = tmem + lane_off + LY::S_COL(t);
+        const uint32_t oadr = tmem + lane_off + LY::O_COL(t);
+        const float sl2 = p.scale_log2;
+        uint32_t cnt_s = 0, cnt_u = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-            const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-            const int qpos = w.tile * BM + r;
+            const FUnit f = decode_funit(p, u);
+            const int nt = t == 0 ? f.n0 : f.n1;
+            if (nt == 0) continue;
+            const int qpos = f.w.tile * QB + t * BQ + r;
             float m_run = 0.f, l_run = 0.f;
-            for (int j = 0; j < w.hi; ++j) {
-                const int sb = s_it & 1;
-                if (!(ok = wait_warp(bar(S_FULL + sb), (s_it >> 1) & 1, abort))) break;
+            for (int j = 0; j < nt; ++j) {
+                if (!(ok = wait_warp(bar(S_FULL + t), cnt_s & 1, abort))) break;
+                ++cnt_s;
                 tc_fence_after();
-                float x[BN];
-#pragma unroll
+                // allowed key columns of this tile: c <= lim (only the last tile is masked)
+                const int lim = (j == nt - 1) ? min(qpos, f.w.L - 1) - j * BN : BN - 1;
+                // pass 1: row max of the raw scores
+                float mx = -INFINITY;
+#pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t rr[32];
-                    tmem_ld32(tmem + lane_off + LY::S_COL + sb * 128 + c * 32, rr);
+                    tmem_ld32(sadr + c * 32, rr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(rr[e]);
+                    for (int e = 0; e < 32; ++e)
+                        mx = fmaxf(mx, (c * 32 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY);
                 }
-                tc_fence_before();
-                mbar_arrive(bar(S_EMPTY + sb));
-                ++s_it;
-
-                // scale to the log2 domain; mask only on the last (diagonal / tail) tile
-                // raw scores; the mask only on the last (diagonal / tail) tile.  The max of
-                // the raw scores times scale_log2 (> 0) is the max in the log2 domain.
-                float mt = -INFINITY;
-                if (j == w.hi - 1) {
-                    const int lim = min(qpos, w.L - 1) - j * BN;   // allowed key columns: c <= lim
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) {
-                        x[c] = (c <= lim) ? x[c] : -INFINITY;
-                        mt = fmaxf(mt, x[c]);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) mt = fmaxf(mt, x[c]);
-                }
-                mt *= p.scale_log2;
+                const float mt = mx * sl2;
                 float m_use = m_run, alpha = 1.f;
                 bool rescale = false;
                 if (j == 0) {
                     m_use = mt;
                 } else {
-                    const bool need = mt > m_run + kRescaleThreshold;
-                    rescale = __any_sync(0xffffffffu, need);
+                    rescale = __any_sync(0xffffffffu, mt > m_run + kRescaleThreshold);
                     if (rescale) {
                         m_use = fmaxf(m_run, mt);
                         alpha = ex2_approx(m_run - m_use);
                     }
                 }
-                float rs = 0.f;
-                uint32_t pk[BN / 2];
-#pragma unroll
-                for (int c = 0; c < BN / 2; ++c) {
-                    const float p0 = ex2_approx(fmaf(x[2 * c], p.scale_log2, -m_use));
-                    const float p1 = ex2_approx(fmaf(x[2 * c + 1], p.scale_log2, -m_use));
-                    rs += p0 + p1;
-                    pk[c] = pack_bf16x2(p0, p1);
-                }
-                // previous P·V must be done: frees the P buffer and makes O stable
-                if (pv_it > 0 && !(ok = wait_warp(bar(PV_DONE), (pv_it - 1) & 1, abort))) break;
-                if (rescale) {
-                    tc_fence_after();
+                if (rescale) {   // O_t is stable: S_t(j) done implies P_t V(j-1) done
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t rr[32];
-                        const uint32_t ta = tmem + lane_off + LY::O_COL + c * 32;
-                        tmem_ld32(ta, rr);
+                        tmem_ld32(oadr + c * 32, rr);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-                        tmem_st32(ta, rr);
+                        tmem_st32(oadr + c * 32, rr);
                     }
-                    tmem_wait_st();
                     l_run *= alpha;
                 }
-                l_run += rs;
-                m_run = m_use;
+                // pass 2: P = exp2(s * scale_log2 - m), bf16, written over consumed S columns
+                const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
+                float2 rs2 = make_float2(0.f, 0.f);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(sadr + c * 32, rr);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
 #pragma unroll
-                for (int ci = 0; ci < BN / 8; ++ci) {
-                    const uint32_t addr = sw128(sP + (ci >> 3) * LY::BLK, r, ci & 7);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(addr), "r"(pk[4 * ci]), "r"(pk[4 * ci + 1]),
-                                 "r"(pk[4 * ci + 2]), "r"(pk[4 * ci + 3]) : "memory");
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 x = fma2(make_float2(__uint_as_float(rr[2 * e]),
+                                                          __uint_as_float(rr[2 * e + 1])), sc2, nm2);
+                        const int col = c * 32 + 2 * e;
+                        const float p0 = (col <= lim) ? ex2_approx(x.x) : 0.f;
+                        const float p1 = (col + 1 <= lim) ? ex2_approx(x.y) : 0.f;
+                        rs2 = add2(rs2, make_float2(p0, p1));
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(sadr + c * 16, pk);
                 }
-                fence_proxy_async_smem();
+                tmem_wait_st();
+                l_run += rs2.x + rs2.y;
+                m_run = m_use;
                 tc_fence_before();
-                mbar_arrive(bar(P_FULL));
-                ++pv_it;
+                mbar_arrive(bar(P_FULL + t));
             }
             if (!ok) break;
             // ---- epilogue: O / l -> bf16, LSE
-            if (!(ok = wait_warp(bar(PV_DONE), (pv_it - 1) & 1, abort))) break;
+            if (!(ok = wait_warp(bar(O_FULL + t), cnt_u & 1, abort))) break;
             tc_fence_after();
-            const bool valid = qpos < w.L;
-            const int64_t tok = static_cast<int64_t>(w.row0) + qpos;
+            const bool valid = qpos < f.w.L;
+            const int64_t tok = static_cast<int64_t>(f.w.row0) + qpos;
             const float inv_l = 1.f / l_run;
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                            ((valid ? tok : 0) * p.H + w.h) * static_cast<int64_t>(D) * 2;
+                            ((valid ? tok : 0) * p.H + f.w.h) * static_cast<int64_t>(D) * 2;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + lane_off + LY::O_COL + c * 32, rr);
+                tmem_ld32(oadr + c * 32, rr);
                 tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
@@ -358,32 +373,39 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
             }
-            if (valid) p.lse[static_cast<int64_t>(w.h) * p.total + tok] = (m_run + __log2f(l_run)) * kLn2;
+            if (valid)
+                p.lse[static_cast<int64_t>(f.w.h) * p.total + tok] = (m_run + __log2f(l_run)) * kLn2;
             tc_fence_before();
-            mbar_arrive(bar(O_EMPTY));
+            mbar_arrive(bar(O_EMPTY + t));
+            ++cnt_u;
         }
-    } else if (warp >= 8) {
-        // ------------------------------------------------------------ RoPE on staged Q/K
-        const int wr = warp - 8;
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ RoPE on staged q / K tiles
+        const int wr = warp - 12;
         RopeStep<D> step{};
         if (p.use_rope) step = rope_step<D>(p.table, lane);
-        uint32_t q_it = 0, kv_it = 0;
+        uint32_t qm = 0, kvn = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-            const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-            const int qs = q_it & 1;
-            if (!(ok = wait_warp(bar(Q_FULL + qs), (q_it >> 1) & 1, abort))) break;
-            if (p.use_rope) rope_tile<D, 128>(sbase + LY::Q0 + qs * LY::TILE, w.tile * BM, p.table, step, wr, lane);
-            fence_proxy_async_smem();
-            mbar_arrive(bar(Q_READY + qs));
-            ++q_it;
-            for (int j = 0; j < w.hi; ++j) {
-                const int ks = kv_it & 1;
-                if (!(ok = wait_warp(bar(K_FULL + ks), (kv_it >> 1) & 1, abort))) break;
-                if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * BN, p.table, step, wr, lane);
+            const FUnit f = decode_funit(p, u);
+            for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
+                const int slot = qm % kQSlots;
+                if (!(ok = wait_warp(bar(Q_FULL + slot), (qm / kQSlots) & 1, abort))) break;
+                if (p.use_rope)
+                    rope_tile<D, 128>(sbase + LY::Q0 + slot * LY::TILE, f.w.tile * QB + t * BQ, p.table,
+                                      step, wr, lane);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(Q_READY + slot));
+                ++qm;
+            }
+            for (int j = 0; j < f.w.hi && ok; ++j) {
+                const int ks = kvn & 1;
+                if (!(ok = wait_warp(bar(K_FULL + ks), (kvn >> 1) & 1, abort))) break;
+                if (p.use_rope)
+                    rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * BN, p.table, step, wr, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(K_READY + ks));
-                ++kv_it;
+                ++kvn;
             }
         }
     }
@@ -391,18 +413,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     if (*abort) {
         if (warp == 0 && lane == 0) {
-            // wait (bounded) for the last copy issued on every stage
-            for (int s = 0; s < 2; ++s) {
+            // wait (bounded) for the last copy issued into every slot and stage
+            for (int s = 0; s < kQSlots; ++s)
                 if (q_issued > static_cast<uint32_t>(s)) {
-                    const uint32_t n = ((q_issued - 1 - s) & ~1u) + s;
-                    mbar_wait_limit(bar(Q_FULL + s), (n >> 1) & 1, 200000000ull);
+                    const uint32_t n = q_issued - 1 - ((q_issued - 1 - s) % kQSlots);
+                    mbar_wait_limit(bar(Q_FULL + s), (n / kQSlots) & 1, 200000000ull);
                 }
+            for (int s = 0; s < 2; ++s)
                 if (kv_issued > static_cast<uint32_t>(s)) {
                     const uint32_t n = ((kv_issued - 1 - s) & ~1u) + s;
                     mbar_wait_limit(bar(K_FULL + s), (n >> 1) & 1, 200000000ull);
                     mbar_wait_limit(bar(V_FULL + s), (n >> 1) & 1, 200000000ull);
                 }
-            }
         }
         if (threadIdx.x == 0) atomicOr(p.err, VLC_DEVERR_TIMEOUT);
         __syncthreads();

@@ -6,7 +6,8 @@
 
 namespace vlc {
 
-constexpr int kFwdBM = 128;   // query rows per forward tile
+constexpr int kFwdBM = 128;   // query rows per tile (dQ pass work list)
+constexpr int kFwdQB = 256;   // query rows per forward work unit (two q tiles)
 constexpr int kFwdBN = 128;   // key rows per forward tile
 constexpr int kBwdBM = 64;    // query rows per backward step
 constexpr int kBwdBN = 64;    // key rows per backward tile
