@@ -75,7 +75,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 // RoPE table's row ROWS_PER_IT.  Loaded once per kernel.
 template <int D>
 struct RopeStep {
-    float c[8], s[8];
+    float2 c[4], s[4], ns[4];   // pairs (2q, 2q+1): cos, sin, -sin of the per-step angle
 };
 
 template <int D>
@@ -89,18 +89,19 @@ __device__ __forceinline__ RopeStep<D> rope_step(const float2* __restrict__ tabl
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const float4 f = __ldg(t4 + q);
-        st.c[2 * q] = f.x; st.s[2 * q] = f.y;
-        st.c[2 * q + 1] = f.z; st.s[2 * q + 1] = f.w;
+        st.c[q] = make_float2(f.x, f.z);
+        st.s[q] = make_float2(f.y, f.w);
+        st.ns[q] = make_float2(-f.y, -f.w);
     }
     return st;
 }
 
 // Rotate a staged tile of ROWS rows (segment-local positions pos0 + row) in
 // place: rotate-half pairs (c, c + D/2), x' = x cos - y sin, y' = y cos + x sin,
-// computed in fp32 and rounded to bf16.  Executed by 128 threads (4 warps,
-// wr = 0..3); each 64-column block holds ROWS x 128 B.  A thread reads the
-// cos/sin of its first row from the table and advances the angle by complex
-// multiplication with its RopeStep (a few 1e-7 of drift over the tile).
+// computed in fp32 (packed pairs) and rounded to bf16.  Executed by 128 threads
+// (4 warps, wr = 0..3); each 64-column block holds ROWS x 128 B.  A thread
+// reads the cos/sin of its first row from the table and advances the angle by
+// complex multiplication with its RopeStep (a few 1e-7 of drift over a tile).
 template <int D, int ROWS>
 __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2* __restrict__ table,
                                           const RopeStep<D>& step, int wr, int lane) {
@@ -112,15 +113,15 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2*
     const int rsub = lane / PAIRS_PER_ROW;
     const int ci = lane % PAIRS_PER_ROW;
     const int r0 = wr * ROWS_PER_WARP + rsub;
-    float cs[8], sn[8];
+    float2 cs[4], sn[4];   // cos/sin of rotation pairs (2q, 2q+1) at the current row
     {
         const float4* t4 = reinterpret_cast<const float4*>(
             table + static_cast<int64_t>(pos0 + r0) * half + ci * 8);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 f = __ldg(t4 + q);
-            cs[2 * q] = f.x; sn[2 * q] = f.y;
-            cs[2 * q + 1] = f.z; sn[2 * q + 1] = f.w;
+            cs[q] = make_float2(f.x, f.z);
+            sn[q] = make_float2(f.y, f.w);
         }
     }
 #pragma unroll 2
@@ -142,21 +143,23 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2*
         uint32_t na[4], nb[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float x0 = bf16_lo(a[q]), x1 = bf16_hi(a[q]);
-            const float y0 = bf16_lo(b[q]), y1 = bf16_hi(b[q]);
-            const float c0 = cs[2 * q], s0 = sn[2 * q], c1 = cs[2 * q + 1], s1 = sn[2 * q + 1];
-            na[q] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
-            nb[q] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+            const float2 x = make_float2(bf16_lo(a[q]), bf16_hi(a[q]));
+            const float2 y = make_float2(bf16_lo(b[q]), bf16_hi(b[q]));
+            const float2 nsn = make_float2(-sn[q].x, -sn[q].y);
+            const float2 xr = fma2(x, cs[q], mul2(y, nsn));    // x cos - y sin
+            const float2 yr = fma2(y, cs[q], mul2(x, sn[q]));  // y cos + x sin
+            na[q] = pack_bf16x2(xr.x, xr.y);
+            nb[q] = pack_bf16x2(yr.x, yr.y);
         }
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                      ::"r"(lo_addr), "r"(na[0]), "r"(na[1]), "r"(na[2]), "r"(na[3]) : "memory");
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                      ::"r"(hi_addr), "r"(nb[0]), "r"(nb[1]), "r"(nb[2]), "r"(nb[3]) : "memory");
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {   // advance the angle by ROWS_PER_IT rows
-            const float c = cs[q], sv = sn[q];
-            cs[q] = fmaf(c, step.c[q], -sv * step.s[q]);
-            sn[q] = fmaf(sv, step.c[q], c * step.s[q]);
+        for (int q = 0; q < 4; ++q) {   // advance the angle by ROWS_PER_IT rows
+            const float2 c = cs[q], sv = sn[q];
+            cs[q] = fma2(c, step.c[q], mul2(sv, step.ns[q]));   // c cos_d - s sin_d
+            sn[q] = fma2(sv, step.c[q], mul2(c, step.s[q]));    // s cos_d + c sin_d
         }
     }
 }

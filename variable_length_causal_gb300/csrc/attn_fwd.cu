@@ -52,9 +52,9 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 enum : int {
     Q_FULL = 0, Q_READY = 3, Q_EMPTY = 6,
-    K_FULL = 9, K_READY = 11, V_FULL = 13, KV_EMPTY = 15,
-    S_FULL = 17, P_FULL = 19, O_FULL = 21, O_EMPTY = 23,
-    DRAIN = 25, NUM_BARS = 26
+    K_FULL = 9, K_READY = 11, K_EMPTY = 13, V_FULL = 15, V_EMPTY = 17,
+    S_FULL = 19, P_FULL = 21, O_FULL = 23, O_EMPTY = 25,
+    DRAIN = 27, NUM_BARS = 28
 };
 
 template <int D>
@@ -123,8 +123,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(K_FULL + i), 1);
             mbar_init(bar(K_READY + i), 128);
+            mbar_init(bar(K_EMPTY + i), 1);
             mbar_init(bar(V_FULL + i), 1);
-            mbar_init(bar(KV_EMPTY + i), 1);
+            mbar_init(bar(V_EMPTY + i), 1);
             mbar_init(bar(S_FULL + i), 1);
             mbar_init(bar(P_FULL + i), 128);
             mbar_init(bar(O_FULL + i), 1);
@@ -146,7 +147,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    uint32_t q_issued = 0, kv_issued = 0;   // for the teardown drain
+    uint32_t q_issued = 0, k_issued = 0, kv_issued = 0;   // for the teardown drain
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -166,21 +167,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                     f.w.h, row, bar(Q_FULL + slot));
                     q_issued = ++qm;
                 }
-                for (int j = 0; j < f.w.hi && ok; ++j) {
-                    const int ks = kvn & 1;
-                    if (!(ok = mbar_wait(bar(KV_EMPTY + ks), ((kvn >> 1) & 1) ^ 1, abort))) break;
-                    const int row = f.w.row0 + j * BN;
-                    mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
-                    mbar_expect_tx(bar(V_FULL + ks), LY::TILE);
+                // K tile j is loaded one step ahead of V tile j-1, so the RoPE warps
+                // can rotate K while the MMAs of the previous tile still read V.
+                for (int j = 0; j <= f.w.hi && ok; ++j) {
+                    if (j < f.w.hi) {
+                        const uint32_t n = kvn + j;
+                        const int ks = n & 1;
+                        if (!(ok = mbar_wait(bar(K_EMPTY + ks), ((n >> 1) & 1) ^ 1, abort))) break;
+                        mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
 #pragma unroll
-                    for (int kb = 0; kb < LY::KB; ++kb) {
-                        tma_load_3d(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
-                                    f.w.h, row, bar(K_FULL + ks));
-                        tma_load_3d(sbase + LY::V0 + ks * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
-                                    f.w.h, row, bar(V_FULL + ks));
+                        for (int kb = 0; kb < LY::KB; ++kb)
+                            tma_load_3d(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
+                                        f.w.h, f.w.row0 + j * BN, bar(K_FULL + ks));
+                        k_issued = n + 1;
                     }
-                    kv_issued = ++kvn;
+                    if (j >= 1) {
+                        const uint32_t n = kvn + j - 1;
+                        const int vs = n & 1;
+                        if (!(ok = mbar_wait(bar(V_EMPTY + vs), ((n >> 1) & 1) ^ 1, abort))) break;
+                        mbar_expect_tx(bar(V_FULL + vs), LY::TILE);
+#pragma unroll
+                        for (int kb = 0; kb < LY::KB; ++kb)
+                            tma_load_3d(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
+                                        f.w.h, f.w.row0 + (j - 1) * BN, bar(V_FULL + vs));
+                        kv_issued = n + 1;
+                    }
                 }
+                kvn += f.w.hi;
             }
         }
         __syncwarp();
@@ -218,6 +231,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         issue_s(t, slot[t], ks);
                         if (n[t] == 1) mma_commit(bar(Q_EMPTY + slot[t]));
                     }
+                    mma_commit(bar(K_EMPTY + ks));
                 }
                 for (int j = 0; j < f.w.hi && ok; ++j) {
                     const uint32_t kvj = kvn + j;
@@ -249,7 +263,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         }
                     }
                     if (!ok) break;
-                    mma_commit(bar(KV_EMPTY + vs));
+                    mma_commit(bar(V_EMPTY + vs));
+                    if (k_next) mma_commit(bar(K_EMPTY + ((kvj + 1) & 1)));
                 }
                 if (!ok) break;
                 kvn += f.w.hi;
@@ -283,17 +298,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ++cnt_s;
                 tc_fence_after();
                 // allowed key columns of this tile: c <= lim (only the last tile is masked)
-                const int lim = (j == nt - 1) ? min(qpos, f.w.L - 1) - j * BN : BN - 1;
-                // pass 1: row max of the raw scores
+                const bool edge = (j == nt - 1);
+                const int lim = edge ? min(qpos, f.w.L - 1) - j * BN : BN - 1;
+                // pass 1: row max of the raw scores (two 32-column loads in flight)
                 float mx = -INFINITY;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(sadr + c * 32, rr);
+                for (int c = 0; c < BN / 32; c += 2) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32(sadr + c * 32, ra);
+                    tmem_ld32(sadr + c * 32 + 32, rb);
                     tmem_wait_ld();
+                    if (edge) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        mx = fmaxf(mx, (c * 32 + e <= lim) ? __uint_as_float(rr[e]) : -INFINITY);
+                        for (int e = 0; e < 32; ++e) {
+                            mx = fmaxf(mx, (c * 32 + e <= lim) ? __uint_as_float(ra[e]) : -INFINITY);
+                            mx = fmaxf(mx, (c * 32 + 32 + e <= lim) ? __uint_as_float(rb[e]) : -INFINITY);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            mx = fmaxf(mx, fmaxf(__uint_as_float(ra[e]), __uint_as_float(rb[e])));
+                    }
                 }
                 const float mt = mx * sl2;
                 float m_use = m_run, alpha = 1.f;
@@ -308,7 +333,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                 }
                 if (rescale) {   // O_t is stable: S_t(j) done implies P_t V(j-1) done
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t rr[32];
                         tmem_ld32(oadr + c * 32, rr);
@@ -320,26 +345,43 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                     l_run *= alpha;
                 }
-                // pass 2: P = exp2(s * scale_log2 - m), bf16, written over consumed S columns
+                // pass 2: P = exp2(s * scale_log2 - m), bf16, written over consumed S columns;
+                // the next chunk's load is in flight while this chunk is exponentiated.
                 const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
                 float2 rs2 = make_float2(0.f, 0.f);
+                uint32_t rr[32];
+                tmem_ld32(sadr, rr);
+                tmem_wait_ld();
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(sadr + c * 32, rr);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
+                    uint32_t cur[32];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 x = fma2(make_float2(__uint_as_float(rr[2 * e]),
-                                                          __uint_as_float(rr[2 * e + 1])), sc2, nm2);
-                        const int col = c * 32 + 2 * e;
-                        const float p0 = (col <= lim) ? ex2_approx(x.x) : 0.f;
-                        const float p1 = (col + 1 <= lim) ? ex2_approx(x.y) : 0.f;
-                        rs2 = add2(rs2, make_float2(p0, p1));
-                        pk[e] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 32; ++e) cur[e] = rr[e];
+                    if (c + 1 < BN / 32) tmem_ld32(sadr + (c + 1) * 32, rr);
+                    uint32_t pk[16];
+                    if (edge) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 x = fma2(make_float2(__uint_as_float(cur[2 * e]),
+                                                              __uint_as_float(cur[2 * e + 1])), sc2, nm2);
+                            const int col = c * 32 + 2 * e;
+                            const float p0 = (col <= lim) ? ex2_approx(x.x) : 0.f;
+                            const float p1 = (col + 1 <= lim) ? ex2_approx(x.y) : 0.f;
+                            rs2 = add2(rs2, make_float2(p0, p1));
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 x = fma2(make_float2(__uint_as_float(cur[2 * e]),
+                                                              __uint_as_float(cur[2 * e + 1])), sc2, nm2);
+                            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                            rs2 = add2(rs2, make_float2(p0, p1));
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
                     }
                     tmem_st16(sadr + c * 16, pk);
+                    tmem_wait_ld();
                 }
                 tmem_wait_st();
                 l_run += rs2.x + rs2.y;
@@ -419,12 +461,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const uint32_t n = q_issued - 1 - ((q_issued - 1 - s) % kQSlots);
                     mbar_wait_limit(bar(Q_FULL + s), (n / kQSlots) & 1, 200000000ull);
                 }
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < 2; ++s) {
+                if (k_issued > static_cast<uint32_t>(s)) {
+                    const uint32_t n = ((k_issued - 1 - s) & ~1u) + s;
+                    mbar_wait_limit(bar(K_FULL + s), (n >> 1) & 1, 200000000ull);
+                }
                 if (kv_issued > static_cast<uint32_t>(s)) {
                     const uint32_t n = ((kv_issued - 1 - s) & ~1u) + s;
-                    mbar_wait_limit(bar(K_FULL + s), (n >> 1) & 1, 200000000ull);
                     mbar_wait_limit(bar(V_FULL + s), (n >> 1) & 1, 200000000ull);
                 }
+            }
         }
         if (threadIdx.x == 0) atomicOr(p.err, VLC_DEVERR_TIMEOUT);
         __syncthreads();
