@@ -36,10 +36,15 @@ WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t ma
     off = align256(off + sizeof(int32_t) * static_cast<size_t>(nseg + 1) * (is_bwd ? 2 : 1));
     L.table = off;
     off = align256(off + sizeof(float2) * static_cast<size_t>(L.table_rows) * (d / 2));
-    L.delta = off;
+    L.delta = L.qrot = L.krot = off;
     if (is_bwd) {
         L.delta = off;
         off = align256(off + sizeof(float) * static_cast<size_t>(H) * total);
+        const size_t qkbytes = static_cast<size_t>(total) * H * d * 2;
+        L.qrot = off;
+        off = align256(off + qkbytes);
+        L.krot = off;
+        off = align256(off + qkbytes);
     }
     L.total = off;
     return L;
@@ -263,6 +268,8 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
     p.items_k = items_k; p.seg_base_k = seg_base_k; p.count_k = &hdr->pad[0];
     p.table = rope ? table : nullptr;
     p.delta = reinterpret_cast<float*>(w + L.delta);
+    p.qrot = w + L.qrot;
+    p.krot = w + L.krot;
     p.nseg = nseg; p.total = total; p.H = H; p.d = d;
     p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
     p.use_rope = rope ? 1 : 0;

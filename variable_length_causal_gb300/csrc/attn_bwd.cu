@@ -10,7 +10,8 @@
 //   dQ = R(p)^T dQ',  dK = R(p)^T dK'   (RoPE is orthogonal: its inverse is R(-p)).
 //
 // Three kernels, no atomics (results are bitwise reproducible):
-//   delta_kernel   D = rowsum(dO * O) in fp32, layout [H, total].
+//   prep_kernel    D = rowsum(dO * O) in fp32, layout [H, total]; with RoPE also
+//                  q' = R(p) q and k' = R(p) k once into the workspace (bf16).
 //   dq_kernel      q-major, one unit = (q tile of 128 rows, head): for every key
 //                  tile, tcgen05 computes S = Q'K'^T and dP = dO V^T into TMEM,
 //                  128 threads form dS (bf16, shared memory), tcgen05 adds
@@ -22,7 +23,7 @@
 //                  threads form P^T and dS^T, tcgen05 accumulates dV += P^T dO
 //                  and dK += dS^T Q' in TMEM; epilogue stores dV and R(p)^T dK.
 // Both attention kernels are persistent (one CTA per SM), warp-specialised
-// like the forward (TMA warp, MMA warp, TMEM warp, 4 math warps, 4 RoPE
+// like the forward (TMA warp, MMA warp, TMEM warp, 4 math warps, 4 hand-off
 // warps), and use only bounded waits.
 #include <cuda.h>
 #include <cmath>
@@ -45,35 +46,77 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kDrainNs = 200000000ull;
 
-// ====================================================================== delta
-// One (token, head) row per D/8 threads; each thread reads 16 B of dO and O.
+// ====================================================================== prep
+// One pass over the (token, head) rows: D = rowsum(dO * O) in fp32 ([H, total]),
+// and with RoPE the rotated q' = R(p) q and k' = R(p) k (bf16, rounded once),
+// so the attention passes below read pre-rotated operands.  D/16 threads per
+// row; thread c handles the rotation pairs j = 8c .. 8c+7 (columns j and j+D/2).
 template <int D>
 __global__ void __launch_bounds__(256)
-delta_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, float* __restrict__ delta,
-             int32_t total, int32_t H, const int32_t* __restrict__ err) {
+prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const uint4* __restrict__ q,
+            const uint4* __restrict__ k, uint4* __restrict__ qrot, uint4* __restrict__ krot,
+            float* __restrict__ delta, const int32_t* __restrict__ cu, int32_t nseg,
+            const float2* __restrict__ table, int32_t total, int32_t H, int rope,
+            const int32_t* __restrict__ err) {
     if (*err != 0) return;
-    constexpr int TPR = D / 8;   // threads per row
+    constexpr int TPR = D / 16;        // threads per row
+    constexpr int HALF = D / 16;       // uint4 chunks per half row
     const int64_t rows = static_cast<int64_t>(total) * H;
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int sub = threadIdx.x % TPR;
+    const int c = threadIdx.x % TPR;
     const int64_t per_iter = nthreads / TPR;
-    // uniform trip count across the grid, so every lane joins the shuffles
-    for (int64_t first = 0; first < rows; first += per_iter) {
+    for (int64_t first = 0; first < rows; first += per_iter) {   // uniform trip count
         const int64_t row = first + gtid / TPR;
         const bool in = row < rows;
         float acc = 0.f;
         if (in) {
-            const uint4 a = __ldg(dout + row * TPR + sub);
-            const uint4 b = __ldg(o + row * TPR + sub);
-            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+            const int64_t lo = row * (2 * HALF) + c, hi = lo + HALF;
+            const uint4 g0 = __ldg(dout + lo), g1 = __ldg(dout + hi);
+            const uint4 o0 = __ldg(o + lo), o1 = __ldg(o + hi);
+            const uint32_t gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const uint32_t ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                acc += bf16_lo(av[q]) * bf16_lo(bv[q]) + bf16_hi(av[q]) * bf16_hi(bv[q]);
+            for (int e = 0; e < 8; ++e)
+                acc += bf16_lo(gv[e]) * bf16_lo(ov[e]) + bf16_hi(gv[e]) * bf16_hi(ov[e]);
+            if (rope) {
+                const int64_t tok = row / H;
+                int a = 0, b = nseg - 1;   // segment of tok (clamped, in bounds)
+                while (a < b) {
+                    const int mid = (a + b + 1) >> 1;
+                    if (__ldg(cu + mid) <= tok) a = mid; else b = mid - 1;
+                }
+                const int64_t pos = tok - __ldg(cu + a);
+                const float4* t4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 8);
+                float cs[8], sn[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 f = __ldg(t4 + e);
+                    cs[2 * e] = f.x; sn[2 * e] = f.y; cs[2 * e + 1] = f.z; sn[2 * e + 1] = f.w;
+                }
+#pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    const uint4* src = which ? k : q;
+                    uint4* dst = which ? krot : qrot;
+                    const uint4 x4 = __ldg(src + lo), y4 = __ldg(src + hi);
+                    const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
+                    uint32_t nx[4], ny[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float x0 = bf16_lo(xv[e]), x1 = bf16_hi(xv[e]);
+                        const float y0 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
+                        const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
+                        nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
+                        ny[e] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+                    }
+                    dst[lo] = make_uint4(nx[0], nx[1], nx[2], nx[3]);
+                    dst[hi] = make_uint4(ny[0], ny[1], ny[2], ny[3]);
+                }
+            }
         }
 #pragma unroll
         for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        if (in && sub == 0) {
+        if (in && c == 0) {
             const int64_t tok = row / H, h = row - tok * H;
             delta[h * total + tok] = acc;
         }
@@ -355,22 +398,18 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             mbar_arrive(bar(ACC_EMPTY));
         }
     } else if (warp >= 8) {
-        // ------------------------------------------------------------ RoPE on staged Q / K
-        const int wr = warp - 8;
-        RopeStep<D> step{};
-        if (p.use_rope) step = rope_step<D>(p.table, lane);
+        // ------------------------------------------------------------ staged Q / K hand-off
+        // (operands arrive pre-rotated from the prep pass; these warps order the hand-off)
         uint32_t unit_it = 0, kv_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
             const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
             if (!(ok = wait_warp(bar(QD_FULL), unit_it & 1, abort))) break;
-            if (p.use_rope) rope_tile<D, 128>(sbase + LY::Q0, w.tile * 128, p.table, step, wr, lane);
             fence_proxy_async_smem();
             mbar_arrive(bar(Q_READY));
             for (int j = 0; j < w.hi; ++j) {
                 const int ks = kv_it & 1;
                 if (!(ok = wait_warp(bar(K_FULL + ks), (kv_it >> 1) & 1, abort))) break;
-                if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * 128, p.table, step, wr, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(K_READY + ks));
                 ++kv_it;
@@ -694,23 +733,18 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             mbar_arrive(bar(ACC_EMPTY));
         }
     } else if (warp >= 8) {
-        // ------------------------------------------------------------ RoPE on staged K / Q
-        const int wr = warp - 8;
-        RopeStep<D> step128{};
-        RopeStep<D> step64{};
-        if (p.use_rope) step128 = step64 = rope_step<D>(p.table, lane);
+        // ------------------------------------------------------------ staged K / Q hand-off
+        // (operands arrive pre-rotated from the prep pass; these warps order the hand-off)
         uint32_t unit_it = 0, st_it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
             const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
             if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
-            if (p.use_rope) rope_tile<D, 128>(sbase + LY::K0, w.tile * 128, p.table, step128, wr, lane);
             fence_proxy_async_smem();
             mbar_arrive(bar(K_READY));
             for (int i = w.lo; i < w.hi; ++i) {
                 const int s = st_it & 1;
                 if (!(ok = wait_warp(bar(QO_FULL + s), (st_it >> 1) & 1, abort))) break;
-                if (p.use_rope) rope_tile<D, BQ>(sbase + LY::Q0 + s * LY::TILEQ, i * BQ, p.table, step64, wr, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(Q_READY + s));
                 ++st_it;
@@ -744,18 +778,22 @@ template <int D>
 static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s) {
     {
         const int64_t rows = static_cast<int64_t>(p.total) * p.H;
-        int64_t blocks = (rows * (D / 8) + 255) / 256;
+        int64_t blocks = (rows * (D / 16) + 255) / 256;
         if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
-        bwd::delta_kernel<D><<<static_cast<int>(blocks), 256, 0, s>>>(
-            static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.o), p.delta, p.total,
-            p.H, p.err);
+        bwd::prep_kernel<D><<<static_cast<int>(blocks), 256, 0, s>>>(
+            static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.o),
+            static_cast<const uint4*>(p.q), static_cast<const uint4*>(p.k), static_cast<uint4*>(p.qrot),
+            static_cast<uint4*>(p.krot), p.delta, p.cu, p.nseg, p.table, p.total, p.H, p.use_rope, p.err);
     }
+    // with RoPE the attention passes read the rotated copies
+    const void* qop = p.use_rope ? p.qrot : p.q;
+    const void* kop = p.use_rope ? p.krot : p.k;
     CUtensorMap q128, do128, k128, v128, q64, do64;
-    if (!make_tmap_thd(&q128, p.q, p.total, p.H, D, 128) ||
+    if (!make_tmap_thd(&q128, qop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&do128, p.dout, p.total, p.H, D, 128) ||
-        !make_tmap_thd(&k128, p.k, p.total, p.H, D, 128) ||
+        !make_tmap_thd(&k128, kop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&v128, p.v, p.total, p.H, D, 128) ||
-        !make_tmap_thd(&q64, p.q, p.total, p.H, D, bwd::dkdv::BQ) ||
+        !make_tmap_thd(&q64, qop, p.total, p.H, D, bwd::dkdv::BQ) ||
         !make_tmap_thd(&do64, p.dout, p.total, p.H, D, bwd::dkdv::BQ))
         return cudaErrorInvalidValue;
     {

@@ -22,7 +22,7 @@ struct WsHeader {
 
 // Byte offsets of the workspace regions for one problem size.
 struct WsLayout {
-    size_t header, items, order, seg_base, table, delta, total;
+    size_t header, items, order, seg_base, table, delta, qrot, krot, total;
     int64_t item_cap;
     int32_t table_rows;
 };
@@ -82,9 +82,11 @@ struct BwdParams {
     int32_t* err;
     const float2* table;
     float* delta;              // [H, total]: rowsum(dO * O)
+    void* qrot;                // [total, H, d] bf16: R(p) q (workspace; only with RoPE)
+    void* krot;                // [total, H, d] bf16: R(p) k
     int32_t nseg, total, H, d;
     float scale;
-    int use_rope;
+    int use_rope;              // 1: inputs are rotated in the prep pass, gradients un-rotated
 };
 
 cudaError_t launch_attn_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
