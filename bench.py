@@ -167,16 +167,22 @@ def make_inputs(w: synth.Workload, device, rank: int):
 class Step:
     """Pre-allocated buffers and one call per path step (no allocation inside the step)."""
 
-    def __init__(self, vlc, w, q, k, v, g, tokens, cu, ign):
+    def __init__(self, vlc, w, q, k, v, g, tokens, cu, ign, fwd_only=False):
         self.vlc, self.w = vlc, w
         self.q, self.k, self.v, self.g, self.tokens, self.cu, self.ign = q, k, v, g, tokens, cu, ign
         dev = q.device
         self.o = torch.empty_like(q)
         self.lse = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
-        self.dq, self.dk, self.dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        self.fwd_only = fwd_only
+        if fwd_only:
+            self.dq = self.dk = self.dv = None
+        else:
+            self.dq, self.dk, self.dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         self.ws_f = vlc.new_workspace(w.nseg, w.total, w.H, w.d, w.max_seqlen, False, dev)
-        self.ws_b = vlc.new_workspace(w.nseg, w.total, w.H, w.d, w.max_seqlen, True, dev)
+        self.ws_b = None if fwd_only else vlc.new_workspace(w.nseg, w.total, w.H, w.d, w.max_seqlen, True, dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    fwd_only = False
 
     def __call__(self, ev=None):
         vlc, w = self.vlc, self.w
@@ -189,13 +195,14 @@ class Step:
                             workspace=self.ws_f, check=False)
         if ev is not None:
             ev[2].record()
-        vlc.varlen_attn_bwd(self.g, self.q, self.k, self.v, self.o, self.lse, self.cu, w.max_seqlen,
-                            dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws_b, check=False)
+        if not self.fwd_only:
+            vlc.varlen_attn_bwd(self.g, self.q, self.k, self.v, self.o, self.lse, self.cu, w.max_seqlen,
+                                dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws_b, check=False)
         if ev is not None:
             ev[3].record()
 
     def check_errors(self):
-        for ws in (self.ws_f, self.ws_b):
+        for ws in (self.ws_f,) + (() if self.ws_b is None else (self.ws_b,)):
             st, bits = self.vlc.get_error(ws)
             if st != 0:
                 raise RuntimeError(f"device error status {st} bits 0x{bits:x}")
@@ -296,7 +303,9 @@ def gpu_arm(args, w, world, rank, local):
     vlc.load_library()
     peaks = _peaks()
     q, k, v, g, tokens, cu, ign = make_inputs(w, dev, rank)
-    step = Step(vlc, w, q, k, v, g, tokens, cu, ign)
+    if args.fwd_only:
+        g = None
+    step = Step(vlc, w, q, k, v, g, tokens, cu, ign, fwd_only=args.fwd_only)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -320,19 +329,19 @@ def gpu_arm(args, w, world, rank, local):
     t_fwd = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     t_bwd = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
-    fl_f, fl_b = synth.fwd_flops(w), synth.bwd_flops(w)
+    fl_f, fl_b = synth.fwd_flops(w), (0.0 if args.fwd_only else synth.bwd_flops(w))
     flops_all = sum_over_ranks(fl_f + fl_b, world, dev)
     real_tok = sum_over_ranks(float(w.real_lengths.sum()), world, dev)
     value = flops_all / (ms * 1e-3) / 1e12
 
     # ---- end to end through the public API, pinned host buffers in and out
-    e2e = e2e_measure(vlc, w, step, args.steps, world, dev)
+    e2e = None if args.no_e2e else e2e_measure(vlc, w, step, args.steps, world, dev)
 
     if rank != 0:
         return
     tb = w.total * w.H
     fwd_tflops = fl_f / (t_fwd * 1e-3) / 1e12
-    bwd_tflops = fl_b / (t_bwd * 1e-3) / 1e12
+    bwd_tflops = fl_b / (t_bwd * 1e-3) / 1e12 if t_bwd > 0 and fl_b > 0 else 0.0
     pos_bytes = 20.0 * w.total
     kernels = {
         "positions_labels": {"ms": t_pos, "GB/s": pos_bytes / (t_pos * 1e-3) / 1e9},
@@ -359,7 +368,7 @@ def gpu_arm(args, w, world, rank, local):
         "tokens_per_s": real_tok / (ms * 1e-3),
         "fwd_eff_tflops": fwd_tflops, "bwd_eff_tflops": bwd_tflops,
         "kernels": kernels, "roofline": roofline, "roofline_fwd": roofline_fwd,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": (4 if args.fwd_only else LAUNCHES_PER_STEP) * args.steps,
         "clocks": clk.summary(),
         "e2e": e2e,
     }
@@ -371,12 +380,12 @@ def gpu_arm(args, w, world, rank, local):
 def e2e_measure(vlc, w, step, steps, world, dev):
     """Same metric through the public API with pinned host buffers: every step copies this
     step's inputs host->device and reads back every output device->host."""
-    host_in = [t.cpu().pin_memory() for t in (step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign)]
-    outs = (step.o, step.lse, step.dq, step.dk, step.dv)
+    dev_in = [t for t in (step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign) if t is not None]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    outs = tuple(t for t in (step.o, step.lse, step.dq, step.dk, step.dv) if t is not None)
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
     host_pos = torch.empty(w.total, dtype=torch.int32).pin_memory()
     host_lab = torch.empty(w.total, dtype=torch.int64).pin_memory()
-    dev_in = [step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out) + w.total * 12
 
@@ -399,7 +408,7 @@ def e2e_measure(vlc, w, step, steps, world, dev):
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     dt = max_over_ranks(dt, world, dev)
-    flops = sum_over_ranks(synth.fwd_flops(w) + synth.bwd_flops(w), world, dev)
+    flops = sum_over_ranks(synth.fwd_flops(w) + (0.0 if step.fwd_only else synth.bwd_flops(w)), world, dev)
     return {"value": flops / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3}
 
@@ -440,6 +449,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="step = positions/labels + forward only (for profiling the forward kernel)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "vlc" else args.warmup
     world, rank, local = dist_setup()
