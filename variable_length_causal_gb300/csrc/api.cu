@@ -214,6 +214,7 @@ int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
     FwdParams p{};
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu = cu;
     p.items = items; p.seg_base = seg_base; p.count = &hdr->count; p.err = &hdr->err;
+    p.next = &hdr->next[0];
     p.table = rope ? table : nullptr;
     p.nseg = nseg; p.total = total; p.H = H; p.d = d;
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
@@ -254,7 +255,7 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
                         L.item_cap, order, seg_base_q, &hdr->count, &hdr->err, s) != cudaSuccess)
         return VLC_ERR_CUDA;
     if (launch_worklist(cu, nseg, total, max_seqlen, kBwdBM, kFwdBN, VLC_WORKLIST_BWD, items_k,
-                        L.item_cap, order + nseg, seg_base_k, &hdr->pad[0], &hdr->err, s) !=
+                        L.item_cap, order + nseg, seg_base_k, &hdr->count2, &hdr->err, s) !=
         cudaSuccess)
         return VLC_ERR_CUDA;
     const bool rope = rope_theta != 0.f;
@@ -265,7 +266,9 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
     p.dout = dout; p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
     p.dq = dq; p.dk = dk; p.dv = dv; p.cu = cu;
     p.items = items_q; p.seg_base = seg_base_q; p.count = &hdr->count; p.err = &hdr->err;
-    p.items_k = items_k; p.seg_base_k = seg_base_k; p.count_k = &hdr->pad[0];
+    p.items_k = items_k; p.seg_base_k = seg_base_k; p.count_k = &hdr->count2;
+    p.next_q = &hdr->next[1];
+    p.next_k = &hdr->next[2];
     p.table = rope ? table : nullptr;
     p.delta = reinterpret_cast<float*>(w + L.delta);
     p.qrot = w + L.qrot;

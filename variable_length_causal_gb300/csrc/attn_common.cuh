@@ -57,11 +57,57 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// ---------------------------------------------------------------- dynamic unit ring
+// The producer thread claims work units from a global counter (longest first,
+// so CTAs that finish early take the next unit and the units in flight stay a
+// contiguous window of the work list) and publishes each index in a ring of
+// kRing shared-memory slots; every role consumes the same sequence in order.
+// A unit index of -1 ends the sequence.
+constexpr int kRing = 8;
+
+struct Ring {
+    volatile int* slot;     // kRing ints in shared memory
+    uint32_t full0, empty0; // barrier addresses of slot 0 (8-byte stride)
+};
+
+__device__ __forceinline__ bool ring_put(const Ring& rg, int n, int* counter, int nunits,
+                                         volatile int* abort, int& u_out) {
+    const int s = n % kRing;
+    if (!mbar_wait(rg.empty0 + 8u * s, ((n / kRing) & 1) ^ 1, abort)) return false;
+    int u = atomicAdd(counter, 1);
+    if (u >= nunits) u = -1;
+    rg.slot[s] = u;
+    mbar_arrive(rg.full0 + 8u * s);   // release: waiters see the index
+    u_out = u;
+    return true;
+}
+
+// One consumer thread (the MMA issuer).
+__device__ __forceinline__ bool ring_get(const Ring& rg, int n, volatile int* abort, int& u_out) {
+    const int s = n % kRing;
+    if (!mbar_wait(rg.full0 + 8u * s, (n / kRing) & 1, abort)) return false;
+    u_out = rg.slot[s];
+    mbar_arrive(rg.empty0 + 8u * s);
+    return true;
+}
+
+// A whole consumer warp; lane 0 releases the slot once every lane has read it.
+__device__ __forceinline__ bool ring_get_warp(const Ring& rg, int n, volatile int* abort, int& u_out);
+
 // 16-byte chunk `ci` (0..7) of row `r` inside a block of rows x 128 bytes with
 // the 128-byte swizzle used by both TMA and the MMA descriptors.
 __device__ __forceinline__ uint32_t sw128(uint32_t block_base, int r, int ci) {
     return block_base + static_cast<uint32_t>(r) * 128u +
            static_cast<uint32_t>(((ci ^ (r & 7)) & 7) << 4);
+}
+
+__device__ __forceinline__ bool ring_get_warp(const Ring& rg, int n, volatile int* abort, int& u_out) {
+    const int s = n % kRing;
+    if (!wait_warp(rg.full0 + 8u * s, (n / kRing) & 1, abort)) return false;
+    u_out = rg.slot[s];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(rg.empty0 + 8u * s);
+    return true;
 }
 
 // Named barrier among `nthreads` threads (ids 1..15; 0 is __syncthreads).

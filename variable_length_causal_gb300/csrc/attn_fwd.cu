@@ -10,7 +10,9 @@
 // Design: one persistent CTA per SM, 512 threads, warp-specialised.  A work
 // unit is (segment, head, block of 256 query rows) = two 128-row q tiles that
 // share every K/V tile; the work list holds only in-segment, at-or-below-
-// diagonal key tiles, and a q tile stops at its own diagonal key tile.
+// diagonal key tiles, and a q tile stops at its own diagonal key tile.  Units
+// are claimed dynamically (longest first) from a global counter and handed to
+// every role through a shared-memory ring.
 //   warp 0       TMA producer: q tiles into a 3-slot ring, K/V tiles into 2
 //                stages, 128-byte swizzle.
 //   warp 1       MMA issuer (one thread), tcgen05.mma kind::f16, fp32 in TMEM:
@@ -54,7 +56,7 @@ enum : int {
     Q_FULL = 0, Q_READY = 3, Q_EMPTY = 6,
     K_FULL = 9, K_READY = 11, K_EMPTY = 13, V_FULL = 15, V_EMPTY = 17,
     S_FULL = 19, P_FULL = 21, O_FULL = 23, O_EMPTY = 25,
-    DRAIN = 27, NUM_BARS = 28
+    DRAIN = 27, UNIT_FULL = 28, UNIT_EMPTY = 28 + kRing, NUM_BARS = 28 + 2 * kRing
 };
 
 template <int D>
@@ -66,8 +68,8 @@ struct Layout {
     static constexpr uint32_t K0 = kQSlots * TILE;     // 2 stages
     static constexpr uint32_t V0 = K0 + 2 * TILE;      // 2 stages
     static constexpr uint32_t BAR0 = V0 + 2 * TILE;
-    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;
-    static constexpr uint32_t BYTES = MISC + 16;
+    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;   // tmem slot, abort flag, unit ring
+    static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }   // P_t shares these columns
     __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + 128u * t; }
@@ -102,8 +104,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     auto bar = [&](int i) -> uint32_t { return sbase + LY::BAR0 + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
+    const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    constexpr int kRingConsumers = 1 + 8 + 4;   // MMA thread, 8 softmax warps, 4 RoPE warps
 
     __shared__ int s_skip, s_nunits;
     if (threadIdx.x == 0) {   // one read, so every thread takes the same branch
@@ -132,6 +136,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bar(O_EMPTY + i), 128);
         }
         mbar_init(bar(DRAIN), 1);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(bar(UNIT_FULL + i), 1);
+            mbar_init(bar(UNIT_EMPTY + i), kRingConsumers);
+        }
         *abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -152,9 +160,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            const uint64_t pol_stream = make_l2_policy_evict_first();   // q: read once
+            const uint64_t pol_keep = make_l2_policy_evict_last();      // K/V: read by many units
             uint32_t qm = 0, kvn = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+            for (int n = 0; ok; ++n) {
+                int u;
+                if (!(ok = ring_put(rg, n, p.next, nunits, abort, u)) || u < 0) break;
                 const FUnit f = decode_funit(p, u);
                 for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
                     const int slot = qm % kQSlots;
@@ -163,8 +175,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int row = f.w.row0 + f.w.tile * QB + t * BQ;
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
-                        tma_load_3d(sbase + LY::Q0 + slot * LY::TILE + kb * LY::BLK, &tmQ, kb * 64,
-                                    f.w.h, row, bar(Q_FULL + slot));
+                        tma_load_3d_hint(sbase + LY::Q0 + slot * LY::TILE + kb * LY::BLK, &tmQ, kb * 64,
+                                         f.w.h, row, bar(Q_FULL + slot), pol_stream);
                     q_issued = ++qm;
                 }
                 // K tile j is loaded one step ahead of V tile j-1, so the RoPE warps
@@ -177,8 +189,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
 #pragma unroll
                         for (int kb = 0; kb < LY::KB; ++kb)
-                            tma_load_3d(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
-                                        f.w.h, f.w.row0 + j * BN, bar(K_FULL + ks));
+                            tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
+                                             f.w.h, f.w.row0 + j * BN, bar(K_FULL + ks), pol_keep);
                         k_issued = n + 1;
                     }
                     if (j >= 1) {
@@ -188,8 +200,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         mbar_expect_tx(bar(V_FULL + vs), LY::TILE);
 #pragma unroll
                         for (int kb = 0; kb < LY::KB; ++kb)
-                            tma_load_3d(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
-                                        f.w.h, f.w.row0 + (j - 1) * BN, bar(V_FULL + vs));
+                            tma_load_3d_hint(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
+                                             f.w.h, f.w.row0 + (j - 1) * BN, bar(V_FULL + vs), pol_keep);
                         kv_issued = n + 1;
                     }
                 }
@@ -215,7 +227,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 mma_commit(bar(S_FULL + t));
             };
-            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+            for (int un = 0; ok; ++un) {
+                int u;
+                if (!(ok = ring_get(rg, un, abort, u)) || u < 0) break;
                 const FUnit f = decode_funit(p, u);
                 const int n[2] = {f.n0, f.n1};
                 const int slot[2] = {static_cast<int>(qm % kQSlots), static_cast<int>((qm + 1) % kQSlots)};
@@ -287,7 +301,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float sl2 = p.scale_log2;
         uint32_t cnt_s = 0, cnt_u = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        for (int un = 0; ok; ++un) {
+            int u;
+            if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
             const FUnit f = decode_funit(p, u);
             const int nt = t == 0 ? f.n0 : f.n1;
             if (nt == 0) continue;
@@ -428,7 +444,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (p.use_rope) step = rope_step<D>(p.table, lane);
         uint32_t qm = 0, kvn = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        for (int un = 0; ok; ++un) {
+            int u;
+            if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
             const FUnit f = decode_funit(p, u);
             for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
                 const int slot = qm % kQSlots;

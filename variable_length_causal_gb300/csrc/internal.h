@@ -17,7 +17,9 @@ constexpr int kTablePad = 128;  // RoPE table rows are padded to a multiple of t
 struct WsHeader {
     int32_t err;          // VLC_DEVERR_* bits
     int32_t count;        // work items written by the work-list kernel
-    int32_t pad[62];
+    int32_t count2;       // items of the second work list (backward key-major pass)
+    int32_t next[3];      // dynamic unit counters of the attention kernels (zeroed per call)
+    int32_t pad[58];
 };
 
 // Byte offsets of the workspace regions for one problem size.
@@ -53,6 +55,7 @@ struct FwdParams {
     const int4* items;
     const int32_t* seg_base;   // [nseg+1] item offsets of the sorted segments
     const int32_t* count;
+    int32_t* next;             // unit counter (zeroed before the launch)
     int32_t* err;
     const float2* table;       // RoPE cos/sin [rows][d/2], null if no RoPE
     int32_t nseg, total, H, d;
@@ -79,6 +82,8 @@ struct BwdParams {
     const int4* items_k;       // key-tile items (dK/dV pass)
     const int32_t* seg_base_k;
     const int32_t* count_k;
+    int32_t* next_q;           // unit counters of the dQ and dK/dV passes (zeroed per call)
+    int32_t* next_k;
     int32_t* err;
     const float2* table;
     float* delta;              // [H, total]: rowsum(dO * O)
