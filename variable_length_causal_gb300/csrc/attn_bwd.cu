@@ -170,7 +170,7 @@ enum : int {
     QD_FULL = 0, Q_READY = 1, QD_EMPTY = 2,
     K_FULL = 3, K_READY = 5, V_FULL = 7, KV_EMPTY = 9,
     SD_FULL = 11, SD_EMPTY = 12, DS_FULL = 13, DQ_DONE = 14, ACC_EMPTY = 15, DRAIN = 16,
-    NUM_BARS = 17
+    UNIT_FULL = 17, UNIT_EMPTY = 17 + kRing, NUM_BARS = 17 + 2 * kRing
 };
 
 template <int D>
@@ -184,8 +184,8 @@ struct Layout {
     static constexpr uint32_t V0 = 4 * TILE;
     static constexpr uint32_t DS0 = 6 * TILE;
     static constexpr uint32_t BAR0 = DS0 + 128u * 128u * 2u;
-    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;
-    static constexpr uint32_t BYTES = MISC + 16;
+    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;   // tmem slot, abort flag, unit ring
+    static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256;
 };
@@ -202,6 +202,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     auto bar = [&](int i) -> uint32_t { return sbase + LY::BAR0 + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
+    const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
+    constexpr int kRingConsumers = 1 + 4 + 4;   // MMA thread, 4 math warps, 4 hand-off warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     __shared__ int s_skip, s_nunits;
@@ -229,6 +231,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         mbar_init(bar(DQ_DONE), 1);
         mbar_init(bar(ACC_EMPTY), 128);
         mbar_init(bar(DRAIN), 1);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(bar(UNIT_FULL + i), 1);
+            mbar_init(bar(UNIT_EMPTY + i), kRingConsumers);
+        }
         *abort = 0;
         fence_mbar_init();
     }
@@ -244,17 +250,21 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
 
     if (warp == 0) {
         if (lane == 0) {   // ---------------------------------------- TMA producer
+            const uint64_t pol_stream = make_l2_policy_evict_first();
+            const uint64_t pol_keep = make_l2_policy_evict_last();
             uint32_t unit_it = 0, kv_it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+            for (int n = 0; ok; ++n, ++unit_it) {
+                int u;
+                if (!(ok = ring_put(rg, n, p.next_q, nunits, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
                 if (!(ok = mbar_wait(bar(QD_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(QD_FULL), 2 * LY::TILE);
                 const int qrow = w.row0 + w.tile * 128;
 #pragma unroll
                 for (int kb = 0; kb < LY::KB; ++kb) {
-                    tma_load_3d(sbase + LY::Q0 + kb * LY::BLK, &tmQ, kb * 64, w.h, qrow, bar(QD_FULL));
-                    tma_load_3d(sbase + LY::DO0 + kb * LY::BLK, &tmDO, kb * 64, w.h, qrow, bar(QD_FULL));
+                    tma_load_3d_hint(sbase + LY::Q0 + kb * LY::BLK, &tmQ, kb * 64, w.h, qrow, bar(QD_FULL), pol_stream);
+                    tma_load_3d_hint(sbase + LY::DO0 + kb * LY::BLK, &tmDO, kb * 64, w.h, qrow, bar(QD_FULL), pol_stream);
                 }
                 q_issued = unit_it + 1;
                 for (int j = 0; j < w.hi; ++j) {
@@ -265,10 +275,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                     mbar_expect_tx(bar(V_FULL + ks), LY::TILE);
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb) {
-                        tma_load_3d(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64, w.h,
-                                    row, bar(K_FULL + ks));
-                        tma_load_3d(sbase + LY::V0 + ks * LY::TILE + kb * LY::BLK, &tmV, kb * 64, w.h,
-                                    row, bar(V_FULL + ks));
+                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64, w.h,
+                                         row, bar(K_FULL + ks), pol_keep);
+                        tma_load_3d_hint(sbase + LY::V0 + ks * LY::TILE + kb * LY::BLK, &tmV, kb * 64, w.h,
+                                         row, bar(V_FULL + ks), pol_keep);
                     }
                     kv_issued = ++kv_it;
                 }
@@ -299,7 +309,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 ++ds_it;
                 return true;
             };
-            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+            for (int n = 0; ok; ++n, ++unit_it) {
+                int u;
+                if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
                 if (!(ok = mbar_wait(bar(QD_FULL), unit_it & 1, abort))) break;
                 if (!(ok = mbar_wait(bar(Q_READY), unit_it & 1, abort))) break;
@@ -345,7 +357,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         const float scale_log2 = p.scale * kLog2e;
         uint32_t sd_it = 0, ds_it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        for (int n = 0; ok; ++n) {
+            int u;
+            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
             const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
             const int qpos = w.tile * 128 + r;
             const bool valid = qpos < w.L;
@@ -402,7 +416,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         // (operands arrive pre-rotated from the prep pass; these warps order the hand-off)
         uint32_t unit_it = 0, kv_it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+        for (int n = 0; ok; ++n, ++unit_it) {
+            int u;
+            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
             const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
             if (!(ok = wait_warp(bar(QD_FULL), unit_it & 1, abort))) break;
             fence_proxy_async_smem();
@@ -447,7 +463,7 @@ enum : int {
     QO_FULL = 3, Q_READY = 5, QO_EMPTY = 7,
     ST_FULL = 9, ST_EMPTY = 11, PDS_FULL = 13, PDS_EMPTY = 15,
     ACC_FULL = 17, ACC_EMPTY = 18, DRAIN = 19, LSED_FULL = 20,
-    NUM_BARS = 22
+    UNIT_FULL = 22, UNIT_EMPTY = 22 + kRing, NUM_BARS = 22 + 2 * kRing
 };
 
 constexpr int BQ = kBwdBM;    // q rows per step
@@ -469,8 +485,8 @@ struct Layout {
     static constexpr uint32_t DS0 = P0 + 2 * PT;              // 2 buffers
     static constexpr uint32_t LSED = DS0 + 2 * PT;            // 2 x (64 lse2 + 64 delta) floats
     static constexpr uint32_t BAR0 = LSED + 2 * 128 * 4;
-    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;
-    static constexpr uint32_t BYTES = MISC + 16;
+    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;   // tmem slot, abort flag, unit ring
+    static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
 };
@@ -487,6 +503,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     auto bar = [&](int i) -> uint32_t { return sbase + LY::BAR0 + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
+    const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
+    constexpr int kRingConsumers = 1 + 4 + 4;   // MMA thread, 4 math warps, 4 hand-off warps
     float* lsed = reinterpret_cast<float*>(sgen + LY::LSED);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -517,6 +535,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         mbar_init(bar(DRAIN), 1);
         mbar_init(bar(LSED_FULL), 128);
         mbar_init(bar(LSED_FULL + 1), 128);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(bar(UNIT_FULL + i), 1);
+            mbar_init(bar(UNIT_EMPTY + i), kRingConsumers);
+        }
         *abort = 0;
         fence_mbar_init();
     }
@@ -532,17 +554,21 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 
     if (warp == 0) {
         if (lane == 0) {   // ---------------------------------------- TMA producer
+            const uint64_t pol_stream = make_l2_policy_evict_first();
+            const uint64_t pol_keep = make_l2_policy_evict_last();
             uint32_t unit_it = 0, st_it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+            for (int n = 0; ok; ++n, ++unit_it) {
+                int u;
+                if (!(ok = ring_put(rg, n, p.next_k, nunits, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
                 if (!(ok = mbar_wait(bar(KV_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(KV_FULL), 2 * LY::TILEK);
                 const int krow = w.row0 + w.tile * 128;
 #pragma unroll
                 for (int kb = 0; kb < LY::KB; ++kb) {
-                    tma_load_3d(sbase + LY::K0 + kb * LY::BLKK, &tmK, kb * 64, w.h, krow, bar(KV_FULL));
-                    tma_load_3d(sbase + LY::V0 + kb * LY::BLKK, &tmV, kb * 64, w.h, krow, bar(KV_FULL));
+                    tma_load_3d_hint(sbase + LY::K0 + kb * LY::BLKK, &tmK, kb * 64, w.h, krow, bar(KV_FULL), pol_stream);
+                    tma_load_3d_hint(sbase + LY::V0 + kb * LY::BLKK, &tmV, kb * 64, w.h, krow, bar(KV_FULL), pol_stream);
                 }
                 kv_issued = unit_it + 1;
                 for (int i = w.lo; i < w.hi; ++i) {
@@ -552,10 +578,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     const int qrow = w.row0 + i * BQ;
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb) {
-                        tma_load_3d(sbase + LY::Q0 + s * LY::TILEQ + kb * LY::BLKQ, &tmQ, kb * 64, w.h,
-                                    qrow, bar(QO_FULL + s));
-                        tma_load_3d(sbase + LY::DO0 + s * LY::TILEQ + kb * LY::BLKQ, &tmDO, kb * 64, w.h,
-                                    qrow, bar(QO_FULL + s));
+                        tma_load_3d_hint(sbase + LY::Q0 + s * LY::TILEQ + kb * LY::BLKQ, &tmQ, kb * 64, w.h,
+                                         qrow, bar(QO_FULL + s), pol_keep);
+                        tma_load_3d_hint(sbase + LY::DO0 + s * LY::TILEQ + kb * LY::BLKQ, &tmDO, kb * 64, w.h,
+                                         qrow, bar(QO_FULL + s), pol_keep);
                     }
                     q_issued = ++st_it;
                 }
@@ -592,7 +618,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 ++acc_it;
                 return true;
             };
-            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+            for (int n = 0; ok; ++n, ++unit_it) {
+                int u;
+                if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
                 if (!(ok = mbar_wait(bar(KV_FULL), unit_it & 1, abort))) break;
                 if (!(ok = mbar_wait(bar(K_READY), unit_it & 1, abort))) break;
@@ -641,7 +669,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const float scale_log2 = p.scale * kLog2e;
         uint32_t unit_it = 0, st_it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+        for (int n = 0; ok; ++n, ++unit_it) {
+            int u;
+            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
             const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
             const int kvpos = w.tile * 128 + r;
             for (int i = w.lo; i < w.hi; ++i) {
@@ -737,7 +767,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         // (operands arrive pre-rotated from the prep pass; these warps order the hand-off)
         uint32_t unit_it = 0, st_it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++unit_it) {
+        for (int n = 0; ok; ++n, ++unit_it) {
+            int u;
+            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
             const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
             if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
             fence_proxy_async_smem();
