@@ -414,27 +414,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float inv_l = 1.f / l_run;
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                             ((valid ? tok : 0) * p.H + f.w.h) * static_cast<int64_t>(D) * 2;
+            // read O (two 32-column chunks at a time); the columns are released to the
+            // next unit as soon as the last chunk has landed, before packing and storing
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(oadr + c * 32, rr);
+            for (int c = 0; c < D / 32; c += 2) {
+                uint32_t ra[32], rb[32];
+                tmem_ld32(oadr + c * 32, ra);
+                tmem_ld32(oadr + c * 32 + 32, rb);
                 tmem_wait_ld();
-                uint32_t pk[16];
+                if (c + 2 >= D / 32) {
+                    tc_fence_before();
+                    mbar_arrive(bar(O_EMPTY + t));
+                }
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * inv_l,
-                                        __uint_as_float(rr[2 * e + 1]) * inv_l);
+                for (int e = 0; e < 16; ++e) {
+                    pk[e] = pack_bf16x2(__uint_as_float(ra[2 * e]) * inv_l, __uint_as_float(ra[2 * e + 1]) * inv_l);
+                    pk[16 + e] = pack_bf16x2(__uint_as_float(rb[2 * e]) * inv_l, __uint_as_float(rb[2 * e + 1]) * inv_l);
+                }
                 if (valid) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
+                    for (int e = 0; e < 8; ++e)
                         dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
             }
             if (valid)
                 p.lse[static_cast<int64_t>(f.w.h) * p.total + tok] = (m_run + __log2f(l_run)) * kLn2;
-            tc_fence_before();
-            mbar_arrive(bar(O_EMPTY + t));
             ++cnt_u;
         }
     } else if (warp >= 12) {
