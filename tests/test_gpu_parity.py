@@ -335,3 +335,22 @@ def test_bwd_full_size_sampled(vlc):
         _cmp_grads(got, want)
     for t in (dq, dk, dv):
         assert torch.isfinite(t.float()).all()
+
+
+def test_fwd_peaky_scores_rescale_paths(vlc):
+    """Rows whose max score jumps by far more than 2^8 within a tile and across tiles
+    (large-magnitude q/k) exercise the in-row P rescale and the O rescale."""
+    w = synth.custom_workload([300, 129, 520], 2, 128)
+    q, k, v = synth.make_tensors(w, seed=44)
+    g = torch.Generator().manual_seed(45)
+    boost = (torch.rand(w.total, 1, 1, generator=g) < 0.05).float() * 12.0 + 1.0
+    k = (k.float() * boost).bfloat16()
+    q = (q.float() * 3.0).bfloat16()
+    o, lse = vlc.varlen_attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), _cu(w), w.max_seqlen)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.cu)
+    eo = np.abs(o.float().cpu().numpy() - o_ref)
+    el = np.abs(lse.cpu().numpy() - lse_ref)
+    assert np.isfinite(eo).all()
+    assert eo.max() <= O_MAX and eo.mean() <= O_MEAN
+    # LSE magnitudes reach ~1e2 here: compare relative to the fp32 scale of the value
+    assert (el / np.maximum(1.0, np.abs(lse_ref))).max() <= LSE_MAX

@@ -330,10 +330,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                             mx = fmaxf(mx, (c * 32 + e <= lim) ? __uint_as_float(ra[e]) : -INFINITY);
                             mx = fmaxf(mx, (c * 32 + 32 + e <= lim) ? __uint_as_float(rb[e]) : -INFINITY);
                         }
-                    } else {
+                    } else {   // four independent 3-input max chains
+                        float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            mx = fmaxf(mx, fmaxf(__uint_as_float(ra[e]), __uint_as_float(rb[e])));
+                        for (int e = 0; e < 32; e += 2) {
+                            m4[(e >> 1) & 1] = fmax3(m4[(e >> 1) & 1], __uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
+                            m4[2 + ((e >> 1) & 1)] = fmax3(m4[2 + ((e >> 1) & 1)], __uint_as_float(rb[e]),
+                                                           __uint_as_float(rb[e + 1]));
+                        }
+                        mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
                     }
                 }
                 const float mt = mx * sl2;
