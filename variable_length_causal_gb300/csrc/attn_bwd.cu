@@ -20,8 +20,10 @@
 //   dkdv_kernel    key-major, one unit = (key tile of 128 rows, head): for every
 //                  q step of 64 rows from the diagonal to the segment end,
 //                  S^T = K'Q'^T and dP^T = V dO^T into TMEM (double buffered),
-//                  threads form P^T and dS^T, tcgen05 accumulates dV += P^T dO
-//                  and dK += dS^T Q' in TMEM; epilogue stores dV and R(p)^T dK.
+//                  two warpgroups (32 q columns each) form P^T and dS^T and write
+//                  them back packed into TMEM, tcgen05 accumulates dV += P^T dO
+//                  and dK += dS^T Q' (tensor-memory A operands); a stager warp
+//                  prefetches LSE/delta; epilogue stores dV and R(p)^T dK.
 // Both attention kernels are persistent (one CTA per SM), warp-specialised
 // like the forward (TMA warp, MMA warp, TMEM warp, 4 math warps, 4 hand-off
 // warps), and use only bounded waits.
@@ -458,16 +460,19 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
 // ====================================================================== dK/dV pass
 namespace dkdv {
 
-enum : int {
-    KV_FULL = 0, K_READY = 1, KV_EMPTY = 2,
-    QO_FULL = 3, Q_READY = 5, QO_EMPTY = 7,
-    ST_FULL = 9, ST_EMPTY = 11, PDS_FULL = 13, PDS_EMPTY = 15,
-    ACC_FULL = 17, ACC_EMPTY = 18, DRAIN = 19, LSED_FULL = 20,
-    UNIT_FULL = 22, UNIT_EMPTY = 22 + kRing, NUM_BARS = 22 + 2 * kRing
-};
-
 constexpr int BQ = kBwdBM;    // q rows per step
-static_assert(BQ == 64, "the P^T / dS^T tiles are one 128-byte swizzle block wide");
+static_assert(BQ == 64, "a step's S^T / dP^T take 64 TMEM columns each");
+constexpr int kQStages = 3;
+constexpr int kLsedSlots = 3;
+
+enum : int {
+    KV_FULL = 0, KV_EMPTY = 1,
+    QO_FULL = 2, QO_EMPTY = 2 + kQStages,
+    ST_FULL = 2 + 2 * kQStages, PDS_FULL = ST_FULL + 2,
+    LSED_FULL = PDS_FULL + 2, LSED_EMPTY = LSED_FULL + kLsedSlots,
+    ACC_FULL = LSED_EMPTY + kLsedSlots, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2,
+    UNIT_FULL = ACC_FULL + 3, UNIT_EMPTY = UNIT_FULL + kRing, NUM_BARS = UNIT_EMPTY + kRing
+};
 
 template <int D>
 struct Layout {
@@ -476,20 +481,23 @@ struct Layout {
     static constexpr uint32_t TILEK = 128u * D * 2u;
     static constexpr uint32_t BLKQ = BQ * 128u;          // q-side block: 64 rows x 128 B
     static constexpr uint32_t TILEQ = BQ * D * 2u;
-    static constexpr uint32_t PT = 128u * BQ * 2u;       // one P^T or dS^T tile (16 KB)
     static constexpr uint32_t K0 = 0;
     static constexpr uint32_t V0 = TILEK;
-    static constexpr uint32_t Q0 = 2 * TILEK;                 // 2 stages
-    static constexpr uint32_t DO0 = Q0 + 2 * TILEQ;           // 2 stages
-    static constexpr uint32_t P0 = DO0 + 2 * TILEQ;           // 2 buffers
-    static constexpr uint32_t DS0 = P0 + 2 * PT;              // 2 buffers
-    static constexpr uint32_t LSED = DS0 + 2 * PT;            // 2 x (64 lse2 + 64 delta) floats
-    static constexpr uint32_t BAR0 = LSED + 2 * 128 * 4;
-    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;   // tmem slot, abort flag, unit ring
+    static constexpr uint32_t Q0 = 2 * TILEK;                  // kQStages stages
+    static constexpr uint32_t DO0 = Q0 + kQStages * TILEQ;     // kQStages stages
+    static constexpr uint32_t LSED = DO0 + kQStages * TILEQ;   // kLsedSlots x (64 lse2 + 64 delta)
+    static constexpr uint32_t BAR0 = LSED + kLsedSlots * 128 * 4;
+    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;      // tmem slot, abort flag, unit ring
     static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
+    // TMEM: step buffer b at columns 128b: S^T (64 fp32 columns) then dP^T (64); the
+    // packed bf16 P^T / dS^T of a step overwrite the consumed S^T / dP^T columns.
     static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
 };
+
+// TMEM column of the packed P^T / dS^T K-slice k (16 q columns): math warpgroup g
+// owns q columns [32g, 32g + 32) and packs them into columns [32g, 32g + 16).
+__device__ __forceinline__ uint32_t packed_col(int k) { return (k >> 1) * 32 + (k & 1) * 8; }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -504,7 +512,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
-    constexpr int kRingConsumers = 1 + 4 + 4;   // MMA thread, 4 math warps, 4 hand-off warps
+    constexpr int kRingConsumers = 1 + 1 + 8;   // MMA thread, LSE/delta stager warp, 8 math warps
     float* lsed = reinterpret_cast<float*>(sgen + LY::LSED);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -519,22 +527,22 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 
     if (threadIdx.x == 0) {
         mbar_init(bar(KV_FULL), 1);
-        mbar_init(bar(K_READY), 128);
         mbar_init(bar(KV_EMPTY), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQStages; ++i) {
             mbar_init(bar(QO_FULL + i), 1);
-            mbar_init(bar(Q_READY + i), 128);
             mbar_init(bar(QO_EMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(ST_FULL + i), 1);
-            mbar_init(bar(ST_EMPTY + i), 128);
-            mbar_init(bar(PDS_FULL + i), 128);
-            mbar_init(bar(PDS_EMPTY + i), 1);
+            mbar_init(bar(PDS_FULL + i), 256);
+        }
+        for (int i = 0; i < kLsedSlots; ++i) {
+            mbar_init(bar(LSED_FULL + i), 1);
+            mbar_init(bar(LSED_EMPTY + i), 8);
         }
         mbar_init(bar(ACC_FULL), 1);
-        mbar_init(bar(ACC_EMPTY), 128);
+        mbar_init(bar(ACC_EMPTY), 256);
         mbar_init(bar(DRAIN), 1);
-        mbar_init(bar(LSED_FULL), 128);
-        mbar_init(bar(LSED_FULL + 1), 128);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(bar(UNIT_FULL + i), 1);
             mbar_init(bar(UNIT_EMPTY + i), kRingConsumers);
@@ -554,9 +562,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 
     if (warp == 0) {
         if (lane == 0) {   // ---------------------------------------- TMA producer
-            const uint64_t pol_stream = make_l2_policy_evict_first();
-            const uint64_t pol_keep = make_l2_policy_evict_last();
-            uint32_t unit_it = 0, st_it = 0;
+            const uint64_t pol_stream = make_l2_policy_evict_first();   // K/V: once per unit
+            const uint64_t pol_keep = make_l2_policy_evict_last();      // q/dO: re-read by other units
+            uint32_t unit_it = 0, qo = 0;
             bool ok = true;
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
@@ -571,9 +579,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     tma_load_3d_hint(sbase + LY::V0 + kb * LY::BLKK, &tmV, kb * 64, w.h, krow, bar(KV_FULL), pol_stream);
                 }
                 kv_issued = unit_it + 1;
-                for (int i = w.lo; i < w.hi; ++i) {
-                    const int s = st_it & 1;
-                    if (!(ok = mbar_wait(bar(QO_EMPTY + s), ((st_it >> 1) & 1) ^ 1, abort))) break;
+                for (int i = w.lo; i < w.hi && ok; ++i, ++qo) {
+                    const int s = qo % kQStages;
+                    if (!(ok = mbar_wait(bar(QO_EMPTY + s), ((qo / kQStages) & 1) ^ 1, abort))) break;
                     mbar_expect_tx(bar(QO_FULL + s), 2 * LY::TILEQ);
                     const int qrow = w.row0 + i * BQ;
 #pragma unroll
@@ -583,7 +591,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                         tma_load_3d_hint(sbase + LY::DO0 + s * LY::TILEQ + kb * LY::BLKQ, &tmDO, kb * 64, w.h,
                                          qrow, bar(QO_FULL + s), pol_keep);
                     }
-                    q_issued = ++st_it;
+                    q_issued = qo + 1;
                 }
             }
         }
@@ -592,30 +600,27 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         if (lane == 0) {   // ---------------------------------------- MMA issuer
             constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, BQ, false);
             constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, true);
-            uint32_t unit_it = 0, st_it = 0, acc_it = 0;
+            uint32_t unit_it = 0, st = 0;
             bool ok = true;
-            auto issue_acc = [&](bool first) -> bool {
-                const int b = acc_it & 1;   // P^T/dS^T buffer == Q/dO stage of that step
+            // dV += P^T dO and dK += dS^T Q' for step sp (A operands packed in TMEM)
+            auto issue_acc = [&](uint32_t sp, bool first) -> bool {
+                const int b = sp & 1, s = sp % kQStages;
                 if (first && !mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort)) return false;
-                if (!mbar_wait(bar(PDS_FULL + b), (acc_it >> 1) & 1, abort)) return false;
+                if (!mbar_wait(bar(PDS_FULL + b), (sp >> 1) & 1, abort)) return false;
                 tc_fence_after();
-                const uint32_t qb = sbase + LY::Q0 + b * LY::TILEQ;
-                const uint32_t ob = sbase + LY::DO0 + b * LY::TILEQ;
+                const uint32_t qb = sbase + LY::Q0 + s * LY::TILEQ;
+                const uint32_t ob = sbase + LY::DO0 + s * LY::TILEQ;
 #pragma unroll
-                for (int k = 0; k < BQ / 16; ++k) {
-                    const uint64_t a = smem_desc_sw128(sbase + LY::P0 + b * LY::PT + k * 32, 16, 1024);
-                    const uint64_t bb = smem_desc_sw128(ob + k * 16 * 128, LY::BLKQ, 1024);
-                    mma_bf16_ss(tmem + LY::DV_COL, a, bb, IDESC_ACC, (!first || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < BQ / 16; ++k)
+                    mma_bf16_ts(tmem + LY::DV_COL, tmem + b * 128 + packed_col(k),
+                                smem_desc_sw128(ob + k * 16 * 128, LY::BLKQ, 1024), IDESC_ACC,
+                                (!first || k > 0) ? 1u : 0u);
 #pragma unroll
-                for (int k = 0; k < BQ / 16; ++k) {
-                    const uint64_t a = smem_desc_sw128(sbase + LY::DS0 + b * LY::PT + k * 32, 16, 1024);
-                    const uint64_t bb = smem_desc_sw128(qb + k * 16 * 128, LY::BLKQ, 1024);
-                    mma_bf16_ss(tmem + LY::DK_COL, a, bb, IDESC_ACC, (!first || k > 0) ? 1u : 0u);
-                }
-                mma_commit(bar(PDS_EMPTY + b));
-                mma_commit(bar(QO_EMPTY + b));
-                ++acc_it;
+                for (int k = 0; k < BQ / 16; ++k)
+                    mma_bf16_ts(tmem + LY::DK_COL, tmem + b * 128 + 64 + packed_col(k),
+                                smem_desc_sw128(qb + k * 16 * 128, LY::BLKQ, 1024), IDESC_ACC,
+                                (!first || k > 0) ? 1u : 0u);
+                mma_commit(bar(QO_EMPTY + s));
                 return true;
             };
             for (int n = 0; ok; ++n, ++unit_it) {
@@ -623,36 +628,33 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
                 if (!(ok = mbar_wait(bar(KV_FULL), unit_it & 1, abort))) break;
-                if (!(ok = mbar_wait(bar(K_READY), unit_it & 1, abort))) break;
-                for (int i = w.lo; i < w.hi; ++i) {
-                    const int s = st_it & 1;
-                    const uint32_t ph = (st_it >> 1) & 1;
-                    if (!(ok = mbar_wait(bar(QO_FULL + s), ph, abort))) break;
-                    if (!(ok = mbar_wait(bar(Q_READY + s), ph, abort))) break;
-                    if (!(ok = mbar_wait(bar(ST_EMPTY + s), ph ^ 1, abort))) break;
+                for (int i = w.lo; i < w.hi; ++i, ++st) {
+                    const int s = st % kQStages, b = st & 1;
+                    if (!(ok = mbar_wait(bar(QO_FULL + s), (st / kQStages) & 1, abort))) break;
                     tc_fence_after();
                     const uint32_t qb = sbase + LY::Q0 + s * LY::TILEQ;
                     const uint32_t ob = sbase + LY::DO0 + s * LY::TILEQ;
+                    // S^T = K' Q'^T and dP^T = V dO^T into step buffer b; buffer b was last
+                    // read by the dV/dK MMAs of step st-2, issued earlier (in-order).
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
                         const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
-                        mma_bf16_ss(tmem + s * 128, smem_desc_sw128(sbase + LY::K0 + offk, 16, 1024),
+                        mma_bf16_ss(tmem + b * 128, smem_desc_sw128(sbase + LY::K0 + offk, 16, 1024),
                                     smem_desc_sw128(qb + offq, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
                     }
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
                         const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
-                        mma_bf16_ss(tmem + s * 128 + 64, smem_desc_sw128(sbase + LY::V0 + offk, 16, 1024),
+                        mma_bf16_ss(tmem + b * 128 + 64, smem_desc_sw128(sbase + LY::V0 + offk, 16, 1024),
                                     smem_desc_sw128(ob + offq, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(ST_FULL + s));
-                    ++st_it;
-                    if (i > w.lo && !(ok = issue_acc(i == w.lo + 1))) break;
+                    mma_commit(bar(ST_FULL + b));
+                    if (i > w.lo && !(ok = issue_acc(st - 1, i == w.lo + 1))) break;
                 }
                 if (!ok) break;
-                if (!(ok = issue_acc(w.hi - w.lo == 1))) break;
+                if (!(ok = issue_acc(st - 1, w.hi - w.lo == 1))) break;
                 mma_commit(bar(ACC_FULL));
                 mma_commit(bar(KV_EMPTY));
             }
@@ -660,79 +662,96 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             mbar_wait_limit(bar(DRAIN), 0, kDrainNs);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ LSE / delta stager
+        uint32_t st = 0;
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            int u;
+            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
+            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
+            for (int i = w.lo; i < w.hi && ok; ++i, ++st) {
+                const int sl = st % kLsedSlots;
+                if (!(ok = wait_warp(bar(LSED_EMPTY + sl), ((st / kLsedSlots) & 1) ^ 1, abort))) break;
+                float* dst = lsed + sl * 128;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int q = lane + 32 * h2;
+                    const int qq = i * BQ + q;
+                    float l2 = 0.f, dl = 0.f;
+                    if (qq < w.L) {
+                        const int64_t idx = static_cast<int64_t>(w.h) * p.total + w.row0 + qq;
+                        l2 = __ldg(p.lse + idx) * kLog2e;
+                        dl = __ldg(p.delta + idx);
+                    }
+                    dst[q] = l2;
+                    dst[64 + q] = dl;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(LSED_FULL + sl));
+            }
+        }
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ P^T, dS^T + epilogue
-        const int t = threadIdx.x - 128;          // 0..127
-        const int wq = warp - 4;
+        const int g = (warp - 4) >> 2;             // math warpgroup: q columns [32g, 32g + 32)
+        const int wq = warp & 3;
         const int r = wq * 32 + lane;              // key row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float scale_log2 = p.scale * kLog2e;
-        uint32_t unit_it = 0, st_it = 0;
+        const int c0 = 32 * g;
+        uint32_t unit_it = 0, st = 0;
         bool ok = true;
         for (int n = 0; ok; ++n, ++unit_it) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
             const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
             const int kvpos = w.tile * 128 + r;
-            for (int i = w.lo; i < w.hi; ++i) {
-                const int b = st_it & 1;
-                {   // stage LSE (log2 units) and delta of this step's 64 q rows
-                    const int qq = i * BQ + (t & 63);
-                    float val = 0.f;
-                    if (qq < w.L) {
-                        const int64_t idx = static_cast<int64_t>(w.h) * p.total + w.row0 + qq;
-                        val = (t < 64) ? __ldg(p.lse + idx) * kLog2e : __ldg(p.delta + idx);
+            for (int i = w.lo; i < w.hi; ++i, ++st) {
+                const int b = st & 1, sl = st % kLsedSlots;
+                if (!(ok = wait_warp(bar(LSED_FULL + sl), (st / kLsedSlots) & 1, abort))) break;
+                float l2[32], dl[32];
+                {
+                    const float4* src = reinterpret_cast<const float4*>(lsed + sl * 128 + c0);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 a = src[e], d4 = src[16 + e];
+                        l2[4 * e] = a.x; l2[4 * e + 1] = a.y; l2[4 * e + 2] = a.z; l2[4 * e + 3] = a.w;
+                        dl[4 * e] = d4.x; dl[4 * e + 1] = d4.y; dl[4 * e + 2] = d4.z; dl[4 * e + 3] = d4.w;
                     }
-                    lsed[b * 128 + t] = val;
-                    mbar_arrive(bar(LSED_FULL + b));
-                    if (!(ok = wait_warp(bar(LSED_FULL + b), (st_it >> 1) & 1, abort))) break;
                 }
-                const float* l2 = lsed + b * 128;
-                const float* dl = l2 + 64;
-                if (!(ok = wait_warp(bar(ST_FULL + b), (st_it >> 1) & 1, abort))) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(LSED_EMPTY + sl));
+                if (!(ok = wait_warp(bar(ST_FULL + b), (st >> 1) & 1, abort))) break;
                 tc_fence_after();
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + b * 128 + c0, sr);
+                tmem_ld32(tmem + lane_off + b * 128 + 64 + c0, dr);
+                tmem_wait_ld();
+                // allowed q columns: kvpos <= i*BQ + col and i*BQ + col < L
                 const bool edge = (i * BQ < w.tile * 128 + 128) || ((i + 1) * BQ > w.L);
-                // allowed q columns c: kvpos <= i*BQ + c and i*BQ + c < L
-                const int c_lo = kvpos - i * BQ;
-                const int c_hi = w.L - 1 - i * BQ;
-                uint32_t pp[32], pd[32];
+                const int c_lo = kvpos - i * BQ, c_hi = w.L - 1 - i * BQ;
+                uint32_t pp[16], pd[16];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t sr[32], dr[32];
-                    tmem_ld32(tmem + lane_off + b * 128 + c * 32, sr);
-                    tmem_ld32(tmem + lane_off + b * 128 + 64 + c * 32, dr);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int col = c * 32 + e;
-                        float p0 = ex2_approx(__uint_as_float(sr[e]) * scale_log2 - l2[col]);
-                        float p1 = ex2_approx(__uint_as_float(sr[e + 1]) * scale_log2 - l2[col + 1]);
-                        if (edge) {
-                            if (col < c_lo || col > c_hi) p0 = 0.f;
-                            if (col + 1 < c_lo || col + 1 > c_hi) p1 = 0.f;
-                        }
-                        pp[col >> 1] = pack_bf16x2(p0, p1);
-                        pd[col >> 1] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) - dl[col]),
-                                                   p1 * (__uint_as_float(dr[e + 1]) - dl[col + 1]));
+                for (int e = 0; e < 32; e += 2) {
+                    const int col = c0 + e;
+                    const float2 x = fma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                          make_float2(scale_log2, scale_log2), make_float2(-l2[e], -l2[e + 1]));
+                    float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                    if (edge) {
+                        if (col < c_lo || col > c_hi) p0 = 0.f;
+                        if (col + 1 < c_lo || col + 1 > c_hi) p1 = 0.f;
                     }
+                    const float2 dsv = mul2(make_float2(p0, p1),
+                                            make_float2(__uint_as_float(dr[e]) - dl[e],
+                                                        __uint_as_float(dr[e + 1]) - dl[e + 1]));
+                    pp[e >> 1] = pack_bf16x2(p0, p1);
+                    pd[e >> 1] = pack_bf16x2(dsv.x, dsv.y);
                 }
+                tmem_st16(tmem + lane_off + b * 128 + c0, pp);
+                tmem_st16(tmem + lane_off + b * 128 + 64 + c0, pd);
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(ST_EMPTY + b));
-                if (!(ok = wait_warp(bar(PDS_EMPTY + b), ((st_it >> 1) & 1) ^ 1, abort))) break;
-#pragma unroll
-                for (int ci = 0; ci < 8; ++ci) {
-                    const uint32_t pa = sw128(sbase + LY::P0 + b * LY::PT, r, ci);
-                    const uint32_t da = sw128(sbase + LY::DS0 + b * LY::PT, r, ci);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(pa), "r"(pp[4 * ci]), "r"(pp[4 * ci + 1]), "r"(pp[4 * ci + 2]),
-                                 "r"(pp[4 * ci + 3]) : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(da), "r"(pd[4 * ci]), "r"(pd[4 * ci + 1]), "r"(pd[4 * ci + 2]),
-                                 "r"(pd[4 * ci + 3]) : "memory");
-                }
-                fence_proxy_async_smem();
                 mbar_arrive(bar(PDS_FULL + b));
-                ++st_it;
             }
             if (!ok) break;
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
@@ -740,47 +759,29 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             const bool valid = kvpos < w.L;
             const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? kvpos : 0);
             const int64_t roff = (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
-            // dV: plain copy out
+            if (g == 0) {   // dV: plain copy out
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + lane_off + LY::DV_COL + c * 32, rr);
-                tmem_wait_ld();
-                uint32_t pk[16];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tmem + lane_off + LY::DV_COL + c * 32, rr);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dv) + roff + c * 64);
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                    if (valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dv) + roff + c * 64);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    }
                 }
+            } else {        // dK: scale and R(p)^T
+                store_unrotated<D>(tmem + lane_off + LY::DK_COL, p.table, kvpos, p.scale, p.use_rope != 0,
+                                   valid, reinterpret_cast<uint8_t*>(p.dk) + roff);
             }
-            store_unrotated<D>(tmem + lane_off + LY::DK_COL, p.table, kvpos, p.scale, p.use_rope != 0,
-                               valid, reinterpret_cast<uint8_t*>(p.dk) + roff);
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));
-        }
-    } else if (warp >= 8) {
-        // ------------------------------------------------------------ staged K / Q hand-off
-        // (operands arrive pre-rotated from the prep pass; these warps order the hand-off)
-        uint32_t unit_it = 0, st_it = 0;
-        bool ok = true;
-        for (int n = 0; ok; ++n, ++unit_it) {
-            int u;
-            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
-            if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
-            fence_proxy_async_smem();
-            mbar_arrive(bar(K_READY));
-            for (int i = w.lo; i < w.hi; ++i) {
-                const int s = st_it & 1;
-                if (!(ok = wait_warp(bar(QO_FULL + s), (st_it >> 1) & 1, abort))) break;
-                fence_proxy_async_smem();
-                mbar_arrive(bar(Q_READY + s));
-                ++st_it;
-            }
         }
     }
 
@@ -788,10 +789,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     if (*abort) {
         if (warp == 0 && lane == 0) {
             if (kv_issued > 0) mbar_wait_limit(bar(KV_FULL), (kv_issued - 1) & 1, kDrainNs);
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < kQStages; ++s)
                 if (q_issued > static_cast<uint32_t>(s)) {
-                    const uint32_t n = ((q_issued - 1 - s) & ~1u) + s;
-                    mbar_wait_limit(bar(QO_FULL + s), (n >> 1) & 1, kDrainNs);
+                    const uint32_t nn = q_issued - 1 - ((q_issued - 1 - s) % kQStages);
+                    mbar_wait_limit(bar(QO_FULL + s), (nn / kQStages) & 1, kDrainNs);
                 }
         }
         if (threadIdx.x == 0) atomicOr(p.err, VLC_DEVERR_TIMEOUT);
