@@ -13,10 +13,11 @@
 //   prep_kernel    D = rowsum(dO * O) in fp32, layout [H, total]; with RoPE also
 //                  q' = R(p) q and k' = R(p) k once into the workspace (bf16).
 //   dq_kernel      q-major, one unit = (q tile of 128 rows, head): for every key
-//                  tile, tcgen05 computes S = Q'K'^T and dP = dO V^T into TMEM,
-//                  128 threads form dS (bf16, shared memory), tcgen05 adds
-//                  dS K' into a TMEM dQ accumulator; epilogue applies scale and
-//                  R(p)^T and stores bf16.
+//                  step of 64 rows, tcgen05 computes S = Q'K'^T and dP = dO V^T
+//                  into TMEM (double buffered), two warpgroups form dS and write
+//                  it back packed into TMEM, tcgen05 adds dS K' (tensor-memory A
+//                  operand) into a TMEM dQ accumulator; epilogue applies scale
+//                  and R(p)^T and stores bf16.
 //   dkdv_kernel    key-major, one unit = (key tile of 128 rows, head): for every
 //                  q step of 64 rows from the diagonal to the segment end,
 //                  S^T = K'Q'^T and dP^T = V dO^T into TMEM (double buffered),
@@ -165,31 +166,45 @@ __device__ __forceinline__ void store_unrotated(uint32_t taddr, const float2* __
     }
 }
 
+// TMEM column of the packed bf16 K-slice k (16 columns of a 64-column step) when
+// math warpgroup g owns step columns [32g, 32g + 32) and packs them into TMEM
+// columns [32g, 32g + 16) of the step buffer.
+__device__ __forceinline__ uint32_t packed_col(int k) { return (k >> 1) * 32 + (k & 1) * 8; }
+
 // ====================================================================== dQ pass
 namespace dq {
 
+constexpr int BK = kBwdKN;     // key rows per step
+static_assert(BK == 64, "a step's S / dP take 64 TMEM columns each");
+constexpr int kKStages = 3;
+constexpr int kQSlots = 2;
+
 enum : int {
-    QD_FULL = 0, Q_READY = 1, QD_EMPTY = 2,
-    K_FULL = 3, K_READY = 5, V_FULL = 7, KV_EMPTY = 9,
-    SD_FULL = 11, SD_EMPTY = 12, DS_FULL = 13, DQ_DONE = 14, ACC_EMPTY = 15, DRAIN = 16,
-    UNIT_FULL = 17, UNIT_EMPTY = 17 + kRing, NUM_BARS = 17 + 2 * kRing
+    QD_FULL = 0, QD_EMPTY = kQSlots,
+    K_FULL = 2 * kQSlots, V_FULL = K_FULL + kKStages, KV_EMPTY = V_FULL + kKStages,
+    SD_FULL = KV_EMPTY + kKStages, DS_FULL = SD_FULL + 2,
+    ACC_FULL = DS_FULL + 2, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2,
+    UNIT_FULL = ACC_FULL + 3, UNIT_EMPTY = UNIT_FULL + kRing, NUM_BARS = UNIT_EMPTY + kRing
 };
 
 template <int D>
 struct Layout {
     static constexpr int KB = D / 64;
-    static constexpr uint32_t BLK = 128u * 128u;
-    static constexpr uint32_t TILE = 128u * D * 2u;
-    static constexpr uint32_t Q0 = 0;
-    static constexpr uint32_t DO0 = TILE;
-    static constexpr uint32_t K0 = 2 * TILE;
-    static constexpr uint32_t V0 = 4 * TILE;
-    static constexpr uint32_t DS0 = 6 * TILE;
-    static constexpr uint32_t BAR0 = DS0 + 128u * 128u * 2u;
-    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;   // tmem slot, abort flag, unit ring
+    static constexpr uint32_t BLKQ = 128u * 128u;      // q-side block: 128 rows x 128 B
+    static constexpr uint32_t TILEQ = 128u * D * 2u;
+    static constexpr uint32_t BLKK = BK * 128u;        // key-side block: 64 rows x 128 B
+    static constexpr uint32_t TILEK = BK * D * 2u;
+    static constexpr uint32_t Q0 = 0;                          // kQSlots
+    static constexpr uint32_t DO0 = kQSlots * TILEQ;           // kQSlots
+    static constexpr uint32_t K0 = 2 * kQSlots * TILEQ;        // kKStages
+    static constexpr uint32_t V0 = K0 + kKStages * TILEK;      // kKStages
+    static constexpr uint32_t BAR0 = V0 + kKStages * TILEK;
+    static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;      // tmem slot, abort flag, unit ring
     static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
-    static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256;
+    // TMEM: step buffer b at columns 128b: S (64 fp32 columns) then dP (64); the packed
+    // bf16 dS of a step overwrites the consumed S columns.  dQ accumulator after them.
+    static constexpr uint32_t DQ_COL = 256;
 };
 
 template <int D>
@@ -205,7 +220,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
-    constexpr int kRingConsumers = 1 + 4 + 4;   // MMA thread, 4 math warps, 4 hand-off warps
+    constexpr int kRingConsumers = 1 + 8;   // MMA thread, 8 math warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     __shared__ int s_skip, s_nunits;
@@ -218,20 +233,21 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     const int nunits = s_nunits;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(QD_FULL), 1);
-        mbar_init(bar(Q_READY), 128);
-        mbar_init(bar(QD_EMPTY), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQSlots; ++i) {
+            mbar_init(bar(QD_FULL + i), 1);
+            mbar_init(bar(QD_EMPTY + i), 1);
+        }
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(bar(K_FULL + i), 1);
-            mbar_init(bar(K_READY + i), 128);
             mbar_init(bar(V_FULL + i), 1);
             mbar_init(bar(KV_EMPTY + i), 1);
         }
-        mbar_init(bar(SD_FULL), 1);
-        mbar_init(bar(SD_EMPTY), 128);
-        mbar_init(bar(DS_FULL), 128);
-        mbar_init(bar(DQ_DONE), 1);
-        mbar_init(bar(ACC_EMPTY), 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(SD_FULL + i), 1);
+            mbar_init(bar(DS_FULL + i), 256);
+        }
+        mbar_init(bar(ACC_FULL), 1);
+        mbar_init(bar(ACC_EMPTY), 256);
         mbar_init(bar(DRAIN), 1);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(bar(UNIT_FULL + i), 1);
@@ -248,118 +264,124 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    uint32_t q_issued = 0, kv_issued = 0, k_only = 0;
+    uint32_t q_issued = 0, kv_issued = 0;
 
     if (warp == 0) {
         if (lane == 0) {   // ---------------------------------------- TMA producer
-            const uint64_t pol_stream = make_l2_policy_evict_first();
-            const uint64_t pol_keep = make_l2_policy_evict_last();
-            uint32_t unit_it = 0, kv_it = 0;
+            const uint64_t pol_stream = make_l2_policy_evict_first();   // q/dO: once per unit
+            const uint64_t pol_keep = make_l2_policy_evict_last();      // K/V: re-read by other units
+            uint32_t unit_it = 0, kv = 0;
             bool ok = true;
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_put(rg, n, p.next_q, nunits, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-                if (!(ok = mbar_wait(bar(QD_EMPTY), (unit_it & 1) ^ 1, abort))) break;
-                mbar_expect_tx(bar(QD_FULL), 2 * LY::TILE);
+                const int qs = unit_it % kQSlots;
+                if (!(ok = mbar_wait(bar(QD_EMPTY + qs), ((unit_it / kQSlots) & 1) ^ 1, abort))) break;
+                mbar_expect_tx(bar(QD_FULL + qs), 2 * LY::TILEQ);
                 const int qrow = w.row0 + w.tile * 128;
 #pragma unroll
                 for (int kb = 0; kb < LY::KB; ++kb) {
-                    tma_load_3d_hint(sbase + LY::Q0 + kb * LY::BLK, &tmQ, kb * 64, w.h, qrow, bar(QD_FULL), pol_stream);
-                    tma_load_3d_hint(sbase + LY::DO0 + kb * LY::BLK, &tmDO, kb * 64, w.h, qrow, bar(QD_FULL), pol_stream);
+                    tma_load_3d_hint(sbase + LY::Q0 + qs * LY::TILEQ + kb * LY::BLKQ, &tmQ, kb * 64, w.h,
+                                     qrow, bar(QD_FULL + qs), pol_stream);
+                    tma_load_3d_hint(sbase + LY::DO0 + qs * LY::TILEQ + kb * LY::BLKQ, &tmDO, kb * 64, w.h,
+                                     qrow, bar(QD_FULL + qs), pol_stream);
                 }
                 q_issued = unit_it + 1;
-                for (int j = 0; j < w.hi; ++j) {
-                    const int ks = kv_it & 1;
-                    if (!(ok = mbar_wait(bar(KV_EMPTY + ks), ((kv_it >> 1) & 1) ^ 1, abort))) break;
-                    const int row = w.row0 + j * 128;
-                    mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
-                    mbar_expect_tx(bar(V_FULL + ks), LY::TILE);
+                for (int j = 0; j < w.hi && ok; ++j, ++kv) {
+                    const int ks = kv % kKStages;
+                    if (!(ok = mbar_wait(bar(KV_EMPTY + ks), ((kv / kKStages) & 1) ^ 1, abort))) break;
+                    const int row = w.row0 + j * BK;
+                    mbar_expect_tx(bar(K_FULL + ks), LY::TILEK);
+                    mbar_expect_tx(bar(V_FULL + ks), LY::TILEK);
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb) {
-                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64, w.h,
+                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILEK + kb * LY::BLKK, &tmK, kb * 64, w.h,
                                          row, bar(K_FULL + ks), pol_keep);
-                        tma_load_3d_hint(sbase + LY::V0 + ks * LY::TILE + kb * LY::BLK, &tmV, kb * 64, w.h,
+                        tma_load_3d_hint(sbase + LY::V0 + ks * LY::TILEK + kb * LY::BLKK, &tmV, kb * 64, w.h,
                                          row, bar(V_FULL + ks), pol_keep);
                     }
-                    kv_issued = ++kv_it;
+                    kv_issued = kv + 1;
                 }
             }
-            (void)k_only;
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {   // ---------------------------------------- MMA issuer
-            constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BK, false);
             constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, D, true);
-            uint32_t unit_it = 0, kv_it = 0, sd_it = 0, ds_it = 0;
+            uint32_t unit_it = 0, kv = 0;
             bool ok = true;
-            auto issue_dq = [&](bool first) -> bool {
-                const int ks = ds_it & 1;   // key stage of the tile this dS belongs to
+            // dQ += dS K' for step sp (dS packed in TMEM, K' an MN-major operand)
+            auto issue_dq = [&](uint32_t sp, bool first) -> bool {
+                const int b = sp & 1, ks = sp % kKStages;
                 if (first && !mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort)) return false;
-                if (!mbar_wait(bar(DS_FULL), ds_it & 1, abort)) return false;
+                if (!mbar_wait(bar(DS_FULL + b), (sp >> 1) & 1, abort)) return false;
                 tc_fence_after();
-                const uint32_t kbase = sbase + LY::K0 + ks * LY::TILE;
+                const uint32_t kb = sbase + LY::K0 + ks * LY::TILEK;
 #pragma unroll
-                for (int k = 0; k < 128 / 16; ++k) {
-                    const uint64_t a = smem_desc_sw128(sbase + LY::DS0 + (k >> 2) * LY::BLK + (k & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(kbase + k * 16 * 128, LY::BLK, 1024);
-                    mma_bf16_ss(tmem + LY::DQ_COL, a, b, IDESC_DQ, (!first || k > 0) ? 1u : 0u);
-                }
-                mma_commit(bar(DQ_DONE));
+                for (int k = 0; k < BK / 16; ++k)
+                    mma_bf16_ts(tmem + LY::DQ_COL, tmem + b * 128 + packed_col(k),
+                                smem_desc_sw128(kb + k * 16 * 128, LY::BLKK, 1024), IDESC_DQ,
+                                (!first || k > 0) ? 1u : 0u);
                 mma_commit(bar(KV_EMPTY + ks));
-                ++ds_it;
                 return true;
             };
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-                if (!(ok = mbar_wait(bar(QD_FULL), unit_it & 1, abort))) break;
-                if (!(ok = mbar_wait(bar(Q_READY), unit_it & 1, abort))) break;
-                for (int j = 0; j < w.hi; ++j) {
-                    const int ks = kv_it & 1;
-                    const uint32_t ph = (kv_it >> 1) & 1;
-                    if (!(ok = mbar_wait(bar(K_READY + ks), ph, abort))) break;
+                const int qs = unit_it % kQSlots;
+                if (!(ok = mbar_wait(bar(QD_FULL + qs), (unit_it / kQSlots) & 1, abort))) break;
+                const uint32_t qb = sbase + LY::Q0 + qs * LY::TILEQ;
+                const uint32_t ob = sbase + LY::DO0 + qs * LY::TILEQ;
+                for (int j = 0; j < w.hi; ++j, ++kv) {
+                    const int ks = kv % kKStages, b = kv & 1;
+                    const uint32_t ph = (kv / kKStages) & 1;
+                    if (!(ok = mbar_wait(bar(K_FULL + ks), ph, abort))) break;
                     if (!(ok = mbar_wait(bar(V_FULL + ks), ph, abort))) break;
-                    if (!(ok = mbar_wait(bar(SD_EMPTY), (sd_it & 1) ^ 1, abort))) break;
                     tc_fence_after();
-                    const uint32_t kbase = sbase + LY::K0 + ks * LY::TILE;
-                    const uint32_t vbase = sbase + LY::V0 + ks * LY::TILE;
+                    const uint32_t kb = sbase + LY::K0 + ks * LY::TILEK;
+                    const uint32_t vb = sbase + LY::V0 + ks * LY::TILEK;
+                    // S = Q'K'^T and dP = dO V^T into step buffer b (last read by the dQ MMA of
+                    // step kv-2, issued earlier)
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
-                        mma_bf16_ss(tmem + LY::S_COL, smem_desc_sw128(sbase + LY::Q0 + off, 16, 1024),
-                                    smem_desc_sw128(kbase + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                        const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
+                        const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
+                        mma_bf16_ss(tmem + b * 128, smem_desc_sw128(qb + offq, 16, 1024),
+                                    smem_desc_sw128(kb + offk, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
                     }
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
-                        mma_bf16_ss(tmem + LY::DP_COL, smem_desc_sw128(sbase + LY::DO0 + off, 16, 1024),
-                                    smem_desc_sw128(vbase + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                        const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
+                        const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
+                        mma_bf16_ss(tmem + b * 128 + 64, smem_desc_sw128(ob + offq, 16, 1024),
+                                    smem_desc_sw128(vb + offk, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(SD_FULL));
-                    if (j == w.hi - 1) mma_commit(bar(QD_EMPTY));
-                    ++sd_it;
-                    ++kv_it;
-                    if (j > 0 && !(ok = issue_dq(j == 1))) break;
+                    mma_commit(bar(SD_FULL + b));
+                    if (j == w.hi - 1) mma_commit(bar(QD_EMPTY + qs));
+                    if (j > 0 && !(ok = issue_dq(kv - 1, j == 1))) break;
                 }
                 if (!ok) break;
-                if (!(ok = issue_dq(w.hi == 1))) break;
+                if (!(ok = issue_dq(kv - 1, w.hi == 1))) break;
+                mma_commit(bar(ACC_FULL));
             }
             mma_commit(bar(DRAIN));
             mbar_wait_limit(bar(DRAIN), 0, kDrainNs);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ dS + epilogue
-        const int wq = warp - 4;
-        const int r = wq * 32 + lane;
+        const int g = (warp - 4) >> 2;             // math warpgroup: key columns [32g, 32g + 32)
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;              // query row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float scale_log2 = p.scale * kLog2e;
-        uint32_t sd_it = 0, ds_it = 0;
+        const int c0 = 32 * g;
+        uint32_t unit_it = 0, kv = 0;
         bool ok = true;
-        for (int n = 0; ok; ++n) {
+        for (int n = 0; ok; ++n, ++unit_it) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
             const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
@@ -368,82 +390,61 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? qpos : 0);
             const float lse2 = valid ? __ldg(p.lse + static_cast<int64_t>(w.h) * p.total + tok) * kLog2e : 0.f;
             const float dlt = valid ? __ldg(p.delta + static_cast<int64_t>(w.h) * p.total + tok) : 0.f;
-            for (int j = 0; j < w.hi; ++j) {
-                if (!(ok = wait_warp(bar(SD_FULL), sd_it & 1, abort))) break;
+            for (int j = 0; j < w.hi; ++j, ++kv) {
+                const int b = kv & 1;
+                if (!(ok = wait_warp(bar(SD_FULL + b), (kv >> 1) & 1, abort))) break;
                 tc_fence_after();
-                // allowed key columns of this tile: c <= lim
-                const int lim = !valid ? -1 : (j == w.hi - 1 ? min(qpos, w.L - 1) - j * 128 : 127);
-                uint32_t pk[64];
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_off + b * 128 + c0, sr);
+                tmem_ld32(tmem + lane_off + b * 128 + 64 + c0, dr);
+                tmem_wait_ld();
+                // allowed key columns of this step: c <= lim (diagonal steps and the tail)
+                const bool edge = (j * BK + BK - 1 > w.tile * 128) || ((j + 1) * BK > w.L);
+                const int lim = !valid ? -1 : (edge ? min(qpos, w.L - 1) - j * BK : BK - 1);
+                const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
+                const float2 nd2 = make_float2(-dlt, -dlt);
+                uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t sr[32], dr[32];
-                    tmem_ld32(tmem + lane_off + LY::S_COL + c * 32, sr);
-                    tmem_ld32(tmem + lane_off + LY::DP_COL + c * 32, dr);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int col = c * 32 + e;
-                        const float p0 = (col <= lim) ? ex2_approx(__uint_as_float(sr[e]) * scale_log2 - lse2) : 0.f;
-                        const float p1 = (col + 1 <= lim) ? ex2_approx(__uint_as_float(sr[e + 1]) * scale_log2 - lse2) : 0.f;
-                        pk[(col >> 1)] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) - dlt),
-                                                     p1 * (__uint_as_float(dr[e + 1]) - dlt));
-                    }
+                for (int e = 0; e < 32; e += 2) {
+                    const int col = c0 + e;
+                    const float2 x = fma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, nl2);
+                    const float p0 = (col <= lim) ? ex2_approx(x.x) : 0.f;
+                    const float p1 = (col + 1 <= lim) ? ex2_approx(x.y) : 0.f;
+                    const float2 ds = mul2(make_float2(p0, p1),
+                                           add2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd2));
+                    pk[e >> 1] = pack_bf16x2(ds.x, ds.y);
                 }
+                tmem_st16(tmem + lane_off + b * 128 + c0, pk);
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(SD_EMPTY));
-                ++sd_it;
-                if (ds_it > 0 && !(ok = wait_warp(bar(DQ_DONE), (ds_it - 1) & 1, abort))) break;
-#pragma unroll
-                for (int ci = 0; ci < 16; ++ci) {
-                    const uint32_t addr = sw128(sbase + LY::DS0 + (ci >> 3) * LY::BLK, r, ci & 7);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(addr), "r"(pk[4 * ci]), "r"(pk[4 * ci + 1]), "r"(pk[4 * ci + 2]),
-                                 "r"(pk[4 * ci + 3]) : "memory");
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(bar(DS_FULL));
-                ++ds_it;
+                mbar_arrive(bar(DS_FULL + b));
             }
             if (!ok) break;
-            if (!(ok = wait_warp(bar(DQ_DONE), (ds_it - 1) & 1, abort))) break;
+            if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
             tc_fence_after();
-            uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dq) + (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
-            store_unrotated<D>(tmem + lane_off + LY::DQ_COL, p.table, qpos, p.scale, p.use_rope != 0,
-                               valid, row_out);
+            if (g == 0) {
+                uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dq) + (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
+                store_unrotated<D>(tmem + lane_off + LY::DQ_COL, p.table, qpos, p.scale, p.use_rope != 0,
+                                   valid, row_out);
+            }
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));
-        }
-    } else if (warp >= 8) {
-        // ------------------------------------------------------------ staged Q / K hand-off
-        // (operands arrive pre-rotated from the prep pass; these warps order the hand-off)
-        uint32_t unit_it = 0, kv_it = 0;
-        bool ok = true;
-        for (int n = 0; ok; ++n, ++unit_it) {
-            int u;
-            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-            if (!(ok = wait_warp(bar(QD_FULL), unit_it & 1, abort))) break;
-            fence_proxy_async_smem();
-            mbar_arrive(bar(Q_READY));
-            for (int j = 0; j < w.hi; ++j) {
-                const int ks = kv_it & 1;
-                if (!(ok = wait_warp(bar(K_FULL + ks), (kv_it >> 1) & 1, abort))) break;
-                fence_proxy_async_smem();
-                mbar_arrive(bar(K_READY + ks));
-                ++kv_it;
-            }
         }
     }
 
     __syncthreads();
     if (*abort) {
         if (warp == 0 && lane == 0) {
-            if (q_issued > 0) mbar_wait_limit(bar(QD_FULL), (q_issued - 1) & 1, kDrainNs);
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < kQSlots; ++s)
+                if (q_issued > static_cast<uint32_t>(s)) {
+                    const uint32_t nn = q_issued - 1 - ((q_issued - 1 - s) % kQSlots);
+                    mbar_wait_limit(bar(QD_FULL + s), (nn / kQSlots) & 1, kDrainNs);
+                }
+            for (int s = 0; s < kKStages; ++s)
                 if (kv_issued > static_cast<uint32_t>(s)) {
-                    const uint32_t n = ((kv_issued - 1 - s) & ~1u) + s;
-                    mbar_wait_limit(bar(K_FULL + s), (n >> 1) & 1, kDrainNs);
-                    mbar_wait_limit(bar(V_FULL + s), (n >> 1) & 1, kDrainNs);
+                    const uint32_t nn = kv_issued - 1 - ((kv_issued - 1 - s) % kKStages);
+                    mbar_wait_limit(bar(K_FULL + s), (nn / kKStages) & 1, kDrainNs);
+                    mbar_wait_limit(bar(V_FULL + s), (nn / kKStages) & 1, kDrainNs);
                 }
         }
         if (threadIdx.x == 0) atomicOr(p.err, VLC_DEVERR_TIMEOUT);
@@ -494,10 +495,6 @@ struct Layout {
     // packed bf16 P^T / dS^T of a step overwrite the consumed S^T / dP^T columns.
     static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
 };
-
-// TMEM column of the packed P^T / dS^T K-slice k (16 q columns): math warpgroup g
-// owns q columns [32g, 32g + 32) and packs them into columns [32g, 32g + 16).
-__device__ __forceinline__ uint32_t packed_col(int k) { return (k >> 1) * 32 + (k & 1) * 8; }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -821,20 +818,22 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
     // with RoPE the attention passes read the rotated copies
     const void* qop = p.use_rope ? p.qrot : p.q;
     const void* kop = p.use_rope ? p.krot : p.k;
-    CUtensorMap q128, do128, k128, v128, q64, do64;
+    CUtensorMap q128, do128, k128, v128, q64, do64, k64, v64;
     if (!make_tmap_thd(&q128, qop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&do128, p.dout, p.total, p.H, D, 128) ||
         !make_tmap_thd(&k128, kop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&v128, p.v, p.total, p.H, D, 128) ||
         !make_tmap_thd(&q64, qop, p.total, p.H, D, bwd::dkdv::BQ) ||
-        !make_tmap_thd(&do64, p.dout, p.total, p.H, D, bwd::dkdv::BQ))
+        !make_tmap_thd(&do64, p.dout, p.total, p.H, D, bwd::dkdv::BQ) ||
+        !make_tmap_thd(&k64, kop, p.total, p.H, D, bwd::dq::BK) ||
+        !make_tmap_thd(&v64, p.v, p.total, p.H, D, bwd::dq::BK))
         return cudaErrorInvalidValue;
     {
         constexpr uint32_t smem = bwd::dq::Layout<D>::ALLOC;
         cudaError_t e = cudaFuncSetAttribute(bwd::dq::dq_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        bwd::dq::dq_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
+        bwd::dq::dq_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k64, v64, p);
     }
     {
         constexpr uint32_t smem = bwd::dkdv::Layout<D>::ALLOC;
