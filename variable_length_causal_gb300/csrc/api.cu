@@ -251,7 +251,7 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
 
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
     // q-tile items (dQ pass) and key-tile items (dK/dV pass)
-    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdBM, kBwdKN, VLC_WORKLIST_FWD, items_q,
+    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items_q,
                         L.item_cap, order, seg_base_q, &hdr->count, &hdr->err, s) != cudaSuccess)
         return VLC_ERR_CUDA;
     if (launch_worklist(cu, nseg, total, max_seqlen, kBwdBM, kFwdBN, VLC_WORKLIST_BWD, items_k,

@@ -13,9 +13,10 @@
 //   prep_kernel    D = rowsum(dO * O) in fp32, layout [H, total]; with RoPE also
 //                  q' = R(p) q and k' = R(p) k once into the workspace (bf16).
 //   dq_kernel      q-major, one unit = (q tile of 128 rows, head): for every key
-//                  step of 64 rows, tcgen05 computes S = Q'K'^T and dP = dO V^T
-//                  into TMEM (double buffered), two warpgroups form dS and write
-//                  it back packed into TMEM, tcgen05 adds dS K' (tensor-memory A
+//                  step of 128 rows, tcgen05 computes S = Q'K'^T (two TMEM buffers)
+//                  and dP = dO V^T; two warpgroups (64 key columns each) form P
+//                  as soon as S lands and dS once dP lands, writing dS back packed
+//                  over the dP columns; tcgen05 adds dS K' (tensor-memory A
 //                  operand) into a TMEM dQ accumulator; epilogue applies scale
 //                  and R(p)^T and stores bf16.
 //   dkdv_kernel    key-major, one unit = (key tile of 128 rows, head): for every
@@ -174,38 +175,39 @@ __device__ __forceinline__ uint32_t packed_col(int k) { return (k >> 1) * 32 + (
 // ====================================================================== dQ pass
 namespace dq {
 
-constexpr int BK = kBwdKN;     // key rows per step
-static_assert(BK == 64, "a step's S / dP take 64 TMEM columns each");
-constexpr int kKStages = 3;
+constexpr int BK = 128;        // key rows per step (N = 128 keeps the S / dP MMAs at full rate)
+constexpr int kKStages = 2;
 constexpr int kQSlots = 2;
 
 enum : int {
     QD_FULL = 0, QD_EMPTY = kQSlots,
-    K_FULL = 2 * kQSlots, V_FULL = K_FULL + kKStages, KV_EMPTY = V_FULL + kKStages,
-    SD_FULL = KV_EMPTY + kKStages, DS_FULL = SD_FULL + 2,
-    ACC_FULL = DS_FULL + 2, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2,
+    K_FULL = 2 * kQSlots, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages, V_EMPTY = V_FULL + 1,
+    S_FULL = V_EMPTY + 1, S_EMPTY = S_FULL + 2, DP_FULL = S_EMPTY + 2, DS_FULL = DP_FULL + 1,
+    ACC_FULL = DS_FULL + 1, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2,
     UNIT_FULL = ACC_FULL + 3, UNIT_EMPTY = UNIT_FULL + kRing, NUM_BARS = UNIT_EMPTY + kRing
 };
 
 template <int D>
 struct Layout {
     static constexpr int KB = D / 64;
-    static constexpr uint32_t BLKQ = 128u * 128u;      // q-side block: 128 rows x 128 B
-    static constexpr uint32_t TILEQ = 128u * D * 2u;
-    static constexpr uint32_t BLKK = BK * 128u;        // key-side block: 64 rows x 128 B
-    static constexpr uint32_t TILEK = BK * D * 2u;
+    static constexpr uint32_t BLK = 128u * 128u;       // 128 rows x 128 B
+    static constexpr uint32_t TILE = 128u * D * 2u;
     static constexpr uint32_t Q0 = 0;                          // kQSlots
-    static constexpr uint32_t DO0 = kQSlots * TILEQ;           // kQSlots
-    static constexpr uint32_t K0 = 2 * kQSlots * TILEQ;        // kKStages
-    static constexpr uint32_t V0 = K0 + kKStages * TILEK;      // kKStages
-    static constexpr uint32_t BAR0 = V0 + kKStages * TILEK;
+    static constexpr uint32_t DO0 = kQSlots * TILE;            // kQSlots
+    static constexpr uint32_t K0 = 2 * kQSlots * TILE;         // kKStages
+    static constexpr uint32_t V0 = K0 + kKStages * TILE;       // 1 stage
+    static constexpr uint32_t BAR0 = V0 + TILE;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;      // tmem slot, abort flag, unit ring
     static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
-    // TMEM: step buffer b at columns 128b: S (64 fp32 columns) then dP (64); the packed
-    // bf16 dS of a step overwrites the consumed S columns.  dQ accumulator after them.
-    static constexpr uint32_t DQ_COL = 256;
+    // TMEM: S buffers at columns 0 and 128, dP at 256 (the packed bf16 dS of a step
+    // overwrites the consumed dP columns), dQ accumulator at 384.
+    static constexpr uint32_t DP_COL = 256, DQ_COL = 384;
 };
+
+// TMEM column of dS K-slice k (16 key columns): warpgroup g owns key columns
+// [64g, 64g + 64) and packs them into dP columns [64g, 64g + 32).
+__device__ __forceinline__ uint32_t ds_col(int k) { return (k >> 2) * 64 + (k & 3) * 8; }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -239,13 +241,16 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         }
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(bar(K_FULL + i), 1);
-            mbar_init(bar(V_FULL + i), 1);
-            mbar_init(bar(KV_EMPTY + i), 1);
+            mbar_init(bar(K_EMPTY + i), 1);
         }
+        mbar_init(bar(V_FULL), 1);
+        mbar_init(bar(V_EMPTY), 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(SD_FULL + i), 1);
-            mbar_init(bar(DS_FULL + i), 256);
+            mbar_init(bar(S_FULL + i), 1);
+            mbar_init(bar(S_EMPTY + i), 256);
         }
+        mbar_init(bar(DP_FULL), 1);
+        mbar_init(bar(DS_FULL), 256);
         mbar_init(bar(ACC_FULL), 1);
         mbar_init(bar(ACC_EMPTY), 256);
         mbar_init(bar(DRAIN), 1);
@@ -264,7 +269,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    uint32_t q_issued = 0, kv_issued = 0;
+    uint32_t q_issued = 0, k_issued = 0, v_issued = 0;
 
     if (warp == 0) {
         if (lane == 0) {   // ---------------------------------------- TMA producer
@@ -278,31 +283,41 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
                 const int qs = unit_it % kQSlots;
                 if (!(ok = mbar_wait(bar(QD_EMPTY + qs), ((unit_it / kQSlots) & 1) ^ 1, abort))) break;
-                mbar_expect_tx(bar(QD_FULL + qs), 2 * LY::TILEQ);
+                mbar_expect_tx(bar(QD_FULL + qs), 2 * LY::TILE);
                 const int qrow = w.row0 + w.tile * 128;
 #pragma unroll
                 for (int kb = 0; kb < LY::KB; ++kb) {
-                    tma_load_3d_hint(sbase + LY::Q0 + qs * LY::TILEQ + kb * LY::BLKQ, &tmQ, kb * 64, w.h,
+                    tma_load_3d_hint(sbase + LY::Q0 + qs * LY::TILE + kb * LY::BLK, &tmQ, kb * 64, w.h,
                                      qrow, bar(QD_FULL + qs), pol_stream);
-                    tma_load_3d_hint(sbase + LY::DO0 + qs * LY::TILEQ + kb * LY::BLKQ, &tmDO, kb * 64, w.h,
+                    tma_load_3d_hint(sbase + LY::DO0 + qs * LY::TILE + kb * LY::BLK, &tmDO, kb * 64, w.h,
                                      qrow, bar(QD_FULL + qs), pol_stream);
                 }
                 q_issued = unit_it + 1;
-                for (int j = 0; j < w.hi && ok; ++j, ++kv) {
-                    const int ks = kv % kKStages;
-                    if (!(ok = mbar_wait(bar(KV_EMPTY + ks), ((kv / kKStages) & 1) ^ 1, abort))) break;
-                    const int row = w.row0 + j * BK;
-                    mbar_expect_tx(bar(K_FULL + ks), LY::TILEK);
-                    mbar_expect_tx(bar(V_FULL + ks), LY::TILEK);
+                // K tile j is loaded one step ahead of V tile j-1 (V has a single stage)
+                for (int j = 0; j <= w.hi && ok; ++j) {
+                    if (j < w.hi) {
+                        const uint32_t nn = kv + j;
+                        const int ks = nn % kKStages;
+                        if (!(ok = mbar_wait(bar(K_EMPTY + ks), ((nn / kKStages) & 1) ^ 1, abort))) break;
+                        mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
 #pragma unroll
-                    for (int kb = 0; kb < LY::KB; ++kb) {
-                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILEK + kb * LY::BLKK, &tmK, kb * 64, w.h,
-                                         row, bar(K_FULL + ks), pol_keep);
-                        tma_load_3d_hint(sbase + LY::V0 + ks * LY::TILEK + kb * LY::BLKK, &tmV, kb * 64, w.h,
-                                         row, bar(V_FULL + ks), pol_keep);
+                        for (int kb = 0; kb < LY::KB; ++kb)
+                            tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64, w.h,
+                                             w.row0 + j * BK, bar(K_FULL + ks), pol_keep);
+                        k_issued = nn + 1;
                     }
-                    kv_issued = kv + 1;
+                    if (j >= 1) {
+                        const uint32_t nn = kv + j - 1;
+                        if (!(ok = mbar_wait(bar(V_EMPTY), (nn & 1) ^ 1, abort))) break;
+                        mbar_expect_tx(bar(V_FULL), LY::TILE);
+#pragma unroll
+                        for (int kb = 0; kb < LY::KB; ++kb)
+                            tma_load_3d_hint(sbase + LY::V0 + kb * LY::BLK, &tmV, kb * 64, w.h,
+                                             w.row0 + (j - 1) * BK, bar(V_FULL), pol_keep);
+                        v_issued = nn + 1;
+                    }
                 }
+                kv += w.hi;
             }
         }
         __syncwarp();
@@ -312,19 +327,35 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, D, true);
             uint32_t unit_it = 0, kv = 0;
             bool ok = true;
-            // dQ += dS K' for step sp (dS packed in TMEM, K' an MN-major operand)
-            auto issue_dq = [&](uint32_t sp, bool first) -> bool {
-                const int b = sp & 1, ks = sp % kKStages;
-                if (first && !mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort)) return false;
-                if (!mbar_wait(bar(DS_FULL + b), (sp >> 1) & 1, abort)) return false;
+            // S(n) = Q'K'(n)^T into S buffer n & 1 (free once the math released step n-2)
+            auto issue_s = [&](uint32_t qb, uint32_t nn) -> bool {
+                const int ks = nn % kKStages, b = nn & 1;
+                if (!mbar_wait(bar(K_FULL + ks), (nn / kKStages) & 1, abort)) return false;
+                if (!mbar_wait(bar(S_EMPTY + b), ((nn >> 1) & 1) ^ 1, abort)) return false;
                 tc_fence_after();
-                const uint32_t kb = sbase + LY::K0 + ks * LY::TILEK;
+                const uint32_t kb = sbase + LY::K0 + ks * LY::TILE;
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    mma_bf16_ts(tmem + LY::DQ_COL, tmem + b * 128 + packed_col(k),
-                                smem_desc_sw128(kb + k * 16 * 128, LY::BLKK, 1024), IDESC_DQ,
-                                (!first || k > 0) ? 1u : 0u);
-                mma_commit(bar(KV_EMPTY + ks));
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
+                    mma_bf16_ss(tmem + b * 128, smem_desc_sw128(qb + off, 16, 1024),
+                                smem_desc_sw128(kb + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(S_FULL + b));
+                return true;
+            };
+            // dP(n) = dO V(n)^T (the dP columns were last read by dQ(n-1), issued earlier)
+            auto issue_dp = [&](uint32_t ob, uint32_t nn) -> bool {
+                if (!mbar_wait(bar(V_FULL), nn & 1, abort)) return false;
+                tc_fence_after();
+                const uint32_t vb = sbase + LY::V0;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
+                    mma_bf16_ss(tmem + LY::DP_COL, smem_desc_sw128(ob + off, 16, 1024),
+                                smem_desc_sw128(vb + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(DP_FULL));
+                mma_commit(bar(V_EMPTY));
                 return true;
             };
             for (int n = 0; ok; ++n, ++unit_it) {
@@ -333,52 +364,44 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
                 const int qs = unit_it % kQSlots;
                 if (!(ok = mbar_wait(bar(QD_FULL + qs), (unit_it / kQSlots) & 1, abort))) break;
-                const uint32_t qb = sbase + LY::Q0 + qs * LY::TILEQ;
-                const uint32_t ob = sbase + LY::DO0 + qs * LY::TILEQ;
-                for (int j = 0; j < w.hi; ++j, ++kv) {
-                    const int ks = kv % kKStages, b = kv & 1;
-                    const uint32_t ph = (kv / kKStages) & 1;
-                    if (!(ok = mbar_wait(bar(K_FULL + ks), ph, abort))) break;
-                    if (!(ok = mbar_wait(bar(V_FULL + ks), ph, abort))) break;
+                const uint32_t qb = sbase + LY::Q0 + qs * LY::TILE;
+                const uint32_t ob = sbase + LY::DO0 + qs * LY::TILE;
+                if (!(ok = issue_s(qb, kv))) break;
+                if (!(ok = issue_dp(ob, kv))) break;
+                for (int j = 0; j < w.hi; ++j) {
+                    const uint32_t nn = kv + j;
+                    if (j + 1 < w.hi && !(ok = issue_s(qb, nn + 1))) break;
+                    if (j == w.hi - 1) mma_commit(bar(QD_EMPTY + qs));   // after the last S / dP
+                    // dQ += dS(n) K'(n): dS packed over the dP columns
+                    if (j == 0 && !(ok = mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
+                    if (!(ok = mbar_wait(bar(DS_FULL), nn & 1, abort))) break;
                     tc_fence_after();
-                    const uint32_t kb = sbase + LY::K0 + ks * LY::TILEK;
-                    const uint32_t vb = sbase + LY::V0 + ks * LY::TILEK;
-                    // S = Q'K'^T and dP = dO V^T into step buffer b (last read by the dQ MMA of
-                    // step kv-2, issued earlier)
+                    const int ks = nn % kKStages;
+                    const uint32_t kb = sbase + LY::K0 + ks * LY::TILE;
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
-                        const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
-                        mma_bf16_ss(tmem + b * 128, smem_desc_sw128(qb + offq, 16, 1024),
-                                    smem_desc_sw128(kb + offk, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
-                        const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
-                        mma_bf16_ss(tmem + b * 128 + 64, smem_desc_sw128(ob + offq, 16, 1024),
-                                    smem_desc_sw128(vb + offk, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(SD_FULL + b));
-                    if (j == w.hi - 1) mma_commit(bar(QD_EMPTY + qs));
-                    if (j > 0 && !(ok = issue_dq(kv - 1, j == 1))) break;
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_bf16_ts(tmem + LY::DQ_COL, tmem + LY::DP_COL + ds_col(k),
+                                    smem_desc_sw128(kb + k * 16 * 128, LY::BLK, 1024), IDESC_DQ,
+                                    (j > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(bar(K_EMPTY + ks));
+                    if (j + 1 < w.hi && !(ok = issue_dp(ob, nn + 1))) break;
                 }
                 if (!ok) break;
-                if (!(ok = issue_dq(kv - 1, w.hi == 1))) break;
                 mma_commit(bar(ACC_FULL));
+                kv += w.hi;
             }
             mma_commit(bar(DRAIN));
             mbar_wait_limit(bar(DRAIN), 0, kDrainNs);
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ------------------------------------------------------------ dS + epilogue
-        const int g = (warp - 4) >> 2;             // math warpgroup: key columns [32g, 32g + 32)
+        // ------------------------------------------------------------ P, dS + epilogue
+        const int g = (warp - 4) >> 2;             // math warpgroup: key columns [64g, 64g + 64)
         const int wq = warp & 3;
         const int r = wq * 32 + lane;              // query row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float scale_log2 = p.scale * kLog2e;
-        const int c0 = 32 * g;
+        const int c0 = 64 * g;
         uint32_t unit_it = 0, kv = 0;
         bool ok = true;
         for (int n = 0; ok; ++n, ++unit_it) {
@@ -392,32 +415,55 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             const float dlt = valid ? __ldg(p.delta + static_cast<int64_t>(w.h) * p.total + tok) : 0.f;
             for (int j = 0; j < w.hi; ++j, ++kv) {
                 const int b = kv & 1;
-                if (!(ok = wait_warp(bar(SD_FULL + b), (kv >> 1) & 1, abort))) break;
+                // ---- phase A: P = exp2(s * scale_log2 - lse2) (masked), kept packed
+                if (!(ok = wait_warp(bar(S_FULL + b), (kv >> 1) & 1, abort))) break;
                 tc_fence_after();
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + b * 128 + c0, sr);
-                tmem_ld32(tmem + lane_off + b * 128 + 64 + c0, dr);
+                uint32_t sa[32], sb[32];
+                tmem_ld32(tmem + lane_off + b * 128 + c0, sa);
+                tmem_ld32(tmem + lane_off + b * 128 + c0 + 32, sb);
                 tmem_wait_ld();
-                // allowed key columns of this step: c <= lim (diagonal steps and the tail)
-                const bool edge = (j * BK + BK - 1 > w.tile * 128) || ((j + 1) * BK > w.L);
+                tc_fence_before();
+                mbar_arrive(bar(S_EMPTY + b));
+                const bool edge = (j == w.hi - 1);   // diagonal step (and the segment tail)
                 const int lim = !valid ? -1 : (edge ? min(qpos, w.L - 1) - j * BK : BK - 1);
                 const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
-                const float2 nd2 = make_float2(-dlt, -dlt);
-                uint32_t pk[16];
+                uint32_t pp[32];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
+                for (int e = 0; e < 64; e += 2) {
+                    const uint32_t* src = (e < 32) ? sa : sb;
+                    const int ee = e & 31;
+                    const float2 x = fma2(make_float2(__uint_as_float(src[ee]), __uint_as_float(src[ee + 1])),
+                                          sc2, nl2);
                     const int col = c0 + e;
-                    const float2 x = fma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, nl2);
                     const float p0 = (col <= lim) ? ex2_approx(x.x) : 0.f;
                     const float p1 = (col + 1 <= lim) ? ex2_approx(x.y) : 0.f;
-                    const float2 ds = mul2(make_float2(p0, p1),
-                                           add2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd2));
+                    pp[e >> 1] = pack_bf16x2(p0, p1);
+                }
+                // ---- phase B: dS = P (dP - D), packed over the consumed dP columns
+                if (!(ok = wait_warp(bar(DP_FULL), kv & 1, abort))) break;
+                tc_fence_after();
+                tmem_ld32(tmem + lane_off + LY::DP_COL + c0, sa);
+                tmem_ld32(tmem + lane_off + LY::DP_COL + c0 + 32, sb);
+                tmem_wait_ld();
+                const float2 nd2 = make_float2(-dlt, -dlt);
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const uint32_t* src = (e < 32) ? sa : sb;
+                    const int ee = e & 31;
+                    const float2 pv = make_float2(bf16_lo(pp[e >> 1]), bf16_hi(pp[e >> 1]));
+                    const float2 ds = mul2(pv, add2(make_float2(__uint_as_float(src[ee]),
+                                                                __uint_as_float(src[ee + 1])), nd2));
                     pk[e >> 1] = pack_bf16x2(ds.x, ds.y);
                 }
-                tmem_st16(tmem + lane_off + b * 128 + c0, pk);
+                uint32_t lo[16], hi[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) { lo[e] = pk[e]; hi[e] = pk[16 + e]; }
+                tmem_st16(tmem + lane_off + LY::DP_COL + c0, lo);
+                tmem_st16(tmem + lane_off + LY::DP_COL + c0 + 16, hi);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(DS_FULL + b));
+                mbar_arrive(bar(DS_FULL));
             }
             if (!ok) break;
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
@@ -435,17 +481,17 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     __syncthreads();
     if (*abort) {
         if (warp == 0 && lane == 0) {
-            for (int s = 0; s < kQSlots; ++s)
-                if (q_issued > static_cast<uint32_t>(s)) {
-                    const uint32_t nn = q_issued - 1 - ((q_issued - 1 - s) % kQSlots);
-                    mbar_wait_limit(bar(QD_FULL + s), (nn / kQSlots) & 1, kDrainNs);
+            for (int s2 = 0; s2 < kQSlots; ++s2)
+                if (q_issued > static_cast<uint32_t>(s2)) {
+                    const uint32_t nn = q_issued - 1 - ((q_issued - 1 - s2) % kQSlots);
+                    mbar_wait_limit(bar(QD_FULL + s2), (nn / kQSlots) & 1, kDrainNs);
                 }
-            for (int s = 0; s < kKStages; ++s)
-                if (kv_issued > static_cast<uint32_t>(s)) {
-                    const uint32_t nn = kv_issued - 1 - ((kv_issued - 1 - s) % kKStages);
-                    mbar_wait_limit(bar(K_FULL + s), (nn / kKStages) & 1, kDrainNs);
-                    mbar_wait_limit(bar(V_FULL + s), (nn / kKStages) & 1, kDrainNs);
+            for (int s2 = 0; s2 < kKStages; ++s2)
+                if (k_issued > static_cast<uint32_t>(s2)) {
+                    const uint32_t nn = k_issued - 1 - ((k_issued - 1 - s2) % kKStages);
+                    mbar_wait_limit(bar(K_FULL + s2), (nn / kKStages) & 1, kDrainNs);
                 }
+            if (v_issued > 0) mbar_wait_limit(bar(V_FULL), (v_issued - 1) & 1, kDrainNs);
         }
         if (threadIdx.x == 0) atomicOr(p.err, VLC_DEVERR_TIMEOUT);
         __syncthreads();
@@ -818,22 +864,20 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
     // with RoPE the attention passes read the rotated copies
     const void* qop = p.use_rope ? p.qrot : p.q;
     const void* kop = p.use_rope ? p.krot : p.k;
-    CUtensorMap q128, do128, k128, v128, q64, do64, k64, v64;
+    CUtensorMap q128, do128, k128, v128, q64, do64;
     if (!make_tmap_thd(&q128, qop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&do128, p.dout, p.total, p.H, D, 128) ||
         !make_tmap_thd(&k128, kop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&v128, p.v, p.total, p.H, D, 128) ||
         !make_tmap_thd(&q64, qop, p.total, p.H, D, bwd::dkdv::BQ) ||
-        !make_tmap_thd(&do64, p.dout, p.total, p.H, D, bwd::dkdv::BQ) ||
-        !make_tmap_thd(&k64, kop, p.total, p.H, D, bwd::dq::BK) ||
-        !make_tmap_thd(&v64, p.v, p.total, p.H, D, bwd::dq::BK))
+        !make_tmap_thd(&do64, p.dout, p.total, p.H, D, bwd::dkdv::BQ))
         return cudaErrorInvalidValue;
     {
         constexpr uint32_t smem = bwd::dq::Layout<D>::ALLOC;
         cudaError_t e = cudaFuncSetAttribute(bwd::dq::dq_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        bwd::dq::dq_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k64, v64, p);
+        bwd::dq::dq_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
     }
     {
         constexpr uint32_t smem = bwd::dkdv::Layout<D>::ALLOC;

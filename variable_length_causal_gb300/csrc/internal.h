@@ -10,7 +10,6 @@ constexpr int kFwdBM = 128;   // query rows per tile (dQ pass work list)
 constexpr int kFwdQB = 256;   // query rows per forward work unit (two q tiles)
 constexpr int kFwdBN = 128;   // key rows per forward tile
 constexpr int kBwdBM = 64;    // query rows per backward step
-constexpr int kBwdKN = 64;    // key rows per dQ-pass step
 constexpr int kTablePad = 128;  // RoPE table rows are padded to a multiple of this
 
 // Workspace header (first 256 bytes).
