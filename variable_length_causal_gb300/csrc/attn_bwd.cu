@@ -20,12 +20,14 @@
 //                  operand) into a TMEM dQ accumulator; epilogue applies scale
 //                  and R(p)^T and stores bf16.
 //   dkdv_kernel    key-major, one unit = (key tile of 128 rows, head): for every
-//                  q step of 64 rows from the diagonal to the segment end,
-//                  S^T = K'Q'^T and dP^T = V dO^T into TMEM (double buffered),
-//                  two warpgroups (32 q columns each) form P^T and dS^T and write
-//                  them back packed into TMEM, tcgen05 accumulates dV += P^T dO
-//                  and dK += dS^T Q' (tensor-memory A operands); a stager warp
-//                  prefetches LSE/delta; epilogue stores dV and R(p)^T dK.
+//                  q step of 128 rows from the diagonal to the segment end,
+//                  S^T = K'Q'^T and dP^T = V dO^T into TMEM; two warpgroups (64 q
+//                  columns each) form P^T as soon as S^T lands and dS^T once dP^T
+//                  lands, writing them back packed into TMEM; tcgen05 accumulates
+//                  dV += P^T dO and dK += dS^T Q' (tensor-memory A operands) in
+//                  the order dP^T(i) dV(i) S^T(i+1) dK(i) dP^T(i+1), so each math
+//                  phase has a two-MMA window; a stager warp prefetches LSE/delta;
+//                  epilogue stores dV and R(p)^T dK.
 // Both attention kernels are persistent (one CTA per SM), warp-specialised
 // like the forward (TMA warp, MMA warp, TMEM warp, 4 math warps, 4 hand-off
 // warps), and use only bounded waits.
@@ -507,16 +509,15 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
 // ====================================================================== dK/dV pass
 namespace dkdv {
 
-constexpr int BQ = kBwdBM;    // q rows per step
-static_assert(BQ == 64, "a step's S^T / dP^T take 64 TMEM columns each");
-constexpr int kQStages = 3;
+constexpr int BQ = 128;       // q rows per step (N = 128 keeps the S^T / dP^T MMAs at full rate)
+constexpr int kQStages = 2;
 constexpr int kLsedSlots = 3;
 
 enum : int {
     KV_FULL = 0, KV_EMPTY = 1,
     QO_FULL = 2, QO_EMPTY = 2 + kQStages,
-    ST_FULL = 2 + 2 * kQStages, PDS_FULL = ST_FULL + 2,
-    LSED_FULL = PDS_FULL + 2, LSED_EMPTY = LSED_FULL + kLsedSlots,
+    ST_FULL = 2 + 2 * kQStages, DPT_FULL = ST_FULL + 1, PT_FULL = ST_FULL + 2, DST_FULL = ST_FULL + 3,
+    LSED_FULL = ST_FULL + 4, LSED_EMPTY = LSED_FULL + kLsedSlots,
     ACC_FULL = LSED_EMPTY + kLsedSlots, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2,
     UNIT_FULL = ACC_FULL + 3, UNIT_EMPTY = UNIT_FULL + kRing, NUM_BARS = UNIT_EMPTY + kRing
 };
@@ -524,22 +525,20 @@ enum : int {
 template <int D>
 struct Layout {
     static constexpr int KB = D / 64;
-    static constexpr uint32_t BLKK = 128u * 128u;       // key-side block: 128 rows x 128 B
-    static constexpr uint32_t TILEK = 128u * D * 2u;
-    static constexpr uint32_t BLKQ = BQ * 128u;          // q-side block: 64 rows x 128 B
-    static constexpr uint32_t TILEQ = BQ * D * 2u;
+    static constexpr uint32_t BLK = 128u * 128u;        // 128 rows x 128 B
+    static constexpr uint32_t TILE = 128u * D * 2u;
     static constexpr uint32_t K0 = 0;
-    static constexpr uint32_t V0 = TILEK;
-    static constexpr uint32_t Q0 = 2 * TILEK;                  // kQStages stages
-    static constexpr uint32_t DO0 = Q0 + kQStages * TILEQ;     // kQStages stages
-    static constexpr uint32_t LSED = DO0 + kQStages * TILEQ;   // kLsedSlots x (64 lse2 + 64 delta)
-    static constexpr uint32_t BAR0 = LSED + kLsedSlots * 128 * 4;
+    static constexpr uint32_t V0 = TILE;
+    static constexpr uint32_t Q0 = 2 * TILE;                   // kQStages stages
+    static constexpr uint32_t DO0 = Q0 + kQStages * TILE;      // kQStages stages
+    static constexpr uint32_t LSED = DO0 + kQStages * TILE;    // kLsedSlots x (128 lse2 + 128 delta)
+    static constexpr uint32_t BAR0 = LSED + kLsedSlots * 256 * 4;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;      // tmem slot, abort flag, unit ring
     static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
-    // TMEM: step buffer b at columns 128b: S^T (64 fp32 columns) then dP^T (64); the
-    // packed bf16 P^T / dS^T of a step overwrite the consumed S^T / dP^T columns.
-    static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
+    // TMEM: S^T at 0, dP^T at 128 (the packed bf16 P^T / dS^T of a step overwrite the
+    // consumed S^T / dP^T columns), dV and dK accumulators after them.
+    static constexpr uint32_t DPT_COL = 128, DV_COL = 256, DK_COL = 256 + D;
 };
 
 template <int D>
@@ -575,10 +574,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             mbar_init(bar(QO_FULL + i), 1);
             mbar_init(bar(QO_EMPTY + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(ST_FULL + i), 1);
-            mbar_init(bar(PDS_FULL + i), 256);
-        }
+        mbar_init(bar(ST_FULL), 1);
+        mbar_init(bar(DPT_FULL), 1);
+        mbar_init(bar(PT_FULL), 256);
+        mbar_init(bar(DST_FULL), 256);
         for (int i = 0; i < kLsedSlots; ++i) {
             mbar_init(bar(LSED_FULL + i), 1);
             mbar_init(bar(LSED_EMPTY + i), 8);
@@ -614,24 +613,24 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 if (!(ok = ring_put(rg, n, p.next_k, nunits, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
                 if (!(ok = mbar_wait(bar(KV_EMPTY), (unit_it & 1) ^ 1, abort))) break;
-                mbar_expect_tx(bar(KV_FULL), 2 * LY::TILEK);
+                mbar_expect_tx(bar(KV_FULL), 2 * LY::TILE);
                 const int krow = w.row0 + w.tile * 128;
 #pragma unroll
                 for (int kb = 0; kb < LY::KB; ++kb) {
-                    tma_load_3d_hint(sbase + LY::K0 + kb * LY::BLKK, &tmK, kb * 64, w.h, krow, bar(KV_FULL), pol_stream);
-                    tma_load_3d_hint(sbase + LY::V0 + kb * LY::BLKK, &tmV, kb * 64, w.h, krow, bar(KV_FULL), pol_stream);
+                    tma_load_3d_hint(sbase + LY::K0 + kb * LY::BLK, &tmK, kb * 64, w.h, krow, bar(KV_FULL), pol_stream);
+                    tma_load_3d_hint(sbase + LY::V0 + kb * LY::BLK, &tmV, kb * 64, w.h, krow, bar(KV_FULL), pol_stream);
                 }
                 kv_issued = unit_it + 1;
                 for (int i = w.lo; i < w.hi && ok; ++i, ++qo) {
                     const int s = qo % kQStages;
                     if (!(ok = mbar_wait(bar(QO_EMPTY + s), ((qo / kQStages) & 1) ^ 1, abort))) break;
-                    mbar_expect_tx(bar(QO_FULL + s), 2 * LY::TILEQ);
+                    mbar_expect_tx(bar(QO_FULL + s), 2 * LY::TILE);
                     const int qrow = w.row0 + i * BQ;
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb) {
-                        tma_load_3d_hint(sbase + LY::Q0 + s * LY::TILEQ + kb * LY::BLKQ, &tmQ, kb * 64, w.h,
+                        tma_load_3d_hint(sbase + LY::Q0 + s * LY::TILE + kb * LY::BLK, &tmQ, kb * 64, w.h,
                                          qrow, bar(QO_FULL + s), pol_keep);
-                        tma_load_3d_hint(sbase + LY::DO0 + s * LY::TILEQ + kb * LY::BLKQ, &tmDO, kb * 64, w.h,
+                        tma_load_3d_hint(sbase + LY::DO0 + s * LY::TILE + kb * LY::BLK, &tmDO, kb * 64, w.h,
                                          qrow, bar(QO_FULL + s), pol_keep);
                     }
                     q_issued = qo + 1;
@@ -645,59 +644,66 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, true);
             uint32_t unit_it = 0, st = 0;
             bool ok = true;
-            // dV += P^T dO and dK += dS^T Q' for step sp (A operands packed in TMEM)
-            auto issue_acc = [&](uint32_t sp, bool first) -> bool {
-                const int b = sp & 1, s = sp % kQStages;
-                if (first && !mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort)) return false;
-                if (!mbar_wait(bar(PDS_FULL + b), (sp >> 1) & 1, abort)) return false;
+            // S^T = K'Q'(step)^T into columns 0..127 (read by dV of the previous step,
+            // issued earlier); dP^T = V dO(step)^T into 128..255 (read by dK before).
+            auto issue_st = [&](uint32_t sp) -> bool {
+                const int s = sp % kQStages;
+                if (!mbar_wait(bar(QO_FULL + s), (sp / kQStages) & 1, abort)) return false;
                 tc_fence_after();
-                const uint32_t qb = sbase + LY::Q0 + s * LY::TILEQ;
-                const uint32_t ob = sbase + LY::DO0 + s * LY::TILEQ;
+                const uint32_t qb = sbase + LY::Q0 + s * LY::TILE;
 #pragma unroll
-                for (int k = 0; k < BQ / 16; ++k)
-                    mma_bf16_ts(tmem + LY::DV_COL, tmem + b * 128 + packed_col(k),
-                                smem_desc_sw128(ob + k * 16 * 128, LY::BLKQ, 1024), IDESC_ACC,
-                                (!first || k > 0) ? 1u : 0u);
-#pragma unroll
-                for (int k = 0; k < BQ / 16; ++k)
-                    mma_bf16_ts(tmem + LY::DK_COL, tmem + b * 128 + 64 + packed_col(k),
-                                smem_desc_sw128(qb + k * 16 * 128, LY::BLKQ, 1024), IDESC_ACC,
-                                (!first || k > 0) ? 1u : 0u);
-                mma_commit(bar(QO_EMPTY + s));
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
+                    mma_bf16_ss(tmem, smem_desc_sw128(sbase + LY::K0 + off, 16, 1024),
+                                smem_desc_sw128(qb + off, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(ST_FULL));
                 return true;
+            };
+            auto issue_dpt = [&](uint32_t sp) {
+                const int s = sp % kQStages;
+                const uint32_t ob = sbase + LY::DO0 + s * LY::TILE;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
+                    mma_bf16_ss(tmem + LY::DPT_COL, smem_desc_sw128(sbase + LY::V0 + off, 16, 1024),
+                                smem_desc_sw128(ob + off, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(DPT_FULL));
             };
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
                 if (!(ok = mbar_wait(bar(KV_FULL), unit_it & 1, abort))) break;
+                if (!(ok = issue_st(st))) break;
+                issue_dpt(st);
                 for (int i = w.lo; i < w.hi; ++i, ++st) {
-                    const int s = st % kQStages, b = st & 1;
-                    if (!(ok = mbar_wait(bar(QO_FULL + s), (st / kQStages) & 1, abort))) break;
+                    const int s = st % kQStages;
+                    const uint32_t qb = sbase + LY::Q0 + s * LY::TILE;
+                    const uint32_t ob = sbase + LY::DO0 + s * LY::TILE;
+                    // dV += P^T dO (P^T packed over the S^T columns)
+                    if (i == w.lo && !(ok = mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
+                    if (!(ok = mbar_wait(bar(PT_FULL), st & 1, abort))) break;
                     tc_fence_after();
-                    const uint32_t qb = sbase + LY::Q0 + s * LY::TILEQ;
-                    const uint32_t ob = sbase + LY::DO0 + s * LY::TILEQ;
-                    // S^T = K' Q'^T and dP^T = V dO^T into step buffer b; buffer b was last
-                    // read by the dV/dK MMAs of step st-2, issued earlier (in-order).
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
-                        const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
-                        mma_bf16_ss(tmem + b * 128, smem_desc_sw128(sbase + LY::K0 + offk, 16, 1024),
-                                    smem_desc_sw128(qb + offq, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
-                    }
+                    for (int k = 0; k < BQ / 16; ++k)
+                        mma_bf16_ts(tmem + LY::DV_COL, tmem + dq::ds_col(k),
+                                    smem_desc_sw128(ob + k * 16 * 128, LY::BLK, 1024), IDESC_ACC,
+                                    (i > w.lo || k > 0) ? 1u : 0u);
+                    if (i + 1 < w.hi && !(ok = issue_st(st + 1))) break;
+                    // dK += dS^T Q' (dS^T packed over the dP^T columns)
+                    if (!(ok = mbar_wait(bar(DST_FULL), st & 1, abort))) break;
+                    tc_fence_after();
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t offk = (k >> 2) * LY::BLKK + (k & 3) * 32;
-                        const uint32_t offq = (k >> 2) * LY::BLKQ + (k & 3) * 32;
-                        mma_bf16_ss(tmem + b * 128 + 64, smem_desc_sw128(sbase + LY::V0 + offk, 16, 1024),
-                                    smem_desc_sw128(ob + offq, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(ST_FULL + b));
-                    if (i > w.lo && !(ok = issue_acc(st - 1, i == w.lo + 1))) break;
+                    for (int k = 0; k < BQ / 16; ++k)
+                        mma_bf16_ts(tmem + LY::DK_COL, tmem + LY::DPT_COL + dq::ds_col(k),
+                                    smem_desc_sw128(qb + k * 16 * 128, LY::BLK, 1024), IDESC_ACC,
+                                    (i > w.lo || k > 0) ? 1u : 0u);
+                    mma_commit(bar(QO_EMPTY + s));
+                    if (i + 1 < w.hi) issue_dpt(st + 1);
                 }
                 if (!ok) break;
-                if (!(ok = issue_acc(st - 1, w.hi - w.lo == 1))) break;
                 mma_commit(bar(ACC_FULL));
                 mma_commit(bar(KV_EMPTY));
             }
@@ -716,10 +722,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             for (int i = w.lo; i < w.hi && ok; ++i, ++st) {
                 const int sl = st % kLsedSlots;
                 if (!(ok = wait_warp(bar(LSED_EMPTY + sl), ((st / kLsedSlots) & 1) ^ 1, abort))) break;
-                float* dst = lsed + sl * 128;
+                float* dst = lsed + sl * 256;
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int q = lane + 32 * h2;
+                for (int h4 = 0; h4 < 4; ++h4) {
+                    const int q = lane + 32 * h4;
                     const int qq = i * BQ + q;
                     float l2 = 0.f, dl = 0.f;
                     if (qq < w.L) {
@@ -728,7 +734,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                         dl = __ldg(p.delta + idx);
                     }
                     dst[q] = l2;
-                    dst[64 + q] = dl;
+                    dst[128 + q] = dl;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(LSED_FULL + sl));
@@ -736,12 +742,12 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ P^T, dS^T + epilogue
-        const int g = (warp - 4) >> 2;             // math warpgroup: q columns [32g, 32g + 32)
+        const int g = (warp - 4) >> 2;             // math warpgroup: q columns [64g, 64g + 64)
         const int wq = warp & 3;
         const int r = wq * 32 + lane;              // key row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float scale_log2 = p.scale * kLog2e;
-        const int c0 = 32 * g;
+        const int c0 = 64 * g;
         uint32_t unit_it = 0, st = 0;
         bool ok = true;
         for (int n = 0; ok; ++n, ++unit_it) {
@@ -750,51 +756,77 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
             const int kvpos = w.tile * 128 + r;
             for (int i = w.lo; i < w.hi; ++i, ++st) {
-                const int b = st & 1, sl = st % kLsedSlots;
+                const int sl = st % kLsedSlots;
+                const float* l2s = lsed + sl * 256 + c0;
+                const float* dls = lsed + sl * 256 + 128 + c0;
                 if (!(ok = wait_warp(bar(LSED_FULL + sl), (st / kLsedSlots) & 1, abort))) break;
-                float l2[32], dl[32];
-                {
-                    const float4* src = reinterpret_cast<const float4*>(lsed + sl * 128 + c0);
+                // allowed q columns: kvpos <= i*BQ + col and i*BQ + col < L
+                const bool edge = (i == w.lo) || ((i + 1) * BQ > w.L);
+                const int c_lo = kvpos - i * BQ, c_hi = w.L - 1 - i * BQ;
+                // ---- phase A: P^T = exp2(s * scale_log2 - lse2) over this group's 64 columns
+                if (!(ok = wait_warp(bar(ST_FULL), st & 1, abort))) break;
+                tc_fence_after();
+                uint32_t pp[32];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 a = src[e], d4 = src[16 + e];
-                        l2[4 * e] = a.x; l2[4 * e + 1] = a.y; l2[4 * e + 2] = a.z; l2[4 * e + 3] = a.w;
-                        dl[4 * e] = d4.x; dl[4 * e + 1] = d4.y; dl[4 * e + 2] = d4.z; dl[4 * e + 3] = d4.w;
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t sr[32];
+                    tmem_ld32(tmem + lane_off + c0 + 32 * h, sr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int col = c0 + 32 * h + e;
+                        const float2 lz = *reinterpret_cast<const float2*>(l2s + 32 * h + e);
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                              make_float2(scale_log2, scale_log2), make_float2(-lz.x, -lz.y));
+                        float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                        if (edge) {
+                            if (col < c_lo || col > c_hi) p0 = 0.f;
+                            if (col + 1 < c_lo || col + 1 > c_hi) p1 = 0.f;
+                        }
+                        pp[16 * h + (e >> 1)] = pack_bf16x2(p0, p1);
+                    }
+                }
+                {
+                    uint32_t lo[16], hi[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) { lo[e] = pp[e]; hi[e] = pp[16 + e]; }
+                    tmem_st16(tmem + lane_off + c0, lo);
+                    tmem_st16(tmem + lane_off + c0 + 16, hi);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(PT_FULL));
+                // ---- phase B: dS^T = P^T (dP^T - D), packed over the consumed dP^T columns
+                if (!(ok = wait_warp(bar(DPT_FULL), st & 1, abort))) break;
+                tc_fence_after();
+                uint32_t pd[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t dr[32];
+                    tmem_ld32(tmem + lane_off + LY::DPT_COL + c0 + 32 * h, dr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 dz = *reinterpret_cast<const float2*>(dls + 32 * h + e);
+                        const uint32_t pv = pp[16 * h + (e >> 1)];
+                        const float2 ds = mul2(make_float2(bf16_lo(pv), bf16_hi(pv)),
+                                               make_float2(__uint_as_float(dr[e]) - dz.x,
+                                                           __uint_as_float(dr[e + 1]) - dz.y));
+                        pd[16 * h + (e >> 1)] = pack_bf16x2(ds.x, ds.y);
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(LSED_EMPTY + sl));
-                if (!(ok = wait_warp(bar(ST_FULL + b), (st >> 1) & 1, abort))) break;
-                tc_fence_after();
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_off + b * 128 + c0, sr);
-                tmem_ld32(tmem + lane_off + b * 128 + 64 + c0, dr);
-                tmem_wait_ld();
-                // allowed q columns: kvpos <= i*BQ + col and i*BQ + col < L
-                const bool edge = (i * BQ < w.tile * 128 + 128) || ((i + 1) * BQ > w.L);
-                const int c_lo = kvpos - i * BQ, c_hi = w.L - 1 - i * BQ;
-                uint32_t pp[16], pd[16];
+                {
+                    uint32_t lo[16], hi[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int col = c0 + e;
-                    const float2 x = fma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                          make_float2(scale_log2, scale_log2), make_float2(-l2[e], -l2[e + 1]));
-                    float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-                    if (edge) {
-                        if (col < c_lo || col > c_hi) p0 = 0.f;
-                        if (col + 1 < c_lo || col + 1 > c_hi) p1 = 0.f;
-                    }
-                    const float2 dsv = mul2(make_float2(p0, p1),
-                                            make_float2(__uint_as_float(dr[e]) - dl[e],
-                                                        __uint_as_float(dr[e + 1]) - dl[e + 1]));
-                    pp[e >> 1] = pack_bf16x2(p0, p1);
-                    pd[e >> 1] = pack_bf16x2(dsv.x, dsv.y);
+                    for (int e = 0; e < 16; ++e) { lo[e] = pd[e]; hi[e] = pd[16 + e]; }
+                    tmem_st16(tmem + lane_off + LY::DPT_COL + c0, lo);
+                    tmem_st16(tmem + lane_off + LY::DPT_COL + c0 + 16, hi);
                 }
-                tmem_st16(tmem + lane_off + b * 128 + c0, pp);
-                tmem_st16(tmem + lane_off + b * 128 + 64 + c0, pd);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(PDS_FULL + b));
+                mbar_arrive(bar(DST_FULL));
             }
             if (!ok) break;
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
@@ -832,10 +864,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     if (*abort) {
         if (warp == 0 && lane == 0) {
             if (kv_issued > 0) mbar_wait_limit(bar(KV_FULL), (kv_issued - 1) & 1, kDrainNs);
-            for (int s = 0; s < kQStages; ++s)
-                if (q_issued > static_cast<uint32_t>(s)) {
-                    const uint32_t nn = q_issued - 1 - ((q_issued - 1 - s) % kQStages);
-                    mbar_wait_limit(bar(QO_FULL + s), (nn / kQStages) & 1, kDrainNs);
+            for (int s2 = 0; s2 < kQStages; ++s2)
+                if (q_issued > static_cast<uint32_t>(s2)) {
+                    const uint32_t nn = q_issued - 1 - ((q_issued - 1 - s2) % kQStages);
+                    mbar_wait_limit(bar(QO_FULL + s2), (nn / kQStages) & 1, kDrainNs);
                 }
         }
         if (threadIdx.x == 0) atomicOr(p.err, VLC_DEVERR_TIMEOUT);
@@ -864,13 +896,11 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
     // with RoPE the attention passes read the rotated copies
     const void* qop = p.use_rope ? p.qrot : p.q;
     const void* kop = p.use_rope ? p.krot : p.k;
-    CUtensorMap q128, do128, k128, v128, q64, do64;
+    CUtensorMap q128, do128, k128, v128;
     if (!make_tmap_thd(&q128, qop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&do128, p.dout, p.total, p.H, D, 128) ||
         !make_tmap_thd(&k128, kop, p.total, p.H, D, 128) ||
-        !make_tmap_thd(&v128, p.v, p.total, p.H, D, 128) ||
-        !make_tmap_thd(&q64, qop, p.total, p.H, D, bwd::dkdv::BQ) ||
-        !make_tmap_thd(&do64, p.dout, p.total, p.H, D, bwd::dkdv::BQ))
+        !make_tmap_thd(&v128, p.v, p.total, p.H, D, 128))
         return cudaErrorInvalidValue;
     {
         constexpr uint32_t smem = bwd::dq::Layout<D>::ALLOC;
@@ -884,7 +914,7 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
         cudaError_t e = cudaFuncSetAttribute(bwd::dkdv::dkdv_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        bwd::dkdv::dkdv_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q64, do64, k128, v128, p);
+        bwd::dkdv::dkdv_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
     }
     return cudaGetLastError();
 }

@@ -9,7 +9,7 @@ namespace vlc {
 constexpr int kFwdBM = 128;   // query rows per tile (dQ pass work list)
 constexpr int kFwdQB = 256;   // query rows per forward work unit (two q tiles)
 constexpr int kFwdBN = 128;   // key rows per forward tile
-constexpr int kBwdBM = 64;    // query rows per backward step
+constexpr int kBwdBM = 128;   // query rows per backward (key-major pass) step
 constexpr int kTablePad = 128;  // RoPE table rows are padded to a multiple of this
 
 // Workspace header (first 256 bytes).
