@@ -50,6 +50,17 @@ constexpr int kThreads = 512;
 constexpr int kQSlots = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr uint32_t kLaunchRegs = 65536 / kThreads;   // registers per thread at launch
+#ifndef VLC_FWD_CTRL_REGS
+#define VLC_FWD_CTRL_REGS 88
+#define VLC_FWD_ROPE_REGS 72
+#endif
+// per-thread registers of each warpgroup after the split: producer/MMA/TMEM,
+// RoPE, and the two softmax warpgroups
+constexpr uint32_t kCtrlRegs = VLC_FWD_CTRL_REGS, kRopeRegs = VLC_FWD_ROPE_REGS;
+constexpr uint32_t kSoftmaxRegs = (4 * kLaunchRegs - kCtrlRegs - kRopeRegs) / 2 / 8 * 8;
+static_assert(kCtrlRegs % 8 == 0 && kRopeRegs % 8 == 0, "register counts are multiples of 8");
+static_assert(kCtrlRegs + kRopeRegs + 2 * kSoftmaxRegs <= 4 * kLaunchRegs, "register split exceeds the pool");
 constexpr float kLn2 = 0.69314718055994530942f;
 
 enum : int {
@@ -157,8 +168,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     uint32_t q_issued = 0, k_issued = 0, kv_issued = 0;   // for the teardown drain
 
+    // Softmax warpgroups hold a whole S row per thread; the producer/MMA/TMEM and
+    // RoPE warpgroups give registers up for them (each role sets its budget first).
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        setmaxnreg_dec<kCtrlRegs>();
         if (lane == 0) {
             const uint64_t pol_stream = make_l2_policy_evict_first();   // q: read once
             const uint64_t pol_keep = make_l2_policy_evict_last();      // K/V: read by many units
@@ -211,19 +225,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        setmaxnreg_dec<kCtrlRegs>();
         if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false);
             constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
             uint32_t qm = 0, kvn = 0, cnt_p[2] = {0, 0}, cnt_u[2] = {0, 0};
             bool ok = true;
+            // Descriptors are built once per tile; the K-step offsets are added to the
+            // start-address field (addresses stay below 2^18, so the field cannot carry).
             auto issue_s = [&](int t, int slot, int ks) {
-                const uint32_t qb = sbase + LY::Q0 + slot * LY::TILE;
-                const uint32_t kb = sbase + LY::K0 + ks * LY::TILE;
+                const uint64_t qd = smem_desc_sw128(sbase + LY::Q0 + slot * LY::TILE, 16, 1024);
+                const uint64_t kd = smem_desc_sw128(sbase + LY::K0 + ks * LY::TILE, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
-                    mma_bf16_ss(tmem + LY::S_COL(t), smem_desc_sw128(qb + off, 16, 1024),
-                                smem_desc_sw128(kb + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                    const uint32_t off = ((k >> 2) * LY::BLK + (k & 3) * 32) >> 4;
+                    mma_bf16_ss(tmem + LY::S_COL(t), qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(S_FULL + t));
             };
@@ -258,12 +274,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         ++cnt_p[t];
                         if (j == 0 && !(ok = mbar_wait(bar(O_EMPTY + t), (cnt_u[t] & 1) ^ 1, abort))) break;
                         tc_fence_after();
-                        const uint32_t vb = sbase + LY::V0 + vs * LY::TILE;
+                        const uint64_t vd = smem_desc_sw128(sbase + LY::V0 + vs * LY::TILE, LY::BLK, 1024);
 #pragma unroll
                         for (int k = 0; k < BN / 16; ++k)
                             mma_bf16_ts(tmem + LY::O_COL(t), tmem + LY::S_COL(t) + 8 * k,
-                                        smem_desc_sw128(vb + k * 16 * 128, LY::BLK, 1024), IDESC_O,
-                                        (j > 0 || k > 0) ? 1u : 0u);
+                                        vd + ((k * 16 * 128) >> 4), IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
                         if (j == n[t] - 1) mma_commit(bar(O_FULL + t));
                         if (j + 1 < n[t]) {
                             const uint32_t kvn1 = kvj + 1;
@@ -292,6 +307,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         __syncwarp();
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ softmax + epilogue
+        setmaxnreg_inc<kSoftmaxRegs>();
         const int t = (warp - 4) >> 2;             // q tile slot handled by this warpgroup
         const int wq = warp & 3;                   // TMEM lane quadrant
         const int r = wq * 32 + lane;              // query row in the tile = TMEM lane
@@ -316,32 +332,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // allowed key columns of this tile: c <= lim (only the last tile is masked)
                 const bool edge = (j == nt - 1);
                 const int lim = edge ? min(qpos, f.w.L - 1) - j * BN : BN - 1;
-                // pass 1: row max of the raw scores (two 32-column loads in flight)
-                float mx = -INFINITY;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; c += 2) {
-                    uint32_t ra[32], rb[32];
-                    tmem_ld32(sadr + c * 32, ra);
-                    tmem_ld32(sadr + c * 32 + 32, rb);
-                    tmem_wait_ld();
-                    if (edge) {
+                // the thread's whole S row (BN fp32 columns) in registers: four loads, one wait
+                uint32_t s[BN];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            mx = fmaxf(mx, (c * 32 + e <= lim) ? __uint_as_float(ra[e]) : -INFINITY);
-                            mx = fmaxf(mx, (c * 32 + 32 + e <= lim) ? __uint_as_float(rb[e]) : -INFINITY);
-                        }
-                    } else {   // four independent 3-input max chains
-                        float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
+                for (int c = 0; c < BN / 32; ++c)
+                    tmem_ld32(sadr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(s + c * 32));
+                tmem_wait_ld();
+                if (edge) {   // masked scores -> -inf: they drop out of the max and exp2 gives 0
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            m4[(e >> 1) & 1] = fmax3(m4[(e >> 1) & 1], __uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
-                            m4[2 + ((e >> 1) & 1)] = fmax3(m4[2 + ((e >> 1) & 1)], __uint_as_float(rb[e]),
-                                                           __uint_as_float(rb[e + 1]));
-                        }
-                        mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-                    }
+                    for (int e = 0; e < BN; ++e)
+                        if (e > lim) s[e] = 0xff800000u;
                 }
-                const float mt = mx * sl2;
+                // row max of the raw scores: four independent 3-input max chains
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < BN; e += 8) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        m4[q] = fmax3(m4[q], __uint_as_float(s[e + 2 * q]), __uint_as_float(s[e + 2 * q + 1]));
+                }
+                const float mt = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * sl2;
                 float m_use = m_run, alpha = 1.f;
                 bool rescale = false;
                 if (j == 0) {
@@ -352,6 +362,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         m_use = fmaxf(m_run, mt);
                         alpha = ex2_approx(m_run - m_use);
                     }
+                }
+                // P = exp2(s * scale_log2 - m) -> bf16 pairs written over the first BN/2
+                // S columns, each half as soon as it is packed
+                const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
+                float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    uint32_t pk[BN / 4];
+#pragma unroll
+                    for (int e = 0; e < BN / 4; ++e) {
+                        const int c = hlf * (BN / 2) + 2 * e;
+                        const float2 x = fma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
+                        const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                        rs2[e & 1] = add2(rs2[e & 1], make_float2(p0, p1));
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(sadr + hlf * (BN / 4), pk);
                 }
                 if (rescale) {   // O_t is stable: S_t(j) done implies P_t V(j-1) done
 #pragma unroll 1
@@ -366,46 +393,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                     l_run *= alpha;
                 }
-                // pass 2: P = exp2(s * scale_log2 - m), bf16, written over consumed S columns;
-                // the next chunk's load is in flight while this chunk is exponentiated.
-                const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
-                float2 rs2 = make_float2(0.f, 0.f);
-                uint32_t rr[32];
-                tmem_ld32(sadr, rr);
-                tmem_wait_ld();
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t cur[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) cur[e] = rr[e];
-                    if (c + 1 < BN / 32) tmem_ld32(sadr + (c + 1) * 32, rr);
-                    uint32_t pk[16];
-                    if (edge) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 x = fma2(make_float2(__uint_as_float(cur[2 * e]),
-                                                              __uint_as_float(cur[2 * e + 1])), sc2, nm2);
-                            const int col = c * 32 + 2 * e;
-                            const float p0 = (col <= lim) ? ex2_approx(x.x) : 0.f;
-                            const float p1 = (col + 1 <= lim) ? ex2_approx(x.y) : 0.f;
-                            rs2 = add2(rs2, make_float2(p0, p1));
-                            pk[e] = pack_bf16x2(p0, p1);
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float2 x = fma2(make_float2(__uint_as_float(cur[2 * e]),
-                                                              __uint_as_float(cur[2 * e + 1])), sc2, nm2);
-                            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-                            rs2 = add2(rs2, make_float2(p0, p1));
-                            pk[e] = pack_bf16x2(p0, p1);
-                        }
-                    }
-                    tmem_st16(sadr + c * 16, pk);
-                    tmem_wait_ld();
-                }
                 tmem_wait_st();
-                l_run += rs2.x + rs2.y;
+                l_run += (rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y);
                 m_run = m_use;
                 tc_fence_before();
                 mbar_arrive(bar(P_FULL + t));
@@ -450,6 +439,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ RoPE on staged q / K tiles
+        setmaxnreg_dec<kRopeRegs>();
         const int wr = warp - 12;
         RopeStep<D> step{};
         if (p.use_rope) step = rope_step<D>(p.table, lane);
@@ -479,6 +469,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ++kvn;
             }
         }
+    } else {
+        setmaxnreg_dec<kCtrlRegs>();   // warps 2 and 3: TMEM allocator and spare
     }
 
     __syncthreads();
@@ -523,6 +515,15 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
         !make_tmap_thd(&tv, p.v, p.total, p.H, p.d, 128))
         return cudaErrorInvalidValue;
     const dim3 grid(num_sms), block(fwd::kThreads);
+    // The warpgroups re-split the block's register pool at run time, which is only
+    // valid if every thread is launched with exactly kLaunchRegs registers.
+    {
+        cudaFuncAttributes fa{};
+        cudaError_t e = p.d == 128 ? cudaFuncGetAttributes(&fa, fwd::attn_fwd_kernel<128>)
+                                   : cudaFuncGetAttributes(&fa, fwd::attn_fwd_kernel<64>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(fwd::kLaunchRegs)) return cudaErrorInvalidConfiguration;
+    }
     if (p.d == 128) {
         constexpr uint32_t smem = fwd::Layout<128>::ALLOC;
         cudaError_t e = cudaFuncSetAttribute(fwd::attn_fwd_kernel<128>,

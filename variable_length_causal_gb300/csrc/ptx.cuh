@@ -8,6 +8,9 @@
 namespace vlc {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+// A waiting thread sleeps (instead of polling) until the phase completes or this
+// many ns pass, so waiting warps leave their scheduler's issue slots to the others.
+constexpr uint32_t kTryWaitSuspendNs = 1000000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -41,10 +44,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kTryWaitSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -252,6 +255,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
            | ((b_mn_major ? 1u : 0u) << 16)
            | (static_cast<uint32_t>(N >> 3) << 17)
            | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute the same
+// call).  The block's pool is fixed at launch (threads x registers per thread);
+// increases wait for decreases elsewhere, so a split must sum to at most the pool.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ scalar helpers
