@@ -41,6 +41,7 @@ __device__ __forceinline__ Unit decode_unit(const int4* __restrict__ items,
 
 // All 32 lanes poll; succeed together or give up together.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
     uint64_t t0 = 0;
     const int lane = threadIdx.x & 31;
 #pragma unroll 1

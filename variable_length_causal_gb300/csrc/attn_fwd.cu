@@ -13,9 +13,10 @@
 // diagonal key tiles, and a q tile stops at its own diagonal key tile.  Units
 // are claimed dynamically (longest first) from a global counter and handed to
 // every role through a shared-memory ring.
-//   warp 0       TMA producer: q tiles into a 3-slot ring, K/V tiles into 2
-//                stages, 128-byte swizzle.
-//   warp 1       MMA issuer (one thread), tcgen05.mma kind::f16, fp32 in TMEM:
+//   warp 0       TMA producer of q tiles (3-slot ring) and K tiles (2 stages),
+//                128-byte swizzle; warp 3 the same for V tiles (2 stages).
+//   warp 1       MMA issuer (one elected lane of the converged warp), tcgen05.mma
+//                kind::f16, fp32 accumulators in TMEM:
 //                S_t = Q'_t K'^T (shared-memory operands) and O_t += P_t V with
 //                P_t read from TMEM; issue order S0 S1 | PV0(j) S0(j+1)
 //                PV1(j) S1(j+1) | ..., so each q tile's softmax overlaps the
@@ -118,7 +119,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr int kRingConsumers = 1 + 8 + 4;   // MMA thread, 8 softmax warps, 4 RoPE warps
+    constexpr int kRingConsumers = 1 + 1 + 8 + 4;   // MMA warp, V producer, 8 softmax warps, 4 RoPE warps
 
     __shared__ int s_skip, s_nunits;
     if (threadIdx.x == 0) {   // one read, so every thread takes the same branch
@@ -193,31 +194,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                          f.w.h, row, bar(Q_FULL + slot), pol_stream);
                     q_issued = ++qm;
                 }
-                // K tile j is loaded one step ahead of V tile j-1, so the RoPE warps
-                // can rotate K while the MMAs of the previous tile still read V.
-                for (int j = 0; j <= f.w.hi && ok; ++j) {
-                    if (j < f.w.hi) {
-                        const uint32_t n = kvn + j;
-                        const int ks = n & 1;
-                        if (!(ok = mbar_wait(bar(K_EMPTY + ks), ((n >> 1) & 1) ^ 1, abort))) break;
-                        mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
+                // K tiles only: V tiles come from their own producer (warp 3), so a V
+                // load never waits behind a K stage and vice versa.
+                for (int j = 0; j < f.w.hi && ok; ++j) {
+                    const uint32_t n = kvn + j;
+                    const int ks = n & 1;
+                    if (!(ok = mbar_wait(bar(K_EMPTY + ks), ((n >> 1) & 1) ^ 1, abort))) break;
+                    mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
 #pragma unroll
-                        for (int kb = 0; kb < LY::KB; ++kb)
-                            tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
-                                             f.w.h, f.w.row0 + j * BN, bar(K_FULL + ks), pol_keep);
-                        k_issued = n + 1;
-                    }
-                    if (j >= 1) {
-                        const uint32_t n = kvn + j - 1;
-                        const int vs = n & 1;
-                        if (!(ok = mbar_wait(bar(V_EMPTY + vs), ((n >> 1) & 1) ^ 1, abort))) break;
-                        mbar_expect_tx(bar(V_FULL + vs), LY::TILE);
-#pragma unroll
-                        for (int kb = 0; kb < LY::KB; ++kb)
-                            tma_load_3d_hint(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
-                                             f.w.h, f.w.row0 + (j - 1) * BN, bar(V_FULL + vs), pol_keep);
-                        kv_issued = n + 1;
-                    }
+                    for (int kb = 0; kb < LY::KB; ++kb)
+                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
+                                         f.w.h, f.w.row0 + j * BN, bar(K_FULL + ks), pol_keep);
+                    k_issued = n + 1;
                 }
                 kvn += f.w.hi;
             }
@@ -225,75 +213,87 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // The whole warp runs this loop (so descriptors and addresses stay warp-uniform);
+        // one elected lane issues every MMA and commit.
         setmaxnreg_dec<kCtrlRegs>();
-        if (lane == 0) {
+        {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false);
             constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
             uint32_t qm = 0, kvn = 0, cnt_p[2] = {0, 0}, cnt_u[2] = {0, 0};
             bool ok = true;
+            auto commit = [&](uint32_t b) {
+                if (elect_one()) mma_commit(b);
+                __syncwarp();
+            };
             // Descriptors are built once per tile; the K-step offsets are added to the
             // start-address field (addresses stay below 2^18, so the field cannot carry).
             auto issue_s = [&](int t, int slot, int ks) {
                 const uint64_t qd = smem_desc_sw128(sbase + LY::Q0 + slot * LY::TILE, 16, 1024);
                 const uint64_t kd = smem_desc_sw128(sbase + LY::K0 + ks * LY::TILE, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = ((k >> 2) * LY::BLK + (k & 3) * 32) >> 4;
-                    mma_bf16_ss(tmem + LY::S_COL(t), qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = ((k >> 2) * LY::BLK + (k & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + LY::S_COL(t), qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(S_FULL + t));
                 }
-                mma_commit(bar(S_FULL + t));
+                __syncwarp();
             };
             for (int un = 0; ok; ++un) {
                 int u;
-                if (!(ok = ring_get(rg, un, abort, u)) || u < 0) break;
+                if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
                 const FUnit f = decode_funit(p, u);
                 const int n[2] = {f.n0, f.n1};
                 const int slot[2] = {static_cast<int>(qm % kQSlots), static_cast<int>((qm + 1) % kQSlots)};
-                if (!(ok = mbar_wait(bar(Q_READY + slot[0]), (qm / kQSlots) & 1, abort))) break;
-                if (f.has1 && !(ok = mbar_wait(bar(Q_READY + slot[1]), ((qm + 1) / kQSlots) & 1, abort)))
+                if (!(ok = wait_warp(bar(Q_READY + slot[0]), (qm / kQSlots) & 1, abort))) break;
+                if (f.has1 && !(ok = wait_warp(bar(Q_READY + slot[1]), ((qm + 1) / kQSlots) & 1, abort)))
                     break;
                 {
                     const int ks = kvn & 1;
-                    if (!(ok = mbar_wait(bar(K_READY + ks), (kvn >> 1) & 1, abort))) break;
+                    if (!(ok = wait_warp(bar(K_READY + ks), (kvn >> 1) & 1, abort))) break;
                     tc_fence_after();
                     for (int t = 0; t < 2; ++t) {
                         if (n[t] == 0) continue;
                         issue_s(t, slot[t], ks);
-                        if (n[t] == 1) mma_commit(bar(Q_EMPTY + slot[t]));
+                        if (n[t] == 1) commit(bar(Q_EMPTY + slot[t]));
                     }
-                    mma_commit(bar(K_EMPTY + ks));
+                    commit(bar(K_EMPTY + ks));
                 }
                 for (int j = 0; j < f.w.hi && ok; ++j) {
                     const uint32_t kvj = kvn + j;
                     const int vs = kvj & 1;
-                    if (!(ok = mbar_wait(bar(V_FULL + vs), (kvj >> 1) & 1, abort))) break;
+                    if (!(ok = wait_warp(bar(V_FULL + vs), (kvj >> 1) & 1, abort))) break;
                     bool k_next = false;
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (j >= n[t]) continue;
-                        if (!(ok = mbar_wait(bar(P_FULL + t), cnt_p[t] & 1, abort))) break;
+                        if (!(ok = wait_warp(bar(P_FULL + t), cnt_p[t] & 1, abort))) break;
                         ++cnt_p[t];
-                        if (j == 0 && !(ok = mbar_wait(bar(O_EMPTY + t), (cnt_u[t] & 1) ^ 1, abort))) break;
+                        if (j == 0 && !(ok = wait_warp(bar(O_EMPTY + t), (cnt_u[t] & 1) ^ 1, abort))) break;
                         tc_fence_after();
                         const uint64_t vd = smem_desc_sw128(sbase + LY::V0 + vs * LY::TILE, LY::BLK, 1024);
+                        if (elect_one()) {
 #pragma unroll
-                        for (int k = 0; k < BN / 16; ++k)
-                            mma_bf16_ts(tmem + LY::O_COL(t), tmem + LY::S_COL(t) + 8 * k,
-                                        vd + ((k * 16 * 128) >> 4), IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
-                        if (j == n[t] - 1) mma_commit(bar(O_FULL + t));
+                            for (int k = 0; k < BN / 16; ++k)
+                                mma_bf16_ts(tmem + LY::O_COL(t), tmem + LY::S_COL(t) + 8 * k,
+                                            vd + ((k * 16 * 128) >> 4), IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+                            if (j == n[t] - 1) mma_commit(bar(O_FULL + t));
+                        }
+                        __syncwarp();
                         if (j + 1 < n[t]) {
                             const uint32_t kvn1 = kvj + 1;
                             if (!k_next) {
-                                if (!(ok = mbar_wait(bar(K_READY + (kvn1 & 1)), (kvn1 >> 1) & 1, abort))) break;
+                                if (!(ok = wait_warp(bar(K_READY + (kvn1 & 1)), (kvn1 >> 1) & 1, abort))) break;
                                 tc_fence_after();
                                 k_next = true;
                             }
                             issue_s(t, slot[t], kvn1 & 1);
-                            if (j + 1 == n[t] - 1) mma_commit(bar(Q_EMPTY + slot[t]));
+                            if (j + 1 == n[t] - 1) commit(bar(Q_EMPTY + slot[t]));
                         }
                     }
                     if (!ok) break;
-                    mma_commit(bar(V_EMPTY + vs));
-                    if (k_next) mma_commit(bar(K_EMPTY + ((kvj + 1) & 1)));
+                    commit(bar(V_EMPTY + vs));
+                    if (k_next) commit(bar(K_EMPTY + ((kvj + 1) & 1)));
                 }
                 if (!ok) break;
                 kvn += f.w.hi;
@@ -301,7 +301,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ++cnt_u[0];
                 if (f.has1) ++cnt_u[1];
             }
-            mma_commit(bar(DRAIN));
+            commit(bar(DRAIN));
             mbar_wait_limit(bar(DRAIN), 0, 200000000ull);
         }
         __syncwarp();
@@ -469,14 +469,40 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ++kvn;
             }
         }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ TMA producer of V tiles
+        setmaxnreg_dec<kCtrlRegs>();
+        if (lane == 0) {
+            const uint64_t pol_keep = make_l2_policy_evict_last();
+            uint32_t vn = 0;
+            bool ok = true;
+            for (int un = 0; ok; ++un) {
+                int u;
+                if (!(ok = ring_get(rg, un, abort, u)) || u < 0) break;
+                const FUnit f = decode_funit(p, u);
+                for (int j = 0; j < f.w.hi && ok; ++j) {
+                    const uint32_t n = vn + j;
+                    const int vs = n & 1;
+                    if (!(ok = mbar_wait(bar(V_EMPTY + vs), ((n >> 1) & 1) ^ 1, abort))) break;
+                    mbar_expect_tx(bar(V_FULL + vs), LY::TILE);
+#pragma unroll
+                    for (int kb = 0; kb < LY::KB; ++kb)
+                        tma_load_3d_hint(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
+                                         f.w.h, f.w.row0 + j * BN, bar(V_FULL + vs), pol_keep);
+                    kv_issued = n + 1;
+                }
+                vn += f.w.hi;
+            }
+        }
+        __syncwarp();
     } else {
-        setmaxnreg_dec<kCtrlRegs>();   // warps 2 and 3: TMEM allocator and spare
+        setmaxnreg_dec<kCtrlRegs>();   // warp 2: TMEM allocator
     }
 
     __syncthreads();
     if (*abort) {
-        if (warp == 0 && lane == 0) {
-            // wait (bounded) for the last copy issued into every slot and stage
+        // each producer waits (bounded) for the last copy it issued into every slot and stage
+        if ((warp == 0 || warp == 3) && lane == 0) {
             for (int s = 0; s < kQSlots; ++s)
                 if (q_issued > static_cast<uint32_t>(s)) {
                     const uint32_t n = q_issued - 1 - ((q_issued - 1 - s) % kQSlots);
