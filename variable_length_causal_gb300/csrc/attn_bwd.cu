@@ -224,7 +224,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
-    constexpr int kRingConsumers = 1 + 8;   // MMA thread, 8 math warps
+    constexpr int kRingConsumers = 1 + 8;   // MMA warp, 8 math warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     __shared__ int s_skip, s_nunits;
@@ -324,48 +324,58 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {   // ---------------------------------------- MMA issuer
+        {   // ---------------------------------------- MMA issuer (converged warp, one elected lane issues)
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BK, false);
             constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, D, true);
             uint32_t unit_it = 0, kv = 0;
             bool ok = true;
+            auto commit = [&](uint32_t b) {
+                if (elect_one()) mma_commit(b);
+                __syncwarp();
+            };
             // S(n) = Q'K'(n)^T into S buffer n & 1 (free once the math released step n-2)
             auto issue_s = [&](uint32_t qb, uint32_t nn) -> bool {
                 const int ks = nn % kKStages, b = nn & 1;
-                if (!mbar_wait(bar(K_FULL + ks), (nn / kKStages) & 1, abort)) return false;
-                if (!mbar_wait(bar(S_EMPTY + b), ((nn >> 1) & 1) ^ 1, abort)) return false;
+                if (!wait_warp(bar(K_FULL + ks), (nn / kKStages) & 1, abort)) return false;
+                if (!wait_warp(bar(S_EMPTY + b), ((nn >> 1) & 1) ^ 1, abort)) return false;
                 tc_fence_after();
-                const uint32_t kb = sbase + LY::K0 + ks * LY::TILE;
+                const uint64_t qd = smem_desc_sw128(qb, 16, 1024);
+                const uint64_t kd = smem_desc_sw128(sbase + LY::K0 + ks * LY::TILE, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
-                    mma_bf16_ss(tmem + b * 128, smem_desc_sw128(qb + off, 16, 1024),
-                                smem_desc_sw128(kb + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = ((k >> 2) * LY::BLK + (k & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + b * 128, qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(S_FULL + b));
                 }
-                mma_commit(bar(S_FULL + b));
+                __syncwarp();
                 return true;
             };
             // dP(n) = dO V(n)^T (the dP columns were last read by dQ(n-1), issued earlier)
             auto issue_dp = [&](uint32_t ob, uint32_t nn) -> bool {
-                if (!mbar_wait(bar(V_FULL), nn & 1, abort)) return false;
+                if (!wait_warp(bar(V_FULL), nn & 1, abort)) return false;
                 tc_fence_after();
-                const uint32_t vb = sbase + LY::V0;
+                const uint64_t od = smem_desc_sw128(ob, 16, 1024);
+                const uint64_t vd = smem_desc_sw128(sbase + LY::V0, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
-                    mma_bf16_ss(tmem + LY::DP_COL, smem_desc_sw128(ob + off, 16, 1024),
-                                smem_desc_sw128(vb + off, 16, 1024), IDESC_S, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = ((k >> 2) * LY::BLK + (k & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + LY::DP_COL, od + off, vd + off, IDESC_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(DP_FULL));
+                    mma_commit(bar(V_EMPTY));
                 }
-                mma_commit(bar(DP_FULL));
-                mma_commit(bar(V_EMPTY));
+                __syncwarp();
                 return true;
             };
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
-                if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
+                if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
                 const int qs = unit_it % kQSlots;
-                if (!(ok = mbar_wait(bar(QD_FULL + qs), (unit_it / kQSlots) & 1, abort))) break;
+                if (!(ok = wait_warp(bar(QD_FULL + qs), (unit_it / kQSlots) & 1, abort))) break;
                 const uint32_t qb = sbase + LY::Q0 + qs * LY::TILE;
                 const uint32_t ob = sbase + LY::DO0 + qs * LY::TILE;
                 if (!(ok = issue_s(qb, kv))) break;
@@ -373,26 +383,28 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 for (int j = 0; j < w.hi; ++j) {
                     const uint32_t nn = kv + j;
                     if (j + 1 < w.hi && !(ok = issue_s(qb, nn + 1))) break;
-                    if (j == w.hi - 1) mma_commit(bar(QD_EMPTY + qs));   // after the last S / dP
+                    if (j == w.hi - 1) commit(bar(QD_EMPTY + qs));   // after the last S / dP
                     // dQ += dS(n) K'(n): dS packed over the dP columns
-                    if (j == 0 && !(ok = mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
-                    if (!(ok = mbar_wait(bar(DS_FULL), nn & 1, abort))) break;
+                    if (j == 0 && !(ok = wait_warp(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
+                    if (!(ok = wait_warp(bar(DS_FULL), nn & 1, abort))) break;
                     tc_fence_after();
                     const int ks = nn % kKStages;
-                    const uint32_t kb = sbase + LY::K0 + ks * LY::TILE;
+                    const uint64_t kd = smem_desc_sw128(sbase + LY::K0 + ks * LY::TILE, LY::BLK, 1024);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        mma_bf16_ts(tmem + LY::DQ_COL, tmem + LY::DP_COL + ds_col(k),
-                                    smem_desc_sw128(kb + k * 16 * 128, LY::BLK, 1024), IDESC_DQ,
-                                    (j > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(bar(K_EMPTY + ks));
+                        for (int k = 0; k < BK / 16; ++k)
+                            mma_bf16_ts(tmem + LY::DQ_COL, tmem + LY::DP_COL + ds_col(k),
+                                        kd + ((k * 16 * 128) >> 4), IDESC_DQ, (j > 0 || k > 0) ? 1u : 0u);
+                        mma_commit(bar(K_EMPTY + ks));
+                    }
+                    __syncwarp();
                     if (j + 1 < w.hi && !(ok = issue_dp(ob, nn + 1))) break;
                 }
                 if (!ok) break;
-                mma_commit(bar(ACC_FULL));
+                commit(bar(ACC_FULL));
                 kv += w.hi;
             }
-            mma_commit(bar(DRAIN));
+            commit(bar(DRAIN));
             mbar_wait_limit(bar(DRAIN), 0, kDrainNs);
         }
         __syncwarp();
@@ -554,7 +566,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
-    constexpr int kRingConsumers = 1 + 1 + 8;   // MMA thread, LSE/delta stager warp, 8 math warps
+    constexpr int kRingConsumers = 1 + 1 + 8;   // MMA warp, LSE/delta stager warp, 8 math warps
     float* lsed = reinterpret_cast<float*>(sgen + LY::LSED);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -639,75 +651,89 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {   // ---------------------------------------- MMA issuer
+        {   // ---------------------------------------- MMA issuer (converged warp, one elected lane issues)
             constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, BQ, false);
             constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, true);
             uint32_t unit_it = 0, st = 0;
             bool ok = true;
+            auto commit = [&](uint32_t b) {
+                if (elect_one()) mma_commit(b);
+                __syncwarp();
+            };
+            const uint64_t kd0 = smem_desc_sw128(sbase + LY::K0, 16, 1024);
+            const uint64_t vd0 = smem_desc_sw128(sbase + LY::V0, 16, 1024);
             // S^T = K'Q'(step)^T into columns 0..127 (read by dV of the previous step,
             // issued earlier); dP^T = V dO(step)^T into 128..255 (read by dK before).
             auto issue_st = [&](uint32_t sp) -> bool {
                 const int s = sp % kQStages;
-                if (!mbar_wait(bar(QO_FULL + s), (sp / kQStages) & 1, abort)) return false;
+                if (!wait_warp(bar(QO_FULL + s), (sp / kQStages) & 1, abort)) return false;
                 tc_fence_after();
-                const uint32_t qb = sbase + LY::Q0 + s * LY::TILE;
+                const uint64_t qd = smem_desc_sw128(sbase + LY::Q0 + s * LY::TILE, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
-                    mma_bf16_ss(tmem, smem_desc_sw128(sbase + LY::K0 + off, 16, 1024),
-                                smem_desc_sw128(qb + off, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = ((k >> 2) * LY::BLK + (k & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem, kd0 + off, qd + off, IDESC_ST, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(ST_FULL));
                 }
-                mma_commit(bar(ST_FULL));
+                __syncwarp();
                 return true;
             };
             auto issue_dpt = [&](uint32_t sp) {
                 const int s = sp % kQStages;
-                const uint32_t ob = sbase + LY::DO0 + s * LY::TILE;
+                const uint64_t od = smem_desc_sw128(sbase + LY::DO0 + s * LY::TILE, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * LY::BLK + (k & 3) * 32;
-                    mma_bf16_ss(tmem + LY::DPT_COL, smem_desc_sw128(sbase + LY::V0 + off, 16, 1024),
-                                smem_desc_sw128(ob + off, 16, 1024), IDESC_ST, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = ((k >> 2) * LY::BLK + (k & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + LY::DPT_COL, vd0 + off, od + off, IDESC_ST, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(DPT_FULL));
                 }
-                mma_commit(bar(DPT_FULL));
+                __syncwarp();
             };
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
-                if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
+                if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
-                if (!(ok = mbar_wait(bar(KV_FULL), unit_it & 1, abort))) break;
+                if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_st(st))) break;
                 issue_dpt(st);
                 for (int i = w.lo; i < w.hi; ++i, ++st) {
                     const int s = st % kQStages;
-                    const uint32_t qb = sbase + LY::Q0 + s * LY::TILE;
-                    const uint32_t ob = sbase + LY::DO0 + s * LY::TILE;
+                    const uint64_t qdm = smem_desc_sw128(sbase + LY::Q0 + s * LY::TILE, LY::BLK, 1024);
+                    const uint64_t odm = smem_desc_sw128(sbase + LY::DO0 + s * LY::TILE, LY::BLK, 1024);
                     // dV += P^T dO (P^T packed over the S^T columns)
-                    if (i == w.lo && !(ok = mbar_wait(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
-                    if (!(ok = mbar_wait(bar(PT_FULL), st & 1, abort))) break;
+                    if (i == w.lo && !(ok = wait_warp(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
+                    if (!(ok = wait_warp(bar(PT_FULL), st & 1, abort))) break;
                     tc_fence_after();
+                    if (elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < BQ / 16; ++k)
-                        mma_bf16_ts(tmem + LY::DV_COL, tmem + dq::ds_col(k),
-                                    smem_desc_sw128(ob + k * 16 * 128, LY::BLK, 1024), IDESC_ACC,
-                                    (i > w.lo || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < BQ / 16; ++k)
+                            mma_bf16_ts(tmem + LY::DV_COL, tmem + dq::ds_col(k), odm + ((k * 16 * 128) >> 4),
+                                        IDESC_ACC, (i > w.lo || k > 0) ? 1u : 0u);
+                    }
+                    __syncwarp();
                     if (i + 1 < w.hi && !(ok = issue_st(st + 1))) break;
                     // dK += dS^T Q' (dS^T packed over the dP^T columns)
-                    if (!(ok = mbar_wait(bar(DST_FULL), st & 1, abort))) break;
+                    if (!(ok = wait_warp(bar(DST_FULL), st & 1, abort))) break;
                     tc_fence_after();
+                    if (elect_one()) {
 #pragma unroll
-                    for (int k = 0; k < BQ / 16; ++k)
-                        mma_bf16_ts(tmem + LY::DK_COL, tmem + LY::DPT_COL + dq::ds_col(k),
-                                    smem_desc_sw128(qb + k * 16 * 128, LY::BLK, 1024), IDESC_ACC,
-                                    (i > w.lo || k > 0) ? 1u : 0u);
-                    mma_commit(bar(QO_EMPTY + s));
+                        for (int k = 0; k < BQ / 16; ++k)
+                            mma_bf16_ts(tmem + LY::DK_COL, tmem + LY::DPT_COL + dq::ds_col(k),
+                                        qdm + ((k * 16 * 128) >> 4), IDESC_ACC, (i > w.lo || k > 0) ? 1u : 0u);
+                        mma_commit(bar(QO_EMPTY + s));
+                    }
+                    __syncwarp();
                     if (i + 1 < w.hi) issue_dpt(st + 1);
                 }
                 if (!ok) break;
-                mma_commit(bar(ACC_FULL));
-                mma_commit(bar(KV_EMPTY));
+                commit(bar(ACC_FULL));
+                commit(bar(KV_EMPTY));
             }
-            mma_commit(bar(DRAIN));
+            commit(bar(DRAIN));
             mbar_wait_limit(bar(DRAIN), 0, kDrainNs);
         }
         __syncwarp();
