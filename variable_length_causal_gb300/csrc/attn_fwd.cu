@@ -53,8 +53,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr uint32_t kLaunchRegs = 65536 / kThreads;   // registers per thread at launch
 #ifndef VLC_FWD_CTRL_REGS
-#define VLC_FWD_CTRL_REGS 88
-#define VLC_FWD_ROPE_REGS 72
+#define VLC_FWD_CTRL_REGS 72
+#define VLC_FWD_ROPE_REGS 88
 #endif
 // per-thread registers of each warpgroup after the split: producer/MMA/TMEM,
 // RoPE, and the two softmax warpgroups
