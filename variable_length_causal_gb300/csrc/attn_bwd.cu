@@ -177,15 +177,15 @@ __device__ __forceinline__ uint32_t packed_col(int k) { return (k >> 1) * 32 + (
 // ====================================================================== dQ pass
 namespace dq {
 
-constexpr int BK = 128;        // key rows per step (N = 128 keeps the S / dP MMAs at full rate)
+constexpr int BK = 128;        // key rows per step (N = 128 keeps the MMAs at full rate)
 constexpr int kKStages = 2;
-constexpr int kQSlots = 2;
+constexpr int kVStages = 2;
 
 enum : int {
-    QD_FULL = 0, QD_EMPTY = kQSlots,
-    K_FULL = 2 * kQSlots, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages, V_EMPTY = V_FULL + 1,
-    S_FULL = V_EMPTY + 1, S_EMPTY = S_FULL + 2, DP_FULL = S_EMPTY + 2, DS_FULL = DP_FULL + 1,
-    ACC_FULL = DS_FULL + 1, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2,
+    QD_FULL = 0, QD_EMPTY = 1, QT_FULL = 2, QT_EMPTY = 3,
+    K_FULL = 4, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages, V_EMPTY = V_FULL + kVStages,
+    S_FULL = V_EMPTY + kVStages, S_EMPTY = S_FULL + 1, DP_FULL = S_FULL + 2, DS_FULL = S_FULL + 3,
+    ACC_FULL = S_FULL + 4, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2,
     UNIT_FULL = ACC_FULL + 3, UNIT_EMPTY = UNIT_FULL + kRing, NUM_BARS = UNIT_EMPTY + kRing
 };
 
@@ -194,22 +194,51 @@ struct Layout {
     static constexpr int KB = D / 64;
     static constexpr uint32_t BLK = 128u * 128u;       // 128 rows x 128 B
     static constexpr uint32_t TILE = 128u * D * 2u;
-    static constexpr uint32_t Q0 = 0;                          // kQSlots
-    static constexpr uint32_t DO0 = kQSlots * TILE;            // kQSlots
-    static constexpr uint32_t K0 = 2 * kQSlots * TILE;         // kKStages
-    static constexpr uint32_t V0 = K0 + kKStages * TILE;       // 1 stage
-    static constexpr uint32_t BAR0 = V0 + TILE;
+    static constexpr uint32_t Q0 = 0;                          // one staging slot
+    static constexpr uint32_t DO0 = TILE;                      // one staging slot
+    static constexpr uint32_t K0 = 2 * TILE;                   // kKStages
+    static constexpr uint32_t V0 = K0 + kKStages * TILE;       // kVStages
+    static constexpr uint32_t BAR0 = V0 + kVStages * TILE;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;      // tmem slot, abort flag, unit ring
     static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
-    // TMEM: S buffers at columns 0 and 128, dP at 256 (the packed bf16 dS of a step
-    // overwrites the consumed dP columns), dQ accumulator at 384.
-    static constexpr uint32_t DP_COL = 256, DQ_COL = 384;
+    // TMEM: S at columns 0..127, dP at 128 (the packed bf16 dS of a step overwrites
+    // the consumed dP columns), the dQ accumulator at 256, and the unit's Q' and dO
+    // (bf16 pairs, one lane per query row) as the A operands of the S and dP MMAs.
+    static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256;
+    static constexpr uint32_t QT_COL = 256 + D, DOT_COL = 256 + D + D / 2;
+    static_assert(DOT_COL + D / 2 <= 512, "TMEM columns");
 };
 
 // TMEM column of dS K-slice k (16 key columns): warpgroup g owns key columns
 // [64g, 64g + 64) and packs them into dP columns [64g, 64g + 32).
 __device__ __forceinline__ uint32_t ds_col(int k) { return (k >> 2) * 64 + (k & 3) * 8; }
+
+// Copy this thread's row of a staged [128 x D] bf16 tile (128-byte swizzle,
+// 64-column blocks) into TMEM as bf16 pairs: warpgroup g copies the row's
+// columns [D/2 * g, D/2 * (g + 1)) to TMEM columns col0 + [D/4 * g, D/4 * (g + 1)).
+template <int D>
+__device__ __forceinline__ void stage_row_to_tmem(uint32_t tile, int r, int g, uint32_t taddr_row) {
+    constexpr uint32_t BLK = 128u * 128u;
+    if constexpr (D == 128) {
+        uint32_t v[32];
+        const uint32_t blk = tile + g * BLK;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[4 * c]), "=r"(v[4 * c + 1]), "=r"(v[4 * c + 2]), "=r"(v[4 * c + 3])
+                         : "r"(sw128(blk, r, c)));
+        tmem_st32(taddr_row + 32 * g, v);
+    } else {
+        uint32_t v[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[4 * c]), "=r"(v[4 * c + 1]), "=r"(v[4 * c + 2]), "=r"(v[4 * c + 3])
+                         : "r"(sw128(tile, r, 4 * g + c)));
+        tmem_st16(taddr_row + 16 * g, v);
+    }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -224,7 +253,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
-    constexpr int kRingConsumers = 1 + 8;   // MMA warp, 8 math warps
+    constexpr int kRingConsumers = 1 + 1 + 8;   // MMA warp, V producer, 8 math warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     __shared__ int s_skip, s_nunits;
@@ -237,20 +266,20 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     const int nunits = s_nunits;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kQSlots; ++i) {
-            mbar_init(bar(QD_FULL + i), 1);
-            mbar_init(bar(QD_EMPTY + i), 1);
-        }
+        mbar_init(bar(QD_FULL), 1);
+        mbar_init(bar(QD_EMPTY), 8);      // one arrival per math warp once its rows are in TMEM
+        mbar_init(bar(QT_FULL), 256);
+        mbar_init(bar(QT_EMPTY), 1);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(bar(K_FULL + i), 1);
             mbar_init(bar(K_EMPTY + i), 1);
         }
-        mbar_init(bar(V_FULL), 1);
-        mbar_init(bar(V_EMPTY), 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(S_FULL + i), 1);
-            mbar_init(bar(S_EMPTY + i), 256);
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(bar(V_FULL + i), 1);
+            mbar_init(bar(V_EMPTY + i), 1);
         }
+        mbar_init(bar(S_FULL), 1);
+        mbar_init(bar(S_EMPTY), 256);
         mbar_init(bar(DP_FULL), 1);
         mbar_init(bar(DS_FULL), 256);
         mbar_init(bar(ACC_FULL), 1);
@@ -274,7 +303,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     uint32_t q_issued = 0, k_issued = 0, v_issued = 0;
 
     if (warp == 0) {
-        if (lane == 0) {   // ---------------------------------------- TMA producer
+        if (lane == 0) {   // ---------------------------------------- TMA producer: Q' / dO and K'
             const uint64_t pol_stream = make_l2_policy_evict_first();   // q/dO: once per unit
             const uint64_t pol_keep = make_l2_policy_evict_last();      // K/V: re-read by other units
             uint32_t unit_it = 0, kv = 0;
@@ -283,41 +312,52 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 int u;
                 if (!(ok = ring_put(rg, n, p.next_q, nunits, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-                const int qs = unit_it % kQSlots;
-                if (!(ok = mbar_wait(bar(QD_EMPTY + qs), ((unit_it / kQSlots) & 1) ^ 1, abort))) break;
-                mbar_expect_tx(bar(QD_FULL + qs), 2 * LY::TILE);
+                // the staging slot frees as soon as the math warps copied the last unit's rows to TMEM
+                if (!(ok = mbar_wait(bar(QD_EMPTY), (unit_it & 1) ^ 1, abort))) break;
+                mbar_expect_tx(bar(QD_FULL), 2 * LY::TILE);
                 const int qrow = w.row0 + w.tile * 128;
 #pragma unroll
                 for (int kb = 0; kb < LY::KB; ++kb) {
-                    tma_load_3d_hint(sbase + LY::Q0 + qs * LY::TILE + kb * LY::BLK, &tmQ, kb * 64, w.h,
-                                     qrow, bar(QD_FULL + qs), pol_stream);
-                    tma_load_3d_hint(sbase + LY::DO0 + qs * LY::TILE + kb * LY::BLK, &tmDO, kb * 64, w.h,
-                                     qrow, bar(QD_FULL + qs), pol_stream);
+                    tma_load_3d_hint(sbase + LY::Q0 + kb * LY::BLK, &tmQ, kb * 64, w.h, qrow, bar(QD_FULL),
+                                     pol_stream);
+                    tma_load_3d_hint(sbase + LY::DO0 + kb * LY::BLK, &tmDO, kb * 64, w.h, qrow, bar(QD_FULL),
+                                     pol_stream);
                 }
                 q_issued = unit_it + 1;
-                // K tile j is loaded one step ahead of V tile j-1 (V has a single stage)
-                for (int j = 0; j <= w.hi && ok; ++j) {
-                    if (j < w.hi) {
-                        const uint32_t nn = kv + j;
-                        const int ks = nn % kKStages;
-                        if (!(ok = mbar_wait(bar(K_EMPTY + ks), ((nn / kKStages) & 1) ^ 1, abort))) break;
-                        mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
+                for (int j = 0; j < w.hi && ok; ++j) {
+                    const uint32_t nn = kv + j;
+                    const int ks = nn % kKStages;
+                    if (!(ok = mbar_wait(bar(K_EMPTY + ks), ((nn / kKStages) & 1) ^ 1, abort))) break;
+                    mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
 #pragma unroll
-                        for (int kb = 0; kb < LY::KB; ++kb)
-                            tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64, w.h,
-                                             w.row0 + j * BK, bar(K_FULL + ks), pol_keep);
-                        k_issued = nn + 1;
-                    }
-                    if (j >= 1) {
-                        const uint32_t nn = kv + j - 1;
-                        if (!(ok = mbar_wait(bar(V_EMPTY), (nn & 1) ^ 1, abort))) break;
-                        mbar_expect_tx(bar(V_FULL), LY::TILE);
+                    for (int kb = 0; kb < LY::KB; ++kb)
+                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64, w.h,
+                                         w.row0 + j * BK, bar(K_FULL + ks), pol_keep);
+                    k_issued = nn + 1;
+                }
+                kv += w.hi;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        if (lane == 0) {   // ---------------------------------------- TMA producer: V
+            const uint64_t pol_keep = make_l2_policy_evict_last();
+            uint32_t kv = 0;
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                int u;
+                if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+                for (int j = 0; j < w.hi && ok; ++j) {
+                    const uint32_t nn = kv + j;
+                    const int vs = nn % kVStages;
+                    if (!(ok = mbar_wait(bar(V_EMPTY + vs), ((nn / kVStages) & 1) ^ 1, abort))) break;
+                    mbar_expect_tx(bar(V_FULL + vs), LY::TILE);
 #pragma unroll
-                        for (int kb = 0; kb < LY::KB; ++kb)
-                            tma_load_3d_hint(sbase + LY::V0 + kb * LY::BLK, &tmV, kb * 64, w.h,
-                                             w.row0 + (j - 1) * BK, bar(V_FULL), pol_keep);
-                        v_issued = nn + 1;
-                    }
+                    for (int kb = 0; kb < LY::KB; ++kb)
+                        tma_load_3d_hint(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64, w.h,
+                                         w.row0 + j * BK, bar(V_FULL + vs), pol_keep);
+                    v_issued = nn + 1;
                 }
                 kv += w.hi;
             }
@@ -333,39 +373,41 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 if (elect_one()) mma_commit(b);
                 __syncwarp();
             };
-            // S(n) = Q'K'(n)^T into S buffer n & 1 (free once the math released step n-2)
-            auto issue_s = [&](uint32_t qb, uint32_t nn) -> bool {
-                const int ks = nn % kKStages, b = nn & 1;
+            // S(n) = Q'K'(n)^T: Q' from TMEM, K' from shared memory; the S columns are free
+            // once the math warps have read S(n-1)
+            auto issue_s = [&](uint32_t nn) -> bool {
+                const int ks = nn % kKStages;
                 if (!wait_warp(bar(K_FULL + ks), (nn / kKStages) & 1, abort)) return false;
-                if (!wait_warp(bar(S_EMPTY + b), ((nn >> 1) & 1) ^ 1, abort)) return false;
+                if (!wait_warp(bar(S_EMPTY), (nn & 1) ^ 1, abort)) return false;
                 tc_fence_after();
-                const uint64_t qd = smem_desc_sw128(qb, 16, 1024);
                 const uint64_t kd = smem_desc_sw128(sbase + LY::K0 + ks * LY::TILE, 16, 1024);
                 if (elect_one()) {
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t off = ((k >> 2) * LY::BLK + (k & 3) * 32) >> 4;
-                        mma_bf16_ss(tmem + b * 128, qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
+                        mma_bf16_ts(tmem + LY::S_COL, tmem + LY::QT_COL + 8 * k, kd + off, IDESC_S,
+                                    k > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(S_FULL + b));
+                    mma_commit(bar(S_FULL));
                 }
                 __syncwarp();
                 return true;
             };
-            // dP(n) = dO V(n)^T (the dP columns were last read by dQ(n-1), issued earlier)
-            auto issue_dp = [&](uint32_t ob, uint32_t nn) -> bool {
-                if (!wait_warp(bar(V_FULL), nn & 1, abort)) return false;
+            // dP(n) = dO V(n)^T: dO from TMEM (the dP columns were last read by dQ(n-1), issued earlier)
+            auto issue_dp = [&](uint32_t nn) -> bool {
+                const int vs = nn % kVStages;
+                if (!wait_warp(bar(V_FULL + vs), (nn / kVStages) & 1, abort)) return false;
                 tc_fence_after();
-                const uint64_t od = smem_desc_sw128(ob, 16, 1024);
-                const uint64_t vd = smem_desc_sw128(sbase + LY::V0, 16, 1024);
+                const uint64_t vd = smem_desc_sw128(sbase + LY::V0 + vs * LY::TILE, 16, 1024);
                 if (elect_one()) {
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t off = ((k >> 2) * LY::BLK + (k & 3) * 32) >> 4;
-                        mma_bf16_ss(tmem + LY::DP_COL, od + off, vd + off, IDESC_S, k > 0 ? 1u : 0u);
+                        mma_bf16_ts(tmem + LY::DP_COL, tmem + LY::DOT_COL + 8 * k, vd + off, IDESC_S,
+                                    k > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(DP_FULL));
-                    mma_commit(bar(V_EMPTY));
+                    mma_commit(bar(V_EMPTY + vs));
                 }
                 __syncwarp();
                 return true;
@@ -374,16 +416,13 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 int u;
                 if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
                 const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-                const int qs = unit_it % kQSlots;
-                if (!(ok = wait_warp(bar(QD_FULL + qs), (unit_it / kQSlots) & 1, abort))) break;
-                const uint32_t qb = sbase + LY::Q0 + qs * LY::TILE;
-                const uint32_t ob = sbase + LY::DO0 + qs * LY::TILE;
-                if (!(ok = issue_s(qb, kv))) break;
-                if (!(ok = issue_dp(ob, kv))) break;
+                if (!(ok = wait_warp(bar(QT_FULL), unit_it & 1, abort))) break;
+                if (!(ok = issue_s(kv))) break;
+                if (!(ok = issue_dp(kv))) break;
                 for (int j = 0; j < w.hi; ++j) {
                     const uint32_t nn = kv + j;
-                    if (j + 1 < w.hi && !(ok = issue_s(qb, nn + 1))) break;
-                    if (j == w.hi - 1) commit(bar(QD_EMPTY + qs));   // after the last S / dP
+                    if (j + 1 < w.hi && !(ok = issue_s(nn + 1))) break;
+                    if (j == w.hi - 1) commit(bar(QT_EMPTY));   // after the last S / dP of the unit
                     // dQ += dS(n) K'(n): dS packed over the dP columns
                     if (j == 0 && !(ok = wait_warp(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                     if (!(ok = wait_warp(bar(DS_FULL), nn & 1, abort))) break;
@@ -398,7 +437,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                         mma_commit(bar(K_EMPTY + ks));
                     }
                     __syncwarp();
-                    if (j + 1 < w.hi && !(ok = issue_dp(ob, nn + 1))) break;
+                    if (j + 1 < w.hi && !(ok = issue_dp(nn + 1))) break;
                 }
                 if (!ok) break;
                 commit(bar(ACC_FULL));
@@ -409,7 +448,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ------------------------------------------------------------ P, dS + epilogue
+        // ------------------------------------------------------------ Q'/dO staging, P, dS + epilogue
         const int g = (warp - 4) >> 2;             // math warpgroup: key columns [64g, 64g + 64)
         const int wq = warp & 3;
         const int r = wq * 32 + lane;              // query row = TMEM lane
@@ -417,27 +456,45 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         const float scale_log2 = p.scale * kLog2e;
         const int c0 = 64 * g;
         uint32_t unit_it = 0, kv = 0;
-        bool ok = true;
-        for (int n = 0; ok; ++n, ++unit_it) {
-            int u;
-            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+        // Copy unit k's Q' and dO rows into TMEM once its tiles have landed and the
+        // previous unit's last S / dP MMAs are done; then free the staging slot.
+        auto stage = [&](uint32_t k) -> bool {
+            if (!wait_warp(bar(QD_FULL), k & 1, abort)) return false;
+            if (!wait_warp(bar(QT_EMPTY), (k & 1) ^ 1, abort)) return false;
+            tc_fence_after();
+            stage_row_to_tmem<D>(sbase + LY::Q0, r, g, tmem + lane_off + LY::QT_COL);
+            stage_row_to_tmem<D>(sbase + LY::DO0, r, g, tmem + lane_off + LY::DOT_COL);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(QT_FULL));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(QD_EMPTY));
+            return true;
+        };
+        int u = -1;
+        bool ok = ring_get_warp(rg, 0, abort, u);
+        bool have = ok && u >= 0;
+        Unit w{};
+        if (have) {
+            w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+            ok = have = stage(0);
+        }
+        while (have) {
             const int qpos = w.tile * 128 + r;
             const bool valid = qpos < w.L;
             const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? qpos : 0);
             const float lse2 = valid ? __ldg(p.lse + static_cast<int64_t>(w.h) * p.total + tok) * kLog2e : 0.f;
             const float dlt = valid ? __ldg(p.delta + static_cast<int64_t>(w.h) * p.total + tok) : 0.f;
             for (int j = 0; j < w.hi; ++j, ++kv) {
-                const int b = kv & 1;
                 // ---- phase A: P = exp2(s * scale_log2 - lse2) (masked), kept packed
-                if (!(ok = wait_warp(bar(S_FULL + b), (kv >> 1) & 1, abort))) break;
+                if (!(ok = wait_warp(bar(S_FULL), kv & 1, abort))) break;
                 tc_fence_after();
                 uint32_t sa[32], sb[32];
-                tmem_ld32(tmem + lane_off + b * 128 + c0, sa);
-                tmem_ld32(tmem + lane_off + b * 128 + c0 + 32, sb);
+                tmem_ld32(tmem + lane_off + LY::S_COL + c0, sa);
+                tmem_ld32(tmem + lane_off + LY::S_COL + c0 + 32, sb);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(bar(S_EMPTY + b));
+                mbar_arrive(bar(S_EMPTY));
                 const bool edge = (j == w.hi - 1);   // diagonal step (and the segment tail)
                 const int lim = !valid ? -1 : (edge ? min(qpos, w.L - 1) - j * BK : BK - 1);
                 const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
@@ -470,16 +527,21 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                                                                 __uint_as_float(src[ee + 1])), nd2));
                     pk[e >> 1] = pack_bf16x2(ds.x, ds.y);
                 }
-                uint32_t lo[16], hi[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) { lo[e] = pk[e]; hi[e] = pk[16 + e]; }
-                tmem_st16(tmem + lane_off + LY::DP_COL + c0, lo);
-                tmem_st16(tmem + lane_off + LY::DP_COL + c0 + 16, hi);
+                tmem_st32(tmem + lane_off + LY::DP_COL + c0, pk);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(DS_FULL));
             }
             if (!ok) break;
+            // stage the next unit before this unit's epilogue, so its first MMAs can start
+            Unit w2{};
+            int u2 = -1;
+            if (!(ok = ring_get_warp(rg, static_cast<int>(unit_it) + 1, abort, u2))) break;
+            const bool have_next = u2 >= 0;
+            if (have_next) {
+                w2 = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u2);
+                if (!(ok = stage(unit_it + 1))) break;
+            }
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
             tc_fence_after();
             if (g == 0) {
@@ -489,23 +551,29 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             }
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));
+            w = w2;
+            have = have_next;
+            ++unit_it;
         }
     }
 
     __syncthreads();
     if (*abort) {
+        // each producer waits (bounded) for the last copy it issued into every slot and stage
         if (warp == 0 && lane == 0) {
-            for (int s2 = 0; s2 < kQSlots; ++s2)
-                if (q_issued > static_cast<uint32_t>(s2)) {
-                    const uint32_t nn = q_issued - 1 - ((q_issued - 1 - s2) % kQSlots);
-                    mbar_wait_limit(bar(QD_FULL + s2), (nn / kQSlots) & 1, kDrainNs);
-                }
+            if (q_issued > 0) mbar_wait_limit(bar(QD_FULL), (q_issued - 1) & 1, kDrainNs);
             for (int s2 = 0; s2 < kKStages; ++s2)
                 if (k_issued > static_cast<uint32_t>(s2)) {
                     const uint32_t nn = k_issued - 1 - ((k_issued - 1 - s2) % kKStages);
                     mbar_wait_limit(bar(K_FULL + s2), (nn / kKStages) & 1, kDrainNs);
                 }
-            if (v_issued > 0) mbar_wait_limit(bar(V_FULL), (v_issued - 1) & 1, kDrainNs);
+        }
+        if (warp == 3 && lane == 0) {
+            for (int s2 = 0; s2 < kVStages; ++s2)
+                if (v_issued > static_cast<uint32_t>(s2)) {
+                    const uint32_t nn = v_issued - 1 - ((v_issued - 1 - s2) % kVStages);
+                    mbar_wait_limit(bar(V_FULL + s2), (nn / kVStages) & 1, kDrainNs);
+                }
         }
         if (threadIdx.x == 0) atomicOr(p.err, VLC_DEVERR_TIMEOUT);
         __syncthreads();
