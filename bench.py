@@ -223,23 +223,22 @@ def oracle_sample(w: synth.Workload, q, k, v, g, budget_s: float):
     rng = np.random.default_rng(12345)
     real = np.nonzero(w.seg_ignore == 0)[0]
     order = rng.permutation(len(real))
+    heads = rng.integers(0, w.H, size=len(order))
     threads = max(oracle.num_threads(), 1)
-    r0 = int(real[order[0]])
+    # calibrate on one parallel batch of `threads` pairs: legal pairs per second on all threads
+    calib = [(int(real[i]), int(h)) for i, h in zip(order[:threads], heads[:threads])]
     t0 = time.perf_counter()
-    oracle.attn_fwd(q, k, v, w.cu, seg_heads=[(r0, 0)])
-    oracle.attn_bwd(g, q, k, v, w.cu, seg_heads=[(r0, 0)])
+    oracle.attn_fwd(q, k, v, w.cu, seg_heads=calib)
+    oracle.attn_bwd(g, q, k, v, w.cu, seg_heads=calib)
     dt = max(time.perf_counter() - t0, 1e-4)
-    L0 = int(w.lengths[r0])
-    per_pair = dt / max(L0 * (L0 + 1) // 2, 1)          # single-thread seconds per legal pair
-    pairs, total_pairs, work = [], 0, 0.0
-    for n, i in enumerate(order):
+    rate = sum(int(w.lengths[r]) * (int(w.lengths[r]) + 1) // 2 for r, _ in calib) / dt
+    pairs, total_pairs = [], 0
+    for i, h in zip(order, heads):
         r = int(real[i])
         L = int(w.lengths[r])
-        pc = L * (L + 1) // 2
-        pairs.append((r, int(rng.integers(0, w.H))))
-        total_pairs += pc
-        work += pc * per_pair
-        if work >= budget_s * threads and n + 1 >= threads:
+        pairs.append((r, int(h)))
+        total_pairs += L * (L + 1) // 2
+        if total_pairs >= rate * budget_s and len(pairs) >= threads:
             break
     return pairs, total_pairs
 
@@ -352,7 +351,7 @@ def gpu_arm(args, w, world, rank, local):
     }
     dominant = "attn_bwd_call" if t_bwd >= t_fwd else "attn_fwd_call"
     ach = bwd_tflops if dominant == "attn_bwd_call" else fwd_tflops
-    traffic = _traffic_from_profiles(dominant)
+    traffic = _traffic_from_profiles(dominant, w.name) if args.bins is None else None
     roofline = {"bound": "tensor", "kernel": dominant, "achieved": ach, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} bf16 burst",
@@ -429,12 +428,31 @@ def cpu_baseline(w, q, k, v, g, seconds):
                       f"fwd + bwd in fp64, plus positions/labels of the whole pack; {dt:.1f} s"}
 
 
-def _traffic_from_profiles(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if one matches this build."""
+def _source_digest() -> str:
+    """sha256 over the kernel sources and the C header (names and bytes)."""
+    import glob
+    import hashlib
+
+    files = sorted(glob.glob(os.path.join(ROOT, "variable_length_causal_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "vlc.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _traffic_from_profiles(kernel: str, workload: str):
+    """DRAM bytes per call from the committed ncu capture (profiles/traffic.json), or None when
+    that capture was taken on other kernel sources or another workload."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get(kernel)
+            doc = json.load(f)
+        if doc.get("source_sha256") != _source_digest():
+            return None
+        return doc["workloads"][workload][kernel]
     except Exception:
         return None
 
@@ -452,10 +470,12 @@ def main():
     ap.add_argument("--fwd-only", action="store_true",
                     help="step = positions/labels + forward only (for profiling the forward kernel)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--bins", type=int, default=None,
+                    help="number of 4096-token windows (default: the workload's own); for small profiling runs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "vlc" else args.warmup
     world, rank, local = dist_setup()
-    w = synth.workload(WORKLOAD_BY_NAME[args.workload])
+    w = synth.workload(WORKLOAD_BY_NAME[args.workload], bins=args.bins)
     if args.impl == "reference":
         reference_arm(args, w, world, rank)
     else:

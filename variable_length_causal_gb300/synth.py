@@ -142,8 +142,10 @@ def _long_buffer(rng, capacity: int):
 WORKLOAD_NAMES = ["tiny", "sft", "pt", "long", "pt_bwd"]
 
 
-def workload(index: int) -> Workload:
-    """The five seeded workloads (see module docstring)."""
+def workload(index: int, bins: Optional[int] = None) -> Workload:
+    """The five seeded workloads (see module docstring).  ``bins`` shrinks (or grows) a
+    workload to that many 4096-token windows with the same length distribution (used for
+    small profiling captures); the tiny workload ignores it."""
     rng = np.random.default_rng(index)
     if index == 0:
         lens = rng.integers(1, 257, size=16)
@@ -151,17 +153,17 @@ def workload(index: int) -> Workload:
         return Workload("tiny", 0, 4, 64, cu, np.zeros(16, np.uint8),
                         description="16 segments, U[1,256], H=4, d=64, forward")
     if index == 1:
-        cu, ign = _ffd_pack(rng, 16, 4096, 300.0, 1.0, 16, 4096)
+        cu, ign = _ffd_pack(rng, bins or 16, 4096, 300.0, 1.0, 16, 4096)
         return Workload("sft", 1, 32, 128, cu, ign,
                         description="SFT pack: lognormal(300,1.0) FFD into 16x4096, H=32, d=128")
     if index in (2, 4):
-        cu, ign = _ffd_pack(rng, 32, 4096, 400.0, 0.8, 32, 4096)
+        cu, ign = _ffd_pack(rng, bins or 32, 4096, 400.0, 0.8, 32, 4096)
         return Workload("pt" if index == 2 else "pt_bwd", index, 32, 128, cu, ign,
                         backward=(index == 4),
                         description="pretraining windows: lognormal(400,0.8) FFD into 32x4096, "
                                     "H=32, d=128" + (", forward+backward" if index == 4 else ""))
     if index == 3:
-        cu, ign = _long_buffer(rng, 131072)
+        cu, ign = _long_buffer(rng, 4096 * (bins or 32))
         return Workload("long", 3, 32, 128, cu, ign,
                         description="long context: one 131072-token buffer, lognormal(2048,1.2) "
                                     "+10% at 128, H=32, d=128")
