@@ -378,38 +378,70 @@ def gpu_arm(args, w, world, rank, local):
 
 def e2e_measure(vlc, w, step, steps, world, dev):
     """Same metric through the public API with pinned host buffers: every step copies this
-    step's inputs host->device and reads back every output device->host."""
-    dev_in = [t for t in (step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign) if t is not None]
-    host_in = [t.cpu().pin_memory() for t in dev_in]
-    outs = tuple(t for t in (step.o, step.lse, step.dq, step.dk, step.dv) if t is not None)
-    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    step's inputs host->device and reads every output back device->host.  Steps are pipelined
+    over three streams (copy-in, compute, copy-out) with two device buffer sets, so step k's
+    outputs travel back while step k+1 computes and step k+2's inputs arrive."""
+    sets = [step, Step(vlc, w, *(torch.empty_like(t) if t is not None else None
+                                 for t in (step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign)),
+                       fwd_only=step.fwd_only)]
+    host_in = [t.cpu().pin_memory() for t in (step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign)
+               if t is not None]
+
+    def dev_in(s):
+        return [t for t in (s.q, s.k, s.v, s.g, s.tokens, s.cu, s.ign) if t is not None]
+
+    def dev_out(s):
+        return [t for t in (s.o, s.lse, s.dq, s.dk, s.dv) if t is not None]
+
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out(step)]
     host_pos = torch.empty(w.total, dtype=torch.int32).pin_memory()
     host_lab = torch.empty(w.total, dtype=torch.int64).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out) + w.total * 12
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_done = [torch.cuda.Event() for _ in sets]
+    cmp_done = [torch.cuda.Event() for _ in sets]
+    out_done = [torch.cuda.Event() for _ in sets]
 
-    def one():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in zip(host_out, outs):
-            h.copy_(d, non_blocking=True)
-        host_pos.copy_(step.pos, non_blocking=True)
-        host_lab.copy_(step.lab, non_blocking=True)
+    def one(k):
+        s = sets[k % 2]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(cmp_done[k % 2])          # the previous user of this set is done computing
+            for d, h in zip(dev_in(s), host_in):
+                d.copy_(h, non_blocking=True)
+            in_done[k % 2].record(s_in)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(in_done[k % 2])
+            s_cmp.wait_event(out_done[k % 2])         # its outputs of two steps ago were read back
+            s()
+            cmp_done[k % 2].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(cmp_done[k % 2])
+            for h, d in zip(host_out, dev_out(s)):
+                h.copy_(d, non_blocking=True)
+            host_pos.copy_(s.pos, non_blocking=True)
+            host_lab.copy_(s.lab, non_blocking=True)
+            s.pos.record_stream(s_out)                # allocated per call on the compute stream
+            s.lab.record_stream(s_out)
+            out_done[k % 2].record(s_out)
 
-    one()
+    for k in range(2):
+        one(k)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    for k in range(steps):
+        one(k)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     dt = max_over_ranks(dt, world, dev)
+    for s in sets:
+        s.check_errors()
     flops = sum_over_ranks(synth.fwd_flops(w) + (0.0 if step.fwd_only else synth.bwd_flops(w)), world, dev)
     return {"value": flops / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3,
+            "pipelining": "copy-in, compute and copy-out streams, two device buffer sets"}
 
 
 def cpu_baseline(w, q, k, v, g, seconds):
