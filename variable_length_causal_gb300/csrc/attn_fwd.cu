@@ -87,21 +87,28 @@ struct Layout {
     __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + 128u * t; }
 };
 
-// One work unit: q tile t (t = 0, 1) covers rows qb*256 + t*128 + [0, 128) of
-// the segment and needs key tiles [0, n_t): n_0 = 2qb + 1 (up to its diagonal),
-// n_1 = 2qb + 2 when the second tile holds any row of the segment, else absent.
+// One work unit pairs two adjacent 128-row q tiles of a segment that share every
+// K/V tile.  With T = ceil(L / 128) q tiles, unit qb holds tiles (2qb - s, 2qb - s + 1)
+// where s = T mod 2, so an odd T leaves tile 0 alone in unit 0 (one key tile of work)
+// rather than the last, longest tile.  Slot t of the unit is q tile q0 + t and needs
+// key tiles [0, q0 + t + 1) (up to its diagonal); nk is the length of the K/V stream.
 struct FUnit {
     Unit w;
     bool has1;
-    int n0, n1;
+    int q0, n0, n1, nk;
 };
 
 __device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
     FUnit f;
     f.w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
-    f.has1 = f.w.L > f.w.tile * QB + BQ;
-    f.n0 = 2 * f.w.tile + 1;
-    f.n1 = f.has1 ? f.w.hi : 0;
+    const int T = (f.w.L + BQ - 1) / BQ;
+    const int s = T & 1;
+    const bool lone = (s != 0) && (f.w.tile == 0);
+    f.has1 = !lone;
+    f.q0 = lone ? 0 : 2 * f.w.tile - s;
+    f.n0 = f.q0 + 1;
+    f.n1 = f.has1 ? f.q0 + 2 : 0;
+    f.nk = f.has1 ? f.n1 : f.n0;
     return f;
 }
 
@@ -187,7 +194,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int slot = qm % kQSlots;
                     if (!(ok = mbar_wait(bar(Q_EMPTY + slot), ((qm / kQSlots) & 1) ^ 1, abort))) break;
                     mbar_expect_tx(bar(Q_FULL + slot), LY::TILE);
-                    const int row = f.w.row0 + f.w.tile * QB + t * BQ;
+                    const int row = f.w.row0 + (f.q0 + t) * BQ;
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
                         tma_load_3d_hint(sbase + LY::Q0 + slot * LY::TILE + kb * LY::BLK, &tmQ, kb * 64,
@@ -196,7 +203,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 // K tiles only: V tiles come from their own producer (warp 3), so a V
                 // load never waits behind a K stage and vice versa.
-                for (int j = 0; j < f.w.hi && ok; ++j) {
+                for (int j = 0; j < f.nk && ok; ++j) {
                     const uint32_t n = kvn + j;
                     const int ks = n & 1;
                     if (!(ok = mbar_wait(bar(K_EMPTY + ks), ((n >> 1) & 1) ^ 1, abort))) break;
@@ -207,7 +214,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                          f.w.h, f.w.row0 + j * BN, bar(K_FULL + ks), pol_keep);
                     k_issued = n + 1;
                 }
-                kvn += f.w.hi;
+                kvn += f.nk;
             }
         }
         __syncwarp();
@@ -260,7 +267,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                     commit(bar(K_EMPTY + ks));
                 }
-                for (int j = 0; j < f.w.hi && ok; ++j) {
+                for (int j = 0; j < f.nk && ok; ++j) {
                     const uint32_t kvj = kvn + j;
                     const int vs = kvj & 1;
                     if (!(ok = wait_warp(bar(V_FULL + vs), (kvj >> 1) & 1, abort))) break;
@@ -296,7 +303,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (k_next) commit(bar(K_EMPTY + ((kvj + 1) & 1)));
                 }
                 if (!ok) break;
-                kvn += f.w.hi;
+                kvn += f.nk;
                 qm += f.has1 ? 2 : 1;
                 ++cnt_u[0];
                 if (f.has1) ++cnt_u[1];
@@ -323,7 +330,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const FUnit f = decode_funit(p, u);
             const int nt = t == 0 ? f.n0 : f.n1;
             if (nt == 0) continue;
-            const int qpos = f.w.tile * QB + t * BQ + r;
+            const int qpos = (f.q0 + t) * BQ + r;
             float m_run = 0.f, l_run = 0.f;
             for (int j = 0; j < nt; ++j) {
                 if (!(ok = wait_warp(bar(S_FULL + t), cnt_s & 1, abort))) break;
@@ -453,13 +460,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const int slot = qm % kQSlots;
                 if (!(ok = wait_warp(bar(Q_FULL + slot), (qm / kQSlots) & 1, abort))) break;
                 if (p.use_rope)
-                    rope_tile<D, 128>(sbase + LY::Q0 + slot * LY::TILE, f.w.tile * QB + t * BQ, p.table,
+                    rope_tile<D, 128>(sbase + LY::Q0 + slot * LY::TILE, (f.q0 + t) * BQ, p.table,
                                       step, wr, lane);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(Q_READY + slot));
                 ++qm;
             }
-            for (int j = 0; j < f.w.hi && ok; ++j) {
+            for (int j = 0; j < f.nk && ok; ++j) {
                 const int ks = kvn & 1;
                 if (!(ok = wait_warp(bar(K_FULL + ks), (kvn >> 1) & 1, abort))) break;
                 if (p.use_rope)
@@ -480,7 +487,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 int u;
                 if (!(ok = ring_get(rg, un, abort, u)) || u < 0) break;
                 const FUnit f = decode_funit(p, u);
-                for (int j = 0; j < f.w.hi && ok; ++j) {
+                for (int j = 0; j < f.nk && ok; ++j) {
                     const uint32_t n = vn + j;
                     const int vs = n & 1;
                     if (!(ok = mbar_wait(bar(V_EMPTY + vs), ((n >> 1) & 1) ^ 1, abort))) break;
@@ -491,7 +498,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                          f.w.h, f.w.row0 + j * BN, bar(V_FULL + vs), pol_keep);
                     kv_issued = n + 1;
                 }
-                vn += f.w.hi;
+                vn += f.nk;
             }
         }
         __syncwarp();
