@@ -178,7 +178,7 @@ __device__ __forceinline__ uint32_t packed_col(int k) { return (k >> 1) * 32 + (
 namespace dq {
 
 constexpr int BK = 128;        // key rows per step (N = 128 keeps the MMAs at full rate)
-constexpr int kKStages = 2;
+constexpr int kKStages = 3;   // K(j) is held from S(j) until dQ(j) completes
 constexpr int kVStages = 2;
 
 enum : int {
