@@ -371,9 +371,71 @@ def gpu_arm(args, w, world, rank, local):
         "clocks": clk.summary(),
         "e2e": e2e,
     }
+    if not args.no_extras and args.bins is None and world == 1:
+        line["extras"] = extra_measurements(vlc, w, dev, peaks, q, k, v, step)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, q, k, v, g, args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+def _time_ms(fn, reps: int) -> float:
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
+    """Positions/labels bandwidth on large packs with the workload's length mix, and (long-context
+    workload) the padded comparator: every document padded to the buffer length costs one full
+    causal run of that length, and the whole pack run as one causal segment ignores the boundaries."""
+    out = {}
+    sweep = {}
+    lens = np.diff(w.cu).astype(np.int64)
+    for logT in (24, 26):
+        T = 1 << logT
+        reps = -(-T // int(lens.sum()))
+        L = np.tile(lens, reps)
+        cut = np.searchsorted(np.cumsum(L), T)
+        L = L[:cut + 1].copy()
+        L[-1] -= int(L.sum()) - T
+        L = L[L > 0]
+        cu = torch.from_numpy(np.concatenate([[0], np.cumsum(L)]).astype(np.int32)).to(dev)
+        tok = torch.randint(0, 32000, (T,), dtype=torch.int64, device=dev)
+        pos = torch.empty(T, dtype=torch.int32, device=dev)
+        lab = torch.empty(T, dtype=torch.int64, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ms = _time_ms(lambda: vlc.build_positions_labels(cu, tok, None, err=err, out=(pos, lab)), 20)
+        gbs = 20.0 * T / (ms * 1e-3) / 1e9
+        sweep[f"T=2^{logT}"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
+        del cu, tok, pos, lab
+    out["positions_labels_sweep"] = sweep
+    if w.name == "long":
+        cu1 = torch.tensor([0, w.total], dtype=torch.int32, device=dev)
+        o1 = torch.empty_like(q)
+        lse1 = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
+        ws1 = vlc.new_workspace(1, w.total, w.H, w.d, w.total, False, dev)
+        ms1 = _time_ms(lambda: vlc.varlen_attn_fwd(q, k, v, cu1, w.total, out=o1, lse=lse1, workspace=ws1,
+                                                    check=False), 3)
+        docs = int((w.seg_ignore == 0).sum())
+        ms_packed = _time_ms(lambda: vlc.varlen_attn_fwd(q, k, v, step.cu, w.max_seqlen, out=step.o, lse=step.lse,
+                                                          workspace=step.ws_f, check=False), 5)
+        out["padded_comparator"] = {
+            "docs": docs,
+            "causal_run_ms": ms1,
+            "padded_forward_ms": ms1 * docs,
+            "whole_pack_causal_forward_ms": ms1,
+            "packed_forward_ms": ms_packed,
+            "speedup_packed_vs_padded": ms1 * docs / ms_packed,
+            "causal_run_tflops": 4.0 * w.d * w.H * (w.total * (w.total + 1) / 2) / (ms1 * 1e-3) / 1e12,
+        }
+        del o1, lse1, ws1
+    return out
 
 
 def e2e_measure(vlc, w, step, steps, world, dev):
@@ -502,6 +564,8 @@ def main():
     ap.add_argument("--fwd-only", action="store_true",
                     help="step = positions/labels + forward only (for profiling the forward kernel)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the positions/labels sweep and the padded comparator")
     ap.add_argument("--bins", type=int, default=None,
                     help="number of 4096-token windows (default: the workload's own); for small profiling runs")
     args = ap.parse_args()

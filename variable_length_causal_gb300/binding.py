@@ -132,8 +132,10 @@ def _raise_device_error(ws, where):
 
 def build_positions_labels(cu_seqlens: torch.Tensor, tokens: torch.Tensor,
                            seg_ignore: Optional[torch.Tensor] = None,
-                           err: Optional[torch.Tensor] = None):
-    """Per-segment positions (int32) and pre-shifted labels (int64, -100 at segment ends)."""
+                           err: Optional[torch.Tensor] = None,
+                           out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """Per-segment positions (int32) and pre-shifted labels (int64, -100 at segment ends).
+    ``out`` = (positions, labels) receives the result instead of new tensors."""
     lib = load_library()
     _require_cuda(cu_seqlens, tokens, seg_ignore, err)
     nseg = _cu_info(cu_seqlens)
@@ -142,8 +144,15 @@ def build_positions_labels(cu_seqlens: torch.Tensor, tokens: torch.Tensor,
     total = tokens.numel()
     if seg_ignore is not None and (seg_ignore.dtype != torch.uint8 or seg_ignore.numel() != nseg):
         raise ValueError("seg_ignore must be uint8 with one entry per segment")
-    pos = torch.empty(total, dtype=torch.int32, device=tokens.device)
-    lab = torch.empty(total, dtype=torch.int64, device=tokens.device)
+    if out is None:
+        pos = torch.empty(total, dtype=torch.int32, device=tokens.device)
+        lab = torch.empty(total, dtype=torch.int64, device=tokens.device)
+    else:
+        pos, lab = out
+        if (pos.dtype != torch.int32 or lab.dtype != torch.int64 or pos.numel() != total
+                or lab.numel() != total or not pos.is_contiguous() or not lab.is_contiguous()):
+            raise ValueError("out must be contiguous (int32 positions, int64 labels) of one entry per token")
+        _require_cuda(pos, lab)
     st = lib.vlc_build_positions_labels(_ptr(cu_seqlens), nseg, _ptr(tokens), total,
                                         _ptr(seg_ignore), _ptr(pos), _ptr(lab), _ptr(err),
                                         _stream(tokens.device))
