@@ -216,11 +216,16 @@ cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int3
 
 // ============================================================== positions + labels
 //
-// Each thread handles 4 consecutive tokens: one binary search over cu for the
-// first, then forward steps.  Loads and stores are vectorised (16 B).
+// Each warp owns one contiguous run of tokens (a multiple of 128) and walks it
+// 128 tokens at a time, 4 consecutive tokens per lane: one binary search over cu
+// per warp for the run's first token, then every lane steps forward from the
+// warp's current segment (segments are at least one token long, so a lane
+// crosses at most a few boundaries).  Token loads and position / label stores are
+// 16-byte vectors, and consecutive lanes touch consecutive bytes.
 
 constexpr int kPlThreads = 256;
 constexpr int kPlVec = 4;
+constexpr int kPlWarpSpan = 32 * kPlVec;   // tokens per warp per step
 
 __global__ void __launch_bounds__(kPlThreads)
 positions_labels_kernel(const int32_t* __restrict__ cu, int32_t nseg,
@@ -229,6 +234,7 @@ positions_labels_kernel(const int32_t* __restrict__ cu, int32_t nseg,
                         int64_t* __restrict__ labels, int32_t* __restrict__ err) {
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
 
     if (err != nullptr) {   // validity bits (cheap: nseg reads in total)
         int e = 0;
@@ -240,25 +246,45 @@ positions_labels_kernel(const int32_t* __restrict__ cu, int32_t nseg,
         if (e) atomicOr(err, e);
     }
 
-    const bool vec_ok = ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(labels)) & 15) == 0;
-    const int64_t ngroups = (static_cast<int64_t>(total) + kPlVec - 1) / kPlVec;
-    for (int64_t g = gtid; g < ngroups; g += nthreads) {
-        const int64_t i0 = g * kPlVec;
-        // largest r in [0, nseg-1] with cu[r] <= i0 (clamped; in bounds even for bad cu)
+    const int64_t nwarps = nthreads >> 5;
+    const int64_t gwarp = gtid >> 5;
+    const int64_t span = ((static_cast<int64_t>(total) + nwarps - 1) / nwarps + kPlWarpSpan - 1) /
+                         kPlWarpSpan * kPlWarpSpan;
+    const int64_t begin = gwarp * span;
+    const int64_t end = min(static_cast<int64_t>(total), begin + span);
+    if (begin >= end) return;   // warp-uniform
+    const bool vec_ok = ((reinterpret_cast<uintptr_t>(pos) | reinterpret_cast<uintptr_t>(labels) |
+                          reinterpret_cast<uintptr_t>(tokens)) & 15) == 0;
+
+    // largest r in [0, nseg-1] with cu[r] <= begin (clamped; in bounds even for bad cu)
+    int rw = 0;
+    if (lane == 0) {
         int lo = 0, hi = nseg - 1;
         while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (__ldg(cu + mid) <= i0) lo = mid; else hi = mid - 1;
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(cu + mid) <= begin) lo = mid; else hi = mid - 1;
         }
-        int r = lo;
+        rw = lo;
+    }
+    rw = __shfl_sync(0xffffffffu, rw, 0);
+
+    for (int64_t base = begin; base < end; base += kPlWarpSpan) {   // warp-uniform trip count
+        const int64_t i0 = base + kPlVec * lane;
+        int r = rw;
+        int32_t seg_start = __ldg(cu + r), seg_end = __ldg(cu + r + 1);
+        int64_t tk[kPlVec + 1];
+        const bool full = (i0 + kPlVec <= end);
+        if (full && vec_ok) {
+            const longlong2 a = __ldg(reinterpret_cast<const longlong2*>(tokens + i0));
+            const longlong2 b = __ldg(reinterpret_cast<const longlong2*>(tokens + i0) + 1);
+            tk[0] = a.x; tk[1] = a.y; tk[2] = b.x; tk[3] = b.y;
+        } else {
+#pragma unroll
+            for (int t = 0; t < kPlVec; ++t) tk[t] = (i0 + t < total) ? __ldg(tokens + i0 + t) : 0;
+        }
+        tk[kPlVec] = (i0 + kPlVec < total) ? __ldg(tokens + i0 + kPlVec) : 0;
         int32_t p[kPlVec];
         int64_t lab[kPlVec];
-        int32_t seg_start = __ldg(cu + r), seg_end = __ldg(cu + r + 1);
-        bool full = (i0 + kPlVec <= total);
-        int64_t tk[kPlVec + 1];
-#pragma unroll
-        for (int t = 0; t <= kPlVec; ++t)
-            tk[t] = (i0 + t < total) ? __ldg(tokens + i0 + t) : 0;
 #pragma unroll
         for (int t = 0; t < kPlVec; ++t) {
             const int64_t i = i0 + t;
@@ -277,11 +303,12 @@ positions_labels_kernel(const int32_t* __restrict__ cu, int32_t nseg,
             reinterpret_cast<longlong2*>(labels + i0)[1] = make_longlong2(lab[2], lab[3]);
         } else {
             for (int t = 0; t < kPlVec; ++t)
-                if (i0 + t < total) {
+                if (i0 + t < end) {
                     pos[i0 + t] = p[t];
                     labels[i0 + t] = lab[t];
                 }
         }
+        rw = __shfl_sync(0xffffffffu, r, 31);   // segment of the last token of this step
     }
 }
 
@@ -291,9 +318,11 @@ cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t groups = (static_cast<int64_t>(total) + kPlVec - 1) / kPlVec;
-    int64_t blocks = (groups + kPlThreads - 1) / kPlThreads;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;   // 8 resident CTAs per SM, grid-stride beyond
+    // one warp per 128-token step at small sizes; at most 8 resident CTAs per SM, each warp
+    // then walks a longer contiguous run
+    const int64_t steps = (static_cast<int64_t>(total) + kPlWarpSpan - 1) / kPlWarpSpan;
+    int64_t blocks = (steps + kPlThreads / 32 - 1) / (kPlThreads / 32);
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     positions_labels_kernel<<<static_cast<int>(blocks), kPlThreads, 0, s>>>(
