@@ -12,8 +12,11 @@ Pins (see tests/test_oracle_pins.py): the pages' nine-token example, the
 pre-shifted label example, the 10-versus-3.25 contamination counterexample,
 closed forms at Q = 0, packed == per-sample, change-A-keeps-B, brute force
 (numpy, full T x T mask), torch CPU fp64 SDPA with a boolean block mask, RoPE
-shift invariance and closed-form angles, and finite differences for the
-backward pass.  No oracle function is "parity unpinned".
+shift invariance and closed-form angles, finite differences for the backward
+pass, and for the shifted cross-entropy: uniform-logit closed form, the pages'
+token-mean 2.5 versus sample-mean 2 example, torch's fp64 cross_entropy, and
+pre-shifted labels == the internal-shift formulation.  No oracle function is
+"parity unpinned".
 """
 from __future__ import annotations
 
@@ -75,6 +78,8 @@ def _load():
             lib.orc_attn_bwd_seg_heads.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, f64,
                                                    ctypes.c_int, P, P, i64, P, P, P]
             lib.orc_attn_bwd_seg_heads.restype = None
+            lib.orc_shifted_ce.argtypes = [P, ctypes.c_int, i32, i32, P, P, i32, P, P, P, P]
+            lib.orc_shifted_ce.restype = ctypes.c_int
             lib.orc_num_threads.argtypes = []
             lib.orc_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -243,3 +248,27 @@ def attn_bwd(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, cont
                                    total, H, d, float(scale), float(theta), int(bool(contract)),
                                    _ptr(segs), _ptr(heads), sh.shape[0], _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
+
+
+def shifted_ce(logits, labels, cu=None):
+    """Shifted next-token cross-entropy statistics (charlestar: "After isolation one
+    cross-boundary prediction pair remains"; "Packing should not decide how much a long
+    sample weighs").  logits: [total, vocab] as bf16 bit patterns (uint16) or float64;
+    labels: int64 [total], pre-shifted, -100 = ignored.  Returns (status, loss_sum,
+    count, seg_loss [nseg], seg_count [nseg]); status 1 flags a label outside [0, vocab)."""
+    lib = _load()
+    z = np.ascontiguousarray(logits)
+    is_f64 = 1 if z.dtype == np.float64 else 0
+    if not is_f64 and z.dtype != np.uint16:
+        raise TypeError("logits must be uint16 bf16 bits or float64")
+    total, vocab = z.shape
+    lab = _c(labels, np.int64)
+    cuc = None if cu is None else _c(cu, np.int32)
+    nseg = 1 if cu is None else len(cuc) - 1
+    ls = np.zeros(1, np.float64)
+    cnt = np.zeros(1, np.int64)
+    sl = np.zeros(nseg, np.float64)
+    sc = np.zeros(nseg, np.int64)
+    st = lib.orc_shifted_ce(_ptr(z), is_f64, vocab, total, _ptr(lab), None if cuc is None else _ptr(cuc),
+                            nseg, _ptr(ls), _ptr(cnt), _ptr(sl), _ptr(sc))
+    return int(st), float(ls[0]), int(cnt[0]), sl, sc

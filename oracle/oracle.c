@@ -23,6 +23,11 @@
  *      section 06 "positions and labels": targets [12,13,ignore,22,ignore].
  *  [COMPASS] "Sequence Packing" (brenchcc llm-compass), "Implementation notes":
  *      padding tail as its own segment whose labels are all -100.
+ *  [CSTAR] "After isolation one cross-boundary prediction pair remains" and
+ *      "Packing should not decide how much a long sample weighs": the next-token
+ *      loss is kept as a sum of per-target cross-entropies plus a count of valid
+ *      targets (ignore index -100), per sample and per pack, so the training loop
+ *      chooses the denominator (token mean sum S / sum n, or sample mean of S_r / n_r).
  *
  * Everything is computed one segment at a time; there is no tiling, fusion or
  * reordering beyond the definitions above.  Inputs are the raw bf16 bit
@@ -493,6 +498,67 @@ void orc_attn_bwd_seg_heads(const void* dout, const void* q, const void* k,
     orc_problem P = make_problem(q, k, v, dout, cu, nseg, total, H, d, scale, theta, contract);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < n; ++t) bwd_seg_head(&P, segs[t], heads[t], dq, dk, dv);
+}
+
+/* ---------------------------------------------------------------- shifted cross-entropy
+ * [CSTAR] "After isolation one cross-boundary prediction pair remains": with the
+ * pre-shifted labels (lab_i = token_{i+1} inside a segment, -100 on its last
+ * token and on ignored segments) the loss term of logit row i is the
+ * cross-entropy  CE_i = ln(sum_c exp(z_ic)) - z_i,lab_i  for lab_i != -100.
+ * [CSTAR] "Packing should not decide how much a long sample weighs": keep the
+ * per-segment sums S_r = sum_{i in r} CE_i and counts n_r = #{i in r : lab_i !=
+ * -100}, and the pack totals sum_r S_r and sum_r n_r.  Logits are [total, vocab],
+ * either bf16 bit patterns (is_f64 == 0) or doubles (is_f64 == 1).  A label
+ * outside [0, vocab) other than -100 makes the call return 1 and counts nothing
+ * for that row.  cu may be NULL (one segment covering the whole buffer). */
+int orc_shifted_ce(const void* logits, int is_f64, int32_t vocab, int32_t total,
+                   const int64_t* labels, const int32_t* cu, int32_t nseg, double* loss_sum,
+                   int64_t* count, double* seg_loss, int64_t* seg_count) {
+    int bad = 0;
+    int32_t cu1[2] = {0, total};
+    if (cu == NULL) { cu = cu1; nseg = 1; }
+    double* row = (double*)calloc((size_t)total, sizeof(double));
+    int8_t* ok = (int8_t*)calloc((size_t)total, 1);
+#pragma omp parallel for schedule(dynamic, 64) reduction(| : bad)
+    for (int64_t i = 0; i < total; ++i) {
+        const int64_t y = labels[i];
+        if (y == -100) continue;
+        if (y < 0 || y >= vocab) { bad = 1; continue; }
+        double mx = -INFINITY;
+        for (int32_t c = 0; c < vocab; ++c) {
+            const int64_t at = i * (int64_t)vocab + c;
+            const double z = is_f64 ? ((const double*)logits)[at]
+                                    : bf16_bits_to_double(((const uint16_t*)logits)[at]);
+            if (z > mx) mx = z;
+        }
+        double s = 0.0, zy = 0.0;
+        for (int32_t c = 0; c < vocab; ++c) {
+            const int64_t at = i * (int64_t)vocab + c;
+            const double z = is_f64 ? ((const double*)logits)[at]
+                                    : bf16_bits_to_double(((const uint16_t*)logits)[at]);
+            s += exp(z - mx);
+            if (c == y) zy = z;
+        }
+        row[i] = (mx + log(s)) - zy;
+        ok[i] = 1;
+    }
+    double tot = 0.0;
+    int64_t cnt = 0;
+    for (int32_t r = 0; r < nseg; ++r) {
+        double sr = 0.0;
+        int64_t nr = 0;
+        for (int64_t i = cu[r]; i < cu[r + 1]; ++i)
+            if (ok[i]) { sr += row[i]; ++nr; }
+        if (seg_loss) seg_loss[r] = sr;
+        if (seg_count) seg_count[r] = nr;
+        tot += sr;
+        cnt += nr;
+    }
+    *loss_sum = tot;
+    *count = cnt;
+    free(row);
+    free(ok);
+    return bad;
 }
 
 int orc_num_threads(void) {

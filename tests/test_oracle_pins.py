@@ -432,3 +432,79 @@ def test_forward_seg_heads_subset_matches_full():
     o2, lse2 = oracle.attn_fwd(q, k, v, w.cu, seg_heads=[(1, 1), (2, 0)])
     assert np.array_equal(o2[4:13, 1], o[4:13, 1]) and np.array_equal(lse2[1, 4:13], lse[1, 4:13])
     assert np.array_equal(o2[13:16, 0], o[13:16, 0]) and not o2[:4].any()
+
+
+# ------------------------------------------------------------------ shifted cross-entropy (next row)
+def test_ce_uniform_logits_closed_form():
+    # uniform logits: every valid target costs ln(vocab)
+    V = 37
+    z = np.zeros((11, V))
+    lab = np.array([0, 5, -100, 36, 1, 2, -100, 3, 4, 9, -100], dtype=np.int64)
+    st, s, n, sl, sc = oracle.shifted_ce(z, lab, [0, 3, 7, 11])
+    assert st == 0 and n == 8
+    assert s == pytest.approx(8 * math.log(V), rel=1e-13)
+    assert list(sc) == [2, 3, 3]
+    assert sl == pytest.approx([2 * math.log(V), 3 * math.log(V), 3 * math.log(V)], rel=1e-13)
+
+
+def test_ce_token_mean_vs_sample_mean_example():
+    # charlestar, "Packing should not decide how much a long sample weighs": A has 2 targets
+    # of loss 1, B has 6 of loss 3; token mean (2 + 18) / 8 = 2.5, sample mean (1 + 3) / 2 = 2.
+    def row(loss):   # two classes, label 1: CE = ln(1 + e^a) = loss
+        return [math.log(math.expm1(loss)), 0.0]
+    z = np.array([row(1.0)] * 3 + [row(3.0)] * 7)
+    lab = np.array([1, 1, -100] + [1] * 6 + [-100], dtype=np.int64)
+    st, s, n, sl, sc = oracle.shifted_ce(z, lab, [0, 3, 10])
+    assert st == 0 and list(sc) == [2, 6]
+    assert sl == pytest.approx([2.0, 18.0], rel=1e-12)
+    assert s / n == pytest.approx(2.5, rel=1e-12)
+    assert np.mean(sl / sc) == pytest.approx(2.0, rel=1e-12)
+
+
+def test_ce_against_torch_cross_entropy():
+    # an independent library routine: torch's fp64 cross_entropy with ignore_index = -100
+    rng = np.random.default_rng(7)
+    T, V = 64, 301
+    z = rng.normal(0, 3, size=(T, V))
+    lab = rng.integers(0, V, size=T)
+    lab[rng.random(T) < 0.2] = -100
+    st, s, n, _, _ = oracle.shifted_ce(z, lab)
+    ref = torch.nn.functional.cross_entropy(torch.from_numpy(z), torch.from_numpy(lab), ignore_index=-100,
+                                            reduction="sum").item()
+    assert st == 0 and n == int((lab != -100).sum())
+    assert s == pytest.approx(ref, rel=1e-12)
+
+
+def test_ce_preshifted_equals_internal_shift():
+    # charlestar, "After isolation one cross-boundary prediction pair remains": the pre-shifted
+    # labels on logit row i and the internal shift (labels = tokens with -100 at every segment
+    # start, logits[:-1] against labels[1:]) give the same pairs, hence the same sum and count.
+    rng = np.random.default_rng(11)
+    lens = [3, 1, 5, 2, 6]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T, V = int(cu[-1]), 23
+    tokens = rng.integers(0, V, size=T).astype(np.int64)
+    z = rng.normal(0, 2, size=(T, V))
+    _, lab = oracle.positions_labels(cu, tokens)
+    st, s, n, sl, sc = oracle.shifted_ce(z, lab, cu)
+    lab2 = tokens.copy()
+    lab2[cu[:-1]] = -100
+    ref = torch.nn.functional.cross_entropy(torch.from_numpy(z[:-1]), torch.from_numpy(lab2[1:]),
+                                            ignore_index=-100, reduction="sum").item()
+    assert st == 0 and n == int((lab2[1:] != -100).sum()) == sum(L - 1 for L in lens)
+    assert s == pytest.approx(ref, rel=1e-12)
+    assert list(sc) == [L - 1 for L in lens]
+
+
+def test_ce_bf16_bits_and_bad_label():
+    rng = np.random.default_rng(3)
+    z = rng.normal(0, 2, size=(8, 40)).astype(np.float32)
+    bits = oracle.bf16_bits(torch.from_numpy(z).to(torch.bfloat16))
+    z64 = oracle.bits_to_f64(bits)
+    lab = rng.integers(0, 40, size=8)
+    a = oracle.shifted_ce(bits, lab)
+    b = oracle.shifted_ce(z64, lab)
+    assert a[0] == 0 and a[1] == pytest.approx(b[1], rel=1e-15) and a[2] == b[2]
+    lab[3] = 40   # outside the vocabulary: flagged and not counted
+    st, s, n, _, _ = oracle.shifted_ce(z64, lab)
+    assert st == 1 and n == 7
