@@ -415,6 +415,20 @@ def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
         sweep[f"T=2^{logT}"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
         del cu, tok, pos, lab
     out["positions_labels_sweep"] = sweep
+    # shifted cross-entropy over this pack's labels with a 32000-token vocabulary (bf16 logits)
+    V = 32000
+    gen = torch.Generator(device=dev).manual_seed(4242)
+    logits = (torch.randn((w.total, V), generator=gen, device=dev) * 2.0).to(torch.bfloat16)
+    ws_ce = torch.empty(vlc.load_library().vlc_ce_workspace_bytes(w.total, w.nseg), dtype=torch.uint8,
+                        device=dev)
+    ms_ce = _time_ms(lambda: vlc.shifted_cross_entropy(logits, step.lab, step.cu, workspace=ws_ce,
+                                                       check=False), 10)
+    rows_read = int((step.lab != -100).sum().item())
+    ce_bytes = rows_read * V * 2.0 + w.total * (8 + 4 + 1 + 4 + 1)
+    out["shifted_cross_entropy"] = {"vocab": V, "rows_read": rows_read, "ms": ms_ce,
+                                    "GB/s": ce_bytes / (ms_ce * 1e-3) / 1e9,
+                                    "frac_hbm": ce_bytes / (ms_ce * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    del logits, ws_ce
     if w.name == "long":
         cu1 = torch.tensor([0, w.total], dtype=torch.int32, device=dev)
         o1 = torch.empty_like(q)

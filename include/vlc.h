@@ -56,7 +56,8 @@ typedef enum {
     VLC_ERR_UNSUPPORTED = 3,   /* head_dim not 64/128, sizes beyond the limits below */
     VLC_ERR_WORKSPACE = 4,     /* workspace pointer null / too small / misaligned */
     VLC_ERR_CUDA = 5,          /* a CUDA runtime call failed */
-    VLC_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up */
+    VLC_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up */
+    VLC_ERR_LABEL = 7          /* device found a label outside [0, vocab) other than -100 */
 } vlc_status;
 
 /* Device error word bits (vlc_get_error folds them into a vlc_status). */
@@ -64,6 +65,7 @@ typedef enum {
 #define VLC_DEVERR_CU_ORDER 0x2    /* some cu[r+1] <= cu[r] */
 #define VLC_DEVERR_CU_TOTAL 0x4    /* cu[nseg] != total */
 #define VLC_DEVERR_MAXLEN 0x8      /* max_seqlen != largest segment length */
+#define VLC_DEVERR_LABEL 0x10      /* a label outside [0, vocab) and not -100 */
 #define VLC_DEVERR_TIMEOUT 0x100   /* a bounded mbarrier wait expired */
 
 /* Limits checked on the host. */
@@ -173,9 +175,34 @@ int vlc_attn_fwd_noalloc(const void* q, const void* k, const void* v, const int3
                          float softmax_scale, float rope_theta, void* o, float* lse,
                          int32_t* err_out, void* stream);
 
+/* Shifted next-token cross-entropy statistics of a packed buffer
+ * ("Sequence packing and variable-length attention", charlestar, sections
+ * "After isolation one cross-boundary prediction pair remains" and "Packing
+ * should not decide how much a long sample weighs").  With pre-shifted labels
+ * (vlc_build_positions_labels), logit row i contributes
+ *   CE_i = ln sum_c exp(logits[i][c]) - logits[i][labels[i]]   if labels[i] != -100.
+ *   logits        bf16 [total, vocab] row-major (vocab >= 1; rows with a -100
+ *                 label are not read)
+ *   labels        int64 [total]
+ *   cu            int32 [nseg + 1] segment offsets, or NULL for one segment
+ *                 covering the buffer (nseg is then ignored and taken as 1)
+ *   loss_sum      float [1]: sum of CE_i over the pack (fp32; accumulated in fp64)
+ *   target_count  int64 [1]: number of rows with a label other than -100
+ *   seg_loss      float [nseg] or NULL: per-segment sums S_r
+ *   seg_count     int32 [nseg] or NULL: per-segment target counts n_r
+ *   ws, ws_bytes  workspace of at least vlc_ce_workspace_bytes(total, nseg) bytes,
+ *                 256-byte aligned; its error word (vlc_get_error) receives
+ *                 VLC_DEVERR_LABEL for an out-of-range label (that row counts
+ *                 nothing) and the VLC_DEVERR_CU_* bits for an invalid cu.
+ * All reductions have a fixed order: results are bitwise reproducible. */
+size_t vlc_ce_workspace_bytes(int32_t total, int32_t nseg);
+int vlc_shifted_ce(const void* logits, int32_t vocab, int32_t total, const int64_t* labels,
+                   const int32_t* cu, int32_t nseg, float* loss_sum, int64_t* target_count,
+                   float* seg_loss, int32_t* seg_count, void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronise `stream` and read the workspace's device error word.
- * Returns VLC_OK, VLC_ERR_CU_SEQLENS or VLC_ERR_TIMEOUT; *bits_out (if not
- * NULL) receives the raw VLC_DEVERR_* bits. */
+ * Returns VLC_OK, VLC_ERR_CU_SEQLENS, VLC_ERR_LABEL or VLC_ERR_TIMEOUT;
+ * *bits_out (if not NULL) receives the raw VLC_DEVERR_* bits. */
 int vlc_get_error(const void* ws, int32_t* bits_out, void* stream);
 
 #ifdef __cplusplus

@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libvlc.so")
 
 VLC_OK, VLC_ERR_ARG, VLC_ERR_CU_SEQLENS, VLC_ERR_UNSUPPORTED = 0, 1, 2, 3
-VLC_ERR_WORKSPACE, VLC_ERR_CUDA, VLC_ERR_TIMEOUT = 4, 5, 6
+VLC_ERR_WORKSPACE, VLC_ERR_CUDA, VLC_ERR_TIMEOUT, VLC_ERR_LABEL = 4, 5, 6, 7
 DEVERR_CU_FIRST, DEVERR_CU_ORDER, DEVERR_CU_TOTAL, DEVERR_MAXLEN = 0x1, 0x2, 0x4, 0x8
 DEVERR_TIMEOUT = 0x100
 WORKLIST_FWD, WORKLIST_BWD = 0, 1
@@ -27,7 +27,7 @@ WORKLIST_FWD, WORKLIST_BWD = 0, 1
 EXPORTED = [
     "vlc_status_string", "vlc_version", "vlc_workspace_bytes", "vlc_worklist_capacity",
     "vlc_build_positions_labels", "vlc_build_worklist", "vlc_attn_fwd", "vlc_attn_bwd",
-    "vlc_get_error", "vlc_attn_fwd_noalloc",
+    "vlc_get_error", "vlc_attn_fwd_noalloc", "vlc_ce_workspace_bytes", "vlc_shifted_ce",
 ]
 
 _lock = threading.Lock()
@@ -77,6 +77,10 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_get_error.restype = cint
         lib.vlc_attn_fwd_noalloc.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, f32, P, P, P, P]
         lib.vlc_attn_fwd_noalloc.restype = cint
+        lib.vlc_ce_workspace_bytes.argtypes = [i32, i32]
+        lib.vlc_ce_workspace_bytes.restype = sz
+        lib.vlc_shifted_ce.argtypes = [P, i32, i32, P, P, i32, P, P, P, P, P, sz, P]
+        lib.vlc_shifted_ce.restype = cint
         _lib = lib
         return lib
 
@@ -242,3 +246,32 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
     if check:
         _raise_device_error(ws, "vlc_attn_bwd")
     return dq, dk, dv
+
+
+def shifted_cross_entropy(logits: torch.Tensor, labels: torch.Tensor,
+                          cu_seqlens: Optional[torch.Tensor] = None, per_segment: bool = False,
+                          workspace: Optional[torch.Tensor] = None, check: bool = True):
+    """Next-token cross-entropy statistics over pre-shifted labels (-100 = ignored):
+    returns (loss_sum fp32 [1], target_count int64 [1]) and, with per_segment, also
+    (seg_loss fp32 [nseg], seg_count int32 [nseg]).  logits: bf16 [total, vocab]."""
+    lib = load_library()
+    _require_cuda(logits, labels, cu_seqlens, workspace)
+    if logits.dtype != torch.bfloat16 or logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous bf16 [total, vocab] tensor")
+    total, vocab = logits.shape
+    if labels.dtype != torch.int64 or labels.numel() != total or not labels.is_contiguous():
+        raise ValueError("labels must be contiguous int64 with one entry per logit row")
+    nseg = 1 if cu_seqlens is None else _cu_info(cu_seqlens)
+    dev = logits.device
+    need = lib.vlc_ce_workspace_bytes(total, nseg)
+    ws = workspace if workspace is not None else torch.empty(need, dtype=torch.uint8, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    count = torch.empty(1, dtype=torch.int64, device=dev)
+    seg_loss = torch.empty(nseg, dtype=torch.float32, device=dev) if per_segment else None
+    seg_count = torch.empty(nseg, dtype=torch.int32, device=dev) if per_segment else None
+    st = lib.vlc_shifted_ce(_ptr(logits), vocab, total, _ptr(labels), _ptr(cu_seqlens), nseg, _ptr(loss),
+                            _ptr(count), _ptr(seg_loss), _ptr(seg_count), _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "vlc_shifted_ce")
+    if check:
+        _raise_device_error(ws, "vlc_shifted_ce")
+    return (loss, count, seg_loss, seg_count) if per_segment else (loss, count)

@@ -116,6 +116,7 @@ const char* vlc_status_string(int status) {
         case VLC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case VLC_ERR_CUDA: return "CUDA error";
         case VLC_ERR_TIMEOUT: return "device wait timed out";
+        case VLC_ERR_LABEL: return "label outside [0, vocab) and not -100";
         default: return "unknown status";
     }
 }
@@ -289,8 +290,30 @@ int vlc_get_error(const void* ws, int32_t* bits_out, void* stream) {
     if (cudaStreamSynchronize(s) != cudaSuccess) return VLC_ERR_CUDA;
     if (bits_out != nullptr) *bits_out = bits;
     if (bits & VLC_DEVERR_TIMEOUT) return VLC_ERR_TIMEOUT;
-    if (bits != 0) return VLC_ERR_CU_SEQLENS;
+    if (bits & ~VLC_DEVERR_LABEL) return VLC_ERR_CU_SEQLENS;
+    if (bits != 0) return VLC_ERR_LABEL;
     return VLC_OK;
+}
+
+size_t vlc_ce_workspace_bytes(int32_t total, int32_t nseg) {
+    if (total < 1 || nseg < 1) return 0;
+    return vlc::ce_layout(total, nseg).total;
+}
+
+int vlc_shifted_ce(const void* logits, int32_t vocab, int32_t total, const int64_t* labels,
+                   const int32_t* cu, int32_t nseg, float* loss_sum, int64_t* target_count,
+                   float* seg_loss, int32_t* seg_count, void* ws, size_t ws_bytes, void* stream) {
+    if (cu == nullptr) nseg = 1;
+    if (logits == nullptr || labels == nullptr || loss_sum == nullptr || target_count == nullptr ||
+        vocab < 1 || total < 1 || nseg < 1)
+        return VLC_ERR_ARG;
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 ||
+        ws_bytes < vlc_ce_workspace_bytes(total, nseg))
+        return VLC_ERR_WORKSPACE;
+    const cudaError_t e = vlc::launch_shifted_ce(logits, vocab, total, labels, cu, nseg, loss_sum,
+                                                 target_count, seg_loss, seg_count,
+                                                 static_cast<uint8_t*>(ws), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VLC_OK : VLC_ERR_CUDA;
 }
 
 }  // extern "C"

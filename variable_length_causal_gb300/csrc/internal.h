@@ -95,4 +95,15 @@ struct BwdParams {
 
 cudaError_t launch_attn_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
 
+// Workspace of the shifted cross-entropy call: header (error word), per-row
+// losses and valid flags, per-segment sums and counts.
+struct CeLayout {
+    size_t header, row_loss, row_valid, seg_loss, seg_count, total;
+};
+CeLayout ce_layout(int32_t total, int32_t nseg);
+
+cudaError_t launch_shifted_ce(const void* logits, int32_t vocab, int32_t total, const int64_t* labels,
+                              const int32_t* cu, int32_t nseg, float* loss_sum, int64_t* count,
+                              float* seg_loss, int32_t* seg_count, uint8_t* ws, cudaStream_t s);
+
 }  // namespace vlc
