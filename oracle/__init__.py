@@ -64,18 +64,18 @@ def _load():
                 f.restype = i64
             lib.orc_rope_rows.argtypes = [P, P, i64, i32, f64, P]
             lib.orc_rope_rows.restype = None
-            lib.orc_attn_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int, P, P]
+            lib.orc_attn_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, f64, ctypes.c_int, P, P]
             lib.orc_attn_fwd.restype = None
-            lib.orc_attn_fwd_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int,
+            lib.orc_attn_fwd_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, f64, ctypes.c_int,
                                               P, P, i64, P, P]
             lib.orc_attn_fwd_rows.restype = None
-            lib.orc_attn_fwd_seg_heads.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int,
-                                                   P, P, i64, P, P]
+            lib.orc_attn_fwd_seg_heads.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, f64,
+                                                   ctypes.c_int, P, P, i64, P, P]
             lib.orc_attn_fwd_seg_heads.restype = None
-            lib.orc_attn_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, f64, ctypes.c_int,
+            lib.orc_attn_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, f64, ctypes.c_int,
                                          P, P, P]
             lib.orc_attn_bwd.restype = None
-            lib.orc_attn_bwd_seg_heads.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, f64,
+            lib.orc_attn_bwd_seg_heads.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, f64,
                                                    ctypes.c_int, P, P, i64, P, P, P]
             lib.orc_attn_bwd_seg_heads.restype = None
             lib.orc_shifted_ce.argtypes = [P, ctypes.c_int, i32, i32, P, P, i32, P, P, P, P]
@@ -165,22 +165,25 @@ def rope_rows(x, pos, theta: float = 10000.0) -> np.ndarray:
 def attn_fwd(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
              seg_heads=None):
     """Exact per-segment causal attention in fp64.  q/k/v: bf16 tensors or uint16 bit arrays
-    [total, H, d].  Returns (o [total, H, d] f64, lse [H, total] f64, natural log).  With
-    ``seg_heads`` (a list of (segment, head) pairs) only those are computed; the rest stay 0."""
+    [total, H, d] (k and v may have fewer heads Hkv dividing H: query head h reads key/value
+    head h // (H // Hkv)).  Returns (o [total, H, d] f64, lse [H, total] f64, natural log).
+    With ``seg_heads`` (a list of (segment, head) pairs) only those are computed; the rest
+    stay 0."""
     qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
     total, H, d = qb.shape
+    Hkv = kb.shape[1]
     cu = _c(cu, np.int32)
     o = np.zeros((total, H, d), np.float64)
     lse = np.zeros((H, total), np.float64)
     if seg_heads is None:
-        _load().orc_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, d,
+        _load().orc_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
                              float(scale), float(theta), int(bool(contract)), _ptr(o), _ptr(lse))
     else:
         sh = np.asarray(seg_heads, np.int32).reshape(-1, 2)
         segs, heads = np.ascontiguousarray(sh[:, 0]), np.ascontiguousarray(sh[:, 1])
         _load().orc_attn_fwd_seg_heads(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H,
-                                       d, float(scale), float(theta), int(bool(contract)), _ptr(segs),
-                                       _ptr(heads), sh.shape[0], _ptr(o), _ptr(lse))
+                                       Hkv, d, float(scale), float(theta), int(bool(contract)),
+                                       _ptr(segs), _ptr(heads), sh.shape[0], _ptr(o), _ptr(lse))
     return o, lse
 
 
@@ -189,13 +192,14 @@ def attn_fwd_rows(q, k, v, cu, rows, heads, scale: float = 0.0, theta: float = 1
     """Forward for selected (token row, head) pairs: returns (o [n, d], lse [n])."""
     qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
     total, H, d = qb.shape
+    Hkv = kb.shape[1]
     cu = _c(cu, np.int32)
     rows = _c(rows, np.int64)
     heads = _c(heads, np.int32)
     n = rows.shape[0]
     o = np.zeros((n, d), np.float64)
     lse = np.zeros(n, np.float64)
-    _load().orc_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, d,
+    _load().orc_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
                               float(scale), float(theta), int(bool(contract)), _ptr(rows),
                               _ptr(heads), n, _ptr(o), _ptr(lse))
     return o, lse
@@ -205,10 +209,11 @@ def attn_fwd_f64(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0):
     """Exact-mode forward on float64 inputs [total, H, d] (finite-difference tests)."""
     q, k, v = (_c(x, np.float64) for x in (q, k, v))
     total, H, d = q.shape
+    Hkv = k.shape[1]
     cu = _c(cu, np.int32)
     o = np.zeros((total, H, d), np.float64)
     lse = np.zeros((H, total), np.float64)
-    _load().orc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, d,
+    _load().orc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
                          float(scale), float(theta), -1, _ptr(o), _ptr(lse))
     return o, lse
 
@@ -217,35 +222,38 @@ def attn_bwd_f64(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0):
     """Exact-mode gradients on float64 inputs (finite-difference tests)."""
     g, q, k, v = (_c(x, np.float64) for x in (dout, q, k, v))
     total, H, d = q.shape
+    Hkv = k.shape[1]
     cu = _c(cu, np.int32)
     dq = np.zeros((total, H, d), np.float64)
-    dk = np.zeros_like(dq)
-    dv = np.zeros_like(dq)
-    _load().orc_attn_bwd(_ptr(g), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, d,
+    dk = np.zeros((total, Hkv, d), np.float64)
+    dv = np.zeros_like(dk)
+    _load().orc_attn_bwd(_ptr(g), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
                          float(scale), float(theta), -1, _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
 
 
 def attn_bwd(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
              seg_heads=None):
-    """Gradients (dq, dk, dv) [total, H, d] f64 of sum(O * dO).  With ``seg_heads`` (a list of
-    (segment, head) pairs) only those segment-heads are computed; other entries stay 0."""
+    """Gradients (dq [total, H, d], dk and dv [total, Hkv, d]) f64 of sum(O * dO).  With
+    ``seg_heads`` (a list of (segment, key/value head) pairs) only those are computed (dq for
+    every query head of each pair's group); other entries stay 0."""
     gb, qb, kb, vb = bf16_bits(dout), bf16_bits(q), bf16_bits(k), bf16_bits(v)
     total, H, d = qb.shape
+    Hkv = kb.shape[1]
     cu = _c(cu, np.int32)
     dq = np.zeros((total, H, d), np.float64)
-    dk = np.zeros_like(dq)
-    dv = np.zeros_like(dq)
+    dk = np.zeros((total, Hkv, d), np.float64)
+    dv = np.zeros_like(dk)
     lib = _load()
     if seg_heads is None:
-        lib.orc_attn_bwd(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, d,
+        lib.orc_attn_bwd(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
                          float(scale), float(theta), int(bool(contract)), _ptr(dq), _ptr(dk), _ptr(dv))
     else:
         sh = np.asarray(seg_heads, np.int32).reshape(-1, 2)
         segs = np.ascontiguousarray(sh[:, 0])
         heads = np.ascontiguousarray(sh[:, 1])
         lib.orc_attn_bwd_seg_heads(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1,
-                                   total, H, d, float(scale), float(theta), int(bool(contract)),
+                                   total, H, Hkv, d, float(scale), float(theta), int(bool(contract)),
                                    _ptr(segs), _ptr(heads), sh.shape[0], _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
 

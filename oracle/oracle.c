@@ -15,6 +15,8 @@
  *      - "EOS is content; isolation happens before softmax":
  *        allow(i,j) = (s_i == s_j) and (p_j <= p_i); additive mask M (0 / -inf)
  *        added to QK^T/sqrt(d) before the softmax, O = softmax(QK^T/sqrt(d)+M) V.
+ *      Grouped key/value heads (Hkv dividing H, query head h reading key/value head
+ *      h / (H / Hkv)) are this library's extension of the pages' equal-head setting.
  *      - "Positions are reset per segment; the pure-RoPE argument": fixed-frequency
  *        RoPE rotation R(p) with (R(m+c)q)^T (R(n+c)k) = q^T R(n-m) k.
  *      - "After isolation one cross-boundary prediction pair remains": the
@@ -254,16 +256,22 @@ typedef struct {
     const void *q, *k, *v, *dout;       /* [total][H][d]: bf16 bits, or fp64 when f64_inputs */
     int f64_inputs;
     const int32_t* cu;
-    int32_t nseg, total, H, d;
+    int32_t nseg, total, H, Hkv, d;      /* q / dO have H heads, k / v have Hkv (H % Hkv == 0) */
     double scale, theta;                 /* theta == 0: no RoPE */
     int contract;
 } orc_problem;
+
+/* Grouped heads: query head h reads key/value head h / (H / Hkv), so each run of
+ * H / Hkv consecutive query heads shares one key/value head (Hkv == H is plain
+ * multi-head attention). */
+static int32_t kv_head(const orc_problem* P, int32_t h) { return h / (P->H / P->Hkv); }
 
 /* q' (or k') for token row i of head h: widen, rotate by its local position,
  * and round to bf16 in contract mode. */
 /* Element c of token row i, head h of an input tensor, widened to fp64. */
 static double input_elem(const orc_problem* P, const void* x, int64_t i, int32_t h, int c) {
-    size_t off = ((size_t)i * P->H + h) * P->d + c;
+    const int32_t nh = (x == P->k || x == P->v) ? P->Hkv : P->H;
+    size_t off = ((size_t)i * nh + h) * P->d + c;
     if (P->f64_inputs) return ((const double*)x)[off];
     return bf16_bits_to_double(((const uint16_t*)x)[off]);
 }
@@ -305,8 +313,8 @@ static void seg_head_load(const orc_problem* P, int32_t r, int32_t h, int want_g
     for (int64_t p = 0; p < S->L; ++p) {
         int64_t i = S->base + p;
         load_rotated(P, P->q, i, h, p, S->q + p * d);
-        load_rotated(P, P->k, i, h, p, S->k + p * d);
-        load_plain(P, P->v, i, h, S->v + p * d);
+        load_rotated(P, P->k, i, kv_head(P, h), p, S->k + p * d);
+        load_plain(P, P->v, i, kv_head(P, h), S->v + p * d);
         if (want_grad) load_plain(P, P->dout, i, h, S->g + p * d);
     }
 }
@@ -348,13 +356,13 @@ static double fwd_row(const seg_head* S, int64_t p, int d, double scale, double*
 
 static orc_problem make_problem(const void* q, const void* k, const void* v,
                                 const void* dout, const int32_t* cu, int32_t nseg,
-                                int32_t total, int32_t H, int32_t d, double scale,
+                                int32_t total, int32_t H, int32_t Hkv, int32_t d, double scale,
                                 double theta, int contract) {
     orc_problem P;
     P.q = q; P.k = k; P.v = v; P.dout = dout; P.cu = cu;
     P.f64_inputs = contract < 0;   /* contract == -1 selects fp64 inputs, exact mode */
     if (contract < 0) contract = 0;
-    P.nseg = nseg; P.total = total; P.H = H; P.d = d;
+    P.nseg = nseg; P.total = total; P.H = H; P.Hkv = Hkv; P.d = d;
     P.scale = scale > 0.0 ? scale : 1.0 / sqrt((double)d);
     P.theta = theta; P.contract = contract;
     return P;
@@ -364,9 +372,9 @@ static void fwd_seg_head(const orc_problem* P, int32_t r, int32_t h, double* o, 
 
 /* Full forward: o [total][H][d], lse [H][total] (natural log). */
 void orc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
-                  int32_t nseg, int32_t total, int32_t H, int32_t d, double scale, double theta,
-                  int contract, double* o, double* lse) {
-    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, d, scale, theta, contract);
+                  int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d, double scale,
+                  double theta, int contract, double* o, double* lse) {
+    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, Hkv, d, scale, theta, contract);
     int64_t nwork = (int64_t)nseg * H;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t w = 0; w < nwork; ++w) fwd_seg_head(&P, (int32_t)(w / H), (int32_t)(w % H), o, lse);
@@ -387,10 +395,10 @@ static void fwd_seg_head(const orc_problem* P, int32_t r, int32_t h, double* o, 
 
 /* Forward restricted to a set of (segment, head) pairs; other entries untouched. */
 void orc_attn_fwd_seg_heads(const void* q, const void* k, const void* v, const int32_t* cu,
-                            int32_t nseg, int32_t total, int32_t H, int32_t d, double scale,
-                            double theta, int contract, const int32_t* segs, const int32_t* heads,
-                            int64_t n, double* o, double* lse) {
-    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, d, scale, theta, contract);
+                            int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
+                            double scale, double theta, int contract, const int32_t* segs,
+                            const int32_t* heads, int64_t n, double* o, double* lse) {
+    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, Hkv, d, scale, theta, contract);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < n; ++t) fwd_seg_head(&P, segs[t], heads[t], o, lse);
 }
@@ -398,10 +406,10 @@ void orc_attn_fwd_seg_heads(const void* q, const void* k, const void* v, const i
 /* Sampled forward: the same result for selected (token, head) pairs only,
  * so that full-size problems can be checked row by row. */
 void orc_attn_fwd_rows(const void* q, const void* k, const void* v, const int32_t* cu,
-                       int32_t nseg, int32_t total, int32_t H, int32_t d, double scale,
-                       double theta, int contract, const int64_t* rows, const int32_t* heads,
-                       int64_t n, double* o, double* lse) {
-    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, d, scale, theta, contract);
+                       int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
+                       double scale, double theta, int contract, const int64_t* rows,
+                       const int32_t* heads, int64_t n, double* o, double* lse) {
+    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, Hkv, d, scale, theta, contract);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < n; ++t) {
         int64_t i = rows[t];
@@ -418,8 +426,8 @@ void orc_attn_fwd_rows(const void* q, const void* k, const void* v, const int32_
         S.g = NULL;
         load_rotated(&P, q, i, h, p, S.q + p * d);
         for (int64_t j = 0; j <= p; ++j) {
-            load_rotated(&P, k, S.base + j, h, j, S.k + j * d);
-            load_plain(&P, v, S.base + j, h, S.v + j * d);
+            load_rotated(&P, k, S.base + j, kv_head(&P, h), j, S.k + j * d);
+            load_plain(&P, v, S.base + j, kv_head(&P, h), S.v + j * d);
         }
         double* s = (double*)malloc(sizeof(double) * (size_t)(p + 1));
         lse[t] = fwd_row(&S, p, d, P.scale, s, o + t * d);
@@ -428,76 +436,82 @@ void orc_attn_fwd_rows(const void* q, const void* k, const void* v, const int32_
     }
 }
 
-/* Backward of one segment-head (the standard softmax-attention derivatives):
+/* Backward of one segment and one key/value head (the standard softmax-attention
+ * derivatives), for every query head h of its group:
  *   P = exp(S - LSE) on allowed entries, dV = P^T dO, dP = dO V^T,
  *   D_p = sum_j P_pj dP_pj, dS = P o (dP - D), dQ' = scale dS K', dK' = scale dS^T Q',
- * then dQ = R(p)^T dQ', dK = R(p)^T dK'.
- * dq/dk/dv are written at the segment's rows (layout [total][H][d]). */
-static void bwd_seg_head(const orc_problem* P, int32_t r, int32_t h, double* dq, double* dk,
-                         double* dv) {
+ * then dQ = R(p)^T dQ', dK = R(p)^T dK'; the group's contributions to dK and dV
+ * add up (each query head reads the shared K and V).  dq has H heads, dk/dv Hkv. */
+static void bwd_seg_kvhead(const orc_problem* P, int32_t r, int32_t hk, double* dq, double* dk,
+                           double* dv) {
     int d = P->d;
-    seg_head S;
-    seg_head_load(P, r, h, 1, &S);
-    int64_t L = S.L;
-    double* lse = (double*)malloc(sizeof(double) * (size_t)L);
-    double* s = (double*)malloc(sizeof(double) * (size_t)L);
-    for (int64_t p = 0; p < L; ++p) lse[p] = softmax_row(&S, p, d, P->scale, s);
-    double* gq = (double*)calloc((size_t)L * d, sizeof(double));
+    const int32_t group = P->H / P->Hkv;
+    const int64_t L = (int64_t)P->cu[r + 1] - P->cu[r], base = P->cu[r];
     double* gk = (double*)calloc((size_t)L * d, sizeof(double));
     double* gv = (double*)calloc((size_t)L * d, sizeof(double));
+    double* gq = (double*)malloc(sizeof(double) * (size_t)L * d);
+    double* lse = (double*)malloc(sizeof(double) * (size_t)L);
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
     double* pr = (double*)malloc(sizeof(double) * (size_t)L);
     double* dp = (double*)malloc(sizeof(double) * (size_t)L);
-    for (int64_t p = 0; p < L; ++p) {
-        double D = 0.0;
-        for (int64_t j = 0; j <= p; ++j) {
-            pr[j] = exp(dot(S.q + p * d, S.k + j * d, d) * P->scale - lse[p]);
-            dp[j] = dot(S.g + p * d, S.v + j * d, d);
-            D += pr[j] * dp[j];
-        }
-        for (int64_t j = 0; j <= p; ++j) {
-            double ds = pr[j] * (dp[j] - D);
-            for (int c = 0; c < d; ++c) {
-                gv[j * d + c] += pr[j] * S.g[p * d + c];
-                gq[p * d + c] += P->scale * ds * S.k[j * d + c];
-                gk[j * d + c] += P->scale * ds * S.q[p * d + c];
+    for (int32_t h = hk * group; h < (hk + 1) * group; ++h) {
+        seg_head S;
+        seg_head_load(P, r, h, 1, &S);
+        for (int64_t p = 0; p < L; ++p) lse[p] = softmax_row(&S, p, d, P->scale, s);
+        memset(gq, 0, sizeof(double) * (size_t)L * d);
+        for (int64_t p = 0; p < L; ++p) {
+            double D = 0.0;
+            for (int64_t j = 0; j <= p; ++j) {
+                pr[j] = exp(dot(S.q + p * d, S.k + j * d, d) * P->scale - lse[p]);
+                dp[j] = dot(S.g + p * d, S.v + j * d, d);
+                D += pr[j] * dp[j];
+            }
+            for (int64_t j = 0; j <= p; ++j) {
+                double ds = pr[j] * (dp[j] - D);
+                for (int c = 0; c < d; ++c) {
+                    gv[j * d + c] += pr[j] * S.g[p * d + c];
+                    gq[p * d + c] += P->scale * ds * S.k[j * d + c];
+                    gk[j * d + c] += P->scale * ds * S.q[p * d + c];
+                }
             }
         }
+        for (int64_t p = 0; p < L; ++p) {
+            size_t off = ((size_t)(base + p) * P->H + h) * d;
+            if (P->theta != 0.0) rope_rotate_transpose(gq + p * d, dq + off, p, d, P->theta);
+            else memcpy(dq + off, gq + p * d, sizeof(double) * (size_t)d);
+        }
+        seg_head_free(&S);
     }
     for (int64_t p = 0; p < L; ++p) {
-        size_t off = ((size_t)(S.base + p) * P->H + h) * d;
-        if (P->theta != 0.0) {
-            rope_rotate_transpose(gq + p * d, dq + off, p, d, P->theta);
-            rope_rotate_transpose(gk + p * d, dk + off, p, d, P->theta);
-        } else {
-            memcpy(dq + off, gq + p * d, sizeof(double) * (size_t)d);
-            memcpy(dk + off, gk + p * d, sizeof(double) * (size_t)d);
-        }
+        size_t off = ((size_t)(base + p) * P->Hkv + hk) * d;
+        if (P->theta != 0.0) rope_rotate_transpose(gk + p * d, dk + off, p, d, P->theta);
+        else memcpy(dk + off, gk + p * d, sizeof(double) * (size_t)d);
         memcpy(dv + off, gv + p * d, sizeof(double) * (size_t)d);
     }
     free(lse); free(s); free(gq); free(gk); free(gv); free(pr); free(dp);
-    seg_head_free(&S);
 }
 
 void orc_attn_bwd(const void* dout, const void* q, const void* k, const void* v,
-                  const int32_t* cu, int32_t nseg, int32_t total, int32_t H, int32_t d,
+                  const int32_t* cu, int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
                   double scale, double theta, int contract, double* dq, double* dk, double* dv) {
-    orc_problem P = make_problem(q, k, v, dout, cu, nseg, total, H, d, scale, theta, contract);
-    int64_t nwork = (int64_t)nseg * H;
+    orc_problem P = make_problem(q, k, v, dout, cu, nseg, total, H, Hkv, d, scale, theta, contract);
+    int64_t nwork = (int64_t)nseg * Hkv;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t w = 0; w < nwork; ++w)
-        bwd_seg_head(&P, (int32_t)(w / H), (int32_t)(w % H), dq, dk, dv);
+        bwd_seg_kvhead(&P, (int32_t)(w / Hkv), (int32_t)(w % Hkv), dq, dk, dv);
 }
 
-/* Backward restricted to a set of (segment, head) pairs; the other rows of
- * dq/dk/dv are left untouched.  Used for sampled checks at full size. */
+/* Backward restricted to a set of (segment, key/value head) pairs: dq of every
+ * query head of each pair's group and dk/dv of the pair; the other rows are left
+ * untouched.  Used for sampled checks at full size. */
 void orc_attn_bwd_seg_heads(const void* dout, const void* q, const void* k,
                             const void* v, const int32_t* cu, int32_t nseg, int32_t total,
-                            int32_t H, int32_t d, double scale, double theta, int contract,
-                            const int32_t* segs, const int32_t* heads, int64_t n, double* dq,
-                            double* dk, double* dv) {
-    orc_problem P = make_problem(q, k, v, dout, cu, nseg, total, H, d, scale, theta, contract);
+                            int32_t H, int32_t Hkv, int32_t d, double scale, double theta,
+                            int contract, const int32_t* segs, const int32_t* heads, int64_t n,
+                            double* dq, double* dk, double* dv) {
+    orc_problem P = make_problem(q, k, v, dout, cu, nseg, total, H, Hkv, d, scale, theta, contract);
 #pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t t = 0; t < n; ++t) bwd_seg_head(&P, segs[t], heads[t], dq, dk, dv);
+    for (int64_t t = 0; t < n; ++t) bwd_seg_kvhead(&P, segs[t], heads[t], dq, dk, dv);
 }
 
 /* ---------------------------------------------------------------- shifted cross-entropy

@@ -30,6 +30,8 @@ MUTATIONS = {
     "worklist_extra_tile": ("items[4 * n + 3] = (int32_t)ceil_div(last_row, BN);",
                             "items[4 * n + 3] = (int32_t)ceil_div(last_row, BN) + (t == 0);"),
     "worklist_unstable_ties": ("if (ny >= nx) break;", "if (ny > nx) break;"),
+    "gqa_interleaved_heads": ("static int32_t kv_head(const orc_problem* P, int32_t h) { return h / (P->H / P->Hkv); }",
+                              "static int32_t kv_head(const orc_problem* P, int32_t h) { return h % P->Hkv; }"),
     "ce_label_logit_sign": ("row[i] = (mx + log(s)) - zy;", "row[i] = (mx + log(s)) + zy;"),
     "ce_max_not_restored": ("row[i] = (mx + log(s)) - zy;", "row[i] = log(s) - zy;"),
     "ce_counts_ignored": ("if (ok[i]) { sr += row[i]; ++nr; }", "{ sr += row[i]; ++nr; }"),

@@ -290,11 +290,13 @@ def test_round_bf16_against_torch():
 
 # ------------------------------------------------------------------ attention backward
 
-def _fd_check(lens, H, d, theta, seed):
+def _fd_check(lens, H, d, theta, seed, Hkv=None):
     rng = np.random.default_rng(seed)
     w = synth.custom_workload(lens, H, d)
     T = w.total
-    q, k, v, g = (rng.standard_normal((T, H, d)) for _ in range(4))
+    Hkv = H if Hkv is None else Hkv
+    q, g = (rng.standard_normal((T, H, d)) for _ in range(2))
+    k, v = (rng.standard_normal((T, Hkv, d)) for _ in range(2))
     dq, dk, dv = oracle.attn_bwd_f64(g, q, k, v, w.cu, theta=theta)
     eps = 1e-6
 
@@ -319,6 +321,46 @@ def test_backward_finite_differences(theta):
     """charlestar, 'change A, B must not change' (its CPU recheck uses finite differences
     for the Q/K/V gradients)."""
     _fd_check([3, 1, 5], 2, 8, theta, seed=7)
+
+
+@pytest.mark.parametrize("theta", [0.0, 10000.0])
+def test_backward_finite_differences_grouped_heads(theta):
+    # four query heads sharing two key/value heads: dK and dV sum the group's contributions
+    _fd_check([4, 2, 3], 4, 8, theta, seed=8, Hkv=2)
+
+
+def _rope_torch(x, pos, d, theta=10000.0):
+    half = d // 2
+    wfreq = theta ** (-2.0 * torch.arange(half, dtype=torch.float64) / d)
+    rot = torch.polar(torch.ones(len(pos), half, dtype=torch.float64), pos[:, None] * wfreq[None])
+    z = torch.complex(x[..., :half], x[..., half:]) * rot[:, None, :]
+    return torch.cat([z.real, z.imag], dim=-1)
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (8, 1), (6, 3)])
+def test_grouped_heads_against_torch_sdpa_autograd(H, Hkv):
+    # torch fp64 SDPA with enable_gqa (query head h reads key/value head h // (H // Hkv)) and a
+    # boolean block mask, differentiated by autograd, against the oracle's forward and backward
+    lens = [5, 1, 7, 3]
+    d = 16
+    w = synth.custom_workload(lens, H, d)
+    g0 = torch.Generator().manual_seed(31)
+    q, g = (torch.randn((w.total, H, d), generator=g0).bfloat16() for _ in range(2))
+    k, v = (torch.randn((w.total, Hkv, d), generator=g0).bfloat16() for _ in range(2))
+    pos = torch.from_numpy(brute.local_positions(w.cu)).double()
+    qt, kt, vt = (torch.from_numpy(_f64(x)).requires_grad_() for x in (q, k, v))
+    mask = torch.from_numpy(brute.block_causal_allow(w.cu))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        _rope_torch(qt, pos, d).permute(1, 0, 2), _rope_torch(kt, pos, d).permute(1, 0, 2),
+        vt.permute(1, 0, 2), attn_mask=mask, enable_gqa=True).permute(1, 0, 2)
+    (o * torch.from_numpy(_f64(g))).sum().backward()
+    o_orc, _ = oracle.attn_fwd(q, k, v, w.cu, contract=False)
+    assert np.max(np.abs(o_orc - o.detach().numpy())) < 1e-12
+    dq, dk, dv = oracle.attn_bwd(g, q, k, v, w.cu, contract=False)
+    assert dk.shape == (w.total, Hkv, d)
+    assert np.max(np.abs(dq - qt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dk - kt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dv - vt.grad.numpy())) < 1e-11
 
 
 def test_backward_against_torch_autograd():
