@@ -152,6 +152,25 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
                  int32_t d, int32_t max_seqlen, float softmax_scale, float rope_theta, void* dq,
                  void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
+/* Grouped key/value heads (an extension of the pages' equal-head setting, which
+ * they list next to the varlen interface): k, v, dk, dv are [total, H_kv, d] with
+ * H_kv dividing H, and query head h attends with key/value head h / (H / H_kv);
+ * dk and dv sum the contributions of the H / H_kv query heads of their group.
+ * Everything else is as in vlc_attn_fwd / vlc_attn_bwd, which are these calls
+ * with H_kv = H.  Workspace sizes come from vlc_workspace_bytes_gqa (the
+ * backward's rotated-k copy has H_kv heads). */
+size_t vlc_workspace_bytes_gqa(int32_t nseg, int32_t total, int32_t H, int32_t H_kv, int32_t d,
+                               int32_t max_seqlen, int is_bwd);
+int vlc_attn_fwd_gqa(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                     int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                     float softmax_scale, float rope_theta, void* o, float* lse, void* ws,
+                     size_t ws_bytes, void* stream);
+int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
+                     int32_t H_kv, int32_t d, int32_t max_seqlen, float softmax_scale,
+                     float rope_theta, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                     void* stream);
+
 /* Forward attention for callers that cannot allocate device memory.  No
  * counterpart on the pages: it exists for callers that may not obtain memory
  * per call, such as code running inside another runtime's execution hook (a

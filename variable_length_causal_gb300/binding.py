@@ -28,6 +28,7 @@ EXPORTED = [
     "vlc_status_string", "vlc_version", "vlc_workspace_bytes", "vlc_worklist_capacity",
     "vlc_build_positions_labels", "vlc_build_worklist", "vlc_attn_fwd", "vlc_attn_bwd",
     "vlc_get_error", "vlc_attn_fwd_noalloc", "vlc_ce_workspace_bytes", "vlc_shifted_ce",
+    "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa",
 ]
 
 _lock = threading.Lock()
@@ -81,6 +82,13 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_ce_workspace_bytes.restype = sz
         lib.vlc_shifted_ce.argtypes = [P, i32, i32, P, P, i32, P, P, P, P, P, sz, P]
         lib.vlc_shifted_ce.restype = cint
+        lib.vlc_workspace_bytes_gqa.argtypes = [i32, i32, i32, i32, i32, i32, cint]
+        lib.vlc_workspace_bytes_gqa.restype = sz
+        lib.vlc_attn_fwd_gqa.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, P, P, P, sz, P]
+        lib.vlc_attn_fwd_gqa.restype = cint
+        lib.vlc_attn_bwd_gqa.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32,
+                                         P, P, P, P, sz, P]
+        lib.vlc_attn_bwd_gqa.restype = cint
         _lib = lib
         return lib
 
@@ -110,12 +118,16 @@ def _cu_info(cu_seqlens: torch.Tensor):
     return cu_seqlens.numel() - 1
 
 
-def workspace_bytes(nseg: int, total: int, H: int, d: int, max_seqlen: int, backward: bool) -> int:
-    return int(load_library().vlc_workspace_bytes(nseg, total, H, d, max_seqlen, int(backward)))
+def workspace_bytes(nseg: int, total: int, H: int, d: int, max_seqlen: int, backward: bool,
+                    H_kv: Optional[int] = None) -> int:
+    """Workspace bytes for the forward (backward=False) or backward call; H_kv key/value heads
+    (default H)."""
+    return int(load_library().vlc_workspace_bytes_gqa(nseg, total, H, H if H_kv is None else H_kv, d,
+                                                      max_seqlen, int(backward)))
 
 
-def new_workspace(nseg, total, H, d, max_seqlen, backward, device) -> torch.Tensor:
-    n = workspace_bytes(nseg, total, H, d, max_seqlen, backward)
+def new_workspace(nseg, total, H, d, max_seqlen, backward, device, H_kv=None) -> torch.Tensor:
+    n = workspace_bytes(nseg, total, H, d, max_seqlen, backward, H_kv)
     if n == 0:
         raise VlcError(VLC_ERR_UNSUPPORTED, "workspace_bytes")
     return torch.empty(n, dtype=torch.uint8, device=device)
@@ -188,13 +200,25 @@ def _scale(softmax_scale, d):
     return float(softmax_scale) if softmax_scale else 1.0 / math.sqrt(d)
 
 
-def _check_qkv(*ts):
-    ref = ts[0]
-    for t in ts:
+def _check_qkv(qs, kvs):
+    """qs: tensors shaped like q [total, H, d]; kvs: shaped like k [total, H_kv, d] with
+    H_kv dividing H.  Returns H_kv."""
+    ref = qs[0]
+    for t in list(qs) + list(kvs):
         if t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
-            raise ValueError("q/k/v/o tensors must be contiguous bf16 [total, H, d]")
-        if t.shape != ref.shape or t.device != ref.device:
-            raise ValueError("q/k/v/o tensors must share shape and device")
+            raise ValueError("q/k/v/o tensors must be contiguous bf16 [total, heads, d]")
+        if t.device != ref.device:
+            raise ValueError("q/k/v/o tensors must share a device")
+    for t in qs:
+        if t.shape != ref.shape:
+            raise ValueError("q, o and dO must share one shape [total, H, d]")
+    kref = kvs[0]
+    for t in kvs:
+        if t.shape != kref.shape:
+            raise ValueError("k and v must share one shape [total, H_kv, d]")
+    if kref.shape[0] != ref.shape[0] or kref.shape[2] != ref.shape[2] or ref.shape[1] % kref.shape[1]:
+        raise ValueError("k/v must be [total, H_kv, d] with H_kv dividing q's H")
+    return kref.shape[1]
 
 
 def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
@@ -202,18 +226,19 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     rope_theta: float = 10000.0, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     check: bool = True):
-    """Segment-local causal attention with per-segment RoPE reset.  Returns (O, LSE[H, total])."""
+    """Segment-local causal attention with per-segment RoPE reset.  Returns (O, LSE[H, total]).
+    k and v may have fewer heads than q (grouped: query head h reads head h // (H // H_kv))."""
     lib = load_library()
     _require_cuda(q, k, v, cu_seqlens)
-    _check_qkv(q, k, v)
+    H_kv = _check_qkv([q] + ([] if out is None else [out]), [k, v])
     total, H, d = q.shape
     nseg = _cu_info(cu_seqlens)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
-    ws = new_workspace(nseg, total, H, d, max_seqlen, False, q.device) if workspace is None else workspace
-    st = lib.vlc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseg, total, H, d,
-                          int(max_seqlen), _scale(softmax_scale, d), float(rope_theta), _ptr(out),
-                          _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device))
+    ws = new_workspace(nseg, total, H, d, max_seqlen, False, q.device, H_kv) if workspace is None else workspace
+    st = lib.vlc_attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseg, total, H, H_kv, d,
+                              int(max_seqlen), _scale(softmax_scale, d), float(rope_theta), _ptr(out),
+                              _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device))
     _check(st, "vlc_attn_fwd")
     if check:
         _raise_device_error(ws, "vlc_attn_fwd")
@@ -226,10 +251,10 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                     dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
                     dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     check: bool = True):
-    """Gradients (dQ, dK, dV) of sum(O * dO) for the forward above."""
+    """Gradients (dQ, dK, dV) of sum(O * dO) for the forward above (dK, dV shaped like k, v)."""
     lib = load_library()
     _require_cuda(dout, q, k, v, o, lse, cu_seqlens)
-    _check_qkv(dout, q, k, v, o)
+    H_kv = _check_qkv([q, dout, o], [k, v])
     total, H, d = q.shape
     nseg = _cu_info(cu_seqlens)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
@@ -237,11 +262,11 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws = new_workspace(nseg, total, H, d, max_seqlen, True, q.device) if workspace is None else workspace
-    st = lib.vlc_attn_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                          _ptr(cu_seqlens), nseg, total, H, d, int(max_seqlen),
-                          _scale(softmax_scale, d), float(rope_theta), _ptr(dq), _ptr(dk), _ptr(dv),
-                          _ptr(ws), ws.numel(), _stream(q.device))
+    ws = new_workspace(nseg, total, H, d, max_seqlen, True, q.device, H_kv) if workspace is None else workspace
+    st = lib.vlc_attn_bwd_gqa(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                              _ptr(cu_seqlens), nseg, total, H, H_kv, d, int(max_seqlen),
+                              _scale(softmax_scale, d), float(rope_theta), _ptr(dq), _ptr(dk), _ptr(dv),
+                              _ptr(ws), ws.numel(), _stream(q.device))
     _check(st, "vlc_attn_bwd")
     if check:
         _raise_device_error(ws, "vlc_attn_bwd")

@@ -19,8 +19,8 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 static int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t max_seqlen,
-                   int is_bwd) {
+WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
+                   int32_t max_seqlen, int is_bwd) {
     WsLayout L{};
     const int min_tile = is_bwd ? (kBwdBM < kFwdBM ? kBwdBM : kFwdBM) : kFwdBM;
     L.item_cap = static_cast<int64_t>(nseg) + static_cast<int64_t>(total) / min_tile + 1;
@@ -40,11 +40,10 @@ WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t ma
     if (is_bwd) {
         L.delta = off;
         off = align256(off + sizeof(float) * static_cast<size_t>(H) * total);
-        const size_t qkbytes = static_cast<size_t>(total) * H * d * 2;
         L.qrot = off;
-        off = align256(off + qkbytes);
+        off = align256(off + static_cast<size_t>(total) * H * d * 2);
         L.krot = off;
-        off = align256(off + qkbytes);
+        off = align256(off + static_cast<size_t>(total) * Hkv * d * 2);
     }
     L.total = off;
     return L;
@@ -123,12 +122,17 @@ const char* vlc_status_string(int status) {
 
 int vlc_version(void) { return 100; }
 
+size_t vlc_workspace_bytes_gqa(int32_t nseg, int32_t total, int32_t H, int32_t H_kv, int32_t d,
+                               int32_t max_seqlen, int is_bwd) {
+    if (nseg < 1 || total < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || (d != 64 && d != 128) ||
+        max_seqlen < 1 || max_seqlen > VLC_MAX_SEQLEN)
+        return 0;
+    return ws_layout(nseg, total, H, H_kv, d, max_seqlen, is_bwd ? 1 : 0).total;
+}
+
 size_t vlc_workspace_bytes(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t max_seqlen,
                            int is_bwd) {
-    if (nseg < 1 || total < 1 || H < 1 || (d != 64 && d != 128) || max_seqlen < 1 ||
-        max_seqlen > VLC_MAX_SEQLEN)
-        return 0;
-    return ws_layout(nseg, total, H, d, max_seqlen, is_bwd ? 1 : 0).total;
+    return vlc_workspace_bytes_gqa(nseg, total, H, H, d, max_seqlen, is_bwd);
 }
 
 int64_t vlc_worklist_capacity(int32_t nseg, int32_t total, int32_t tile) {
@@ -172,31 +176,33 @@ int vlc_build_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t m
     return e == cudaSuccess ? VLC_OK : VLC_ERR_CUDA;
 }
 
-static int check_attn_args(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t max_seqlen,
-                           void* ws, size_t ws_bytes, int is_bwd) {
+static int check_attn_args(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
+                           int32_t max_seqlen, void* ws, size_t ws_bytes, int is_bwd) {
     if (nseg < 1 || total < 1 || H < 1 || max_seqlen < 1) return VLC_ERR_ARG;
+    if (Hkv < 1 || H % Hkv != 0) return VLC_ERR_ARG;
     if (d != 64 && d != 128) return VLC_ERR_UNSUPPORTED;
     if (max_seqlen > VLC_MAX_SEQLEN) return VLC_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(total) * H * d > (int64_t(1) << 40)) return VLC_ERR_UNSUPPORTED;
     if (ws == nullptr || !aligned(ws, 256)) return VLC_ERR_WORKSPACE;
-    if (ws_bytes < ws_layout(nseg, total, H, d, max_seqlen, is_bwd).total) return VLC_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(nseg, total, H, Hkv, d, max_seqlen, is_bwd).total) return VLC_ERR_WORKSPACE;
     return VLC_OK;
 }
 
-int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
-                 int32_t total, int32_t H, int32_t d, int32_t max_seqlen, float softmax_scale,
-                 float rope_theta, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+int vlc_attn_fwd_gqa(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                     int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                     float softmax_scale, float rope_theta, void* o, float* lse, void* ws,
+                     size_t ws_bytes, void* stream) {
     if (q == nullptr || k == nullptr || v == nullptr || cu == nullptr || o == nullptr ||
         lse == nullptr)
         return VLC_ERR_ARG;
-    int st = check_attn_args(nseg, total, H, d, max_seqlen, ws, ws_bytes, 0);
+    int st = check_attn_args(nseg, total, H, H_kv, d, max_seqlen, ws, ws_bytes, 0);
     if (st != VLC_OK) return st;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
         !aligned(lse, 4))
         return VLC_ERR_ARG;
     if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return VLC_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const WsLayout L = ws_layout(nseg, total, H, d, max_seqlen, 0);
+    const WsLayout L = ws_layout(nseg, total, H, H_kv, d, max_seqlen, 0);
     uint8_t* w = static_cast<uint8_t*>(ws);
     WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
     int4* items = reinterpret_cast<int4*>(w + L.items);
@@ -217,7 +223,7 @@ int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
     p.items = items; p.seg_base = seg_base; p.count = &hdr->count; p.err = &hdr->err;
     p.next = &hdr->next[0];
     p.table = rope ? table : nullptr;
-    p.nseg = nseg; p.total = total; p.H = H; p.d = d;
+    p.nseg = nseg; p.total = total; p.H = H; p.d = d; p.Hkv = H_kv;
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
     p.scale_log2 = scale * 1.4426950408889634f;
     p.use_rope = rope ? 1 : 0;
@@ -225,14 +231,22 @@ int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
     return VLC_OK;
 }
 
-int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
-                 const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
-                 int32_t d, int32_t max_seqlen, float softmax_scale, float rope_theta, void* dq,
-                 void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                 int32_t total, int32_t H, int32_t d, int32_t max_seqlen, float softmax_scale,
+                 float rope_theta, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    return vlc_attn_fwd_gqa(q, k, v, cu, nseg, total, H, H, d, max_seqlen, softmax_scale, rope_theta,
+                            o, lse, ws, ws_bytes, stream);
+}
+
+int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
+                     int32_t H_kv, int32_t d, int32_t max_seqlen, float softmax_scale,
+                     float rope_theta, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                     void* stream) {
     if (dout == nullptr || q == nullptr || k == nullptr || v == nullptr || o == nullptr ||
         lse == nullptr || cu == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
         return VLC_ERR_ARG;
-    int st = check_attn_args(nseg, total, H, d, max_seqlen, ws, ws_bytes, 1);
+    int st = check_attn_args(nseg, total, H, H_kv, d, max_seqlen, ws, ws_bytes, 1);
     if (st != VLC_OK) return st;
     for (const void* ptr : {dout, q, k, v, o, static_cast<const void*>(dq),
                             static_cast<const void*>(dk), static_cast<const void*>(dv)})
@@ -240,7 +254,7 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
     if (!aligned(lse, 4)) return VLC_ERR_ARG;
     if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return VLC_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const WsLayout L = ws_layout(nseg, total, H, d, max_seqlen, 1);
+    const WsLayout L = ws_layout(nseg, total, H, H_kv, d, max_seqlen, 1);
     uint8_t* w = static_cast<uint8_t*>(ws);
     WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
     int4* items_q = reinterpret_cast<int4*>(w + L.items);
@@ -274,11 +288,19 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
     p.delta = reinterpret_cast<float*>(w + L.delta);
     p.qrot = w + L.qrot;
     p.krot = w + L.krot;
-    p.nseg = nseg; p.total = total; p.H = H; p.d = d;
+    p.nseg = nseg; p.total = total; p.H = H; p.d = d; p.Hkv = H_kv;
     p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
     p.use_rope = rope ? 1 : 0;
     if (launch_attn_bwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
     return VLC_OK;
+}
+
+int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
+                 int32_t d, int32_t max_seqlen, float softmax_scale, float rope_theta, void* dq,
+                 void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+    return vlc_attn_bwd_gqa(dout, q, k, v, o, lse, cu, nseg, total, H, H, d, max_seqlen, softmax_scale,
+                            rope_theta, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 int vlc_get_error(const void* ws, int32_t* bits_out, void* stream) {

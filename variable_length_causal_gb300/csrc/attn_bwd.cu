@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(256)
 prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const uint4* __restrict__ q,
             const uint4* __restrict__ k, uint4* __restrict__ qrot, uint4* __restrict__ krot,
             float* __restrict__ delta, const int32_t* __restrict__ cu, int32_t nseg,
-            const float2* __restrict__ table, int32_t total, int32_t H, int rope,
+            const float2* __restrict__ table, int32_t total, int32_t H, int32_t Hkv, int rope,
             const int32_t* __restrict__ err) {
     if (*err != 0) return;
     constexpr int TPR = D / 16;        // threads per row
@@ -100,11 +100,15 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
                     const float4 f = __ldg(t4 + e);
                     cs[2 * e] = f.x; sn[2 * e] = f.y; cs[2 * e + 1] = f.z; sn[2 * e + 1] = f.w;
                 }
+                const int64_t hh = row - tok * H;   // head of this row: k has only Hkv heads
+                const int64_t klo = (tok * Hkv + hh) * (2 * HALF) + c, khi = klo + HALF;
 #pragma unroll
                 for (int which = 0; which < 2; ++which) {
+                    if (which == 1 && hh >= Hkv) break;
                     const uint4* src = which ? k : q;
                     uint4* dst = which ? krot : qrot;
-                    const uint4 x4 = __ldg(src + lo), y4 = __ldg(src + hi);
+                    const int64_t a0 = which ? klo : lo, a1 = which ? khi : hi;
+                    const uint4 x4 = __ldg(src + a0), y4 = __ldg(src + a1);
                     const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
                     uint32_t nx[4], ny[4];
 #pragma unroll
@@ -115,8 +119,8 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
                         nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
                         ny[e] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
                     }
-                    dst[lo] = make_uint4(nx[0], nx[1], nx[2], nx[3]);
-                    dst[hi] = make_uint4(ny[0], ny[1], ny[2], ny[3]);
+                    dst[a0] = make_uint4(nx[0], nx[1], nx[2], nx[3]);
+                    dst[a1] = make_uint4(ny[0], ny[1], ny[2], ny[3]);
                 }
             }
         }
@@ -331,8 +335,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                     mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
-                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64, w.h,
-                                         w.row0 + j * BK, bar(K_FULL + ks), pol_keep);
+                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
+                                         w.h / (p.H / p.Hkv), w.row0 + j * BK, bar(K_FULL + ks), pol_keep);
                     k_issued = nn + 1;
                 }
                 kv += w.hi;
@@ -355,8 +359,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                     mbar_expect_tx(bar(V_FULL + vs), LY::TILE);
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
-                        tma_load_3d_hint(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64, w.h,
-                                         w.row0 + j * BK, bar(V_FULL + vs), pol_keep);
+                        tma_load_3d_hint(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
+                                         w.h / (p.H / p.Hkv), w.row0 + j * BK, bar(V_FULL + vs), pol_keep);
                     v_issued = nn + 1;
                 }
                 kv += w.hi;
@@ -637,11 +641,12 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     constexpr int kRingConsumers = 1 + 1 + 8;   // MMA warp, LSE/delta stager warp, 8 math warps
     float* lsed = reinterpret_cast<float*>(sgen + LY::LSED);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = p.H / p.Hkv;   // query heads per key/value head: a unit runs over all of them
 
     __shared__ int s_skip, s_nunits;
     if (threadIdx.x == 0) {
         s_skip = *reinterpret_cast<volatile int32_t*>(p.err);
-        s_nunits = *reinterpret_cast<const volatile int32_t*>(p.count_k) * p.H;
+        s_nunits = *reinterpret_cast<const volatile int32_t*>(p.count_k) * p.Hkv;
     }
     __syncthreads();
     if (s_skip != 0) return;
@@ -691,7 +696,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_put(rg, n, p.next_k, nunits, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
+                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.Hkv, u);   // w.h: key/value head
                 if (!(ok = mbar_wait(bar(KV_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(KV_FULL), 2 * LY::TILE);
                 const int krow = w.row0 + w.tile * 128;
@@ -701,16 +706,18 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     tma_load_3d_hint(sbase + LY::V0 + kb * LY::BLK, &tmV, kb * 64, w.h, krow, bar(KV_FULL), pol_stream);
                 }
                 kv_issued = unit_it + 1;
-                for (int i = w.lo; i < w.hi && ok; ++i, ++qo) {
+                const int nq = w.hi - w.lo;
+                for (int sq = 0; sq < grp * nq && ok; ++sq, ++qo) {   // every q tile of every query head
+                    const int i = w.lo + sq % nq, hq = w.h * grp + sq / nq;
                     const int s = qo % kQStages;
                     if (!(ok = mbar_wait(bar(QO_EMPTY + s), ((qo / kQStages) & 1) ^ 1, abort))) break;
                     mbar_expect_tx(bar(QO_FULL + s), 2 * LY::TILE);
                     const int qrow = w.row0 + i * BQ;
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb) {
-                        tma_load_3d_hint(sbase + LY::Q0 + s * LY::TILE + kb * LY::BLK, &tmQ, kb * 64, w.h,
+                        tma_load_3d_hint(sbase + LY::Q0 + s * LY::TILE + kb * LY::BLK, &tmQ, kb * 64, hq,
                                          qrow, bar(QO_FULL + s), pol_keep);
-                        tma_load_3d_hint(sbase + LY::DO0 + s * LY::TILE + kb * LY::BLK, &tmDO, kb * 64, w.h,
+                        tma_load_3d_hint(sbase + LY::DO0 + s * LY::TILE + kb * LY::BLK, &tmDO, kb * 64, hq,
                                          qrow, bar(QO_FULL + s), pol_keep);
                     }
                     q_issued = qo + 1;
@@ -764,26 +771,27 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
+                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.Hkv, u);
                 if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_st(st))) break;
                 issue_dpt(st);
-                for (int i = w.lo; i < w.hi; ++i, ++st) {
+                const int nsteps = grp * (w.hi - w.lo);
+                for (int sq = 0; sq < nsteps; ++sq, ++st) {
                     const int s = st % kQStages;
                     const uint64_t qdm = smem_desc_sw128(sbase + LY::Q0 + s * LY::TILE, LY::BLK, 1024);
                     const uint64_t odm = smem_desc_sw128(sbase + LY::DO0 + s * LY::TILE, LY::BLK, 1024);
                     // dV += P^T dO (P^T packed over the S^T columns)
-                    if (i == w.lo && !(ok = wait_warp(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
+                    if (sq == 0 && !(ok = wait_warp(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                     if (!(ok = wait_warp(bar(PT_FULL), st & 1, abort))) break;
                     tc_fence_after();
                     if (elect_one()) {
 #pragma unroll
                         for (int k = 0; k < BQ / 16; ++k)
                             mma_bf16_ts(tmem + LY::DV_COL, tmem + dq::ds_col(k), odm + ((k * 16 * 128) >> 4),
-                                        IDESC_ACC, (i > w.lo || k > 0) ? 1u : 0u);
+                                        IDESC_ACC, (sq > 0 || k > 0) ? 1u : 0u);
                     }
                     __syncwarp();
-                    if (i + 1 < w.hi && !(ok = issue_st(st + 1))) break;
+                    if (sq + 1 < nsteps && !(ok = issue_st(st + 1))) break;
                     // dK += dS^T Q' (dS^T packed over the dP^T columns)
                     if (!(ok = wait_warp(bar(DST_FULL), st & 1, abort))) break;
                     tc_fence_after();
@@ -791,11 +799,11 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 #pragma unroll
                         for (int k = 0; k < BQ / 16; ++k)
                             mma_bf16_ts(tmem + LY::DK_COL, tmem + LY::DPT_COL + dq::ds_col(k),
-                                        qdm + ((k * 16 * 128) >> 4), IDESC_ACC, (i > w.lo || k > 0) ? 1u : 0u);
+                                        qdm + ((k * 16 * 128) >> 4), IDESC_ACC, (sq > 0 || k > 0) ? 1u : 0u);
                         mma_commit(bar(QO_EMPTY + s));
                     }
                     __syncwarp();
-                    if (i + 1 < w.hi) issue_dpt(st + 1);
+                    if (sq + 1 < nsteps) issue_dpt(st + 1);
                 }
                 if (!ok) break;
                 commit(bar(ACC_FULL));
@@ -812,8 +820,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int n = 0; ok; ++n) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
-            for (int i = w.lo; i < w.hi && ok; ++i, ++st) {
+            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.Hkv, u);
+            const int nq = w.hi - w.lo;
+            for (int sq = 0; sq < grp * nq && ok; ++sq, ++st) {
+                const int i = w.lo + sq % nq, hq = w.h * grp + sq / nq;
                 const int sl = st % kLsedSlots;
                 if (!(ok = wait_warp(bar(LSED_EMPTY + sl), ((st / kLsedSlots) & 1) ^ 1, abort))) break;
                 float* dst = lsed + sl * 256;
@@ -823,7 +833,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     const int qq = i * BQ + q;
                     float l2 = 0.f, dl = 0.f;
                     if (qq < w.L) {
-                        const int64_t idx = static_cast<int64_t>(w.h) * p.total + w.row0 + qq;
+                        const int64_t idx = static_cast<int64_t>(hq) * p.total + w.row0 + qq;
                         l2 = __ldg(p.lse + idx) * kLog2e;
                         dl = __ldg(p.delta + idx);
                     }
@@ -847,9 +857,11 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int n = 0; ok; ++n, ++unit_it) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.H, u);
+            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.Hkv, u);
             const int kvpos = w.tile * 128 + r;
-            for (int i = w.lo; i < w.hi; ++i, ++st) {
+            const int nq = w.hi - w.lo;
+            for (int sq = 0; sq < grp * nq; ++sq, ++st) {
+                const int i = w.lo + sq % nq;
                 const int sl = st % kLsedSlots;
                 const float* l2s = lsed + sl * 256 + c0;
                 const float* dls = lsed + sl * 256 + 128 + c0;
@@ -927,7 +939,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             tc_fence_after();
             const bool valid = kvpos < w.L;
             const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? kvpos : 0);
-            const int64_t roff = (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
+            const int64_t roff = (tok * p.Hkv + w.h) * static_cast<int64_t>(D) * 2;
             if (g == 0) {   // dV: plain copy out
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -985,7 +997,8 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
         bwd::prep_kernel<D><<<static_cast<int>(blocks), 256, 0, s>>>(
             static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.o),
             static_cast<const uint4*>(p.q), static_cast<const uint4*>(p.k), static_cast<uint4*>(p.qrot),
-            static_cast<uint4*>(p.krot), p.delta, p.cu, p.nseg, p.table, p.total, p.H, p.use_rope, p.err);
+            static_cast<uint4*>(p.krot), p.delta, p.cu, p.nseg, p.table, p.total, p.H, p.Hkv, p.use_rope,
+            p.err);
     }
     // with RoPE the attention passes read the rotated copies
     const void* qop = p.use_rope ? p.qrot : p.q;
@@ -993,8 +1006,8 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
     CUtensorMap q128, do128, k128, v128;
     if (!make_tmap_thd(&q128, qop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&do128, p.dout, p.total, p.H, D, 128) ||
-        !make_tmap_thd(&k128, kop, p.total, p.H, D, 128) ||
-        !make_tmap_thd(&v128, p.v, p.total, p.H, D, 128))
+        !make_tmap_thd(&k128, kop, p.total, p.Hkv, D, 128) ||
+        !make_tmap_thd(&v128, p.v, p.total, p.Hkv, D, 128))
         return cudaErrorInvalidValue;
     {
         constexpr uint32_t smem = bwd::dq::Layout<D>::ALLOC;

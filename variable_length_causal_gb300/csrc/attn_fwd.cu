@@ -96,6 +96,7 @@ struct FUnit {
     Unit w;
     bool has1;
     int q0, n0, n1, nk;
+    int hkv;   // key/value head of query head w.h
 };
 
 __device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
@@ -109,6 +110,7 @@ __device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
     f.n0 = f.q0 + 1;
     f.n1 = f.has1 ? f.q0 + 2 : 0;
     f.nk = f.has1 ? f.n1 : f.n0;
+    f.hkv = p.Hkv == p.H ? f.w.h : f.w.h / (p.H / p.Hkv);
     return f;
 }
 
@@ -211,7 +213,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
                         tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
-                                         f.w.h, f.w.row0 + j * BN, bar(K_FULL + ks), pol_keep);
+                                         f.hkv, f.w.row0 + j * BN, bar(K_FULL + ks), pol_keep);
                     k_issued = n + 1;
                 }
                 kvn += f.nk;
@@ -495,7 +497,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
                         tma_load_3d_hint(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
-                                         f.w.h, f.w.row0 + j * BN, bar(V_FULL + vs), pol_keep);
+                                         f.hkv, f.w.row0 + j * BN, bar(V_FULL + vs), pol_keep);
                     kv_issued = n + 1;
                 }
                 vn += f.nk;
@@ -544,8 +546,8 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int32_t total, int32_t H,
 cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     if (!make_tmap_thd(&tq, p.q, p.total, p.H, p.d, 128) ||
-        !make_tmap_thd(&tk, p.k, p.total, p.H, p.d, 128) ||
-        !make_tmap_thd(&tv, p.v, p.total, p.H, p.d, 128))
+        !make_tmap_thd(&tk, p.k, p.total, p.Hkv, p.d, 128) ||
+        !make_tmap_thd(&tv, p.v, p.total, p.Hkv, p.d, 128))
         return cudaErrorInvalidValue;
     const dim3 grid(num_sms), block(fwd::kThreads);
     // The warpgroups re-split the block's register pool at run time, which is only

@@ -28,8 +28,8 @@ struct WsLayout {
     int32_t table_rows;
 };
 
-WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t d, int32_t max_seqlen,
-                   int is_bwd);
+WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
+                   int32_t max_seqlen, int is_bwd);
 
 // Kernel launchers (return cudaGetLastError()).
 cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64_t* tokens,
@@ -58,6 +58,7 @@ struct FwdParams {
     int32_t* err;
     const float2* table;       // RoPE cos/sin [rows][d/2], null if no RoPE
     int32_t nseg, total, H, d;
+    int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
     float scale_log2;          // softmax_scale * log2(e)
     int use_rope;
 };
@@ -87,8 +88,9 @@ struct BwdParams {
     const float2* table;
     float* delta;              // [H, total]: rowsum(dO * O)
     void* qrot;                // [total, H, d] bf16: R(p) q (workspace; only with RoPE)
-    void* krot;                // [total, H, d] bf16: R(p) k
+    void* krot;                // [total, Hkv, d] bf16: R(p) k
     int32_t nseg, total, H, d;
+    int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
     float scale;
     int use_rope;              // 1: inputs are rotated in the prep pass, gradients un-rotated
 };
