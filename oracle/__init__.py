@@ -62,7 +62,7 @@ def _load():
             for f in (lib.orc_worklist_fwd, lib.orc_worklist_bwd):
                 f.argtypes = [P, i32, i32, i32, P, i64]
                 f.restype = i64
-            lib.orc_rope_rows.argtypes = [P, P, i64, i32, f64, P]
+            lib.orc_rope_rows.argtypes = [P, P, i64, i32, f64, ctypes.c_int, P]
             lib.orc_rope_rows.restype = None
             lib.orc_attn_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, f64, ctypes.c_int, P, P]
             lib.orc_attn_fwd.restype = None
@@ -153,17 +153,25 @@ def worklist_bwd(cu, BM: int = 128, BN: int = 128) -> np.ndarray:
     return _worklist(_load().orc_worklist_bwd, cu, BM, BN)
 
 
-def rope_rows(x, pos, theta: float = 10000.0) -> np.ndarray:
+def rope_rows(x, pos, theta: float = 10000.0, interleaved: bool = False) -> np.ndarray:
     x = _c(x, np.float64)
     n, d = x.shape
     pos = _c(pos, np.int64)
     out = np.zeros_like(x)
-    _load().orc_rope_rows(_ptr(x), _ptr(pos), n, d, float(theta), _ptr(out))
+    _load().orc_rope_rows(_ptr(x), _ptr(pos), n, d, float(theta), int(bool(interleaved)), _ptr(out))
     return out
 
 
+def _mode(contract: bool, interleaved: bool) -> int:
+    return int(bool(contract)) + (4 if interleaved else 0)
+
+
+def _mode_f64(interleaved: bool) -> int:
+    return -5 if interleaved else -1
+
+
 def attn_fwd(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
-             seg_heads=None):
+             seg_heads=None, interleaved: bool = False):
     """Exact per-segment causal attention in fp64.  q/k/v: bf16 tensors or uint16 bit arrays
     [total, H, d] (k and v may have fewer heads Hkv dividing H: query head h reads key/value
     head h // (H // Hkv)).  Returns (o [total, H, d] f64, lse [H, total] f64, natural log).
@@ -177,18 +185,18 @@ def attn_fwd(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: 
     lse = np.zeros((H, total), np.float64)
     if seg_heads is None:
         _load().orc_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                             float(scale), float(theta), int(bool(contract)), _ptr(o), _ptr(lse))
+                             float(scale), float(theta), _mode(contract, interleaved), _ptr(o), _ptr(lse))
     else:
         sh = np.asarray(seg_heads, np.int32).reshape(-1, 2)
         segs, heads = np.ascontiguousarray(sh[:, 0]), np.ascontiguousarray(sh[:, 1])
         _load().orc_attn_fwd_seg_heads(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H,
-                                       Hkv, d, float(scale), float(theta), int(bool(contract)),
+                                       Hkv, d, float(scale), float(theta), _mode(contract, interleaved),
                                        _ptr(segs), _ptr(heads), sh.shape[0], _ptr(o), _ptr(lse))
     return o, lse
 
 
 def attn_fwd_rows(q, k, v, cu, rows, heads, scale: float = 0.0, theta: float = 10000.0,
-                  contract: bool = True):
+                  contract: bool = True, interleaved: bool = False):
     """Forward for selected (token row, head) pairs: returns (o [n, d], lse [n])."""
     qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
     total, H, d = qb.shape
@@ -200,12 +208,12 @@ def attn_fwd_rows(q, k, v, cu, rows, heads, scale: float = 0.0, theta: float = 1
     o = np.zeros((n, d), np.float64)
     lse = np.zeros(n, np.float64)
     _load().orc_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                              float(scale), float(theta), int(bool(contract)), _ptr(rows),
+                              float(scale), float(theta), _mode(contract, interleaved), _ptr(rows),
                               _ptr(heads), n, _ptr(o), _ptr(lse))
     return o, lse
 
 
-def attn_fwd_f64(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0):
+def attn_fwd_f64(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, interleaved: bool = False):
     """Exact-mode forward on float64 inputs [total, H, d] (finite-difference tests)."""
     q, k, v = (_c(x, np.float64) for x in (q, k, v))
     total, H, d = q.shape
@@ -214,11 +222,11 @@ def attn_fwd_f64(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0):
     o = np.zeros((total, H, d), np.float64)
     lse = np.zeros((H, total), np.float64)
     _load().orc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                         float(scale), float(theta), -1, _ptr(o), _ptr(lse))
+                         float(scale), float(theta), _mode_f64(interleaved), _ptr(o), _ptr(lse))
     return o, lse
 
 
-def attn_bwd_f64(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0):
+def attn_bwd_f64(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, interleaved: bool = False):
     """Exact-mode gradients on float64 inputs (finite-difference tests)."""
     g, q, k, v = (_c(x, np.float64) for x in (dout, q, k, v))
     total, H, d = q.shape
@@ -228,12 +236,12 @@ def attn_bwd_f64(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0):
     dk = np.zeros((total, Hkv, d), np.float64)
     dv = np.zeros_like(dk)
     _load().orc_attn_bwd(_ptr(g), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                         float(scale), float(theta), -1, _ptr(dq), _ptr(dk), _ptr(dv))
+                         float(scale), float(theta), _mode_f64(interleaved), _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
 
 
 def attn_bwd(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
-             seg_heads=None):
+             seg_heads=None, interleaved: bool = False):
     """Gradients (dq [total, H, d], dk and dv [total, Hkv, d]) f64 of sum(O * dO).  With
     ``seg_heads`` (a list of (segment, key/value head) pairs) only those are computed (dq for
     every query head of each pair's group); other entries stay 0."""
@@ -247,13 +255,13 @@ def attn_bwd(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, cont
     lib = _load()
     if seg_heads is None:
         lib.orc_attn_bwd(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                         float(scale), float(theta), int(bool(contract)), _ptr(dq), _ptr(dk), _ptr(dv))
+                         float(scale), float(theta), _mode(contract, interleaved), _ptr(dq), _ptr(dk), _ptr(dv))
     else:
         sh = np.asarray(seg_heads, np.int32).reshape(-1, 2)
         segs = np.ascontiguousarray(sh[:, 0])
         heads = np.ascontiguousarray(sh[:, 1])
         lib.orc_attn_bwd_seg_heads(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1,
-                                   total, H, Hkv, d, float(scale), float(theta), int(bool(contract)),
+                                   total, H, Hkv, d, float(scale), float(theta), _mode(contract, interleaved),
                                    _ptr(segs), _ptr(heads), sh.shape[0], _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
 

@@ -92,29 +92,43 @@ static double rope_angle(int64_t p, int j, int d, double theta) {
     return (double)p * pow(theta, -2.0 * (double)j / (double)d);
 }
 
-/* Rotate one head vector x[0..d) by R(p), rotate-half pairing
- * (x_j, x_{j+d/2}):  x'_j = x_j cos - x_{j+d/2} sin,
- *                    x'_{j+d/2} = x_{j+d/2} cos + x_j sin. */
-static void rope_rotate(const double* x, double* out, int64_t p, int d, double theta) {
+/* Elements of rotation pair j: rotate-half pairing (x_j, x_{j+d/2}) by default;
+ * with interleaved != 0 the adjacent pairing (x_{2j}, x_{2j+1}) (the complex-number
+ * form of RoFormer, which "Positions are reset per segment" cites; rotate-half is the
+ * HF Llama form it also cites).  Both use frequency theta^(-2j/d) for pair j. */
+static void rope_pair(int j, int d, int interleaved, int* ia, int* ib) {
+    if (interleaved) { *ia = 2 * j; *ib = 2 * j + 1; }
+    else { *ia = j; *ib = j + d / 2; }
+}
+
+/* Rotate one head vector x[0..d) by R(p):  x'_a = x_a cos - x_b sin,
+ * x'_b = x_b cos + x_a sin  for every pair (a, b). */
+static void rope_rotate(const double* x, double* out, int64_t p, int d, double theta,
+                        int interleaved) {
     int half = d / 2;
     for (int j = 0; j < half; ++j) {
         double phi = rope_angle(p, j, d, theta);
         double c = cos(phi), s = sin(phi);
-        double a = x[j], b = x[j + half];
-        out[j] = a * c - b * s;
-        out[j + half] = b * c + a * s;
+        int ia, ib;
+        rope_pair(j, d, interleaved, &ia, &ib);
+        double a = x[ia], b = x[ib];
+        out[ia] = a * c - b * s;
+        out[ib] = b * c + a * s;
     }
 }
 
 /* Transpose rotation R(p)^T = R(-p), used to carry gradients back through RoPE. */
-static void rope_rotate_transpose(const double* g, double* out, int64_t p, int d, double theta) {
+static void rope_rotate_transpose(const double* g, double* out, int64_t p, int d, double theta,
+                                  int interleaved) {
     int half = d / 2;
     for (int j = 0; j < half; ++j) {
         double phi = rope_angle(p, j, d, theta);
         double c = cos(phi), s = sin(phi);
-        double a = g[j], b = g[j + half];
-        out[j] = a * c + b * s;
-        out[j + half] = b * c - a * s;
+        int ia, ib;
+        rope_pair(j, d, interleaved, &ia, &ib);
+        double a = g[ia], b = g[ib];
+        out[ia] = a * c + b * s;
+        out[ib] = b * c - a * s;
     }
 }
 
@@ -246,8 +260,8 @@ int64_t orc_worklist_bwd(const int32_t* cu, int32_t nseg, int32_t BM, int32_t BN
 /* Apply R(pos[n]) to rows of x ([n][d] fp64).  Exposed so tests can probe the
  * rotation at arbitrary positions (shift invariance, R(0) = I, ...). */
 void orc_rope_rows(const double* x, const int64_t* pos, int64_t n, int32_t d,
-                   double theta, double* out) {
-    for (int64_t i = 0; i < n; ++i) rope_rotate(x + i * d, out + i * d, pos[i], d, theta);
+                   double theta, int interleaved, double* out) {
+    for (int64_t i = 0; i < n; ++i) rope_rotate(x + i * d, out + i * d, pos[i], d, theta, interleaved);
 }
 
 /* ---------------------------------------------------------------- attention */
@@ -259,6 +273,7 @@ typedef struct {
     int32_t nseg, total, H, Hkv, d;      /* q / dO have H heads, k / v have Hkv (H % Hkv == 0) */
     double scale, theta;                 /* theta == 0: no RoPE */
     int contract;
+    int rope_interleaved;                /* pairing of the rotation (rope_pair) */
 } orc_problem;
 
 /* Grouped heads: query head h reads key/value head h / (H / Hkv), so each run of
@@ -282,7 +297,7 @@ static void load_rotated(const orc_problem* P, const void* x, int64_t i, int32_t
     double* tmp = (double*)malloc(sizeof(double) * (size_t)d);
     for (int c = 0; c < d; ++c) tmp[c] = input_elem(P, x, i, h, c);
     if (P->theta != 0.0) {
-        rope_rotate(tmp, out, p, d, P->theta);
+        rope_rotate(tmp, out, p, d, P->theta, P->rope_interleaved);
         if (P->contract)
             for (int c = 0; c < d; ++c) out[c] = round_to_bf16(out[c]);
     } else {
@@ -360,6 +375,11 @@ static orc_problem make_problem(const void* q, const void* k, const void* v,
                                 double theta, int contract) {
     orc_problem P;
     P.q = q; P.k = k; P.v = v; P.dout = dout; P.cu = cu;
+    /* contract: 1 contract mode, 0 exact mode, -1 exact mode on fp64 inputs; adding 4 (or, for
+     * fp64 inputs, passing -5) selects the interleaved RoPE pairing. */
+    P.rope_interleaved = 0;
+    if (contract >= 0 && (contract & 4)) { P.rope_interleaved = 1; contract &= ~4; }
+    else if (contract < 0 && contract != -1) { P.rope_interleaved = 1; contract = -1; }
     P.f64_inputs = contract < 0;   /* contract == -1 selects fp64 inputs, exact mode */
     if (contract < 0) contract = 0;
     P.nseg = nseg; P.total = total; P.H = H; P.Hkv = Hkv; P.d = d;
@@ -477,14 +497,14 @@ static void bwd_seg_kvhead(const orc_problem* P, int32_t r, int32_t hk, double* 
         }
         for (int64_t p = 0; p < L; ++p) {
             size_t off = ((size_t)(base + p) * P->H + h) * d;
-            if (P->theta != 0.0) rope_rotate_transpose(gq + p * d, dq + off, p, d, P->theta);
+            if (P->theta != 0.0) rope_rotate_transpose(gq + p * d, dq + off, p, d, P->theta, P->rope_interleaved);
             else memcpy(dq + off, gq + p * d, sizeof(double) * (size_t)d);
         }
         seg_head_free(&S);
     }
     for (int64_t p = 0; p < L; ++p) {
         size_t off = ((size_t)(base + p) * P->Hkv + hk) * d;
-        if (P->theta != 0.0) rope_rotate_transpose(gk + p * d, dk + off, p, d, P->theta);
+        if (P->theta != 0.0) rope_rotate_transpose(gk + p * d, dk + off, p, d, P->theta, P->rope_interleaved);
         else memcpy(dk + off, gk + p * d, sizeof(double) * (size_t)d);
         memcpy(dv + off, gv + p * d, sizeof(double) * (size_t)d);
     }

@@ -15,7 +15,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MUTATIONS = {
-    "rope_sign": ("out[j + half] = b * c + a * s;", "out[j + half] = b * c - a * s;"),
+    "rope_sign": ("out[ib] = b * c + a * s;", "out[ib] = b * c - a * s;"),
     "rope_frequency": ("return (double)p * pow(theta, -2.0 * (double)j / (double)d);",
                        "return (double)p * pow(theta, -1.0 * (double)j / (double)d);"),
     "position_not_reset": ("load_rotated(P, P->q, i, h, p, S->q + p * d);",
@@ -30,6 +30,8 @@ MUTATIONS = {
     "worklist_extra_tile": ("items[4 * n + 3] = (int32_t)ceil_div(last_row, BN);",
                             "items[4 * n + 3] = (int32_t)ceil_div(last_row, BN) + (t == 0);"),
     "worklist_unstable_ties": ("if (ny >= nx) break;", "if (ny > nx) break;"),
+    "rope_interleaved_pairing": ("if (interleaved) { *ia = 2 * j; *ib = 2 * j + 1; }",
+                                 "if (interleaved) { *ia = j; *ib = j + 1; }"),
     "gqa_interleaved_heads": ("static int32_t kv_head(const orc_problem* P, int32_t h) { return h / (P->H / P->Hkv); }",
                               "static int32_t kv_head(const orc_problem* P, int32_t h) { return h % P->Hkv; }"),
     "ce_label_logit_sign": ("row[i] = (mx + log(s)) - zy;", "row[i] = (mx + log(s)) + zy;"),

@@ -550,3 +550,72 @@ def test_ce_bf16_bits_and_bad_label():
     lab[3] = 40   # outside the vocabulary: flagged and not counted
     st, s, n, _, _ = oracle.shifted_ce(z64, lab)
     assert st == 1 and n == 7
+
+
+# ------------------------------------------------------------------ interleaved RoPE pairing
+def _rope_interleaved_np(x, pos, theta=10000.0):
+    # the complex form of consecutive pairs: z_j = x_2j + i x_2j+1, times e^{i p w_j}
+    d = x.shape[-1]
+    w = theta ** (-2.0 * np.arange(d // 2) / d)
+    z = (x[..., 0::2] + 1j * x[..., 1::2]) * np.exp(1j * np.asarray(pos, np.float64)[:, None] * w[None])
+    out = np.empty_like(x)
+    out[..., 0::2], out[..., 1::2] = z.real, z.imag
+    return out
+
+
+def test_rope_interleaved_rows_complex_form():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((9, 16))
+    pos = rng.integers(0, 5000, size=9)
+    assert np.allclose(oracle.rope_rows(x, pos, interleaved=True), _rope_interleaved_np(x, pos), atol=1e-9)
+    # the two pairings are the same rotation up to a permutation of the coordinates
+    perm = np.concatenate([np.arange(0, 16, 2), np.arange(1, 16, 2)])   # interleaved -> halves
+    a = oracle.rope_rows(x[:, perm], pos)
+    b = oracle.rope_rows(x, pos, interleaved=True)[:, perm]
+    assert np.allclose(a, b, atol=1e-12)
+
+
+def test_interleaved_attention_against_torch_autograd():
+    lens = [6, 1, 9]
+    H, Hkv, d = 4, 2, 16
+    w = synth.custom_workload(lens, H, d)
+    g0 = torch.Generator().manual_seed(41)
+    q, g = (torch.randn((w.total, H, d), generator=g0).bfloat16() for _ in range(2))
+    k, v = (torch.randn((w.total, Hkv, d), generator=g0).bfloat16() for _ in range(2))
+    pos = torch.from_numpy(brute.local_positions(w.cu)).double()
+    wfreq = 10000.0 ** (-2.0 * torch.arange(d // 2, dtype=torch.float64) / d)
+    rot = torch.polar(torch.ones(len(pos), d // 2, dtype=torch.float64), pos[:, None] * wfreq[None])
+
+    def rope(x):
+        z = torch.view_as_complex(x.reshape(*x.shape[:-1], d // 2, 2).contiguous()) * rot[:, None, :]
+        return torch.view_as_real(z).reshape(x.shape)
+
+    qt, kt, vt = (torch.from_numpy(_f64(x)).requires_grad_() for x in (q, k, v))
+    mask = torch.from_numpy(brute.block_causal_allow(w.cu))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        rope(qt).permute(1, 0, 2), rope(kt).permute(1, 0, 2), vt.permute(1, 0, 2), attn_mask=mask,
+        enable_gqa=True).permute(1, 0, 2)
+    (o * torch.from_numpy(_f64(g))).sum().backward()
+    o_orc, _ = oracle.attn_fwd(q, k, v, w.cu, contract=False, interleaved=True)
+    assert np.max(np.abs(o_orc - o.detach().numpy())) < 1e-12
+    dq, dk, dv = oracle.attn_bwd(g, q, k, v, w.cu, contract=False, interleaved=True)
+    assert np.max(np.abs(dq - qt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dk - kt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dv - vt.grad.numpy())) < 1e-11
+
+
+def test_interleaved_backward_finite_differences():
+    rng = np.random.default_rng(17)
+    w = synth.custom_workload([4, 3], 2, 8)
+    q, k, v, g = (rng.standard_normal((w.total, 2, 8)) for _ in range(4))
+    dq, dk, dv = oracle.attn_bwd_f64(g, q, k, v, w.cu, interleaved=True)
+    eps = 1e-6
+    for name, x, gx in (("q", q, dq), ("k", k, dk)):
+        for ix in [tuple(rng.integers(0, s) for s in x.shape) for _ in range(8)]:
+            xp, xm = x.copy(), x.copy()
+            xp[ix] += eps
+            xm[ix] -= eps
+            f = lambda a: float(np.sum(oracle.attn_fwd_f64(*((a, k, v) if name == "q" else (q, a, v)), w.cu,
+                                                           interleaved=True)[0] * g))
+            num = (f(xp) - f(xm)) / (2 * eps)
+            assert abs(num - gx[ix]) < 1e-6 * (1 + abs(num)), (name, ix)
