@@ -171,6 +171,28 @@ int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void*
                      float rope_theta, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
                      void* stream);
 
+/* Option bits of vlc_attn_fwd_ex / vlc_attn_bwd_ex. */
+#define VLC_ROPE_INTERLEAVED 0x1u  /* RoPE pairs (x_{2j}, x_{2j+1}) instead of (x_j, x_{j+d/2}) */
+
+/* vlc_attn_fwd_gqa / vlc_attn_bwd_gqa with an option word.  flags == 0 is
+ * exactly those calls; VLC_ROPE_INTERLEAVED rotates the adjacent pairs
+ * (x_{2j}, x_{2j+1}) of q and k by p_i * theta^(-2j/d), the complex-number form
+ * of RoFormer's rotation that "Sequence packing and variable-length attention"
+ * (charlestar, "Positions are reset per segment") cites next to the
+ * rotate-half form of HF Llama; the per-segment reset and the frequencies are
+ * unchanged, and the backward un-rotates dq and dk with the same pairing.  The
+ * bit has no effect when rope_theta == 0.  Unknown bits return VLC_ERR_ARG.
+ * Workspace sizes are those of vlc_workspace_bytes_gqa. */
+int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                    int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                    float softmax_scale, float rope_theta, uint32_t flags, void* o, float* lse,
+                    void* ws, size_t ws_bytes, void* stream);
+int vlc_attn_bwd_ex(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
+                    int32_t H_kv, int32_t d, int32_t max_seqlen, float softmax_scale,
+                    float rope_theta, uint32_t flags, void* dq, void* dk, void* dv, void* ws,
+                    size_t ws_bytes, void* stream);
+
 /* Forward attention for callers that cannot allocate device memory.  No
  * counterpart on the pages: it exists for callers that may not obtain memory
  * per call, such as code running inside another runtime's execution hook (a

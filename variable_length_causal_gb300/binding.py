@@ -23,12 +23,14 @@ VLC_ERR_WORKSPACE, VLC_ERR_CUDA, VLC_ERR_TIMEOUT, VLC_ERR_LABEL = 4, 5, 6, 7
 DEVERR_CU_FIRST, DEVERR_CU_ORDER, DEVERR_CU_TOTAL, DEVERR_MAXLEN = 0x1, 0x2, 0x4, 0x8
 DEVERR_TIMEOUT = 0x100
 WORKLIST_FWD, WORKLIST_BWD = 0, 1
+ROPE_INTERLEAVED = 0x1
 
 EXPORTED = [
     "vlc_status_string", "vlc_version", "vlc_workspace_bytes", "vlc_worklist_capacity",
     "vlc_build_positions_labels", "vlc_build_worklist", "vlc_attn_fwd", "vlc_attn_bwd",
     "vlc_get_error", "vlc_attn_fwd_noalloc", "vlc_ce_workspace_bytes", "vlc_shifted_ce",
-    "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa",
+    "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa", "vlc_attn_fwd_ex",
+    "vlc_attn_bwd_ex",
 ]
 
 _lock = threading.Lock()
@@ -89,6 +91,13 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_attn_bwd_gqa.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32,
                                          P, P, P, P, sz, P]
         lib.vlc_attn_bwd_gqa.restype = cint
+        u32 = ctypes.c_uint32
+        lib.vlc_attn_fwd_ex.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, u32, P, P, P,
+                                        sz, P]
+        lib.vlc_attn_fwd_ex.restype = cint
+        lib.vlc_attn_bwd_ex.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, u32,
+                                        P, P, P, P, sz, P]
+        lib.vlc_attn_bwd_ex.restype = cint
         _lib = lib
         return lib
 
@@ -225,9 +234,10 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     max_seqlen: int, softmax_scale: Optional[float] = None,
                     rope_theta: float = 10000.0, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                    check: bool = True):
+                    check: bool = True, rope_interleaved: bool = False):
     """Segment-local causal attention with per-segment RoPE reset.  Returns (O, LSE[H, total]).
-    k and v may have fewer heads than q (grouped: query head h reads head h // (H // H_kv))."""
+    k and v may have fewer heads than q (grouped: query head h reads head h // (H // H_kv)).
+    rope_interleaved rotates the pairs (x[2j], x[2j+1]) instead of (x[j], x[j + d/2])."""
     lib = load_library()
     _require_cuda(q, k, v, cu_seqlens)
     H_kv = _check_qkv([q] + ([] if out is None else [out]), [k, v])
@@ -236,9 +246,10 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
     ws = new_workspace(nseg, total, H, d, max_seqlen, False, q.device, H_kv) if workspace is None else workspace
-    st = lib.vlc_attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseg, total, H, H_kv, d,
-                              int(max_seqlen), _scale(softmax_scale, d), float(rope_theta), _ptr(out),
-                              _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device))
+    st = lib.vlc_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseg, total, H, H_kv, d,
+                             int(max_seqlen), _scale(softmax_scale, d), float(rope_theta),
+                             ROPE_INTERLEAVED if rope_interleaved else 0, _ptr(out), _ptr(lse), _ptr(ws),
+                             ws.numel(), _stream(q.device))
     _check(st, "vlc_attn_fwd")
     if check:
         _raise_device_error(ws, "vlc_attn_fwd")
@@ -250,7 +261,7 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                     softmax_scale: Optional[float] = None, rope_theta: float = 10000.0,
                     dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
                     dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                    check: bool = True):
+                    check: bool = True, rope_interleaved: bool = False):
     """Gradients (dQ, dK, dV) of sum(O * dO) for the forward above (dK, dV shaped like k, v)."""
     lib = load_library()
     _require_cuda(dout, q, k, v, o, lse, cu_seqlens)
@@ -263,10 +274,11 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws = new_workspace(nseg, total, H, d, max_seqlen, True, q.device, H_kv) if workspace is None else workspace
-    st = lib.vlc_attn_bwd_gqa(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                              _ptr(cu_seqlens), nseg, total, H, H_kv, d, int(max_seqlen),
-                              _scale(softmax_scale, d), float(rope_theta), _ptr(dq), _ptr(dk), _ptr(dv),
-                              _ptr(ws), ws.numel(), _stream(q.device))
+    st = lib.vlc_attn_bwd_ex(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                             _ptr(cu_seqlens), nseg, total, H, H_kv, d, int(max_seqlen),
+                             _scale(softmax_scale, d), float(rope_theta),
+                             ROPE_INTERLEAVED if rope_interleaved else 0, _ptr(dq), _ptr(dk), _ptr(dv),
+                             _ptr(ws), ws.numel(), _stream(q.device))
     _check(st, "vlc_attn_bwd")
     if check:
         _raise_device_error(ws, "vlc_attn_bwd")

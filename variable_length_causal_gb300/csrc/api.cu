@@ -188,13 +188,19 @@ static int check_attn_args(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, 
     return VLC_OK;
 }
 
-int vlc_attn_fwd_gqa(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
-                     int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
-                     float softmax_scale, float rope_theta, void* o, float* lse, void* ws,
-                     size_t ws_bytes, void* stream) {
+static int rope_mode(float rope_theta, uint32_t flags) {
+    if (rope_theta == 0.f) return kRopeNone;
+    return (flags & VLC_ROPE_INTERLEAVED) ? kRopeInterleaved : kRopeHalf;
+}
+
+int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                    int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                    float softmax_scale, float rope_theta, uint32_t flags, void* o, float* lse,
+                    void* ws, size_t ws_bytes, void* stream) {
     if (q == nullptr || k == nullptr || v == nullptr || cu == nullptr || o == nullptr ||
         lse == nullptr)
         return VLC_ERR_ARG;
+    if (flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED)) return VLC_ERR_ARG;
     int st = check_attn_args(nseg, total, H, H_kv, d, max_seqlen, ws, ws_bytes, 0);
     if (st != VLC_OK) return st;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
@@ -226,9 +232,17 @@ int vlc_attn_fwd_gqa(const void* q, const void* k, const void* v, const int32_t*
     p.nseg = nseg; p.total = total; p.H = H; p.d = d; p.Hkv = H_kv;
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.use_rope = rope ? 1 : 0;
+    p.use_rope = rope_mode(rope_theta, flags);
     if (launch_attn_fwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
     return VLC_OK;
+}
+
+int vlc_attn_fwd_gqa(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                     int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                     float softmax_scale, float rope_theta, void* o, float* lse, void* ws,
+                     size_t ws_bytes, void* stream) {
+    return vlc_attn_fwd_ex(q, k, v, cu, nseg, total, H, H_kv, d, max_seqlen, softmax_scale, rope_theta,
+                           0u, o, lse, ws, ws_bytes, stream);
 }
 
 int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
@@ -238,14 +252,15 @@ int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
                             o, lse, ws, ws_bytes, stream);
 }
 
-int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void* v, const void* o,
-                     const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
-                     int32_t H_kv, int32_t d, int32_t max_seqlen, float softmax_scale,
-                     float rope_theta, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
-                     void* stream) {
+int vlc_attn_bwd_ex(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
+                    int32_t H_kv, int32_t d, int32_t max_seqlen, float softmax_scale,
+                    float rope_theta, uint32_t flags, void* dq, void* dk, void* dv, void* ws,
+                    size_t ws_bytes, void* stream) {
     if (dout == nullptr || q == nullptr || k == nullptr || v == nullptr || o == nullptr ||
         lse == nullptr || cu == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
         return VLC_ERR_ARG;
+    if (flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED)) return VLC_ERR_ARG;
     int st = check_attn_args(nseg, total, H, H_kv, d, max_seqlen, ws, ws_bytes, 1);
     if (st != VLC_OK) return st;
     for (const void* ptr : {dout, q, k, v, o, static_cast<const void*>(dq),
@@ -290,9 +305,18 @@ int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void*
     p.krot = w + L.krot;
     p.nseg = nseg; p.total = total; p.H = H; p.d = d; p.Hkv = H_kv;
     p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
-    p.use_rope = rope ? 1 : 0;
+    p.use_rope = rope_mode(rope_theta, flags);
     if (launch_attn_bwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
     return VLC_OK;
+}
+
+int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
+                     int32_t H_kv, int32_t d, int32_t max_seqlen, float softmax_scale,
+                     float rope_theta, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                     void* stream) {
+    return vlc_attn_bwd_ex(dout, q, k, v, o, lse, cu, nseg, total, H, H_kv, d, max_seqlen, softmax_scale,
+                           rope_theta, 0u, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,

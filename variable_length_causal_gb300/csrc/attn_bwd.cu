@@ -56,7 +56,9 @@ constexpr uint64_t kDrainNs = 200000000ull;
 // One pass over the (token, head) rows: D = rowsum(dO * O) in fp32 ([H, total]),
 // and with RoPE the rotated q' = R(p) q and k' = R(p) k (bf16, rounded once),
 // so the attention passes below read pre-rotated operands.  D/16 threads per
-// row; thread c handles the rotation pairs j = 8c .. 8c+7 (columns j and j+D/2).
+// row; thread c handles 16-byte chunks c and c + D/16 of the row: rotate-half
+// pairs j = 8c .. 8c+7 (columns j and j+D/2), or, with the interleaved pairing,
+// pairs 4c .. 4c+3 and D/4 + 4c .. D/4 + 4c+3 (columns 2j and 2j+1).
 template <int D>
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const uint4* __restrict__ q,
@@ -93,12 +95,27 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
                     if (__ldg(cu + mid) <= tok) a = mid; else b = mid - 1;
                 }
                 const int64_t pos = tok - __ldg(cu + a);
-                const float4* t4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 8);
+                const bool il = rope == kRopeInterleaved;
+                // cs/sn[2e], [2e+1]: angles of the two pairs that the e-th words of the lo
+                // and hi chunks take part in (rotate-half: the pairs at word e's two
+                // columns; interleaved: word e of lo, word e of hi)
                 float cs[8], sn[8];
+                if (!il) {
+                    const float4* t4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 8);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 f = __ldg(t4 + e);
-                    cs[2 * e] = f.x; sn[2 * e] = f.y; cs[2 * e + 1] = f.z; sn[2 * e + 1] = f.w;
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 f = __ldg(t4 + e);
+                        cs[2 * e] = f.x; sn[2 * e] = f.y; cs[2 * e + 1] = f.z; sn[2 * e + 1] = f.w;
+                    }
+                } else {
+                    const float4* l4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 4);
+                    const float4* h4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + D / 4 + c * 4);
+#pragma unroll
+                    for (int e2 = 0; e2 < 2; ++e2) {
+                        const float4 f = __ldg(l4 + e2), g = __ldg(h4 + e2);
+                        cs[4 * e2] = f.x; sn[4 * e2] = f.y; cs[4 * e2 + 1] = g.x; sn[4 * e2 + 1] = g.y;
+                        cs[4 * e2 + 2] = f.z; sn[4 * e2 + 2] = f.w; cs[4 * e2 + 3] = g.z; sn[4 * e2 + 3] = g.w;
+                    }
                 }
                 const int64_t hh = row - tok * H;   // head of this row: k has only Hkv heads
                 const int64_t klo = (tok * Hkv + hh) * (2 * HALF) + c, khi = klo + HALF;
@@ -113,11 +130,18 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
                     uint32_t nx[4], ny[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float x0 = bf16_lo(xv[e]), x1 = bf16_hi(xv[e]);
-                        const float y0 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
                         const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
-                        nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
-                        ny[e] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+                        if (!il) {   // pairs (lo word e, hi word e) at columns 2e and 2e+1
+                            const float x0 = bf16_lo(xv[e]), x1 = bf16_hi(xv[e]);
+                            const float y0 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
+                            nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
+                            ny[e] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+                        } else {     // lo word e and hi word e are pairs of their own
+                            const float x0 = bf16_lo(xv[e]), y0 = bf16_hi(xv[e]);
+                            const float x1 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
+                            nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(y0, c0, x0 * s0));
+                            ny[e] = pack_bf16x2(fmaf(x1, c1, -y1 * s1), fmaf(y1, c1, x1 * s1));
+                        }
                     }
                     dst[a0] = make_uint4(nx[0], nx[1], nx[2], nx[3]);
                     dst[a1] = make_uint4(ny[0], ny[1], ny[2], ny[3]);
@@ -134,12 +158,43 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
 }
 
 // Apply scale and R(p)^T to one row of fp32 gradients held in TMEM columns
-// [col0, col0 + D) of this thread's lane, and store it as bf16.
-template <int D>
+// [col0, col0 + D) of this thread's lane, and store it as bf16.  IL selects the
+// interleaved pairing (columns 2j, 2j+1), else rotate-half (j, j + D/2).
+template <int D, bool IL>
 __device__ __forceinline__ void store_unrotated(uint32_t taddr, const float2* __restrict__ table,
                                                 int pos, float scale, bool rope, bool valid,
                                                 uint8_t* __restrict__ row_out) {
     constexpr int half = D / 2;
+    if constexpr (IL) {
+#pragma unroll
+        for (int a = 0; a < D / 32; ++a) {
+            uint32_t r[32];
+            tmem_ld32(taddr + a * 32, r);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {   // columns a*32+e .. +3: pairs a*16 + e/2, +1
+                float x0 = __uint_as_float(r[e]) * scale, y0 = __uint_as_float(r[e + 1]) * scale;
+                float x1 = __uint_as_float(r[e + 2]) * scale, y1 = __uint_as_float(r[e + 3]) * scale;
+                if (rope) {
+                    const float4 cs = __ldg(reinterpret_cast<const float4*>(
+                        table + static_cast<int64_t>(pos) * half + a * 16 + e / 2));
+                    const float u0 = x0 * cs.x + y0 * cs.y, v0 = y0 * cs.x - x0 * cs.y;
+                    const float u1 = x1 * cs.z + y1 * cs.w, v1 = y1 * cs.z - x1 * cs.w;
+                    x0 = u0; y0 = v0; x1 = u1; y1 = v1;
+                }
+                pk[e / 2] = pack_bf16x2(x0, y0);
+                pk[e / 2 + 1] = pack_bf16x2(x1, y1);
+            }
+            if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(row_out + a * 64);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int a = 0; a < half / 32; ++a) {
         uint32_t lo[32], hi[32];
@@ -550,8 +605,12 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             tc_fence_after();
             if (g == 0) {
                 uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dq) + (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
-                store_unrotated<D>(tmem + lane_off + LY::DQ_COL, p.table, qpos, p.scale, p.use_rope != 0,
-                                   valid, row_out);
+                if (p.use_rope == kRopeInterleaved)
+                    store_unrotated<D, true>(tmem + lane_off + LY::DQ_COL, p.table, qpos, p.scale, true,
+                                             valid, row_out);
+                else
+                    store_unrotated<D, false>(tmem + lane_off + LY::DQ_COL, p.table, qpos, p.scale,
+                                              p.use_rope != 0, valid, row_out);
             }
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));
@@ -958,8 +1017,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     }
                 }
             } else {        // dK: scale and R(p)^T
-                store_unrotated<D>(tmem + lane_off + LY::DK_COL, p.table, kvpos, p.scale, p.use_rope != 0,
-                                   valid, reinterpret_cast<uint8_t*>(p.dk) + roff);
+                uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dk) + roff;
+                if (p.use_rope == kRopeInterleaved)
+                    store_unrotated<D, true>(tmem + lane_off + LY::DK_COL, p.table, kvpos, p.scale, true,
+                                             valid, row_out);
+                else
+                    store_unrotated<D, false>(tmem + lane_off + LY::DK_COL, p.table, kvpos, p.scale,
+                                              p.use_rope != 0, valid, row_out);
             }
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));

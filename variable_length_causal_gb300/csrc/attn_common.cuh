@@ -116,61 +116,84 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// RoPE pairings.  Rotate-half (IL = false) rotates columns (j, j + D/2);
+// interleaved (IL = true) rotates columns (2j, 2j + 1).  Both use the
+// frequencies w_j = theta^(-2j/D) of the table rows table[p][j] = (cos, sin).
+//
+// A RoPE thread owns two 16-byte chunks of a row: chunk ci and chunk
+// ci + D/16 (its "lo" and "hi" chunks, 8 columns each).  Rotate-half pairs
+// column c of the lo chunk with the same column of the hi chunk (pairs
+// j = 8ci .. 8ci+7); interleaved pairs neighbours inside each chunk (pairs
+// 4ci .. 4ci+3 in lo, D/4 + 4ci .. D/4 + 4ci+3 in hi).  For both, the thread
+// keeps 8 angles as 4 float2 values so the arithmetic runs on packed pairs:
+//   rotate-half  c[q] = (cos w_{8ci+2q}, cos w_{8ci+2q+1})
+//   interleaved  c[q] = (cos w_{4ci+q},  cos w_{D/4+4ci+q})
+// and likewise s[q] for the sines.
+template <int D, bool IL>
+__device__ __forceinline__ void rope_load(const float2* __restrict__ row, int ci, float2 c[4], float2 s[4]) {
+    if constexpr (!IL) {
+        const float4* t4 = reinterpret_cast<const float4*>(row + ci * 8);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 f = __ldg(t4 + q);
+            c[q] = make_float2(f.x, f.z);
+            s[q] = make_float2(f.y, f.w);
+        }
+    } else {
+        const float4* lo = reinterpret_cast<const float4*>(row + ci * 4);
+        const float4* hi = reinterpret_cast<const float4*>(row + D / 4 + ci * 4);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float4 a = __ldg(lo + h), b = __ldg(hi + h);
+            c[2 * h] = make_float2(a.x, b.x);
+            s[2 * h] = make_float2(a.y, b.y);
+            c[2 * h + 1] = make_float2(a.z, b.z);
+            s[2 * h + 1] = make_float2(a.w, b.w);
+        }
+    }
+}
+
 // Per-thread RoPE state for rope_tile: this thread always handles the same
-// 8 rotation pairs j = 8*ci .. 8*ci+7 of rows spaced ROWS_PER_IT apart, so the
-// angle steps by the constant rotation e^{i * ROWS_PER_IT * w_j}, which is the
-// RoPE table's row ROWS_PER_IT.  Loaded once per kernel.
+// 8 rotation pairs of rows spaced ROWS_PER_IT apart, so the angle steps by the
+// constant rotation e^{i * ROWS_PER_IT * w_j}, which is the RoPE table's row
+// ROWS_PER_IT.  Loaded once per kernel.
 template <int D>
 struct RopeStep {
-    float2 c[4], s[4], ns[4];   // pairs (2q, 2q+1): cos, sin, -sin of the per-step angle
+    float2 c[4], s[4], ns[4];   // cos, sin, -sin of the per-step angle (packed as in rope_load)
 };
 
-template <int D>
+template <int D, bool IL>
 __device__ __forceinline__ RopeStep<D> rope_step(const float2* __restrict__ table, int lane) {
     constexpr int half = D / 2;
     constexpr int PAIRS_PER_ROW = half / 8;
     constexpr int ROWS_PER_IT = 32 / PAIRS_PER_ROW;
-    const int ci = lane % PAIRS_PER_ROW;
     RopeStep<D> st;
-    const float4* t4 = reinterpret_cast<const float4*>(table + ROWS_PER_IT * half + ci * 8);
+    rope_load<D, IL>(table + ROWS_PER_IT * half, lane % PAIRS_PER_ROW, st.c, st.s);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float4 f = __ldg(t4 + q);
-        st.c[q] = make_float2(f.x, f.z);
-        st.s[q] = make_float2(f.y, f.w);
-        st.ns[q] = make_float2(-f.y, -f.w);
-    }
+    for (int q = 0; q < 4; ++q) st.ns[q] = make_float2(-st.s[q].x, -st.s[q].y);
     return st;
 }
 
 // Rotate a staged tile of ROWS rows (segment-local positions pos0 + row) in
-// place: rotate-half pairs (c, c + D/2), x' = x cos - y sin, y' = y cos + x sin,
-// computed in fp32 (packed pairs) and rounded to bf16.  Executed by 128 threads
-// (4 warps, wr = 0..3); each 64-column block holds ROWS x 128 B.  A thread
-// reads the cos/sin of its first row from the table and advances the angle by
-// complex multiplication with its RopeStep (a few 1e-7 of drift over a tile).
-template <int D, int ROWS>
+// place: x' = x cos - y sin, y' = y cos + x sin for each pair (x, y) of the
+// pairing IL, computed in fp32 (packed pairs) and rounded to bf16.  Executed
+// by 128 threads (4 warps, wr = 0..3); each 64-column block holds ROWS x 128 B.
+// A thread reads the cos/sin of its first row from the table and advances the
+// angle by complex multiplication with its RopeStep (a few 1e-7 of drift over
+// a tile).
+template <int D, int ROWS, bool IL>
 __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2* __restrict__ table,
                                           const RopeStep<D>& step, int wr, int lane) {
     constexpr int half = D / 2;
     constexpr uint32_t BLK = ROWS * 128u;
-    constexpr int PAIRS_PER_ROW = half / 8;            // 16-byte chunk pairs per row
+    constexpr int PAIRS_PER_ROW = half / 8;            // threads per row
     constexpr int ROWS_PER_IT = 32 / PAIRS_PER_ROW;
     constexpr int ROWS_PER_WARP = ROWS / 4;
     const int rsub = lane / PAIRS_PER_ROW;
     const int ci = lane % PAIRS_PER_ROW;
     const int r0 = wr * ROWS_PER_WARP + rsub;
-    float2 cs[4], sn[4];   // cos/sin of rotation pairs (2q, 2q+1) at the current row
-    {
-        const float4* t4 = reinterpret_cast<const float4*>(
-            table + static_cast<int64_t>(pos0 + r0) * half + ci * 8);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 f = __ldg(t4 + q);
-            cs[q] = make_float2(f.x, f.z);
-            sn[q] = make_float2(f.y, f.w);
-        }
-    }
+    float2 cs[4], sn[4];   // cos/sin at the current row (packed as in rope_load)
+    rope_load<D, IL>(table + static_cast<int64_t>(pos0 + r0) * half, ci, cs, sn);
 #pragma unroll 2
     for (int it = 0; it < ROWS_PER_WARP / ROWS_PER_IT; ++it) {
         const int r = r0 + it * ROWS_PER_IT;
@@ -190,13 +213,19 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2*
         uint32_t na[4], nb[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float2 x = make_float2(bf16_lo(a[q]), bf16_hi(a[q]));
-            const float2 y = make_float2(bf16_lo(b[q]), bf16_hi(b[q]));
+            // (x, y) of the two pairs that share the angles cs[q], sn[q]
+            const float2 x = IL ? make_float2(bf16_lo(a[q]), bf16_lo(b[q])) : make_float2(bf16_lo(a[q]), bf16_hi(a[q]));
+            const float2 y = IL ? make_float2(bf16_hi(a[q]), bf16_hi(b[q])) : make_float2(bf16_lo(b[q]), bf16_hi(b[q]));
             const float2 nsn = make_float2(-sn[q].x, -sn[q].y);
             const float2 xr = fma2(x, cs[q], mul2(y, nsn));    // x cos - y sin
             const float2 yr = fma2(y, cs[q], mul2(x, sn[q]));  // y cos + x sin
-            na[q] = pack_bf16x2(xr.x, xr.y);
-            nb[q] = pack_bf16x2(yr.x, yr.y);
+            if constexpr (IL) {
+                na[q] = pack_bf16x2(xr.x, yr.x);
+                nb[q] = pack_bf16x2(xr.y, yr.y);
+            } else {
+                na[q] = pack_bf16x2(xr.x, xr.y);
+                nb[q] = pack_bf16x2(yr.x, yr.y);
+            }
         }
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                      ::"r"(lo_addr), "r"(na[0]), "r"(na[1]), "r"(na[2]), "r"(na[3]) : "memory");

@@ -31,6 +31,7 @@
 //   warps 12-15  RoPE on the staged q and K tiles (segment-local positions).
 // Every wait is bounded; on expiry the kernel sets VLC_DEVERR_TIMEOUT, drains
 // its own in-flight copies and MMAs, frees TMEM and returns.
+#include <type_traits>
 #include <cuda.h>
 #include <cmath>
 #include <cstdint>
@@ -450,34 +451,40 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // ------------------------------------------------------------ RoPE on staged q / K tiles
         setmaxnreg_dec<kRopeRegs>();
         const int wr = warp - 12;
-        RopeStep<D> step{};
-        if (p.use_rope) step = rope_step<D>(p.table, lane);
-        uint32_t qm = 0, kvn = 0;
-        bool ok = true;
-        for (int un = 0; ok; ++un) {
-            int u;
-            if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
-            const FUnit f = decode_funit(p, u);
-            for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
-                const int slot = qm % kQSlots;
-                if (!(ok = wait_warp(bar(Q_FULL + slot), (qm / kQSlots) & 1, abort))) break;
-                if (p.use_rope)
-                    rope_tile<D, 128>(sbase + LY::Q0 + slot * LY::TILE, (f.q0 + t) * BQ, p.table,
-                                      step, wr, lane);
-                fence_proxy_async_smem();
-                mbar_arrive(bar(Q_READY + slot));
-                ++qm;
+        // one copy of the loop per pairing, so neither carries the other's state
+        auto run = [&](auto il_tag) {
+            constexpr bool IL = decltype(il_tag)::value;
+            RopeStep<D> step{};
+            if (p.use_rope) step = rope_step<D, IL>(p.table, lane);
+            uint32_t qm = 0, kvn = 0;
+            bool ok = true;
+            for (int un = 0; ok; ++un) {
+                int u;
+                if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
+                const FUnit f = decode_funit(p, u);
+                for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
+                    const int slot = qm % kQSlots;
+                    if (!(ok = wait_warp(bar(Q_FULL + slot), (qm / kQSlots) & 1, abort))) break;
+                    if (p.use_rope)
+                        rope_tile<D, 128, IL>(sbase + LY::Q0 + slot * LY::TILE, (f.q0 + t) * BQ, p.table,
+                                              step, wr, lane);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(Q_READY + slot));
+                    ++qm;
+                }
+                for (int j = 0; j < f.nk && ok; ++j) {
+                    const int ks = kvn & 1;
+                    if (!(ok = wait_warp(bar(K_FULL + ks), (kvn >> 1) & 1, abort))) break;
+                    if (p.use_rope)
+                        rope_tile<D, 128, IL>(sbase + LY::K0 + ks * LY::TILE, j * BN, p.table, step, wr, lane);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(K_READY + ks));
+                    ++kvn;
+                }
             }
-            for (int j = 0; j < f.nk && ok; ++j) {
-                const int ks = kvn & 1;
-                if (!(ok = wait_warp(bar(K_FULL + ks), (kvn >> 1) & 1, abort))) break;
-                if (p.use_rope)
-                    rope_tile<D, 128>(sbase + LY::K0 + ks * LY::TILE, j * BN, p.table, step, wr, lane);
-                fence_proxy_async_smem();
-                mbar_arrive(bar(K_READY + ks));
-                ++kvn;
-            }
-        }
+        };
+        if (p.use_rope == kRopeInterleaved) run(std::true_type{});
+        else run(std::false_type{});
     } else if (warp == 3) {
         // ------------------------------------------------------------ TMA producer of V tiles
         setmaxnreg_dec<kCtrlRegs>();

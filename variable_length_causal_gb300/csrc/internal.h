@@ -44,6 +44,9 @@ cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int3
 cudaError_t launch_rope_table(float2* table, int32_t rows, int32_t d, double theta,
                               const int32_t* err, cudaStream_t s);
 
+// RoPE modes of FwdParams::use_rope / BwdParams::use_rope.
+constexpr int kRopeNone = 0, kRopeHalf = 1, kRopeInterleaved = 2;
+
 struct FwdParams {
     const void* q;
     const void* k;
@@ -60,7 +63,7 @@ struct FwdParams {
     int32_t nseg, total, H, d;
     int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
     float scale_log2;          // softmax_scale * log2(e)
-    int use_rope;
+    int use_rope;              // kRopeNone, kRopeHalf (rotate-half pairs) or kRopeInterleaved
 };
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s);
@@ -92,7 +95,8 @@ struct BwdParams {
     int32_t nseg, total, H, d;
     int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
     float scale;
-    int use_rope;              // 1: inputs are rotated in the prep pass, gradients un-rotated
+    int use_rope;              // kRopeHalf / kRopeInterleaved: inputs are rotated in the prep
+                               // pass with that pairing, gradients un-rotated; kRopeNone: no RoPE
 };
 
 cudaError_t launch_attn_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
