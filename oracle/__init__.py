@@ -15,8 +15,10 @@ closed forms at Q = 0, packed == per-sample, change-A-keeps-B, brute force
 shift invariance and closed-form angles, finite differences for the backward
 pass, and for the shifted cross-entropy: uniform-logit closed form, the pages'
 token-mean 2.5 versus sample-mean 2 example, torch's fp64 cross_entropy, and
-pre-shifted labels == the internal-shift formulation.  No oracle function is
-"parity unpinned".
+pre-shifted labels == the internal-shift formulation; the interleaved RoPE pairing by its
+complex-multiplication form and torch autograd; grouped key/value heads by torch SDPA with
+enable_gqa; padded layouts (cu_padded) by a masked attention written directly on the padded
+rows.  No oracle function is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -162,6 +164,21 @@ def rope_rows(x, pos, theta: float = 10000.0, interleaved: bool = False) -> np.n
     return out
 
 
+
+def real_rows(cu, cu_padded) -> np.ndarray:
+    """Row indices of the real tokens of a padded layout: segment r's L_r = cu[r+1] - cu[r]
+    tokens sit at rows cu_padded[r] .. cu_padded[r] + L_r - 1 and the rest of its slot
+    [cu_padded[r], cu_padded[r+1]) is padding ("Sequence packing and variable-length
+    attention", charlestar: Megatron's PackedSeqParams carries padded q/kv offsets next to
+    cu_seqlens, and TE's pad_between_seqs leaves padding between the samples).  Padding rows
+    are not tokens: no query attends to them and they attend to nothing."""
+    cu = np.asarray(cu, np.int64)
+    cp = np.asarray(cu_padded, np.int64)
+    L = np.diff(cu)
+    if len(cp) != len(cu) or cp[0] != 0 or np.any(np.diff(cp) < L):
+        raise ValueError("cu_padded must start at 0 and give every segment a slot >= its length")
+    return np.concatenate([np.arange(p, p + n) for p, n in zip(cp[:-1], L)]).astype(np.int64)
+
 def _mode(contract: bool, interleaved: bool) -> int:
     return int(bool(contract)) + (4 if interleaved else 0)
 
@@ -171,12 +188,23 @@ def _mode_f64(interleaved: bool) -> int:
 
 
 def attn_fwd(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
-             seg_heads=None, interleaved: bool = False):
+             seg_heads=None, interleaved: bool = False, cu_padded=None):
     """Exact per-segment causal attention in fp64.  q/k/v: bf16 tensors or uint16 bit arrays
     [total, H, d] (k and v may have fewer heads Hkv dividing H: query head h reads key/value
     head h // (H // Hkv)).  Returns (o [total, H, d] f64, lse [H, total] f64, natural log).
     With ``seg_heads`` (a list of (segment, head) pairs) only those are computed; the rest
-    stay 0."""
+    stay 0.  With ``cu_padded`` the rows follow the padded layout of ``real_rows``: the real
+    rows are gathered, attended as a contiguous pack, and scattered back; padding rows get
+    O = 0 and LSE = -inf (the log of an empty sum)."""
+    if cu_padded is not None:
+        idx = real_rows(cu, cu_padded)
+        qb, kb, vb = (bf16_bits(x)[idx] for x in (q, k, v))
+        o_r, lse_r = attn_fwd(qb, kb, vb, cu, scale, theta, contract, seg_heads, interleaved)
+        total, H, d = bf16_bits(q).shape
+        o = np.zeros((total, H, d), np.float64)
+        lse = np.full((H, total), -np.inf)
+        o[idx], lse[:, idx] = o_r, lse_r
+        return o, lse
     qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
     total, H, d = qb.shape
     Hkv = kb.shape[1]
@@ -241,10 +269,21 @@ def attn_bwd_f64(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, 
 
 
 def attn_bwd(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
-             seg_heads=None, interleaved: bool = False):
+             seg_heads=None, interleaved: bool = False, cu_padded=None):
     """Gradients (dq [total, H, d], dk and dv [total, Hkv, d]) f64 of sum(O * dO).  With
     ``seg_heads`` (a list of (segment, key/value head) pairs) only those are computed (dq for
-    every query head of each pair's group); other entries stay 0."""
+    every query head of each pair's group); other entries stay 0.  With ``cu_padded`` the
+    padding rows (``real_rows``) take no part and their gradients are 0."""
+    if cu_padded is not None:
+        idx = real_rows(cu, cu_padded)
+        gb, qb, kb, vb = (bf16_bits(x)[idx] for x in (dout, q, k, v))
+        r = attn_bwd(gb, qb, kb, vb, cu, scale, theta, contract, seg_heads, interleaved)
+        out = []
+        for full, part in zip((q, k, v), r):
+            z = np.zeros(bf16_bits(full).shape, np.float64)
+            z[idx] = part
+            out.append(z)
+        return tuple(out)
     gb, qb, kb, vb = bf16_bits(dout), bf16_bits(q), bf16_bits(k), bf16_bits(v)
     total, H, d = qb.shape
     Hkv = kb.shape[1]

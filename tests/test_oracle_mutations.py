@@ -1,6 +1,7 @@
 """Planted mistakes in a COPY of the oracle must fail its pins (CPU only).
 
-Each case edits one line of a temporary copy of oracle/oracle.c (a sign, an
+Each case edits one line of a temporary copy of oracle/oracle.c (or, where named,
+of the oracle's Python wrapper: a padded-layout gather) (a sign, an
 index, a dropped term, a transposed operand, an unreset position, an unstable
 order), rebuilds that copy, and runs tests/test_oracle_pins.py against it in a
 subprocess.  The committed oracle is never modified.
@@ -32,6 +33,7 @@ MUTATIONS = {
     "worklist_unstable_ties": ("if (ny >= nx) break;", "if (ny > nx) break;"),
     "rope_interleaved_pairing": ("if (interleaved) { *ia = 2 * j; *ib = 2 * j + 1; }",
                                  "if (interleaved) { *ia = j; *ib = j + 1; }"),
+    "padded_rows_from_cu": ("for p, n in zip(cp[:-1], L)", "for p, n in zip(cu[:-1], L)", "__init__.py"),
     "gqa_interleaved_heads": ("static int32_t kv_head(const orc_problem* P, int32_t h) { return h / (P->H / P->Hkv); }",
                               "static int32_t kv_head(const orc_problem* P, int32_t h) { return h % P->Hkv; }"),
     "ce_label_logit_sign": ("row[i] = (mx + log(s)) - zy;", "row[i] = (mx + log(s)) + zy;"),
@@ -42,14 +44,15 @@ MUTATIONS = {
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_planted_mistake_is_caught(name, tmp_path):
-    old, new = MUTATIONS[name]
+    old, new, *where = MUTATIONS[name]
+    fname = where[0] if where else "oracle.c"
     for sub in ("oracle", "tests", "variable_length_causal_gb300"):
         shutil.copytree(os.path.join(ROOT, sub), tmp_path / sub,
                         ignore=shutil.ignore_patterns("*.so", "__pycache__", "lib"))
     shutil.copy(os.path.join(ROOT, "pytest.ini"), tmp_path / "pytest.ini")
-    src = (tmp_path / "oracle" / "oracle.c").read_text()
+    src = (tmp_path / "oracle" / fname).read_text()
     assert src.count(old) == 1, name
-    (tmp_path / "oracle" / "oracle.c").write_text(src.replace(old, new))
+    (tmp_path / "oracle" / fname).write_text(src.replace(old, new))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_oracle_pins.py"], cwd=tmp_path, capture_output=True, text=True,
                        timeout=600)

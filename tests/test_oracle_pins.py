@@ -619,3 +619,58 @@ def test_interleaved_backward_finite_differences():
                                                            interleaved=True)[0] * g))
             num = (f(xp) - f(xm)) / (2 * eps)
             assert abs(num - gx[ix]) < 1e-6 * (1 + abs(num)), (name, ix)
+
+
+# ------------------------------------------------------------------ padded layouts (cu_padded)
+def _padded_case(seed=0):
+    lens = [5, 1, 9, 4]
+    slots = [8, 3, 9, 7]          # slot >= length; padding after each segment
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cp = np.concatenate([[0], np.cumsum(slots)]).astype(np.int32)
+    return lens, slots, cu, cp
+
+
+def test_padded_attention_against_masked_torch_on_padded_rows():
+    # the masked attention written directly on the padded rows: a real query sees the real
+    # keys of its own slot at positions <= its own; a padding query sees only itself and its
+    # output is zeroed, so nothing flows into or out of padding rows
+    lens, slots, cu, cp = _padded_case()
+    total, H, Hkv, d = int(cp[-1]), 4, 2, 16
+    g0 = torch.Generator().manual_seed(3)
+    q, g = (torch.randn((total, H, d), generator=g0).bfloat16() for _ in range(2))
+    k, v = (torch.randn((total, Hkv, d), generator=g0).bfloat16() for _ in range(2))
+    seg = np.repeat(np.arange(len(slots)), slots)
+    pos = np.arange(total) - cp[seg]
+    real = pos < np.asarray(lens)[seg]
+    allow = (seg[:, None] == seg[None, :]) & (pos[None, :] <= pos[:, None]) & real[None, :] & real[:, None]
+    allow |= np.diag(~real)
+    posd = torch.from_numpy(pos).double()
+    qt, kt, vt = (torch.from_numpy(_f64(x)).requires_grad_() for x in (q, k, v))
+    rq, rk = _rope_torch(qt, posd, d), _rope_torch(kt, posd, d)
+    kr, vr = (x.repeat_interleave(H // Hkv, dim=1) for x in (rk, vt))
+    s = torch.einsum("ihd,jhd->hij", rq, kr) / np.sqrt(d)
+    s = s.masked_fill(~torch.from_numpy(allow)[None], float("-inf"))
+    lse_t = torch.logsumexp(s, dim=-1)
+    o = torch.einsum("hij,jhd->ihd", torch.softmax(s, dim=-1), vr) * torch.from_numpy(real)[:, None, None]
+    (o * torch.from_numpy(_f64(g))).sum().backward()
+    o_orc, lse_orc = oracle.attn_fwd(q, k, v, cu, contract=False, cu_padded=cp)
+    assert np.max(np.abs(o_orc - o.detach().numpy())) < 1e-12
+    assert np.max(np.abs(lse_orc[:, real] - lse_t.detach().numpy()[:, real])) < 1e-12
+    assert np.all(np.isneginf(lse_orc[:, ~real])) and np.all(o_orc[~real] == 0)
+    dq, dk, dv = oracle.attn_bwd(g, q, k, v, cu, contract=False, cu_padded=cp)
+    assert np.max(np.abs(dq - qt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dk - kt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dv - vt.grad.numpy())) < 1e-11
+    assert np.all(dq[~real] == 0) and np.all(dk[~real] == 0) and np.all(dv[~real] == 0)
+
+
+def test_padded_equals_unpadded_when_slots_are_tight():
+    lens, _, cu, _ = _padded_case()
+    w = synth.custom_workload(lens, 2, 16)
+    rng = np.random.default_rng(8)
+    q, k, v = (torch.from_numpy(rng.standard_normal((w.total, 2, 16))).bfloat16() for _ in range(3))
+    a = oracle.attn_fwd(q, k, v, cu)
+    b = oracle.attn_fwd(q, k, v, cu, cu_padded=cu)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    with pytest.raises(ValueError):
+        oracle.real_rows(cu, np.array([0, 4, 5, 14, 18]))   # first slot shorter than its segment
