@@ -66,6 +66,8 @@ typedef enum {
 #define VLC_DEVERR_CU_TOTAL 0x4    /* cu[nseg] != total */
 #define VLC_DEVERR_MAXLEN 0x8      /* max_seqlen != largest segment length */
 #define VLC_DEVERR_LABEL 0x10      /* a label outside [0, vocab) and not -100 */
+#define VLC_DEVERR_CU_PADDED 0x20  /* cu_padded[0] != 0, a slot shorter than its segment,
+                                      or cu_padded[nseg] != total */
 #define VLC_DEVERR_TIMEOUT 0x100   /* a bounded mbarrier wait expired */
 
 /* Limits checked on the host. */
@@ -174,24 +176,42 @@ int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void*
 /* Option bits of vlc_attn_fwd_ex / vlc_attn_bwd_ex. */
 #define VLC_ROPE_INTERLEAVED 0x1u  /* RoPE pairs (x_{2j}, x_{2j+1}) instead of (x_j, x_{j+d/2}) */
 
-/* vlc_attn_fwd_gqa / vlc_attn_bwd_gqa with an option word.  flags == 0 is
- * exactly those calls; VLC_ROPE_INTERLEAVED rotates the adjacent pairs
- * (x_{2j}, x_{2j+1}) of q and k by p_i * theta^(-2j/d), the complex-number form
- * of RoFormer's rotation that "Sequence packing and variable-length attention"
- * (charlestar, "Positions are reset per segment") cites next to the
- * rotate-half form of HF Llama; the per-segment reset and the frequencies are
- * unchanged, and the backward un-rotates dq and dk with the same pairing.  The
- * bit has no effect when rope_theta == 0.  Unknown bits return VLC_ERR_ARG.
- * Workspace sizes are those of vlc_workspace_bytes_gqa. */
-int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
-                    int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
-                    float softmax_scale, float rope_theta, uint32_t flags, void* o, float* lse,
-                    void* ws, size_t ws_bytes, void* stream);
+/* vlc_attn_fwd_gqa / vlc_attn_bwd_gqa with a padded layout and an option word;
+ * cu_padded == NULL and flags == 0 is exactly those calls.
+ *
+ * cu_padded (device int32 [nseg+1] or NULL): padding between segments, the
+ * padded q/kv offsets of Megatron's PackedSeqParams and TE's pad_between_seqs
+ * that "Sequence packing and variable-length attention" (charlestar, the
+ * Megatron/TE data path) describes.  Segment r still has L_r = cu[r+1] - cu[r]
+ * tokens, now at rows cu_padded[r] .. cu_padded[r] + L_r - 1; the rest of its
+ * slot, up to cu_padded[r+1], is padding.  total counts all rows (cu_padded[nseg]).
+ * Positions restart at 0 at each slot start.  Padding rows are not tokens: no
+ * query attends to them and they attend to nothing.  Outputs at padding rows:
+ * o = 0 and lse = -inf (the log of an empty sum); dq, dk, dv = 0.  Inputs at
+ * padding rows (q, k, v, dout, o) must be finite: they never reach a result,
+ * but the tensor cores multiply them by zero weights.  Validity (cu_padded[0]
+ * == 0, every slot at least its segment's length, cu_padded[nseg] == total) is
+ * checked on the device and reported as VLC_DEVERR_CU_PADDED; cu must then
+ * still start at 0, increase, and have max_seqlen as its largest step.
+ *
+ * flags: VLC_ROPE_INTERLEAVED rotates the adjacent pairs (x_{2j}, x_{2j+1}) of
+ * q and k by p_i * theta^(-2j/d), the complex-number form of RoFormer's
+ * rotation that the same page ("Positions are reset per segment") cites next
+ * to the rotate-half form of HF Llama; the per-segment reset and the
+ * frequencies are unchanged, and the backward un-rotates dq and dk with the
+ * same pairing.  The bit has no effect when rope_theta == 0.  Unknown bits
+ * return VLC_ERR_ARG.
+ *
+ * Workspace sizes are those of vlc_workspace_bytes_gqa with total = all rows. */
+int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* cu,
+                    const int32_t* cu_padded, int32_t nseg, int32_t total, int32_t H, int32_t H_kv,
+                    int32_t d, int32_t max_seqlen, float softmax_scale, float rope_theta,
+                    uint32_t flags, void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 int vlc_attn_bwd_ex(const void* dout, const void* q, const void* k, const void* v, const void* o,
-                    const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
-                    int32_t H_kv, int32_t d, int32_t max_seqlen, float softmax_scale,
-                    float rope_theta, uint32_t flags, void* dq, void* dk, void* dv, void* ws,
-                    size_t ws_bytes, void* stream);
+                    const float* lse, const int32_t* cu, const int32_t* cu_padded, int32_t nseg,
+                    int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                    float softmax_scale, float rope_theta, uint32_t flags, void* dq, void* dk,
+                    void* dv, void* ws, size_t ws_bytes, void* stream);
 
 /* Forward attention for callers that cannot allocate device memory.  No
  * counterpart on the pages: it exists for callers that may not obtain memory

@@ -22,6 +22,7 @@ VLC_OK, VLC_ERR_ARG, VLC_ERR_CU_SEQLENS, VLC_ERR_UNSUPPORTED = 0, 1, 2, 3
 VLC_ERR_WORKSPACE, VLC_ERR_CUDA, VLC_ERR_TIMEOUT, VLC_ERR_LABEL = 4, 5, 6, 7
 DEVERR_CU_FIRST, DEVERR_CU_ORDER, DEVERR_CU_TOTAL, DEVERR_MAXLEN = 0x1, 0x2, 0x4, 0x8
 DEVERR_TIMEOUT = 0x100
+DEVERR_LABEL, DEVERR_CU_PADDED = 0x10, 0x20
 WORKLIST_FWD, WORKLIST_BWD = 0, 1
 ROPE_INTERLEAVED = 0x1
 
@@ -92,11 +93,11 @@ def load_library(path: str = LIB_PATH):
                                          P, P, P, P, sz, P]
         lib.vlc_attn_bwd_gqa.restype = cint
         u32 = ctypes.c_uint32
-        lib.vlc_attn_fwd_ex.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, u32, P, P, P,
-                                        sz, P]
+        lib.vlc_attn_fwd_ex.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, u32, P, P,
+                                        P, sz, P]
         lib.vlc_attn_fwd_ex.restype = cint
-        lib.vlc_attn_bwd_ex.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, u32,
-                                        P, P, P, P, sz, P]
+        lib.vlc_attn_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32,
+                                        u32, P, P, P, P, sz, P]
         lib.vlc_attn_bwd_ex.restype = cint
         _lib = lib
         return lib
@@ -121,9 +122,13 @@ def _require_cuda(*ts):
             raise ValueError("all tensors must be CUDA tensors (the library has no CPU path)")
 
 
-def _cu_info(cu_seqlens: torch.Tensor):
-    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
-        raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor")
+def _cu_info(cu_seqlens: torch.Tensor, cu_padded: Optional[torch.Tensor] = None):
+    for c in (cu_seqlens, cu_padded):
+        if c is not None and (c.dtype != torch.int32 or c.dim() != 1 or not c.is_contiguous()):
+            raise ValueError("cu_seqlens / cu_seqlens_padded must be contiguous 1-D int32 tensors")
+    if cu_padded is not None and (cu_padded.numel() != cu_seqlens.numel() or
+                                  cu_padded.device != cu_seqlens.device):
+        raise ValueError("cu_seqlens_padded must match cu_seqlens in size and device")
     return cu_seqlens.numel() - 1
 
 
@@ -234,19 +239,23 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     max_seqlen: int, softmax_scale: Optional[float] = None,
                     rope_theta: float = 10000.0, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                    check: bool = True, rope_interleaved: bool = False):
+                    check: bool = True, rope_interleaved: bool = False,
+                    cu_seqlens_padded: Optional[torch.Tensor] = None):
     """Segment-local causal attention with per-segment RoPE reset.  Returns (O, LSE[H, total]).
     k and v may have fewer heads than q (grouped: query head h reads head h // (H // H_kv)).
-    rope_interleaved rotates the pairs (x[2j], x[2j+1]) instead of (x[j], x[j + d/2])."""
+    rope_interleaved rotates the pairs (x[2j], x[2j+1]) instead of (x[j], x[j + d/2]).
+    cu_seqlens_padded gives each segment a slot of rows starting at cu_seqlens_padded[r]
+    (padding between segments; padding rows get O = 0, LSE = -inf)."""
     lib = load_library()
-    _require_cuda(q, k, v, cu_seqlens)
+    _require_cuda(q, k, v, cu_seqlens, cu_seqlens_padded)
     H_kv = _check_qkv([q] + ([] if out is None else [out]), [k, v])
     total, H, d = q.shape
-    nseg = _cu_info(cu_seqlens)
+    nseg = _cu_info(cu_seqlens, cu_seqlens_padded)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
     ws = new_workspace(nseg, total, H, d, max_seqlen, False, q.device, H_kv) if workspace is None else workspace
-    st = lib.vlc_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseg, total, H, H_kv, d,
+    st = lib.vlc_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
+                             nseg, total, H, H_kv, d,
                              int(max_seqlen), _scale(softmax_scale, d), float(rope_theta),
                              ROPE_INTERLEAVED if rope_interleaved else 0, _ptr(out), _ptr(lse), _ptr(ws),
                              ws.numel(), _stream(q.device))
@@ -261,13 +270,15 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                     softmax_scale: Optional[float] = None, rope_theta: float = 10000.0,
                     dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
                     dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                    check: bool = True, rope_interleaved: bool = False):
-    """Gradients (dQ, dK, dV) of sum(O * dO) for the forward above (dK, dV shaped like k, v)."""
+                    check: bool = True, rope_interleaved: bool = False,
+                    cu_seqlens_padded: Optional[torch.Tensor] = None):
+    """Gradients (dQ, dK, dV) of sum(O * dO) for the forward above (dK, dV shaped like k, v;
+    zero at padding rows)."""
     lib = load_library()
-    _require_cuda(dout, q, k, v, o, lse, cu_seqlens)
+    _require_cuda(dout, q, k, v, o, lse, cu_seqlens, cu_seqlens_padded)
     H_kv = _check_qkv([q, dout, o], [k, v])
     total, H, d = q.shape
-    nseg = _cu_info(cu_seqlens)
+    nseg = _cu_info(cu_seqlens, cu_seqlens_padded)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous fp32 [H, total]")
     dq = torch.empty_like(q) if dq is None else dq
@@ -275,7 +286,8 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
     dv = torch.empty_like(v) if dv is None else dv
     ws = new_workspace(nseg, total, H, d, max_seqlen, True, q.device, H_kv) if workspace is None else workspace
     st = lib.vlc_attn_bwd_ex(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                             _ptr(cu_seqlens), nseg, total, H, H_kv, d, int(max_seqlen),
+                             _ptr(cu_seqlens), _ptr(cu_seqlens_padded), nseg, total, H, H_kv, d,
+                             int(max_seqlen),
                              _scale(softmax_scale, d), float(rope_theta),
                              ROPE_INTERLEAVED if rope_interleaved else 0, _ptr(dq), _ptr(dk), _ptr(dv),
                              _ptr(ws), ws.numel(), _stream(q.device))

@@ -193,10 +193,10 @@ static int rope_mode(float rope_theta, uint32_t flags) {
     return (flags & VLC_ROPE_INTERLEAVED) ? kRopeInterleaved : kRopeHalf;
 }
 
-int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
-                    int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
-                    float softmax_scale, float rope_theta, uint32_t flags, void* o, float* lse,
-                    void* ws, size_t ws_bytes, void* stream) {
+int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* cu,
+                    const int32_t* cu_padded, int32_t nseg, int32_t total, int32_t H, int32_t H_kv,
+                    int32_t d, int32_t max_seqlen, float softmax_scale, float rope_theta,
+                    uint32_t flags, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
     if (q == nullptr || k == nullptr || v == nullptr || cu == nullptr || o == nullptr ||
         lse == nullptr)
         return VLC_ERR_ARG;
@@ -218,7 +218,11 @@ int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* 
 
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
     if (launch_worklist(cu, nseg, total, max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD, items,
-                        L.item_cap, order, seg_base, &hdr->count, &hdr->err, s) != cudaSuccess)
+                        L.item_cap, order, seg_base, &hdr->count, &hdr->err, s, cu_padded) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    if (cu_padded != nullptr &&
+        launch_pad_fill(cu, cu_padded, nseg, total, o, int64_t(H) * d * 2, nullptr, 0, nullptr, 0, lse, H,
+                        &hdr->err, num_sms_cached(), s) != cudaSuccess)
         return VLC_ERR_CUDA;
     const bool rope = rope_theta != 0.f;
     if (rope && launch_rope_table(table, L.table_rows, d, static_cast<double>(rope_theta),
@@ -226,6 +230,7 @@ int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* 
         return VLC_ERR_CUDA;
     FwdParams p{};
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu = cu;
+    p.rows = cu_padded != nullptr ? cu_padded : cu;
     p.items = items; p.seg_base = seg_base; p.count = &hdr->count; p.err = &hdr->err;
     p.next = &hdr->next[0];
     p.table = rope ? table : nullptr;
@@ -241,8 +246,8 @@ int vlc_attn_fwd_gqa(const void* q, const void* k, const void* v, const int32_t*
                      int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
                      float softmax_scale, float rope_theta, void* o, float* lse, void* ws,
                      size_t ws_bytes, void* stream) {
-    return vlc_attn_fwd_ex(q, k, v, cu, nseg, total, H, H_kv, d, max_seqlen, softmax_scale, rope_theta,
-                           0u, o, lse, ws, ws_bytes, stream);
+    return vlc_attn_fwd_ex(q, k, v, cu, nullptr, nseg, total, H, H_kv, d, max_seqlen, softmax_scale,
+                           rope_theta, 0u, o, lse, ws, ws_bytes, stream);
 }
 
 int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
@@ -253,10 +258,10 @@ int vlc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
 }
 
 int vlc_attn_bwd_ex(const void* dout, const void* q, const void* k, const void* v, const void* o,
-                    const float* lse, const int32_t* cu, int32_t nseg, int32_t total, int32_t H,
-                    int32_t H_kv, int32_t d, int32_t max_seqlen, float softmax_scale,
-                    float rope_theta, uint32_t flags, void* dq, void* dk, void* dv, void* ws,
-                    size_t ws_bytes, void* stream) {
+                    const float* lse, const int32_t* cu, const int32_t* cu_padded, int32_t nseg,
+                    int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                    float softmax_scale, float rope_theta, uint32_t flags, void* dq, void* dk,
+                    void* dv, void* ws, size_t ws_bytes, void* stream) {
     if (dout == nullptr || q == nullptr || k == nullptr || v == nullptr || o == nullptr ||
         lse == nullptr || cu == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
         return VLC_ERR_ARG;
@@ -282,11 +287,15 @@ int vlc_attn_bwd_ex(const void* dout, const void* q, const void* k, const void* 
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
     // q-tile items (dQ pass) and key-tile items (dK/dV pass)
     if (launch_worklist(cu, nseg, total, max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items_q,
-                        L.item_cap, order, seg_base_q, &hdr->count, &hdr->err, s) != cudaSuccess)
+                        L.item_cap, order, seg_base_q, &hdr->count, &hdr->err, s, cu_padded) != cudaSuccess)
         return VLC_ERR_CUDA;
     if (launch_worklist(cu, nseg, total, max_seqlen, kBwdBM, kFwdBN, VLC_WORKLIST_BWD, items_k,
-                        L.item_cap, order + nseg, seg_base_k, &hdr->count2, &hdr->err, s) !=
+                        L.item_cap, order + nseg, seg_base_k, &hdr->count2, &hdr->err, s, cu_padded) !=
         cudaSuccess)
+        return VLC_ERR_CUDA;
+    if (cu_padded != nullptr &&
+        launch_pad_fill(cu, cu_padded, nseg, total, dq, int64_t(H) * d * 2, dk, int64_t(H_kv) * d * 2, dv,
+                        int64_t(H_kv) * d * 2, nullptr, H, &hdr->err, num_sms_cached(), s) != cudaSuccess)
         return VLC_ERR_CUDA;
     const bool rope = rope_theta != 0.f;
     if (rope && launch_rope_table(table, L.table_rows, d, static_cast<double>(rope_theta),
@@ -295,6 +304,7 @@ int vlc_attn_bwd_ex(const void* dout, const void* q, const void* k, const void* 
     BwdParams p{};
     p.dout = dout; p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
     p.dq = dq; p.dk = dk; p.dv = dv; p.cu = cu;
+    p.rows = cu_padded != nullptr ? cu_padded : cu;
     p.items = items_q; p.seg_base = seg_base_q; p.count = &hdr->count; p.err = &hdr->err;
     p.items_k = items_k; p.seg_base_k = seg_base_k; p.count_k = &hdr->count2;
     p.next_q = &hdr->next[1];
@@ -315,8 +325,8 @@ int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void*
                      int32_t H_kv, int32_t d, int32_t max_seqlen, float softmax_scale,
                      float rope_theta, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
                      void* stream) {
-    return vlc_attn_bwd_ex(dout, q, k, v, o, lse, cu, nseg, total, H, H_kv, d, max_seqlen, softmax_scale,
-                           rope_theta, 0u, dq, dk, dv, ws, ws_bytes, stream);
+    return vlc_attn_bwd_ex(dout, q, k, v, o, lse, cu, nullptr, nseg, total, H, H_kv, d, max_seqlen,
+                           softmax_scale, rope_theta, 0u, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,

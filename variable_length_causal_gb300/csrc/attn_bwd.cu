@@ -63,7 +63,8 @@ template <int D>
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const uint4* __restrict__ q,
             const uint4* __restrict__ k, uint4* __restrict__ qrot, uint4* __restrict__ krot,
-            float* __restrict__ delta, const int32_t* __restrict__ cu, int32_t nseg,
+            float* __restrict__ delta, const int32_t* __restrict__ cu,
+            const int32_t* __restrict__ seg_rows, int32_t nseg,
             const float2* __restrict__ table, int32_t total, int32_t H, int32_t Hkv, int rope,
             const int32_t* __restrict__ err) {
     if (*err != 0) return;
@@ -89,12 +90,16 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
                 acc += bf16_lo(gv[e]) * bf16_lo(ov[e]) + bf16_hi(gv[e]) * bf16_hi(ov[e]);
             if (rope) {
                 const int64_t tok = row / H;
-                int a = 0, b = nseg - 1;   // segment of tok (clamped, in bounds)
+                int a = 0, b = nseg - 1;   // segment (slot) of tok (clamped, in bounds)
                 while (a < b) {
                     const int mid = (a + b + 1) >> 1;
-                    if (__ldg(cu + mid) <= tok) a = mid; else b = mid - 1;
+                    if (__ldg(seg_rows + mid) <= tok) a = mid; else b = mid - 1;
                 }
-                const int64_t pos = tok - __ldg(cu + a);
+                // rows past the segment's length are padding (padded layouts only):
+                // their rotated copies are zeros, so every operand row stays finite
+                const int64_t pos0 = tok - __ldg(seg_rows + a);
+                const bool real = pos0 < __ldg(cu + a + 1) - __ldg(cu + a);
+                const int64_t pos = real ? pos0 : 0;
                 const bool il = rope == kRopeInterleaved;
                 // cs/sn[2e], [2e+1]: angles of the two pairs that the e-th words of the lo
                 // and hi chunks take part in (rotate-half: the pairs at word e's two
@@ -125,6 +130,11 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
                     const uint4* src = which ? k : q;
                     uint4* dst = which ? krot : qrot;
                     const int64_t a0 = which ? klo : lo, a1 = which ? khi : hi;
+                    if (!real) {
+                        dst[a0] = make_uint4(0u, 0u, 0u, 0u);
+                        dst[a1] = make_uint4(0u, 0u, 0u, 0u);
+                        continue;
+                    }
                     const uint4 x4 = __ldg(src + a0), y4 = __ldg(src + a1);
                     const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
                     uint32_t nx[4], ny[4];
@@ -370,7 +380,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_put(rg, n, p.next_q, nunits, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
                 // the staging slot frees as soon as the math warps copied the last unit's rows to TMEM
                 if (!(ok = mbar_wait(bar(QD_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(QD_FULL), 2 * LY::TILE);
@@ -406,7 +416,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             for (int n = 0; ok; ++n) {
                 int u;
                 if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
                 for (int j = 0; j < w.hi && ok; ++j) {
                     const uint32_t nn = kv + j;
                     const int vs = nn % kVStages;
@@ -474,7 +484,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
                 if (!(ok = wait_warp(bar(QT_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_s(kv))) break;
                 if (!(ok = issue_dp(kv))) break;
@@ -535,7 +545,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         bool have = ok && u >= 0;
         Unit w{};
         if (have) {
-            w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+            w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
             ok = have = stage(0);
         }
         while (have) {
@@ -598,7 +608,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             if (!(ok = ring_get_warp(rg, static_cast<int>(unit_it) + 1, abort, u2))) break;
             const bool have_next = u2 >= 0;
             if (have_next) {
-                w2 = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u2);
+                w2 = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u2);
                 if (!(ok = stage(unit_it + 1))) break;
             }
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
@@ -755,7 +765,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_put(rg, n, p.next_k, nunits, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.Hkv, u);   // w.h: key/value head
+                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.nseg, p.Hkv, u);   // w.h: key/value head
                 if (!(ok = mbar_wait(bar(KV_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(KV_FULL), 2 * LY::TILE);
                 const int krow = w.row0 + w.tile * 128;
@@ -830,7 +840,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.Hkv, u);
+                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.nseg, p.Hkv, u);
                 if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_st(st))) break;
                 issue_dpt(st);
@@ -879,7 +889,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int n = 0; ok; ++n) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.Hkv, u);
+            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.nseg, p.Hkv, u);
             const int nq = w.hi - w.lo;
             for (int sq = 0; sq < grp * nq && ok; ++sq, ++st) {
                 const int i = w.lo + sq % nq, hq = w.h * grp + sq / nq;
@@ -916,7 +926,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int n = 0; ok; ++n, ++unit_it) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.nseg, p.Hkv, u);
+            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.nseg, p.Hkv, u);
             const int kvpos = w.tile * 128 + r;
             const int nq = w.hi - w.lo;
             for (int sq = 0; sq < grp * nq; ++sq, ++st) {
@@ -1061,7 +1071,7 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
         bwd::prep_kernel<D><<<static_cast<int>(blocks), 256, 0, s>>>(
             static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.o),
             static_cast<const uint4*>(p.q), static_cast<const uint4*>(p.k), static_cast<uint4*>(p.qrot),
-            static_cast<uint4*>(p.krot), p.delta, p.cu, p.nseg, p.table, p.total, p.H, p.Hkv, p.use_rope,
+            static_cast<uint4*>(p.krot), p.delta, p.cu, p.rows, p.nseg, p.table, p.total, p.H, p.Hkv, p.use_rope,
             p.err);
     }
     // with RoPE the attention passes read the rotated copies

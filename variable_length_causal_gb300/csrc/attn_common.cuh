@@ -14,10 +14,13 @@ struct Unit {
 };
 
 // Unit u -> (item, head).  Units run over the sorted segments; inside a
-// segment head-major, then the segment's items in work-list order.
+// segment head-major, then the segment's items in work-list order.  The
+// segment's length comes from cu, its first row from rows (cu itself, or the
+// padded offsets of a layout with padding between segments).
 __device__ __forceinline__ Unit decode_unit(const int4* __restrict__ items,
                                             const int32_t* __restrict__ seg_base,
-                                            const int32_t* __restrict__ cu, int nseg, int H, int u) {
+                                            const int32_t* __restrict__ cu,
+                                            const int32_t* __restrict__ rows, int nseg, int H, int u) {
     const int64_t HH = H;
     int lo = 0, hi = nseg - 1;
     while (lo < hi) {
@@ -34,8 +37,8 @@ __device__ __forceinline__ Unit decode_unit(const int4* __restrict__ items,
     w.tile = it.y;
     w.lo = it.z;
     w.hi = it.w;
-    w.row0 = __ldg(cu + it.x);
-    w.L = __ldg(cu + it.x + 1) - w.row0;
+    w.L = __ldg(cu + it.x + 1) - __ldg(cu + it.x);
+    w.row0 = __ldg(rows + it.x);
     return w;
 }
 

@@ -102,7 +102,7 @@ struct FUnit {
 
 __device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
     FUnit f;
-    f.w = decode_unit(p.items, p.seg_base, p.cu, p.nseg, p.H, u);
+    f.w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
     const int T = (f.w.L + BQ - 1) / BQ;
     const int s = T & 1;
     const bool lone = (s != 0) && (f.w.tile == 0);

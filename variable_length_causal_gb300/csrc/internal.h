@@ -39,7 +39,15 @@ cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64
 cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
                             int32_t BM, int32_t BN, int kind, int4* items, int64_t cap,
                             int32_t* order, int32_t* seg_base, int32_t* count, int32_t* err,
-                            cudaStream_t s);
+                            cudaStream_t s, const int32_t* cu_padded = nullptr);
+
+// Padded layouts: zero the padding rows [cu_padded[r] + L_r, cu_padded[r+1]) of up
+// to three bf16 row-major tensors (row_bytes each; null to skip) and set those
+// columns of lse ([H, total], null to skip) to -inf.  No-op if *err != 0.
+cudaError_t launch_pad_fill(const int32_t* cu, const int32_t* cu_padded, int32_t nseg, int32_t total,
+                            void* a, int64_t a_row_bytes, void* b, int64_t b_row_bytes, void* c,
+                            int64_t c_row_bytes, float* lse, int32_t H, const int32_t* err,
+                            int num_sms, cudaStream_t s);
 
 cudaError_t launch_rope_table(float2* table, int32_t rows, int32_t d, double theta,
                               const int32_t* err, cudaStream_t s);
@@ -54,6 +62,7 @@ struct FwdParams {
     void* o;
     float* lse;
     const int32_t* cu;
+    const int32_t* rows;       // [nseg+1] first row of each segment (cu_padded, or cu if unpadded)
     const int4* items;
     const int32_t* seg_base;   // [nseg+1] item offsets of the sorted segments
     const int32_t* count;
@@ -79,6 +88,7 @@ struct BwdParams {
     void* dk;
     void* dv;
     const int32_t* cu;
+    const int32_t* rows;       // [nseg+1] first row of each segment (cu_padded, or cu if unpadded)
     const int4* items;         // q-tile items (dQ pass), as in the forward
     const int32_t* seg_base;
     const int32_t* count;

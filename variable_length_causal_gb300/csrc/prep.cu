@@ -7,6 +7,8 @@
 //   * positions and labels: p_i = i - cu_r and pre-shifted labels with -100 at
 //     segment ends ("Length grouping, de-padding and packing", M020 section 06);
 //   * RoPE cos/sin table for fixed frequencies theta^(-2j/d).
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 
 #include "../../include/vlc.h"
@@ -56,7 +58,8 @@ __global__ void __launch_bounds__(kWlThreads, 1)
 worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int32_t max_seqlen,
                 int32_t BM, int32_t BN, int kind, int4* __restrict__ items, int64_t cap,
                 int32_t* __restrict__ order, int32_t* __restrict__ seg_base,
-                int32_t* __restrict__ count, int32_t* __restrict__ err) {
+                int32_t* __restrict__ count, int32_t* __restrict__ err,
+                const int32_t* __restrict__ cu_padded) {
     extern __shared__ int wl_smem[];
     int* hist = wl_smem;                    // [nbins] counts, then running positions
     __shared__ int warp_sums[33];
@@ -79,8 +82,16 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
         if (r == 0 && a != 0) local_err |= VLC_DEVERR_CU_FIRST;
         if (b <= a) local_err |= VLC_DEVERR_CU_ORDER;
         local_max = max(local_max, b - a);
+        if (cu_padded != nullptr) {   // slot r holds segment r: it starts at 0 and is long enough
+            const int pa = cu_padded[r], pb = cu_padded[r + 1];
+            if ((r == 0 && pa != 0) || static_cast<int64_t>(pb) - pa < static_cast<int64_t>(b) - a)
+                local_err |= VLC_DEVERR_CU_PADDED;
+        }
     }
-    if (tid == 0 && cu[nseg] != total) local_err |= VLC_DEVERR_CU_TOTAL;
+    if (tid == 0) {
+        if (cu_padded == nullptr ? cu[nseg] != total : cu_padded[nseg] != total)
+            local_err |= (cu_padded == nullptr ? VLC_DEVERR_CU_TOTAL : VLC_DEVERR_CU_PADDED);
+    }
     if (local_err) atomicOr(&s_err, local_err);
     atomicMax(&s_maxlen, local_max);
     __syncthreads();
@@ -199,7 +210,7 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
 cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
                             int32_t BM, int32_t BN, int kind, int4* items, int64_t cap,
                             int32_t* order, int32_t* seg_base, int32_t* count, int32_t* err,
-                            cudaStream_t s) {
+                            cudaStream_t s, const int32_t* cu_padded) {
     const int tile = (kind == VLC_WORKLIST_FWD) ? BM : BN;
     const int nbins = (max_seqlen + tile - 1) / tile + 1;
     const size_t smem = sizeof(int) * static_cast<size_t>(nbins);
@@ -210,7 +221,57 @@ cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int3
         if (e != cudaSuccess) return e;
     }
     worklist_kernel<<<1, kWlThreads, smem, s>>>(cu, nseg, total, max_seqlen, BM, BN, kind, items,
-                                                cap, order, seg_base, count, err);
+                                                cap, order, seg_base, count, err, cu_padded);
+    return cudaGetLastError();
+}
+
+// ============================================================== padding rows
+//
+// Padded layouts: the rows [cu_padded[r] + L_r, cu_padded[r+1]) of slot r are
+// not tokens.  One block per slot (grid-stride over slots) zeroes them in each
+// given bf16 tensor with 16-byte stores (a row is H * d * 2 >= 128 bytes, so a
+// slot's padding is one contiguous, aligned byte range) and writes -inf into
+// those columns of lse.  Ranges are clamped to [0, total) rows.
+
+__global__ void __launch_bounds__(256)
+pad_fill_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_padded, int32_t nseg,
+                int32_t total, uint4* __restrict__ a, int64_t a_row16, uint4* __restrict__ b,
+                int64_t b_row16, uint4* __restrict__ c, int64_t c_row16, float* __restrict__ lse,
+                int32_t H, const int32_t* __restrict__ err) {
+    if (*err != 0) return;
+    for (int r = blockIdx.x; r < nseg; r += gridDim.x) {
+        const int64_t p0 = max(static_cast<int64_t>(0),
+                               min(static_cast<int64_t>(total),
+                                   static_cast<int64_t>(cu_padded[r]) + (cu[r + 1] - cu[r])));
+        const int64_t p1 = max(static_cast<int64_t>(0), min(static_cast<int64_t>(total),
+                                                            static_cast<int64_t>(cu_padded[r + 1])));
+        if (p0 >= p1) continue;   // block-uniform
+        uint4* const dst[3] = {a, b, c};
+        const int64_t row16[3] = {a_row16, b_row16, c_row16};
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            if (dst[t] == nullptr) continue;
+            for (int64_t i = p0 * row16[t] + threadIdx.x; i < p1 * row16[t]; i += blockDim.x)
+                dst[t][i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (lse != nullptr) {
+            const int64_t n = p1 - p0;
+            for (int64_t i = threadIdx.x; i < n * H; i += blockDim.x) {
+                const int64_t h = i / n;
+                lse[h * total + p0 + (i - h * n)] = -INFINITY;
+            }
+        }
+    }
+}
+
+cudaError_t launch_pad_fill(const int32_t* cu, const int32_t* cu_padded, int32_t nseg, int32_t total,
+                            void* a, int64_t a_row_bytes, void* b, int64_t b_row_bytes, void* c,
+                            int64_t c_row_bytes, float* lse, int32_t H, const int32_t* err,
+                            int num_sms, cudaStream_t s) {
+    const int blocks = static_cast<int>(std::min<int64_t>(nseg, 4LL * num_sms));
+    pad_fill_kernel<<<blocks, 256, 0, s>>>(cu, cu_padded, nseg, total, static_cast<uint4*>(a),
+                                           a_row_bytes / 16, static_cast<uint4*>(b), b_row_bytes / 16,
+                                           static_cast<uint4*>(c), c_row_bytes / 16, lse, H, err);
     return cudaGetLastError();
 }
 
