@@ -66,18 +66,19 @@ def _load():
                 f.restype = i64
             lib.orc_rope_rows.argtypes = [P, P, i64, i32, f64, ctypes.c_int, P]
             lib.orc_rope_rows.restype = None
-            lib.orc_attn_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, f64, ctypes.c_int, P, P]
+            lib.orc_attn_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, f64, ctypes.c_int,
+                                         P, P]
             lib.orc_attn_fwd.restype = None
-            lib.orc_attn_fwd_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, f64, ctypes.c_int,
-                                              P, P, i64, P, P]
+            lib.orc_attn_fwd_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, f64,
+                                              ctypes.c_int, P, P, i64, P, P]
             lib.orc_attn_fwd_rows.restype = None
-            lib.orc_attn_fwd_seg_heads.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, f64,
+            lib.orc_attn_fwd_seg_heads.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, f64,
                                                    ctypes.c_int, P, P, i64, P, P]
             lib.orc_attn_fwd_seg_heads.restype = None
-            lib.orc_attn_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, f64, ctypes.c_int,
-                                         P, P, P]
+            lib.orc_attn_bwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, f64,
+                                         ctypes.c_int, P, P, P]
             lib.orc_attn_bwd.restype = None
-            lib.orc_attn_bwd_seg_heads.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, f64,
+            lib.orc_attn_bwd_seg_heads.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, f64,
                                                    ctypes.c_int, P, P, i64, P, P, P]
             lib.orc_attn_bwd_seg_heads.restype = None
             lib.orc_shifted_ce.argtypes = [P, ctypes.c_int, i32, i32, P, P, i32, P, P, P, P]
@@ -187,15 +188,30 @@ def _mode_f64(interleaved: bool) -> int:
     return -5 if interleaved else -1
 
 
+def _kv_args(cu, cu_kv, total_kv):
+    """cu_kv pointer and key/value row count for the C calls (None: self-attention)."""
+    if cu_kv is None:
+        return None, 0, None
+    cu_kv = _c(cu_kv, np.int32)
+    if len(cu_kv) != len(cu) or cu_kv[0] != 0 or np.any(np.diff(cu_kv) < np.diff(np.asarray(cu))):
+        raise ValueError("cu_kv must start at 0 and give every segment at least as many keys as queries")
+    if cu_kv[-1] != total_kv:
+        raise ValueError("cu_kv must end at the number of key/value rows")
+    return cu_kv, int(total_kv), _ptr(cu_kv)
+
+
 def attn_fwd(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
-             seg_heads=None, interleaved: bool = False, cu_padded=None):
+             seg_heads=None, interleaved: bool = False, cu_padded=None, cu_kv=None):
     """Exact per-segment causal attention in fp64.  q/k/v: bf16 tensors or uint16 bit arrays
     [total, H, d] (k and v may have fewer heads Hkv dividing H: query head h reads key/value
     head h // (H // Hkv)).  Returns (o [total, H, d] f64, lse [H, total] f64, natural log).
     With ``seg_heads`` (a list of (segment, head) pairs) only those are computed; the rest
     stay 0.  With ``cu_padded`` the rows follow the padded layout of ``real_rows``: the real
     rows are gathered, attended as a contiguous pack, and scattered back; padding rows get
-    O = 0 and LSE = -inf (the log of an empty sum)."""
+    O = 0 and LSE = -inf (the log of an empty sum).  With ``cu_kv`` the keys and values
+    ([total_kv, Hkv, d]) have segments of their own, at least as long as the query segments;
+    queries are bottom-right aligned (query p of a segment with L queries and Lk keys sits at
+    position p + Lk - L and sees keys 0 .. p + Lk - L)."""
     if cu_padded is not None:
         idx = real_rows(cu, cu_padded)
         qb, kb, vb = (bf16_bits(x)[idx] for x in (q, k, v))
@@ -209,71 +225,81 @@ def attn_fwd(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: 
     total, H, d = qb.shape
     Hkv = kb.shape[1]
     cu = _c(cu, np.int32)
+    cu_kv, total_kv, kvp = _kv_args(cu, cu_kv, kb.shape[0])
     o = np.zeros((total, H, d), np.float64)
     lse = np.zeros((H, total), np.float64)
     if seg_heads is None:
-        _load().orc_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                             float(scale), float(theta), _mode(contract, interleaved), _ptr(o), _ptr(lse))
+        _load().orc_attn_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), kvp, len(cu) - 1, total, total_kv, H,
+                             Hkv, d, float(scale), float(theta), _mode(contract, interleaved), _ptr(o),
+                             _ptr(lse))
     else:
         sh = np.asarray(seg_heads, np.int32).reshape(-1, 2)
         segs, heads = np.ascontiguousarray(sh[:, 0]), np.ascontiguousarray(sh[:, 1])
-        _load().orc_attn_fwd_seg_heads(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H,
-                                       Hkv, d, float(scale), float(theta), _mode(contract, interleaved),
-                                       _ptr(segs), _ptr(heads), sh.shape[0], _ptr(o), _ptr(lse))
+        _load().orc_attn_fwd_seg_heads(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), kvp, len(cu) - 1, total,
+                                       total_kv, H, Hkv, d, float(scale), float(theta),
+                                       _mode(contract, interleaved), _ptr(segs), _ptr(heads), sh.shape[0],
+                                       _ptr(o), _ptr(lse))
     return o, lse
 
 
 def attn_fwd_rows(q, k, v, cu, rows, heads, scale: float = 0.0, theta: float = 10000.0,
-                  contract: bool = True, interleaved: bool = False):
+                  contract: bool = True, interleaved: bool = False, cu_kv=None):
     """Forward for selected (token row, head) pairs: returns (o [n, d], lse [n])."""
     qb, kb, vb = bf16_bits(q), bf16_bits(k), bf16_bits(v)
     total, H, d = qb.shape
     Hkv = kb.shape[1]
     cu = _c(cu, np.int32)
+    cu_kv, total_kv, kvp = _kv_args(cu, cu_kv, kb.shape[0])
     rows = _c(rows, np.int64)
     heads = _c(heads, np.int32)
     n = rows.shape[0]
     o = np.zeros((n, d), np.float64)
     lse = np.zeros(n, np.float64)
-    _load().orc_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                              float(scale), float(theta), _mode(contract, interleaved), _ptr(rows),
-                              _ptr(heads), n, _ptr(o), _ptr(lse))
+    _load().orc_attn_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), kvp, len(cu) - 1, total, total_kv,
+                              H, Hkv, d, float(scale), float(theta), _mode(contract, interleaved),
+                              _ptr(rows), _ptr(heads), n, _ptr(o), _ptr(lse))
     return o, lse
 
 
-def attn_fwd_f64(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, interleaved: bool = False):
+def attn_fwd_f64(q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, interleaved: bool = False,
+                 cu_kv=None):
     """Exact-mode forward on float64 inputs [total, H, d] (finite-difference tests)."""
     q, k, v = (_c(x, np.float64) for x in (q, k, v))
     total, H, d = q.shape
     Hkv = k.shape[1]
     cu = _c(cu, np.int32)
+    cu_kv, total_kv, kvp = _kv_args(cu, cu_kv, k.shape[0])
     o = np.zeros((total, H, d), np.float64)
     lse = np.zeros((H, total), np.float64)
-    _load().orc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                         float(scale), float(theta), _mode_f64(interleaved), _ptr(o), _ptr(lse))
+    _load().orc_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), kvp, len(cu) - 1, total, total_kv, H, Hkv,
+                         d, float(scale), float(theta), _mode_f64(interleaved), _ptr(o), _ptr(lse))
     return o, lse
 
 
-def attn_bwd_f64(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, interleaved: bool = False):
+def attn_bwd_f64(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, interleaved: bool = False,
+                 cu_kv=None):
     """Exact-mode gradients on float64 inputs (finite-difference tests)."""
     g, q, k, v = (_c(x, np.float64) for x in (dout, q, k, v))
     total, H, d = q.shape
     Hkv = k.shape[1]
     cu = _c(cu, np.int32)
+    cu_kv, total_kv, kvp = _kv_args(cu, cu_kv, k.shape[0])
     dq = np.zeros((total, H, d), np.float64)
-    dk = np.zeros((total, Hkv, d), np.float64)
+    dk = np.zeros(k.shape, np.float64)
     dv = np.zeros_like(dk)
-    _load().orc_attn_bwd(_ptr(g), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                         float(scale), float(theta), _mode_f64(interleaved), _ptr(dq), _ptr(dk), _ptr(dv))
+    _load().orc_attn_bwd(_ptr(g), _ptr(q), _ptr(k), _ptr(v), _ptr(cu), kvp, len(cu) - 1, total, total_kv,
+                         H, Hkv, d, float(scale), float(theta), _mode_f64(interleaved), _ptr(dq), _ptr(dk),
+                         _ptr(dv))
     return dq, dk, dv
 
 
 def attn_bwd(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, contract: bool = True,
-             seg_heads=None, interleaved: bool = False, cu_padded=None):
-    """Gradients (dq [total, H, d], dk and dv [total, Hkv, d]) f64 of sum(O * dO).  With
+             seg_heads=None, interleaved: bool = False, cu_padded=None, cu_kv=None):
+    """Gradients (dq [total, H, d], dk and dv shaped like k and v) f64 of sum(O * dO).  With
     ``seg_heads`` (a list of (segment, key/value head) pairs) only those are computed (dq for
     every query head of each pair's group); other entries stay 0.  With ``cu_padded`` the
-    padding rows (``real_rows``) take no part and their gradients are 0."""
+    padding rows (``real_rows``) take no part and their gradients are 0.  ``cu_kv`` as in
+    ``attn_fwd``."""
     if cu_padded is not None:
         idx = real_rows(cu, cu_padded)
         gb, qb, kb, vb = (bf16_bits(x)[idx] for x in (dout, q, k, v))
@@ -288,20 +314,23 @@ def attn_bwd(dout, q, k, v, cu, scale: float = 0.0, theta: float = 10000.0, cont
     total, H, d = qb.shape
     Hkv = kb.shape[1]
     cu = _c(cu, np.int32)
+    cu_kv, total_kv, kvp = _kv_args(cu, cu_kv, kb.shape[0])
     dq = np.zeros((total, H, d), np.float64)
-    dk = np.zeros((total, Hkv, d), np.float64)
+    dk = np.zeros(kb.shape, np.float64)
     dv = np.zeros_like(dk)
     lib = _load()
     if seg_heads is None:
-        lib.orc_attn_bwd(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1, total, H, Hkv, d,
-                         float(scale), float(theta), _mode(contract, interleaved), _ptr(dq), _ptr(dk), _ptr(dv))
+        lib.orc_attn_bwd(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), kvp, len(cu) - 1, total,
+                         total_kv, H, Hkv, d, float(scale), float(theta), _mode(contract, interleaved),
+                         _ptr(dq), _ptr(dk), _ptr(dv))
     else:
         sh = np.asarray(seg_heads, np.int32).reshape(-1, 2)
         segs = np.ascontiguousarray(sh[:, 0])
         heads = np.ascontiguousarray(sh[:, 1])
-        lib.orc_attn_bwd_seg_heads(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), len(cu) - 1,
-                                   total, H, Hkv, d, float(scale), float(theta), _mode(contract, interleaved),
-                                   _ptr(segs), _ptr(heads), sh.shape[0], _ptr(dq), _ptr(dk), _ptr(dv))
+        lib.orc_attn_bwd_seg_heads(_ptr(gb), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), kvp, len(cu) - 1,
+                                   total, total_kv, H, Hkv, d, float(scale), float(theta),
+                                   _mode(contract, interleaved), _ptr(segs), _ptr(heads), sh.shape[0],
+                                   _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
 
 

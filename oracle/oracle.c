@@ -267,10 +267,12 @@ void orc_rope_rows(const double* x, const int64_t* pos, int64_t n, int32_t d,
 /* ---------------------------------------------------------------- attention */
 
 typedef struct {
-    const void *q, *k, *v, *dout;       /* [total][H][d]: bf16 bits, or fp64 when f64_inputs */
+    const void *q, *k, *v, *dout;       /* q / dO [total][H][d], k / v [total_kv][Hkv][d]: bf16
+                                           bits, or fp64 when f64_inputs */
     int f64_inputs;
-    const int32_t* cu;
-    int32_t nseg, total, H, Hkv, d;      /* q / dO have H heads, k / v have Hkv (H % Hkv == 0) */
+    const int32_t* cu;                   /* query segments */
+    const int32_t* cu_kv;                /* key/value segments (the same array for self-attention) */
+    int32_t nseg, total, total_kv, H, Hkv, d;   /* H % Hkv == 0 */
     double scale, theta;                 /* theta == 0: no RoPE */
     int contract;
     int rope_interleaved;                /* pairing of the rotation (rope_pair) */
@@ -281,8 +283,6 @@ typedef struct {
  * multi-head attention). */
 static int32_t kv_head(const orc_problem* P, int32_t h) { return h / (P->H / P->Hkv); }
 
-/* q' (or k') for token row i of head h: widen, rotate by its local position,
- * and round to bf16 in contract mode. */
 /* Element c of token row i, head h of an input tensor, widened to fp64. */
 static double input_elem(const orc_problem* P, const void* x, int64_t i, int32_t h, int c) {
     const int32_t nh = (x == P->k || x == P->v) ? P->Hkv : P->H;
@@ -291,6 +291,8 @@ static double input_elem(const orc_problem* P, const void* x, int64_t i, int32_t
     return bf16_bits_to_double(((const uint16_t*)x)[off]);
 }
 
+/* q' (or k') for token row i of head h: widen, rotate by position p, and round
+ * to bf16 in contract mode. */
 static void load_rotated(const orc_problem* P, const void* x, int64_t i, int32_t h,
                          int64_t p, double* out) {
     int d = P->d;
@@ -310,27 +312,37 @@ static void load_plain(const orc_problem* P, const void* x, int64_t i, int32_t h
     for (int c = 0; c < P->d; ++c) out[c] = input_elem(P, x, i, h, c);
 }
 
-/* One segment r, one head h: Q', K', V (and dO) of the segment in fp64. */
+/* One segment r, one head h: Q', dO of its L queries and K', V of its Lk keys in
+ * fp64.  Self-attention has Lk == L.  With Lk > L the queries are the last L
+ * positions of the segment (bottom-right alignment, the convention for q and kv
+ * of different lengths that "Sequence packing and variable-length attention"
+ * says differs from the square case): query p sits at position p + off,
+ * off = Lk - L, sees keys j <= p + off, and is rotated by that position. */
 typedef struct {
-    int64_t L, base;
-    double *q, *k, *v, *g;  /* [L][d] each */
+    int64_t L, Lk, off, base, base_k;
+    double *q, *g;          /* [L][d] */
+    double *k, *v;          /* [Lk][d] */
 } seg_head;
 
 static void seg_head_load(const orc_problem* P, int32_t r, int32_t h, int want_grad, seg_head* S) {
     int d = P->d;
     S->base = P->cu[r];
     S->L = (int64_t)P->cu[r + 1] - P->cu[r];
-    size_t n = (size_t)S->L * d;
-    S->q = (double*)malloc(sizeof(double) * n);
-    S->k = (double*)malloc(sizeof(double) * n);
-    S->v = (double*)malloc(sizeof(double) * n);
-    S->g = want_grad ? (double*)malloc(sizeof(double) * n) : NULL;
+    S->base_k = P->cu_kv[r];
+    S->Lk = (int64_t)P->cu_kv[r + 1] - P->cu_kv[r];
+    S->off = S->Lk - S->L;
+    S->q = (double*)malloc(sizeof(double) * (size_t)S->L * d);
+    S->g = want_grad ? (double*)malloc(sizeof(double) * (size_t)S->L * d) : NULL;
+    S->k = (double*)malloc(sizeof(double) * (size_t)S->Lk * d);
+    S->v = (double*)malloc(sizeof(double) * (size_t)S->Lk * d);
     for (int64_t p = 0; p < S->L; ++p) {
         int64_t i = S->base + p;
-        load_rotated(P, P->q, i, h, p, S->q + p * d);
-        load_rotated(P, P->k, i, kv_head(P, h), p, S->k + p * d);
-        load_plain(P, P->v, i, kv_head(P, h), S->v + p * d);
+        load_rotated(P, P->q, i, h, p + S->off, S->q + p * d);
         if (want_grad) load_plain(P, P->dout, i, h, S->g + p * d);
+    }
+    for (int64_t j = 0; j < S->Lk; ++j) {
+        load_rotated(P, P->k, S->base_k + j, kv_head(P, h), j, S->k + j * d);
+        load_plain(P, P->v, S->base_k + j, kv_head(P, h), S->v + j * d);
     }
 }
 
@@ -345,24 +357,25 @@ static double dot(const double* a, const double* b, int d) {
 }
 
 /* Masked softmax row p of one segment-head: scores s_j = q'_p . k'_j * scale
- * for the allowed keys j <= p (the -inf entries of the additive mask
+ * for the allowed keys j <= p + off (the -inf entries of the additive mask
  * contribute exp(-inf) = 0 to the normaliser), LSE_p = ln sum_j exp(s_j). */
 static double softmax_row(const seg_head* S, int64_t p, int d, double scale, double* s) {
+    const int64_t last = p + S->off;
     double m = -INFINITY;
-    for (int64_t j = 0; j <= p; ++j) {
+    for (int64_t j = 0; j <= last; ++j) {
         s[j] = dot(S->q + p * d, S->k + j * d, d) * scale;
         if (s[j] > m) m = s[j];
     }
     double z = 0.0;
-    for (int64_t j = 0; j <= p; ++j) z += exp(s[j] - m);
+    for (int64_t j = 0; j <= last; ++j) z += exp(s[j] - m);
     return m + log(z);
 }
 
-/* Forward for one row: o[d] = sum_{j<=p} exp(s_j - LSE) v_j, returns LSE. */
+/* Forward for one row: o[d] = sum_{j<=p+off} exp(s_j - LSE) v_j, returns LSE. */
 static double fwd_row(const seg_head* S, int64_t p, int d, double scale, double* s, double* o) {
     double lse = softmax_row(S, p, d, scale, s);
     for (int c = 0; c < d; ++c) o[c] = 0.0;
-    for (int64_t j = 0; j <= p; ++j) {
+    for (int64_t j = 0; j <= p + S->off; ++j) {
         double w = exp(s[j] - lse);
         for (int c = 0; c < d; ++c) o[c] += w * S->v[j * d + c];
     }
@@ -370,11 +383,12 @@ static double fwd_row(const seg_head* S, int64_t p, int d, double scale, double*
 }
 
 static orc_problem make_problem(const void* q, const void* k, const void* v,
-                                const void* dout, const int32_t* cu, int32_t nseg,
-                                int32_t total, int32_t H, int32_t Hkv, int32_t d, double scale,
-                                double theta, int contract) {
+                                const void* dout, const int32_t* cu, const int32_t* cu_kv,
+                                int32_t nseg, int32_t total, int32_t total_kv, int32_t H,
+                                int32_t Hkv, int32_t d, double scale, double theta, int contract) {
     orc_problem P;
     P.q = q; P.k = k; P.v = v; P.dout = dout; P.cu = cu;
+    P.cu_kv = cu_kv != NULL ? cu_kv : cu;
     /* contract: 1 contract mode, 0 exact mode, -1 exact mode on fp64 inputs; adding 4 (or, for
      * fp64 inputs, passing -5) selects the interleaved RoPE pairing. */
     P.rope_interleaved = 0;
@@ -382,7 +396,8 @@ static orc_problem make_problem(const void* q, const void* k, const void* v,
     else if (contract < 0 && contract != -1) { P.rope_interleaved = 1; contract = -1; }
     P.f64_inputs = contract < 0;   /* contract == -1 selects fp64 inputs, exact mode */
     if (contract < 0) contract = 0;
-    P.nseg = nseg; P.total = total; P.H = H; P.Hkv = Hkv; P.d = d;
+    P.nseg = nseg; P.total = total; P.total_kv = cu_kv != NULL ? total_kv : total;
+    P.H = H; P.Hkv = Hkv; P.d = d;
     P.scale = scale > 0.0 ? scale : 1.0 / sqrt((double)d);
     P.theta = theta; P.contract = contract;
     return P;
@@ -390,11 +405,14 @@ static orc_problem make_problem(const void* q, const void* k, const void* v,
 
 static void fwd_seg_head(const orc_problem* P, int32_t r, int32_t h, double* o, double* lse);
 
-/* Full forward: o [total][H][d], lse [H][total] (natural log). */
+/* Full forward: o [total][H][d], lse [H][total] (natural log).  cu_kv == NULL is
+ * self-attention (keys and values segmented like the queries, total_kv ignored). */
 void orc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu,
-                  int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d, double scale,
-                  double theta, int contract, double* o, double* lse) {
-    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, Hkv, d, scale, theta, contract);
+                  const int32_t* cu_kv, int32_t nseg, int32_t total, int32_t total_kv, int32_t H,
+                  int32_t Hkv, int32_t d, double scale, double theta, int contract, double* o,
+                  double* lse) {
+    orc_problem P = make_problem(q, k, v, NULL, cu, cu_kv, nseg, total, total_kv, H, Hkv, d, scale,
+                                 theta, contract);
     int64_t nwork = (int64_t)nseg * H;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t w = 0; w < nwork; ++w) fwd_seg_head(&P, (int32_t)(w / H), (int32_t)(w % H), o, lse);
@@ -404,7 +422,7 @@ void orc_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu
 static void fwd_seg_head(const orc_problem* P, int32_t r, int32_t h, double* o, double* lse) {
     seg_head S;
     seg_head_load(P, r, h, 0, &S);
-    double* s = (double*)malloc(sizeof(double) * (size_t)S.L);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(S.Lk > 0 ? S.Lk : 1));
     for (int64_t p = 0; p < S.L; ++p) {
         int64_t i = S.base + p;
         lse[(size_t)h * P->total + i] = fwd_row(&S, p, P->d, P->scale, s, o + ((size_t)i * P->H + h) * P->d);
@@ -415,10 +433,12 @@ static void fwd_seg_head(const orc_problem* P, int32_t r, int32_t h, double* o, 
 
 /* Forward restricted to a set of (segment, head) pairs; other entries untouched. */
 void orc_attn_fwd_seg_heads(const void* q, const void* k, const void* v, const int32_t* cu,
-                            int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
-                            double scale, double theta, int contract, const int32_t* segs,
-                            const int32_t* heads, int64_t n, double* o, double* lse) {
-    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, Hkv, d, scale, theta, contract);
+                            const int32_t* cu_kv, int32_t nseg, int32_t total, int32_t total_kv,
+                            int32_t H, int32_t Hkv, int32_t d, double scale, double theta,
+                            int contract, const int32_t* segs, const int32_t* heads, int64_t n,
+                            double* o, double* lse) {
+    orc_problem P = make_problem(q, k, v, NULL, cu, cu_kv, nseg, total, total_kv, H, Hkv, d, scale,
+                                 theta, contract);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < n; ++t) fwd_seg_head(&P, segs[t], heads[t], o, lse);
 }
@@ -426,30 +446,34 @@ void orc_attn_fwd_seg_heads(const void* q, const void* k, const void* v, const i
 /* Sampled forward: the same result for selected (token, head) pairs only,
  * so that full-size problems can be checked row by row. */
 void orc_attn_fwd_rows(const void* q, const void* k, const void* v, const int32_t* cu,
-                       int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
-                       double scale, double theta, int contract, const int64_t* rows,
-                       const int32_t* heads, int64_t n, double* o, double* lse) {
-    orc_problem P = make_problem(q, k, v, NULL, cu, nseg, total, H, Hkv, d, scale, theta, contract);
+                       const int32_t* cu_kv, int32_t nseg, int32_t total, int32_t total_kv,
+                       int32_t H, int32_t Hkv, int32_t d, double scale, double theta, int contract,
+                       const int64_t* rows, const int32_t* heads, int64_t n, double* o, double* lse) {
+    orc_problem P = make_problem(q, k, v, NULL, cu, cu_kv, nseg, total, total_kv, H, Hkv, d, scale,
+                                 theta, contract);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < n; ++t) {
         int64_t i = rows[t];
         int32_t h = heads[t];
         int32_t r = segment_of(cu, nseg, i);
         int64_t p = i - cu[r];
-        /* only the prefix 0..p of the segment is needed */
+        /* only query p and the keys 0..p+off it sees are needed */
         seg_head S;
         S.base = cu[r];
+        S.base_k = P.cu_kv[r];
+        S.off = ((int64_t)P.cu_kv[r + 1] - P.cu_kv[r]) - ((int64_t)cu[r + 1] - cu[r]);
         S.L = p + 1;
+        S.Lk = p + S.off + 1;
         S.q = (double*)malloc(sizeof(double) * (size_t)(p + 1) * d);
-        S.k = (double*)malloc(sizeof(double) * (size_t)(p + 1) * d);
-        S.v = (double*)malloc(sizeof(double) * (size_t)(p + 1) * d);
+        S.k = (double*)malloc(sizeof(double) * (size_t)S.Lk * d);
+        S.v = (double*)malloc(sizeof(double) * (size_t)S.Lk * d);
         S.g = NULL;
-        load_rotated(&P, q, i, h, p, S.q + p * d);
-        for (int64_t j = 0; j <= p; ++j) {
-            load_rotated(&P, k, S.base + j, kv_head(&P, h), j, S.k + j * d);
-            load_plain(&P, v, S.base + j, kv_head(&P, h), S.v + j * d);
+        load_rotated(&P, q, i, h, p + S.off, S.q + p * d);
+        for (int64_t j = 0; j < S.Lk; ++j) {
+            load_rotated(&P, k, S.base_k + j, kv_head(&P, h), j, S.k + j * d);
+            load_plain(&P, v, S.base_k + j, kv_head(&P, h), S.v + j * d);
         }
-        double* s = (double*)malloc(sizeof(double) * (size_t)(p + 1));
+        double* s = (double*)malloc(sizeof(double) * (size_t)S.Lk);
         lse[t] = fwd_row(&S, p, d, P.scale, s, o + t * d);
         free(s);
         seg_head_free(&S);
@@ -460,20 +484,23 @@ void orc_attn_fwd_rows(const void* q, const void* k, const void* v, const int32_
  * derivatives), for every query head h of its group:
  *   P = exp(S - LSE) on allowed entries, dV = P^T dO, dP = dO V^T,
  *   D_p = sum_j P_pj dP_pj, dS = P o (dP - D), dQ' = scale dS K', dK' = scale dS^T Q',
- * then dQ = R(p)^T dQ', dK = R(p)^T dK'; the group's contributions to dK and dV
+ * then dQ = R(p + off)^T dQ', dK = R(j)^T dK'; the group's contributions to dK and dV
  * add up (each query head reads the shared K and V).  dq has H heads, dk/dv Hkv. */
 static void bwd_seg_kvhead(const orc_problem* P, int32_t r, int32_t hk, double* dq, double* dk,
                            double* dv) {
     int d = P->d;
     const int32_t group = P->H / P->Hkv;
     const int64_t L = (int64_t)P->cu[r + 1] - P->cu[r], base = P->cu[r];
-    double* gk = (double*)calloc((size_t)L * d, sizeof(double));
-    double* gv = (double*)calloc((size_t)L * d, sizeof(double));
+    const int64_t Lk = (int64_t)P->cu_kv[r + 1] - P->cu_kv[r], base_k = P->cu_kv[r];
+    const int64_t off = Lk - L;
+    const size_t nk = (size_t)(Lk > 0 ? Lk : 1);
+    double* gk = (double*)calloc(nk * d, sizeof(double));
+    double* gv = (double*)calloc(nk * d, sizeof(double));
     double* gq = (double*)malloc(sizeof(double) * (size_t)L * d);
     double* lse = (double*)malloc(sizeof(double) * (size_t)L);
-    double* s = (double*)malloc(sizeof(double) * (size_t)L);
-    double* pr = (double*)malloc(sizeof(double) * (size_t)L);
-    double* dp = (double*)malloc(sizeof(double) * (size_t)L);
+    double* s = (double*)malloc(sizeof(double) * nk);
+    double* pr = (double*)malloc(sizeof(double) * nk);
+    double* dp = (double*)malloc(sizeof(double) * nk);
     for (int32_t h = hk * group; h < (hk + 1) * group; ++h) {
         seg_head S;
         seg_head_load(P, r, h, 1, &S);
@@ -481,12 +508,12 @@ static void bwd_seg_kvhead(const orc_problem* P, int32_t r, int32_t hk, double* 
         memset(gq, 0, sizeof(double) * (size_t)L * d);
         for (int64_t p = 0; p < L; ++p) {
             double D = 0.0;
-            for (int64_t j = 0; j <= p; ++j) {
+            for (int64_t j = 0; j <= p + off; ++j) {
                 pr[j] = exp(dot(S.q + p * d, S.k + j * d, d) * P->scale - lse[p]);
                 dp[j] = dot(S.g + p * d, S.v + j * d, d);
                 D += pr[j] * dp[j];
             }
-            for (int64_t j = 0; j <= p; ++j) {
+            for (int64_t j = 0; j <= p + off; ++j) {
                 double ds = pr[j] * (dp[j] - D);
                 for (int c = 0; c < d; ++c) {
                     gv[j * d + c] += pr[j] * S.g[p * d + c];
@@ -496,25 +523,27 @@ static void bwd_seg_kvhead(const orc_problem* P, int32_t r, int32_t hk, double* 
             }
         }
         for (int64_t p = 0; p < L; ++p) {
-            size_t off = ((size_t)(base + p) * P->H + h) * d;
-            if (P->theta != 0.0) rope_rotate_transpose(gq + p * d, dq + off, p, d, P->theta, P->rope_interleaved);
-            else memcpy(dq + off, gq + p * d, sizeof(double) * (size_t)d);
+            size_t o2 = ((size_t)(base + p) * P->H + h) * d;
+            if (P->theta != 0.0) rope_rotate_transpose(gq + p * d, dq + o2, p + off, d, P->theta, P->rope_interleaved);
+            else memcpy(dq + o2, gq + p * d, sizeof(double) * (size_t)d);
         }
         seg_head_free(&S);
     }
-    for (int64_t p = 0; p < L; ++p) {
-        size_t off = ((size_t)(base + p) * P->Hkv + hk) * d;
-        if (P->theta != 0.0) rope_rotate_transpose(gk + p * d, dk + off, p, d, P->theta, P->rope_interleaved);
-        else memcpy(dk + off, gk + p * d, sizeof(double) * (size_t)d);
-        memcpy(dv + off, gv + p * d, sizeof(double) * (size_t)d);
+    for (int64_t j = 0; j < Lk; ++j) {
+        size_t o2 = ((size_t)(base_k + j) * P->Hkv + hk) * d;
+        if (P->theta != 0.0) rope_rotate_transpose(gk + j * d, dk + o2, j, d, P->theta, P->rope_interleaved);
+        else memcpy(dk + o2, gk + j * d, sizeof(double) * (size_t)d);
+        memcpy(dv + o2, gv + j * d, sizeof(double) * (size_t)d);
     }
     free(lse); free(s); free(gq); free(gk); free(gv); free(pr); free(dp);
 }
 
 void orc_attn_bwd(const void* dout, const void* q, const void* k, const void* v,
-                  const int32_t* cu, int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
-                  double scale, double theta, int contract, double* dq, double* dk, double* dv) {
-    orc_problem P = make_problem(q, k, v, dout, cu, nseg, total, H, Hkv, d, scale, theta, contract);
+                  const int32_t* cu, const int32_t* cu_kv, int32_t nseg, int32_t total,
+                  int32_t total_kv, int32_t H, int32_t Hkv, int32_t d, double scale, double theta,
+                  int contract, double* dq, double* dk, double* dv) {
+    orc_problem P = make_problem(q, k, v, dout, cu, cu_kv, nseg, total, total_kv, H, Hkv, d, scale,
+                                 theta, contract);
     int64_t nwork = (int64_t)nseg * Hkv;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t w = 0; w < nwork; ++w)
@@ -525,11 +554,12 @@ void orc_attn_bwd(const void* dout, const void* q, const void* k, const void* v,
  * query head of each pair's group and dk/dv of the pair; the other rows are left
  * untouched.  Used for sampled checks at full size. */
 void orc_attn_bwd_seg_heads(const void* dout, const void* q, const void* k,
-                            const void* v, const int32_t* cu, int32_t nseg, int32_t total,
-                            int32_t H, int32_t Hkv, int32_t d, double scale, double theta,
-                            int contract, const int32_t* segs, const int32_t* heads, int64_t n,
-                            double* dq, double* dk, double* dv) {
-    orc_problem P = make_problem(q, k, v, dout, cu, nseg, total, H, Hkv, d, scale, theta, contract);
+                            const void* v, const int32_t* cu, const int32_t* cu_kv, int32_t nseg,
+                            int32_t total, int32_t total_kv, int32_t H, int32_t Hkv, int32_t d,
+                            double scale, double theta, int contract, const int32_t* segs,
+                            const int32_t* heads, int64_t n, double* dq, double* dk, double* dv) {
+    orc_problem P = make_problem(q, k, v, dout, cu, cu_kv, nseg, total, total_kv, H, Hkv, d, scale,
+                                 theta, contract);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < n; ++t) bwd_seg_kvhead(&P, segs[t], heads[t], dq, dk, dv);
 }

@@ -19,10 +19,13 @@ MUTATIONS = {
     "rope_sign": ("out[ib] = b * c + a * s;", "out[ib] = b * c - a * s;"),
     "rope_frequency": ("return (double)p * pow(theta, -2.0 * (double)j / (double)d);",
                        "return (double)p * pow(theta, -1.0 * (double)j / (double)d);"),
-    "position_not_reset": ("load_rotated(P, P->q, i, h, p, S->q + p * d);",
-                           "load_rotated(P, P->q, i, h, i, S->q + p * d);"),
-    "mask_off_by_one": ("for (int64_t j = 0; j <= p; ++j) z += exp(s[j] - m);",
-                        "for (int64_t j = 0; j < p; ++j) z += exp(s[j] - m); z += (p == 0);"),
+    "position_not_reset": ("load_rotated(P, P->q, i, h, p + S->off, S->q + p * d);",
+                           "load_rotated(P, P->q, i, h, i + S->off, S->q + p * d);"),
+    "qkv_query_position_unshifted": ("load_rotated(P, P->q, i, h, p + S->off, S->q + p * d);",
+                                     "load_rotated(P, P->q, i, h, p, S->q + p * d);"),
+    "qkv_top_left_alignment": ("const int64_t last = p + S->off;", "const int64_t last = p;"),
+    "mask_off_by_one": ("for (int64_t j = 0; j <= last; ++j) z += exp(s[j] - m);",
+                        "for (int64_t j = 0; j < last; ++j) z += exp(s[j] - m); z += (last == 0);"),
     "bwd_dropped_D": ("double ds = pr[j] * (dp[j] - D);", "double ds = pr[j] * dp[j];"),
     "bwd_dk_wrong_operand": ("gk[j * d + c] += P->scale * ds * S.q[p * d + c];",
                              "gk[j * d + c] += P->scale * ds * S.k[p * d + c];"),

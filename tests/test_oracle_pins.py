@@ -674,3 +674,89 @@ def test_padded_equals_unpadded_when_slots_are_tight():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
     with pytest.raises(ValueError):
         oracle.real_rows(cu, np.array([0, 4, 5, 14, 18]))   # first slot shorter than its segment
+
+
+# ------------------------------------------------------------------ q and kv of different lengths
+def _qkv_case():
+    lq = [3, 1, 6, 4]
+    lk = [7, 1, 6, 9]         # Lk >= Lq; one square segment, one single-token decode step
+    cu = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cuk = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    return lq, lk, cu, cuk
+
+
+def test_qkv_bottom_right_against_torch_autograd():
+    # a mask written on the (query, key) rows directly: query p of segment r sees key j of the
+    # same segment iff j <= p + (Lk - Lq); queries rotate at position p + Lk - Lq, keys at j
+    lq, lk, cu, cuk = _qkv_case()
+    Tq, Tk, H, Hkv, d = int(cu[-1]), int(cuk[-1]), 4, 2, 16
+    g0 = torch.Generator().manual_seed(12)
+    q, g = (torch.randn((Tq, H, d), generator=g0).bfloat16() for _ in range(2))
+    k, v = (torch.randn((Tk, Hkv, d), generator=g0).bfloat16() for _ in range(2))
+    sq, sk = np.repeat(np.arange(len(lq)), lq), np.repeat(np.arange(len(lk)), lk)
+    off = (np.asarray(lk) - np.asarray(lq))[sq]
+    pq = np.arange(Tq) - cu[sq] + off
+    pk = np.arange(Tk) - cuk[sk]
+    allow = (sq[:, None] == sk[None, :]) & (pk[None, :] <= pq[:, None])
+    qt, kt, vt = (torch.from_numpy(_f64(x)).requires_grad_() for x in (q, k, v))
+    rq = _rope_torch(qt, torch.from_numpy(pq).double(), d)
+    rk = _rope_torch(kt, torch.from_numpy(pk).double(), d)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        rq.permute(1, 0, 2), rk.permute(1, 0, 2), vt.permute(1, 0, 2), attn_mask=torch.from_numpy(allow),
+        enable_gqa=True).permute(1, 0, 2)
+    (o * torch.from_numpy(_f64(g))).sum().backward()
+    o_orc, lse_orc = oracle.attn_fwd(q, k, v, cu, contract=False, cu_kv=cuk)
+    assert np.max(np.abs(o_orc - o.detach().numpy())) < 1e-12
+    s = torch.einsum("ihd,jhd->hij", rq.detach(), rk.detach().repeat_interleave(H // Hkv, 1)) / np.sqrt(d)
+    lse_t = torch.logsumexp(s.masked_fill(~torch.from_numpy(allow)[None], float("-inf")), -1).numpy()
+    assert np.max(np.abs(lse_orc - lse_t)) < 1e-12
+    dq, dk, dv = oracle.attn_bwd(g, q, k, v, cu, contract=False, cu_kv=cuk)
+    assert dk.shape == (Tk, Hkv, d)
+    assert np.max(np.abs(dq - qt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dk - kt.grad.numpy())) < 1e-11
+    assert np.max(np.abs(dv - vt.grad.numpy())) < 1e-11
+
+
+def test_qkv_single_query_with_zero_q_averages_all_values():
+    # Lq = 1: the one query sees every key; with q = 0 all scores are 0, so O is the mean of V
+    lk = [5, 8]
+    cu = np.array([0, 1, 2], np.int32)
+    cuk = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((13, 2, 8))
+    o, lse = oracle.attn_fwd_f64(np.zeros((2, 2, 8)), rng.standard_normal((13, 2, 8)), v, cu, cu_kv=cuk)
+    assert np.allclose(o[0], v[:5].mean(0), atol=1e-14) and np.allclose(o[1], v[5:].mean(0), atol=1e-14)
+    assert np.allclose(lse[:, 0], np.log(5)) and np.allclose(lse[:, 1], np.log(8))
+
+
+def test_qkv_queries_equal_the_tail_of_a_self_attention():
+    # the last Lq rows of a self-attention over the Lk-token segment, asked as Lq queries
+    # against all Lk keys, give the same outputs and gradients (dk, dv: their share)
+    lk, lq = [9, 4], [3, 4]
+    cuk = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    rng = np.random.default_rng(21)
+    qf, k, v, gf = (rng.standard_normal((13, 2, 8)) for _ in range(4))
+    tail = np.concatenate([np.arange(a - n, a) for a, n in zip(cuk[1:], lq)])
+    gz = np.zeros_like(gf)
+    gz[tail] = gf[tail]
+    o_self, lse_self = oracle.attn_fwd_f64(qf, k, v, cuk)
+    o, lse = oracle.attn_fwd_f64(qf[tail], k, v, cu, cu_kv=cuk)
+    assert np.allclose(o, o_self[tail], atol=1e-13) and np.allclose(lse, lse_self[:, tail], atol=1e-13)
+    dq_s, dk_s, dv_s = oracle.attn_bwd_f64(gz, qf, k, v, cuk)
+    dq, dk, dv = oracle.attn_bwd_f64(gf[tail], qf[tail], k, v, cu, cu_kv=cuk)
+    assert np.allclose(dq, dq_s[tail], atol=1e-12)
+    assert np.allclose(dk, dk_s, atol=1e-12) and np.allclose(dv, dv_s, atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.attn_fwd_f64(qf, k, v, cuk, cu_kv=cu)     # more queries than keys
+
+
+def test_qkv_rows_sampler_matches_the_full_forward():
+    lq, lk, cu, cuk = _qkv_case()
+    rng = np.random.default_rng(2)
+    q = torch.from_numpy(rng.standard_normal((int(cu[-1]), 2, 16))).bfloat16()
+    k, v = (torch.from_numpy(rng.standard_normal((int(cuk[-1]), 2, 16))).bfloat16() for _ in range(2))
+    o, lse = oracle.attn_fwd(q, k, v, cu, cu_kv=cuk)
+    rows, heads = np.arange(int(cu[-1])), np.arange(int(cu[-1])) % 2
+    o_r, lse_r = oracle.attn_fwd_rows(q, k, v, cu, rows, heads, cu_kv=cuk)
+    assert np.array_equal(o_r, o[rows, heads]) and np.array_equal(lse_r, lse[heads, rows])
