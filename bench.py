@@ -429,6 +429,7 @@ def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
                                     "GB/s": ce_bytes / (ms_ce * 1e-3) / 1e9,
                                     "frac_hbm": ce_bytes / (ms_ce * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     del logits, ws_ce
+    out["varlen_variants"] = variant_measurements(vlc, w, dev, peaks, step)
     if w.name == "long":
         cu1 = torch.tensor([0, w.total], dtype=torch.int32, device=dev)
         o1 = torch.empty_like(q)
@@ -450,6 +451,56 @@ def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
         }
         del o1, lse1, ws1
     return out
+
+
+def variant_measurements(vlc, w, dev, peaks, step):
+    """Forward and backward of the varlen variants on this workload's pack, same effective FLOPs
+    (4 d H pairs forward, 10 d H pairs backward over the real segments' legal pairs): the
+    interleaved RoPE pairing, grouped key/value heads (H / 4 of them), and a padded layout with
+    every segment's slot rounded up to a multiple of 64 rows."""
+    pairs = synth.causal_pairs(w.real_lengths)
+    f_fl, b_fl = 4.0 * w.d * w.H * pairs, 10.0 * w.d * w.H * pairs
+    mx = w.max_seqlen
+
+    def run(name, q, k, v, g, cu, **kw):
+        o = torch.empty_like(q)
+        lse = torch.empty((w.H, q.shape[0]), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsf = vlc.new_workspace(w.nseg, q.shape[0], w.H, w.d, mx, False, dev, k.shape[1])
+        wsb = vlc.new_workspace(w.nseg, q.shape[0], w.H, w.d, mx, True, dev, k.shape[1])
+        fwd = lambda: vlc.varlen_attn_fwd(q, k, v, cu, mx, out=o, lse=lse, workspace=wsf, check=False, **kw)
+        fwd()
+        vlc.get_error(wsf)
+        bwd = lambda: vlc.varlen_attn_bwd(g, q, k, v, o, lse, cu, mx, dq=dq, dk=dk, dv=dv, workspace=wsb,
+                                          check=False, **kw)
+        ms_f, ms_b = _time_ms(fwd, 5), _time_ms(bwd, 5)
+        for ws in (wsf, wsb):
+            st, bits = vlc.get_error(ws)
+            if st != 0:
+                raise RuntimeError(f"{name}: device error status {st} bits 0x{bits:x}")
+        return {"fwd_ms": ms_f, "bwd_ms": ms_b, "fwd_eff_TFLOP/s": f_fl / (ms_f * 1e-3) / 1e12,
+                "bwd_eff_TFLOP/s": b_fl / (ms_b * 1e-3) / 1e12}
+
+    res = {"interleaved_rope": run("interleaved", step.q, step.k, step.v, step.g, step.cu, rope_interleaved=True)}
+    hk = max(1, w.H // 4)
+    k4, v4 = step.k[:, :hk].contiguous(), step.v[:, :hk].contiguous()
+    res[f"gqa_{w.H}q_{hk}kv"] = run("gqa", step.q, k4, v4, step.g, step.cu)
+    del k4, v4
+    lens = np.diff(w.cu).astype(np.int64)
+    slots = lens + (-lens) % 64
+    cp = np.concatenate([[0], np.cumsum(slots)])
+    idx = torch.from_numpy(np.concatenate([np.arange(a, a + n) for a, n in zip(cp[:-1], lens)])).to(dev)
+    padded = []
+    for x in (step.q, step.k, step.v, step.g):
+        y = torch.zeros((int(cp[-1]),) + tuple(x.shape[1:]), dtype=x.dtype, device=dev)
+        y[idx] = x
+        padded.append(y)
+    cpt = torch.from_numpy(cp.astype(np.int32)).to(dev)
+    r = run("padded", *padded, step.cu, cu_seqlens_padded=cpt)
+    r["padding_rows"] = int(cp[-1] - w.total)
+    res["padded_slots_x64"] = r
+    del padded
+    return res
 
 
 def e2e_measure(vlc, w, step, steps, world, dev):

@@ -68,6 +68,7 @@ typedef enum {
 #define VLC_DEVERR_LABEL 0x10      /* a label outside [0, vocab) and not -100 */
 #define VLC_DEVERR_CU_PADDED 0x20  /* cu_padded[0] != 0, a slot shorter than its segment,
                                       or cu_padded[nseg] != total */
+#define VLC_DEVERR_QKV 0x40        /* a segment with fewer keys than queries (cu_kv) */
 #define VLC_DEVERR_TIMEOUT 0x100   /* a bounded mbarrier wait expired */
 
 /* Limits checked on the host. */
@@ -212,6 +213,38 @@ int vlc_attn_bwd_ex(const void* dout, const void* q, const void* k, const void* 
                     int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
                     float softmax_scale, float rope_theta, uint32_t flags, void* dq, void* dk,
                     void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* Queries and keys/values with segments of their own (cu_seqlens_q != cu_seqlens_kv),
+ * the non-square case that "Sequence packing and variable-length attention"
+ * (charlestar, section "The varlen interface makes each logical segment the
+ * compute range") says follows a convention of its own rather than the square
+ * lower-triangle rule.  The convention taken is
+ * bottom-right alignment (the one FlashAttention's varlen interface uses since
+ * 2.1): segment r has L_r = cu_q[r+1] - cu_q[r] queries and Lk_r = cu_kv[r+1] -
+ * cu_kv[r] >= L_r keys; its queries are the last L_r positions, so query p sits
+ * at position p + Lk_r - L_r, attends keys j <= p + Lk_r - L_r of its own
+ * segment, and RoPE rotates it by that position (keys by j).  L_r == Lk_r is the
+ * self-attention of vlc_attn_fwd_ex.
+ *   q, dout, o, dq  bf16 [total_q, H, d];  k, v, dk, dv  bf16 [total_kv, H_kv, d]
+ *   lse             fp32 [H, total_q]
+ *   cu_q, cu_kv     device int32 [nseg+1] each; both start at 0 and increase,
+ *                   cu_q[nseg] == total_q, cu_kv[nseg] == total_kv, every
+ *                   Lk_r >= L_r (else VLC_DEVERR_QKV), max_seqlen_q / _kv the
+ *                   largest L_r / Lk_r (checked on the device like cu_seqlens)
+ *   flags           as in vlc_attn_fwd_ex
+ * Workspace: vlc_workspace_bytes_qkv.  No padded layout on this path. */
+size_t vlc_workspace_bytes_qkv(int32_t nseg, int32_t total_q, int32_t total_kv, int32_t H, int32_t H_kv,
+                               int32_t d, int32_t max_seqlen_q, int32_t max_seqlen_kv, int is_bwd);
+int vlc_attn_fwd_qkv(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                     const int32_t* cu_kv, int32_t nseg, int32_t total_q, int32_t total_kv, int32_t H,
+                     int32_t H_kv, int32_t d, int32_t max_seqlen_q, int32_t max_seqlen_kv,
+                     float softmax_scale, float rope_theta, uint32_t flags, void* o, float* lse, void* ws,
+                     size_t ws_bytes, void* stream);
+int vlc_attn_bwd_qkv(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const int32_t* cu_q, const int32_t* cu_kv, int32_t nseg,
+                     int32_t total_q, int32_t total_kv, int32_t H, int32_t H_kv, int32_t d,
+                     int32_t max_seqlen_q, int32_t max_seqlen_kv, float softmax_scale, float rope_theta,
+                     uint32_t flags, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
 /* Forward attention for callers that cannot allocate device memory.  No
  * counterpart on the pages: it exists for callers that may not obtain memory

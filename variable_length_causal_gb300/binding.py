@@ -22,7 +22,7 @@ VLC_OK, VLC_ERR_ARG, VLC_ERR_CU_SEQLENS, VLC_ERR_UNSUPPORTED = 0, 1, 2, 3
 VLC_ERR_WORKSPACE, VLC_ERR_CUDA, VLC_ERR_TIMEOUT, VLC_ERR_LABEL = 4, 5, 6, 7
 DEVERR_CU_FIRST, DEVERR_CU_ORDER, DEVERR_CU_TOTAL, DEVERR_MAXLEN = 0x1, 0x2, 0x4, 0x8
 DEVERR_TIMEOUT = 0x100
-DEVERR_LABEL, DEVERR_CU_PADDED = 0x10, 0x20
+DEVERR_LABEL, DEVERR_CU_PADDED, DEVERR_QKV = 0x10, 0x20, 0x40
 WORKLIST_FWD, WORKLIST_BWD = 0, 1
 ROPE_INTERLEAVED = 0x1
 
@@ -31,7 +31,7 @@ EXPORTED = [
     "vlc_build_positions_labels", "vlc_build_worklist", "vlc_attn_fwd", "vlc_attn_bwd",
     "vlc_get_error", "vlc_attn_fwd_noalloc", "vlc_ce_workspace_bytes", "vlc_shifted_ce",
     "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa", "vlc_attn_fwd_ex",
-    "vlc_attn_bwd_ex",
+    "vlc_attn_bwd_ex", "vlc_workspace_bytes_qkv", "vlc_attn_fwd_qkv", "vlc_attn_bwd_qkv",
 ]
 
 _lock = threading.Lock()
@@ -99,6 +99,14 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_attn_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32,
                                         u32, P, P, P, P, sz, P]
         lib.vlc_attn_bwd_ex.restype = cint
+        lib.vlc_workspace_bytes_qkv.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, cint]
+        lib.vlc_workspace_bytes_qkv.restype = sz
+        lib.vlc_attn_fwd_qkv.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, f32,
+                                         u32, P, P, P, sz, P]
+        lib.vlc_attn_fwd_qkv.restype = cint
+        lib.vlc_attn_bwd_qkv.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                         f32, f32, u32, P, P, P, P, sz, P]
+        lib.vlc_attn_bwd_qkv.restype = cint
         _lib = lib
         return lib
 
@@ -133,15 +141,21 @@ def _cu_info(cu_seqlens: torch.Tensor, cu_padded: Optional[torch.Tensor] = None)
 
 
 def workspace_bytes(nseg: int, total: int, H: int, d: int, max_seqlen: int, backward: bool,
-                    H_kv: Optional[int] = None) -> int:
+                    H_kv: Optional[int] = None, total_kv: Optional[int] = None,
+                    max_seqlen_kv: Optional[int] = None) -> int:
     """Workspace bytes for the forward (backward=False) or backward call; H_kv key/value heads
-    (default H)."""
-    return int(load_library().vlc_workspace_bytes_gqa(nseg, total, H, H if H_kv is None else H_kv, d,
-                                                      max_seqlen, int(backward)))
+    (default H).  total_kv / max_seqlen_kv: key/value segments of their own (q != kv)."""
+    lib = load_library()
+    hk = H if H_kv is None else H_kv
+    if total_kv is None:
+        return int(lib.vlc_workspace_bytes_gqa(nseg, total, H, hk, d, max_seqlen, int(backward)))
+    return int(lib.vlc_workspace_bytes_qkv(nseg, total, total_kv, H, hk, d, max_seqlen, max_seqlen_kv,
+                                           int(backward)))
 
 
-def new_workspace(nseg, total, H, d, max_seqlen, backward, device, H_kv=None) -> torch.Tensor:
-    n = workspace_bytes(nseg, total, H, d, max_seqlen, backward, H_kv)
+def new_workspace(nseg, total, H, d, max_seqlen, backward, device, H_kv=None, total_kv=None,
+                  max_seqlen_kv=None) -> torch.Tensor:
+    n = workspace_bytes(nseg, total, H, d, max_seqlen, backward, H_kv, total_kv, max_seqlen_kv)
     if n == 0:
         raise VlcError(VLC_ERR_UNSUPPORTED, "workspace_bytes")
     return torch.empty(n, dtype=torch.uint8, device=device)
@@ -214,9 +228,9 @@ def _scale(softmax_scale, d):
     return float(softmax_scale) if softmax_scale else 1.0 / math.sqrt(d)
 
 
-def _check_qkv(qs, kvs):
+def _check_qkv(qs, kvs, separate_kv: bool = False):
     """qs: tensors shaped like q [total, H, d]; kvs: shaped like k [total, H_kv, d] with
-    H_kv dividing H.  Returns H_kv."""
+    H_kv dividing H (with separate_kv, k has its own row count).  Returns H_kv."""
     ref = qs[0]
     for t in list(qs) + list(kvs):
         if t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
@@ -230,7 +244,8 @@ def _check_qkv(qs, kvs):
     for t in kvs:
         if t.shape != kref.shape:
             raise ValueError("k and v must share one shape [total, H_kv, d]")
-    if kref.shape[0] != ref.shape[0] or kref.shape[2] != ref.shape[2] or ref.shape[1] % kref.shape[1]:
+    if ((kref.shape[0] != ref.shape[0] and not separate_kv) or kref.shape[2] != ref.shape[2]
+            or ref.shape[1] % kref.shape[1]):
         raise ValueError("k/v must be [total, H_kv, d] with H_kv dividing q's H")
     return kref.shape[1]
 
@@ -240,25 +255,47 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     rope_theta: float = 10000.0, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     check: bool = True, rope_interleaved: bool = False,
-                    cu_seqlens_padded: Optional[torch.Tensor] = None):
+                    cu_seqlens_padded: Optional[torch.Tensor] = None,
+                    cu_seqlens_kv: Optional[torch.Tensor] = None, max_seqlen_kv: Optional[int] = None):
     """Segment-local causal attention with per-segment RoPE reset.  Returns (O, LSE[H, total]).
     k and v may have fewer heads than q (grouped: query head h reads head h // (H // H_kv)).
     rope_interleaved rotates the pairs (x[2j], x[2j+1]) instead of (x[j], x[j + d/2]).
     cu_seqlens_padded gives each segment a slot of rows starting at cu_seqlens_padded[r]
-    (padding between segments; padding rows get O = 0, LSE = -inf)."""
+    (padding between segments; padding rows get O = 0, LSE = -inf).
+    cu_seqlens_kv / max_seqlen_kv give k and v segments of their own, at least as long as the
+    query segments; queries are bottom-right aligned (query p of a segment with L queries and
+    Lk keys sits at position p + Lk - L and sees keys up to there)."""
     lib = load_library()
-    _require_cuda(q, k, v, cu_seqlens, cu_seqlens_padded)
-    H_kv = _check_qkv([q] + ([] if out is None else [out]), [k, v])
+    _require_cuda(q, k, v, cu_seqlens, cu_seqlens_padded, cu_seqlens_kv)
+    qkv = cu_seqlens_kv is not None
+    if qkv and (cu_seqlens_padded is not None or max_seqlen_kv is None):
+        raise ValueError("cu_seqlens_kv needs max_seqlen_kv and takes no padded layout")
+    H_kv = _check_qkv([q] + ([] if out is None else [out]), [k, v], qkv)
     total, H, d = q.shape
     nseg = _cu_info(cu_seqlens, cu_seqlens_padded)
+    if qkv:
+        _cu_info(cu_seqlens_kv)
+        if cu_seqlens_kv.numel() != nseg + 1:
+            raise ValueError("cu_seqlens_kv must have one entry per segment boundary, like cu_seqlens")
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
-    ws = new_workspace(nseg, total, H, d, max_seqlen, False, q.device, H_kv) if workspace is None else workspace
-    st = lib.vlc_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
-                             nseg, total, H, H_kv, d,
-                             int(max_seqlen), _scale(softmax_scale, d), float(rope_theta),
-                             ROPE_INTERLEAVED if rope_interleaved else 0, _ptr(out), _ptr(lse), _ptr(ws),
-                             ws.numel(), _stream(q.device))
+    total_kv = k.shape[0]
+    if workspace is None:
+        ws = new_workspace(nseg, total, H, d, max_seqlen, False, q.device, H_kv,
+                           total_kv if qkv else None, max_seqlen_kv if qkv else None)
+    else:
+        ws = workspace
+    flags = ROPE_INTERLEAVED if rope_interleaved else 0
+    if qkv:
+        st = lib.vlc_attn_fwd_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cu_seqlens_kv), nseg,
+                                  total, total_kv, H, H_kv, d, int(max_seqlen), int(max_seqlen_kv),
+                                  _scale(softmax_scale, d), float(rope_theta), flags, _ptr(out), _ptr(lse),
+                                  _ptr(ws), ws.numel(), _stream(q.device))
+    else:
+        st = lib.vlc_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
+                                 nseg, total, H, H_kv, d, int(max_seqlen), _scale(softmax_scale, d),
+                                 float(rope_theta), flags, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                 _stream(q.device))
     _check(st, "vlc_attn_fwd")
     if check:
         _raise_device_error(ws, "vlc_attn_fwd")
@@ -271,26 +308,44 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                     dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
                     dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     check: bool = True, rope_interleaved: bool = False,
-                    cu_seqlens_padded: Optional[torch.Tensor] = None):
+                    cu_seqlens_padded: Optional[torch.Tensor] = None,
+                    cu_seqlens_kv: Optional[torch.Tensor] = None, max_seqlen_kv: Optional[int] = None):
     """Gradients (dQ, dK, dV) of sum(O * dO) for the forward above (dK, dV shaped like k, v;
     zero at padding rows)."""
     lib = load_library()
-    _require_cuda(dout, q, k, v, o, lse, cu_seqlens, cu_seqlens_padded)
-    H_kv = _check_qkv([q, dout, o], [k, v])
+    _require_cuda(dout, q, k, v, o, lse, cu_seqlens, cu_seqlens_padded, cu_seqlens_kv)
+    qkv = cu_seqlens_kv is not None
+    if qkv and (cu_seqlens_padded is not None or max_seqlen_kv is None):
+        raise ValueError("cu_seqlens_kv needs max_seqlen_kv and takes no padded layout")
+    H_kv = _check_qkv([q, dout, o], [k, v], qkv)
     total, H, d = q.shape
     nseg = _cu_info(cu_seqlens, cu_seqlens_padded)
+    if qkv:
+        _cu_info(cu_seqlens_kv)
+        if cu_seqlens_kv.numel() != nseg + 1:
+            raise ValueError("cu_seqlens_kv must have one entry per segment boundary, like cu_seqlens")
     if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous fp32 [H, total]")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws = new_workspace(nseg, total, H, d, max_seqlen, True, q.device, H_kv) if workspace is None else workspace
-    st = lib.vlc_attn_bwd_ex(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                             _ptr(cu_seqlens), _ptr(cu_seqlens_padded), nseg, total, H, H_kv, d,
-                             int(max_seqlen),
-                             _scale(softmax_scale, d), float(rope_theta),
-                             ROPE_INTERLEAVED if rope_interleaved else 0, _ptr(dq), _ptr(dk), _ptr(dv),
-                             _ptr(ws), ws.numel(), _stream(q.device))
+    total_kv = k.shape[0]
+    if workspace is None:
+        ws = new_workspace(nseg, total, H, d, max_seqlen, True, q.device, H_kv,
+                           total_kv if qkv else None, max_seqlen_kv if qkv else None)
+    else:
+        ws = workspace
+    flags = ROPE_INTERLEAVED if rope_interleaved else 0
+    if qkv:
+        st = lib.vlc_attn_bwd_qkv(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
+                                  _ptr(cu_seqlens_kv), nseg, total, total_kv, H, H_kv, d, int(max_seqlen),
+                                  int(max_seqlen_kv), _scale(softmax_scale, d), float(rope_theta), flags,
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(q.device))
+    else:
+        st = lib.vlc_attn_bwd_ex(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                 _ptr(cu_seqlens), _ptr(cu_seqlens_padded), nseg, total, H, H_kv, d,
+                                 int(max_seqlen), _scale(softmax_scale, d), float(rope_theta), flags,
+                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(q.device))
     _check(st, "vlc_attn_bwd")
     if check:
         _raise_device_error(ws, "vlc_attn_bwd")

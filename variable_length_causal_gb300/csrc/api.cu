@@ -20,11 +20,20 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 static int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
-                   int32_t max_seqlen, int is_bwd) {
+                   int32_t max_seqlen, int is_bwd, int32_t total_kv, int32_t max_seqlen_kv) {
     WsLayout L{};
+    const bool qkv = total_kv >= 0;
+    if (!qkv) {
+        total_kv = total;
+        max_seqlen_kv = max_seqlen;
+    }
     const int min_tile = is_bwd ? (kBwdBM < kFwdBM ? kBwdBM : kFwdBM) : kFwdBM;
-    L.item_cap = static_cast<int64_t>(nseg) + static_cast<int64_t>(total) / min_tile + 1;
-    L.table_rows = static_cast<int32_t>(ceil_div64(max_seqlen, kTablePad) * kTablePad);
+    const int32_t rows_max = total > total_kv ? total : total_kv;
+    L.item_cap = static_cast<int64_t>(nseg) + static_cast<int64_t>(rows_max) / min_tile + 1;
+    // RoPE positions reach the last key tile; bottom-right aligned queries of a partial
+    // first tile reach up to one tile further
+    const int32_t max_pos = max_seqlen > max_seqlen_kv ? max_seqlen : max_seqlen_kv;
+    L.table_rows = static_cast<int32_t>(ceil_div64(max_pos, kTablePad) * kTablePad + (qkv ? kTablePad : 0));
     size_t off = 0;
     L.header = off;
     off = align256(off + sizeof(WsHeader));
@@ -43,7 +52,7 @@ WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t 
         L.qrot = off;
         off = align256(off + static_cast<size_t>(total) * H * d * 2);
         L.krot = off;
-        off = align256(off + static_cast<size_t>(total) * Hkv * d * 2);
+        off = align256(off + static_cast<size_t>(total_kv) * Hkv * d * 2);
     }
     L.total = off;
     return L;
@@ -102,6 +111,192 @@ using namespace vlc;
 
 static bool aligned(const void* p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Arguments of one attention call (forward or backward).  cu_kv == nullptr is
+// self-attention (keys and values segmented like the queries, total_kv and
+// max_seqlen_kv taken from the query side).
+struct AttnArgs {
+    const void *q, *k, *v, *dout, *o_in;
+    const float* lse_in;
+    const int32_t *cu, *cu_padded, *cu_kv;
+    int32_t nseg, total, total_kv, H, Hkv, d, max_seqlen, max_seqlen_kv;
+    float softmax_scale, rope_theta;
+    uint32_t flags;
+    void* o;
+    float* lse;
+    void *dq, *dk, *dv;
+    void* ws;
+    size_t ws_bytes;
+    void* stream;
+};
+
+static int check_attn_args(const AttnArgs& a, int is_bwd) {
+    if (a.nseg < 1 || a.total < 1 || a.H < 1 || a.max_seqlen < 1) return VLC_ERR_ARG;
+    if (a.cu_kv != nullptr && (a.total_kv < 1 || a.max_seqlen_kv < 1)) return VLC_ERR_ARG;
+    if (a.Hkv < 1 || a.H % a.Hkv != 0) return VLC_ERR_ARG;
+    if (a.flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED)) return VLC_ERR_ARG;
+    if (!(a.rope_theta >= 0.f) || !std::isfinite(a.rope_theta)) return VLC_ERR_ARG;
+    if (a.d != 64 && a.d != 128) return VLC_ERR_UNSUPPORTED;
+    if (a.max_seqlen > VLC_MAX_SEQLEN || a.max_seqlen_kv > VLC_MAX_SEQLEN) return VLC_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(a.total) * a.H * a.d > (int64_t(1) << 40)) return VLC_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(a.total_kv) * a.Hkv * a.d > (int64_t(1) << 40)) return VLC_ERR_UNSUPPORTED;
+    if (a.ws == nullptr || !aligned(a.ws, 256)) return VLC_ERR_WORKSPACE;
+    const bool qkv = a.cu_kv != nullptr;
+    if (a.ws_bytes < ws_layout(a.nseg, a.total, a.H, a.Hkv, a.d, a.max_seqlen, is_bwd, qkv ? a.total_kv : -1,
+                               qkv ? a.max_seqlen_kv : -1).total)
+        return VLC_ERR_WORKSPACE;
+    return VLC_OK;
+}
+
+static int rope_mode(float rope_theta, uint32_t flags) {
+    if (rope_theta == 0.f) return kRopeNone;
+    return (flags & VLC_ROPE_INTERLEAVED) ? kRopeInterleaved : kRopeHalf;
+}
+
+static int attn_fwd_impl(AttnArgs a) {
+    if (a.q == nullptr || a.k == nullptr || a.v == nullptr || a.cu == nullptr || a.o == nullptr ||
+        a.lse == nullptr)
+        return VLC_ERR_ARG;
+    const bool qkv = a.cu_kv != nullptr;
+    if (!qkv) {
+        a.total_kv = a.total;
+        a.max_seqlen_kv = a.max_seqlen;
+    }
+    int st = check_attn_args(a, 0);
+    if (st != VLC_OK) return st;
+    if (!aligned(a.q, 16) || !aligned(a.k, 16) || !aligned(a.v, 16) || !aligned(a.o, 16) || !aligned(a.lse, 4))
+        return VLC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(a.stream);
+    const WsLayout L = ws_layout(a.nseg, a.total, a.H, a.Hkv, a.d, a.max_seqlen, 0, qkv ? a.total_kv : -1,
+                                 qkv ? a.max_seqlen_kv : -1);
+    uint8_t* w = static_cast<uint8_t*>(a.ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
+    int4* items = reinterpret_cast<int4*>(w + L.items);
+    int32_t* order = reinterpret_cast<int32_t*>(w + L.order);
+    int32_t* seg_base = reinterpret_cast<int32_t*>(w + L.seg_base);
+    float2* table = reinterpret_cast<float2*>(w + L.table);
+
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
+    if (launch_worklist(a.cu, a.nseg, a.total, a.max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD, items,
+                        L.item_cap, order, seg_base, &hdr->count, &hdr->err, s, a.cu_padded, a.cu_kv,
+                        a.total_kv, a.max_seqlen_kv) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    if (a.cu_padded != nullptr &&
+        launch_pad_fill(a.cu, a.cu_padded, a.nseg, a.total, a.o, int64_t(a.H) * a.d * 2, nullptr, 0, nullptr,
+                        0, a.lse, a.H, &hdr->err, num_sms_cached(), s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    const int mode = rope_mode(a.rope_theta, a.flags);
+    if (mode != kRopeNone && launch_rope_table(table, L.table_rows, a.d, static_cast<double>(a.rope_theta),
+                                               &hdr->err, s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    FwdParams p{};
+    p.q = a.q; p.k = a.k; p.v = a.v; p.o = a.o; p.lse = a.lse; p.cu = a.cu;
+    p.rows = a.cu_padded != nullptr ? a.cu_padded : a.cu;
+    p.cu_kv = qkv ? a.cu_kv : a.cu;
+    p.rows_kv = qkv ? a.cu_kv : p.rows;
+    p.items = items; p.seg_base = seg_base; p.count = &hdr->count; p.err = &hdr->err;
+    p.next = &hdr->next[0];
+    p.table = mode != kRopeNone ? table : nullptr;
+    p.nseg = a.nseg; p.total = a.total; p.H = a.H; p.d = a.d; p.Hkv = a.Hkv; p.total_kv = a.total_kv;
+    const float scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / std::sqrt(static_cast<float>(a.d));
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.use_rope = mode;
+    if (launch_attn_fwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
+    return VLC_OK;
+}
+
+static int attn_bwd_impl(AttnArgs a) {
+    if (a.dout == nullptr || a.q == nullptr || a.k == nullptr || a.v == nullptr || a.o_in == nullptr ||
+        a.lse_in == nullptr || a.cu == nullptr || a.dq == nullptr || a.dk == nullptr || a.dv == nullptr)
+        return VLC_ERR_ARG;
+    const bool qkv = a.cu_kv != nullptr;
+    if (!qkv) {
+        a.total_kv = a.total;
+        a.max_seqlen_kv = a.max_seqlen;
+    }
+    int st = check_attn_args(a, 1);
+    if (st != VLC_OK) return st;
+    for (const void* ptr : {a.dout, a.q, a.k, a.v, a.o_in, static_cast<const void*>(a.dq),
+                            static_cast<const void*>(a.dk), static_cast<const void*>(a.dv)})
+        if (!aligned(ptr, 16)) return VLC_ERR_ARG;
+    if (!aligned(a.lse_in, 4)) return VLC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(a.stream);
+    const WsLayout L = ws_layout(a.nseg, a.total, a.H, a.Hkv, a.d, a.max_seqlen, 1, qkv ? a.total_kv : -1,
+                                 qkv ? a.max_seqlen_kv : -1);
+    uint8_t* w = static_cast<uint8_t*>(a.ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
+    int4* items_q = reinterpret_cast<int4*>(w + L.items);
+    int4* items_k = items_q + L.item_cap;
+    int32_t* order = reinterpret_cast<int32_t*>(w + L.order);
+    int32_t* seg_base_q = reinterpret_cast<int32_t*>(w + L.seg_base);
+    int32_t* seg_base_k = seg_base_q + (a.nseg + 1);
+    float2* table = reinterpret_cast<float2*>(w + L.table);
+
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
+    // q-tile items (dQ pass) and key-tile items (dK/dV pass)
+    if (launch_worklist(a.cu, a.nseg, a.total, a.max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items_q,
+                        L.item_cap, order, seg_base_q, &hdr->count, &hdr->err, s, a.cu_padded, a.cu_kv,
+                        a.total_kv, a.max_seqlen_kv) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    if (launch_worklist(a.cu, a.nseg, a.total, a.max_seqlen, kBwdBM, kFwdBN, VLC_WORKLIST_BWD, items_k,
+                        L.item_cap, order + a.nseg, seg_base_k, &hdr->count2, &hdr->err, s, a.cu_padded,
+                        a.cu_kv, a.total_kv, a.max_seqlen_kv) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    if (a.cu_padded != nullptr &&
+        launch_pad_fill(a.cu, a.cu_padded, a.nseg, a.total, a.dq, int64_t(a.H) * a.d * 2, a.dk,
+                        int64_t(a.Hkv) * a.d * 2, a.dv, int64_t(a.Hkv) * a.d * 2, nullptr, a.H, &hdr->err,
+                        num_sms_cached(), s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    const int mode = rope_mode(a.rope_theta, a.flags);
+    if (mode != kRopeNone && launch_rope_table(table, L.table_rows, a.d, static_cast<double>(a.rope_theta),
+                                               &hdr->err, s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    BwdParams p{};
+    p.dout = a.dout; p.q = a.q; p.k = a.k; p.v = a.v; p.o = a.o_in; p.lse = a.lse_in;
+    p.dq = a.dq; p.dk = a.dk; p.dv = a.dv; p.cu = a.cu;
+    p.rows = a.cu_padded != nullptr ? a.cu_padded : a.cu;
+    p.cu_kv = qkv ? a.cu_kv : a.cu;
+    p.rows_kv = qkv ? a.cu_kv : p.rows;
+    p.items = items_q; p.seg_base = seg_base_q; p.count = &hdr->count; p.err = &hdr->err;
+    p.items_k = items_k; p.seg_base_k = seg_base_k; p.count_k = &hdr->count2;
+    p.next_q = &hdr->next[1];
+    p.next_k = &hdr->next[2];
+    p.table = mode != kRopeNone ? table : nullptr;
+    p.delta = reinterpret_cast<float*>(w + L.delta);
+    p.qrot = w + L.qrot;
+    p.krot = w + L.krot;
+    p.nseg = a.nseg; p.total = a.total; p.H = a.H; p.d = a.d; p.Hkv = a.Hkv; p.total_kv = a.total_kv;
+    p.scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / std::sqrt(static_cast<float>(a.d));
+    p.use_rope = mode;
+    if (launch_attn_bwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
+    return VLC_OK;
+}
+
+static AttnArgs fwd_args(const void* q, const void* k, const void* v, const int32_t* cu,
+                         const int32_t* cu_padded, const int32_t* cu_kv, int32_t nseg, int32_t total,
+                         int32_t total_kv, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                         int32_t max_seqlen_kv, float softmax_scale, float rope_theta, uint32_t flags,
+                         void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    AttnArgs a{};
+    a.q = q; a.k = k; a.v = v; a.cu = cu; a.cu_padded = cu_padded; a.cu_kv = cu_kv;
+    a.nseg = nseg; a.total = total; a.total_kv = total_kv; a.H = H; a.Hkv = H_kv; a.d = d;
+    a.max_seqlen = max_seqlen; a.max_seqlen_kv = max_seqlen_kv;
+    a.softmax_scale = softmax_scale; a.rope_theta = rope_theta; a.flags = flags;
+    a.o = o; a.lse = lse; a.ws = ws; a.ws_bytes = ws_bytes; a.stream = stream;
+    return a;
+}
+
+static AttnArgs bwd_args(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const int32_t* cu, const int32_t* cu_padded, const int32_t* cu_kv,
+                         int32_t nseg, int32_t total, int32_t total_kv, int32_t H, int32_t H_kv, int32_t d,
+                         int32_t max_seqlen, int32_t max_seqlen_kv, float softmax_scale, float rope_theta,
+                         uint32_t flags, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+    AttnArgs a = fwd_args(q, k, v, cu, cu_padded, cu_kv, nseg, total, total_kv, H, H_kv, d, max_seqlen,
+                          max_seqlen_kv, softmax_scale, rope_theta, flags, nullptr, nullptr, ws, ws_bytes,
+                          stream);
+    a.dout = dout; a.o_in = o; a.lse_in = lse; a.dq = dq; a.dk = dk; a.dv = dv;
+    return a;
 }
 
 extern "C" {
@@ -176,70 +371,12 @@ int vlc_build_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t m
     return e == cudaSuccess ? VLC_OK : VLC_ERR_CUDA;
 }
 
-static int check_attn_args(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
-                           int32_t max_seqlen, void* ws, size_t ws_bytes, int is_bwd) {
-    if (nseg < 1 || total < 1 || H < 1 || max_seqlen < 1) return VLC_ERR_ARG;
-    if (Hkv < 1 || H % Hkv != 0) return VLC_ERR_ARG;
-    if (d != 64 && d != 128) return VLC_ERR_UNSUPPORTED;
-    if (max_seqlen > VLC_MAX_SEQLEN) return VLC_ERR_UNSUPPORTED;
-    if (static_cast<int64_t>(total) * H * d > (int64_t(1) << 40)) return VLC_ERR_UNSUPPORTED;
-    if (ws == nullptr || !aligned(ws, 256)) return VLC_ERR_WORKSPACE;
-    if (ws_bytes < ws_layout(nseg, total, H, Hkv, d, max_seqlen, is_bwd).total) return VLC_ERR_WORKSPACE;
-    return VLC_OK;
-}
-
-static int rope_mode(float rope_theta, uint32_t flags) {
-    if (rope_theta == 0.f) return kRopeNone;
-    return (flags & VLC_ROPE_INTERLEAVED) ? kRopeInterleaved : kRopeHalf;
-}
-
 int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* cu,
                     const int32_t* cu_padded, int32_t nseg, int32_t total, int32_t H, int32_t H_kv,
                     int32_t d, int32_t max_seqlen, float softmax_scale, float rope_theta,
                     uint32_t flags, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
-    if (q == nullptr || k == nullptr || v == nullptr || cu == nullptr || o == nullptr ||
-        lse == nullptr)
-        return VLC_ERR_ARG;
-    if (flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED)) return VLC_ERR_ARG;
-    int st = check_attn_args(nseg, total, H, H_kv, d, max_seqlen, ws, ws_bytes, 0);
-    if (st != VLC_OK) return st;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-        !aligned(lse, 4))
-        return VLC_ERR_ARG;
-    if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return VLC_ERR_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const WsLayout L = ws_layout(nseg, total, H, H_kv, d, max_seqlen, 0);
-    uint8_t* w = static_cast<uint8_t*>(ws);
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
-    int4* items = reinterpret_cast<int4*>(w + L.items);
-    int32_t* order = reinterpret_cast<int32_t*>(w + L.order);
-    int32_t* seg_base = reinterpret_cast<int32_t*>(w + L.seg_base);
-    float2* table = reinterpret_cast<float2*>(w + L.table);
-
-    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
-    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD, items,
-                        L.item_cap, order, seg_base, &hdr->count, &hdr->err, s, cu_padded) != cudaSuccess)
-        return VLC_ERR_CUDA;
-    if (cu_padded != nullptr &&
-        launch_pad_fill(cu, cu_padded, nseg, total, o, int64_t(H) * d * 2, nullptr, 0, nullptr, 0, lse, H,
-                        &hdr->err, num_sms_cached(), s) != cudaSuccess)
-        return VLC_ERR_CUDA;
-    const bool rope = rope_theta != 0.f;
-    if (rope && launch_rope_table(table, L.table_rows, d, static_cast<double>(rope_theta),
-                                  &hdr->err, s) != cudaSuccess)
-        return VLC_ERR_CUDA;
-    FwdParams p{};
-    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu = cu;
-    p.rows = cu_padded != nullptr ? cu_padded : cu;
-    p.items = items; p.seg_base = seg_base; p.count = &hdr->count; p.err = &hdr->err;
-    p.next = &hdr->next[0];
-    p.table = rope ? table : nullptr;
-    p.nseg = nseg; p.total = total; p.H = H; p.d = d; p.Hkv = H_kv;
-    const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.use_rope = rope_mode(rope_theta, flags);
-    if (launch_attn_fwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
-    return VLC_OK;
+    return attn_fwd_impl(fwd_args(q, k, v, cu, cu_padded, nullptr, nseg, total, 0, H, H_kv, d, max_seqlen, 0,
+                                  softmax_scale, rope_theta, flags, o, lse, ws, ws_bytes, stream));
 }
 
 int vlc_attn_fwd_gqa(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
@@ -262,62 +399,9 @@ int vlc_attn_bwd_ex(const void* dout, const void* q, const void* k, const void* 
                     int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
                     float softmax_scale, float rope_theta, uint32_t flags, void* dq, void* dk,
                     void* dv, void* ws, size_t ws_bytes, void* stream) {
-    if (dout == nullptr || q == nullptr || k == nullptr || v == nullptr || o == nullptr ||
-        lse == nullptr || cu == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
-        return VLC_ERR_ARG;
-    if (flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED)) return VLC_ERR_ARG;
-    int st = check_attn_args(nseg, total, H, H_kv, d, max_seqlen, ws, ws_bytes, 1);
-    if (st != VLC_OK) return st;
-    for (const void* ptr : {dout, q, k, v, o, static_cast<const void*>(dq),
-                            static_cast<const void*>(dk), static_cast<const void*>(dv)})
-        if (!aligned(ptr, 16)) return VLC_ERR_ARG;
-    if (!aligned(lse, 4)) return VLC_ERR_ARG;
-    if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return VLC_ERR_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const WsLayout L = ws_layout(nseg, total, H, H_kv, d, max_seqlen, 1);
-    uint8_t* w = static_cast<uint8_t*>(ws);
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
-    int4* items_q = reinterpret_cast<int4*>(w + L.items);
-    int4* items_k = items_q + L.item_cap;
-    int32_t* order = reinterpret_cast<int32_t*>(w + L.order);
-    int32_t* seg_base_q = reinterpret_cast<int32_t*>(w + L.seg_base);
-    int32_t* seg_base_k = seg_base_q + (nseg + 1);
-    float2* table = reinterpret_cast<float2*>(w + L.table);
-
-    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
-    // q-tile items (dQ pass) and key-tile items (dK/dV pass)
-    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items_q,
-                        L.item_cap, order, seg_base_q, &hdr->count, &hdr->err, s, cu_padded) != cudaSuccess)
-        return VLC_ERR_CUDA;
-    if (launch_worklist(cu, nseg, total, max_seqlen, kBwdBM, kFwdBN, VLC_WORKLIST_BWD, items_k,
-                        L.item_cap, order + nseg, seg_base_k, &hdr->count2, &hdr->err, s, cu_padded) !=
-        cudaSuccess)
-        return VLC_ERR_CUDA;
-    if (cu_padded != nullptr &&
-        launch_pad_fill(cu, cu_padded, nseg, total, dq, int64_t(H) * d * 2, dk, int64_t(H_kv) * d * 2, dv,
-                        int64_t(H_kv) * d * 2, nullptr, H, &hdr->err, num_sms_cached(), s) != cudaSuccess)
-        return VLC_ERR_CUDA;
-    const bool rope = rope_theta != 0.f;
-    if (rope && launch_rope_table(table, L.table_rows, d, static_cast<double>(rope_theta),
-                                  &hdr->err, s) != cudaSuccess)
-        return VLC_ERR_CUDA;
-    BwdParams p{};
-    p.dout = dout; p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
-    p.dq = dq; p.dk = dk; p.dv = dv; p.cu = cu;
-    p.rows = cu_padded != nullptr ? cu_padded : cu;
-    p.items = items_q; p.seg_base = seg_base_q; p.count = &hdr->count; p.err = &hdr->err;
-    p.items_k = items_k; p.seg_base_k = seg_base_k; p.count_k = &hdr->count2;
-    p.next_q = &hdr->next[1];
-    p.next_k = &hdr->next[2];
-    p.table = rope ? table : nullptr;
-    p.delta = reinterpret_cast<float*>(w + L.delta);
-    p.qrot = w + L.qrot;
-    p.krot = w + L.krot;
-    p.nseg = nseg; p.total = total; p.H = H; p.d = d; p.Hkv = H_kv;
-    p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(d));
-    p.use_rope = rope_mode(rope_theta, flags);
-    if (launch_attn_bwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
-    return VLC_OK;
+    return attn_bwd_impl(bwd_args(dout, q, k, v, o, lse, cu, cu_padded, nullptr, nseg, total, 0, H, H_kv, d,
+                                  max_seqlen, 0, softmax_scale, rope_theta, flags, dq, dk, dv, ws, ws_bytes,
+                                  stream));
 }
 
 int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void* v, const void* o,
@@ -335,6 +419,37 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
                  void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
     return vlc_attn_bwd_gqa(dout, q, k, v, o, lse, cu, nseg, total, H, H, d, max_seqlen, softmax_scale,
                             rope_theta, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+size_t vlc_workspace_bytes_qkv(int32_t nseg, int32_t total_q, int32_t total_kv, int32_t H, int32_t H_kv,
+                               int32_t d, int32_t max_seqlen_q, int32_t max_seqlen_kv, int is_bwd) {
+    if (nseg < 1 || total_q < 1 || total_kv < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 ||
+        (d != 64 && d != 128) || max_seqlen_q < 1 || max_seqlen_kv < 1 || max_seqlen_q > VLC_MAX_SEQLEN ||
+        max_seqlen_kv > VLC_MAX_SEQLEN)
+        return 0;
+    return ws_layout(nseg, total_q, H, H_kv, d, max_seqlen_q, is_bwd ? 1 : 0, total_kv, max_seqlen_kv).total;
+}
+
+int vlc_attn_fwd_qkv(const void* q, const void* k, const void* v, const int32_t* cu_q,
+                     const int32_t* cu_kv, int32_t nseg, int32_t total_q, int32_t total_kv, int32_t H,
+                     int32_t H_kv, int32_t d, int32_t max_seqlen_q, int32_t max_seqlen_kv,
+                     float softmax_scale, float rope_theta, uint32_t flags, void* o, float* lse, void* ws,
+                     size_t ws_bytes, void* stream) {
+    if (cu_kv == nullptr) return VLC_ERR_ARG;
+    return attn_fwd_impl(fwd_args(q, k, v, cu_q, nullptr, cu_kv, nseg, total_q, total_kv, H, H_kv, d,
+                                  max_seqlen_q, max_seqlen_kv, softmax_scale, rope_theta, flags, o, lse, ws,
+                                  ws_bytes, stream));
+}
+
+int vlc_attn_bwd_qkv(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const int32_t* cu_q, const int32_t* cu_kv, int32_t nseg,
+                     int32_t total_q, int32_t total_kv, int32_t H, int32_t H_kv, int32_t d,
+                     int32_t max_seqlen_q, int32_t max_seqlen_kv, float softmax_scale, float rope_theta,
+                     uint32_t flags, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+    if (cu_kv == nullptr) return VLC_ERR_ARG;
+    return attn_bwd_impl(bwd_args(dout, q, k, v, o, lse, cu_q, nullptr, cu_kv, nseg, total_q, total_kv, H,
+                                  H_kv, d, max_seqlen_q, max_seqlen_kv, softmax_scale, rope_theta, flags, dq,
+                                  dk, dv, ws, ws_bytes, stream));
 }
 
 int vlc_get_error(const void* ws, int32_t* bits_out, void* stream) {

@@ -55,31 +55,98 @@ constexpr uint64_t kDrainNs = 200000000ull;
 // ====================================================================== prep
 // One pass over the (token, head) rows: D = rowsum(dO * O) in fp32 ([H, total]),
 // and with RoPE the rotated q' = R(p) q and k' = R(p) k (bf16, rounded once),
-// so the attention passes below read pre-rotated operands.  D/16 threads per
-// row; thread c handles 16-byte chunks c and c + D/16 of the row: rotate-half
-// pairs j = 8c .. 8c+7 (columns j and j+D/2), or, with the interleaved pairing,
-// pairs 4c .. 4c+3 and D/4 + 4c .. D/4 + 4c+3 (columns 2j and 2j+1).
+// so the attention passes below read pre-rotated operands.  The rows are the
+// total * H query rows followed (with RoPE) by the total_kv * Hkv key rows.
+// D/16 threads per row; thread c handles 16-byte chunks c and c + D/16 of the
+// row: rotate-half pairs j = 8c .. 8c+7 (columns j and j+D/2), or, with the
+// interleaved pairing, pairs 4c .. 4c+3 and D/4 + 4c .. D/4 + 4c+3 (columns 2j
+// and 2j+1).  A query of segment r sits at position p + Lk_r - L_r (bottom-right
+// alignment; 0 extra for self-attention), a key at its own index.
+template <int D>
+__device__ __forceinline__ void rotate_row(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                           int64_t a0, int64_t a1, const float2* __restrict__ table,
+                                           int64_t pos, bool real, bool il, int c) {
+    if (!real) {   // padding rows: zeros, so every operand row stays finite
+        dst[a0] = make_uint4(0u, 0u, 0u, 0u);
+        dst[a1] = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    // cs/sn[2e], [2e+1]: angles of the two pairs that the e-th words of the lo
+    // and hi chunks take part in (rotate-half: the pairs at word e's two
+    // columns; interleaved: word e of lo, word e of hi)
+    float cs[8], sn[8];
+    if (!il) {
+        const float4* t4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 8);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 f = __ldg(t4 + e);
+            cs[2 * e] = f.x; sn[2 * e] = f.y; cs[2 * e + 1] = f.z; sn[2 * e + 1] = f.w;
+        }
+    } else {
+        const float4* l4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 4);
+        const float4* h4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + D / 4 + c * 4);
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+            const float4 f = __ldg(l4 + e2), g = __ldg(h4 + e2);
+            cs[4 * e2] = f.x; sn[4 * e2] = f.y; cs[4 * e2 + 1] = g.x; sn[4 * e2 + 1] = g.y;
+            cs[4 * e2 + 2] = f.z; sn[4 * e2 + 2] = f.w; cs[4 * e2 + 3] = g.z; sn[4 * e2 + 3] = g.w;
+        }
+    }
+    const uint4 x4 = __ldg(src + a0), y4 = __ldg(src + a1);
+    const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
+    uint32_t nx[4], ny[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
+        if (!il) {   // pairs (lo word e, hi word e) at columns 2e and 2e+1
+            const float x0 = bf16_lo(xv[e]), x1 = bf16_hi(xv[e]);
+            const float y0 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
+            nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
+            ny[e] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+        } else {     // lo word e and hi word e are pairs of their own
+            const float x0 = bf16_lo(xv[e]), y0 = bf16_hi(xv[e]);
+            const float x1 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
+            nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(y0, c0, x0 * s0));
+            ny[e] = pack_bf16x2(fmaf(x1, c1, -y1 * s1), fmaf(y1, c1, x1 * s1));
+        }
+    }
+    dst[a0] = make_uint4(nx[0], nx[1], nx[2], nx[3]);
+    dst[a1] = make_uint4(ny[0], ny[1], ny[2], ny[3]);
+}
+
+// Largest r in [0, nseg-1] with rows[r] <= tok (clamped, in bounds).
+__device__ __forceinline__ int segment_of_row(const int32_t* __restrict__ rows, int nseg, int64_t tok) {
+    int a = 0, b = nseg - 1;
+    while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (__ldg(rows + mid) <= tok) a = mid; else b = mid - 1;
+    }
+    return a;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const uint4* __restrict__ q,
             const uint4* __restrict__ k, uint4* __restrict__ qrot, uint4* __restrict__ krot,
             float* __restrict__ delta, const int32_t* __restrict__ cu,
-            const int32_t* __restrict__ seg_rows, int32_t nseg,
-            const float2* __restrict__ table, int32_t total, int32_t H, int32_t Hkv, int rope,
-            const int32_t* __restrict__ err) {
+            const int32_t* __restrict__ seg_rows, const int32_t* __restrict__ cu_kv,
+            const int32_t* __restrict__ seg_rows_kv, int32_t nseg,
+            const float2* __restrict__ table, int32_t total, int32_t H, int32_t Hkv, int32_t total_kv,
+            int rope, const int32_t* __restrict__ err) {
     if (*err != 0) return;
     constexpr int TPR = D / 16;        // threads per row
     constexpr int HALF = D / 16;       // uint4 chunks per half row
-    const int64_t rows = static_cast<int64_t>(total) * H;
+    const int64_t qrows = static_cast<int64_t>(total) * H;
+    const int64_t rows = qrows + (rope ? static_cast<int64_t>(total_kv) * Hkv : 0);
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int c = threadIdx.x % TPR;
     const int64_t per_iter = nthreads / TPR;
+    const bool il = rope == kRopeInterleaved;
     for (int64_t first = 0; first < rows; first += per_iter) {   // uniform trip count
         const int64_t row = first + gtid / TPR;
-        const bool in = row < rows;
         float acc = 0.f;
-        if (in) {
+        if (row < qrows) {          // query row: D, and q' with RoPE
             const int64_t lo = row * (2 * HALF) + c, hi = lo + HALF;
             const uint4 g0 = __ldg(dout + lo), g1 = __ldg(dout + hi);
             const uint4 o0 = __ldg(o + lo), o1 = __ldg(o + hi);
@@ -90,77 +157,25 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
                 acc += bf16_lo(gv[e]) * bf16_lo(ov[e]) + bf16_hi(gv[e]) * bf16_hi(ov[e]);
             if (rope) {
                 const int64_t tok = row / H;
-                int a = 0, b = nseg - 1;   // segment (slot) of tok (clamped, in bounds)
-                while (a < b) {
-                    const int mid = (a + b + 1) >> 1;
-                    if (__ldg(seg_rows + mid) <= tok) a = mid; else b = mid - 1;
-                }
-                // rows past the segment's length are padding (padded layouts only):
-                // their rotated copies are zeros, so every operand row stays finite
+                const int a = segment_of_row(seg_rows, nseg, tok);
+                const int64_t L = __ldg(cu + a + 1) - __ldg(cu + a);
                 const int64_t pos0 = tok - __ldg(seg_rows + a);
-                const bool real = pos0 < __ldg(cu + a + 1) - __ldg(cu + a);
-                const int64_t pos = real ? pos0 : 0;
-                const bool il = rope == kRopeInterleaved;
-                // cs/sn[2e], [2e+1]: angles of the two pairs that the e-th words of the lo
-                // and hi chunks take part in (rotate-half: the pairs at word e's two
-                // columns; interleaved: word e of lo, word e of hi)
-                float cs[8], sn[8];
-                if (!il) {
-                    const float4* t4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 8);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 f = __ldg(t4 + e);
-                        cs[2 * e] = f.x; sn[2 * e] = f.y; cs[2 * e + 1] = f.z; sn[2 * e + 1] = f.w;
-                    }
-                } else {
-                    const float4* l4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 4);
-                    const float4* h4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + D / 4 + c * 4);
-#pragma unroll
-                    for (int e2 = 0; e2 < 2; ++e2) {
-                        const float4 f = __ldg(l4 + e2), g = __ldg(h4 + e2);
-                        cs[4 * e2] = f.x; sn[4 * e2] = f.y; cs[4 * e2 + 1] = g.x; sn[4 * e2 + 1] = g.y;
-                        cs[4 * e2 + 2] = f.z; sn[4 * e2 + 2] = f.w; cs[4 * e2 + 3] = g.z; sn[4 * e2 + 3] = g.w;
-                    }
-                }
-                const int64_t hh = row - tok * H;   // head of this row: k has only Hkv heads
-                const int64_t klo = (tok * Hkv + hh) * (2 * HALF) + c, khi = klo + HALF;
-#pragma unroll
-                for (int which = 0; which < 2; ++which) {
-                    if (which == 1 && hh >= Hkv) break;
-                    const uint4* src = which ? k : q;
-                    uint4* dst = which ? krot : qrot;
-                    const int64_t a0 = which ? klo : lo, a1 = which ? khi : hi;
-                    if (!real) {
-                        dst[a0] = make_uint4(0u, 0u, 0u, 0u);
-                        dst[a1] = make_uint4(0u, 0u, 0u, 0u);
-                        continue;
-                    }
-                    const uint4 x4 = __ldg(src + a0), y4 = __ldg(src + a1);
-                    const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
-                    uint32_t nx[4], ny[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
-                        if (!il) {   // pairs (lo word e, hi word e) at columns 2e and 2e+1
-                            const float x0 = bf16_lo(xv[e]), x1 = bf16_hi(xv[e]);
-                            const float y0 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
-                            nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
-                            ny[e] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
-                        } else {     // lo word e and hi word e are pairs of their own
-                            const float x0 = bf16_lo(xv[e]), y0 = bf16_hi(xv[e]);
-                            const float x1 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
-                            nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(y0, c0, x0 * s0));
-                            ny[e] = pack_bf16x2(fmaf(x1, c1, -y1 * s1), fmaf(y1, c1, x1 * s1));
-                        }
-                    }
-                    dst[a0] = make_uint4(nx[0], nx[1], nx[2], nx[3]);
-                    dst[a1] = make_uint4(ny[0], ny[1], ny[2], ny[3]);
-                }
+                const bool real = pos0 < L;   // rows past the length: padding (padded layouts)
+                const int64_t pos = real ? pos0 + (__ldg(cu_kv + a + 1) - __ldg(cu_kv + a)) - L : 0;
+                rotate_row<D>(q, qrot, lo, hi, table, pos, real, il, c);
             }
+        } else if (row < rows) {    // key row (RoPE only): k'
+            const int64_t kr = row - qrows;
+            const int64_t lo = kr * (2 * HALF) + c, hi = lo + HALF;
+            const int64_t tok = kr / Hkv;
+            const int a = segment_of_row(seg_rows_kv, nseg, tok);
+            const int64_t pos0 = tok - __ldg(seg_rows_kv + a);
+            const bool real = pos0 < __ldg(cu_kv + a + 1) - __ldg(cu_kv + a);
+            rotate_row<D>(k, krot, lo, hi, table, real ? pos0 : 0, real, il, c);
         }
 #pragma unroll
         for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        if (in && c == 0) {
+        if (row < qrows && c == 0) {
             const int64_t tok = row / H, h = row - tok * H;
             delta[h * total + tok] = acc;
         }
@@ -380,7 +395,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_put(rg, n, p.next_q, nunits, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
                 // the staging slot frees as soon as the math warps copied the last unit's rows to TMEM
                 if (!(ok = mbar_wait(bar(QD_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(QD_FULL), 2 * LY::TILE);
@@ -401,7 +416,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
                         tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
-                                         w.h / (p.H / p.Hkv), w.row0 + j * BK, bar(K_FULL + ks), pol_keep);
+                                         w.h / (p.H / p.Hkv), w.row0k + j * BK, bar(K_FULL + ks), pol_keep);
                     k_issued = nn + 1;
                 }
                 kv += w.hi;
@@ -416,7 +431,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             for (int n = 0; ok; ++n) {
                 int u;
                 if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
                 for (int j = 0; j < w.hi && ok; ++j) {
                     const uint32_t nn = kv + j;
                     const int vs = nn % kVStages;
@@ -425,7 +440,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
                         tma_load_3d_hint(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
-                                         w.h / (p.H / p.Hkv), w.row0 + j * BK, bar(V_FULL + vs), pol_keep);
+                                         w.h / (p.H / p.Hkv), w.row0k + j * BK, bar(V_FULL + vs), pol_keep);
                     v_issued = nn + 1;
                 }
                 kv += w.hi;
@@ -484,7 +499,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
+                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
                 if (!(ok = wait_warp(bar(QT_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_s(kv))) break;
                 if (!(ok = issue_dp(kv))) break;
@@ -545,12 +560,13 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         bool have = ok && u >= 0;
         Unit w{};
         if (have) {
-            w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
+            w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
             ok = have = stage(0);
         }
         while (have) {
             const int qpos = w.tile * 128 + r;
             const bool valid = qpos < w.L;
+            const int rpos = valid ? qpos + w.off : 0;   // RoPE position of the query
             const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? qpos : 0);
             const float lse2 = valid ? __ldg(p.lse + static_cast<int64_t>(w.h) * p.total + tok) * kLog2e : 0.f;
             const float dlt = valid ? __ldg(p.delta + static_cast<int64_t>(w.h) * p.total + tok) : 0.f;
@@ -564,8 +580,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(bar(S_EMPTY));
-                const bool edge = (j == w.hi - 1);   // diagonal step (and the segment tail)
-                const int lim = !valid ? -1 : (edge ? min(qpos, w.L - 1) - j * BK : BK - 1);
+                // diagonal step(s) and the segment tail: the last key tile, and the one before
+                // it when the diagonal is not tile-aligned (off % BK != 0)
+                const bool edge = (j == w.hi - 1) || (j == w.hi - 2 && (w.off & (BK - 1)) != 0);
+                const int lim = !valid ? -1 : (edge ? min(qpos + w.off, w.Lk - 1) - j * BK : BK - 1);
                 const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
                 uint32_t pp[32];
 #pragma unroll
@@ -608,7 +626,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             if (!(ok = ring_get_warp(rg, static_cast<int>(unit_it) + 1, abort, u2))) break;
             const bool have_next = u2 >= 0;
             if (have_next) {
-                w2 = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u2);
+                w2 = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u2);
                 if (!(ok = stage(unit_it + 1))) break;
             }
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
@@ -616,10 +634,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             if (g == 0) {
                 uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dq) + (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
                 if (p.use_rope == kRopeInterleaved)
-                    store_unrotated<D, true>(tmem + lane_off + LY::DQ_COL, p.table, qpos, p.scale, true,
+                    store_unrotated<D, true>(tmem + lane_off + LY::DQ_COL, p.table, rpos, p.scale, true,
                                              valid, row_out);
                 else
-                    store_unrotated<D, false>(tmem + lane_off + LY::DQ_COL, p.table, qpos, p.scale,
+                    store_unrotated<D, false>(tmem + lane_off + LY::DQ_COL, p.table, rpos, p.scale,
                                               p.use_rope != 0, valid, row_out);
             }
             tc_fence_before();
@@ -765,10 +783,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_put(rg, n, p.next_k, nunits, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.nseg, p.Hkv, u);   // w.h: key/value head
+                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);   // w.h: key/value head
                 if (!(ok = mbar_wait(bar(KV_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(KV_FULL), 2 * LY::TILE);
-                const int krow = w.row0 + w.tile * 128;
+                const int krow = w.row0k + w.tile * 128;
 #pragma unroll
                 for (int kb = 0; kb < LY::KB; ++kb) {
                     tma_load_3d_hint(sbase + LY::K0 + kb * LY::BLK, &tmK, kb * 64, w.h, krow, bar(KV_FULL), pol_stream);
@@ -840,7 +858,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.nseg, p.Hkv, u);
+                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
                 if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_st(st))) break;
                 issue_dpt(st);
@@ -889,7 +907,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int n = 0; ok; ++n) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.nseg, p.Hkv, u);
+            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
             const int nq = w.hi - w.lo;
             for (int sq = 0; sq < grp * nq && ok; ++sq, ++st) {
                 const int i = w.lo + sq % nq, hq = w.h * grp + sq / nq;
@@ -926,7 +944,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int n = 0; ok; ++n, ++unit_it) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.nseg, p.Hkv, u);
+            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
             const int kvpos = w.tile * 128 + r;
             const int nq = w.hi - w.lo;
             for (int sq = 0; sq < grp * nq; ++sq, ++st) {
@@ -935,9 +953,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 const float* l2s = lsed + sl * 256 + c0;
                 const float* dls = lsed + sl * 256 + 128 + c0;
                 if (!(ok = wait_warp(bar(LSED_FULL + sl), (st / kLsedSlots) & 1, abort))) break;
-                // allowed q columns: kvpos <= i*BQ + col and i*BQ + col < L
-                const bool edge = (i == w.lo) || ((i + 1) * BQ > w.L);
-                const int c_lo = kvpos - i * BQ, c_hi = w.L - 1 - i * BQ;
+                // allowed q columns: kvpos <= i*BQ + col + off and i*BQ + col < L; only steps
+                // whose first column does not see the tile's last key need the check
+                const bool edge = (i * BQ + w.off < w.tile * 128 + 127) || ((i + 1) * BQ > w.L);
+                const int c_lo = kvpos - w.off - i * BQ, c_hi = w.L - 1 - i * BQ;
                 // ---- phase A: P^T = exp2(s * scale_log2 - lse2) over this group's 64 columns
                 if (!(ok = wait_warp(bar(ST_FULL), st & 1, abort))) break;
                 tc_fence_after();
@@ -1006,8 +1025,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             if (!ok) break;
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
             tc_fence_after();
-            const bool valid = kvpos < w.L;
-            const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? kvpos : 0);
+            const bool valid = kvpos < w.Lk;
+            const int64_t tok = static_cast<int64_t>(w.row0k) + (valid ? kvpos : 0);
             const int64_t roff = (tok * p.Hkv + w.h) * static_cast<int64_t>(D) * 2;
             if (g == 0) {   // dV: plain copy out
 #pragma unroll
@@ -1065,13 +1084,15 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 template <int D>
 static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s) {
     {
-        const int64_t rows = static_cast<int64_t>(p.total) * p.H;
+        const int64_t rows = static_cast<int64_t>(p.total) * p.H +
+                             (p.use_rope ? static_cast<int64_t>(p.total_kv) * p.Hkv : 0);
         int64_t blocks = (rows * (D / 16) + 255) / 256;
         if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
         bwd::prep_kernel<D><<<static_cast<int>(blocks), 256, 0, s>>>(
             static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.o),
             static_cast<const uint4*>(p.q), static_cast<const uint4*>(p.k), static_cast<uint4*>(p.qrot),
-            static_cast<uint4*>(p.krot), p.delta, p.cu, p.rows, p.nseg, p.table, p.total, p.H, p.Hkv, p.use_rope,
+            static_cast<uint4*>(p.krot), p.delta, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.table, p.total, p.H,
+            p.Hkv, p.total_kv, p.use_rope,
             p.err);
     }
     // with RoPE the attention passes read the rotated copies
@@ -1080,8 +1101,8 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
     CUtensorMap q128, do128, k128, v128;
     if (!make_tmap_thd(&q128, qop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&do128, p.dout, p.total, p.H, D, 128) ||
-        !make_tmap_thd(&k128, kop, p.total, p.Hkv, D, 128) ||
-        !make_tmap_thd(&v128, p.v, p.total, p.Hkv, D, 128))
+        !make_tmap_thd(&k128, kop, p.total_kv, p.Hkv, D, 128) ||
+        !make_tmap_thd(&v128, p.v, p.total_kv, p.Hkv, D, 128))
         return cudaErrorInvalidValue;
     {
         constexpr uint32_t smem = bwd::dq::Layout<D>::ALLOC;

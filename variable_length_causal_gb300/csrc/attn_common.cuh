@@ -10,17 +10,23 @@
 namespace vlc {
 
 struct Unit {
-    int seg, tile, lo, hi, h, L, row0;   // tile = q tile (forward items) or key tile (backward items)
+    int seg, tile, lo, hi, h;   // tile = q tile (forward items) or key tile (backward items)
+    int L, row0;                // queries: count and first row
+    int Lk, row0k;              // keys / values: count and first row (== L, row0 for self-attention)
+    int off;                    // Lk - L: query p sits at position p + off and sees keys 0 .. p + off
 };
 
 // Unit u -> (item, head).  Units run over the sorted segments; inside a
 // segment head-major, then the segment's items in work-list order.  The
 // segment's length comes from cu, its first row from rows (cu itself, or the
-// padded offsets of a layout with padding between segments).
+// padded offsets of a layout with padding between segments); likewise for the
+// keys and values from cu_kv / rows_kv (the same arrays for self-attention).
 __device__ __forceinline__ Unit decode_unit(const int4* __restrict__ items,
                                             const int32_t* __restrict__ seg_base,
                                             const int32_t* __restrict__ cu,
-                                            const int32_t* __restrict__ rows, int nseg, int H, int u) {
+                                            const int32_t* __restrict__ rows,
+                                            const int32_t* __restrict__ cu_kv,
+                                            const int32_t* __restrict__ rows_kv, int nseg, int H, int u) {
     const int64_t HH = H;
     int lo = 0, hi = nseg - 1;
     while (lo < hi) {
@@ -39,6 +45,9 @@ __device__ __forceinline__ Unit decode_unit(const int4* __restrict__ items,
     w.hi = it.w;
     w.L = __ldg(cu + it.x + 1) - __ldg(cu + it.x);
     w.row0 = __ldg(rows + it.x);
+    w.Lk = __ldg(cu_kv + it.x + 1) - __ldg(cu_kv + it.x);
+    w.row0k = __ldg(rows_kv + it.x);
+    w.off = w.Lk - w.L;
     return w;
 }
 

@@ -92,7 +92,9 @@ struct Layout {
 // K/V tile.  With T = ceil(L / 128) q tiles, unit qb holds tiles (2qb - s, 2qb - s + 1)
 // where s = T mod 2, so an odd T leaves tile 0 alone in unit 0 (one key tile of work)
 // rather than the last, longest tile.  Slot t of the unit is q tile q0 + t and needs
-// key tiles [0, q0 + t + 1) (up to its diagonal); nk is the length of the K/V stream.
+// the key tiles up to the one holding key (q0 + t + 1) * 128 - 1 + off (its diagonal;
+// off = Lk - L is 0 for self-attention, where that is [0, q0 + t + 1)); nk is the
+// length of the K/V stream.
 struct FUnit {
     Unit w;
     bool has1;
@@ -102,14 +104,15 @@ struct FUnit {
 
 __device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
     FUnit f;
-    f.w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.nseg, p.H, u);
+    f.w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
     const int T = (f.w.L + BQ - 1) / BQ;
     const int s = T & 1;
     const bool lone = (s != 0) && (f.w.tile == 0);
     f.has1 = !lone;
     f.q0 = lone ? 0 : 2 * f.w.tile - s;
-    f.n0 = f.q0 + 1;
-    f.n1 = f.has1 ? f.q0 + 2 : 0;
+    const int nkt = (f.w.Lk + BN - 1) / BN;
+    f.n0 = min(nkt, ((f.q0 + 1) * BQ + f.w.off + BN - 1) / BN);
+    f.n1 = f.has1 ? min(nkt, ((f.q0 + 2) * BQ + f.w.off + BN - 1) / BN) : 0;
     f.nk = f.has1 ? f.n1 : f.n0;
     f.hkv = p.Hkv == p.H ? f.w.h : f.w.h / (p.H / p.Hkv);
     return f;
@@ -214,7 +217,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
                         tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
-                                         f.hkv, f.w.row0 + j * BN, bar(K_FULL + ks), pol_keep);
+                                         f.hkv, f.w.row0k + j * BN, bar(K_FULL + ks), pol_keep);
                     k_issued = n + 1;
                 }
                 kvn += f.nk;
@@ -339,9 +342,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (!(ok = wait_warp(bar(S_FULL + t), cnt_s & 1, abort))) break;
                 ++cnt_s;
                 tc_fence_after();
-                // allowed key columns of this tile: c <= lim (only the last tile is masked)
-                const bool edge = (j == nt - 1);
-                const int lim = edge ? min(qpos, f.w.L - 1) - j * BN : BN - 1;
+                // allowed key columns of this tile: c <= lim.  Only the last tile is masked,
+                // or the last two when the diagonal is not tile-aligned (off % BN != 0)
+                const bool edge = (j == nt - 1) || (j == nt - 2 && (f.w.off & (BN - 1)) != 0);
+                const int lim = edge ? min(qpos + f.w.off, f.w.Lk - 1) - j * BN : BN - 1;
                 // the thread's whole S row (BN fp32 columns) in registers: four loads, one wait
                 uint32_t s[BN];
 #pragma unroll
@@ -466,8 +470,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int slot = qm % kQSlots;
                     if (!(ok = wait_warp(bar(Q_FULL + slot), (qm / kQSlots) & 1, abort))) break;
                     if (p.use_rope)
-                        rope_tile<D, 128, IL>(sbase + LY::Q0 + slot * LY::TILE, (f.q0 + t) * BQ, p.table,
-                                              step, wr, lane);
+                        rope_tile<D, 128, IL>(sbase + LY::Q0 + slot * LY::TILE, (f.q0 + t) * BQ + f.w.off,
+                                              p.table, step, wr, lane);
                     fence_proxy_async_smem();
                     mbar_arrive(bar(Q_READY + slot));
                     ++qm;
@@ -504,7 +508,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
                         tma_load_3d_hint(sbase + LY::V0 + vs * LY::TILE + kb * LY::BLK, &tmV, kb * 64,
-                                         f.hkv, f.w.row0 + j * BN, bar(V_FULL + vs), pol_keep);
+                                         f.hkv, f.w.row0k + j * BN, bar(V_FULL + vs), pol_keep);
                     kv_issued = n + 1;
                 }
                 vn += f.nk;
@@ -553,8 +557,8 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int32_t total, int32_t H,
 cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     if (!make_tmap_thd(&tq, p.q, p.total, p.H, p.d, 128) ||
-        !make_tmap_thd(&tk, p.k, p.total, p.Hkv, p.d, 128) ||
-        !make_tmap_thd(&tv, p.v, p.total, p.Hkv, p.d, 128))
+        !make_tmap_thd(&tk, p.k, p.total_kv, p.Hkv, p.d, 128) ||
+        !make_tmap_thd(&tv, p.v, p.total_kv, p.Hkv, p.d, 128))
         return cudaErrorInvalidValue;
     const dim3 grid(num_sms), block(fwd::kThreads);
     // The warpgroups re-split the block's register pool at run time, which is only

@@ -28,8 +28,9 @@ struct WsLayout {
     int32_t table_rows;
 };
 
+// total_kv / max_seqlen_kv < 0: self-attention (the query sizes).
 WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t d,
-                   int32_t max_seqlen, int is_bwd);
+                   int32_t max_seqlen, int is_bwd, int32_t total_kv = -1, int32_t max_seqlen_kv = -1);
 
 // Kernel launchers (return cudaGetLastError()).
 cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64_t* tokens,
@@ -39,7 +40,9 @@ cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64
 cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
                             int32_t BM, int32_t BN, int kind, int4* items, int64_t cap,
                             int32_t* order, int32_t* seg_base, int32_t* count, int32_t* err,
-                            cudaStream_t s, const int32_t* cu_padded = nullptr);
+                            cudaStream_t s, const int32_t* cu_padded = nullptr,
+                            const int32_t* cu_kv = nullptr, int32_t total_kv = 0,
+                            int32_t max_seqlen_kv = 0);
 
 // Padded layouts: zero the padding rows [cu_padded[r] + L_r, cu_padded[r+1]) of up
 // to three bf16 row-major tensors (row_bytes each; null to skip) and set those
@@ -63,6 +66,8 @@ struct FwdParams {
     float* lse;
     const int32_t* cu;
     const int32_t* rows;       // [nseg+1] first row of each segment (cu_padded, or cu if unpadded)
+    const int32_t* cu_kv;      // [nseg+1] key/value segments (== cu for self-attention)
+    const int32_t* rows_kv;    // [nseg+1] first key/value row of each segment (== rows for self-attention)
     const int4* items;
     const int32_t* seg_base;   // [nseg+1] item offsets of the sorted segments
     const int32_t* count;
@@ -71,6 +76,7 @@ struct FwdParams {
     const float2* table;       // RoPE cos/sin [rows][d/2], null if no RoPE
     int32_t nseg, total, H, d;
     int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
+    int32_t total_kv;          // key/value rows (== total for self-attention)
     float scale_log2;          // softmax_scale * log2(e)
     int use_rope;              // kRopeNone, kRopeHalf (rotate-half pairs) or kRopeInterleaved
 };
@@ -89,6 +95,8 @@ struct BwdParams {
     void* dv;
     const int32_t* cu;
     const int32_t* rows;       // [nseg+1] first row of each segment (cu_padded, or cu if unpadded)
+    const int32_t* cu_kv;      // [nseg+1] key/value segments (== cu for self-attention)
+    const int32_t* rows_kv;    // [nseg+1] first key/value row of each segment (== rows for self-attention)
     const int4* items;         // q-tile items (dQ pass), as in the forward
     const int32_t* seg_base;
     const int32_t* count;
@@ -101,9 +109,10 @@ struct BwdParams {
     const float2* table;
     float* delta;              // [H, total]: rowsum(dO * O)
     void* qrot;                // [total, H, d] bf16: R(p) q (workspace; only with RoPE)
-    void* krot;                // [total, Hkv, d] bf16: R(p) k
+    void* krot;                // [total_kv, Hkv, d] bf16: R(p) k
     int32_t nseg, total, H, d;
     int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
+    int32_t total_kv;          // key/value rows (== total for self-attention)
     float scale;
     int use_rope;              // kRopeHalf / kRopeInterleaved: inputs are rotated in the prep
                                // pass with that pairing, gradients un-rotated; kRopeNone: no RoPE

@@ -59,29 +59,42 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
                 int32_t BM, int32_t BN, int kind, int4* __restrict__ items, int64_t cap,
                 int32_t* __restrict__ order, int32_t* __restrict__ seg_base,
                 int32_t* __restrict__ count, int32_t* __restrict__ err,
-                const int32_t* __restrict__ cu_padded) {
+                const int32_t* __restrict__ cu_padded, const int32_t* __restrict__ cu_kv,
+                int32_t total_kv, int32_t max_seqlen_kv) {
     extern __shared__ int wl_smem[];
     int* hist = wl_smem;                    // [nbins] counts, then running positions
     __shared__ int warp_sums[33];
-    __shared__ int s_err, s_maxlen;
+    __shared__ int s_err, s_maxlen, s_maxlen_kv;
     const int tid = threadIdx.x;
     const int tile = (kind == VLC_WORKLIST_FWD) ? BM : BN;
-    const int nbins = (max_seqlen + tile - 1) / tile + 1;
+    // a segment's item count: its q tiles (forward) or key tiles (backward); keys and
+    // values have segments of their own when cu_kv is given (bottom-right aligned)
+    const int32_t* const ck = cu_kv != nullptr ? cu_kv : cu;
+    const int32_t* const cn = (kind == VLC_WORKLIST_FWD) ? cu : ck;
+    const int nbins = ((kind == VLC_WORKLIST_FWD || cu_kv == nullptr ? max_seqlen : max_seqlen_kv) + tile - 1) /
+                      tile + 1;
 
     if (tid == 0) {
         s_err = 0;
         s_maxlen = 0;
+        s_maxlen_kv = 0;
     }
     for (int b = tid; b < nbins; b += kWlThreads) hist[b] = 0;
     __syncthreads();
 
     // ---- 1. validate cu_seqlens
-    int local_err = 0, local_max = 0;
+    int local_err = 0, local_max = 0, local_max_kv = 0;
     for (int r = tid; r < nseg; r += kWlThreads) {
         int a = cu[r], b = cu[r + 1];
         if (r == 0 && a != 0) local_err |= VLC_DEVERR_CU_FIRST;
         if (b <= a) local_err |= VLC_DEVERR_CU_ORDER;
         local_max = max(local_max, b - a);
+        if (cu_kv != nullptr) {   // key segments start at 0 and are at least as long as the query ones
+            const int ka = cu_kv[r], kb = cu_kv[r + 1];
+            if (r == 0 && ka != 0) local_err |= VLC_DEVERR_CU_FIRST;
+            if (static_cast<int64_t>(kb) - ka < static_cast<int64_t>(b) - a) local_err |= VLC_DEVERR_QKV;
+            local_max_kv = max(local_max_kv, kb - ka);
+        }
         if (cu_padded != nullptr) {   // slot r holds segment r: it starts at 0 and is long enough
             const int pa = cu_padded[r], pb = cu_padded[r + 1];
             if ((r == 0 && pa != 0) || static_cast<int64_t>(pb) - pa < static_cast<int64_t>(b) - a)
@@ -91,11 +104,14 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
     if (tid == 0) {
         if (cu_padded == nullptr ? cu[nseg] != total : cu_padded[nseg] != total)
             local_err |= (cu_padded == nullptr ? VLC_DEVERR_CU_TOTAL : VLC_DEVERR_CU_PADDED);
+        if (cu_kv != nullptr && cu_kv[nseg] != total_kv) local_err |= VLC_DEVERR_CU_TOTAL;
     }
     if (local_err) atomicOr(&s_err, local_err);
     atomicMax(&s_maxlen, local_max);
+    atomicMax(&s_maxlen_kv, local_max_kv);
     __syncthreads();
     if (tid == 0 && s_maxlen != max_seqlen) s_err |= VLC_DEVERR_MAXLEN;
+    if (tid == 0 && cu_kv != nullptr && s_maxlen_kv != max_seqlen_kv) s_err |= VLC_DEVERR_MAXLEN;
     __syncthreads();
     if (s_err != 0) {
         if (tid == 0) {
@@ -107,7 +123,7 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
 
     // ---- 2. histogram of tile counts
     for (int r = tid; r < nseg; r += kWlThreads) {
-        int n = (cu[r + 1] - cu[r] + tile - 1) / tile;
+        int n = (cn[r + 1] - cn[r] + tile - 1) / tile;
         atomicAdd(&hist[n], 1);
     }
     __syncthreads();
@@ -144,7 +160,7 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
     for (int c0 = 0; c0 < nseg; c0 += kWlThreads) {
         const int r = c0 + tid;
         const bool valid = r < nseg;
-        const int n = valid ? (cu[r + 1] - cu[r] + tile - 1) / tile : -1;
+        const int n = valid ? (cn[r + 1] - cn[r] + tile - 1) / tile : -1;
         for (int w = 0; w < kWlThreads / 32; ++w) {
             if (warp == w) {
                 unsigned peers = __match_any_sync(0xffffffffu, n);
@@ -170,7 +186,7 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
         int n = 0;
         if (k < nseg) {
             int r = order[k];
-            n = (cu[r + 1] - cu[r] + tile - 1) / tile;
+            n = (cn[r + 1] - cn[r] + tile - 1) / tile;
         }
         int tot;
         int ex = block_excl_scan(n, warp_sums, &tot);
@@ -184,6 +200,8 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
     for (int k = tid; k < nseg; k += kWlThreads) {
         const int r = order[k];
         const int L = cu[r + 1] - cu[r];
+        const int Lk = ck[r + 1] - ck[r];
+        const int off = Lk - L;   // queries are the last L of the Lk positions
         const int base = seg_base[k];
         const int n = seg_base[k + 1] - base;
         for (int j = 0; j < n; ++j) {
@@ -191,14 +209,14 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
             it.x = r;
             if (kind == VLC_WORKLIST_FWD) {
                 const int qt = n - 1 - j;
-                const int last = min(L, (qt + 1) * BM);
+                const int last = min(Lk, min(L, (qt + 1) * BM) + off);   // keys the tile sees
                 it.y = qt;
                 it.z = 0;
                 it.w = (last + BN - 1) / BN;
             } else {
                 const int kt = j;
                 it.y = kt;
-                it.z = (kt * BN) / BM;
+                it.z = max(0, kt * BN - off) / BM;
                 it.w = (L + BM - 1) / BM;
             }
             if (base + j < cap) items[base + j] = it;
@@ -210,9 +228,11 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
 cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
                             int32_t BM, int32_t BN, int kind, int4* items, int64_t cap,
                             int32_t* order, int32_t* seg_base, int32_t* count, int32_t* err,
-                            cudaStream_t s, const int32_t* cu_padded) {
+                            cudaStream_t s, const int32_t* cu_padded, const int32_t* cu_kv,
+                            int32_t total_kv, int32_t max_seqlen_kv) {
     const int tile = (kind == VLC_WORKLIST_FWD) ? BM : BN;
-    const int nbins = (max_seqlen + tile - 1) / tile + 1;
+    const int nbins = ((kind == VLC_WORKLIST_FWD || cu_kv == nullptr ? max_seqlen : max_seqlen_kv) + tile - 1) /
+                      tile + 1;
     const size_t smem = sizeof(int) * static_cast<size_t>(nbins);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(worklist_kernel,
@@ -221,7 +241,8 @@ cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int3
         if (e != cudaSuccess) return e;
     }
     worklist_kernel<<<1, kWlThreads, smem, s>>>(cu, nseg, total, max_seqlen, BM, BN, kind, items,
-                                                cap, order, seg_base, count, err, cu_padded);
+                                                cap, order, seg_base, count, err, cu_padded, cu_kv,
+                                                total_kv, max_seqlen_kv);
     return cudaGetLastError();
 }
 
