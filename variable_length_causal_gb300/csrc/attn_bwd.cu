@@ -62,19 +62,12 @@ constexpr uint64_t kDrainNs = 200000000ull;
 // interleaved pairing, pairs 4c .. 4c+3 and D/4 + 4c .. D/4 + 4c+3 (columns 2j
 // and 2j+1).  A query of segment r sits at position p + Lk_r - L_r (bottom-right
 // alignment; 0 extra for self-attention), a key at its own index.
+// cs/sn[2e], [2e+1]: angles of the two pairs that the e-th 32-bit words of a
+// thread's lo and hi chunks take part in (rotate-half: the pairs at word e's two
+// columns; interleaved: word e of lo, word e of hi), at position pos.
 template <int D>
-__device__ __forceinline__ void rotate_row(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                           int64_t a0, int64_t a1, const float2* __restrict__ table,
-                                           int64_t pos, bool real, bool il, int c) {
-    if (!real) {   // padding rows: zeros, so every operand row stays finite
-        dst[a0] = make_uint4(0u, 0u, 0u, 0u);
-        dst[a1] = make_uint4(0u, 0u, 0u, 0u);
-        return;
-    }
-    // cs/sn[2e], [2e+1]: angles of the two pairs that the e-th words of the lo
-    // and hi chunks take part in (rotate-half: the pairs at word e's two
-    // columns; interleaved: word e of lo, word e of hi)
-    float cs[8], sn[8];
+__device__ __forceinline__ void load_angles(const float2* __restrict__ table, int64_t pos, bool il, int c,
+                                            float cs[8], float sn[8]) {
     if (!il) {
         const float4* t4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 8);
 #pragma unroll
@@ -91,6 +84,19 @@ __device__ __forceinline__ void rotate_row(const uint4* __restrict__ src, uint4*
             cs[4 * e2] = f.x; sn[4 * e2] = f.y; cs[4 * e2 + 1] = g.x; sn[4 * e2 + 1] = g.y;
             cs[4 * e2 + 2] = f.z; sn[4 * e2 + 2] = f.w; cs[4 * e2 + 3] = g.z; sn[4 * e2 + 3] = g.w;
         }
+    }
+}
+
+// Rotate chunks a0 (lo) and a1 (hi) of one row of src into dst with the angles of
+// load_angles; padding rows (real == false) become zeros, so every operand row
+// stays finite.
+__device__ __forceinline__ void rotate_chunks(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                              int64_t a0, int64_t a1, const float cs[8], const float sn[8],
+                                              bool real, bool il) {
+    if (!real) {
+        dst[a0] = make_uint4(0u, 0u, 0u, 0u);
+        dst[a1] = make_uint4(0u, 0u, 0u, 0u);
+        return;
     }
     const uint4 x4 = __ldg(src + a0), y4 = __ldg(src + a1);
     const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
@@ -124,7 +130,11 @@ __device__ __forceinline__ int segment_of_row(const int32_t* __restrict__ rows, 
     return a;
 }
 
-template <int D>
+// SEP == false (self-attention): the row (token, head hh) also rotates key row
+// (token, hh) when hh < Hkv, with the same position and angles.  SEP == true
+// (keys with segments of their own): key rows follow the query rows as a range
+// of their own.
+template <int D, bool SEP>
 __global__ void __launch_bounds__(256)
 prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const uint4* __restrict__ q,
             const uint4* __restrict__ k, uint4* __restrict__ qrot, uint4* __restrict__ krot,
@@ -137,7 +147,7 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
     constexpr int TPR = D / 16;        // threads per row
     constexpr int HALF = D / 16;       // uint4 chunks per half row
     const int64_t qrows = static_cast<int64_t>(total) * H;
-    const int64_t rows = qrows + (rope ? static_cast<int64_t>(total_kv) * Hkv : 0);
+    const int64_t rows = qrows + (SEP && rope ? static_cast<int64_t>(total_kv) * Hkv : 0);
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int c = threadIdx.x % TPR;
@@ -146,7 +156,7 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
     for (int64_t first = 0; first < rows; first += per_iter) {   // uniform trip count
         const int64_t row = first + gtid / TPR;
         float acc = 0.f;
-        if (row < qrows) {          // query row: D, and q' with RoPE
+        if (row < qrows) {          // query row: D, and q' (self-attention: and k') with RoPE
             const int64_t lo = row * (2 * HALF) + c, hi = lo + HALF;
             const uint4 g0 = __ldg(dout + lo), g1 = __ldg(dout + hi);
             const uint4 o0 = __ldg(o + lo), o1 = __ldg(o + hi);
@@ -161,17 +171,28 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
                 const int64_t L = __ldg(cu + a + 1) - __ldg(cu + a);
                 const int64_t pos0 = tok - __ldg(seg_rows + a);
                 const bool real = pos0 < L;   // rows past the length: padding (padded layouts)
-                const int64_t pos = real ? pos0 + (__ldg(cu_kv + a + 1) - __ldg(cu_kv + a)) - L : 0;
-                rotate_row<D>(q, qrot, lo, hi, table, pos, real, il, c);
+                const int64_t off = SEP ? (__ldg(cu_kv + a + 1) - __ldg(cu_kv + a)) - L : 0;
+                float cs[8], sn[8];
+                if (real) load_angles<D>(table, pos0 + off, il, c, cs, sn);
+                rotate_chunks(q, qrot, lo, hi, cs, sn, real, il);
+                if (!SEP) {
+                    const int64_t hh = row - tok * H;   // k has only Hkv heads
+                    if (hh < Hkv) {
+                        const int64_t klo = (tok * Hkv + hh) * (2 * HALF) + c;
+                        rotate_chunks(k, krot, klo, klo + HALF, cs, sn, real, il);
+                    }
+                }
             }
-        } else if (row < rows) {    // key row (RoPE only): k'
+        } else if (SEP && row < rows) {   // key row (RoPE only): k'
             const int64_t kr = row - qrows;
             const int64_t lo = kr * (2 * HALF) + c, hi = lo + HALF;
             const int64_t tok = kr / Hkv;
             const int a = segment_of_row(seg_rows_kv, nseg, tok);
             const int64_t pos0 = tok - __ldg(seg_rows_kv + a);
             const bool real = pos0 < __ldg(cu_kv + a + 1) - __ldg(cu_kv + a);
-            rotate_row<D>(k, krot, lo, hi, table, real ? pos0 : 0, real, il, c);
+            float cs[8], sn[8];
+            if (real) load_angles<D>(table, pos0, il, c, cs, sn);
+            rotate_chunks(k, krot, lo, hi, cs, sn, real, il);
         }
 #pragma unroll
         for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
@@ -324,7 +345,7 @@ __device__ __forceinline__ void stage_row_to_tmem(uint32_t tile, int r, int g, u
     }
 }
 
-template <int D>
+template <int D, bool KV>
 __global__ void __launch_bounds__(kThreads, 1)
 dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
           const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -395,7 +416,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_put(rg, n, p.next_q, nunits, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                const Unit w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
                 // the staging slot frees as soon as the math warps copied the last unit's rows to TMEM
                 if (!(ok = mbar_wait(bar(QD_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(QD_FULL), 2 * LY::TILE);
@@ -431,7 +452,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             for (int n = 0; ok; ++n) {
                 int u;
                 if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                const Unit w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
                 for (int j = 0; j < w.hi && ok; ++j) {
                     const uint32_t nn = kv + j;
                     const int vs = nn % kVStages;
@@ -499,7 +520,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                const Unit w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
                 if (!(ok = wait_warp(bar(QT_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_s(kv))) break;
                 if (!(ok = issue_dp(kv))) break;
@@ -560,13 +581,17 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         bool have = ok && u >= 0;
         Unit w{};
         if (have) {
-            w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+            w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
             ok = have = stage(0);
         }
         while (have) {
             const int qpos = w.tile * 128 + r;
             const bool valid = qpos < w.L;
             const int rpos = valid ? qpos + w.off : 0;   // RoPE position of the query
+            // last key this row sees; the mask applies from key tile j_edge on (the last
+            // tile, or the last two when the diagonal is not tile-aligned: off % BK != 0)
+            const int lastk = min(qpos + w.off, w.Lk - 1);
+            const int j_edge = w.hi - 1 - ((w.off & (BK - 1)) != 0 ? 1 : 0);
             const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? qpos : 0);
             const float lse2 = valid ? __ldg(p.lse + static_cast<int64_t>(w.h) * p.total + tok) * kLog2e : 0.f;
             const float dlt = valid ? __ldg(p.delta + static_cast<int64_t>(w.h) * p.total + tok) : 0.f;
@@ -580,10 +605,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(bar(S_EMPTY));
-                // diagonal step(s) and the segment tail: the last key tile, and the one before
-                // it when the diagonal is not tile-aligned (off % BK != 0)
-                const bool edge = (j == w.hi - 1) || (j == w.hi - 2 && (w.off & (BK - 1)) != 0);
-                const int lim = !valid ? -1 : (edge ? min(qpos + w.off, w.Lk - 1) - j * BK : BK - 1);
+                const bool edge = j >= j_edge;   // diagonal step(s) and the segment tail
+                const int lim = !valid ? -1 : (edge ? lastk - j * BK : BK - 1);
                 const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
                 uint32_t pp[32];
 #pragma unroll
@@ -626,7 +649,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             if (!(ok = ring_get_warp(rg, static_cast<int>(unit_it) + 1, abort, u2))) break;
             const bool have_next = u2 >= 0;
             if (have_next) {
-                w2 = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u2);
+                w2 = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u2);
                 if (!(ok = stage(unit_it + 1))) break;
             }
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
@@ -712,7 +735,7 @@ struct Layout {
     static constexpr uint32_t DPT_COL = 128, DV_COL = 256, DK_COL = 256 + D;
 };
 
-template <int D>
+template <int D, bool KV>
 __global__ void __launch_bounds__(kThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -783,7 +806,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_put(rg, n, p.next_k, nunits, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);   // w.h: key/value head
+                const Unit w = decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);   // w.h: key/value head
                 if (!(ok = mbar_wait(bar(KV_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(KV_FULL), 2 * LY::TILE);
                 const int krow = w.row0k + w.tile * 128;
@@ -858,7 +881,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
                 if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+                const Unit w = decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
                 if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_st(st))) break;
                 issue_dpt(st);
@@ -907,7 +930,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int n = 0; ok; ++n) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+            const Unit w = decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
             const int nq = w.hi - w.lo;
             for (int sq = 0; sq < grp * nq && ok; ++sq, ++st) {
                 const int i = w.lo + sq % nq, hq = w.h * grp + sq / nq;
@@ -944,7 +967,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int n = 0; ok; ++n, ++unit_it) {
             int u;
             if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+            const Unit w = decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
             const int kvpos = w.tile * 128 + r;
             const int nq = w.hi - w.lo;
             for (int sq = 0; sq < grp * nq; ++sq, ++st) {
@@ -1084,16 +1107,17 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
 template <int D>
 static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s) {
     {
+        const bool sep = p.cu_kv != p.cu;   // keys with segments of their own
         const int64_t rows = static_cast<int64_t>(p.total) * p.H +
-                             (p.use_rope ? static_cast<int64_t>(p.total_kv) * p.Hkv : 0);
+                             (sep && p.use_rope ? static_cast<int64_t>(p.total_kv) * p.Hkv : 0);
         int64_t blocks = (rows * (D / 16) + 255) / 256;
         if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
-        bwd::prep_kernel<D><<<static_cast<int>(blocks), 256, 0, s>>>(
+        auto prep = sep ? bwd::prep_kernel<D, true> : bwd::prep_kernel<D, false>;
+        prep<<<static_cast<int>(blocks), 256, 0, s>>>(
             static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.o),
             static_cast<const uint4*>(p.q), static_cast<const uint4*>(p.k), static_cast<uint4*>(p.qrot),
             static_cast<uint4*>(p.krot), p.delta, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.table, p.total, p.H,
-            p.Hkv, p.total_kv, p.use_rope,
-            p.err);
+            p.Hkv, p.total_kv, p.use_rope, p.err);
     }
     // with RoPE the attention passes read the rotated copies
     const void* qop = p.use_rope ? p.qrot : p.q;
@@ -1104,19 +1128,20 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
         !make_tmap_thd(&k128, kop, p.total_kv, p.Hkv, D, 128) ||
         !make_tmap_thd(&v128, p.v, p.total_kv, p.Hkv, D, 128))
         return cudaErrorInvalidValue;
+    const bool kv = p.cu_kv != p.cu;
     {
         constexpr uint32_t smem = bwd::dq::Layout<D>::ALLOC;
-        cudaError_t e = cudaFuncSetAttribute(bwd::dq::dq_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        auto kernel = kv ? bwd::dq::dq_kernel<D, true> : bwd::dq::dq_kernel<D, false>;
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        bwd::dq::dq_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
+        kernel<<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
     }
     {
         constexpr uint32_t smem = bwd::dkdv::Layout<D>::ALLOC;
-        cudaError_t e = cudaFuncSetAttribute(bwd::dkdv::dkdv_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        auto kernel = kv ? bwd::dkdv::dkdv_kernel<D, true> : bwd::dkdv::dkdv_kernel<D, false>;
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        bwd::dkdv::dkdv_kernel<D><<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
+        kernel<<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
     }
     return cudaGetLastError();
 }

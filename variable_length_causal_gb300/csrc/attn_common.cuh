@@ -20,7 +20,9 @@ struct Unit {
 // segment head-major, then the segment's items in work-list order.  The
 // segment's length comes from cu, its first row from rows (cu itself, or the
 // padded offsets of a layout with padding between segments); likewise for the
-// keys and values from cu_kv / rows_kv (the same arrays for self-attention).
+// keys and values from cu_kv / rows_kv.  KV == false is self-attention: the key
+// side equals the query side and is not loaded.
+template <bool KV>
 __device__ __forceinline__ Unit decode_unit(const int4* __restrict__ items,
                                             const int32_t* __restrict__ seg_base,
                                             const int32_t* __restrict__ cu,
@@ -45,9 +47,15 @@ __device__ __forceinline__ Unit decode_unit(const int4* __restrict__ items,
     w.hi = it.w;
     w.L = __ldg(cu + it.x + 1) - __ldg(cu + it.x);
     w.row0 = __ldg(rows + it.x);
-    w.Lk = __ldg(cu_kv + it.x + 1) - __ldg(cu_kv + it.x);
-    w.row0k = __ldg(rows_kv + it.x);
-    w.off = w.Lk - w.L;
+    if constexpr (KV) {
+        w.Lk = __ldg(cu_kv + it.x + 1) - __ldg(cu_kv + it.x);
+        w.row0k = __ldg(rows_kv + it.x);
+        w.off = w.Lk - w.L;
+    } else {
+        w.Lk = w.L;
+        w.row0k = w.row0;
+        w.off = 0;
+    }
     return w;
 }
 

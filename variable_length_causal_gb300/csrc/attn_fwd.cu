@@ -102,23 +102,30 @@ struct FUnit {
     int hkv;   // key/value head of query head w.h
 };
 
+template <bool KV>
 __device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
     FUnit f;
-    f.w = decode_unit(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+    f.w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
     const int T = (f.w.L + BQ - 1) / BQ;
     const int s = T & 1;
     const bool lone = (s != 0) && (f.w.tile == 0);
     f.has1 = !lone;
     f.q0 = lone ? 0 : 2 * f.w.tile - s;
-    const int nkt = (f.w.Lk + BN - 1) / BN;
-    f.n0 = min(nkt, ((f.q0 + 1) * BQ + f.w.off + BN - 1) / BN);
-    f.n1 = f.has1 ? min(nkt, ((f.q0 + 2) * BQ + f.w.off + BN - 1) / BN) : 0;
+    if constexpr (KV) {
+        const int nkt = (f.w.Lk + BN - 1) / BN;
+        f.n0 = min(nkt, ((f.q0 + 1) * BQ + f.w.off + BN - 1) / BN);
+        f.n1 = f.has1 ? min(nkt, ((f.q0 + 2) * BQ + f.w.off + BN - 1) / BN) : 0;
+    } else {
+        f.n0 = f.q0 + 1;
+        f.n1 = f.has1 ? f.q0 + 2 : 0;
+    }
     f.nk = f.has1 ? f.n1 : f.n0;
     f.hkv = p.Hkv == p.H ? f.w.h : f.w.h / (p.H / p.Hkv);
     return f;
 }
 
-template <int D>
+// KV: keys and values have segments of their own (bottom-right aligned queries).
+template <int D, bool KV>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -195,7 +202,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int n = 0; ok; ++n) {
                 int u;
                 if (!(ok = ring_put(rg, n, p.next, nunits, abort, u)) || u < 0) break;
-                const FUnit f = decode_funit(p, u);
+                const FUnit f = decode_funit<KV>(p, u);
                 for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
                     const int slot = qm % kQSlots;
                     if (!(ok = mbar_wait(bar(Q_EMPTY + slot), ((qm / kQSlots) & 1) ^ 1, abort))) break;
@@ -256,7 +263,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int un = 0; ok; ++un) {
                 int u;
                 if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
-                const FUnit f = decode_funit(p, u);
+                const FUnit f = decode_funit<KV>(p, u);
                 const int n[2] = {f.n0, f.n1};
                 const int slot[2] = {static_cast<int>(qm % kQSlots), static_cast<int>((qm + 1) % kQSlots)};
                 if (!(ok = wait_warp(bar(Q_READY + slot[0]), (qm / kQSlots) & 1, abort))) break;
@@ -333,7 +340,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int un = 0; ok; ++un) {
             int u;
             if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
-            const FUnit f = decode_funit(p, u);
+            const FUnit f = decode_funit<KV>(p, u);
             const int nt = t == 0 ? f.n0 : f.n1;
             if (nt == 0) continue;
             const int qpos = (f.q0 + t) * BQ + r;
@@ -344,7 +351,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tc_fence_after();
                 // allowed key columns of this tile: c <= lim.  Only the last tile is masked,
                 // or the last two when the diagonal is not tile-aligned (off % BN != 0)
-                const bool edge = (j == nt - 1) || (j == nt - 2 && (f.w.off & (BN - 1)) != 0);
+                const bool edge = (j == nt - 1) || (KV && j == nt - 2 && (f.w.off & (BN - 1)) != 0);
                 const int lim = edge ? min(qpos + f.w.off, f.w.Lk - 1) - j * BN : BN - 1;
                 // the thread's whole S row (BN fp32 columns) in registers: four loads, one wait
                 uint32_t s[BN];
@@ -465,7 +472,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int un = 0; ok; ++un) {
                 int u;
                 if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
-                const FUnit f = decode_funit(p, u);
+                const FUnit f = decode_funit<KV>(p, u);
                 for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
                     const int slot = qm % kQSlots;
                     if (!(ok = wait_warp(bar(Q_FULL + slot), (qm / kQSlots) & 1, abort))) break;
@@ -499,7 +506,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int un = 0; ok; ++un) {
                 int u;
                 if (!(ok = ring_get(rg, un, abort, u)) || u < 0) break;
-                const FUnit f = decode_funit(p, u);
+                const FUnit f = decode_funit<KV>(p, u);
                 for (int j = 0; j < f.nk && ok; ++j) {
                     const uint32_t n = vn + j;
                     const int vs = n & 1;
@@ -561,28 +568,21 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
         !make_tmap_thd(&tv, p.v, p.total_kv, p.Hkv, p.d, 128))
         return cudaErrorInvalidValue;
     const dim3 grid(num_sms), block(fwd::kThreads);
+    const bool kv = p.cu_kv != p.cu;
+    auto kernel = p.d == 128 ? (kv ? fwd::attn_fwd_kernel<128, true> : fwd::attn_fwd_kernel<128, false>)
+                             : (kv ? fwd::attn_fwd_kernel<64, true> : fwd::attn_fwd_kernel<64, false>);
+    const uint32_t smem = p.d == 128 ? fwd::Layout<128>::ALLOC : fwd::Layout<64>::ALLOC;
     // The warpgroups re-split the block's register pool at run time, which is only
     // valid if every thread is launched with exactly kLaunchRegs registers.
     {
         cudaFuncAttributes fa{};
-        cudaError_t e = p.d == 128 ? cudaFuncGetAttributes(&fa, fwd::attn_fwd_kernel<128>)
-                                   : cudaFuncGetAttributes(&fa, fwd::attn_fwd_kernel<64>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != static_cast<int>(fwd::kLaunchRegs)) return cudaErrorInvalidConfiguration;
     }
-    if (p.d == 128) {
-        constexpr uint32_t smem = fwd::Layout<128>::ALLOC;
-        cudaError_t e = cudaFuncSetAttribute(fwd::attn_fwd_kernel<128>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        fwd::attn_fwd_kernel<128><<<grid, block, smem, s>>>(tq, tk, tv, p);
-    } else {
-        constexpr uint32_t smem = fwd::Layout<64>::ALLOC;
-        cudaError_t e = cudaFuncSetAttribute(fwd::attn_fwd_kernel<64>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        fwd::attn_fwd_kernel<64><<<grid, block, smem, s>>>(tq, tk, tv, p);
-    }
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, block, smem, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
