@@ -454,24 +454,28 @@ def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
 
 
 def variant_measurements(vlc, w, dev, peaks, step):
-    """Forward and backward of the varlen variants on this workload's pack, same effective FLOPs
-    (4 d H pairs forward, 10 d H pairs backward over the real segments' legal pairs): the
-    interleaved RoPE pairing, grouped key/value heads (H / 4 of them), and a padded layout with
-    every segment's slot rounded up to a multiple of 64 rows."""
+    """Forward and backward of the varlen variants on this workload's pack (4 d H pairs forward,
+    10 d H pairs backward over the legal (query, key) pairs of the real segments): the
+    interleaved RoPE pairing, grouped key/value heads (H / 4 of them), a padded layout with every
+    segment's slot rounded up to a multiple of 64 rows (same pairs), and bottom-right aligned
+    queries that are the last quarter of each segment against all its keys (chunked prefill)."""
     pairs = synth.causal_pairs(w.real_lengths)
-    f_fl, b_fl = 4.0 * w.d * w.H * pairs, 10.0 * w.d * w.H * pairs
     mx = w.max_seqlen
 
-    def run(name, q, k, v, g, cu, **kw):
+    def run(name, q, k, v, g, cu, n_pairs=pairs, max_q=mx, **kw):
+        f_fl, b_fl = 4.0 * w.d * w.H * n_pairs, 10.0 * w.d * w.H * n_pairs
         o = torch.empty_like(q)
         lse = torch.empty((w.H, q.shape[0]), dtype=torch.float32, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        wsf = vlc.new_workspace(w.nseg, q.shape[0], w.H, w.d, mx, False, dev, k.shape[1])
-        wsb = vlc.new_workspace(w.nseg, q.shape[0], w.H, w.d, mx, True, dev, k.shape[1])
-        fwd = lambda: vlc.varlen_attn_fwd(q, k, v, cu, mx, out=o, lse=lse, workspace=wsf, check=False, **kw)
+        kvw = {}
+        if "cu_seqlens_kv" in kw:
+            kvw = {"total_kv": k.shape[0], "max_seqlen_kv": kw["max_seqlen_kv"]}
+        wsf = vlc.new_workspace(w.nseg, q.shape[0], w.H, w.d, max_q, False, dev, k.shape[1], **kvw)
+        wsb = vlc.new_workspace(w.nseg, q.shape[0], w.H, w.d, max_q, True, dev, k.shape[1], **kvw)
+        fwd = lambda: vlc.varlen_attn_fwd(q, k, v, cu, max_q, out=o, lse=lse, workspace=wsf, check=False, **kw)
         fwd()
         vlc.get_error(wsf)
-        bwd = lambda: vlc.varlen_attn_bwd(g, q, k, v, o, lse, cu, mx, dq=dq, dk=dk, dv=dv, workspace=wsb,
+        bwd = lambda: vlc.varlen_attn_bwd(g, q, k, v, o, lse, cu, max_q, dq=dq, dk=dk, dv=dv, workspace=wsb,
                                           check=False, **kw)
         ms_f, ms_b = _time_ms(fwd, 5), _time_ms(bwd, 5)
         for ws in (wsf, wsb):
@@ -500,6 +504,20 @@ def variant_measurements(vlc, w, dev, peaks, step):
     r["padding_rows"] = int(cp[-1] - w.total)
     res["padded_slots_x64"] = r
     del padded
+    # chunked prefill: the last quarter of each real segment's tokens as queries
+    real = w.seg_ignore == 0
+    lq = np.maximum(1, lens // 4)
+    qidx = torch.from_numpy(np.concatenate([np.arange(b - n, b) for b, n in zip(w.cu[1:], lq)])).to(dev)
+    off = (lens - lq)[real]
+    lqr = lq[real]
+    qk_pairs = int(np.sum(lqr * (off + 1) + lqr * (lqr - 1) // 2))
+    cuq = torch.from_numpy(np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)).to(dev)
+    qq, gq = step.q[qidx].contiguous(), step.g[qidx].contiguous()
+    r = run("qkv", qq, step.k, step.v, gq, cuq, n_pairs=qk_pairs, max_q=int(lq.max()),
+            cu_seqlens_kv=step.cu, max_seqlen_kv=mx)
+    r["query_rows"] = int(lq.sum())
+    res["qkv_last_quarter"] = r
+    del qq, gq
     return res
 
 
