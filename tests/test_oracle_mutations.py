@@ -37,6 +37,11 @@ MUTATIONS = {
     "rope_interleaved_pairing": ("if (interleaved) { *ia = 2 * j; *ib = 2 * j + 1; }",
                                  "if (interleaved) { *ia = j; *ib = j + 1; }"),
     "padded_rows_from_cu": ("for p, n in zip(cp[:-1], L)", "for p, n in zip(cu[:-1], L)", "__init__.py"),
+    "ffd_ascending": ("order = sorted(range(len(sizes)), key=lambda i: (-sizes[i], i))",
+                      "order = sorted(range(len(sizes)), key=lambda i: (sizes[i], i))", "packing.py"),
+    "ffd_room_off_by_one": ("if room[b] >= s:", "if room[b] > s:", "packing.py"),
+    "lpt_fullest_rank": ("r = min(range(ranks), key=lambda k: (load[k], k))",
+                         "r = max(range(ranks), key=lambda k: (load[k], k))", "packing.py"),
     "gqa_interleaved_heads": ("static int32_t kv_head(const orc_problem* P, int32_t h) { return h / (P->H / P->Hkv); }",
                               "static int32_t kv_head(const orc_problem* P, int32_t h) { return h % P->Hkv; }"),
     "ce_label_logit_sign": ("row[i] = (mx + log(s)) - zy;", "row[i] = (mx + log(s)) + zy;"),

@@ -760,3 +760,92 @@ def test_qkv_rows_sampler_matches_the_full_forward():
     rows, heads = np.arange(int(cu[-1])), np.arange(int(cu[-1])) % 2
     o_r, lse_r = oracle.attn_fwd_rows(q, k, v, cu, rows, heads, cu_kv=cuk)
     assert np.array_equal(o_r, o[rows, heads]) and np.array_equal(lse_r, lse[heads, rows])
+
+
+# ------------------------------------------------------------------ host packing (oracle/packing.py)
+from oracle import packing  # noqa: E402
+
+
+@pytest.mark.parametrize("name", ["table_4_1_example_A", "table_4_1_example_B"])
+def test_ffd_reaches_the_pages_lower_bound_examples(name):
+    # the worked examples of "Long-context training: remove padding": ceil(T/L) = 2 windows,
+    # and the printed padding / saved slot numbers follow from the windows FFD builds
+    g = _golden("ledgers.json")[name]
+    L, lens = g["L"], g["lengths"]
+    bin_of, order, bin_start = packing.ffd(lens, L)
+    nbins = len(bin_start) - 1
+    assert nbins == g["packs"] == math.ceil(g["T"] / L)
+    assert nbins * L == g["packed"]
+    assert nbins * L - sum(lens) == g["pack_padding"]
+    assert g["fixed"] - nbins * L == g["saved"]
+    assert round(100 * (1 - packing.eta(lens, nbins, L)), 1) == round(100 * g["pack_padding"] / g["packed"], 1)
+    fills = packing.pack_costs(lens, order, bin_start, "tokens")
+    assert fills.max() <= L and sorted(order.tolist()) == list(range(len(lens)))
+
+
+def test_ffd_on_example_b_by_hand():
+    # 1024 opens window 0, 768 joins it (256 left), 512 opens window 1, 256 fills window 0,
+    # 96 joins window 1
+    _, order, bin_start = packing.ffd([1024, 768, 512, 256, 96], 2048)
+    assert [order[bin_start[b]:bin_start[b + 1]].tolist() for b in range(2)] == [[0, 1, 3], [2, 4]]
+
+
+def test_packers_against_exhaustive_optimum():
+    # textbook bounds against the exhaustive optimum OPT: ceil(T/L) <= OPT <= FFD <= 11/9 OPT + 6/9,
+    # first-fit <= 1.7 OPT (+1 slack for small cases), next-fit <= 2 OPT
+    rng = np.random.default_rng(0)
+    worst_ffd = 0.0
+    for _ in range(60):
+        n = int(rng.integers(3, 8))
+        cap = int(rng.integers(10, 21))
+        lens = [int(x) for x in rng.integers(1, cap + 1, size=n)]
+        opt = packing.brute_min_bins(lens, cap)
+        assert math.ceil(sum(lens) / cap) <= opt
+        nb = {f.__name__: len(f(lens, cap)[2]) - 1 for f in (packing.ffd, packing.first_fit, packing.next_fit)}
+        assert opt <= nb["ffd"] <= math.floor(11 * opt / 9 + 6 / 9)
+        assert opt <= nb["first_fit"] <= math.floor(1.7 * opt) + 1
+        assert opt <= nb["next_fit"] <= 2 * opt
+        worst_ffd = max(worst_ffd, nb["ffd"] / opt)
+    # a family where first-fit in arrival order (small items first) is poor and FFD optimal
+    lens = [2, 2, 2, 7, 7, 7]
+    assert len(packing.ffd(lens, 9)[2]) - 1 == packing.brute_min_bins(lens, 9) == 3
+    assert len(packing.first_fit(lens, 9)[2]) - 1 == 4
+
+
+def test_oversize_samples_get_a_window_of_their_own():
+    lens = [10, 3, 25, 4, 12]
+    bin_of, order, bin_start = packing.ffd(lens, 12, extra=1)   # 25 + 1 and 12 + 1 exceed 12
+    assert packing.oversize_count(lens, 12, extra=1) == 2
+    for i in (2, 4):
+        w = bin_of[i]
+        assert bin_start[w + 1] - bin_start[w] == 1
+    sizes = np.asarray(lens) + 1
+    for b in range(len(bin_start) - 1):
+        members = order[bin_start[b]:bin_start[b + 1]]
+        assert len(members) == 1 or sizes[members].sum() <= 12
+
+
+def test_lpt_against_exhaustive_makespan():
+    # Graham's bound for longest-processing-time: LPT <= (4/3 - 1/(3R)) OPT
+    rng = np.random.default_rng(1)
+    for _ in range(60):
+        R = int(rng.integers(2, 4))
+        costs = [int(x) for x in rng.integers(1, 50, size=int(rng.integers(R, 8)))]
+        rank_of, load = packing.lpt(costs, R)
+        assert np.array_equal(np.bincount(rank_of, weights=costs, minlength=R).astype(np.int64), load)
+        opt = packing.brute_min_makespan(costs, R)
+        assert opt <= load.max() <= (4 / 3 - 1 / (3 * R)) * opt + 1e-9
+
+
+def test_sum_of_squares_balance_beats_token_balance():
+    # charlestar's point: equal token counts can hide unequal attention work; two ranks, one
+    # pack of a single 4096-token document and four packs of 1024 short ones (4096 tokens each)
+    lens = [4096] + [256] * 64
+    bin_of, order, bin_start = packing.ffd(lens, 4096)
+    tok = packing.pack_costs(lens, order, bin_start, "tokens")
+    sq = packing.pack_costs(lens, order, bin_start, "sumsq")
+    assert len(tok) == 5 and np.all(tok == 4096)
+    by_tok, _ = packing.lpt(tok, 2)
+    by_sq, load_sq = packing.lpt(sq, 2)
+    work_tok = np.bincount(by_tok, weights=sq, minlength=2)
+    assert load_sq.max() == 4096 ** 2 and load_sq.max() < work_tok.max()
