@@ -430,6 +430,7 @@ def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
                                     "frac_hbm": ce_bytes / (ms_ce * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     del logits, ws_ce
     out["varlen_variants"] = variant_measurements(vlc, w, dev, peaks, step)
+    out["host_packer"] = packer_measurement(vlc)
     if w.name == "long":
         cu1 = torch.tensor([0, w.total], dtype=torch.int32, device=dev)
         o1 = torch.empty_like(q)
@@ -451,6 +452,24 @@ def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
         }
         del o1, lse1, ws1
     return out
+
+
+def packer_measurement(vlc, n: int = 10_000_000, capacity: int = 4096, ranks: int = 8):
+    """Host packer on n samples of the SFT length mix (lognormal median 300, sigma 1.0, clipped to
+    [16, capacity - 1], one reserved token each): first-fit decreasing into windows, then the
+    windows to ranks by sum of squared lengths.  Host code, one thread: samples/s, not a roofline."""
+    rng = np.random.default_rng(77)
+    L = np.clip(np.round(rng.lognormal(np.log(300), 1.0, size=n)), 16, capacity - 1).astype(np.int32)
+    t0 = time.perf_counter()
+    p = vlc.pack(L, capacity, extra=1)
+    t1 = time.perf_counter()
+    _, load = vlc.shard_packs(L, p, ranks)
+    t2 = time.perf_counter()
+    nf = vlc.pack(L, capacity, extra=1, mode="next_fit")
+    return {"samples": n, "capacity": capacity, "pack_ms": (t1 - t0) * 1e3,
+            "samples_per_s": n / (t1 - t0), "windows": p.nbins, "eta": p.eta,
+            "eta_next_fit": nf.eta, "shard_ms": (t2 - t1) * 1e3, "ranks": ranks,
+            "sumsq_load_max_over_min": float(load.max() / load.min())}
 
 
 def variant_measurements(vlc, w, dev, peaks, step):

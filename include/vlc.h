@@ -246,6 +246,52 @@ int vlc_attn_bwd_qkv(const void* dout, const void* q, const void* k, const void*
                      int32_t max_seqlen_q, int32_t max_seqlen_kv, float softmax_scale, float rope_theta,
                      uint32_t flags, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- host packing
+ * The data step in front of the path; plain host functions (no device, no
+ * stream), deterministic (ties go to the smaller index).
+ *
+ * vlc_pack: windows of `capacity` tokens from samples of lengths[i] >= 1 tokens,
+ * each occupying lengths[i] + extra (the BOS/EOS reserve that "Packing document
+ * boundary" (operatorworld, practical checklist) asks first-fit decreasing to
+ * keep).  mode ("Sequence Packing", llm-compass, section on binning):
+ *   VLC_PACK_FFD        sort by size, largest first, then first fit
+ *   VLC_PACK_FIRST_FIT  first fit in the given order (Megatron's dp_balanced
+ *                       order, as "Long-context training: remove padding"
+ *                       describes it)
+ *   VLC_PACK_NEXT_FIT   streaming: the current window, else a new one
+ * A sample larger than a window is not cut (the same page: over-long samples
+ * are reported, not truncated): it gets a window of its own and is counted in
+ * *oversize_out.  Outputs (caller-owned host arrays):
+ *   bin_of     int32 [n]    window of sample i (windows numbered as opened)
+ *   order      int64 [n]    samples grouped by window, each window's samples in
+ *                           placement order (its cu_seqlens are their prefix sums)
+ *   bin_start  int64 [n+1]  window w holds order[bin_start[w] .. bin_start[w+1])
+ *   *nbins_out, *oversize_out (oversize_out may be NULL)
+ * The window count over capacity gives the nominal tokens; sum(lengths) /
+ * (nbins * capacity) is eta, the effective share the checklist monitors.
+ * Returns VLC_ERR_ARG for a null pointer, n < 1, capacity < 1, extra < 0, a
+ * length < 1 or an unknown mode. */
+#define VLC_PACK_FFD 0
+#define VLC_PACK_FIRST_FIT 1
+#define VLC_PACK_NEXT_FIT 2
+int vlc_pack(const int32_t* lengths, int64_t n, int32_t capacity, int32_t extra, int mode, int32_t* bin_of,
+             int64_t* order, int64_t* bin_start, int64_t* nbins_out, int64_t* oversize_out);
+
+/* vlc_shard_packs: windows to `ranks` data-parallel ranks by their attention
+ * work ("Sequence packing and variable-length attention", charlestar: equal
+ * token counts can hide unequal sum(L_r^2); balance that).  A window's cost is
+ * the sum of its samples' lengths (VLC_COST_TOKENS) or of their squares
+ * (VLC_COST_SUMSQ); windows by cost, largest first, each to the rank with the
+ * least load so far (longest-processing-time greedy).  order / bin_start as
+ * written by vlc_pack.  Outputs: rank_of_bin int32 [nbins], rank_load int64
+ * [ranks].  Every rank that runs it on the same inputs gets the same answer, so
+ * the ranks split the packs without exchanging anything.  VLC_ERR_UNSUPPORTED
+ * if a load overflows int64. */
+#define VLC_COST_TOKENS 0
+#define VLC_COST_SUMSQ 1
+int vlc_shard_packs(const int32_t* lengths, const int64_t* order, const int64_t* bin_start, int64_t nbins,
+                    int32_t ranks, int cost_kind, int32_t* rank_of_bin, int64_t* rank_load);
+
 /* Forward attention for callers that cannot allocate device memory.  No
  * counterpart on the pages: it exists for callers that may not obtain memory
  * per call, such as code running inside another runtime's execution hook (a

@@ -59,3 +59,42 @@ def test_pack_assignment_by_quadratic_cost_across_ranks():
     loads = [sum(costs[i] for i in p) for p in parts]
     assert sorted(sum(parts, [])) == list(range(32))
     assert max(loads) / min(loads) < 1.25
+
+
+def _shard_worker(rank, world, port, out):
+    # every rank packs the same seeded length draw and shards the windows on its own;
+    # the only exchange is this test's check that the shares agree
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import numpy as np
+    import torch.distributed as dist
+
+    import variable_length_causal_gb300 as vlc
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    rng = np.random.default_rng(2024)
+    L = np.clip(np.round(rng.lognormal(np.log(400), 0.8, size=20000)), 32, 4095).astype(np.int32)
+    p = vlc.pack(L, 4096, extra=1)
+    rank_of, load = vlc.shard_packs(L, p, world)
+    mine = np.nonzero(rank_of == rank)[0]
+    sq = sum(int((L[p.order[p.bin_start[b]:p.bin_start[b + 1]]].astype(np.int64) ** 2).sum()) for b in mine)
+    gathered = [None] * world
+    dist.all_gather_object(gathered, (mine.tolist(), sq, load.tolist(), p.nbins))
+    out[rank] = gathered
+    dist.destroy_process_group()
+
+
+def test_ranks_shard_packs_consistently_without_exchange():
+    world = 2
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_shard_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+    for r in range(world):
+        g = out[r]
+        nbins = g[0][3]
+        owned = sorted(sum((x[0] for x in g), []))
+        assert owned == list(range(nbins))                   # every window on exactly one rank
+        assert all(x[2] == g[0][2] for x in g)               # every rank computed the same loads
+        assert [x[1] for x in g] == g[0][2]                  # a rank's load is its windows' sum L^2
+    assert out[0] == out[1]

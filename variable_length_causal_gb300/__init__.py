@@ -4,15 +4,20 @@ The compute path is the C-ABI library ``lib/libvlc.so`` (CUDA kernels for
 sm_103a, declared in ``include/vlc.h``); ``binding`` marshals torch tensors to
 it.  ``synth`` draws the seeded synthetic workloads used by tests and bench.
 ``shifted_cross_entropy`` is the next step after attention on the pages'
-pipeline: loss sum and target count over the pre-shifted labels.
+pipeline: loss sum and target count over the pre-shifted labels; ``pack`` and
+``shard_packs`` are the host step before it (windows by first-fit decreasing,
+windows to ranks by sum of squared lengths).
 """
 from .binding import (  # noqa: F401
+    Packing,
     VlcError,
     build_positions_labels,
     build_worklist,
     get_error,
     load_library,
     new_workspace,
+    pack,
+    shard_packs,
     shifted_cross_entropy,
     varlen_attn_bwd,
     varlen_attn_fwd,

@@ -11,8 +11,9 @@ import ctypes
 import math
 import os
 import threading
-from typing import Optional, Tuple
+from typing import NamedTuple, Optional, Tuple
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -24,6 +25,8 @@ DEVERR_CU_FIRST, DEVERR_CU_ORDER, DEVERR_CU_TOTAL, DEVERR_MAXLEN = 0x1, 0x2, 0x4
 DEVERR_TIMEOUT = 0x100
 DEVERR_LABEL, DEVERR_CU_PADDED, DEVERR_QKV = 0x10, 0x20, 0x40
 WORKLIST_FWD, WORKLIST_BWD = 0, 1
+PACK_MODES = {"ffd": 0, "first_fit": 1, "next_fit": 2}
+COST_KINDS = {"tokens": 0, "sumsq": 1}
 ROPE_INTERLEAVED = 0x1
 
 EXPORTED = [
@@ -31,7 +34,8 @@ EXPORTED = [
     "vlc_build_positions_labels", "vlc_build_worklist", "vlc_attn_fwd", "vlc_attn_bwd",
     "vlc_get_error", "vlc_attn_fwd_noalloc", "vlc_ce_workspace_bytes", "vlc_shifted_ce",
     "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa", "vlc_attn_fwd_ex",
-    "vlc_attn_bwd_ex", "vlc_workspace_bytes_qkv", "vlc_attn_fwd_qkv", "vlc_attn_bwd_qkv",
+    "vlc_attn_bwd_ex", "vlc_workspace_bytes_qkv", "vlc_attn_fwd_qkv", "vlc_attn_bwd_qkv", "vlc_pack",
+    "vlc_shard_packs",
 ]
 
 _lock = threading.Lock()
@@ -107,6 +111,10 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_attn_bwd_qkv.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                          f32, f32, u32, P, P, P, P, sz, P]
         lib.vlc_attn_bwd_qkv.restype = cint
+        lib.vlc_pack.argtypes = [P, i64, i32, i32, cint, P, P, P, P, P]
+        lib.vlc_pack.restype = cint
+        lib.vlc_shard_packs.argtypes = [P, P, P, i64, i32, cint, P, P]
+        lib.vlc_shard_packs.restype = cint
         _lib = lib
         return lib
 
@@ -379,3 +387,59 @@ def shifted_cross_entropy(logits: torch.Tensor, labels: torch.Tensor,
     if check:
         _raise_device_error(ws, "vlc_shifted_ce")
     return (loss, count, seg_loss, seg_count) if per_segment else (loss, count)
+
+
+class Packing(NamedTuple):
+    """Windows built by ``pack``: ``order[bin_start[w]:bin_start[w+1]]`` are window w's samples."""
+    bin_of: np.ndarray      # int32 [n]
+    order: np.ndarray       # int64 [n]
+    bin_start: np.ndarray   # int64 [nbins + 1]
+    nbins: int
+    oversize: int
+    capacity: int
+    eta: float              # sum(lengths) / (nbins * capacity)
+
+    def cu_seqlens(self, lengths, w: int) -> np.ndarray:
+        """int32 cu_seqlens of window w (its samples in placement order)."""
+        L = np.asarray(lengths, np.int64)[self.order[self.bin_start[w]:self.bin_start[w + 1]]]
+        return np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+
+
+def _host_i32(x) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(x), dtype=np.int32)
+    if a.ndim != 1:
+        raise ValueError("lengths must be 1-D")
+    return a
+
+
+def pack(lengths, capacity: int, extra: int = 0, mode: str = "ffd") -> Packing:
+    """Pack samples into windows of ``capacity`` tokens (host; see vlc_pack)."""
+    lib = load_library()
+    L = _host_i32(lengths)
+    n = L.shape[0]
+    bin_of = np.empty(n, np.int32)
+    order = np.empty(n, np.int64)
+    bin_start = np.empty(n + 1, np.int64)
+    nb, ov = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = lib.vlc_pack(L.ctypes.data_as(ctypes.c_void_p), n, int(capacity), int(extra), PACK_MODES[mode],
+                      bin_of.ctypes.data_as(ctypes.c_void_p), order.ctypes.data_as(ctypes.c_void_p),
+                      bin_start.ctypes.data_as(ctypes.c_void_p), ctypes.byref(nb), ctypes.byref(ov))
+    _check(st, "vlc_pack")
+    nbins = int(nb.value)
+    return Packing(bin_of, order, bin_start[:nbins + 1].copy(), nbins, int(ov.value), int(capacity),
+                   float(L.astype(np.int64).sum()) / float(nbins * int(capacity)))
+
+
+def shard_packs(lengths, packing: Packing, ranks: int, cost: str = "sumsq"):
+    """Windows to ranks by attention work (host; see vlc_shard_packs): (rank_of_bin, rank_load)."""
+    lib = load_library()
+    L = _host_i32(lengths)
+    order = np.ascontiguousarray(packing.order, np.int64)
+    bs = np.ascontiguousarray(packing.bin_start, np.int64)
+    rank_of = np.empty(packing.nbins, np.int32)
+    load = np.empty(int(ranks), np.int64)
+    st = lib.vlc_shard_packs(L.ctypes.data_as(ctypes.c_void_p), order.ctypes.data_as(ctypes.c_void_p),
+                             bs.ctypes.data_as(ctypes.c_void_p), packing.nbins, int(ranks), COST_KINDS[cost],
+                             rank_of.ctypes.data_as(ctypes.c_void_p), load.ctypes.data_as(ctypes.c_void_p))
+    _check(st, "vlc_shard_packs")
+    return rank_of, load

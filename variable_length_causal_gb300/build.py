@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libvlc.so")
-SOURCES = ["api.cu", "prep.cu", "attn_fwd.cu", "attn_bwd.cu", "noalloc.cu", "ce.cu"]
+SOURCES = ["api.cu", "prep.cu", "attn_fwd.cu", "attn_bwd.cu", "noalloc.cu", "ce.cu", "packer.cpp"]
 HEADERS = ["ptx.cuh", "internal.h", "attn_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -45,7 +45,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     def compile_one(src):
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         if force or _stale(o, [s] + hdrs):
             cmd = [nvcc, *ARCH, *FLAGS, "-c", s, "-o", o]
             if verbose:
