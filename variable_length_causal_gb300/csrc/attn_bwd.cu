@@ -886,6 +886,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 if (!(ok = issue_st(st))) break;
                 issue_dpt(st);
                 const int nsteps = grp * (w.hi - w.lo);
+                // K and V are read only by S^T and dP^T: once the last step's pair is issued
+                // the tiles go back to the producer, which loads the next unit's K/V under the
+                // rest of this unit (its last P^T / dS^T, dV and dK MMAs and the epilogue)
+                if (nsteps == 1) commit(bar(KV_EMPTY));
                 for (int sq = 0; sq < nsteps; ++sq, ++st) {
                     const int s = st % kQStages;
                     const uint64_t qdm = smem_desc_sw128(sbase + LY::Q0 + s * LY::TILE, LY::BLK, 1024);
@@ -913,11 +917,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                         mma_commit(bar(QO_EMPTY + s));
                     }
                     __syncwarp();
-                    if (sq + 1 < nsteps) issue_dpt(st + 1);
+                    if (sq + 1 < nsteps) {
+                        issue_dpt(st + 1);
+                        if (sq + 2 == nsteps) commit(bar(KV_EMPTY));
+                    }
                 }
                 if (!ok) break;
                 commit(bar(ACC_FULL));
-                commit(bar(KV_EMPTY));
             }
             commit(bar(DRAIN));
             mbar_wait_limit(bar(DRAIN), 0, kDrainNs);
