@@ -45,8 +45,10 @@ WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t 
     off = align256(off + sizeof(int32_t) * static_cast<size_t>(nseg + 1) * (is_bwd ? 2 : 1));
     L.table = off;
     off = align256(off + sizeof(float2) * static_cast<size_t>(L.table_rows) * (d / 2));
-    L.delta = L.qrot = L.krot = off;
+    L.table2 = L.delta = L.qrot = L.krot = off;
     if (is_bwd) {
+        L.table2 = off;
+        off = align256(off + sizeof(float2) * static_cast<size_t>(L.table_rows) * (d / 2));
         L.delta = off;
         off = align256(off + sizeof(float) * static_cast<size_t>(H) * total);
         L.qrot = off;
@@ -249,8 +251,9 @@ static int attn_bwd_impl(AttnArgs a) {
                         num_sms_cached(), s) != cudaSuccess)
         return VLC_ERR_CUDA;
     const int mode = rope_mode(a.rope_theta, a.flags);
+    float2* table2 = reinterpret_cast<float2*>(w + L.table2);
     if (mode != kRopeNone && launch_rope_table(table, L.table_rows, a.d, static_cast<double>(a.rope_theta),
-                                               &hdr->err, s) != cudaSuccess)
+                                               &hdr->err, s, table2) != cudaSuccess)
         return VLC_ERR_CUDA;
     BwdParams p{};
     p.dout = a.dout; p.q = a.q; p.k = a.k; p.v = a.v; p.o = a.o_in; p.lse = a.lse_in;
@@ -263,6 +266,8 @@ static int attn_bwd_impl(AttnArgs a) {
     p.next_q = &hdr->next[1];
     p.next_k = &hdr->next[2];
     p.table = mode != kRopeNone ? table : nullptr;
+    p.table2 = mode != kRopeNone ? table2 : nullptr;
+    p.table_rows = L.table_rows;
     p.delta = reinterpret_cast<float*>(w + L.delta);
     p.qrot = w + L.qrot;
     p.krot = w + L.krot;

@@ -205,71 +205,83 @@ prep_kernel(const uint4* __restrict__ dout, const uint4* __restrict__ o, const u
 
 // Apply scale and R(p)^T to one row of fp32 gradients held in TMEM columns
 // [col0, col0 + D) of this thread's lane, and store it as bf16.  IL selects the
-// interleaved pairing (columns 2j, 2j+1), else rotate-half (j, j + D/2).
+// interleaved pairing (columns 2j, 2j+1), else rotate-half (j, j + D/2).  The two
+// math warpgroups share a row: `part` (0 or 1) takes half of the rotation pairs.
+// The cos/sin come from the blocked table (tab2[j/4][pos][j%4], tab_rows
+// positions): with one row per thread and consecutive rows at consecutive
+// positions, each 32-byte load of a warp covers 32 consecutive pieces; a
+// sub-chunk's loads are issued before its TMEM loads.  v8: row_out is 32-byte
+// aligned (256-bit stores).
 template <int D, bool IL>
-__device__ __forceinline__ void store_unrotated(uint32_t taddr, const float2* __restrict__ table,
+__device__ __forceinline__ void store_unrotated(uint32_t taddr, const float2* __restrict__ tab2, int tab_rows,
                                                 int pos, float scale, bool rope, bool valid,
-                                                uint8_t* __restrict__ row_out) {
+                                                uint8_t* __restrict__ row_out, bool v8, int part) {
     constexpr int half = D / 2;
+    const float2* trow = rope ? tab2 + static_cast<int64_t>(pos) * 4 : nullptr;
+    const int64_t jstride = static_cast<int64_t>(tab_rows) * 4;   // float2 per group of 4 frequencies
     if constexpr (IL) {
+        // 16-column sub-chunks (8 pairs: two table loads); this part's half of the columns
 #pragma unroll
-        for (int a = 0; a < D / 32; ++a) {
-            uint32_t r[32];
-            tmem_ld32(taddr + a * 32, r);
+        for (int b = 0; b < D / 32; ++b) {
+            const int cb = part * (D / 2) + b * 16;   // first column
+            float tb[2][8];
+            if (rope) {
+                ld_nc_v8(trow + (cb / 8) * jstride, tb[0]);
+                ld_nc_v8(trow + (cb / 8 + 1) * jstride, tb[1]);
+            }
+            uint32_t r[16];
+            tmem_ld16(taddr + cb, r);
             tmem_wait_ld();
-            uint32_t pk[16];
+            uint32_t pk[8];
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {   // columns a*32+e .. +3: pairs a*16 + e/2, +1
-                float x0 = __uint_as_float(r[e]) * scale, y0 = __uint_as_float(r[e + 1]) * scale;
-                float x1 = __uint_as_float(r[e + 2]) * scale, y1 = __uint_as_float(r[e + 3]) * scale;
+            for (int q = 0; q < 8; ++q) {   // pair cb/2 + q at columns cb + 2q, cb + 2q + 1
+                float x = __uint_as_float(r[2 * q]) * scale, y = __uint_as_float(r[2 * q + 1]) * scale;
                 if (rope) {
-                    const float4 cs = __ldg(reinterpret_cast<const float4*>(
-                        table + static_cast<int64_t>(pos) * half + a * 16 + e / 2));
-                    const float u0 = x0 * cs.x + y0 * cs.y, v0 = y0 * cs.x - x0 * cs.y;
-                    const float u1 = x1 * cs.z + y1 * cs.w, v1 = y1 * cs.z - x1 * cs.w;
-                    x0 = u0; y0 = v0; x1 = u1; y1 = v1;
+                    const float c = tb[q >> 2][2 * (q & 3)], s = tb[q >> 2][2 * (q & 3) + 1];
+                    const float u = x * c + y * s, w = y * c - x * s;
+                    x = u; y = w;
                 }
-                pk[e / 2] = pack_bf16x2(x0, y0);
-                pk[e / 2 + 1] = pack_bf16x2(x1, y1);
+                pk[q] = pack_bf16x2(x, y);
             }
-            if (valid) {
-                uint4* dst = reinterpret_cast<uint4*>(row_out + a * 64);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
+            if (valid) st_row32(row_out + cb * 2, pk, v8);
         }
         return;
     }
+    // rotate-half: 16-pair sub-chunks (four table loads), pairs [part*half/2, +half/2)
 #pragma unroll
-    for (int a = 0; a < half / 32; ++a) {
-        uint32_t lo[32], hi[32];
-        tmem_ld32(taddr + a * 32, lo);
-        tmem_ld32(taddr + half + a * 32, hi);
-        tmem_wait_ld();
-        uint32_t plo[16], phi[16];
+    for (int b = 0; b < half / 32; ++b) {
+        const int j0 = part * (half / 2) + b * 16;
+        float tb[4][8];
+        if (rope) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-            float g0 = __uint_as_float(lo[e]) * scale, g1 = __uint_as_float(lo[e + 1]) * scale;
-            float h0 = __uint_as_float(hi[e]) * scale, h1 = __uint_as_float(hi[e + 1]) * scale;
-            if (rope) {
-                const float4 cs = __ldg(reinterpret_cast<const float4*>(
-                    table + static_cast<int64_t>(pos) * half + a * 32 + e));
-                const float x0 = g0 * cs.x + h0 * cs.y, y0 = h0 * cs.x - g0 * cs.y;
-                const float x1 = g1 * cs.z + h1 * cs.w, y1 = h1 * cs.z - g1 * cs.w;
-                g0 = x0; h0 = y0; g1 = x1; h1 = y1;
-            }
-            plo[e / 2] = pack_bf16x2(g0, g1);
-            phi[e / 2] = pack_bf16x2(h0, h1);
+            for (int m = 0; m < 4; ++m) ld_nc_v8(trow + (j0 / 4 + m) * jstride, tb[m]);
         }
-        if (valid) {
-            uint4* dlo = reinterpret_cast<uint4*>(row_out + (a * 32) * 2);
-            uint4* dhi = reinterpret_cast<uint4*>(row_out + (half + a * 32) * 2);
+        uint32_t lo[16], hi[16];
+        tmem_ld16(taddr + j0, lo);
+        tmem_ld16(taddr + half + j0, hi);
+        tmem_wait_ld();
+        uint32_t plo[8], phi[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {   // pairs j0 + 4m .. +3
+            float g[4], h[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                dlo[q] = make_uint4(plo[4 * q], plo[4 * q + 1], plo[4 * q + 2], plo[4 * q + 3]);
-                dhi[q] = make_uint4(phi[4 * q], phi[4 * q + 1], phi[4 * q + 2], phi[4 * q + 3]);
+                g[q] = __uint_as_float(lo[4 * m + q]) * scale;
+                h[q] = __uint_as_float(hi[4 * m + q]) * scale;
+                if (rope) {
+                    const float c = tb[m][2 * q], s = tb[m][2 * q + 1];
+                    const float x = g[q] * c + h[q] * s, y = h[q] * c - g[q] * s;
+                    g[q] = x; h[q] = y;
+                }
             }
+            plo[2 * m] = pack_bf16x2(g[0], g[1]);
+            plo[2 * m + 1] = pack_bf16x2(g[2], g[3]);
+            phi[2 * m] = pack_bf16x2(h[0], h[1]);
+            phi[2 * m + 1] = pack_bf16x2(h[2], h[3]);
+        }
+        if (valid) {
+            st_row32(row_out + j0 * 2, plo, v8);
+            st_row32(row_out + (half + j0) * 2, phi, v8);
         }
     }
 }
@@ -559,6 +571,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         const int r = wq * 32 + lane;              // query row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float scale_log2 = p.scale * kLog2e;
+        const bool v8 = (reinterpret_cast<uintptr_t>(p.dq) & 31) == 0;   // 256-bit row stores
         const int c0 = 64 * g;
         uint32_t unit_it = 0, kv = 0;
         // Copy unit k's Q' and dO rows into TMEM once its tiles have landed and the
@@ -654,14 +667,14 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             }
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
             tc_fence_after();
-            if (g == 0) {
+            {   // both warpgroups: each takes half of the row's rotation pairs
                 uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dq) + (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
                 if (p.use_rope == kRopeInterleaved)
-                    store_unrotated<D, true>(tmem + lane_off + LY::DQ_COL, p.table, rpos, p.scale, true,
-                                             valid, row_out);
+                    store_unrotated<D, true>(tmem + lane_off + LY::DQ_COL, p.table2, p.table_rows, rpos, p.scale,
+                                             true, valid, row_out, v8, g);
                 else
-                    store_unrotated<D, false>(tmem + lane_off + LY::DQ_COL, p.table, rpos, p.scale,
-                                              p.use_rope != 0, valid, row_out);
+                    store_unrotated<D, false>(tmem + lane_off + LY::DQ_COL, p.table2, p.table_rows, rpos,
+                                              p.scale, p.use_rope != 0, valid, row_out, v8, g);
             }
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));
@@ -967,6 +980,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const int r = wq * 32 + lane;              // key row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float scale_log2 = p.scale * kLog2e;
+        const bool v8 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31) == 0;
         const int c0 = 64 * g;
         uint32_t unit_it = 0, st = 0;
         bool ok = true;
@@ -1057,31 +1071,27 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             const bool valid = kvpos < w.Lk;
             const int64_t tok = static_cast<int64_t>(w.row0k) + (valid ? kvpos : 0);
             const int64_t roff = (tok * p.Hkv + w.h) * static_cast<int64_t>(D) * 2;
-            if (g == 0) {   // dV: plain copy out
+            // each warpgroup stores half of dV (plain copy) and half of dK (scale and R(p)^T)
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tmem + lane_off + LY::DV_COL + c * 32, rr);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
+            for (int c = 0; c < D / 64; ++c) {
+                const int col = g * (D / 2) + c * 32;
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_off + LY::DV_COL + col, rr);
+                tmem_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
-                    if (valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dv) + roff + c * 64);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                    }
-                }
-            } else {        // dK: scale and R(p)^T
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
+                if (valid) st_row64(reinterpret_cast<uint8_t*>(p.dv) + roff + col * 2, pk, v8);
+            }
+            {
                 uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dk) + roff;
                 if (p.use_rope == kRopeInterleaved)
-                    store_unrotated<D, true>(tmem + lane_off + LY::DK_COL, p.table, kvpos, p.scale, true,
-                                             valid, row_out);
+                    store_unrotated<D, true>(tmem + lane_off + LY::DK_COL, p.table2, p.table_rows, kvpos, p.scale,
+                                             true, valid, row_out, v8, g);
                 else
-                    store_unrotated<D, false>(tmem + lane_off + LY::DK_COL, p.table, kvpos, p.scale,
-                                              p.use_rope != 0, valid, row_out);
+                    store_unrotated<D, false>(tmem + lane_off + LY::DK_COL, p.table2, p.table_rows, kvpos,
+                                              p.scale, p.use_rope != 0, valid, row_out, v8, g);
             }
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));

@@ -335,6 +335,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t sadr = tmem + lane_off + LY::S_COL(t);
         const uint32_t oadr = tmem + lane_off + LY::O_COL(t);
         const float sl2 = p.scale_log2;
+        const bool v8 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;   // 256-bit row stores
         uint32_t cnt_s = 0, cnt_u = 0;
         bool ok = true;
         for (int un = 0; ok; ++un) {
@@ -448,10 +449,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     pk[16 + e] = pack_bf16x2(__uint_as_float(rb[2 * e]) * inv_l, __uint_as_float(rb[2 * e + 1]) * inv_l);
                 }
                 if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    st_row64(orow + c * 64, pk, v8);
+                    st_row64(orow + c * 64 + 64, pk + 16, v8);
                 }
             }
             if (valid)

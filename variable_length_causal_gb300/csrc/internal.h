@@ -23,7 +23,7 @@ struct WsHeader {
 
 // Byte offsets of the workspace regions for one problem size.
 struct WsLayout {
-    size_t header, items, order, seg_base, table, delta, qrot, krot, total;
+    size_t header, items, order, seg_base, table, table2, delta, qrot, krot, total;
     int64_t item_cap;
     int32_t table_rows;
 };
@@ -52,8 +52,9 @@ cudaError_t launch_pad_fill(const int32_t* cu, const int32_t* cu_padded, int32_t
                             int64_t c_row_bytes, float* lse, int32_t H, const int32_t* err,
                             int num_sms, cudaStream_t s);
 
+// table2 (optional): the same values blocked by four frequencies, [d/8][rows][4].
 cudaError_t launch_rope_table(float2* table, int32_t rows, int32_t d, double theta,
-                              const int32_t* err, cudaStream_t s);
+                              const int32_t* err, cudaStream_t s, float2* table2 = nullptr);
 
 // RoPE modes of FwdParams::use_rope / BwdParams::use_rope.
 constexpr int kRopeNone = 0, kRopeHalf = 1, kRopeInterleaved = 2;
@@ -107,6 +108,8 @@ struct BwdParams {
     int32_t* next_k;
     int32_t* err;
     const float2* table;
+    const float2* table2;      // the table blocked by four frequencies: [d/8][table_rows][4]
+    int32_t table_rows;
     float* delta;              // [H, total]: rowsum(dO * O)
     void* qrot;                // [total, H, d] bf16: R(p) q (workspace; only with RoPE)
     void* krot;                // [total_kv, Hkv, d] bf16: R(p) k

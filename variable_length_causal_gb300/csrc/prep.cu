@@ -418,11 +418,14 @@ cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64
 // formed in fp64 and reduced to [-pi, pi] in fp64 (one fused multiply-add
 // against 2*pi in double), so the fp32 sincos that follows sees a small
 // argument; the result is accurate to a few 1e-7 even at p ~ 1e6.
+// table2 (optional) holds the same values blocked by four frequencies:
+// table2[j/4][p][j%4], so that 32 threads owning 32 consecutive positions read
+// 32 consecutive 32-byte pieces (the backward epilogues, one row per thread).
 
 constexpr double kTwoPi = 6.283185307179586476925286766559;
 
-__global__ void rope_table_kernel(float2* __restrict__ table, int32_t rows, int32_t half,
-                                  double log2_theta, const int32_t* __restrict__ err) {
+__global__ void rope_table_kernel(float2* __restrict__ table, float2* __restrict__ table2, int32_t rows,
+                                  int32_t half, double log2_theta, const int32_t* __restrict__ err) {
     if (err != nullptr && *err != 0) return;
     __shared__ double w[256];
     for (int j = threadIdx.x; j < half; j += blockDim.x)
@@ -439,16 +442,17 @@ __global__ void rope_table_kernel(float2* __restrict__ table, int32_t rows, int3
         float sn, cs;
         sincosf(static_cast<float>(red), &sn, &cs);
         table[idx] = make_float2(cs, sn);
+        if (table2 != nullptr) table2[((static_cast<int64_t>(j >> 2) * rows + p) << 2) + (j & 3)] = make_float2(cs, sn);
     }
 }
 
 cudaError_t launch_rope_table(float2* table, int32_t rows, int32_t d, double theta,
-                              const int32_t* err, cudaStream_t s) {
+                              const int32_t* err, cudaStream_t s, float2* table2) {
     const int half = d / 2;
     const int64_t n = static_cast<int64_t>(rows) * half;
     int64_t blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    rope_table_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(table, rows, half, log2(theta), err);
+    rope_table_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(table, table2, rows, half, log2(theta), err);
     return cudaGetLastError();
 }
 

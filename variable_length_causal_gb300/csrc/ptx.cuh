@@ -341,4 +341,48 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// ---------------------------------------------------------------- 256-bit row traffic
+// Epilogues write one output row per thread, so every store instruction touches 32
+// rows; 32-byte accesses make each lane's piece a whole L2 sector and halve the
+// instruction count.  The 32-byte forms need 32-byte aligned addresses.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// 16 consecutive 32-bit words (64 bytes) to dst: two 32-byte stores when V8 (dst
+// 32-byte aligned), else four 16-byte stores (dst 16-byte aligned).
+__device__ __forceinline__ void st_row64(uint8_t* dst, const uint32_t* w, bool v8) {
+    if (v8) {
+        st_global_v8(dst, w);
+        st_global_v8(dst + 32, w + 8);
+    } else {
+        uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+}
+
+// 8 consecutive 32-bit words (32 bytes) to dst: one 32-byte store when V8, else two
+// 16-byte stores.
+__device__ __forceinline__ void st_row32(uint8_t* dst, const uint32_t* w, bool v8) {
+    if (v8) {
+        st_global_v8(dst, w);
+    } else {
+        uint4* d = reinterpret_cast<uint4*>(dst);
+        d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+// Eight consecutive floats (32 bytes, 32-byte aligned) through the read-only path
+// (data no kernel writes while it runs: the RoPE tables).  Volatile, so it stays
+// where the caller places it (callers issue these a step ahead).
+__device__ __forceinline__ void ld_nc_v8(const void* p, float* f) {
+    asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]), "=f"(f[4]), "=f"(f[5]), "=f"(f[6]), "=f"(f[7])
+                 : "l"(p));
+}
+
 }  // namespace vlc
