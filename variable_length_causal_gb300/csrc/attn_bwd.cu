@@ -31,6 +31,7 @@
 // Both attention kernels are persistent (one CTA per SM), warp-specialised
 // like the forward (TMA warp, MMA warp, TMEM warp, 4 math warps, 4 hand-off
 // warps), and use only bounded waits.
+#include <type_traits>
 #include <cuda.h>
 #include <cmath>
 #include <cstdint>
@@ -606,7 +607,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             const int lastk = min(qpos + w.off, w.Lk - 1);
             const int j_edge = w.hi - 1 - ((w.off & (BK - 1)) != 0 ? 1 : 0);
             const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? qpos : 0);
-            const float lse2 = valid ? __ldg(p.lse + static_cast<int64_t>(w.h) * p.total + tok) * kLog2e : 0.f;
+            // a row past the segment gets lse2 = +inf, so its P is exp2(-inf) = 0 without a mask
+            const float lse2 = valid ? __ldg(p.lse + static_cast<int64_t>(w.h) * p.total + tok) * kLog2e : INFINITY;
             const float dlt = valid ? __ldg(p.delta + static_cast<int64_t>(w.h) * p.total + tok) : 0.f;
             for (int j = 0; j < w.hi; ++j, ++kv) {
                 // ---- phase A: P = exp2(s * scale_log2 - lse2) (masked), kept packed
@@ -618,21 +620,29 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(bar(S_EMPTY));
-                const bool edge = j >= j_edge;   // diagonal step(s) and the segment tail
-                const int lim = !valid ? -1 : (edge ? lastk - j * BK : BK - 1);
+                // diagonal step(s) and the segment tail mask key columns c > lim (scores -> -inf);
+                // the other steps take a loop without the compare
+                const bool edge = j >= j_edge;
+                const int lim = lastk - j * BK;
                 const float2 sc2 = make_float2(scale_log2, scale_log2), nl2 = make_float2(-lse2, -lse2);
                 uint32_t pp[32];
+                auto phase_a = [&](auto masked) {
 #pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    const uint32_t* src = (e < 32) ? sa : sb;
-                    const int ee = e & 31;
-                    const float2 x = fma2(make_float2(__uint_as_float(src[ee]), __uint_as_float(src[ee + 1])),
-                                          sc2, nl2);
-                    const int col = c0 + e;
-                    const float p0 = (col <= lim) ? ex2_approx(x.x) : 0.f;
-                    const float p1 = (col + 1 <= lim) ? ex2_approx(x.y) : 0.f;
-                    pp[e >> 1] = pack_bf16x2(p0, p1);
-                }
+                    for (int e = 0; e < 64; e += 2) {
+                        const uint32_t* src = (e < 32) ? sa : sb;
+                        const int ee = e & 31;
+                        float2 s = make_float2(__uint_as_float(src[ee]), __uint_as_float(src[ee + 1]));
+                        if constexpr (decltype(masked)::value) {
+                            const int col = c0 + e;
+                            if (col > lim) s.x = -INFINITY;
+                            if (col + 1 > lim) s.y = -INFINITY;
+                        }
+                        const float2 x = fma2(s, sc2, nl2);
+                        pp[e >> 1] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
+                    }
+                };
+                if (edge) phase_a(std::true_type{});
+                else phase_a(std::false_type{});
                 // ---- phase B: dS = P (dP - D), packed over the consumed dP columns
                 if (!(ok = wait_warp(bar(DP_FULL), kv & 1, abort))) break;
                 tc_fence_after();
@@ -960,7 +970,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 for (int h4 = 0; h4 < 4; ++h4) {
                     const int q = lane + 32 * h4;
                     const int qq = i * BQ + q;
-                    float l2 = 0.f, dl = 0.f;
+                    // a column past the segment gets lse2 = +inf: its P^T is exp2(-inf) = 0, so
+                    // phase A needs no mask for the segment tail
+                    float l2 = INFINITY, dl = 0.f;
                     if (qq < w.L) {
                         const int64_t idx = static_cast<int64_t>(hq) * p.total + w.row0 + qq;
                         l2 = __ldg(p.lse + idx) * kLog2e;
@@ -996,33 +1008,37 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 const float* l2s = lsed + sl * 256 + c0;
                 const float* dls = lsed + sl * 256 + 128 + c0;
                 if (!(ok = wait_warp(bar(LSED_FULL + sl), (st / kLsedSlots) & 1, abort))) break;
-                // allowed q columns: kvpos <= i*BQ + col + off and i*BQ + col < L; only steps
-                // whose first column does not see the tile's last key need the check
-                const bool edge = (i * BQ + w.off < w.tile * 128 + 127) || ((i + 1) * BQ > w.L);
-                const int c_lo = kvpos - w.off - i * BQ, c_hi = w.L - 1 - i * BQ;
+                // allowed q columns: kvpos <= i*BQ + col + off (the diagonal; the segment tail
+                // comes through lse2 = +inf); only steps whose first column does not see the
+                // tile's last key need the mask, and they take a loop of their own
+                const bool diag = i * BQ + w.off < w.tile * 128 + 127;
+                const int c_lo = kvpos - w.off - i * BQ;
                 // ---- phase A: P^T = exp2(s * scale_log2 - lse2) over this group's 64 columns
                 if (!(ok = wait_warp(bar(ST_FULL), st & 1, abort))) break;
                 tc_fence_after();
                 uint32_t pp[32];
+                auto phase_a = [&](auto masked) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t sr[32];
-                    tmem_ld32(tmem + lane_off + c0 + 32 * h, sr);
-                    tmem_wait_ld();
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t sr[32];
+                        tmem_ld32(tmem + lane_off + c0 + 32 * h, sr);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int col = c0 + 32 * h + e;
-                        const float2 lz = *reinterpret_cast<const float2*>(l2s + 32 * h + e);
-                        const float2 x = fma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                              make_float2(scale_log2, scale_log2), make_float2(-lz.x, -lz.y));
-                        float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-                        if (edge) {
-                            if (col < c_lo || col > c_hi) p0 = 0.f;
-                            if (col + 1 < c_lo || col + 1 > c_hi) p1 = 0.f;
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 lz = *reinterpret_cast<const float2*>(l2s + 32 * h + e);
+                            float2 s = make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                            if constexpr (decltype(masked)::value) {   // above the diagonal -> -inf
+                                const int col = c0 + 32 * h + e;
+                                if (col < c_lo) s.x = -INFINITY;
+                                if (col + 1 < c_lo) s.y = -INFINITY;
+                            }
+                            const float2 x = fma2(s, make_float2(scale_log2, scale_log2), make_float2(-lz.x, -lz.y));
+                            pp[16 * h + (e >> 1)] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
                         }
-                        pp[16 * h + (e >> 1)] = pack_bf16x2(p0, p1);
                     }
-                }
+                };
+                if (diag) phase_a(std::true_type{});
+                else phase_a(std::false_type{});
                 {
                     uint32_t lo[16], hi[16];
 #pragma unroll
