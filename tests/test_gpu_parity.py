@@ -354,3 +354,22 @@ def test_fwd_peaky_scores_rescale_paths(vlc):
     assert eo.max() <= O_MAX and eo.mean() <= O_MEAN
     # LSE magnitudes reach ~1e2 here: compare relative to the fp32 scale of the value
     assert (el / np.maximum(1.0, np.abs(lse_ref))).max() <= LSE_MAX
+
+
+@pytest.mark.parametrize("il", [False, True])
+def test_fwd_bwd_with_prerotated_keys(vlc, il):
+    # a segment with at least 2048 keys takes the forward's rotated-k pass (its K tiles are
+    # not rotated in-kernel); its neighbours are short and keep the in-kernel rotation
+    lens = [2100, 5, 300, 2048]
+    w = synth.custom_workload(lens, 2, 128)
+    q, k, v, g = (t.to(DEV) for t in synth.make_tensors(w, seed=77, with_grad=True))
+    o, lse = vlc.varlen_attn_fwd(q, k, v, _cu(w), w.max_seqlen, rope_interleaved=il)
+    qc, kc, vc, gc = (t.cpu() for t in (q, k, v, g))
+    o_ref, lse_ref = oracle.attn_fwd(qc, kc, vc, w.cu, interleaved=il)
+    e = (o.float().cpu().numpy() - o_ref)
+    assert np.abs(e).max() <= 2e-2 and np.abs(e).mean() <= 2e-3
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-3
+    dq, dk, dv = vlc.varlen_attn_bwd(g, q, k, v, o, lse, _cu(w), w.max_seqlen, rope_interleaved=il)
+    ref = oracle.attn_bwd(gc, qc, kc, vc, w.cu, interleaved=il)
+    for a, b in zip((dq, dk, dv), ref):
+        assert np.abs(a.float().cpu().numpy() - b).max() <= 5e-2

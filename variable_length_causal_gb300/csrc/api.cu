@@ -56,6 +56,11 @@ WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t 
         L.krot = off;
         off = align256(off + static_cast<size_t>(total_kv) * Hkv * d * 2);
     }
+    L.total_min = off;
+    if (!is_bwd) {   // the forward's rotated copy of k (long segments), used when the workspace has room
+        L.krot = off;
+        off = align256(off + static_cast<size_t>(total_kv) * Hkv * d * 2);
+    }
     L.total = off;
     return L;
 }
@@ -146,7 +151,7 @@ static int check_attn_args(const AttnArgs& a, int is_bwd) {
     if (a.ws == nullptr || !aligned(a.ws, 256)) return VLC_ERR_WORKSPACE;
     const bool qkv = a.cu_kv != nullptr;
     if (a.ws_bytes < ws_layout(a.nseg, a.total, a.H, a.Hkv, a.d, a.max_seqlen, is_bwd, qkv ? a.total_kv : -1,
-                               qkv ? a.max_seqlen_kv : -1).total)
+                               qkv ? a.max_seqlen_kv : -1).total_min)
         return VLC_ERR_WORKSPACE;
     return VLC_OK;
 }
@@ -204,6 +209,14 @@ static int attn_fwd_impl(AttnArgs a) {
     const float scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / std::sqrt(static_cast<float>(a.d));
     p.scale_log2 = scale * 1.4426950408889634f;
     p.use_rope = mode;
+    // long segments: k rotated once into the workspace (if it has room), not once per unit
+    p.krot = nullptr;
+    p.prerot_min = kPreRotMinKeys;
+    if (mode != kRopeNone && !qkv && a.ws_bytes >= L.total && a.max_seqlen >= kPreRotMinKeys) {
+        if (launch_krot(p, w + L.krot, order, kPreRotMinKeys, num_sms_cached(), s) != cudaSuccess)
+            return VLC_ERR_CUDA;
+        p.krot = w + L.krot;
+    }
     if (launch_attn_fwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
     return VLC_OK;
 }

@@ -260,4 +260,73 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2*
     }
 }
 
+// ---------------------------------------------------------------- row rotation (HBM passes)
+// cs/sn[2e], [2e+1]: angles of the two pairs that the e-th 32-bit words of a
+// thread's lo and hi chunks take part in (rotate-half: the pairs at word e's two
+// columns; interleaved: word e of lo, word e of hi), at position pos.
+template <int D>
+__device__ __forceinline__ void load_angles(const float2* __restrict__ table, int64_t pos, bool il, int c,
+                                            float cs[8], float sn[8]) {
+    if (!il) {
+        const float4* t4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 8);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 f = __ldg(t4 + e);
+            cs[2 * e] = f.x; sn[2 * e] = f.y; cs[2 * e + 1] = f.z; sn[2 * e + 1] = f.w;
+        }
+    } else {
+        const float4* l4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + c * 4);
+        const float4* h4 = reinterpret_cast<const float4*>(table + pos * (D / 2) + D / 4 + c * 4);
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+            const float4 f = __ldg(l4 + e2), g = __ldg(h4 + e2);
+            cs[4 * e2] = f.x; sn[4 * e2] = f.y; cs[4 * e2 + 1] = g.x; sn[4 * e2 + 1] = g.y;
+            cs[4 * e2 + 2] = f.z; sn[4 * e2 + 2] = f.w; cs[4 * e2 + 3] = g.z; sn[4 * e2 + 3] = g.w;
+        }
+    }
+}
+
+// Rotate chunks a0 (lo) and a1 (hi) of one row of src into dst with the angles of
+// load_angles; padding rows (real == false) become zeros, so every operand row
+// stays finite.
+__device__ __forceinline__ void rotate_chunks(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                              int64_t a0, int64_t a1, const float cs[8], const float sn[8],
+                                              bool real, bool il) {
+    if (!real) {
+        dst[a0] = make_uint4(0u, 0u, 0u, 0u);
+        dst[a1] = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    const uint4 x4 = __ldg(src + a0), y4 = __ldg(src + a1);
+    const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
+    uint32_t nx[4], ny[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
+        if (!il) {   // pairs (lo word e, hi word e) at columns 2e and 2e+1
+            const float x0 = bf16_lo(xv[e]), x1 = bf16_hi(xv[e]);
+            const float y0 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
+            nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
+            ny[e] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+        } else {     // lo word e and hi word e are pairs of their own
+            const float x0 = bf16_lo(xv[e]), y0 = bf16_hi(xv[e]);
+            const float x1 = bf16_lo(yv[e]), y1 = bf16_hi(yv[e]);
+            nx[e] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(y0, c0, x0 * s0));
+            ny[e] = pack_bf16x2(fmaf(x1, c1, -y1 * s1), fmaf(y1, c1, x1 * s1));
+        }
+    }
+    dst[a0] = make_uint4(nx[0], nx[1], nx[2], nx[3]);
+    dst[a1] = make_uint4(ny[0], ny[1], ny[2], ny[3]);
+}
+
+// Largest r in [0, nseg-1] with rows[r] <= tok (clamped, in bounds).
+__device__ __forceinline__ int segment_of_row(const int32_t* __restrict__ rows, int nseg, int64_t tok) {
+    int a = 0, b = nseg - 1;
+    while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (__ldg(rows + mid) <= tok) a = mid; else b = mid - 1;
+    }
+    return a;
+}
+
 }  // namespace vlc

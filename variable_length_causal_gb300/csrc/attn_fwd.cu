@@ -98,6 +98,7 @@ struct Layout {
 struct FUnit {
     Unit w;
     bool has1;
+    bool pre;   // K tiles come rotated from p.krot (long segments), not rotated in-kernel
     int q0, n0, n1, nk;
     int hkv;   // key/value head of query head w.h
 };
@@ -120,6 +121,7 @@ __device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
         f.n1 = f.has1 ? f.q0 + 2 : 0;
     }
     f.nk = f.has1 ? f.n1 : f.n0;
+    f.pre = p.krot != nullptr && f.w.Lk >= p.prerot_min;
     f.hkv = p.Hkv == p.H ? f.w.h : f.w.h / (p.H / p.Hkv);
     return f;
 }
@@ -128,6 +130,7 @@ __device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
 template <int D, bool KV>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmKr,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using LY = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -176,6 +179,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmKr);
         tma_prefetch_desc(&tmV);
     }
     if (warp == 2) {
@@ -223,7 +227,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     mbar_expect_tx(bar(K_FULL + ks), LY::TILE);
 #pragma unroll
                     for (int kb = 0; kb < LY::KB; ++kb)
-                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, &tmK, kb * 64,
+                        tma_load_3d_hint(sbase + LY::K0 + ks * LY::TILE + kb * LY::BLK, f.pre ? &tmKr : &tmK, kb * 64,
                                          f.hkv, f.w.row0k + j * BN, bar(K_FULL + ks), pol_keep);
                     k_issued = n + 1;
                 }
@@ -485,7 +489,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int j = 0; j < f.nk && ok; ++j) {
                     const int ks = kvn & 1;
                     if (!(ok = wait_warp(bar(K_FULL + ks), (kvn >> 1) & 1, abort))) break;
-                    if (p.use_rope)
+                    if (p.use_rope && !f.pre)
                         rope_tile<D, 128, IL>(sbase + LY::K0 + ks * LY::TILE, j * BN, p.table, step, wr, lane);
                     fence_proxy_async_smem();
                     mbar_arrive(bar(K_READY + ks));
@@ -561,9 +565,10 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int32_t total, int32_t H,
                    int box_rows);
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tkr, tv;
     if (!make_tmap_thd(&tq, p.q, p.total, p.H, p.d, 128) ||
         !make_tmap_thd(&tk, p.k, p.total_kv, p.Hkv, p.d, 128) ||
+        !make_tmap_thd(&tkr, p.krot != nullptr ? p.krot : p.k, p.total_kv, p.Hkv, p.d, 128) ||
         !make_tmap_thd(&tv, p.v, p.total_kv, p.Hkv, p.d, 128))
         return cudaErrorInvalidValue;
     const dim3 grid(num_sms), block(fwd::kThreads);
@@ -581,7 +586,57 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
     }
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, block, smem, s>>>(tq, tk, tv, p);
+    kernel<<<grid, block, smem, s>>>(tq, tk, tkr, tv, p);
+    return cudaGetLastError();
+}
+
+
+// ---------------------------------------------------------------- rotated k for long segments
+// One pass over the key rows of segments with at least min_keys keys: k' = R(p) k
+// (bf16, rounded once, the same rotation as the in-kernel tiles), so the forward
+// kernel reads those K tiles ready-made instead of rotating each of them once per
+// work unit that reads it.  The work list's order puts the long segments first:
+// every block walks that order until the segments get short and takes a
+// grid-stride share of each long segment's rows (D/16 threads per row, as in the
+// backward's prep pass).
+namespace fwd {
+template <int D>
+__global__ void __launch_bounds__(256)
+krot_kernel(const uint4* __restrict__ k, uint4* __restrict__ krot, const int32_t* __restrict__ cu,
+            const int32_t* __restrict__ rows, const int32_t* __restrict__ order, int32_t nseg,
+            const float2* __restrict__ table, int32_t Hkv, int rope, int32_t min_keys,
+            const int32_t* __restrict__ err) {
+    if (*err != 0) return;
+    constexpr int TPR = D / 16;
+    constexpr int HALF = D / 16;
+    const int min_tiles = (min_keys + kFwdQB - 1) / kFwdQB;
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int c = static_cast<int>(gtid % TPR);
+    const bool il = rope == kRopeInterleaved;
+    for (int i = 0; i < nseg; ++i) {
+        const int r = __ldg(order + i);
+        const int L = __ldg(cu + r + 1) - __ldg(cu + r);
+        if ((L + kFwdQB - 1) / kFwdQB < min_tiles) break;   // sorted: the rest are shorter
+        if (L < min_keys) continue;
+        const int64_t row0 = static_cast<int64_t>(__ldg(rows + r)) * Hkv;
+        const int64_t nrows = static_cast<int64_t>(L) * Hkv;
+        for (int64_t j = gtid / TPR; j < nrows; j += nthreads / TPR) {
+            const int64_t pos = j / Hkv;
+            float cs[8], sn[8];
+            load_angles<D>(table, pos, il, c, cs, sn);
+            const int64_t lo = (row0 + j) * (2 * HALF) + c;
+            rotate_chunks(k, krot, lo, lo + HALF, cs, sn, true, il);
+        }
+    }
+}
+}  // namespace fwd
+
+cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, int32_t min_keys, int num_sms,
+                        cudaStream_t s) {
+    auto kernel = p.d == 128 ? fwd::krot_kernel<128> : fwd::krot_kernel<64>;
+    kernel<<<num_sms * 8, 256, 0, s>>>(static_cast<const uint4*>(p.k), static_cast<uint4*>(krot), p.cu, p.rows_kv,
+                                       order, p.nseg, p.table, p.Hkv, p.use_rope, min_keys, p.err);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@ struct WsHeader {
 // Byte offsets of the workspace regions for one problem size.
 struct WsLayout {
     size_t header, items, order, seg_base, table, table2, delta, qrot, krot, total;
+    size_t total_min;          // forward: the bytes needed without the rotated-k copy (its fallback)
     int64_t item_cap;
     int32_t table_rows;
 };
@@ -75,6 +76,8 @@ struct FwdParams {
     int32_t* next;             // unit counter (zeroed before the launch)
     int32_t* err;
     const float2* table;       // RoPE cos/sin [rows][d/2], null if no RoPE
+    const void* krot;          // R(p) k for segments with at least prerot_min keys, or null
+    int32_t prerot_min;
     int32_t nseg, total, H, d;
     int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
     int32_t total_kv;          // key/value rows (== total for self-attention)
@@ -83,6 +86,19 @@ struct FwdParams {
 };
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s);
+
+// Segments with at least this many keys get their k rows rotated once, before the
+// forward kernel, instead of once per work unit inside it (a segment of T key
+// tiles is read by ~T/2 units; below ~16 tiles the extra HBM pass costs more than
+// the in-kernel rotations it saves).
+constexpr int32_t kPreRotMinKeys = 2048;
+
+// R(p) k into krot for the key rows of segments with at least min_keys keys
+// (other rows are not written).  order: the forward work list's segment order
+// (descending q-tile count, kFwdQB-row tiles), so the long segments come first;
+// self-attention only.  No-op if *err != 0.
+cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, int32_t min_keys, int num_sms,
+                        cudaStream_t s);
 
 struct BwdParams {
     const void* dout;

@@ -68,11 +68,13 @@ extern "C" int vlc_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                                     int32_t nseg, int32_t total, int32_t H, int32_t d,
                                     int32_t max_seqlen, float softmax_scale, float rope_theta,
                                     void* o, float* lse, int32_t* err_out, void* stream) {
-    const size_t need = vlc_workspace_bytes(nseg, total, H, d, max_seqlen, 0);
-    if (need == 0) {
+    if (vlc_workspace_bytes(nseg, total, H, d, max_seqlen, 0) == 0) {
         if (d != 64 && d != 128) return VLC_ERR_UNSUPPORTED;
         return VLC_ERR_ARG;
     }
+    // the scratch holds the forward's work list, table and error word; the optional
+    // rotated copy of k does not fit, so the forward rotates every K tile in-kernel
+    const size_t need = vlc::ws_layout(nseg, total, H, H, d, max_seqlen, 0).total_min;
     if (need > vlc::kNoAllocScratchBytes) return VLC_ERR_WORKSPACE;
     void* scratch = nullptr;
     const int st = vlc::scratch_for_current_device(&scratch);
