@@ -179,6 +179,8 @@ class Step:
         else:
             self.dq, self.dk, self.dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         self.ws_f = vlc.new_workspace(w.nseg, w.total, w.H, w.d, w.max_seqlen, False, dev)
+        # q' and k' for the step: rotated once, read by the forward and the backward
+        self.qr, self.kr = torch.empty_like(q), torch.empty_like(k)
         self.ws_b = None if fwd_only else vlc.new_workspace(w.nseg, w.total, w.H, w.d, w.max_seqlen, True, dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -191,13 +193,16 @@ class Step:
         self.pos, self.lab = vlc.build_positions_labels(self.cu, self.tokens, self.ign, err=self.err)
         if ev is not None:
             ev[1].record()
-        vlc.varlen_attn_fwd(self.q, self.k, self.v, self.cu, w.max_seqlen, out=self.o, lse=self.lse,
-                            workspace=self.ws_f, check=False)
+        vlc.rope_qk(self.q, self.k, self.cu, w.max_seqlen, rope_theta=w.theta, out=(self.qr, self.kr),
+                    workspace=self.ws_f, check=False)
+        vlc.varlen_attn_fwd(self.qr, self.kr, self.v, self.cu, w.max_seqlen, rope_theta=w.theta, out=self.o,
+                            lse=self.lse, workspace=self.ws_f, check=False, qk_rotated=True)
         if ev is not None:
             ev[2].record()
         if not self.fwd_only:
-            vlc.varlen_attn_bwd(self.g, self.q, self.k, self.v, self.o, self.lse, self.cu, w.max_seqlen,
-                                dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws_b, check=False)
+            vlc.varlen_attn_bwd(self.g, self.qr, self.kr, self.v, self.o, self.lse, self.cu, w.max_seqlen,
+                                rope_theta=w.theta, dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws_b,
+                                check=False, qk_rotated=True)
         if ev is not None:
             ev[3].record()
 
@@ -210,7 +215,9 @@ class Step:
             raise RuntimeError("positions/labels reported invalid cu_seqlens")
 
 
-LAUNCHES_PER_STEP = 1 + 3 + 6   # posl; worklist+table+fwd; 2 worklists+table+delta+dq+dkdv
+# posl; rotation (worklist + table + q'/k'); forward (worklist + attention); backward (2 worklists +
+# table + delta + dq + dkdv)
+LAUNCHES_PER_STEP = 1 + 3 + 2 + 6
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -345,7 +352,7 @@ def gpu_arm(args, w, world, rank, local):
     kernels = {
         "positions_labels": {"ms": t_pos, "GB/s": pos_bytes / (t_pos * 1e-3) / 1e9},
         "attn_fwd_call": {"ms": t_fwd, "eff_TFLOP/s": fwd_tflops,
-                          "kernels": "worklist + rope_table + attn_fwd_kernel"},
+                          "kernels": "rotation (worklist + rope_table + rope_qk_kernel) + worklist + attn_fwd_kernel"},
         "attn_bwd_call": {"ms": t_bwd, "eff_TFLOP/s": bwd_tflops,
                           "kernels": "2 worklists + rope_table + delta + dq_kernel + dkdv_kernel"},
     }
@@ -367,7 +374,7 @@ def gpu_arm(args, w, world, rank, local):
         "tokens_per_s": real_tok / (ms * 1e-3),
         "fwd_eff_tflops": fwd_tflops, "bwd_eff_tflops": bwd_tflops,
         "kernels": kernels, "roofline": roofline, "roofline_fwd": roofline_fwd,
-        "gpu_launches": (4 if args.fwd_only else LAUNCHES_PER_STEP) * args.steps,
+        "gpu_launches": (6 if args.fwd_only else LAUNCHES_PER_STEP) * args.steps,
         "clocks": clk.summary(),
         "e2e": e2e,
     }

@@ -176,6 +176,10 @@ int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void*
 
 /* Option bits of vlc_attn_fwd_ex / vlc_attn_bwd_ex. */
 #define VLC_ROPE_INTERLEAVED 0x1u  /* RoPE pairs (x_{2j}, x_{2j+1}) instead of (x_j, x_{j+d/2}) */
+#define VLC_QK_ROTATED 0x2u        /* q and k hold R(p) q, R(p) k (from vlc_rope_qk): the forward
+                                      rotates nothing; the backward rotates nothing and takes
+                                      dq, dk back through R(p)^T (rope_theta and the pairing bit
+                                      as for the rotation); not with separate key segments */
 
 /* vlc_attn_fwd_gqa / vlc_attn_bwd_gqa with a padded layout and an option word;
  * cu_padded == NULL and flags == 0 is exactly those calls.
@@ -291,6 +295,20 @@ int vlc_pack(const int32_t* lengths, int64_t n, int32_t capacity, int32_t extra,
 #define VLC_COST_SUMSQ 1
 int vlc_shard_packs(const int32_t* lengths, const int64_t* order, const int64_t* bin_start, int64_t nbins,
                     int32_t ranks, int cost_kind, int32_t* rank_of_bin, int64_t* rank_load);
+
+/* q' = R(p_i) q and k' = R(p_i) k for every row (per-segment positions, the
+ * rotation of vlc_attn_fwd, rounded once to bf16), written to caller buffers of
+ * the same layouts (qrot [total, H, d], krot [total, H_kv, d]); rows past a
+ * segment's length in a padded layout become zeros.  A training step can rotate
+ * once and then call vlc_attn_fwd_ex / vlc_attn_bwd_ex with VLC_QK_ROTATED on q',
+ * k': the forward then carries no in-kernel rotation and the backward's prep pass
+ * computes rowsum(dO * O) alone, instead of each pass rotating again.  cu and
+ * cu_padded are validated as in vlc_attn_fwd_ex (errors through the workspace
+ * word); flags: VLC_ROPE_INTERLEAVED.  rope_theta > 0.  Workspace: the forward's
+ * (vlc_workspace_bytes_gqa(..., 0)). */
+int vlc_rope_qk(const void* q, const void* k, const int32_t* cu, const int32_t* cu_padded, int32_t nseg,
+                int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen, float rope_theta,
+                uint32_t flags, void* qrot, void* krot, void* ws, size_t ws_bytes, void* stream);
 
 /* Forward attention for callers that cannot allocate device memory.  No
  * counterpart on the pages: it exists for callers that may not obtain memory

@@ -60,8 +60,13 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.vlc_attn_fwd(dummy, dummy, dummy, dummy, 3, 9, 2, 128, 4, 0.0, 0.0, dummy, dummy,
                             None, 0, None) == 4
     # option words: an unknown bit is refused before the shape checks
-    assert lib.vlc_attn_fwd_ex(dummy, dummy, dummy, dummy, None, 3, 9, 2, 2, 128, 4, 0.0, 1e4, 0x2,
+    assert lib.vlc_attn_fwd_ex(dummy, dummy, dummy, dummy, None, 3, 9, 2, 2, 128, 4, 0.0, 1e4, 0x4,
                                dummy, dummy, dummy, 1 << 20, None) == 1
+    # pre-rotated operands are a self-attention option: refused with separate key segments
+    assert lib.vlc_attn_fwd_qkv(dummy, dummy, dummy, dummy, dummy, 3, 9, 12, 2, 2, 128, 4, 6, 0.0, 1e4, 0x2,
+                                dummy, dummy, dummy, 1 << 20, None) == 1
+    assert lib.vlc_rope_qk(dummy, dummy, dummy, None, 3, 9, 2, 2, 128, 4, 1e4, 0x2, dummy, dummy, dummy,
+                           1 << 20, None) == 1
     assert lib.vlc_attn_bwd_ex(dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 3, 9, 2, 2, 128,
                                4, 0.0, 1e4, 0x80000000, dummy, dummy, dummy, dummy, 1 << 20, None) == 1
     # the interleaved bit itself is accepted: the call proceeds to the shape checks

@@ -1,0 +1,95 @@
+"""vlc_rope_qk and the pre-rotated operand option (VLC_QK_ROTATED): one rotation per
+training step.  The rotated rows match the oracle's rotation to one bf16 rounding; the
+forward and backward on q', k' match the oracle within the usual bounds; the backward on
+q', k' is bit-identical to the backward that rotates in its own prep pass (same table,
+same arithmetic).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import brute
+from variable_length_causal_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+O_MAX, O_MEAN, LSE_MAX, G_MAX = 2e-2, 2e-3, 1e-3, 5e-2
+
+
+@pytest.fixture(scope="module")
+def vlc():
+    import __graft_entry__ as g
+
+    g.build()
+    import variable_length_causal_gb300 as m
+
+    m.load_library()
+    return m
+
+
+def _inputs(lens, H, Hkv, d, seed):
+    w = synth.custom_workload(lens, H, d)
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    q, g = (torch.randn((w.total, H, d), generator=gen, device=DEV).bfloat16() for _ in range(2))
+    k, v = (torch.randn((w.total, Hkv, d), generator=gen, device=DEV).bfloat16() for _ in range(2))
+    return w, q, k, v, g
+
+
+@pytest.mark.parametrize("il", [False, True])
+def test_rotated_rows_match_the_oracle_rotation(vlc, il):
+    w, q, k, _, _ = _inputs([1, 300, 2100, 77], 4, 2, 128, seed=3)
+    cu = torch.from_numpy(w.cu).to(DEV)
+    qr, kr = vlc.rope_qk(q, k, cu, w.max_seqlen, rope_interleaved=il)
+    pos = brute.local_positions(w.cu)
+    for x, xr in ((q, qr), (k, kr)):
+        xs = oracle.bits_to_f64(oracle.bf16_bits(x.cpu()))
+        ref = np.stack([oracle.rope_rows(xs[:, h], pos, interleaved=il) for h in range(x.shape[1])], axis=1)
+        got = xr.float().cpu().numpy()
+        ulp = np.maximum(np.abs(ref), 1e-30) * 2.0 ** -7    # one bf16 rounding step
+        assert np.all(np.abs(got - ref) <= ulp + 1e-6)
+
+
+@pytest.mark.parametrize("il", [False, True])
+def test_step_on_rotated_operands(vlc, il):
+    w, q, k, v, g = _inputs([1, 130, 7, 2100, 300], 4, 2, 128, seed=11)
+    cu = torch.from_numpy(w.cu).to(DEV)
+    qr, kr = vlc.rope_qk(q, k, cu, w.max_seqlen, rope_interleaved=il)
+    o, lse = vlc.varlen_attn_fwd(qr, kr, v, cu, w.max_seqlen, rope_interleaved=il, qk_rotated=True)
+    qc, kc, vc, gc = (t.cpu() for t in (q, k, v, g))
+    o_ref, lse_ref = oracle.attn_fwd(qc, kc, vc, w.cu, interleaved=il)
+    e = np.abs(o.float().cpu().numpy() - o_ref)
+    assert e.max() <= O_MAX and e.mean() <= O_MEAN
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_MAX
+    dq, dk, dv = vlc.varlen_attn_bwd(g, qr, kr, v, o, lse, cu, w.max_seqlen, rope_interleaved=il,
+                                     qk_rotated=True)
+    ref = oracle.attn_bwd(gc, qc, kc, vc, w.cu, interleaved=il)
+    for a, b in zip((dq, dk, dv), ref):
+        assert np.abs(a.float().cpu().numpy() - b).max() <= G_MAX
+    # the backward on q', k' is the backward that rotates in its prep pass, bit for bit
+    g2 = vlc.varlen_attn_bwd(g, q, k, v, o, lse, cu, w.max_seqlen, rope_interleaved=il)
+    for a, b in zip((dq, dk, dv), g2):
+        assert torch.equal(a, b)
+
+
+def test_rotated_padded_layout(vlc):
+    lens, pads = [300, 5, 2100], [20, 0, 44]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cp = np.concatenate([[0], np.cumsum(np.add(lens, pads))]).astype(np.int32)
+    total = int(cp[-1])
+    gen = torch.Generator(device=DEV).manual_seed(5)
+    q, k, v, g = (torch.randn((total, 2, 128), generator=gen, device=DEV).bfloat16() for _ in range(4))
+    cut, cpt = torch.from_numpy(cu).to(DEV), torch.from_numpy(cp).to(DEV)
+    qr, kr = vlc.rope_qk(q, k, cut, max(lens), cu_seqlens_padded=cpt)
+    real = np.zeros(total, bool)
+    real[oracle.real_rows(cu, cp)] = True
+    pad = torch.from_numpy(~real).to(DEV)
+    assert torch.all(qr[pad] == 0) and torch.all(kr[pad] == 0)
+    o, lse = vlc.varlen_attn_fwd(qr, kr, v, cut, max(lens), cu_seqlens_padded=cpt, qk_rotated=True)
+    o_ref, _ = oracle.attn_fwd(q.cpu(), k.cpu(), v.cpu(), cu, cu_padded=cp)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_MAX
+    dq, dk, dv = vlc.varlen_attn_bwd(g, qr, kr, v, o, lse, cut, max(lens), cu_seqlens_padded=cpt, qk_rotated=True)
+    ref = oracle.attn_bwd(g.cpu(), q.cpu(), k.cpu(), v.cpu(), cu, cu_padded=cp)
+    for a, b in zip((dq, dk, dv), ref):
+        assert np.abs(a.float().cpu().numpy() - b).max() <= G_MAX

@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     load_library,
     new_workspace,
     pack,
+    rope_qk,
     shard_packs,
     shifted_cross_entropy,
     varlen_attn_bwd,

@@ -28,6 +28,7 @@ WORKLIST_FWD, WORKLIST_BWD = 0, 1
 PACK_MODES = {"ffd": 0, "first_fit": 1, "next_fit": 2}
 COST_KINDS = {"tokens": 0, "sumsq": 1}
 ROPE_INTERLEAVED = 0x1
+QK_ROTATED = 0x2
 
 EXPORTED = [
     "vlc_status_string", "vlc_version", "vlc_workspace_bytes", "vlc_worklist_capacity",
@@ -35,7 +36,7 @@ EXPORTED = [
     "vlc_get_error", "vlc_attn_fwd_noalloc", "vlc_ce_workspace_bytes", "vlc_shifted_ce",
     "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa", "vlc_attn_fwd_ex",
     "vlc_attn_bwd_ex", "vlc_workspace_bytes_qkv", "vlc_attn_fwd_qkv", "vlc_attn_bwd_qkv", "vlc_pack",
-    "vlc_shard_packs",
+    "vlc_shard_packs", "vlc_rope_qk",
 ]
 
 _lock = threading.Lock()
@@ -111,6 +112,8 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_attn_bwd_qkv.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                          f32, f32, u32, P, P, P, P, sz, P]
         lib.vlc_attn_bwd_qkv.restype = cint
+        lib.vlc_rope_qk.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, f32, u32, P, P, P, sz, P]
+        lib.vlc_rope_qk.restype = cint
         lib.vlc_pack.argtypes = [P, i64, i32, i32, cint, P, P, P, P, P]
         lib.vlc_pack.restype = cint
         lib.vlc_shard_packs.argtypes = [P, P, P, i64, i32, cint, P, P]
@@ -264,7 +267,8 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     check: bool = True, rope_interleaved: bool = False,
                     cu_seqlens_padded: Optional[torch.Tensor] = None,
-                    cu_seqlens_kv: Optional[torch.Tensor] = None, max_seqlen_kv: Optional[int] = None):
+                    cu_seqlens_kv: Optional[torch.Tensor] = None, max_seqlen_kv: Optional[int] = None,
+                    qk_rotated: bool = False):
     """Segment-local causal attention with per-segment RoPE reset.  Returns (O, LSE[H, total]).
     k and v may have fewer heads than q (grouped: query head h reads head h // (H // H_kv)).
     rope_interleaved rotates the pairs (x[2j], x[2j+1]) instead of (x[j], x[j + d/2]).
@@ -272,7 +276,8 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     (padding between segments; padding rows get O = 0, LSE = -inf).
     cu_seqlens_kv / max_seqlen_kv give k and v segments of their own, at least as long as the
     query segments; queries are bottom-right aligned (query p of a segment with L queries and
-    Lk keys sits at position p + Lk - L and sees keys up to there)."""
+    Lk keys sits at position p + Lk - L and sees keys up to there).
+    qk_rotated: q and k already hold the rotated q', k' of ``rope_qk`` (no rotation here)."""
     lib = load_library()
     _require_cuda(q, k, v, cu_seqlens, cu_seqlens_padded, cu_seqlens_kv)
     qkv = cu_seqlens_kv is not None
@@ -293,7 +298,7 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                            total_kv if qkv else None, max_seqlen_kv if qkv else None)
     else:
         ws = workspace
-    flags = ROPE_INTERLEAVED if rope_interleaved else 0
+    flags = (ROPE_INTERLEAVED if rope_interleaved else 0) | (QK_ROTATED if qk_rotated else 0)
     if qkv:
         st = lib.vlc_attn_fwd_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cu_seqlens_kv), nseg,
                                   total, total_kv, H, H_kv, d, int(max_seqlen), int(max_seqlen_kv),
@@ -317,9 +322,11 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                     dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                     check: bool = True, rope_interleaved: bool = False,
                     cu_seqlens_padded: Optional[torch.Tensor] = None,
-                    cu_seqlens_kv: Optional[torch.Tensor] = None, max_seqlen_kv: Optional[int] = None):
+                    cu_seqlens_kv: Optional[torch.Tensor] = None, max_seqlen_kv: Optional[int] = None,
+                    qk_rotated: bool = False):
     """Gradients (dQ, dK, dV) of sum(O * dO) for the forward above (dK, dV shaped like k, v;
-    zero at padding rows)."""
+    zero at padding rows).  qk_rotated: q and k are the rotated q', k' of ``rope_qk``; the
+    gradients returned are still with respect to the unrotated q and k."""
     lib = load_library()
     _require_cuda(dout, q, k, v, o, lse, cu_seqlens, cu_seqlens_padded, cu_seqlens_kv)
     qkv = cu_seqlens_kv is not None
@@ -343,7 +350,7 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                            total_kv if qkv else None, max_seqlen_kv if qkv else None)
     else:
         ws = workspace
-    flags = ROPE_INTERLEAVED if rope_interleaved else 0
+    flags = (ROPE_INTERLEAVED if rope_interleaved else 0) | (QK_ROTATED if qk_rotated else 0)
     if qkv:
         st = lib.vlc_attn_bwd_qkv(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
                                   _ptr(cu_seqlens_kv), nseg, total, total_kv, H, H_kv, d, int(max_seqlen),
@@ -387,6 +394,28 @@ def shifted_cross_entropy(logits: torch.Tensor, labels: torch.Tensor,
     if check:
         _raise_device_error(ws, "vlc_shifted_ce")
     return (loss, count, seg_loss, seg_count) if per_segment else (loss, count)
+
+
+def rope_qk(q: torch.Tensor, k: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,
+            rope_theta: float = 10000.0, rope_interleaved: bool = False,
+            cu_seqlens_padded: Optional[torch.Tensor] = None, out=None,
+            workspace: Optional[torch.Tensor] = None, check: bool = True):
+    """(q', k') = (R(p) q, R(p) k) with per-segment positions, for varlen_attn_fwd / _bwd with
+    qk_rotated=True (one rotation per training step instead of one per pass)."""
+    lib = load_library()
+    _require_cuda(q, k, cu_seqlens, cu_seqlens_padded)
+    H_kv = _check_qkv([q], [k])
+    total, H, d = q.shape
+    nseg = _cu_info(cu_seqlens, cu_seqlens_padded)
+    qrot, krot = (torch.empty_like(q), torch.empty_like(k)) if out is None else out
+    ws = new_workspace(nseg, total, H, d, max_seqlen, False, q.device, H_kv) if workspace is None else workspace
+    st = lib.vlc_rope_qk(_ptr(q), _ptr(k), _ptr(cu_seqlens), _ptr(cu_seqlens_padded), nseg, total, H, H_kv, d,
+                         int(max_seqlen), float(rope_theta), ROPE_INTERLEAVED if rope_interleaved else 0,
+                         _ptr(qrot), _ptr(krot), _ptr(ws), ws.numel(), _stream(q.device))
+    _check(st, "vlc_rope_qk")
+    if check:
+        _raise_device_error(ws, "vlc_rope_qk")
+    return qrot, krot
 
 
 class Packing(NamedTuple):

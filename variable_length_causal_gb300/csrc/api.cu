@@ -142,7 +142,8 @@ static int check_attn_args(const AttnArgs& a, int is_bwd) {
     if (a.nseg < 1 || a.total < 1 || a.H < 1 || a.max_seqlen < 1) return VLC_ERR_ARG;
     if (a.cu_kv != nullptr && (a.total_kv < 1 || a.max_seqlen_kv < 1)) return VLC_ERR_ARG;
     if (a.Hkv < 1 || a.H % a.Hkv != 0) return VLC_ERR_ARG;
-    if (a.flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED)) return VLC_ERR_ARG;
+    if (a.flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED | VLC_QK_ROTATED)) return VLC_ERR_ARG;
+    if ((a.flags & VLC_QK_ROTATED) && a.cu_kv != nullptr) return VLC_ERR_ARG;   // vlc_rope_qk is self-attention
     if (!(a.rope_theta >= 0.f) || !std::isfinite(a.rope_theta)) return VLC_ERR_ARG;
     if (a.d != 64 && a.d != 128) return VLC_ERR_UNSUPPORTED;
     if (a.max_seqlen > VLC_MAX_SEQLEN || a.max_seqlen_kv > VLC_MAX_SEQLEN) return VLC_ERR_UNSUPPORTED;
@@ -193,7 +194,8 @@ static int attn_fwd_impl(AttnArgs a) {
         launch_pad_fill(a.cu, a.cu_padded, a.nseg, a.total, a.o, int64_t(a.H) * a.d * 2, nullptr, 0, nullptr,
                         0, a.lse, a.H, &hdr->err, num_sms_cached(), s) != cudaSuccess)
         return VLC_ERR_CUDA;
-    const int mode = rope_mode(a.rope_theta, a.flags);
+    // operands rotated by vlc_rope_qk: the forward applies no rotation of its own
+    const int mode = (a.flags & VLC_QK_ROTATED) ? kRopeNone : rope_mode(a.rope_theta, a.flags);
     if (mode != kRopeNone && launch_rope_table(table, L.table_rows, a.d, static_cast<double>(a.rope_theta),
                                                &hdr->err, s) != cudaSuccess)
         return VLC_ERR_CUDA;
@@ -287,6 +289,7 @@ static int attn_bwd_impl(AttnArgs a) {
     p.nseg = a.nseg; p.total = a.total; p.H = a.H; p.d = a.d; p.Hkv = a.Hkv; p.total_kv = a.total_kv;
     p.scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / std::sqrt(static_cast<float>(a.d));
     p.use_rope = mode;
+    p.operands_rotated = (a.flags & VLC_QK_ROTATED) ? 1 : 0;
     if (launch_attn_bwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
     return VLC_OK;
 }
@@ -437,6 +440,43 @@ int vlc_attn_bwd(const void* dout, const void* q, const void* k, const void* v, 
                  void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
     return vlc_attn_bwd_gqa(dout, q, k, v, o, lse, cu, nseg, total, H, H, d, max_seqlen, softmax_scale,
                             rope_theta, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+int vlc_rope_qk(const void* q, const void* k, const int32_t* cu, const int32_t* cu_padded, int32_t nseg,
+                int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen, float rope_theta,
+                uint32_t flags, void* qrot, void* krot, void* ws, size_t ws_bytes, void* stream) {
+    if (q == nullptr || k == nullptr || cu == nullptr || qrot == nullptr || krot == nullptr) return VLC_ERR_ARG;
+    AttnArgs a = fwd_args(q, k, k, cu, cu_padded, nullptr, nseg, total, total, H, H_kv, d, max_seqlen, max_seqlen,
+                          0.f, rope_theta, flags, nullptr, nullptr, ws, ws_bytes, stream);
+    if (flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED)) return VLC_ERR_ARG;
+    int st = check_attn_args(a, 0);
+    if (st != VLC_OK) return st;
+    if (!(rope_theta > 0.f)) return VLC_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(qrot, 16) || !aligned(krot, 16)) return VLC_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(nseg, total, H, H_kv, d, max_seqlen, 0);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
+    float2* table = reinterpret_cast<float2*>(w + L.table);
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
+    // the work list validates cu (and cu_padded) before anything reads positions
+    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD,
+                        reinterpret_cast<int4*>(w + L.items), L.item_cap, reinterpret_cast<int32_t*>(w + L.order),
+                        reinterpret_cast<int32_t*>(w + L.seg_base), &hdr->count, &hdr->err, s, cu_padded) !=
+        cudaSuccess)
+        return VLC_ERR_CUDA;
+    const int mode = rope_mode(rope_theta, flags);
+    if (launch_rope_table(table, L.table_rows, d, static_cast<double>(rope_theta), &hdr->err, s) != cudaSuccess)
+        return VLC_ERR_CUDA;
+    FwdParams p{};
+    p.q = q; p.k = k; p.cu = cu;
+    p.rows = cu_padded != nullptr ? cu_padded : cu;
+    p.err = &hdr->err;
+    p.table = table;
+    p.nseg = nseg; p.total = total; p.H = H; p.Hkv = H_kv; p.d = d;
+    p.use_rope = mode;
+    if (launch_rope_qk(p, qrot, krot, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
+    return VLC_OK;
 }
 
 size_t vlc_workspace_bytes_qkv(int32_t nseg, int32_t total_q, int32_t total_kv, int32_t H, int32_t H_kv,

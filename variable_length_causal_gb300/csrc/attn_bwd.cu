@@ -1072,8 +1072,9 @@ template <int D>
 static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s) {
     {
         const bool sep = p.cu_kv != p.cu;   // keys with segments of their own
+        const int rot = p.operands_rotated ? kRopeNone : p.use_rope;   // rotation in this pass
         const int64_t rows = static_cast<int64_t>(p.total) * p.H +
-                             (sep && p.use_rope ? static_cast<int64_t>(p.total_kv) * p.Hkv : 0);
+                             (sep && rot ? static_cast<int64_t>(p.total_kv) * p.Hkv : 0);
         int64_t blocks = (rows * (D / 16) + 255) / 256;
         if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
         auto prep = sep ? bwd::prep_kernel<D, true> : bwd::prep_kernel<D, false>;
@@ -1081,11 +1082,12 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
             static_cast<const uint4*>(p.dout), static_cast<const uint4*>(p.o),
             static_cast<const uint4*>(p.q), static_cast<const uint4*>(p.k), static_cast<uint4*>(p.qrot),
             static_cast<uint4*>(p.krot), p.delta, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.table, p.total, p.H,
-            p.Hkv, p.total_kv, p.use_rope, p.err);
+            p.Hkv, p.total_kv, rot, p.err);
     }
     // with RoPE the attention passes read the rotated copies
-    const void* qop = p.use_rope ? p.qrot : p.q;
-    const void* kop = p.use_rope ? p.krot : p.k;
+    const bool rotated_here = p.use_rope && !p.operands_rotated;
+    const void* qop = rotated_here ? p.qrot : p.q;
+    const void* kop = rotated_here ? p.krot : p.k;
     CUtensorMap q128, do128, k128, v128;
     if (!make_tmap_thd(&q128, qop, p.total, p.H, D, 128) ||
         !make_tmap_thd(&do128, p.dout, p.total, p.H, D, 128) ||

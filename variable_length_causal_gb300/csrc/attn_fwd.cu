@@ -640,4 +640,52 @@ cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, in
     return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------- q', k' for a whole training step
+// R(p) q and R(p) k for every row, once: the forward and backward passes of a step can
+// then run on the rotated operands (no in-kernel rotation, no rotation in the
+// backward's prep pass).  Query rows first, then key rows; D/16 threads per row.
+namespace fwd {
+template <int D>
+__global__ void __launch_bounds__(256)
+rope_qk_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k, uint4* __restrict__ qrot,
+               uint4* __restrict__ krot, const int32_t* __restrict__ cu, const int32_t* __restrict__ rows,
+               int32_t nseg, const float2* __restrict__ table, int32_t total, int32_t H, int32_t Hkv, int rope,
+               const int32_t* __restrict__ err) {
+    if (*err != 0) return;
+    constexpr int TPR = D / 16;
+    constexpr int HALF = D / 16;
+    const int64_t qrows = static_cast<int64_t>(total) * H;
+    const int64_t all = qrows + static_cast<int64_t>(total) * Hkv;
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int c = threadIdx.x % TPR;
+    const bool il = rope == kRopeInterleaved;
+    for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / TPR; row < all;
+         row += nthreads / TPR) {
+        const bool isq = row < qrows;
+        const int64_t r = isq ? row : row - qrows;
+        const int64_t tok = r / (isq ? H : Hkv);
+        const int a = segment_of_row(rows, nseg, tok);
+        const int64_t pos0 = tok - __ldg(rows + a);
+        const bool real = pos0 < __ldg(cu + a + 1) - __ldg(cu + a);
+        const int64_t lo = r * (2 * HALF) + c;
+        float cs[8], sn[8];
+        if (real) load_angles<D>(table, pos0, il, c, cs, sn);
+        rotate_chunks(isq ? q : k, isq ? qrot : krot, lo, lo + HALF, cs, sn, real, il);
+    }
+}
+}  // namespace fwd
+
+cudaError_t launch_rope_qk(const FwdParams& p, void* qrot, void* krot, int num_sms, cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(p.total) * (p.H + p.Hkv);
+    int64_t blocks = (rows * (p.d / 16) + 255) / 256;
+    if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
+    if (blocks < 1) blocks = 1;
+    auto kernel = p.d == 128 ? fwd::rope_qk_kernel<128> : fwd::rope_qk_kernel<64>;
+    kernel<<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const uint4*>(p.q), static_cast<const uint4*>(p.k),
+                                                     static_cast<uint4*>(qrot), static_cast<uint4*>(krot), p.cu,
+                                                     p.rows, p.nseg, p.table, p.total, p.H, p.Hkv, p.use_rope, p.err);
+    return cudaGetLastError();
+}
+
 }  // namespace vlc

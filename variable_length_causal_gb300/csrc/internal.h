@@ -100,6 +100,11 @@ constexpr int32_t kPreRotMinKeys = 2048;
 cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, int32_t min_keys, int num_sms,
                         cudaStream_t s);
 
+// R(p) q into qrot and R(p) k into krot for every row (self-attention; rows past
+// a segment's length in a padded layout become zeros).  Uses p.q, p.k, p.cu,
+// p.rows, p.nseg, p.total, p.H, p.Hkv, p.d, p.table, p.use_rope, p.err.
+cudaError_t launch_rope_qk(const FwdParams& p, void* qrot, void* krot, int num_sms, cudaStream_t s);
+
 struct BwdParams {
     const void* dout;
     const void* q;
@@ -135,6 +140,8 @@ struct BwdParams {
     float scale;
     int use_rope;              // kRopeHalf / kRopeInterleaved: inputs are rotated in the prep
                                // pass with that pairing, gradients un-rotated; kRopeNone: no RoPE
+    int operands_rotated;      // 1: q and k already hold R(p) q, R(p) k; only the gradients are
+                               // un-rotated (the prep pass computes D alone)
 };
 
 cudaError_t launch_attn_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
