@@ -143,6 +143,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int kRingConsumers = 1 + 1 + 8 + 4;   // MMA warp, V producer, 8 softmax warps, 4 RoPE warps
+                                                    // (the RoPE warps only when there is RoPE)
 
     __shared__ int s_skip, s_nunits;
     if (threadIdx.x == 0) {   // one read, so every thread takes the same branch
@@ -173,7 +174,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bar(DRAIN), 1);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(bar(UNIT_FULL + i), 1);
-            mbar_init(bar(UNIT_EMPTY + i), kRingConsumers);
+            mbar_init(bar(UNIT_EMPTY + i), p.use_rope ? kRingConsumers : kRingConsumers - 4);
         }
         *abort = 0;
         fence_mbar_init();
@@ -244,6 +245,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false);
             constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
             uint32_t qm = 0, kvn = 0, cnt_p[2] = {0, 0}, cnt_u[2] = {0, 0};
+            // without RoPE the staged tiles go straight from the TMA barriers to the MMAs
+            const int qrb = p.use_rope ? Q_READY : Q_FULL, krb = p.use_rope ? K_READY : K_FULL;
             bool ok = true;
             auto commit = [&](uint32_t b) {
                 if (elect_one()) mma_commit(b);
@@ -270,12 +273,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const FUnit f = decode_funit<KV>(p, u);
                 const int n[2] = {f.n0, f.n1};
                 const int slot[2] = {static_cast<int>(qm % kQSlots), static_cast<int>((qm + 1) % kQSlots)};
-                if (!(ok = wait_warp(bar(Q_READY + slot[0]), (qm / kQSlots) & 1, abort))) break;
-                if (f.has1 && !(ok = wait_warp(bar(Q_READY + slot[1]), ((qm + 1) / kQSlots) & 1, abort)))
+                if (!(ok = wait_warp(bar(qrb + slot[0]), (qm / kQSlots) & 1, abort))) break;
+                if (f.has1 && !(ok = wait_warp(bar(qrb + slot[1]), ((qm + 1) / kQSlots) & 1, abort)))
                     break;
                 {
                     const int ks = kvn & 1;
-                    if (!(ok = wait_warp(bar(K_READY + ks), (kvn >> 1) & 1, abort))) break;
+                    if (!(ok = wait_warp(bar(krb + ks), (kvn >> 1) & 1, abort))) break;
                     tc_fence_after();
                     for (int t = 0; t < 2; ++t) {
                         if (n[t] == 0) continue;
@@ -307,7 +310,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         if (j + 1 < n[t]) {
                             const uint32_t kvn1 = kvj + 1;
                             if (!k_next) {
-                                if (!(ok = wait_warp(bar(K_READY + (kvn1 & 1)), (kvn1 >> 1) & 1, abort))) break;
+                                if (!(ok = wait_warp(bar(krb + (kvn1 & 1)), (kvn1 >> 1) & 1, abort))) break;
                                 tc_fence_after();
                                 k_next = true;
                             }
@@ -434,28 +437,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float inv_l = 1.f / l_run;
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                             ((valid ? tok : 0) * p.H + f.w.h) * static_cast<int64_t>(D) * 2;
-            // read O (two 32-column chunks at a time); the columns are released to the
-            // next unit as soon as the last chunk has landed, before packing and storing
+            // read all of O (one wait) and release its columns to the next unit before
+            // packing and storing
+            uint32_t ro[D / 32][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; c += 2) {
-                uint32_t ra[32], rb[32];
-                tmem_ld32(oadr + c * 32, ra);
-                tmem_ld32(oadr + c * 32 + 32, rb);
-                tmem_wait_ld();
-                if (c + 2 >= D / 32) {
-                    tc_fence_before();
-                    mbar_arrive(bar(O_EMPTY + t));
-                }
-                uint32_t pk[32];
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(oadr + c * 32, ro[c]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(O_EMPTY + t));
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    pk[e] = pack_bf16x2(__uint_as_float(ra[2 * e]) * inv_l, __uint_as_float(ra[2 * e + 1]) * inv_l);
-                    pk[16 + e] = pack_bf16x2(__uint_as_float(rb[2 * e]) * inv_l, __uint_as_float(rb[2 * e + 1]) * inv_l);
-                }
-                if (valid) {
-                    st_row64(orow + c * 64, pk, v8);
-                    st_row64(orow + c * 64 + 64, pk + 16, v8);
-                }
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(ro[c][2 * e]) * inv_l, __uint_as_float(ro[c][2 * e + 1]) * inv_l);
+                if (valid) st_row64(orow + c * 64, pk, v8);
             }
             if (valid)
                 p.lse[static_cast<int64_t>(f.w.h) * p.total + tok] = (m_run + __log2f(l_run)) * kLn2;
@@ -498,7 +494,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
         };
         if (p.use_rope == kRopeInterleaved) run(std::true_type{});
-        else run(std::false_type{});
+        else if (p.use_rope) run(std::false_type{});   // without RoPE these warps take no units
     } else if (warp == 3) {
         // ------------------------------------------------------------ TMA producer of V tiles
         setmaxnreg_dec<kCtrlRegs>();
