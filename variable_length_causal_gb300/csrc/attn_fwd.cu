@@ -437,21 +437,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float inv_l = 1.f / l_run;
             uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                             ((valid ? tok : 0) * p.H + f.w.h) * static_cast<int64_t>(D) * 2;
-            // read all of O (one wait) and release its columns to the next unit before
-            // packing and storing
-            uint32_t ro[D / 32][32];
+            // read O (two 32-column chunks at a time); the columns are released to the
+            // next unit as soon as the last chunk has landed, before packing and storing
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32(oadr + c * 32, ro[c]);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(O_EMPTY + t));
+            for (int c = 0; c < D / 32; c += 2) {
+                uint32_t ra[32], rb[32];
+                tmem_ld32(oadr + c * 32, ra);
+                tmem_ld32(oadr + c * 32 + 32, rb);
+                tmem_wait_ld();
+                if (c + 2 >= D / 32) {
+                    tc_fence_before();
+                    mbar_arrive(bar(O_EMPTY + t));
+                }
+                uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(ro[c][2 * e]) * inv_l, __uint_as_float(ro[c][2 * e + 1]) * inv_l);
-                if (valid) st_row64(orow + c * 64, pk, v8);
+                for (int e = 0; e < 16; ++e) {
+                    pk[e] = pack_bf16x2(__uint_as_float(ra[2 * e]) * inv_l, __uint_as_float(ra[2 * e + 1]) * inv_l);
+                    pk[16 + e] = pack_bf16x2(__uint_as_float(rb[2 * e]) * inv_l, __uint_as_float(rb[2 * e + 1]) * inv_l);
+                }
+                if (valid) {
+                    st_row64(orow + c * 64, pk, v8);
+                    st_row64(orow + c * 64 + 64, pk + 16, v8);
+                }
             }
             if (valid)
                 p.lse[static_cast<int64_t>(f.w.h) * p.total + tok] = (m_run + __log2f(l_run)) * kLn2;
