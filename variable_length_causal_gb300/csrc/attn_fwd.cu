@@ -647,7 +647,10 @@ cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, in
 // ---------------------------------------------------------------- q', k' for a whole training step
 // R(p) q and R(p) k for every row, once: the forward and backward passes of a step can
 // then run on the rotated operands (no in-kernel rotation, no rotation in the
-// backward's prep pass).  Query rows first, then key rows; D/16 threads per row.
+// backward's prep pass).  A block takes one token at a time: one segment search for
+// the token, each thread loads the cos/sin of its 16-byte chunk pair once and rotates
+// that chunk pair in every query head and every key head of the token (consecutive
+// threads cover consecutive 16-byte chunks of a head row).
 namespace fwd {
 template <int D>
 __global__ void __launch_bounds__(256)
@@ -656,32 +659,39 @@ rope_qk_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k, uint4* 
                int32_t nseg, const float2* __restrict__ table, int32_t total, int32_t H, int32_t Hkv, int rope,
                const int32_t* __restrict__ err) {
     if (*err != 0) return;
-    constexpr int TPR = D / 16;
+    constexpr int TPR = D / 16;               // threads per head row (chunk pairs)
     constexpr int HALF = D / 16;
-    const int64_t qrows = static_cast<int64_t>(total) * H;
-    const int64_t all = qrows + static_cast<int64_t>(total) * Hkv;
-    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int c = threadIdx.x % TPR;
+    constexpr int SLOTS = 256 / TPR;          // heads handled side by side
+    __shared__ int64_t s_pos;
+    __shared__ int s_real;
+    const int c = threadIdx.x % TPR, slot = threadIdx.x / TPR;
     const bool il = rope == kRopeInterleaved;
-    for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / TPR; row < all;
-         row += nthreads / TPR) {
-        const bool isq = row < qrows;
-        const int64_t r = isq ? row : row - qrows;
-        const int64_t tok = r / (isq ? H : Hkv);
-        const int a = segment_of_row(rows, nseg, tok);
-        const int64_t pos0 = tok - __ldg(rows + a);
-        const bool real = pos0 < __ldg(cu + a + 1) - __ldg(cu + a);
-        const int64_t lo = r * (2 * HALF) + c;
+    for (int64_t tok = blockIdx.x; tok < total; tok += gridDim.x) {
+        if (threadIdx.x == 0) {
+            const int a = segment_of_row(rows, nseg, tok);
+            const int64_t pos0 = tok - __ldg(rows + a);
+            s_real = pos0 < __ldg(cu + a + 1) - __ldg(cu + a);   // rows past a padded segment: zeros
+            s_pos = pos0;
+        }
+        __syncthreads();
+        const bool real = s_real != 0;
         float cs[8], sn[8];
-        if (real) load_angles<D>(table, pos0, il, c, cs, sn);
-        rotate_chunks(isq ? q : k, isq ? qrot : krot, lo, lo + HALF, cs, sn, real, il);
+        if (real) load_angles<D>(table, s_pos, il, c, cs, sn);
+        for (int h = slot; h < H; h += SLOTS) {
+            const int64_t lo = (tok * H + h) * (2 * HALF) + c;
+            rotate_chunks(q, qrot, lo, lo + HALF, cs, sn, real, il);
+        }
+        for (int h = slot; h < Hkv; h += SLOTS) {
+            const int64_t lo = (tok * Hkv + h) * (2 * HALF) + c;
+            rotate_chunks(k, krot, lo, lo + HALF, cs, sn, real, il);
+        }
+        __syncthreads();   // s_pos / s_real are rewritten for the next token
     }
 }
 }  // namespace fwd
 
 cudaError_t launch_rope_qk(const FwdParams& p, void* qrot, void* krot, int num_sms, cudaStream_t s) {
-    const int64_t rows = static_cast<int64_t>(p.total) * (p.H + p.Hkv);
-    int64_t blocks = (rows * (p.d / 16) + 255) / 256;
+    int64_t blocks = p.total;
     if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
     if (blocks < 1) blocks = 1;
     auto kernel = p.d == 128 ? fwd::rope_qk_kernel<128> : fwd::rope_qk_kernel<64>;
