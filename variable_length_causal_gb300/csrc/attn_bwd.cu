@@ -530,6 +530,20 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
             ok = have = stage(0);
         }
+        // this row's LSE (base 2) and D of a unit; a row past the segment gets lse2 = +inf, so
+        // its P is exp2(-inf) = 0 without a mask
+        auto row_stats = [&](const Unit& uw, float& l2, float& dd) {
+            const int qp = uw.tile * 128 + r;
+            l2 = INFINITY;
+            dd = 0.f;
+            if (qp < uw.L) {
+                const int64_t idx = static_cast<int64_t>(uw.h) * p.total + uw.row0 + qp;
+                l2 = __ldg(p.lse + idx) * kLog2e;
+                dd = __ldg(p.delta + idx);
+            }
+        };
+        float lse2_next = 0.f, dlt_next = 0.f;   // the next unit's, loaded before this unit's epilogue
+        if (have) row_stats(w, lse2_next, dlt_next);
         while (have) {
             const int qpos = w.tile * 128 + r;
             const bool valid = qpos < w.L;
@@ -539,9 +553,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             const int lastk = min(qpos + w.off, w.Lk - 1);
             const int j_edge = w.hi - 1 - ((w.off & (BK - 1)) != 0 ? 1 : 0);
             const int64_t tok = static_cast<int64_t>(w.row0) + (valid ? qpos : 0);
-            // a row past the segment gets lse2 = +inf, so its P is exp2(-inf) = 0 without a mask
-            const float lse2 = valid ? __ldg(p.lse + static_cast<int64_t>(w.h) * p.total + tok) * kLog2e : INFINITY;
-            const float dlt = valid ? __ldg(p.delta + static_cast<int64_t>(w.h) * p.total + tok) : 0.f;
+            const float lse2 = lse2_next, dlt = dlt_next;
             for (int j = 0; j < w.hi; ++j, ++kv) {
                 // ---- phase A: P = exp2(s * scale_log2 - lse2) (masked), kept packed
                 if (!(ok = wait_warp(bar(S_FULL), kv & 1, abort))) break;
@@ -605,6 +617,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             const bool have_next = u2 >= 0;
             if (have_next) {
                 w2 = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u2);
+                row_stats(w2, lse2_next, dlt_next);   // in flight across the staging and the epilogue
                 if (!(ok = stage(unit_it + 1))) break;
             }
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
