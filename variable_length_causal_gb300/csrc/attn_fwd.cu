@@ -647,9 +647,9 @@ cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, in
 // ---------------------------------------------------------------- q', k' for a whole training step
 // R(p) q and R(p) k for every row, once: the forward and backward passes of a step can
 // then run on the rotated operands (no in-kernel rotation, no rotation in the
-// backward's prep pass).  A block takes one token at a time: one segment search for
-// the token, each thread loads the cos/sin of its 16-byte chunk pair once and rotates
-// that chunk pair in every query head and every key head of the token (consecutive
+// backward's prep pass).  A block takes a contiguous run of tokens, one at a time: each
+// thread loads the cos/sin of its 16-byte chunk pair once per token and rotates that
+// chunk pair in every query head and every key head of the token (consecutive
 // threads cover consecutive 16-byte chunks of a head row).
 namespace fwd {
 template <int D>
@@ -662,21 +662,25 @@ rope_qk_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k, uint4* 
     constexpr int TPR = D / 16;               // threads per head row (chunk pairs)
     constexpr int HALF = D / 16;
     constexpr int SLOTS = 256 / TPR;          // heads handled side by side
-    __shared__ int64_t s_pos;
-    __shared__ int s_real;
     const int c = threadIdx.x % TPR, slot = threadIdx.x / TPR;
     const bool il = rope == kRopeInterleaved;
-    for (int64_t tok = blockIdx.x; tok < total; tok += gridDim.x) {
-        if (threadIdx.x == 0) {
-            const int a = segment_of_row(rows, nseg, tok);
-            const int64_t pos0 = tok - __ldg(rows + a);
-            s_real = pos0 < __ldg(cu + a + 1) - __ldg(cu + a);   // rows past a padded segment: zeros
-            s_pos = pos0;
+    // a contiguous run of tokens per block: one segment search, then the segment index
+    // only moves forward (every thread follows the same tokens, so no block barrier)
+    const int64_t per = (static_cast<int64_t>(total) + gridDim.x - 1) / gridDim.x;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t t1 = min(static_cast<int64_t>(total), t0 + per);
+    if (t0 >= t1) return;
+    int a = segment_of_row(rows, nseg, t0);
+    int64_t next = a + 1 < nseg ? __ldg(rows + a + 1) : INT64_MAX;
+    for (int64_t tok = t0; tok < t1; ++tok) {
+        while (tok >= next) {
+            ++a;
+            next = a + 1 < nseg ? __ldg(rows + a + 1) : INT64_MAX;
         }
-        __syncthreads();
-        const bool real = s_real != 0;
+        const int64_t pos0 = tok - __ldg(rows + a);
+        const bool real = pos0 < __ldg(cu + a + 1) - __ldg(cu + a);   // rows past a padded segment: zeros
         float cs[8], sn[8];
-        if (real) load_angles<D>(table, s_pos, il, c, cs, sn);
+        if (real) load_angles<D>(table, pos0, il, c, cs, sn);
         for (int h = slot; h < H; h += SLOTS) {
             const int64_t lo = (tok * H + h) * (2 * HALF) + c;
             rotate_chunks(q, qrot, lo, lo + HALF, cs, sn, real, il);
@@ -685,7 +689,6 @@ rope_qk_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k, uint4* 
             const int64_t lo = (tok * Hkv + h) * (2 * HALF) + c;
             rotate_chunks(k, krot, lo, lo + HALF, cs, sn, real, il);
         }
-        __syncthreads();   // s_pos / s_real are rewritten for the next token
     }
 }
 }  // namespace fwd
