@@ -250,7 +250,7 @@ struct Layout {
     static constexpr uint32_t V0 = K0 + kKStages * TILE;       // kVStages
     static constexpr uint32_t BAR0 = V0 + kVStages * TILE;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;      // tmem slot, abort flag, unit ring
-    static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
+    static constexpr uint32_t BYTES = MISC + 8 + 4 * kSlotInts * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     // TMEM: S at columns 0..127, dP at 128 (the packed bf16 dS of a step overwrites
     // the consumed dP columns), the dQ accumulator at 256, and the unit's Q' and dO
@@ -303,7 +303,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
-    constexpr int kRingConsumers = 1 + 1 + 8;   // MMA warp, V producer, 8 math warps
+    constexpr int kRingConsumers = 1 + 1 + 1 + 8;   // Q'/dO/K' and V producers, MMA warp, 8 math warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     __shared__ int s_skip, s_nunits;
@@ -360,8 +360,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             bool ok = true;
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
-                if (!(ok = ring_put(rg, n, p.next_q, nunits, abort, u)) || u < 0) break;
-                const Unit w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                Unit w;
+                if (!(ok = ring_get(rg, n, abort, u, w)) || u < 0) break;
                 // the staging slot frees as soon as the math warps copied the last unit's rows to TMEM
                 if (!(ok = mbar_wait(bar(QD_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(QD_FULL), 2 * LY::TILE);
@@ -396,8 +396,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             bool ok = true;
             for (int n = 0; ok; ++n) {
                 int u;
-                if (!(ok = ring_get(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                Unit w;
+                if (!(ok = ring_get(rg, n, abort, u, w)) || u < 0) break;
                 for (int j = 0; j < w.hi && ok; ++j) {
                     const uint32_t nn = kv + j;
                     const int vs = nn % kVStages;
@@ -464,8 +464,8 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             };
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
-                if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                Unit w;
+                if (!(ok = ring_get_warp(rg, n, abort, u, w)) || u < 0) break;
                 if (!(ok = wait_warp(bar(QT_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_s(kv))) break;
                 if (!(ok = issue_dp(kv))) break;
@@ -497,6 +497,19 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             mbar_wait_limit(bar(DRAIN), 0, kDrainNs);
         }
         __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ unit scheduler (after the
+        // TMEM allocation): claims and decodes units ahead of the other roles
+        if (lane == 0) {
+            auto decode = [&](int u) {
+                return decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+            };
+            for (int n = 0;; ++n) {
+                int u;
+                if (!ring_put(rg, n, p.next_q, nunits, abort, decode, u) || u < 0) break;
+            }
+        }
+        __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ Q'/dO staging, P, dS + epilogue
         const int g = (warp - 4) >> 2;             // math warpgroup: key columns [64g, 64g + 64)
@@ -523,13 +536,10 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             return true;
         };
         int u = -1;
-        bool ok = ring_get_warp(rg, 0, abort, u);
-        bool have = ok && u >= 0;
         Unit w{};
-        if (have) {
-            w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
-            ok = have = stage(0);
-        }
+        bool ok = ring_get_warp(rg, 0, abort, u, w);
+        bool have = ok && u >= 0;
+        if (have) ok = have = stage(0);
         // this row's LSE (base 2) and D of a unit; a row past the segment gets lse2 = +inf, so
         // its P is exp2(-inf) = 0 without a mask
         auto row_stats = [&](const Unit& uw, float& l2, float& dd) {
@@ -613,10 +623,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             // stage the next unit before this unit's epilogue, so its first MMAs can start
             Unit w2{};
             int u2 = -1;
-            if (!(ok = ring_get_warp(rg, static_cast<int>(unit_it) + 1, abort, u2))) break;
+            if (!(ok = ring_get_warp(rg, static_cast<int>(unit_it) + 1, abort, u2, w2))) break;
             const bool have_next = u2 >= 0;
             if (have_next) {
-                w2 = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u2);
                 row_stats(w2, lse2_next, dlt_next);   // in flight across the staging and the epilogue
                 if (!(ok = stage(unit_it + 1))) break;
             }
@@ -696,7 +705,7 @@ struct Layout {
     static constexpr uint32_t LSED = DO0 + kQStages * TILE;    // kLsedSlots x (128 lse2 + 128 delta)
     static constexpr uint32_t BAR0 = LSED + kLsedSlots * 256 * 4;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;      // tmem slot, abort flag, unit ring
-    static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
+    static constexpr uint32_t BYTES = MISC + 8 + 4 * kSlotInts * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     // TMEM: S^T at 0, dP^T at 128 (the packed bf16 P^T / dS^T of a step overwrite the
     // consumed S^T / dP^T columns), dV and dK accumulators after them.
@@ -716,7 +725,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
-    constexpr int kRingConsumers = 1 + 1 + 8;   // MMA warp, LSE/delta stager warp, 8 math warps
+    constexpr int kRingConsumers = 1 + 1 + 1 + 8;   // TMA producer, MMA warp, LSE/delta stager, 8 math warps
     float* lsed = reinterpret_cast<float*>(sgen + LY::LSED);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = p.H / p.Hkv;   // query heads per key/value head: a unit runs over all of them
@@ -773,8 +782,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             bool ok = true;
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
-                if (!(ok = ring_put(rg, n, p.next_k, nunits, abort, u)) || u < 0) break;
-                const Unit w = decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);   // w.h: key/value head
+                Unit w;   // w.h: key/value head
+                if (!(ok = ring_get(rg, n, abort, u, w)) || u < 0) break;
                 if (!(ok = mbar_wait(bar(KV_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                 mbar_expect_tx(bar(KV_FULL), 2 * LY::TILE);
                 const int krow = w.row0k + w.tile * 128;
@@ -848,8 +857,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             };
             for (int n = 0; ok; ++n, ++unit_it) {
                 int u;
-                if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-                const Unit w = decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+                Unit w;
+                if (!(ok = ring_get_warp(rg, n, abort, u, w)) || u < 0) break;
                 if (!(ok = wait_warp(bar(KV_FULL), unit_it & 1, abort))) break;
                 if (!(ok = issue_st(st))) break;
                 issue_dpt(st);
@@ -903,8 +912,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         bool ok = true;
         for (int n = 0; ok; ++n) {
             int u;
-            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+            Unit w;
+            if (!(ok = ring_get_warp(rg, n, abort, u, w)) || u < 0) break;
             const int nq = w.hi - w.lo;
             for (int sq = 0; sq < grp * nq && ok; ++sq, ++st) {
                 const int i = w.lo + sq % nq, hq = w.h * grp + sq / nq;
@@ -930,6 +939,19 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 if (lane == 0) mbar_arrive(bar(LSED_FULL + sl));
             }
         }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ unit scheduler (after the
+        // TMEM allocation): claims and decodes units ahead of the other roles
+        if (lane == 0) {
+            auto decode = [&](int u) {
+                return decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+            };
+            for (int n = 0;; ++n) {
+                int u;
+                if (!ring_put(rg, n, p.next_k, nunits, abort, decode, u) || u < 0) break;
+            }
+        }
+        __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ P^T, dS^T + epilogue
         const int g = (warp - 4) >> 2;             // math warpgroup: q columns [64g, 64g + 64)
@@ -940,11 +962,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const bool v8 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31) == 0;
         const int c0 = 64 * g;
         uint32_t unit_it = 0, st = 0;
-        bool ok = true;
-        for (int n = 0; ok; ++n, ++unit_it) {
-            int u;
-            if (!(ok = ring_get_warp(rg, n, abort, u)) || u < 0) break;
-            const Unit w = decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+        int u = -1;
+        Unit w{};
+        bool ok = ring_get_warp(rg, 0, abort, u, w);
+        for (int n = 0; ok && u >= 0; ++n, ++unit_it) {
             const int kvpos = w.tile * 128 + r;
             const int nq = w.hi - w.lo;
             for (int sq = 0; sq < grp * nq; ++sq, ++st) {
@@ -1027,6 +1048,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 mbar_arrive(bar(DST_FULL));
             }
             if (!ok) break;
+            // the next unit is taken from the ring here, so that its first steps follow the epilogue
+            int u2 = -1;
+            Unit w2{};
+            if (!(ok = ring_get_warp(rg, n + 1, abort, u2, w2))) break;
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
             tc_fence_after();
             const bool valid = kvpos < w.Lk;
@@ -1056,6 +1081,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             }
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));
+            w = w2;
+            u = u2;
         }
     }
 

@@ -79,41 +79,60 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 }
 
 // ---------------------------------------------------------------- dynamic unit ring
-// The producer thread claims work units from a global counter (longest first,
-// so CTAs that finish early take the next unit and the units in flight stay a
-// contiguous window of the work list) and publishes each index in a ring of
-// kRing shared-memory slots; every role consumes the same sequence in order.
-// A unit index of -1 ends the sequence.
-constexpr int kRing = 8;
+// A scheduler thread claims work units from a global counter (longest first, so
+// CTAs that finish early take the next unit and the units in flight stay a
+// contiguous window of the work list), decodes each one (a chain of dependent
+// global loads: the binary search over the sorted segments, then the item and
+// the segment's offsets) and publishes index and decoded unit in a ring of kRing
+// shared-memory slots; every other role consumes the same sequence in order and
+// reads the decoded unit from the slot.  The ring depth bounds how far the
+// scheduler claims ahead of the slowest role (kRing - 1 units).  A unit index of
+// -1 ends the sequence.
+constexpr int kRing = 4;
+constexpr int kSlotInts = 12;   // unit index + the 10 fields of Unit, padded
 
 struct Ring {
-    volatile int* slot;     // kRing ints in shared memory
+    volatile int* slot;     // kRing x kSlotInts ints in shared memory
     uint32_t full0, empty0; // barrier addresses of slot 0 (8-byte stride)
 };
 
+// Scheduler thread: `decode(u)` gives the Unit of index u.
+template <class Decode>
 __device__ __forceinline__ bool ring_put(const Ring& rg, int n, int* counter, int nunits,
-                                         volatile int* abort, int& u_out) {
+                                         volatile int* abort, Decode&& decode, int& u_out) {
     const int s = n % kRing;
     if (!mbar_wait(rg.empty0 + 8u * s, ((n / kRing) & 1) ^ 1, abort)) return false;
     int u = atomicAdd(counter, 1);
     if (u >= nunits) u = -1;
-    rg.slot[s] = u;
-    mbar_arrive(rg.full0 + 8u * s);   // release: waiters see the index
+    volatile int* d = rg.slot + s * kSlotInts;
+    if (u >= 0) {
+        const Unit w = decode(u);
+        d[1] = w.seg; d[2] = w.tile; d[3] = w.lo; d[4] = w.hi; d[5] = w.h;
+        d[6] = w.L; d[7] = w.row0; d[8] = w.Lk; d[9] = w.row0k; d[10] = w.off;
+    }
+    d[0] = u;
+    mbar_arrive(rg.full0 + 8u * s);   // release: waiters see the slot
     u_out = u;
     return true;
 }
 
-// One consumer thread (the MMA issuer).
-__device__ __forceinline__ bool ring_get(const Ring& rg, int n, volatile int* abort, int& u_out) {
+__device__ __forceinline__ void ring_read(const volatile int* d, int& u, Unit& w) {
+    u = d[0];
+    w.seg = d[1]; w.tile = d[2]; w.lo = d[3]; w.hi = d[4]; w.h = d[5];
+    w.L = d[6]; w.row0 = d[7]; w.Lk = d[8]; w.row0k = d[9]; w.off = d[10];
+}
+
+// One consumer thread (a TMA producer or the MMA issuer).
+__device__ __forceinline__ bool ring_get(const Ring& rg, int n, volatile int* abort, int& u_out, Unit& w) {
     const int s = n % kRing;
     if (!mbar_wait(rg.full0 + 8u * s, (n / kRing) & 1, abort)) return false;
-    u_out = rg.slot[s];
+    ring_read(rg.slot + s * kSlotInts, u_out, w);
     mbar_arrive(rg.empty0 + 8u * s);
     return true;
 }
 
 // A whole consumer warp; lane 0 releases the slot once every lane has read it.
-__device__ __forceinline__ bool ring_get_warp(const Ring& rg, int n, volatile int* abort, int& u_out);
+__device__ __forceinline__ bool ring_get_warp(const Ring& rg, int n, volatile int* abort, int& u_out, Unit& w);
 
 // 16-byte chunk `ci` (0..7) of row `r` inside a block of rows x 128 bytes with
 // the 128-byte swizzle used by both TMA and the MMA descriptors.
@@ -122,10 +141,10 @@ __device__ __forceinline__ uint32_t sw128(uint32_t block_base, int r, int ci) {
            static_cast<uint32_t>(((ci ^ (r & 7)) & 7) << 4);
 }
 
-__device__ __forceinline__ bool ring_get_warp(const Ring& rg, int n, volatile int* abort, int& u_out) {
+__device__ __forceinline__ bool ring_get_warp(const Ring& rg, int n, volatile int* abort, int& u_out, Unit& w) {
     const int s = n % kRing;
     if (!wait_warp(rg.full0 + 8u * s, (n / kRing) & 1, abort)) return false;
-    u_out = rg.slot[s];
+    ring_read(rg.slot + s * kSlotInts, u_out, w);
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(rg.empty0 + 8u * s);
     return true;

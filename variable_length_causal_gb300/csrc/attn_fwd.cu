@@ -82,7 +82,7 @@ struct Layout {
     static constexpr uint32_t V0 = K0 + 2 * TILE;      // 2 stages
     static constexpr uint32_t BAR0 = V0 + 2 * TILE;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;   // tmem slot, abort flag, unit ring
-    static constexpr uint32_t BYTES = MISC + 8 + 4 * kRing;
+    static constexpr uint32_t BYTES = MISC + 8 + 4 * kSlotInts * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }   // P_t shares these columns
     __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + 128u * t; }
@@ -104,9 +104,9 @@ struct FUnit {
 };
 
 template <bool KV>
-__device__ __forceinline__ FUnit decode_funit(const FwdParams& p, int u) {
+__device__ __forceinline__ FUnit make_funit(const FwdParams& p, const Unit& w) {
     FUnit f;
-    f.w = decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+    f.w = w;
     const int T = (f.w.L + BQ - 1) / BQ;
     const int s = T & 1;
     const bool lone = (s != 0) && (f.w.tile == 0);
@@ -142,7 +142,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr int kRingConsumers = 1 + 1 + 8 + 4;   // MMA warp, V producer, 8 softmax warps, 4 RoPE warps
+    constexpr int kRingConsumers = 1 + 1 + 1 + 8 + 4;   // Q/K and V producers, MMA warp, 8 softmax warps, 4 RoPE warps
                                                     // (the RoPE warps only when there is RoPE)
 
     __shared__ int s_skip, s_nunits;
@@ -206,8 +206,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             bool ok = true;
             for (int n = 0; ok; ++n) {
                 int u;
-                if (!(ok = ring_put(rg, n, p.next, nunits, abort, u)) || u < 0) break;
-                const FUnit f = decode_funit<KV>(p, u);
+                Unit w;
+                if (!(ok = ring_get(rg, n, abort, u, w)) || u < 0) break;
+                const FUnit f = make_funit<KV>(p, w);
                 for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
                     const int slot = qm % kQSlots;
                     if (!(ok = mbar_wait(bar(Q_EMPTY + slot), ((qm / kQSlots) & 1) ^ 1, abort))) break;
@@ -269,8 +270,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             };
             for (int un = 0; ok; ++un) {
                 int u;
-                if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
-                const FUnit f = decode_funit<KV>(p, u);
+                Unit uw;
+                if (!(ok = ring_get_warp(rg, un, abort, u, uw)) || u < 0) break;
+                const FUnit f = make_funit<KV>(p, uw);
                 const int n[2] = {f.n0, f.n1};
                 const int slot[2] = {static_cast<int>(qm % kQSlots), static_cast<int>((qm + 1) % kQSlots)};
                 if (!(ok = wait_warp(bar(qrb + slot[0]), (qm / kQSlots) & 1, abort))) break;
@@ -347,8 +349,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         for (int un = 0; ok; ++un) {
             int u;
-            if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
-            const FUnit f = decode_funit<KV>(p, u);
+            Unit uw;
+            if (!(ok = ring_get_warp(rg, un, abort, u, uw)) || u < 0) break;
+            const FUnit f = make_funit<KV>(p, uw);
             const int nt = t == 0 ? f.n0 : f.n1;
             if (nt == 0) continue;
             const int qpos = (f.q0 + t) * BQ + r;
@@ -477,8 +480,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             bool ok = true;
             for (int un = 0; ok; ++un) {
                 int u;
-                if (!(ok = ring_get_warp(rg, un, abort, u)) || u < 0) break;
-                const FUnit f = decode_funit<KV>(p, u);
+                Unit uw;
+                if (!(ok = ring_get_warp(rg, un, abort, u, uw)) || u < 0) break;
+                const FUnit f = make_funit<KV>(p, uw);
                 for (int t = 0; t < 1 + (f.has1 ? 1 : 0) && ok; ++t) {
                     const int slot = qm % kQSlots;
                     if (!(ok = wait_warp(bar(Q_FULL + slot), (qm / kQSlots) & 1, abort))) break;
@@ -511,8 +515,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             bool ok = true;
             for (int un = 0; ok; ++un) {
                 int u;
-                if (!(ok = ring_get(rg, un, abort, u)) || u < 0) break;
-                const FUnit f = decode_funit<KV>(p, u);
+                Unit uw;
+                if (!(ok = ring_get(rg, un, abort, u, uw)) || u < 0) break;
+                const FUnit f = make_funit<KV>(p, uw);
                 for (int j = 0; j < f.nk && ok; ++j) {
                     const uint32_t n = vn + j;
                     const int vs = n & 1;
@@ -529,7 +534,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         __syncwarp();
     } else {
-        setmaxnreg_dec<kCtrlRegs>();   // warp 2: TMEM allocator
+        // ------------------------------------------------------------ warp 2: TMEM allocator, then
+        // the unit scheduler (claims and decodes units ahead of the other roles)
+        setmaxnreg_dec<kCtrlRegs>();
+        if (lane == 0) {
+            auto decode = [&](int u) {
+                return decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+            };
+            for (int n = 0;; ++n) {
+                int u;
+                if (!ring_put(rg, n, p.next, nunits, abort, decode, u) || u < 0) break;
+            }
+        }
+        __syncwarp();
     }
 
     __syncthreads();
