@@ -88,7 +88,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 // reads the decoded unit from the slot.  The ring depth bounds how far the
 // scheduler claims ahead of the slowest role (kRing - 1 units).  A unit index of
 // -1 ends the sequence.
-constexpr int kRing = 4;
+constexpr int kRing = 2;
 constexpr int kSlotInts = 12;   // unit index + the 10 fields of Unit, padded
 
 struct Ring {
