@@ -984,11 +984,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 tc_fence_after();
                 uint32_t pp[32];
                 auto phase_a = [&](auto masked) {
+                    uint32_t sr0[32], sr1[32];   // both halves in flight before the first wait
+                    tmem_ld32(tmem + lane_off + c0, sr0);
+                    tmem_ld32(tmem + lane_off + c0 + 32, sr1);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        uint32_t sr[32];
-                        tmem_ld32(tmem + lane_off + c0 + 32 * h, sr);
-                        tmem_wait_ld();
+                        const uint32_t* sr = h == 0 ? sr0 : sr1;
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
                             const float2 lz = *reinterpret_cast<const float2*>(l2s + 32 * h + e);
