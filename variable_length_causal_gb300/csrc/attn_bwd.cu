@@ -689,8 +689,8 @@ enum : int {
     QO_FULL = 2, QO_EMPTY = 2 + kQStages,
     ST_FULL = 2 + 2 * kQStages, DPT_FULL = ST_FULL + 1, PT_FULL = ST_FULL + 2, DST_FULL = ST_FULL + 3,
     LSED_FULL = ST_FULL + 4, LSED_EMPTY = LSED_FULL + kLsedSlots,
-    ACC_FULL = LSED_EMPTY + kLsedSlots, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2,
-    UNIT_FULL = ACC_FULL + 3, UNIT_EMPTY = UNIT_FULL + kRing, NUM_BARS = UNIT_EMPTY + kRing
+    ACC_FULL = LSED_EMPTY + kLsedSlots, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2, DV_FULL = ACC_FULL + 3,
+    UNIT_FULL = ACC_FULL + 4, UNIT_EMPTY = UNIT_FULL + kRing, NUM_BARS = UNIT_EMPTY + kRing
 };
 
 template <int D>
@@ -756,6 +756,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         }
         mbar_init(bar(ACC_FULL), 1);
         mbar_init(bar(ACC_EMPTY), 256);
+        mbar_init(bar(DV_FULL), 1);
         mbar_init(bar(DRAIN), 1);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(bar(UNIT_FULL + i), 1);
@@ -882,6 +883,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                                         IDESC_ACC, (sq > 0 || k > 0) ? 1u : 0u);
                     }
                     __syncwarp();
+                    // after the unit's last dV MMA the dV epilogue can start under the last dK MMA
+                    if (sq + 1 == nsteps) commit(bar(DV_FULL));
                     if (sq + 1 < nsteps && !(ok = issue_st(st + 1))) break;
                     // dK += dS^T Q' (dS^T packed over the dP^T columns)
                     if (!(ok = wait_warp(bar(DST_FULL), st & 1, abort))) break;
@@ -1054,7 +1057,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             int u2 = -1;
             Unit w2{};
             if (!(ok = ring_get_warp(rg, n + 1, abort, u2, w2))) break;
-            if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
+            if (!(ok = wait_warp(bar(DV_FULL), unit_it & 1, abort))) break;
             tc_fence_after();
             const bool valid = kvpos < w.Lk;
             const int64_t tok = static_cast<int64_t>(w.row0k) + (valid ? kvpos : 0);
@@ -1072,6 +1075,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
                 if (valid) st_row64(reinterpret_cast<uint8_t*>(p.dv) + roff + col * 2, pk, v8);
             }
+            if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
+            tc_fence_after();
             {
                 uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dk) + roff;
                 if (p.use_rope == kRopeInterleaved)
