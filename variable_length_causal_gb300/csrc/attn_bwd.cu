@@ -681,6 +681,15 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
 namespace dkdv {
 
 constexpr int BQ = 128;       // q rows per step (N = 128 keeps the S^T / dP^T MMAs at full rate)
+// 4 control warps (TMA, MMA, scheduler, LSE/delta stager), 8 math warps (P^T, dS^T) and 4
+// epilogue warps (dV, dK out of TMEM), so that the math warps go on to the next unit while
+// the epilogue warps drain the accumulators.  The block's 128 registers per thread are
+// re-split at run time: the launcher checks that the kernel was built with exactly 128.
+constexpr int kThreadsKV = 512;
+constexpr uint32_t kLaunchRegsKV = 65536 / kThreadsKV;
+constexpr uint32_t kCtrlRegs = 80, kMathRegs = 144, kEpiRegs = 144;
+static_assert(kCtrlRegs % 8 == 0 && kMathRegs % 8 == 0 && kEpiRegs % 8 == 0, "register counts are multiples of 8");
+static_assert(kCtrlRegs + 2 * kMathRegs + kEpiRegs <= 4 * kLaunchRegsKV, "register split exceeds the pool");
 constexpr int kQStages = 2;
 constexpr int kLsedSlots = 3;
 
@@ -690,7 +699,7 @@ enum : int {
     ST_FULL = 2 + 2 * kQStages, DPT_FULL = ST_FULL + 1, PT_FULL = ST_FULL + 2, DST_FULL = ST_FULL + 3,
     LSED_FULL = ST_FULL + 4, LSED_EMPTY = LSED_FULL + kLsedSlots,
     ACC_FULL = LSED_EMPTY + kLsedSlots, ACC_EMPTY = ACC_FULL + 1, DRAIN = ACC_FULL + 2, DV_FULL = ACC_FULL + 3,
-    UNIT_FULL = ACC_FULL + 4, UNIT_EMPTY = UNIT_FULL + kRing, NUM_BARS = UNIT_EMPTY + kRing
+    DV_EMPTY = ACC_FULL + 4, UNIT_FULL = ACC_FULL + 5, UNIT_EMPTY = UNIT_FULL + kRing, NUM_BARS = UNIT_EMPTY + kRing
 };
 
 template <int D>
@@ -713,7 +722,7 @@ struct Layout {
 };
 
 template <int D, bool KV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsKV, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
             const BwdParams p) {
@@ -725,7 +734,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 8), bar(UNIT_FULL), bar(UNIT_EMPTY)};
-    constexpr int kRingConsumers = 1 + 1 + 1 + 8;   // TMA producer, MMA warp, LSE/delta stager, 8 math warps
+    constexpr int kRingConsumers = 1 + 1 + 1 + 8 + 4;   // TMA producer, MMA warp, LSE/delta stager, 8 math warps,
+                                                        // 4 epilogue warps
     float* lsed = reinterpret_cast<float*>(sgen + LY::LSED);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = p.H / p.Hkv;   // query heads per key/value head: a unit runs over all of them
@@ -755,8 +765,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             mbar_init(bar(LSED_EMPTY + i), 8);
         }
         mbar_init(bar(ACC_FULL), 1);
-        mbar_init(bar(ACC_EMPTY), 256);
+        mbar_init(bar(ACC_EMPTY), 128);   // dK columns read by the 4 epilogue warps
         mbar_init(bar(DV_FULL), 1);
+        mbar_init(bar(DV_EMPTY), 128);    // dV columns read
         mbar_init(bar(DRAIN), 1);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(bar(UNIT_FULL + i), 1);
@@ -776,6 +787,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     uint32_t kv_issued = 0, q_issued = 0;
 
     if (warp == 0) {
+        setmaxnreg_dec<kCtrlRegs>();
         if (lane == 0) {   // ---------------------------------------- TMA producer
             const uint64_t pol_stream = make_l2_policy_evict_first();   // K/V: once per unit
             const uint64_t pol_keep = make_l2_policy_evict_last();      // q/dO: re-read by other units
@@ -814,6 +826,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         }
         __syncwarp();
     } else if (warp == 1) {
+        setmaxnreg_dec<kCtrlRegs>();
         {   // ---------------------------------------- MMA issuer (converged warp, one elected lane issues)
             constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, BQ, false);
             constexpr uint32_t IDESC_ACC = idesc_bf16_f32(128, D, true);
@@ -872,8 +885,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     const int s = st % kQStages;
                     const uint64_t qdm = smem_desc_sw128(sbase + LY::Q0 + s * LY::TILE, LY::BLK, 1024);
                     const uint64_t odm = smem_desc_sw128(sbase + LY::DO0 + s * LY::TILE, LY::BLK, 1024);
-                    // dV += P^T dO (P^T packed over the S^T columns)
-                    if (sq == 0 && !(ok = wait_warp(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
+                    // dV += P^T dO (P^T packed over the S^T columns); the first one overwrites dV,
+                    // so the epilogue warps must have read the previous unit's
+                    if (sq == 0 && !(ok = wait_warp(bar(DV_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                     if (!(ok = wait_warp(bar(PT_FULL), st & 1, abort))) break;
                     tc_fence_after();
                     if (elect_one()) {
@@ -887,6 +901,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                     if (sq + 1 == nsteps) commit(bar(DV_FULL));
                     if (sq + 1 < nsteps && !(ok = issue_st(st + 1))) break;
                     // dK += dS^T Q' (dS^T packed over the dP^T columns)
+                    if (sq == 0 && !(ok = wait_warp(bar(ACC_EMPTY), (unit_it & 1) ^ 1, abort))) break;
                     if (!(ok = wait_warp(bar(DST_FULL), st & 1, abort))) break;
                     tc_fence_after();
                     if (elect_one()) {
@@ -910,6 +925,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         }
         __syncwarp();
     } else if (warp == 3) {
+        setmaxnreg_dec<kCtrlRegs>();
         // ------------------------------------------------------------ LSE / delta stager
         uint32_t st = 0;
         bool ok = true;
@@ -943,6 +959,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             }
         }
     } else if (warp == 2) {
+        setmaxnreg_dec<kCtrlRegs>();
         // ------------------------------------------------------------ unit scheduler (after the
         // TMEM allocation): claims and decodes units ahead of the other roles
         if (lane == 0) {
@@ -955,20 +972,21 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ P^T, dS^T + epilogue
+    } else if (warp < 12) {
+        // ------------------------------------------------------------ P^T, dS^T
+        setmaxnreg_inc<kMathRegs>();
         const int g = (warp - 4) >> 2;             // math warpgroup: q columns [64g, 64g + 64)
         const int wq = warp & 3;
         const int r = wq * 32 + lane;              // key row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const float scale_log2 = p.scale * kLog2e;
-        const bool v8 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31) == 0;
         const int c0 = 64 * g;
-        uint32_t unit_it = 0, st = 0;
-        int u = -1;
-        Unit w{};
-        bool ok = ring_get_warp(rg, 0, abort, u, w);
-        for (int n = 0; ok && u >= 0; ++n, ++unit_it) {
+        uint32_t st = 0;
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            int u;
+            Unit w;
+            if (!(ok = ring_get_warp(rg, n, abort, u, w)) || u < 0) break;
             const int kvpos = w.tile * 128 + r;
             const int nq = w.hi - w.lo;
             for (int sq = 0; sq < grp * nq; ++sq, ++st) {
@@ -1052,44 +1070,63 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                 tc_fence_before();
                 mbar_arrive(bar(DST_FULL));
             }
-            if (!ok) break;
-            // the next unit is taken from the ring here, so that its first steps follow the epilogue
-            int u2 = -1;
-            Unit w2{};
-            if (!(ok = ring_get_warp(rg, n + 1, abort, u2, w2))) break;
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue: dV, R(p)^T dK
+        if constexpr (kEpiRegs > kLaunchRegsKV) setmaxnreg_inc<kEpiRegs>();
+        else setmaxnreg_dec<kEpiRegs>();
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;              // key row = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const bool v8 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) & 31) == 0;
+        uint32_t unit_it = 0;
+        bool ok = true;
+        for (int n = 0; ok; ++n, ++unit_it) {
+            int u;
+            Unit w;
+            if (!(ok = ring_get_warp(rg, n, abort, u, w)) || u < 0) break;
+            const int kvpos = w.tile * 128 + r;
             if (!(ok = wait_warp(bar(DV_FULL), unit_it & 1, abort))) break;
             tc_fence_after();
             const bool valid = kvpos < w.Lk;
             const int64_t tok = static_cast<int64_t>(w.row0k) + (valid ? kvpos : 0);
             const int64_t roff = (tok * p.Hkv + w.h) * static_cast<int64_t>(D) * 2;
-            // each warpgroup stores half of dV (plain copy) and half of dK (scale and R(p)^T)
+            // dV: the whole row packed to bf16 first, so its columns go back to the MMA warp
+            // before the stores
+            uint32_t pv[D / 2];
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                const int col = g * (D / 2) + c * 32;
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t rr[32];
-                tmem_ld32(tmem + lane_off + LY::DV_COL + col, rr);
+                tmem_ld32(tmem + lane_off + LY::DV_COL + c * 32, rr);
                 tmem_wait_ld();
-                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
-                if (valid) st_row64(reinterpret_cast<uint8_t*>(p.dv) + roff + col * 2, pk, v8);
+                    pv[16 * c + e] = pack_bf16x2(__uint_as_float(rr[2 * e]), __uint_as_float(rr[2 * e + 1]));
             }
+            tc_fence_before();
+            mbar_arrive(bar(DV_EMPTY));
+            if (valid) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
+                    st_row64(reinterpret_cast<uint8_t*>(p.dv) + roff + c * 64, pv + 16 * c, v8);
+            }
+            // dK: scale and R(p)^T over all of the row's rotation pairs
             if (!(ok = wait_warp(bar(ACC_FULL), unit_it & 1, abort))) break;
             tc_fence_after();
             {
                 uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dk) + roff;
-                if (p.use_rope == kRopeInterleaved)
-                    store_unrotated<D, true>(tmem + lane_off + LY::DK_COL, p.table2, p.table_rows, kvpos, p.scale,
-                                             true, valid, row_out, v8, g);
-                else
-                    store_unrotated<D, false>(tmem + lane_off + LY::DK_COL, p.table2, p.table_rows, kvpos,
-                                              p.scale, p.use_rope != 0, valid, row_out, v8, g);
+#pragma unroll 1
+                for (int part = 0; part < 2; ++part) {
+                    if (p.use_rope == kRopeInterleaved)
+                        store_unrotated<D, true>(tmem + lane_off + LY::DK_COL, p.table2, p.table_rows, kvpos,
+                                                 p.scale, true, valid, row_out, v8, part);
+                    else
+                        store_unrotated<D, false>(tmem + lane_off + LY::DK_COL, p.table2, p.table_rows, kvpos,
+                                                  p.scale, p.use_rope != 0, valid, row_out, v8, part);
+                }
             }
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));
-            w = w2;
-            u = u2;
         }
     }
 
@@ -1152,9 +1189,14 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
     {
         constexpr uint32_t smem = bwd::dkdv::Layout<D>::ALLOC;
         auto kernel = kv ? bwd::dkdv::dkdv_kernel<D, true> : bwd::dkdv::dkdv_kernel<D, false>;
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        // the warp roles re-split the register pool: valid only at the launch count it assumes
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
         if (e != cudaSuccess) return e;
-        kernel<<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
+        if (fa.numRegs != static_cast<int>(bwd::dkdv::kLaunchRegsKV)) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        kernel<<<num_sms, bwd::dkdv::kThreadsKV, smem, s>>>(q128, do128, k128, v128, p);
     }
     return cudaGetLastError();
 }
