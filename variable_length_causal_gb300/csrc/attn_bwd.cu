@@ -178,8 +178,7 @@ __device__ __forceinline__ void store_unrotated(uint32_t taddr, const float2* __
             }
             if (valid) st_row32(row_out + cb * 2, pk, v8);
         }
-        return;
-    }
+    } else {
     // rotate-half: 16-pair sub-chunks (four table loads), pairs [part*half/2, +half/2)
 #pragma unroll
     for (int b = 0; b < half / 32; ++b) {
@@ -217,6 +216,91 @@ __device__ __forceinline__ void store_unrotated(uint32_t taddr, const float2* __
             st_row32(row_out + (half + j0) * 2, phi, v8);
         }
     }
+    }
+}
+
+// The same with the row's cos/sin loaded ahead (load_unrot_tables, D/2 floats for this
+// part's pairs in sub-chunk order), for a warp that has the registers to hold them while
+// it waits for the accumulator.
+template <int D, bool IL>
+__device__ __forceinline__ void load_unrot_tables(const float2* __restrict__ tab2, int tab_rows, int pos,
+                                                  int part, float (&tb)[D / 2]) {
+    const float2* trow = tab2 + static_cast<int64_t>(pos) * 4;
+    const int64_t jstride = static_cast<int64_t>(tab_rows) * 4;   // float2 per group of 4 frequencies
+    if constexpr (IL) {
+#pragma unroll
+        for (int b = 0; b < D / 32; ++b) {   // 16-column sub-chunks: 8 pairs, two loads
+            const int cb = part * (D / 2) + b * 16;
+            ld_nc_v8(trow + (cb / 8) * jstride, tb + 16 * b);
+            ld_nc_v8(trow + (cb / 8 + 1) * jstride, tb + 16 * b + 8);
+        }
+    } else {
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) {   // 16-pair sub-chunks: four loads
+            const int j0 = part * (D / 4) + b * 16;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) ld_nc_v8(trow + (j0 / 4 + m) * jstride, tb + 32 * b + 8 * m);
+        }
+    }
+}
+
+template <int D, bool IL>
+__device__ __forceinline__ void store_unrotated_tb(uint32_t taddr, const float (&tb)[D / 2], float scale, bool rope,
+                                                   bool valid, uint8_t* __restrict__ row_out, bool v8, int part) {
+    constexpr int half = D / 2;
+    if constexpr (IL) {
+#pragma unroll
+        for (int b = 0; b < D / 32; ++b) {
+            const int cb = part * (D / 2) + b * 16;   // first column
+            uint32_t r[16];
+            tmem_ld16(taddr + cb, r);
+            tmem_wait_ld();
+            uint32_t pk[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {   // pair cb/2 + q at columns cb + 2q, cb + 2q + 1
+                float x = __uint_as_float(r[2 * q]) * scale, y = __uint_as_float(r[2 * q + 1]) * scale;
+                if (rope) {
+                    const float c = tb[16 * b + 2 * q], s = tb[16 * b + 2 * q + 1];
+                    const float u = x * c + y * s, w = y * c - x * s;
+                    x = u; y = w;
+                }
+                pk[q] = pack_bf16x2(x, y);
+            }
+            if (valid) st_row32(row_out + cb * 2, pk, v8);
+        }
+    } else {
+#pragma unroll
+        for (int b = 0; b < half / 32; ++b) {
+            const int j0 = part * (half / 2) + b * 16;
+            uint32_t lo[16], hi[16];
+            tmem_ld16(taddr + j0, lo);
+            tmem_ld16(taddr + half + j0, hi);
+            tmem_wait_ld();
+            uint32_t plo[8], phi[8];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {   // pairs j0 + 4m .. +3
+                float g[4], h[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    g[q] = __uint_as_float(lo[4 * m + q]) * scale;
+                    h[q] = __uint_as_float(hi[4 * m + q]) * scale;
+                    if (rope) {
+                        const float c = tb[32 * b + 8 * m + 2 * q], s = tb[32 * b + 8 * m + 2 * q + 1];
+                        const float x = g[q] * c + h[q] * s, y = h[q] * c - g[q] * s;
+                        g[q] = x; h[q] = y;
+                    }
+                }
+                plo[2 * m] = pack_bf16x2(g[0], g[1]);
+                plo[2 * m + 1] = pack_bf16x2(g[2], g[3]);
+                phi[2 * m] = pack_bf16x2(h[0], h[1]);
+                phi[2 * m + 1] = pack_bf16x2(h[2], h[3]);
+            }
+            if (valid) {
+                st_row32(row_out + j0 * 2, plo, v8);
+                st_row32(row_out + (half + j0) * 2, phi, v8);
+            }
+        }
+    }
 }
 
 // TMEM column of the packed bf16 K-slice k (16 columns of a 64-column step) when
@@ -228,6 +312,11 @@ __device__ __forceinline__ uint32_t packed_col(int k) { return (k >> 1) * 32 + (
 namespace dq {
 
 constexpr int BK = 128;        // key rows per step (N = 128 keeps the MMAs at full rate)
+// Register split of the launch's 168 per thread (the launcher checks the count): the
+// control warps (TMA, MMA, scheduler, V producer) give theirs to the math warps, which
+// then hold the epilogue's cos/sin while they wait for the accumulator.
+constexpr uint32_t kLaunchRegsQ = 168, kCtrlRegsQ = 80, kMathRegsQ = 208;
+static_assert(128 * kCtrlRegsQ + 256 * kMathRegsQ <= kThreads * kLaunchRegsQ, "register split exceeds the pool");
 constexpr int kKStages = 3;   // K(j) is held from S(j) until dQ(j) completes
 constexpr int kVStages = 2;
 
@@ -353,6 +442,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     uint32_t q_issued = 0, k_issued = 0, v_issued = 0;
 
     if (warp == 0) {
+        setmaxnreg_dec<kCtrlRegsQ>();
         if (lane == 0) {   // ---------------------------------------- TMA producer: Q' / dO and K'
             const uint64_t pol_stream = make_l2_policy_evict_first();   // q/dO: once per unit
             const uint64_t pol_keep = make_l2_policy_evict_last();      // K/V: re-read by other units
@@ -390,6 +480,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         }
         __syncwarp();
     } else if (warp == 3) {
+        setmaxnreg_dec<kCtrlRegsQ>();
         if (lane == 0) {   // ---------------------------------------- TMA producer: V
             const uint64_t pol_keep = make_l2_policy_evict_last();
             uint32_t kv = 0;
@@ -414,6 +505,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         }
         __syncwarp();
     } else if (warp == 1) {
+        setmaxnreg_dec<kCtrlRegsQ>();
         {   // ---------------------------------------- MMA issuer (converged warp, one elected lane issues)
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BK, false);
             constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, D, true);
@@ -498,6 +590,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         }
         __syncwarp();
     } else if (warp == 2) {
+        setmaxnreg_dec<kCtrlRegsQ>();
         // ------------------------------------------------------------ unit scheduler (after the
         // TMEM allocation): claims and decodes units ahead of the other roles
         if (lane == 0) {
@@ -511,6 +604,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         }
         __syncwarp();
     } else if (warp >= 4) {
+        setmaxnreg_inc<kMathRegsQ>();
         // ------------------------------------------------------------ Q'/dO staging, P, dS + epilogue
         const int g = (warp - 4) >> 2;             // math warpgroup: key columns [64g, 64g + 64)
         const int wq = warp & 3;
@@ -620,6 +714,13 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
                 mbar_arrive(bar(DS_FULL));
             }
             if (!ok) break;
+            // cos/sin of this row's rotation pairs, in flight across the staging and the ACC wait
+            const bool il = p.use_rope == kRopeInterleaved;
+            float tb[D / 2];
+            if (p.use_rope) {
+                if (il) load_unrot_tables<D, true>(p.table2, p.table_rows, rpos, g, tb);
+                else load_unrot_tables<D, false>(p.table2, p.table_rows, rpos, g, tb);
+            }
             // stage the next unit before this unit's epilogue, so its first MMAs can start
             Unit w2{};
             int u2 = -1;
@@ -633,12 +734,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
             tc_fence_after();
             {   // both warpgroups: each takes half of the row's rotation pairs
                 uint8_t* row_out = reinterpret_cast<uint8_t*>(p.dq) + (tok * p.H + w.h) * static_cast<int64_t>(D) * 2;
-                if (p.use_rope == kRopeInterleaved)
-                    store_unrotated<D, true>(tmem + lane_off + LY::DQ_COL, p.table2, p.table_rows, rpos, p.scale,
-                                             true, valid, row_out, v8, g);
-                else
-                    store_unrotated<D, false>(tmem + lane_off + LY::DQ_COL, p.table2, p.table_rows, rpos,
-                                              p.scale, p.use_rope != 0, valid, row_out, v8, g);
+                if (il) store_unrotated_tb<D, true>(tmem + lane_off + LY::DQ_COL, tb, p.scale, true, valid, row_out, v8, g);
+                else store_unrotated_tb<D, false>(tmem + lane_off + LY::DQ_COL, tb, p.scale, p.use_rope != 0, valid,
+                                                  row_out, v8, g);
             }
             tc_fence_before();
             mbar_arrive(bar(ACC_EMPTY));
@@ -1182,7 +1280,12 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
     {
         constexpr uint32_t smem = bwd::dq::Layout<D>::ALLOC;
         auto kernel = kv ? bwd::dq::dq_kernel<D, true> : bwd::dq::dq_kernel<D, false>;
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        // the warp roles re-split the register pool: valid only at the launch count it assumes
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(bwd::dq::kLaunchRegsQ)) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         kernel<<<num_sms, bwd::kThreads, smem, s>>>(q128, do128, k128, v128, p);
     }
