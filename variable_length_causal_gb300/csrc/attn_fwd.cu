@@ -664,10 +664,11 @@ cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, in
 // ---------------------------------------------------------------- q', k' for a whole training step
 // R(p) q and R(p) k for every row, once: the forward and backward passes of a step can
 // then run on the rotated operands (no in-kernel rotation, no rotation in the
-// backward's prep pass).  A block takes a contiguous run of tokens, one at a time: each
-// thread loads the cos/sin of its 16-byte chunk pair once per token and rotates that
-// chunk pair in every query head and every key head of the token (consecutive
-// threads cover consecutive 16-byte chunks of a head row).
+// backward's prep pass).  A block takes a contiguous run of tokens, D/16 threads per
+// token: each thread loads the cos/sin of its 16-byte chunk pair once per token and
+// rotates that chunk pair in every query head and every key head of the token
+// (consecutive threads cover consecutive 16-byte chunks of a head row, so a warp reads
+// and writes whole 128-byte lines).
 namespace fwd {
 template <int D>
 __global__ void __launch_bounds__(256)
@@ -676,20 +677,22 @@ rope_qk_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k, uint4* 
                int32_t nseg, const float2* __restrict__ table, int32_t total, int32_t H, int32_t Hkv, int rope,
                const int32_t* __restrict__ err) {
     if (*err != 0) return;
-    constexpr int TPR = D / 16;               // threads per head row (chunk pairs)
+    constexpr int TPR = D / 16;               // threads per token (16-byte chunk pairs of a head row)
     constexpr int HALF = D / 16;
-    constexpr int SLOTS = 256 / TPR;          // heads handled side by side
-    const int c = threadIdx.x % TPR, slot = threadIdx.x / TPR;
+    constexpr int TOKB = 256 / TPR;           // tokens side by side in a block
+    const int c = threadIdx.x % TPR, ts = threadIdx.x / TPR;
     const bool il = rope == kRopeInterleaved;
-    // a contiguous run of tokens per block: one segment search, then the segment index
-    // only moves forward (every thread follows the same tokens, so no block barrier)
+    // a contiguous run of tokens per block; a thread takes every TOKB-th token of it, so its
+    // segment index only moves forward, and loads its chunk pair's cos/sin once per token for
+    // all of the token's head rows
     const int64_t per = (static_cast<int64_t>(total) + gridDim.x - 1) / gridDim.x;
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * per;
     const int64_t t1 = min(static_cast<int64_t>(total), t0 + per);
-    if (t0 >= t1) return;
-    int a = segment_of_row(rows, nseg, t0);
+    int64_t tok = t0 + ts;
+    if (tok >= t1) return;
+    int a = segment_of_row(rows, nseg, tok);
     int64_t next = a + 1 < nseg ? __ldg(rows + a + 1) : INT64_MAX;
-    for (int64_t tok = t0; tok < t1; ++tok) {
+    for (; tok < t1; tok += TOKB) {
         while (tok >= next) {
             ++a;
             next = a + 1 < nseg ? __ldg(rows + a + 1) : INT64_MAX;
@@ -698,11 +701,13 @@ rope_qk_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k, uint4* 
         const bool real = pos0 < __ldg(cu + a + 1) - __ldg(cu + a);   // rows past a padded segment: zeros
         float cs[8], sn[8];
         if (real) load_angles<D>(table, pos0, il, c, cs, sn);
-        for (int h = slot; h < H; h += SLOTS) {
+#pragma unroll 4
+        for (int h = 0; h < H; ++h) {
             const int64_t lo = (tok * H + h) * (2 * HALF) + c;
             rotate_chunks(q, qrot, lo, lo + HALF, cs, sn, real, il);
         }
-        for (int h = slot; h < Hkv; h += SLOTS) {
+#pragma unroll 4
+        for (int h = 0; h < Hkv; ++h) {
             const int64_t lo = (tok * Hkv + h) * (2 * HALF) + c;
             rotate_chunks(k, krot, lo, lo + HALF, cs, sn, real, il);
         }
@@ -711,7 +716,8 @@ rope_qk_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k, uint4* 
 }  // namespace fwd
 
 cudaError_t launch_rope_qk(const FwdParams& p, void* qrot, void* krot, int num_sms, cudaStream_t s) {
-    int64_t blocks = p.total;
+    const int tokb = 256 / (p.d / 16);   // tokens per block pass
+    int64_t blocks = (static_cast<int64_t>(p.total) + tokb - 1) / tokb;
     if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
     if (blocks < 1) blocks = 1;
     auto kernel = p.d == 128 ? fwd::rope_qk_kernel<128> : fwd::rope_qk_kernel<64>;
