@@ -186,18 +186,18 @@ static int attn_fwd_impl(AttnArgs a) {
     float2* table = reinterpret_cast<float2*>(w + L.table);
 
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
-    if (launch_worklist(a.cu, a.nseg, a.total, a.max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD, items,
-                        L.item_cap, order, seg_base, &hdr->count, &hdr->err, s, a.cu_padded, a.cu_kv,
-                        a.total_kv, a.max_seqlen_kv) != cudaSuccess)
-        return VLC_ERR_CUDA;
+    // operands rotated by vlc_rope_qk: the forward applies no rotation of its own
+    const int mode = (a.flags & VLC_QK_ROTATED) ? kRopeNone : rope_mode(a.rope_theta, a.flags);
+    {   // the work list and (with RoPE) the cos/sin table in one launch
+        const WlSpec wl{a.cu, a.nseg, a.total, a.max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD, items,
+                        L.item_cap, order, seg_base, &hdr->count, &hdr->err, a.cu_padded, a.cu_kv,
+                        a.total_kv, a.max_seqlen_kv};
+        const TabSpec tab = rope_table_spec(table, L.table_rows, a.d, static_cast<double>(a.rope_theta));
+        if (launch_meta(&wl, 1, mode != kRopeNone ? &tab : nullptr, s) != cudaSuccess) return VLC_ERR_CUDA;
+    }
     if (a.cu_padded != nullptr &&
         launch_pad_fill(a.cu, a.cu_padded, a.nseg, a.total, a.o, int64_t(a.H) * a.d * 2, nullptr, 0, nullptr,
                         0, a.lse, a.H, &hdr->err, num_sms_cached(), s) != cudaSuccess)
-        return VLC_ERR_CUDA;
-    // operands rotated by vlc_rope_qk: the forward applies no rotation of its own
-    const int mode = (a.flags & VLC_QK_ROTATED) ? kRopeNone : rope_mode(a.rope_theta, a.flags);
-    if (mode != kRopeNone && launch_rope_table(table, L.table_rows, a.d, static_cast<double>(a.rope_theta),
-                                               &hdr->err, s) != cudaSuccess)
         return VLC_ERR_CUDA;
     FwdParams p{};
     p.q = a.q; p.k = a.k; p.v = a.v; p.o = a.o; p.lse = a.lse; p.cu = a.cu;
@@ -251,24 +251,22 @@ static int attn_bwd_impl(AttnArgs a) {
     float2* table = reinterpret_cast<float2*>(w + L.table);
 
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
-    // q-tile items (dQ pass) and key-tile items (dK/dV pass)
-    if (launch_worklist(a.cu, a.nseg, a.total, a.max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items_q,
-                        L.item_cap, order, seg_base_q, &hdr->count, &hdr->err, s, a.cu_padded, a.cu_kv,
-                        a.total_kv, a.max_seqlen_kv) != cudaSuccess)
-        return VLC_ERR_CUDA;
-    if (launch_worklist(a.cu, a.nseg, a.total, a.max_seqlen, kBwdBM, kFwdBN, VLC_WORKLIST_BWD, items_k,
-                        L.item_cap, order + a.nseg, seg_base_k, &hdr->count2, &hdr->err, s, a.cu_padded,
-                        a.cu_kv, a.total_kv, a.max_seqlen_kv) != cudaSuccess)
-        return VLC_ERR_CUDA;
+    const int mode = rope_mode(a.rope_theta, a.flags);
+    float2* table2 = reinterpret_cast<float2*>(w + L.table2);
+    {   // q-tile items (dQ pass), key-tile items (dK/dV pass) and the cos/sin tables in one launch
+        const WlSpec wl[2] = {
+            {a.cu, a.nseg, a.total, a.max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items_q, L.item_cap, order,
+             seg_base_q, &hdr->count, &hdr->err, a.cu_padded, a.cu_kv, a.total_kv, a.max_seqlen_kv},
+            {a.cu, a.nseg, a.total, a.max_seqlen, kBwdBM, kFwdBN, VLC_WORKLIST_BWD, items_k, L.item_cap,
+             order + a.nseg, seg_base_k, &hdr->count2, &hdr->err, a.cu_padded, a.cu_kv, a.total_kv,
+             a.max_seqlen_kv}};
+        const TabSpec tab = rope_table_spec(table, L.table_rows, a.d, static_cast<double>(a.rope_theta), table2);
+        if (launch_meta(wl, 2, mode != kRopeNone ? &tab : nullptr, s) != cudaSuccess) return VLC_ERR_CUDA;
+    }
     if (a.cu_padded != nullptr &&
         launch_pad_fill(a.cu, a.cu_padded, a.nseg, a.total, a.dq, int64_t(a.H) * a.d * 2, a.dk,
                         int64_t(a.Hkv) * a.d * 2, a.dv, int64_t(a.Hkv) * a.d * 2, nullptr, a.H, &hdr->err,
                         num_sms_cached(), s) != cudaSuccess)
-        return VLC_ERR_CUDA;
-    const int mode = rope_mode(a.rope_theta, a.flags);
-    float2* table2 = reinterpret_cast<float2*>(w + L.table2);
-    if (mode != kRopeNone && launch_rope_table(table, L.table_rows, a.d, static_cast<double>(a.rope_theta),
-                                               &hdr->err, s, table2) != cudaSuccess)
         return VLC_ERR_CUDA;
     BwdParams p{};
     p.dout = a.dout; p.q = a.q; p.k = a.k; p.v = a.v; p.o = a.o_in; p.lse = a.lse_in;
@@ -459,15 +457,17 @@ int vlc_rope_qk(const void* q, const void* k, const int32_t* cu, const int32_t* 
     WsHeader* hdr = reinterpret_cast<WsHeader*>(w + L.header);
     float2* table = reinterpret_cast<float2*>(w + L.table);
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return VLC_ERR_CUDA;
-    // the work list validates cu (and cu_padded) before anything reads positions
-    if (launch_worklist(cu, nseg, total, max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD,
-                        reinterpret_cast<int4*>(w + L.items), L.item_cap, reinterpret_cast<int32_t*>(w + L.order),
-                        reinterpret_cast<int32_t*>(w + L.seg_base), &hdr->count, &hdr->err, s, cu_padded) !=
-        cudaSuccess)
-        return VLC_ERR_CUDA;
+    // the work list validates cu (and cu_padded) before anything reads positions; the table,
+    // which reads no input, is filled in the same launch
     const int mode = rope_mode(rope_theta, flags);
-    if (launch_rope_table(table, L.table_rows, d, static_cast<double>(rope_theta), &hdr->err, s) != cudaSuccess)
-        return VLC_ERR_CUDA;
+    {
+        const WlSpec wl{cu, nseg, total, max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD,
+                        reinterpret_cast<int4*>(w + L.items), L.item_cap, reinterpret_cast<int32_t*>(w + L.order),
+                        reinterpret_cast<int32_t*>(w + L.seg_base), &hdr->count, &hdr->err, cu_padded, nullptr, 0,
+                        0};
+        const TabSpec tab = rope_table_spec(table, L.table_rows, d, static_cast<double>(rope_theta));
+        if (launch_meta(&wl, 1, &tab, s) != cudaSuccess) return VLC_ERR_CUDA;
+    }
     FwdParams p{};
     p.q = q; p.k = k; p.cu = cu;
     p.rows = cu_padded != nullptr ? cu_padded : cu;

@@ -38,6 +38,33 @@ cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64
                                     int32_t total, const uint8_t* seg_ignore, int32_t* pos,
                                     int64_t* labels, int32_t* err, cudaStream_t s);
 
+// Arguments of one work-list build (see launch_worklist) and of one RoPE table fill.
+struct WlSpec {
+    const int32_t* cu;
+    int32_t nseg, total, max_seqlen, BM, BN;
+    int kind;
+    int4* items;
+    int64_t cap;
+    int32_t* order;
+    int32_t* seg_base;
+    int32_t* count;
+    int32_t* err;
+    const int32_t* cu_padded;
+    const int32_t* cu_kv;
+    int32_t total_kv, max_seqlen_kv;
+};
+struct TabSpec {
+    float2* table;
+    float2* table2;   // null: no blocked copy
+    int32_t rows, half;
+    double log2_theta;
+};
+TabSpec rope_table_spec(float2* table, int32_t rows, int32_t d, double theta, float2* table2 = nullptr);
+
+// One kernel launch for up to two work lists and (tab != null) a RoPE table fill,
+// which run side by side in separate blocks.
+cudaError_t launch_meta(const WlSpec* lists, int nwl, const TabSpec* tab, cudaStream_t s);
+
 cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
                             int32_t BM, int32_t BN, int kind, int4* items, int64_t cap,
                             int32_t* order, int32_t* seg_base, int32_t* count, int32_t* err,

@@ -54,13 +54,20 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int* total
     return r;
 }
 
-__global__ void __launch_bounds__(kWlThreads, 1)
-worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int32_t max_seqlen,
-                int32_t BM, int32_t BN, int kind, int4* __restrict__ items, int64_t cap,
-                int32_t* __restrict__ order, int32_t* __restrict__ seg_base,
-                int32_t* __restrict__ count, int32_t* __restrict__ err,
-                const int32_t* __restrict__ cu_padded, const int32_t* __restrict__ cu_kv,
-                int32_t total_kv, int32_t max_seqlen_kv) {
+__device__ __forceinline__ void worklist_body(const WlSpec& spec) {
+    const int32_t* __restrict__ cu = spec.cu;
+    const int32_t nseg = spec.nseg, total = spec.total, max_seqlen = spec.max_seqlen;
+    const int32_t BM = spec.BM, BN = spec.BN;
+    const int kind = spec.kind;
+    int4* __restrict__ items = spec.items;
+    const int64_t cap = spec.cap;
+    int32_t* __restrict__ order = spec.order;
+    int32_t* __restrict__ seg_base = spec.seg_base;
+    int32_t* __restrict__ count = spec.count;
+    int32_t* __restrict__ err = spec.err;
+    const int32_t* __restrict__ cu_padded = spec.cu_padded;
+    const int32_t* __restrict__ cu_kv = spec.cu_kv;
+    const int32_t total_kv = spec.total_kv, max_seqlen_kv = spec.max_seqlen_kv;
     extern __shared__ int wl_smem[];
     int* hist = wl_smem;                    // [nbins] counts, then running positions
     __shared__ int warp_sums[33];
@@ -223,27 +230,6 @@ worklist_kernel(const int32_t* __restrict__ cu, int32_t nseg, int32_t total, int
         }
     }
     if (tid == 0) *count = carry;
-}
-
-cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
-                            int32_t BM, int32_t BN, int kind, int4* items, int64_t cap,
-                            int32_t* order, int32_t* seg_base, int32_t* count, int32_t* err,
-                            cudaStream_t s, const int32_t* cu_padded, const int32_t* cu_kv,
-                            int32_t total_kv, int32_t max_seqlen_kv) {
-    const int tile = (kind == VLC_WORKLIST_FWD) ? BM : BN;
-    const int nbins = ((kind == VLC_WORKLIST_FWD || cu_kv == nullptr ? max_seqlen : max_seqlen_kv) + tile - 1) /
-                      tile + 1;
-    const size_t smem = sizeof(int) * static_cast<size_t>(nbins);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(worklist_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
-    worklist_kernel<<<1, kWlThreads, smem, s>>>(cu, nseg, total, max_seqlen, BM, BN, kind, items,
-                                                cap, order, seg_base, count, err, cu_padded, cu_kv,
-                                                total_kv, max_seqlen_kv);
-    return cudaGetLastError();
 }
 
 // ============================================================== padding rows
@@ -424,16 +410,19 @@ cudaError_t launch_positions_labels(const int32_t* cu, int32_t nseg, const int64
 
 constexpr double kTwoPi = 6.283185307179586476925286766559;
 
-__global__ void rope_table_kernel(float2* __restrict__ table, float2* __restrict__ table2, int32_t rows,
-                                  int32_t half, double log2_theta, const int32_t* __restrict__ err) {
-    if (err != nullptr && *err != 0) return;
+// Rows [0, rows) x frequencies [0, half): table[p][j] = (cos, sin)(p theta^(-2j/d)),
+// table2 (optional) the same blocked by four frequencies.  The angle is formed and
+// reduced modulo 2 pi in fp64, then sincosf on the reduced fp32 argument.  Block `blk`
+// of `nblk` takes a grid-stride share of the rows x half entries.
+__device__ __forceinline__ void rope_table_body(const TabSpec& tab, int blk, int nblk) {
     __shared__ double w[256];
+    const int half = tab.half;
     for (int j = threadIdx.x; j < half; j += blockDim.x)
-        w[j] = exp2(-2.0 * static_cast<double>(j) / static_cast<double>(2 * half) * log2_theta);
+        w[j] = exp2(-2.0 * static_cast<double>(j) / static_cast<double>(2 * half) * tab.log2_theta);
     __syncthreads();
-    const int64_t n = static_cast<int64_t>(rows) * half;
-    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = static_cast<int64_t>(tab.rows) * half;
+    for (int64_t idx = static_cast<int64_t>(blk) * blockDim.x + threadIdx.x; idx < n;
+         idx += static_cast<int64_t>(nblk) * blockDim.x) {
         const int64_t p = idx / half;
         const int j = static_cast<int>(idx - p * half);
         const double x = static_cast<double>(p) * w[j];
@@ -441,19 +430,73 @@ __global__ void rope_table_kernel(float2* __restrict__ table, float2* __restrict
         const double red = fma(-k, kTwoPi, x);
         float sn, cs;
         sincosf(static_cast<float>(red), &sn, &cs);
-        table[idx] = make_float2(cs, sn);
-        if (table2 != nullptr) table2[((static_cast<int64_t>(j >> 2) * rows + p) << 2) + (j & 3)] = make_float2(cs, sn);
+        tab.table[idx] = make_float2(cs, sn);
+        if (tab.table2 != nullptr)
+            tab.table2[((static_cast<int64_t>(j >> 2) * tab.rows + p) << 2) + (j & 3)] = make_float2(cs, sn);
     }
+}
+
+// One launch for a call's metadata: blocks [0, nwl) build work lists w0 (and w1), the
+// remaining blocks fill the RoPE table(s).  The table does not read cu_seqlens, so it
+// needs no validation and runs beside the work lists.
+__global__ void __launch_bounds__(kWlThreads, 1)
+meta_kernel(WlSpec w0, WlSpec w1, int nwl, TabSpec tab) {
+    if (static_cast<int>(blockIdx.x) < nwl) {
+        worklist_body(blockIdx.x == 0 ? w0 : w1);
+        return;
+    }
+    if (tab.table != nullptr) rope_table_body(tab, blockIdx.x - nwl, gridDim.x - nwl);
+}
+
+static int wl_nbins(const WlSpec& w) {
+    const int tile = (w.kind == VLC_WORKLIST_FWD) ? w.BM : w.BN;
+    return ((w.kind == VLC_WORKLIST_FWD || w.cu_kv == nullptr ? w.max_seqlen : w.max_seqlen_kv) + tile - 1) / tile + 1;
+}
+
+cudaError_t launch_meta(const WlSpec* lists, int nwl, const TabSpec* tab, cudaStream_t s) {
+    if (nwl < 0 || nwl > 2 || (nwl == 0 && tab == nullptr)) return cudaErrorInvalidValue;
+    WlSpec w[2] = {};
+    int nbins = 1;
+    for (int i = 0; i < nwl; ++i) {
+        w[i] = lists[i];
+        nbins = std::max(nbins, wl_nbins(w[i]));
+    }
+    TabSpec tb{};
+    int tblocks = 0;
+    if (tab != nullptr && tab->table != nullptr) {
+        tb = *tab;
+        const int64_t n = static_cast<int64_t>(tb.rows) * tb.half;
+        tblocks = static_cast<int>(std::min<int64_t>((n + kWlThreads - 1) / kWlThreads, 296));
+    }
+    const size_t smem = sizeof(int) * static_cast<size_t>(nbins);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(meta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    meta_kernel<<<nwl + tblocks, kWlThreads, smem, s>>>(w[0], w[1], nwl, tb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_worklist(const int32_t* cu, int32_t nseg, int32_t total, int32_t max_seqlen,
+                            int32_t BM, int32_t BN, int kind, int4* items, int64_t cap,
+                            int32_t* order, int32_t* seg_base, int32_t* count, int32_t* err,
+                            cudaStream_t s, const int32_t* cu_padded, const int32_t* cu_kv,
+                            int32_t total_kv, int32_t max_seqlen_kv) {
+    const WlSpec w{cu, nseg, total, max_seqlen, BM, BN, kind, items, cap, order, seg_base, count, err,
+                   cu_padded, cu_kv, total_kv, max_seqlen_kv};
+    return launch_meta(&w, 1, nullptr, s);
+}
+
+TabSpec rope_table_spec(float2* table, int32_t rows, int32_t d, double theta, float2* table2) {
+    return TabSpec{table, table2, rows, d / 2, std::log2(theta)};
 }
 
 cudaError_t launch_rope_table(float2* table, int32_t rows, int32_t d, double theta,
                               const int32_t* err, cudaStream_t s, float2* table2) {
-    const int half = d / 2;
-    const int64_t n = static_cast<int64_t>(rows) * half;
-    int64_t blocks = (n + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    rope_table_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(table, table2, rows, half, log2(theta), err);
-    return cudaGetLastError();
+    (void)err;   // the table reads no input that needs validation
+    const TabSpec tb = rope_table_spec(table, rows, d, theta, table2);
+    return launch_meta(nullptr, 0, &tb, s);
 }
 
 }  // namespace vlc
