@@ -215,9 +215,10 @@ class Step:
             raise RuntimeError("positions/labels reported invalid cu_seqlens")
 
 
-# posl; rotation (worklist + table + q'/k'); forward (worklist + attention); backward (2 worklists +
-# table + delta + dq + dkdv)
-LAUNCHES_PER_STEP = 1 + 3 + 2 + 6
+# posl; rotation (worklist and table in one launch + q'/k'); forward (worklist + attention);
+# backward (2 worklists and table in one launch + delta + dq + dkdv)
+LAUNCHES_PER_STEP = 1 + 2 + 2 + 4
+LAUNCHES_PER_FWD_STEP = 1 + 2 + 2
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -374,7 +375,7 @@ def gpu_arm(args, w, world, rank, local):
         "tokens_per_s": real_tok / (ms * 1e-3),
         "fwd_eff_tflops": fwd_tflops, "bwd_eff_tflops": bwd_tflops,
         "kernels": kernels, "roofline": roofline, "roofline_fwd": roofline_fwd,
-        "gpu_launches": (6 if args.fwd_only else LAUNCHES_PER_STEP) * args.steps,
+        "gpu_launches": (LAUNCHES_PER_FWD_STEP if args.fwd_only else LAUNCHES_PER_STEP) * args.steps,
         "clocks": clk.summary(),
         "e2e": e2e,
     }
