@@ -353,9 +353,9 @@ def gpu_arm(args, w, world, rank, local):
     kernels = {
         "positions_labels": {"ms": t_pos, "GB/s": pos_bytes / (t_pos * 1e-3) / 1e9},
         "attn_fwd_call": {"ms": t_fwd, "eff_TFLOP/s": fwd_tflops,
-                          "kernels": "rotation (worklist + rope_table + rope_qk_kernel) + worklist + attn_fwd_kernel"},
+                          "kernels": "rotation (meta_kernel: work list + RoPE table; rope_qk_kernel) + meta_kernel (work list) + attn_fwd_kernel"},
         "attn_bwd_call": {"ms": t_bwd, "eff_TFLOP/s": bwd_tflops,
-                          "kernels": "2 worklists + rope_table + delta + dq_kernel + dkdv_kernel"},
+                          "kernels": "meta_kernel (2 work lists + RoPE tables) + prep_kernel (delta) + dq_kernel + dkdv_kernel"},
     }
     dominant = "attn_bwd_call" if t_bwd >= t_fwd else "attn_fwd_call"
     ach = bwd_tflops if dominant == "attn_bwd_call" else fwd_tflops
