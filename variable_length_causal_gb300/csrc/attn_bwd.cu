@@ -10,8 +10,9 @@
 //   dQ = R(p)^T dQ',  dK = R(p)^T dK'   (RoPE is orthogonal: its inverse is R(-p)).
 //
 // Three kernels, no atomics (results are bitwise reproducible):
-//   prep_kernel    D = rowsum(dO * O) in fp32, layout [H, total]; with RoPE also
-//                  q' = R(p) q and k' = R(p) k once into the workspace (bf16).
+//   prep_kernel    D = rowsum(dO * O) in fp32, layout [H, total]; with RoPE (on
+//                  operands not rotated beforehand) also q' = R(p) q and
+//                  k' = R(p) k once into the workspace (bf16).
 //   dq_kernel      q-major, one unit = (q tile of 128 rows, head): for every key
 //                  step of 128 rows, tcgen05 computes S = Q'K'^T (two TMEM buffers)
 //                  and dP = dO V^T; two warpgroups (64 key columns each) form P
@@ -27,10 +28,15 @@
 //                  dV += P^T dO and dK += dS^T Q' (tensor-memory A operands) in
 //                  the order dP^T(i) dV(i) S^T(i+1) dK(i) dP^T(i+1), so each math
 //                  phase has a two-MMA window; a stager warp prefetches LSE/delta;
-//                  epilogue stores dV and R(p)^T dK.
-// Both attention kernels are persistent (one CTA per SM), warp-specialised
-// like the forward (TMA warp, MMA warp, TMEM warp, 4 math warps, 4 hand-off
-// warps), and use only bounded waits.
+//                  four epilogue warps store dV and R(p)^T dK while the math
+//                  warps start the next unit.
+// Both attention kernels are persistent (one CTA per SM) and warp-specialised:
+// warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM allocator and then unit
+// scheduler (claims and decodes units for every other role), warp 3 V producer
+// (dQ pass) or LSE/delta stager (dK/dV pass), warps 4-11 two math warpgroups,
+// warps 12-15 (dK/dV pass only) the epilogue warpgroup.  The roles re-split the
+// launch's registers with setmaxnreg inside their own branches.  Every wait is
+// bounded.
 #include <type_traits>
 #include <cuda.h>
 #include <cmath>

@@ -11,8 +11,9 @@
 // unit is (segment, head, block of 256 query rows) = two 128-row q tiles that
 // share every K/V tile; the work list holds only in-segment, at-or-below-
 // diagonal key tiles, and a q tile stops at its own diagonal key tile.  Units
-// are claimed dynamically (longest first) from a global counter and handed to
-// every role through a shared-memory ring.
+// are claimed dynamically (longest first) from a global counter by a scheduler
+// thread, which decodes each one and hands it to every role through a
+// shared-memory ring.
 //   warp 0       TMA producer of q tiles (3-slot ring) and K tiles (2 stages),
 //                128-byte swizzle; warp 3 the same for V tiles (2 stages).
 //   warp 1       MMA issuer (one elected lane of the converged warp), tcgen05.mma
@@ -21,7 +22,8 @@
 //                P_t read from TMEM; issue order S0 S1 | PV0(j) S0(j+1)
 //                PV1(j) S1(j+1) | ..., so each q tile's softmax overlaps the
 //                other tile's MMAs.
-//   warp 2       TMEM allocator (512 columns: S/P 0, S/P 1, O 0, O 1).
+//   warp 2       TMEM allocator (512 columns: S/P 0, S/P 1, O 0, O 1), then the
+//                unit scheduler.
 //   warps 4-7    softmax + epilogue of q tile 0, one thread per query row:
 //   warps 8-11   the same for q tile 1.  Two passes over the S row in TMEM
 //                (row max, then exp2 and bf16 P written back over the consumed
