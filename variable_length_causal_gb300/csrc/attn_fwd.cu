@@ -65,6 +65,11 @@ constexpr uint32_t kCtrlRegs = VLC_FWD_CTRL_REGS, kRopeRegs = VLC_FWD_ROPE_REGS;
 constexpr uint32_t kSoftmaxRegs = (4 * kLaunchRegs - kCtrlRegs - kRopeRegs) / 2 / 8 * 8;
 static_assert(kCtrlRegs % 8 == 0 && kRopeRegs % 8 == 0, "register counts are multiples of 8");
 static_assert(kCtrlRegs + kRopeRegs + 2 * kSoftmaxRegs <= 4 * kLaunchRegs, "register split exceeds the pool");
+// Without RoPE in the kernel (no RoPE, or operands rotated beforehand) the RoPE warpgroup
+// idles at the minimum and the softmax warpgroups take its registers.
+constexpr uint32_t kIdleRegs = 24;
+constexpr uint32_t kSoftmaxRegsNR = (4 * kLaunchRegs - kCtrlRegs - kIdleRegs) / 2 / 8 * 8;
+static_assert(kCtrlRegs + kIdleRegs + 2 * kSoftmaxRegsNR <= 4 * kLaunchRegs, "register split exceeds the pool");
 constexpr float kLn2 = 0.69314718055994530942f;
 
 enum : int {
@@ -129,12 +134,14 @@ __device__ __forceinline__ FUnit make_funit(const FwdParams& p, const Unit& w) {
 }
 
 // KV: keys and values have segments of their own (bottom-right aligned queries).
-template <int D, bool KV>
+template <int D, bool KV, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmKr,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using LY = Layout<D>;
+    constexpr uint32_t kSoft = ROPE ? kSoftmaxRegs : kSoftmaxRegsNR;
+    constexpr uint32_t kFourth = ROPE ? kRopeRegs : kIdleRegs;   // the RoPE warpgroup
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -338,7 +345,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         __syncwarp();
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ softmax + epilogue
-        setmaxnreg_inc<kSoftmaxRegs>();
+        setmaxnreg_inc<kSoft>();
         const int t = (warp - 4) >> 2;             // q tile slot handled by this warpgroup
         const int wq = warp & 3;                   // TMEM lane quadrant
         const int r = wq * 32 + lane;              // query row in the tile = TMEM lane
@@ -471,7 +478,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ RoPE on staged q / K tiles
-        setmaxnreg_dec<kRopeRegs>();
+        setmaxnreg_dec<kFourth>();
         const int wr = warp - 12;
         // one copy of the loop per pairing, so neither carries the other's state
         auto run = [&](auto il_tag) {
@@ -506,8 +513,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
             }
         };
-        if (p.use_rope == kRopeInterleaved) run(std::true_type{});
-        else if (p.use_rope) run(std::false_type{});   // without RoPE these warps take no units
+        if constexpr (ROPE) {
+            if (p.use_rope == kRopeInterleaved) run(std::true_type{});
+            else run(std::false_type{});
+        }   // without RoPE these warps take no units
     } else if (warp == 3) {
         // ------------------------------------------------------------ TMA producer of V tiles
         setmaxnreg_dec<kCtrlRegs>();
@@ -595,8 +604,13 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const dim3 grid(num_sms), block(fwd::kThreads);
     const bool kv = p.cu_kv != p.cu;
-    auto kernel = p.d == 128 ? (kv ? fwd::attn_fwd_kernel<128, true> : fwd::attn_fwd_kernel<128, false>)
-                             : (kv ? fwd::attn_fwd_kernel<64, true> : fwd::attn_fwd_kernel<64, false>);
+    // one instance with RoPE warps, one whose softmax warps take their registers
+    const bool rope = p.use_rope != kRopeNone;
+    auto kernel = p.d == 128
+                      ? (kv ? (rope ? fwd::attn_fwd_kernel<128, true, true> : fwd::attn_fwd_kernel<128, true, false>)
+                            : (rope ? fwd::attn_fwd_kernel<128, false, true> : fwd::attn_fwd_kernel<128, false, false>))
+                      : (kv ? (rope ? fwd::attn_fwd_kernel<64, true, true> : fwd::attn_fwd_kernel<64, true, false>)
+                            : (rope ? fwd::attn_fwd_kernel<64, false, true> : fwd::attn_fwd_kernel<64, false, false>));
     const uint32_t smem = p.d == 128 ? fwd::Layout<128>::ALLOC : fwd::Layout<64>::ALLOC;
     // The warpgroups re-split the block's register pool at run time, which is only
     // valid if every thread is launched with exactly kLaunchRegs registers.
