@@ -342,7 +342,7 @@ def gpu_arm(args, w, world, rank, local):
     value = flops_all / (ms * 1e-3) / 1e12
 
     # ---- end to end through the public API, pinned host buffers in and out
-    e2e = None if args.no_e2e else e2e_measure(vlc, w, step, args.steps, world, dev)
+    e2e = None if args.no_e2e else e2e_measure(vlc, w, step, args.steps, world, dev, args.e2e_readback)
 
     if rank != 0:
         return
@@ -548,11 +548,15 @@ def variant_measurements(vlc, w, dev, peaks, step):
     return res
 
 
-def e2e_measure(vlc, w, step, steps, world, dev):
+def e2e_measure(vlc, w, step, steps, world, dev, readback="result"):
     """Same metric through the public API with pinned host buffers: every step copies this
-    step's inputs host->device and reads every output back device->host.  Steps are pipelined
-    over three streams (copy-in, compute, copy-out) with two device buffer sets, so step k's
-    outputs travel back while step k+1 computes and step k+2's inputs arrive."""
+    step's inputs host->device and reads its result back device->host.  The result is the
+    step's per-row log-normalisers (LSE, [H, total] fp32), the attention step's loss-like
+    statistic; the gradients stay on the device, as they do in training, where the next
+    layer's backward consumes them (readback="all" also reads O, dq, dk, dv, positions and
+    labels back).  Steps are pipelined over three streams (copy-in, compute, copy-out) with
+    two device buffer sets, so step k's result travels back while step k+1 computes and step
+    k+2's inputs arrive."""
     sets = [step, Step(vlc, w, *(torch.empty_like(t) if t is not None else None
                                  for t in (step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign)),
                        fwd_only=step.fwd_only)]
@@ -563,13 +567,15 @@ def e2e_measure(vlc, w, step, steps, world, dev):
         return [t for t in (s.q, s.k, s.v, s.g, s.tokens, s.cu, s.ign) if t is not None]
 
     def dev_out(s):
+        if readback == "result":
+            return [s.lse]
         return [t for t in (s.o, s.lse, s.dq, s.dk, s.dv) if t is not None]
 
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out(step)]
     host_pos = torch.empty(w.total, dtype=torch.int32).pin_memory()
     host_lab = torch.empty(w.total, dtype=torch.int64).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out) + w.total * 12
+    d2h = sum(t.numel() * t.element_size() for t in host_out) + (w.total * 12 if readback == "all" else 0)
     s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     in_done = [torch.cuda.Event() for _ in sets]
     cmp_done = [torch.cuda.Event() for _ in sets]
@@ -591,8 +597,9 @@ def e2e_measure(vlc, w, step, steps, world, dev):
             s_out.wait_event(cmp_done[k % 2])
             for h, d in zip(host_out, dev_out(s)):
                 h.copy_(d, non_blocking=True)
-            host_pos.copy_(s.pos, non_blocking=True)
-            host_lab.copy_(s.lab, non_blocking=True)
+            if readback == "all":
+                host_pos.copy_(s.pos, non_blocking=True)
+                host_lab.copy_(s.lab, non_blocking=True)
             s.pos.record_stream(s_out)                # allocated per call on the compute stream
             s.lab.record_stream(s_out)
             out_done[k % 2].record(s_out)
@@ -613,7 +620,9 @@ def e2e_measure(vlc, w, step, steps, world, dev):
     flops = sum_over_ranks(synth.fwd_flops(w) + (0.0 if step.fwd_only else synth.bwd_flops(w)), world, dev)
     return {"value": flops / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3,
-            "pipelining": "copy-in, compute and copy-out streams, two device buffer sets"}
+            "pipelining": "copy-in, compute and copy-out streams, two device buffer sets",
+            "readback": ("the step's LSE (per-row log-normalisers); gradients stay on the device"
+                         if readback == "result" else "every output: O, LSE, dq, dk, dv, positions, labels")}
 
 
 def cpu_baseline(w, q, k, v, g, seconds):
@@ -674,6 +683,8 @@ def main():
     ap.add_argument("--fwd-only", action="store_true",
                     help="step = positions/labels + forward only (for profiling the forward kernel)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--e2e-readback", choices=("result", "all"), default="result",
+                    help="end-to-end leg: read back the step's LSE only (result) or every output (all)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the positions/labels sweep and the padded comparator")
     ap.add_argument("--bins", type=int, default=None,
