@@ -6,8 +6,13 @@ One step = the whole hot path over one synthetic packed batch:
   ->  backward attention (work lists, delta, dQ pass, dK/dV pass).
 Metric: effective TFLOP/s counting only in-segment causal FLOPs of real (non-pad)
 segments, 4*d*H*pairs (forward) + 10*d*H*pairs (backward); packed real tokens/s
-is reported beside it.  Default workload: the SFT pack (16 x 4096 tokens,
-lognormal(300, 1.0) lengths packed first-fit-decreasing, H=32, d=128).
+is reported beside it.  Default workload: the pretraining-window forward+backward pack
+(32 x 4096 tokens, lognormal(400, 0.8) document lengths clipped to [32, 4096] and packed
+first-fit-decreasing, H=32, d=128, with dO), the largest single-GPU shape with a backward.
+The line's extras also time the forward alone on the 4K-window pack and on the
+131072-token long-context buffer (per-iteration CUDA events over >= 300 iterations,
+median and min), in both RoPE forms: rotation fused into the forward kernel, and q, k
+rotated once by a separate pass followed by the kernel on the rotated operands.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
 
@@ -222,33 +227,37 @@ LAUNCHES_PER_FWD_STEP = 1 + 2 + 2
 
 
 # ----------------------------------------------------------------------------- oracle arm
-def oracle_sample(w: synth.Workload, q, k, v, g, budget_s: float):
-    """Pick (segment, head) pairs of real segments in a seeded order until the oracle's
-    estimated fwd+bwd time on all host threads fills ``budget_s``; returns the pairs and
-    their legal-pair count.  q/k/v/g are uint16 bf16 bit arrays (converted once)."""
-    import oracle
+# Legal (query, key) pairs in one oracle sample: about 5 s of fp64 forward + backward on 16
+# host cores.  Both the cpu_baseline leg and the reference arm time this same sample, so
+# they report one number.
+ORACLE_SAMPLE_PAIRS = 40_000_000
 
+
+def oracle_sample(w: synth.Workload, threads: int):
+    """(segment, head) pairs of real segments, drawn in a seeded order until they hold
+    ORACLE_SAMPLE_PAIRS legal pairs and at least 8 pairs per host thread; returned longest
+    segment first, so that the host threads' dynamic schedule ends together.  The same
+    workload and thread count always give the same sample (no timing decides it)."""
     rng = np.random.default_rng(12345)
     real = np.nonzero(w.seg_ignore == 0)[0]
     order = rng.permutation(len(real))
     heads = rng.integers(0, w.H, size=len(order))
-    threads = max(oracle.num_threads(), 1)
-    # calibrate on one parallel batch of `threads` pairs: legal pairs per second on all threads
-    calib = [(int(real[i]), int(h)) for i, h in zip(order[:threads], heads[:threads])]
-    t0 = time.perf_counter()
-    oracle.attn_fwd(q, k, v, w.cu, seg_heads=calib)
-    oracle.attn_bwd(g, q, k, v, w.cu, seg_heads=calib)
-    dt = max(time.perf_counter() - t0, 1e-4)
-    rate = sum(int(w.lengths[r]) * (int(w.lengths[r]) + 1) // 2 for r, _ in calib) / dt
     pairs, total_pairs = [], 0
     for i, h in zip(order, heads):
         r = int(real[i])
         L = int(w.lengths[r])
         pairs.append((r, int(h)))
         total_pairs += L * (L + 1) // 2
-        if total_pairs >= rate * budget_s and len(pairs) >= threads:
+        if total_pairs >= ORACLE_SAMPLE_PAIRS and len(pairs) >= 8 * threads:
             break
+    pairs.sort(key=lambda p: (-int(w.lengths[p[0]]), p[0], p[1]))
     return pairs, total_pairs
+
+
+def _sample_text(w, pairs, npairs):
+    return (f"{len(pairs)} (segment, head) pairs of the {w.name} pack ({npairs} legal pairs, "
+            f"drawn with a fixed seed, longest first): fwd + bwd in fp64, plus positions/labels "
+            f"of the whole pack")
 
 
 def run_oracle_step(w, q, k, v, g, tokens_np, pairs):
@@ -267,7 +276,7 @@ def reference_arm(args, w, world, rank):
     oracle.build()
     q, k, v, g = (oracle.bf16_bits(t) for t in synth.make_tensors(w, seed=1000 + w.index, with_grad=True))
     tokens_np = synth.make_tokens(w)
-    pairs, npairs = oracle_sample(w, q, k, v, g, budget_s=args.ref_step_seconds)
+    pairs, npairs = oracle_sample(w, oracle.num_threads())
     for _ in range(args.warmup):
         run_oracle_step(w, q, k, v, g, tokens_np, pairs)
     t0 = time.perf_counter()
@@ -277,8 +286,7 @@ def reference_arm(args, w, world, rank):
     flops = 14.0 * w.d * npairs
     value = flops / dt / 1e12
     tok = sum(int(w.lengths[r]) for r, _ in pairs) / w.H
-    sample = (f"{len(pairs)} (segment, head) pairs of the {w.name} pack ({npairs} legal pairs), "
-              f"fwd + bwd + positions/labels of the whole pack, fp64")
+    sample = _sample_text(w, pairs, npairs) + f"; one sample per step"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
@@ -332,9 +340,10 @@ def gpu_arm(args, w, world, rank, local):
     step.check_errors()
     ms_local = start.elapsed_time(stop) / args.steps
     ms = max_over_ranks(ms_local, world, dev)
-    t_pos = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    t_fwd = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    t_bwd = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    per_pos = [e[0].elapsed_time(e[1]) for e in evs]
+    per_fwd = [e[1].elapsed_time(e[2]) for e in evs]
+    per_bwd = [e[2].elapsed_time(e[3]) for e in evs]
+    t_pos, t_fwd, t_bwd = (statistics.mean(x) for x in (per_pos, per_fwd, per_bwd))
 
     fl_f, fl_b = synth.fwd_flops(w), (0.0 if args.fwd_only else synth.bwd_flops(w))
     flops_all = sum_over_ranks(fl_f + fl_b, world, dev)
@@ -352,9 +361,11 @@ def gpu_arm(args, w, world, rank, local):
     pos_bytes = 20.0 * w.total
     kernels = {
         "positions_labels": {"ms": t_pos, "GB/s": pos_bytes / (t_pos * 1e-3) / 1e9},
-        "attn_fwd_call": {"ms": t_fwd, "eff_TFLOP/s": fwd_tflops,
+        "attn_fwd_call": {"ms": t_fwd, "ms_median": statistics.median(per_fwd), "ms_min": min(per_fwd),
+                          "eff_TFLOP/s": fwd_tflops,
                           "kernels": "rotation (meta_kernel: work list + RoPE table; rope_qk_kernel) + meta_kernel (work list) + attn_fwd_kernel"},
-        "attn_bwd_call": {"ms": t_bwd, "eff_TFLOP/s": bwd_tflops,
+        "attn_bwd_call": {"ms": t_bwd, "ms_median": statistics.median(per_bwd), "ms_min": min(per_bwd),
+                          "eff_TFLOP/s": bwd_tflops,
                           "kernels": "meta_kernel (2 work lists + RoPE tables) + prep_kernel (delta) + dq_kernel + dkdv_kernel"},
     }
     dominant = "attn_bwd_call" if t_bwd >= t_fwd else "attn_fwd_call"
@@ -381,6 +392,7 @@ def gpu_arm(args, w, world, rank, local):
     }
     if not args.no_extras and args.bins is None and world == 1:
         line["extras"] = extra_measurements(vlc, w, dev, peaks, q, k, v, step)
+        line["extras"]["forward_configs"] = forward_configs(vlc, dev, peaks)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, q, k, v, g, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -396,6 +408,72 @@ def _time_ms(fn, reps: int) -> float:
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / reps
+
+
+def _time_events(fn, reps: int):
+    """Per-iteration CUDA events around ``reps`` back-to-back calls (no synchronisation
+    between them): (median ms, min ms)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in evs:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ts = [a.elapsed_time(b) for a, b in evs]
+    return statistics.median(ts), min(ts)
+
+
+def forward_configs(vlc, dev, peaks, reps: int = 300):
+    """The forward alone on the 4K-window pack (32 x 4096 tokens) and on the 131072-token
+    long-context buffer, H = 32, d = 128, RoPE theta 10000 with the per-segment reset, in
+    both forms: ``fused_rope`` (vlc_attn_fwd: the rotation runs on the staged tiles inside
+    the attention kernel) and ``rotate_once`` (vlc_rope_qk writes q', k', then the kernel
+    runs on them; the form a training step uses, since the backward reuses q', k').
+    Effective TFLOP/s = 4 d H pairs / median call time; frac against the measured bf16
+    burst peak; traffic = DRAM bytes per call from the committed ncu capture, when it was
+    taken on the current sources."""
+    out = {}
+    with ClockSampler(dev.index or 0) as clk:
+        for name in ("pt", "long"):
+            w = synth.workload(WORKLOAD_BY_NAME[name])
+            q, k, v = synth.make_tensors(w, device=dev, seed=1000 + w.index)
+            cu = torch.from_numpy(w.cu).to(dev)
+            o = torch.empty_like(q)
+            lse = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
+            qr, kr = torch.empty_like(q), torch.empty_like(k)
+            ws = vlc.new_workspace(w.nseg, w.total, w.H, w.d, w.max_seqlen, False, dev)
+
+            def fused():
+                vlc.varlen_attn_fwd(q, k, v, cu, w.max_seqlen, rope_theta=w.theta, out=o, lse=lse, workspace=ws,
+                                    check=False)
+
+            def rotate_once():
+                vlc.rope_qk(q, k, cu, w.max_seqlen, rope_theta=w.theta, out=(qr, kr), workspace=ws, check=False)
+                vlc.varlen_attn_fwd(qr, kr, v, cu, w.max_seqlen, rope_theta=w.theta, out=o, lse=lse, workspace=ws,
+                                    check=False, qk_rotated=True)
+
+            fl = synth.fwd_flops(w)
+            res = {"workload": f"{w.name}: {w.description}", "total_tokens": w.total,
+                   "legal_pairs": synth.causal_pairs(w.real_lengths), "reps": reps}
+            for form, fn in (("fused_rope", fused), ("rotate_once", rotate_once)):
+                med, mn = _time_events(fn, reps)
+                st, bits = vlc.get_error(ws)
+                if st != 0:
+                    raise RuntimeError(f"{name} {form}: device error status {st} bits 0x{bits:x}")
+                tf = fl / (med * 1e-3) / 1e12
+                res[form] = {"ms_median": med, "ms_min": mn, "eff_TFLOP/s": tf,
+                             "eff_TFLOP/s_at_min": fl / (mn * 1e-3) / 1e12,
+                             "frac": tf / peaks["bf16_tflops"],
+                             "traffic": _traffic_from_profiles(f"fwd_{form}", name)}
+            out[name] = res
+            del q, k, v, o, lse, qr, kr, ws
+            torch.cuda.empty_cache()
+    out["clocks"] = clk.summary()
+    out["peak"] = {"bf16_tflops": peaks["bf16_tflops"], "source": f"{peaks['source']} bf16 burst"}
+    return out
 
 
 def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
@@ -626,19 +704,25 @@ def e2e_measure(vlc, w, step, steps, world, dev, readback="result"):
 
 
 def cpu_baseline(w, q, k, v, g, seconds):
+    """The oracle on the host cores, on the same fixed sample the reference arm times: the
+    sample is run until ``seconds`` have passed (at least twice); the median run gives the
+    rate."""
     import oracle
 
     oracle.build()
     qc, kc, vc, gc = (oracle.bf16_bits(t) for t in (q, k, v, g))
-    pairs, npairs = oracle_sample(w, qc, kc, vc, gc, budget_s=seconds)
+    pairs, npairs = oracle_sample(w, oracle.num_threads())
     tokens_np = synth.make_tokens(w)
-    t0 = time.perf_counter()
-    run_oracle_step(w, qc, kc, vc, gc, tokens_np, pairs)
-    dt = time.perf_counter() - t0
+    runs = []
+    t_start = time.perf_counter()
+    while len(runs) < 2 or (time.perf_counter() - t_start < seconds and len(runs) < 10):
+        t0 = time.perf_counter()
+        run_oracle_step(w, qc, kc, vc, gc, tokens_np, pairs)
+        runs.append(time.perf_counter() - t0)
+    dt = statistics.median(runs)
     return {"value": 14.0 * w.d * npairs / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{len(pairs)} (segment, head) pairs of the {w.name} pack ({npairs} legal pairs): "
-                      f"fwd + bwd in fp64, plus positions/labels of the whole pack; {dt:.1f} s"}
+            "sample": _sample_text(w, pairs, npairs) + f"; median of {len(runs)} runs of {dt:.1f} s"}
 
 
 def _source_digest() -> str:
@@ -676,10 +760,9 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="vlc", choices=["vlc", "reference"])
-    ap.add_argument("--workload", default="sft", choices=synth.WORKLOAD_NAMES)
+    ap.add_argument("--workload", default="pt_bwd", choices=synth.WORKLOAD_NAMES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--fwd-only", action="store_true",
                     help="step = positions/labels + forward only (for profiling the forward kernel)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")

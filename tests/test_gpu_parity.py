@@ -337,6 +337,39 @@ def test_bwd_full_size_sampled(vlc):
         assert torch.isfinite(t.float()).all()
 
 
+def test_bwd_long_context_sampled(vlc):
+    """The long-context buffer (131072 tokens, documents up to 20884 tokens) forward and
+    backward at full size in the bench's launch configuration (q, k rotated once, both
+    passes on the rotated operands); the gradients of three (segment, head) pairs are
+    recomputed by the oracle: a segment of more than 8192 keys whose length is not a
+    multiple of 128 (many q steps per key tile, the long-segment paths), a segment of
+    exactly 128 tokens, and a mid-length segment with a ragged last tile."""
+    w = synth.workload(3)
+    q, k, v, g = synth.make_tensors(w, device=DEV, with_grad=True)
+    cu = _cu(w)
+    qr, kr = vlc.rope_qk(q, k, cu, w.max_seqlen)
+    o, lse = vlc.varlen_attn_fwd(qr, kr, v, cu, w.max_seqlen, qk_rotated=True)
+    dq, dk, dv = vlc.varlen_attn_bwd(g, qr, kr, v, o, lse, cu, w.max_seqlen, qk_rotated=True)
+    # the self-rotating backward on the unrotated operands gives the same bits
+    dq2, dk2, dv2 = vlc.varlen_attn_bwd(g, q, k, v, o, lse, cu, w.max_seqlen)
+    for a, b in zip((dq, dk, dv), (dq2, dk2, dv2)):
+        assert torch.equal(a, b)
+    lens = w.lengths
+    real = np.nonzero(w.seg_ignore == 0)[0]
+    big = [int(r) for r in real if lens[r] > 8192 and lens[r] % 128 != 0]
+    exact = [int(r) for r in real if lens[r] == 128]
+    ragged = [int(r) for r in real if 1024 < lens[r] < 4096 and lens[r] % 128 != 0]
+    assert big and exact and ragged
+    pairs = [(min(big, key=lambda r: lens[r]), 5), (exact[0], w.H - 1), (ragged[0], 17)]
+    assert lens[pairs[0][0]] > 8192
+    ref = oracle.attn_bwd(g.cpu(), q.cpu(), k.cpu(), v.cpu(), w.cu, seg_heads=pairs)
+    for s, h in pairs:
+        a, b = int(w.cu[s]), int(w.cu[s + 1])
+        _cmp_grads([t[a:b, h] for t in (dq, dk, dv)], [r[a:b, h] for r in ref])
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+
+
 def test_fwd_peaky_scores_rescale_paths(vlc):
     """Rows whose max score jumps by far more than 2^8 within a tile and across tiles
     (large-magnitude q/k) exercise the in-row P rescale and the O rescale."""
