@@ -319,10 +319,13 @@ int vlc_rope_qk(const void* q, const void* k, const int32_t* cu, const int32_t* 
  * Same arguments and result as vlc_attn_fwd, without ws/ws_bytes; the scratch
  * lives in one file-scope device array of VLC_NOALLOC_SCRATCH_BYTES per GPU,
  * held until the process exits.
- *   err_out  int32 [1] device word or NULL: receives this call's VLC_DEVERR_*
- *            bits in stream order (the caller zeroes it if it wants OR-free bits).
- * Returns VLC_ERR_WORKSPACE, before enqueuing anything, when the problem's
- * forward workspace (vlc_workspace_bytes(..., 0)) exceeds the array.
+ *   err_out  int32 [1] device word or NULL: overwritten, in stream order, with
+ *            this call's VLC_DEVERR_* bits (0 when the call found no error).
+ * Returns VLC_ERR_WORKSPACE, before enqueuing anything, when the forward
+ * workspace without its optional rotated-k region exceeds the array; when the
+ * whole workspace (vlc_workspace_bytes(..., 0)) fits, long segments take the
+ * rotated-k pass as in vlc_attn_fwd.  Invalid or unsupported arguments give the
+ * status vlc_attn_fwd gives for them.
  * The first call on a device looks up the array's address (do it before any
  * stream capture begins).  All calls share the array: calls whose GPU work can
  * overlap race on it, so order them on one stream or with events.  Calls no

@@ -12,9 +12,12 @@
 //
 // Properties a caller must know:
 //  - The array holds kNoAllocScratchBytes (8 MiB) on every GPU that loads this
-//    library, for the lifetime of the process.  Problems whose forward
-//    workspace (vlc_workspace_bytes(..., 0)) is larger are rejected with
-//    VLC_ERR_WORKSPACE before anything is enqueued.
+//    library, for the lifetime of the process.  A problem is accepted when the
+//    forward's workspace without its optional region (the rotated copy of k for
+//    segments of at least 2048 keys) fits; larger ones are rejected with
+//    VLC_ERR_WORKSPACE before anything is enqueued.  When the whole workspace
+//    fits, long segments take the rotated-k pass exactly as vlc_attn_fwd does;
+//    otherwise their K tiles are rotated inside the attention kernel.
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (with that device current) and caches it; make that
 //    first call before any stream capture begins.
@@ -23,7 +26,7 @@
 //    give wrong results; serialise them.  Each call clears the error word
 //    itself; the rest of the array is fully rewritten before it is read.
 //  - Device-side errors (invalid cu_seqlens, an expired wait) are reported by
-//    copying the call's VLC_DEVERR_* bits into the caller's err_out word (if
+//    copying the call's VLC_DEVERR_* bits over the caller's err_out word (if
 //    given), in stream order.
 //  - No cudaMalloc, cudaFree or other allocating routine is called.
 #include <cuda_runtime.h>
@@ -69,11 +72,16 @@ extern "C" int vlc_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                                     int32_t max_seqlen, float softmax_scale, float rope_theta,
                                     void* o, float* lse, int32_t* err_out, void* stream) {
     if (vlc_workspace_bytes(nseg, total, H, d, max_seqlen, 0) == 0) {
-        if (d != 64 && d != 128) return VLC_ERR_UNSUPPORTED;
-        return VLC_ERR_ARG;
+        // invalid or unsupported arguments: the regular entry point's own checks give
+        // the status (they reject these before the workspace is looked at, so nothing
+        // is enqueued)
+        return vlc_attn_fwd(q, k, v, cu, nseg, total, H, d, max_seqlen, softmax_scale, rope_theta, o, lse,
+                            nullptr, 0, stream);
     }
-    // the scratch holds the forward's work list, table and error word; the optional
-    // rotated copy of k does not fit, so the forward rotates every K tile in-kernel
+    // The scratch must hold the forward's work list, segment order, RoPE table and
+    // error word.  If it also holds the optional rotated copy of k (the whole layout
+    // fits), the forward uses it for segments of at least 2048 keys; otherwise it
+    // rotates those K tiles inside the kernel.
     const size_t need = vlc::ws_layout(nseg, total, H, H, d, max_seqlen, 0).total_min;
     if (need > vlc::kNoAllocScratchBytes) return VLC_ERR_WORKSPACE;
     void* scratch = nullptr;
