@@ -599,13 +599,13 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         setmaxnreg_dec<kCtrlRegsQ>();
         // ------------------------------------------------------------ unit scheduler (after the
         // TMEM allocation): claims and decodes units ahead of the other roles
-        if (lane == 0) {
+        {   // the whole warp: lane 0 claims and publishes, all lanes decode
             auto decode = [&](int u) {
-                return decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                return decode_unit_warp<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
             };
             for (int n = 0;; ++n) {
                 int u;
-                if (!ring_put(rg, n, p.next_q, nunits, abort, decode, u) || u < 0) break;
+                if (!ring_put_warp(rg, n, p.next_q, nunits, abort, decode, u) || u < 0) break;
             }
         }
         __syncwarp();
@@ -1066,13 +1066,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         setmaxnreg_dec<kCtrlRegs>();
         // ------------------------------------------------------------ unit scheduler (after the
         // TMEM allocation): claims and decodes units ahead of the other roles
-        if (lane == 0) {
+        {   // the whole warp: lane 0 claims and publishes, all lanes decode
             auto decode = [&](int u) {
-                return decode_unit<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+                return decode_unit_warp<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
             };
             for (int n = 0;; ++n) {
                 int u;
-                if (!ring_put(rg, n, p.next_k, nunits, abort, decode, u) || u < 0) break;
+                if (!ring_put_warp(rg, n, p.next_k, nunits, abort, decode, u) || u < 0) break;
             }
         }
         __syncwarp();

@@ -22,18 +22,31 @@ struct Unit {
 // padded offsets of a layout with padding between segments); likewise for the
 // keys and values from cu_kv / rows_kv.  KV == false is self-attention: the key
 // side equals the query side and is not loaded.
+// Executed by a whole warp: the search for the unit's segment probes 32 sorted-
+// segment offsets at once and keeps the bracket the ballot points to, so a pack
+// of up to 1024 segments is searched in two dependent rounds of loads (32768 in
+// three) instead of one round per halving.  Every lane returns the same Unit.
 template <bool KV>
-__device__ __forceinline__ Unit decode_unit(const int4* __restrict__ items,
-                                            const int32_t* __restrict__ seg_base,
-                                            const int32_t* __restrict__ cu,
-                                            const int32_t* __restrict__ rows,
-                                            const int32_t* __restrict__ cu_kv,
-                                            const int32_t* __restrict__ rows_kv, int nseg, int H, int u) {
+__device__ __forceinline__ Unit decode_unit_warp(const int4* __restrict__ items,
+                                                 const int32_t* __restrict__ seg_base,
+                                                 const int32_t* __restrict__ cu,
+                                                 const int32_t* __restrict__ rows,
+                                                 const int32_t* __restrict__ cu_kv,
+                                                 const int32_t* __restrict__ rows_kv, int nseg, int H, int u) {
     const int64_t HH = H;
+    const int lane = threadIdx.x & 31;
+    // invariant: H * seg_base[lo] <= u, and the answer lies in [lo, hi]
     int lo = 0, hi = nseg - 1;
     while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (HH * __ldg(seg_base + mid) <= u) lo = mid; else hi = mid - 1;
+        const int64_t span = static_cast<int64_t>(hi - lo) + 1;
+        const int pr = lo + static_cast<int>((static_cast<int64_t>(lane) * span) >> 5);   // probe 0 is lo
+        const bool ok = HH * __ldg(seg_base + pr) <= u;
+        const uint32_t m = __ballot_sync(0xffffffffu, ok);
+        const int last = 31 - __clz(m);   // probes are non-decreasing, so the ok ones come first
+        const int nlo = __shfl_sync(0xffffffffu, pr, last);
+        const int nxt = __shfl_sync(0xffffffffu, pr, last < 31 ? last + 1 : 31);
+        hi = last < 31 ? nxt - 1 : hi;
+        lo = nlo;
     }
     const int base = __ldg(seg_base + lo);
     const int n = __ldg(seg_base + lo + 1) - base;
@@ -79,11 +92,11 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 }
 
 // ---------------------------------------------------------------- dynamic unit ring
-// A scheduler thread claims work units from a global counter (longest first, so
+// A scheduler warp claims work units from a global counter (longest first, so
 // CTAs that finish early take the next unit and the units in flight stay a
-// contiguous window of the work list), decodes each one (a chain of dependent
-// global loads: the binary search over the sorted segments, then the item and
-// the segment's offsets) and publishes index and decoded unit in a ring of kRing
+// contiguous window of the work list), decodes each one (dependent global loads:
+// the search over the sorted segments, then the item and the segment's offsets)
+// and publishes index and decoded unit in a ring of kRing
 // shared-memory slots; every other role consumes the same sequence in order and
 // reads the decoded unit from the slot.  The ring depth bounds how far the
 // scheduler claims ahead of the slowest role (kRing - 1 units).  A unit index of
@@ -96,22 +109,31 @@ struct Ring {
     uint32_t full0, empty0; // barrier addresses of slot 0 (8-byte stride)
 };
 
-// Scheduler thread: `decode(u)` gives the Unit of index u.
+// The scheduler as a whole warp: lane 0 claims, every lane takes part in `decode(u)`
+// (a warp-collective decode such as decode_unit_warp), lane 0 publishes.
 template <class Decode>
-__device__ __forceinline__ bool ring_put(const Ring& rg, int n, int* counter, int nunits,
-                                         volatile int* abort, Decode&& decode, int& u_out) {
+__device__ __forceinline__ bool ring_put_warp(const Ring& rg, int n, int* counter, int nunits,
+                                              volatile int* abort, Decode&& decode, int& u_out) {
     const int s = n % kRing;
-    if (!mbar_wait(rg.empty0 + 8u * s, ((n / kRing) & 1) ^ 1, abort)) return false;
-    int u = atomicAdd(counter, 1);
+    const int lane = threadIdx.x & 31;
+    if (!wait_warp(rg.empty0 + 8u * s, ((n / kRing) & 1) ^ 1, abort)) return false;
+    int u = 0;
+    if (lane == 0) u = atomicAdd(counter, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
     if (u >= nunits) u = -1;
     volatile int* d = rg.slot + s * kSlotInts;
     if (u >= 0) {
         const Unit w = decode(u);
-        d[1] = w.seg; d[2] = w.tile; d[3] = w.lo; d[4] = w.hi; d[5] = w.h;
-        d[6] = w.L; d[7] = w.row0; d[8] = w.Lk; d[9] = w.row0k; d[10] = w.off;
+        if (lane == 0) {
+            d[1] = w.seg; d[2] = w.tile; d[3] = w.lo; d[4] = w.hi; d[5] = w.h;
+            d[6] = w.L; d[7] = w.row0; d[8] = w.Lk; d[9] = w.row0k; d[10] = w.off;
+        }
     }
-    d[0] = u;
-    mbar_arrive(rg.full0 + 8u * s);   // release: waiters see the slot
+    if (lane == 0) {
+        d[0] = u;
+        mbar_arrive(rg.full0 + 8u * s);   // release: waiters see the slot
+    }
+    __syncwarp();
     u_out = u;
     return true;
 }

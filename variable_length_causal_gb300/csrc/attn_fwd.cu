@@ -548,13 +548,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // ------------------------------------------------------------ warp 2: TMEM allocator, then
         // the unit scheduler (claims and decodes units ahead of the other roles)
         setmaxnreg_dec<kCtrlRegs>();
-        if (lane == 0) {
+        {   // the whole warp: lane 0 claims and publishes, all lanes decode
             auto decode = [&](int u) {
-                return decode_unit<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                return decode_unit_warp<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
             };
             for (int n = 0;; ++n) {
                 int u;
-                if (!ring_put(rg, n, p.next, nunits, abort, decode, u) || u < 0) break;
+                if (!ring_put_warp(rg, n, p.next, nunits, abort, decode, u) || u < 0) break;
             }
         }
         __syncwarp();
