@@ -82,6 +82,17 @@ const char* vlc_status_string(int status);
 /* Library ABI version (major * 100 + minor). */
 int vlc_version(void);
 
+/* Limit, in microseconds, of each bounded wait inside the attention kernels
+ * launched after this call, for the whole process (0 restores the default of
+ * 2 s).  A wait that expires raises VLC_DEVERR_TIMEOUT: the kernel drains its
+ * own copies and MMAs, frees its tensor memory and returns, later kernels of the
+ * call do nothing, and vlc_get_error reports VLC_ERR_TIMEOUT; the context stays
+ * usable.  A limit below the default also makes the waits poll instead of
+ * sleeping, so a very short limit makes the first wait that is not already
+ * complete expire.  This exists to exercise that failure path (the pages have no
+ * counterpart); a production caller leaves the default. */
+void vlc_set_wait_limit_us(uint32_t us);
+
 /* Bytes of workspace needed by vlc_attn_fwd (is_bwd = 0) or vlc_attn_bwd
  * (is_bwd = 1) for these sizes.  Returns 0 for invalid sizes.  The workspace
  * must be 256-byte aligned; its contents need no initialisation. */

@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     new_workspace,
     pack,
     rope_qk,
+    set_wait_limit_us,
     shard_packs,
     shifted_cross_entropy,
     varlen_attn_bwd,

@@ -36,7 +36,7 @@ EXPORTED = [
     "vlc_get_error", "vlc_attn_fwd_noalloc", "vlc_ce_workspace_bytes", "vlc_shifted_ce",
     "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa", "vlc_attn_fwd_ex",
     "vlc_attn_bwd_ex", "vlc_workspace_bytes_qkv", "vlc_attn_fwd_qkv", "vlc_attn_bwd_qkv", "vlc_pack",
-    "vlc_shard_packs", "vlc_rope_qk",
+    "vlc_shard_packs", "vlc_rope_qk", "vlc_set_wait_limit_us",
 ]
 
 _lock = threading.Lock()
@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_status_string.restype = ctypes.c_char_p
         lib.vlc_version.argtypes = []
         lib.vlc_version.restype = cint
+        lib.vlc_set_wait_limit_us.argtypes = [ctypes.c_uint32]
+        lib.vlc_set_wait_limit_us.restype = None
         lib.vlc_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, cint]
         lib.vlc_workspace_bytes.restype = sz
         lib.vlc_worklist_capacity.argtypes = [i32, i32, i32]
@@ -170,6 +172,12 @@ def new_workspace(nseg, total, H, d, max_seqlen, backward, device, H_kv=None, to
     if n == 0:
         raise VlcError(VLC_ERR_UNSUPPORTED, "workspace_bytes")
     return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def set_wait_limit_us(us: int) -> None:
+    """Limit of each bounded wait inside the attention kernels launched from now on, in
+    microseconds (0: the default of 2 s).  Only for exercising the timeout path."""
+    load_library().vlc_set_wait_limit_us(int(us))
 
 
 def get_error(ws: torch.Tensor) -> Tuple[int, int]:

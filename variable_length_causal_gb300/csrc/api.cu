@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -64,6 +65,10 @@ WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t 
     L.total = off;
     return L;
 }
+
+// Limit of one bounded wait in the attention kernels (vlc_set_wait_limit_us).
+static std::atomic<uint32_t> g_wait_limit_us{kWaitLimitUs};
+uint32_t wait_limit_us() { return g_wait_limit_us.load(std::memory_order_relaxed); }
 
 static int num_sms_cached() {
     static int cache[64] = {0};
@@ -211,6 +216,7 @@ static int attn_fwd_impl(AttnArgs a) {
     const float scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / std::sqrt(static_cast<float>(a.d));
     p.scale_log2 = scale * 1.4426950408889634f;
     p.use_rope = mode;
+    p.wait_limit_us = wait_limit_us();
     // long segments: k rotated once into the workspace (if it has room), not once per unit
     p.krot = nullptr;
     p.prerot_min = kPreRotMinKeys;
@@ -288,6 +294,7 @@ static int attn_bwd_impl(AttnArgs a) {
     p.scale = a.softmax_scale > 0.f ? a.softmax_scale : 1.0f / std::sqrt(static_cast<float>(a.d));
     p.use_rope = mode;
     p.operands_rotated = (a.flags & VLC_QK_ROTATED) ? 1 : 0;
+    p.wait_limit_us = wait_limit_us();
     if (launch_attn_bwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
     return VLC_OK;
 }
@@ -335,6 +342,10 @@ const char* vlc_status_string(int status) {
 }
 
 int vlc_version(void) { return 100; }
+
+void vlc_set_wait_limit_us(uint32_t us) {
+    vlc::g_wait_limit_us.store(us == 0 || us > vlc::kWaitLimitUs ? vlc::kWaitLimitUs : us, std::memory_order_relaxed);
+}
 
 size_t vlc_workspace_bytes_gqa(int32_t nseg, int32_t total, int32_t H, int32_t H_kv, int32_t d,
                                int32_t max_seqlen, int is_bwd) {

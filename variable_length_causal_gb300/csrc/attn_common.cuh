@@ -72,20 +72,22 @@ __device__ __forceinline__ Unit decode_unit_warp(const int4* __restrict__ items,
     return w;
 }
 
-// All 32 lanes poll; succeed together or give up together.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
+// All 32 lanes poll; succeed together or give up together (ctl as in mbar_wait).
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* ctl) {
+    const uint32_t lim = static_cast<uint32_t>(ctl[1]);
     if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+    const bool sleep = lim >= kWaitLimitUs;
     uint64_t t0 = 0;
     const int lane = threadIdx.x & 31;
 #pragma unroll 1
     for (int it = 0;; ++it) {
-        const bool done = mbar_try_wait(bar, parity);
+        const bool done = sleep ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity);
         if (__all_sync(0xffffffffu, done)) return true;
         int give_up = 0;
-        if (lane == 0 && it >= 64) {
+        if (lane == 0 && (!sleep || it >= 64)) {
             if (t0 == 0) t0 = globaltimer_ns();
-            if (*abort) give_up = 1;
-            else if (globaltimer_ns() - t0 > kWaitLimitNs) { *abort = 1; give_up = 1; }
+            if (ctl[0]) give_up = 1;
+            else if (globaltimer_ns() - t0 > 1000ull * lim) { ctl[0] = 1; give_up = 1; }
         }
         if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
     }

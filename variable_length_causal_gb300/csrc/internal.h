@@ -11,6 +11,7 @@ constexpr int kFwdQB = 256;   // query rows per forward work unit (two q tiles)
 constexpr int kFwdBN = 128;   // key rows per forward tile
 constexpr int kBwdBM = 128;   // query rows per backward (key-major pass) step
 constexpr int kTablePad = 128;  // RoPE table rows are padded to a multiple of this
+constexpr uint32_t kWaitLimitUs = 2000000u;   // default limit of one bounded wait in a kernel (2 s)
 
 // Workspace header (first 256 bytes).
 struct WsHeader {
@@ -110,6 +111,7 @@ struct FwdParams {
     int32_t total_kv;          // key/value rows (== total for self-attention)
     float scale_log2;          // softmax_scale * log2(e)
     int use_rope;              // kRopeNone, kRopeHalf (rotate-half pairs) or kRopeInterleaved
+    uint32_t wait_limit_us;    // limit of one bounded wait in the kernel (kWaitLimitUs by default)
 };
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s);
@@ -169,7 +171,12 @@ struct BwdParams {
                                // pass with that pairing, gradients un-rotated; kRopeNone: no RoPE
     int operands_rotated;      // 1: q and k already hold R(p) q, R(p) k; only the gradients are
                                // un-rotated (the prep pass computes D alone)
+    uint32_t wait_limit_us;    // limit of one bounded wait in the kernels (kWaitLimitUs by default)
 };
+
+// Limit of one bounded wait for the attention kernels launched from now on (the
+// process-wide setting of vlc_set_wait_limit_us).
+uint32_t wait_limit_us();
 
 cudaError_t launch_attn_bwd(const BwdParams& p, int num_sms, cudaStream_t s);
 

@@ -1,13 +1,21 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA bulk tensor
 // copies, tcgen05 (TMEM alloc / MMA / commit / ld / st) and a few scalar ops.
-// Every wait is bounded: it gives up after kWaitLimitNs and reports failure so
-// the caller can set the device error word and leave cleanly (no trap).
+// Every wait is bounded: it gives up after the launch's wait limit and reports
+// failure so the caller can set the device error word and leave cleanly (no trap).
 #pragma once
 #include <cstdint>
 
+#include "internal.h"
+
 namespace vlc {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+// A kernel keeps its waits' control words in
+// shared memory: ctl[0] is the abort flag (raised by the first wait that gives up;
+// every role then leaves its loop), ctl[1] the limit of one wait in microseconds,
+// copied from the launch parameters.  A limit below the default (used to exercise
+// the failure path) also makes every wait poll with test_wait instead of sleeping
+// in try_wait, so the limit is the whole budget of the wait.  The default is
+// kWaitLimitUs (internal.h).
 // A waiting thread sleeps (instead of polling) until the phase completes or this
 // many ns pass, so waiting warps leave their scheduler's issue slots to the others.
 constexpr uint32_t kTryWaitSuspendNs = 1000000;
@@ -67,20 +75,24 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
-// (and raises *abort) if it did not within kWaitLimitNs or if another role
+// (and raises ctl[0]) if it did not within the limit ctl[1], or if another role
 // already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* ctl) {
+    const uint32_t lim = static_cast<uint32_t>(ctl[1]);
     if (mbar_test_wait(bar, parity)) return true;
+    const bool sleep = lim >= kWaitLimitUs;
+    if (sleep) {
 #pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = globaltimer_ns();
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+    }
+    const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort = 1;
+        if (sleep ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity)) return true;
+        if (ctl[0]) return false;
+        if (globaltimer_ns() - t0 > 1000ull * lim) {
+            ctl[0] = 1;
             return false;
         }
     }
