@@ -69,6 +69,7 @@ typedef enum {
 #define VLC_DEVERR_CU_PADDED 0x20  /* cu_padded[0] != 0, a slot shorter than its segment,
                                       or cu_padded[nseg] != total */
 #define VLC_DEVERR_QKV 0x40        /* a segment with fewer keys than queries (cu_kv) */
+#define VLC_DEVERR_POS 0x80        /* a position outside [0, max_pos] (vlc_rope_pos) */
 #define VLC_DEVERR_TIMEOUT 0x100   /* a bounded mbarrier wait expired */
 
 /* Limits checked on the host. */
@@ -187,10 +188,16 @@ int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void*
 
 /* Option bits of vlc_attn_fwd_ex / vlc_attn_bwd_ex. */
 #define VLC_ROPE_INTERLEAVED 0x1u  /* RoPE pairs (x_{2j}, x_{2j+1}) instead of (x_j, x_{j+d/2}) */
-#define VLC_QK_ROTATED 0x2u        /* q and k hold R(p) q, R(p) k (from vlc_rope_qk): the forward
-                                      rotates nothing; the backward rotates nothing and takes
-                                      dq, dk back through R(p)^T (rope_theta and the pairing bit
-                                      as for the rotation); not with separate key segments */
+#define VLC_QK_ROTATED 0x2u        /* q and k hold R(p) q, R(p) k (from vlc_rope_qk or
+                                      vlc_rope_pos): the forward rotates nothing; the backward
+                                      rotates nothing and takes dq, dk back through R(p)^T
+                                      (rope_theta and the pairing bit as for the rotation); the
+                                      backward takes it for self-attention only */
+#define VLC_KEYS_ALL_VISIBLE 0x4u  /* vlc_attn_fwd_qkv only, with VLC_QK_ROTATED (or rope_theta
+                                      == 0): every key of a query's key segment is visible (a
+                                      block of keys that all precede the block of queries, as in
+                                      a context-parallel ring); the backward returns
+                                      VLC_ERR_UNSUPPORTED for it */
 
 /* vlc_attn_fwd_gqa / vlc_attn_bwd_gqa with a padded layout and an option word;
  * cu_padded == NULL and flags == 0 is exactly those calls.
@@ -260,6 +267,66 @@ int vlc_attn_bwd_qkv(const void* dout, const void* q, const void* k, const void*
                      int32_t total_q, int32_t total_kv, int32_t H, int32_t H_kv, int32_t d,
                      int32_t max_seqlen_q, int32_t max_seqlen_kv, float softmax_scale, float rope_theta,
                      uint32_t flags, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- context-parallel split
+ * A long segment costs O(L^2) whatever the packing ("Sequence packing and
+ * variable-length attention", charlestar, section on the two ledgers); spreading
+ * it over a context-parallel group needs shards and communication that follow
+ * the global segment boundaries, and a length that is a multiple of 2 * cp
+ * ("Long-context training: remove padding", vllbc, failure-modes section).
+ *
+ * vlc_cp_partition (host): every segment of length L (a multiple of 2 * cp, else
+ * VLC_ERR_ARG with *bad_seg = the first offending segment) is cut into 2 * cp
+ * chunks of m = L / (2 cp); rank `rank` holds chunk `rank` (its low half) and
+ * chunk 2 cp - 1 - rank (its high half) of every segment, so every rank has the
+ * same causal work, (2 cp - 1) m^2 + m (m + 1) per segment.  Outputs (caller-
+ * owned host arrays, total / cp rows):
+ *   rows      int64 [total / cp]: the pack row of each local row: the low chunks
+ *             of all segments in segment order, then the high chunks
+ *   pos       int32 [total / cp]: its position inside its segment (for RoPE)
+ *   cu_chunk  int32 [nseg + 1]: prefix sums of the chunk lengths m_r: each half
+ *             of the local buffer is a packed buffer whose segments are the chunks
+ * vlc_cp_block_mode: what the queries of (q_rank, q_half) see in the keys of
+ * (kv_rank, kv_half) of the same segments: VLC_CP_BLOCK_ALL (the key chunk comes
+ * first: vlc_attn_fwd_qkv with VLC_KEYS_ALL_VISIBLE), VLC_CP_BLOCK_CAUSAL (the
+ * same chunk: the causal square block, L == Lk), VLC_CP_BLOCK_NONE (nothing to
+ * compute); -1 for invalid arguments.  A ring step hands every rank another
+ * rank's two key/value halves; the partial results (O, LSE) of a query half over
+ * the blocks it sees are combined with vlc_lse_merge. */
+#define VLC_CP_BLOCK_NONE 0
+#define VLC_CP_BLOCK_CAUSAL 1
+#define VLC_CP_BLOCK_ALL 2
+int vlc_cp_partition(const int32_t* cu, int32_t nseg, int32_t cp, int32_t rank, int64_t* rows, int32_t* pos,
+                     int32_t* cu_chunk, int32_t* bad_seg);
+int vlc_cp_block_mode(int32_t cp, int32_t q_rank, int32_t q_half, int32_t kv_rank, int32_t kv_half);
+
+/* RoPE by explicit positions: out[i] = R(pos[i]) x[i] for every head of row i
+ * ("Sequence packing and variable-length attention", charlestar, section
+ * "Positions are reset per segment": the rotation of vlc_rope_qk, here with the
+ * positions given, e.g. those of vlc_cp_partition or vlc_build_positions_labels),
+ * rounded once to bf16.
+ *   x, out    bf16 [rows, H, d] (d = 64 or 128), 16-byte aligned, not overlapping
+ *   pos       device int32 [rows], 0 <= pos[i] <= max_pos; a position outside
+ *             sets VLC_DEVERR_POS in the workspace word and that row's out = 0
+ *   flags     VLC_ROPE_INTERLEAVED selects the pairing; rope_theta > 0
+ *   ws        vlc_rope_pos_workspace_bytes(max_pos, d) bytes, 256-byte aligned
+ *             (error word and cos/sin table); vlc_get_error reads it */
+size_t vlc_rope_pos_workspace_bytes(int32_t max_pos, int32_t d);
+int vlc_rope_pos(const void* x, const int32_t* pos, int32_t rows, int32_t H, int32_t d, int32_t max_pos,
+                 float rope_theta, uint32_t flags, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Combine attention results over disjoint key sets into the result over their
+ * union: LSE = ln sum_k e^{LSE_k}, O = sum_k e^{LSE_k - LSE} O_k, in fp32 (a
+ * part with LSE_k = -inf, no visible key, weighs nothing; rows with no part
+ * above -inf get O = 0, LSE = -inf).  The parts of a context-parallel ring
+ * (vlc_cp_block_mode) merge into the rows' full attention.
+ *   o_parts    host array of nparts device pointers, bf16 [rows, H, d] each
+ *   lse_parts  host array of nparts device pointers, fp32 [H, rows] each
+ *   1 <= nparts <= VLC_LSE_MERGE_MAX; o bf16 [rows, H, d], lse fp32 [H, rows],
+ *   not overlapping the parts.  d = 64 or 128; o and the O parts 16-byte aligned. */
+#define VLC_LSE_MERGE_MAX 16
+int vlc_lse_merge(const void* const* o_parts, const float* const* lse_parts, int32_t nparts, int32_t rows,
+                  int32_t H, int32_t d, void* o, float* lse, void* stream);
 
 /* ---------------------------------------------------------------- host packing
  * The data step in front of the path; plain host functions (no device, no
@@ -373,7 +440,8 @@ int vlc_shifted_ce(const void* logits, int32_t vocab, int32_t total, const int64
                    float* seg_loss, int32_t* seg_count, void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronise `stream` and read the workspace's device error word.
- * Returns VLC_OK, VLC_ERR_CU_SEQLENS, VLC_ERR_LABEL or VLC_ERR_TIMEOUT;
+ * Returns VLC_OK, VLC_ERR_CU_SEQLENS, VLC_ERR_LABEL, VLC_ERR_TIMEOUT or (a
+ * position out of range in vlc_rope_pos) VLC_ERR_ARG;
  * *bits_out (if not NULL) receives the raw VLC_DEVERR_* bits. */
 int vlc_get_error(const void* ws, int32_t* bits_out, void* stream);
 

@@ -60,11 +60,27 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.vlc_attn_fwd(dummy, dummy, dummy, dummy, 3, 9, 2, 128, 4, 0.0, 0.0, dummy, dummy,
                             None, 0, None) == 4
     # option words: an unknown bit is refused before the shape checks
-    assert lib.vlc_attn_fwd_ex(dummy, dummy, dummy, dummy, None, 3, 9, 2, 2, 128, 4, 0.0, 1e4, 0x4,
+    assert lib.vlc_attn_fwd_ex(dummy, dummy, dummy, dummy, None, 3, 9, 2, 2, 128, 4, 0.0, 1e4, 0x8,
                                dummy, dummy, dummy, 1 << 20, None) == 1
-    # pre-rotated operands are a self-attention option: refused with separate key segments
-    assert lib.vlc_attn_fwd_qkv(dummy, dummy, dummy, dummy, dummy, 3, 9, 12, 2, 2, 128, 4, 6, 0.0, 1e4, 0x2,
+    # all keys visible needs separate key segments and operands rotated beforehand
+    assert lib.vlc_attn_fwd_ex(dummy, dummy, dummy, dummy, None, 3, 9, 2, 2, 128, 4, 0.0, 1e4, 0x6,
+                               dummy, dummy, dummy, 1 << 20, None) == 1
+    assert lib.vlc_attn_fwd_qkv(dummy, dummy, dummy, dummy, dummy, 3, 9, 12, 2, 2, 128, 4, 6, 0.0, 1e4, 0x4,
                                 dummy, dummy, dummy, 1 << 20, None) == 1
+    # the backward takes pre-rotated operands for self-attention only, and no all-visible blocks
+    assert lib.vlc_attn_bwd_qkv(dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 3, 9, 12, 2, 2, 128, 4,
+                                6, 0.0, 1e4, 0x2, dummy, dummy, dummy, dummy, 1 << 20, None) == 1
+    assert lib.vlc_attn_bwd_qkv(dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 3, 9, 12, 2, 2, 128, 4,
+                                6, 0.0, 1e4, 0x4, dummy, dummy, dummy, dummy, 1 << 20, None) == 3
+    # context-parallel host calls and argument checks
+    assert lib.vlc_cp_block_mode(2, 0, 1, 1, 0) == 2 and lib.vlc_cp_block_mode(2, 0, 2, 0, 0) == -1
+    assert lib.vlc_rope_pos(dummy, dummy, 4, 2, 128, 9, 1e4, 0x2, dummy, dummy, 1 << 20, None) == 1
+    assert lib.vlc_rope_pos(dummy, dummy, 4, 2, 96, 9, 1e4, 0, dummy, dummy, 1 << 20, None) == 3
+    assert lib.vlc_rope_pos(dummy, dummy, 4, 2, 128, 9, 1e4, 0, dummy, None, 0, None) == 4
+    assert lib.vlc_rope_pos_workspace_bytes(127, 128) == 256 + 128 * 64 * 8
+    assert lib.vlc_lse_merge(None, None, 1, 4, 2, 128, dummy, dummy, None) == 1
+    parts = (ctypes.c_void_p * 17)()
+    assert lib.vlc_lse_merge(parts, parts, 17, 4, 2, 128, dummy, dummy, None) == 1
     assert lib.vlc_rope_qk(dummy, dummy, dummy, None, 3, 9, 2, 2, 128, 4, 1e4, 0x2, dummy, dummy, dummy,
                            1 << 20, None) == 1
     assert lib.vlc_attn_bwd_ex(dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 3, 9, 2, 2, 128,

@@ -98,3 +98,66 @@ def test_ranks_shard_packs_consistently_without_exchange():
         assert all(x[2] == g[0][2] for x in g)               # every rank computed the same loads
         assert [x[1] for x in g] == g[0][2]                  # a rank's load is its windows' sum L^2
     assert out[0] == out[1]
+
+
+def _cp_worker(rank, world, port, out):
+    """One rank of a context-parallel ring over gloo: the product's host partition and block
+    rule decide what is held and computed; the oracle stands in for the device attention."""
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import numpy as np
+    import torch.distributed as dist
+
+    import variable_length_causal_gb300 as vlc
+    from oracle import cp as ocp
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    lengths = [48, 16, 96]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T, H, d = int(cu[-1]), 2, 8
+    g = np.random.default_rng(5)                      # every rank draws the same pack
+    q, k, v = (g.standard_normal((T, H, d)) for _ in range(3))
+    seg_all = np.repeat(np.arange(len(lengths)), lengths)
+    rows, pos, cu_chunk = vlc.cp_partition(cu, world, rank)
+    # the rank keeps only its own rows; the ring hands the key/value halves around
+    kv_local = torch.from_numpy(np.concatenate([k[rows], v[rows]], axis=1))
+    gathered = [torch.empty_like(kv_local) for _ in range(world)]
+    dist.all_gather(gathered, kv_local)
+    meta = torch.from_numpy(np.stack([rows, pos.astype(np.int64)]))
+    metas = [torch.empty_like(meta) for _ in range(world)]
+    dist.all_gather(metas, meta)
+    half = len(rows) // 2
+    outs = []
+    for qh in (0, 1):
+        qs = slice(qh * half, (qh + 1) * half)
+        o_parts, l_parts = [], []
+        for step in range(world):
+            src = (rank - step) % world
+            kv = gathered[src].numpy()
+            k_rows, k_pos = metas[src][0].numpy(), metas[src][1].numpy()
+            for kh in (0, 1):
+                mode = vlc.cp_block_mode(world, rank, qh, src, kh)
+                if mode == vlc.binding.CP_BLOCK_NONE:
+                    continue
+                ks = slice(kh * half, (kh + 1) * half)
+                o_p, l_p = ocp.block_attention(q[rows[qs]], kv[ks, :H], kv[ks, H:], seg_all[rows[qs]], pos[qs],
+                                               seg_all[k_rows[ks]], k_pos[ks], 1.0 / np.sqrt(d))
+                o_parts.append(o_p)
+                l_parts.append(l_p)
+        outs.append(ocp.lse_merge(o_parts, l_parts))
+    o_full, l_full = ocp.block_attention(q[rows], k, v, seg_all[rows], pos, seg_all, np.arange(T) - cu[seg_all],
+                                         1.0 / np.sqrt(d))
+    err_o = max(float(np.abs(outs[h][0] - o_full[h * half:(h + 1) * half]).max()) for h in (0, 1))
+    err_l = max(float(np.abs(outs[h][1] - l_full[:, h * half:(h + 1) * half]).max()) for h in (0, 1))
+    out[rank] = (err_o, err_l, rows.tolist())
+    dist.destroy_process_group()
+
+
+def test_context_parallel_ring_over_two_gloo_ranks():
+    world = 2
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_cp_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+    for r in range(world):
+        assert out[r][0] < 1e-12 and out[r][1] < 1e-12
+    assert sorted(out[0][2] + out[1][2]) == list(range(160))

@@ -29,6 +29,10 @@ PACK_MODES = {"ffd": 0, "first_fit": 1, "next_fit": 2}
 COST_KINDS = {"tokens": 0, "sumsq": 1}
 ROPE_INTERLEAVED = 0x1
 QK_ROTATED = 0x2
+KEYS_ALL_VISIBLE = 0x4
+DEVERR_POS = 0x80
+CP_BLOCK_NONE, CP_BLOCK_CAUSAL, CP_BLOCK_ALL = 0, 1, 2
+LSE_MERGE_MAX = 16
 
 EXPORTED = [
     "vlc_status_string", "vlc_version", "vlc_workspace_bytes", "vlc_worklist_capacity",
@@ -36,7 +40,8 @@ EXPORTED = [
     "vlc_get_error", "vlc_attn_fwd_noalloc", "vlc_ce_workspace_bytes", "vlc_shifted_ce",
     "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa", "vlc_attn_fwd_ex",
     "vlc_attn_bwd_ex", "vlc_workspace_bytes_qkv", "vlc_attn_fwd_qkv", "vlc_attn_bwd_qkv", "vlc_pack",
-    "vlc_shard_packs", "vlc_rope_qk", "vlc_set_wait_limit_us",
+    "vlc_shard_packs", "vlc_rope_qk", "vlc_set_wait_limit_us", "vlc_cp_partition", "vlc_cp_block_mode",
+    "vlc_rope_pos_workspace_bytes", "vlc_rope_pos", "vlc_lse_merge",
 ]
 
 _lock = threading.Lock()
@@ -71,6 +76,16 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_version.restype = cint
         lib.vlc_set_wait_limit_us.argtypes = [ctypes.c_uint32]
         lib.vlc_set_wait_limit_us.restype = None
+        lib.vlc_cp_partition.argtypes = [P, i32, i32, i32, P, P, P, P]
+        lib.vlc_cp_partition.restype = cint
+        lib.vlc_cp_block_mode.argtypes = [i32, i32, i32, i32, i32]
+        lib.vlc_cp_block_mode.restype = cint
+        lib.vlc_rope_pos_workspace_bytes.argtypes = [i32, i32]
+        lib.vlc_rope_pos_workspace_bytes.restype = sz
+        lib.vlc_rope_pos.argtypes = [P, P, i32, i32, i32, i32, f32, ctypes.c_uint32, P, P, sz, P]
+        lib.vlc_rope_pos.restype = cint
+        lib.vlc_lse_merge.argtypes = [P, P, i32, i32, i32, i32, P, P, P]
+        lib.vlc_lse_merge.restype = cint
         lib.vlc_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, cint]
         lib.vlc_workspace_bytes.restype = sz
         lib.vlc_worklist_capacity.argtypes = [i32, i32, i32]
@@ -276,7 +291,7 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     check: bool = True, rope_interleaved: bool = False,
                     cu_seqlens_padded: Optional[torch.Tensor] = None,
                     cu_seqlens_kv: Optional[torch.Tensor] = None, max_seqlen_kv: Optional[int] = None,
-                    qk_rotated: bool = False):
+                    qk_rotated: bool = False, keys_all_visible: bool = False):
     """Segment-local causal attention with per-segment RoPE reset.  Returns (O, LSE[H, total]).
     k and v may have fewer heads than q (grouped: query head h reads head h // (H // H_kv)).
     rope_interleaved rotates the pairs (x[2j], x[2j+1]) instead of (x[j], x[j + d/2]).
@@ -285,7 +300,9 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     cu_seqlens_kv / max_seqlen_kv give k and v segments of their own, at least as long as the
     query segments; queries are bottom-right aligned (query p of a segment with L queries and
     Lk keys sits at position p + Lk - L and sees keys up to there).
-    qk_rotated: q and k already hold the rotated q', k' of ``rope_qk`` (no rotation here)."""
+    qk_rotated: q and k already hold the rotated q', k' of ``rope_qk`` (no rotation here).
+    keys_all_visible (with cu_seqlens_kv and qk_rotated): every key of a query's key segment is
+    visible, for a key block that precedes the query block (a context-parallel ring step)."""
     lib = load_library()
     _require_cuda(q, k, v, cu_seqlens, cu_seqlens_padded, cu_seqlens_kv)
     qkv = cu_seqlens_kv is not None
@@ -306,7 +323,8 @@ def varlen_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                            total_kv if qkv else None, max_seqlen_kv if qkv else None)
     else:
         ws = workspace
-    flags = (ROPE_INTERLEAVED if rope_interleaved else 0) | (QK_ROTATED if qk_rotated else 0)
+    flags = ((ROPE_INTERLEAVED if rope_interleaved else 0) | (QK_ROTATED if qk_rotated else 0)
+             | (KEYS_ALL_VISIBLE if keys_all_visible else 0))
     if qkv:
         st = lib.vlc_attn_fwd_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cu_seqlens_kv), nseg,
                                   total, total_kv, H, H_kv, d, int(max_seqlen), int(max_seqlen_kv),
@@ -480,3 +498,77 @@ def shard_packs(lengths, packing: Packing, ranks: int, cost: str = "sumsq"):
                              rank_of.ctypes.data_as(ctypes.c_void_p), load.ctypes.data_as(ctypes.c_void_p))
     _check(st, "vlc_shard_packs")
     return rank_of, load
+
+
+# ----------------------------------------------------------------------------- context-parallel split
+def cp_partition(cu_seqlens, cp: int, rank: int):
+    """Rows of the pack held by ``rank`` of a ``cp``-rank context-parallel group (host):
+    (rows int64 [total / cp], positions int32, cu_chunk int32 [nseg + 1]).  The local buffer
+    is the rank's low chunks of every segment, then its high chunks; each half is a packed
+    buffer with segment offsets cu_chunk.  Every segment length must be a multiple of 2 cp."""
+    lib = load_library()
+    cu = _host_i32(cu_seqlens)
+    nseg = len(cu) - 1
+    total = int(cu[-1])
+    if cp < 1 or total % cp != 0:
+        raise ValueError("the pack length must be a multiple of cp (every segment a multiple of 2 cp)")
+    rows = np.empty(total // cp, np.int64)
+    pos = np.empty(total // cp, np.int32)
+    cu_chunk = np.empty(nseg + 1, np.int32)
+    bad = ctypes.c_int32(-1)
+    st = lib.vlc_cp_partition(cu.ctypes.data, nseg, int(cp), int(rank), rows.ctypes.data, pos.ctypes.data,
+                              cu_chunk.ctypes.data, ctypes.byref(bad))
+    if st != 0 and bad.value >= 0:
+        raise ValueError(f"segment {bad.value} has a length that is not a multiple of 2 * cp = {2 * cp}")
+    _check(st, "vlc_cp_partition")
+    return rows, pos, cu_chunk
+
+
+def cp_block_mode(cp: int, q_rank: int, q_half: int, kv_rank: int, kv_half: int) -> int:
+    """CP_BLOCK_ALL, CP_BLOCK_CAUSAL or CP_BLOCK_NONE for the queries of (q_rank, q_half) against
+    the keys of (kv_rank, kv_half) (half 0 = low chunks, 1 = high chunks)."""
+    m = load_library().vlc_cp_block_mode(int(cp), int(q_rank), int(q_half), int(kv_rank), int(kv_half))
+    if m < 0:
+        raise ValueError("invalid cp / rank / half")
+    return m
+
+
+def rope_pos(x: torch.Tensor, pos: torch.Tensor, max_pos: int, rope_theta: float = 10000.0,
+             rope_interleaved: bool = False, out: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, check: bool = True) -> torch.Tensor:
+    """R(pos[i]) x[i] for every head of every row ([rows, H, d] bf16, pos int32 [rows])."""
+    lib = load_library()
+    _require_cuda(x, pos)
+    rows, H, d = x.shape
+    out = torch.empty_like(x) if out is None else out
+    need = lib.vlc_rope_pos_workspace_bytes(int(max_pos), d)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device) if workspace is None else workspace
+    st = lib.vlc_rope_pos(_ptr(x), _ptr(pos), rows, H, d, int(max_pos), float(rope_theta),
+                          ROPE_INTERLEAVED if rope_interleaved else 0, _ptr(out), _ptr(ws), ws.numel(),
+                          _stream(x.device))
+    _check(st, "vlc_rope_pos")
+    if check:
+        _raise_device_error(ws, "vlc_rope_pos")
+    return out
+
+
+def lse_merge(o_parts, lse_parts, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """Merge attention results over disjoint key sets: O parts bf16 [rows, H, d], LSE parts fp32
+    [H, rows]; returns (O, LSE) over the union."""
+    lib = load_library()
+    n = len(o_parts)
+    if n != len(lse_parts) or not 1 <= n <= LSE_MERGE_MAX:
+        raise ValueError(f"1 to {LSE_MERGE_MAX} parts, as many O as LSE")
+    _require_cuda(*o_parts, *lse_parts)
+    rows, H, d = o_parts[0].shape
+    for a, b in zip(o_parts, lse_parts):
+        if tuple(a.shape) != (rows, H, d) or tuple(b.shape) != (H, rows) or not a.is_contiguous() \
+                or not b.is_contiguous():
+            raise ValueError("parts must be contiguous bf16 [rows, H, d] and fp32 [H, rows]")
+    out = torch.empty_like(o_parts[0]) if out is None else out
+    lse = torch.empty((H, rows), dtype=torch.float32, device=out.device) if lse is None else lse
+    optr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in o_parts])
+    lptr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in lse_parts])
+    st = lib.vlc_lse_merge(optr, lptr, n, rows, H, d, _ptr(out), _ptr(lse), _stream(out.device))
+    _check(st, "vlc_lse_merge")
+    return out, lse

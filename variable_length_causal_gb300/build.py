@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libvlc.so")
-SOURCES = ["api.cu", "prep.cu", "attn_fwd.cu", "attn_bwd.cu", "noalloc.cu", "ce.cu", "packer.cpp"]
+SOURCES = ["api.cu", "prep.cu", "attn_fwd.cu", "attn_bwd.cu", "noalloc.cu", "ce.cu", "packer.cpp", "cp.cpp",
+           "cp_kernels.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "attn_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

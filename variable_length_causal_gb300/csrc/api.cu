@@ -147,8 +147,16 @@ static int check_attn_args(const AttnArgs& a, int is_bwd) {
     if (a.nseg < 1 || a.total < 1 || a.H < 1 || a.max_seqlen < 1) return VLC_ERR_ARG;
     if (a.cu_kv != nullptr && (a.total_kv < 1 || a.max_seqlen_kv < 1)) return VLC_ERR_ARG;
     if (a.Hkv < 1 || a.H % a.Hkv != 0) return VLC_ERR_ARG;
-    if (a.flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED | VLC_QK_ROTATED)) return VLC_ERR_ARG;
-    if ((a.flags & VLC_QK_ROTATED) && a.cu_kv != nullptr) return VLC_ERR_ARG;   // vlc_rope_qk is self-attention
+    if (a.flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED | VLC_QK_ROTATED | VLC_KEYS_ALL_VISIBLE))
+        return VLC_ERR_ARG;
+    // the backward takes rotated operands for self-attention only (the operands of vlc_rope_qk)
+    if (is_bwd && (a.flags & VLC_QK_ROTATED) && a.cu_kv != nullptr) return VLC_ERR_ARG;
+    if (a.flags & VLC_KEYS_ALL_VISIBLE) {
+        // a block of keys that all precede the queries: separate key segments, and no
+        // in-kernel rotation (the positions are not implied by the lengths)
+        if (is_bwd) return VLC_ERR_UNSUPPORTED;
+        if (a.cu_kv == nullptr || !((a.flags & VLC_QK_ROTATED) || a.rope_theta == 0.f)) return VLC_ERR_ARG;
+    }
     if (!(a.rope_theta >= 0.f) || !std::isfinite(a.rope_theta)) return VLC_ERR_ARG;
     if (a.d != 64 && a.d != 128) return VLC_ERR_UNSUPPORTED;
     if (a.max_seqlen > VLC_MAX_SEQLEN || a.max_seqlen_kv > VLC_MAX_SEQLEN) return VLC_ERR_UNSUPPORTED;
@@ -217,6 +225,7 @@ static int attn_fwd_impl(AttnArgs a) {
     p.scale_log2 = scale * 1.4426950408889634f;
     p.use_rope = mode;
     p.wait_limit_us = wait_limit_us();
+    p.keys_all_visible = (a.flags & VLC_KEYS_ALL_VISIBLE) ? 1 : 0;
     // long segments: k rotated once into the workspace (if it has room), not once per unit
     p.krot = nullptr;
     p.prerot_min = kPreRotMinKeys;
@@ -530,6 +539,7 @@ int vlc_get_error(const void* ws, int32_t* bits_out, void* stream) {
     if (cudaStreamSynchronize(s) != cudaSuccess) return VLC_ERR_CUDA;
     if (bits_out != nullptr) *bits_out = bits;
     if (bits & VLC_DEVERR_TIMEOUT) return VLC_ERR_TIMEOUT;
+    if (bits & VLC_DEVERR_POS) return VLC_ERR_ARG;
     if (bits & ~VLC_DEVERR_LABEL) return VLC_ERR_CU_SEQLENS;
     if (bits != 0) return VLC_ERR_LABEL;
     return VLC_OK;

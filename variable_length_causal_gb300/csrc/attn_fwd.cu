@@ -551,7 +551,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         setmaxnreg_dec<kCtrlRegs>();
         {   // the whole warp: lane 0 claims and publishes, all lanes decode
             auto decode = [&](int u) {
-                return decode_unit_warp<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                Unit w = decode_unit_warp<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                // all keys visible: the diagonal moves past the last key (query p sees keys up to p + Lk)
+                if (KV && p.keys_all_visible) w.off = w.Lk;
+                return w;
             };
             for (int n = 0;; ++n) {
                 int u;
@@ -604,7 +607,7 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
         !make_tmap_thd(&tv, p.v, p.total_kv, p.Hkv, p.d, 128))
         return cudaErrorInvalidValue;
     const dim3 grid(num_sms), block(fwd::kThreads);
-    const bool kv = p.cu_kv != p.cu;
+    const bool kv = p.cu_kv != p.cu || p.keys_all_visible;
     // one instance with RoPE warps, one whose softmax warps take their registers
     const bool rope = p.use_rope != kRopeNone;
     auto kernel = p.d == 128

@@ -112,6 +112,8 @@ struct FwdParams {
     float scale_log2;          // softmax_scale * log2(e)
     int use_rope;              // kRopeNone, kRopeHalf (rotate-half pairs) or kRopeInterleaved
     uint32_t wait_limit_us;    // limit of one bounded wait in the kernel (kWaitLimitUs by default)
+    int keys_all_visible;      // 1: every key of a query's key segment is visible (no causal mask;
+                               // separate key segments, operands rotated beforehand)
 };
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s);
