@@ -172,13 +172,14 @@ def make_inputs(w: synth.Workload, device, rank: int):
 class Step:
     """Pre-allocated buffers and one call per path step (no allocation inside the step)."""
 
-    def __init__(self, vlc, w, q, k, v, g, tokens, cu, ign, fwd_only=False):
+    def __init__(self, vlc, w, q, k, v, g, tokens, cu, ign, fwd_only=False, rope="once"):
         self.vlc, self.w = vlc, w
         self.q, self.k, self.v, self.g, self.tokens, self.cu, self.ign = q, k, v, g, tokens, cu, ign
         dev = q.device
         self.o = torch.empty_like(q)
         self.lse = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
         self.fwd_only = fwd_only
+        self.rope = rope   # "once": q, k rotated by one pass for both directions; "fused": in the kernels
         if fwd_only:
             self.dq = self.dk = self.dv = None
         else:
@@ -198,16 +199,19 @@ class Step:
         self.pos, self.lab = vlc.build_positions_labels(self.cu, self.tokens, self.ign, err=self.err)
         if ev is not None:
             ev[1].record()
-        vlc.rope_qk(self.q, self.k, self.cu, w.max_seqlen, rope_theta=w.theta, out=(self.qr, self.kr),
-                    workspace=self.ws_f, check=False)
-        vlc.varlen_attn_fwd(self.qr, self.kr, self.v, self.cu, w.max_seqlen, rope_theta=w.theta, out=self.o,
-                            lse=self.lse, workspace=self.ws_f, check=False, qk_rotated=True)
+        once = self.rope == "once"
+        if once:
+            vlc.rope_qk(self.q, self.k, self.cu, w.max_seqlen, rope_theta=w.theta, out=(self.qr, self.kr),
+                        workspace=self.ws_f, check=False)
+        qa, ka = (self.qr, self.kr) if once else (self.q, self.k)
+        vlc.varlen_attn_fwd(qa, ka, self.v, self.cu, w.max_seqlen, rope_theta=w.theta, out=self.o,
+                            lse=self.lse, workspace=self.ws_f, check=False, qk_rotated=once)
         if ev is not None:
             ev[2].record()
         if not self.fwd_only:
-            vlc.varlen_attn_bwd(self.g, self.qr, self.kr, self.v, self.o, self.lse, self.cu, w.max_seqlen,
+            vlc.varlen_attn_bwd(self.g, qa, ka, self.v, self.o, self.lse, self.cu, w.max_seqlen,
                                 rope_theta=w.theta, dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws_b,
-                                check=False, qk_rotated=True)
+                                check=False, qk_rotated=once)
         if ev is not None:
             ev[3].record()
 
@@ -221,9 +225,13 @@ class Step:
 
 
 # posl; rotation (worklist and table in one launch + q'/k'); forward (worklist + attention);
-# backward (2 worklists and table in one launch + delta + dq + dkdv)
-LAUNCHES_PER_STEP = 1 + 2 + 2 + 4
-LAUNCHES_PER_FWD_STEP = 1 + 2 + 2
+# backward (2 worklists and table in one launch + delta + dq + dkdv).  With RoPE in the
+# kernels there is no rotation pass; the forward adds the rotated-k pass of long segments
+# when the pack has a segment of at least 2048 keys.
+def launches_per_step(w, fwd_only, rope):
+    rot = 2 if rope == "once" else 0
+    krot = 1 if rope == "fused" and int(w.max_seqlen) >= 2048 else 0
+    return 1 + rot + 2 + krot + (0 if fwd_only else 4)
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -320,7 +328,7 @@ def gpu_arm(args, w, world, rank, local):
     q, k, v, g, tokens, cu, ign = make_inputs(w, dev, rank)
     if args.fwd_only:
         g = None
-    step = Step(vlc, w, q, k, v, g, tokens, cu, ign, fwd_only=args.fwd_only)
+    step = Step(vlc, w, q, k, v, g, tokens, cu, ign, fwd_only=args.fwd_only, rope=args.rope)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -363,14 +371,17 @@ def gpu_arm(args, w, world, rank, local):
         "positions_labels": {"ms": t_pos, "GB/s": pos_bytes / (t_pos * 1e-3) / 1e9},
         "attn_fwd_call": {"ms": t_fwd, "ms_median": statistics.median(per_fwd), "ms_min": min(per_fwd),
                           "eff_TFLOP/s": fwd_tflops,
-                          "kernels": "rotation (meta_kernel: work list + RoPE table; rope_qk_kernel) + meta_kernel (work list) + attn_fwd_kernel"},
+                          "kernels": ("rotation (meta_kernel: work list + RoPE table; rope_qk_kernel) + meta_kernel "
+                                      "(work list) + attn_fwd_kernel" if args.rope == "once" else
+                                      "meta_kernel (work list + RoPE table) [+ krot_kernel] + attn_fwd_kernel")},
         "attn_bwd_call": {"ms": t_bwd, "ms_median": statistics.median(per_bwd), "ms_min": min(per_bwd),
                           "eff_TFLOP/s": bwd_tflops,
                           "kernels": "meta_kernel (2 work lists + RoPE tables) + prep_kernel (delta) + dq_kernel + dkdv_kernel"},
     }
     dominant = "attn_bwd_call" if t_bwd >= t_fwd else "attn_fwd_call"
     ach = bwd_tflops if dominant == "attn_bwd_call" else fwd_tflops
-    traffic = _traffic_from_profiles(dominant, w.name) if args.bins is None else None
+    traffic = (_traffic_from_profiles(dominant if args.rope == "once" else dominant + "_fused", w.name)
+               if args.bins is None else None)
     roofline = {"bound": "tensor", "kernel": dominant, "achieved": ach, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} bf16 burst",
@@ -386,13 +397,19 @@ def gpu_arm(args, w, world, rank, local):
         "tokens_per_s": real_tok / (ms * 1e-3),
         "fwd_eff_tflops": fwd_tflops, "bwd_eff_tflops": bwd_tflops,
         "kernels": kernels, "roofline": roofline, "roofline_fwd": roofline_fwd,
-        "gpu_launches": (LAUNCHES_PER_FWD_STEP if args.fwd_only else LAUNCHES_PER_STEP) * args.steps,
+        "gpu_launches": launches_per_step(w, args.fwd_only, args.rope) * args.steps,
+        "rope": ("q, k rotated once per step (vlc_rope_qk), both passes on the rotated operands"
+                 if args.rope == "once" else "RoPE inside the attention kernels (forward tiles, backward prep)"),
         "clocks": clk.summary(),
         "e2e": e2e,
     }
     if not args.no_extras and args.bins is None and world == 1:
         line["extras"] = extra_measurements(vlc, w, dev, peaks, q, k, v, step)
         line["extras"]["forward_configs"] = forward_configs(vlc, dev, peaks)
+        if not args.fwd_only:
+            line["extras"]["step_other_rope_form"] = step_form_measurement(
+                vlc, w, q, k, v, g, tokens, cu, ign, "fused" if args.rope == "once" else "once")
+        line["extras"]["context_parallel"] = context_parallel_measurement(vlc, dev, peaks)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, q, k, v, g, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -474,6 +491,97 @@ def forward_configs(vlc, dev, peaks, reps: int = 300):
     out["clocks"] = clk.summary()
     out["peak"] = {"bf16_tflops": peaks["bf16_tflops"], "source": f"{peaks['source']} bf16 burst"}
     return out
+
+
+def step_form_measurement(vlc, w, q, k, v, g, tokens, cu, ign, rope, reps: int = 30):
+    """The same step with the other RoPE form (median of per-step CUDA events)."""
+    st = Step(vlc, w, q, k, v, g, tokens, cu, ign, rope=rope)
+    med, mn = _time_events(st, reps)
+    st.check_errors()
+    fl = synth.fwd_flops(w) + synth.bwd_flops(w)
+    return {"rope": rope, "ms_median": med, "ms_min": mn, "eff_TFLOP/s": fl / (med * 1e-3) / 1e12}
+
+
+def context_parallel_measurement(vlc, dev, peaks, L: int = 131072, cp: int = 4, H: int = 32, d: int = 128,
+                                 reps: int = 5):
+    """One 131072-token document split over a 4-rank context-parallel group (2 cp chunks, rank i
+    holding chunks i and 2cp-1-i), the ranks' work run one after another on this GPU: every
+    rank rotates its rows by their positions in the document, computes its blocks of the ring
+    (the chunk's own causal block, and every earlier chunk with all keys visible) and merges
+    the partial results.  No communication is timed (one GPU).  Compared with the whole
+    document's causal forward on this GPU: balance = max rank time / mean rank time, and
+    split overhead = cp * mean rank time / whole-document time."""
+    w = synth.custom_workload([L], H, d)
+    q, k, v = synth.make_tensors(w, device=dev, seed=4321)
+    cu = torch.from_numpy(w.cu).to(dev)
+    qr, kr = vlc.rope_qk(q, k, cu, L)
+    o1 = torch.empty_like(q)
+    l1 = torch.empty((H, L), dtype=torch.float32, device=dev)
+    ws1 = vlc.new_workspace(1, L, H, d, L, False, dev)
+    full_ms, _ = _time_events(lambda: vlc.varlen_attn_fwd(qr, kr, v, cu, L, out=o1, lse=l1, workspace=ws1,
+                                                          check=False, qk_rotated=True), reps)
+    del o1, l1, ws1
+    locs = {}
+    for r in range(cp):
+        rows, pos, cu_chunk = vlc.cp_partition(w.cu, cp, r)
+        rows_d = torch.from_numpy(rows).to(dev)
+        locs[r] = (rows_d, torch.from_numpy(pos).to(dev), torch.from_numpy(cu_chunk).to(dev), q[rows_d].contiguous(),
+                   k[rows_d].contiguous(), v[rows_d].contiguous())
+    half = L // cp // 2
+    m = L // (2 * cp)
+    rank_ms = []
+    for r in range(cp):
+        rows_d, pos_d, cuc, ql, kl, vl = locs[r]
+        qrl, krl = torch.empty_like(ql), torch.empty_like(kl)
+        wsr = torch.empty(vlc.load_library().vlc_rope_pos_workspace_bytes(L - 1, d), dtype=torch.uint8, device=dev)
+        # every other rank's rotated k/v halves, as the ring would deliver them
+        peers = {}
+        for s2 in range(cp):
+            _, p2, _, _, k2, v2 = locs[s2]
+            peers[s2] = (vlc.rope_pos(k2, p2, L - 1), v2)
+        blocks = []
+        for qh in (0, 1):
+            for step in range(cp):
+                src = (r - step) % cp
+                for kh in (0, 1):
+                    mode = vlc.cp_block_mode(cp, r, qh, src, kh)
+                    if mode != vlc.binding.CP_BLOCK_NONE:
+                        blocks.append((qh, src, kh, mode))
+        outs = {qh: [] for qh in (0, 1)}
+        wsb = vlc.new_workspace(1, m, H, d, m, False, dev, total_kv=m, max_seqlen_kv=m)
+        for qh, src, kh, mode in blocks:
+            outs[qh].append((torch.empty((half, H, d), dtype=torch.bfloat16, device=dev),
+                             torch.empty((H, half), dtype=torch.float32, device=dev)))
+        om = [torch.empty((half, H, d), dtype=torch.bfloat16, device=dev) for _ in (0, 1)]
+        lm = [torch.empty((H, half), dtype=torch.float32, device=dev) for _ in (0, 1)]
+
+        def rank_fwd():
+            vlc.rope_pos(ql, pos_d, L - 1, out=qrl, workspace=wsr, check=False)
+            vlc.rope_pos(kl, pos_d, L - 1, out=krl, workspace=wsr, check=False)
+            cnt = {0: 0, 1: 0}
+            for qh, src, kh, mode in blocks:
+                o_p, l_p = outs[qh][cnt[qh]]
+                cnt[qh] += 1
+                kk, vv = peers[src]
+                vlc.varlen_attn_fwd(qrl[qh * half:(qh + 1) * half], kk[kh * half:(kh + 1) * half],
+                                    vv[kh * half:(kh + 1) * half], cuc, m, out=o_p, lse=l_p, workspace=wsb,
+                                    check=False, cu_seqlens_kv=cuc, max_seqlen_kv=m, qk_rotated=True,
+                                    keys_all_visible=mode == vlc.binding.CP_BLOCK_ALL)
+            for qh in (0, 1):
+                vlc.lse_merge([a for a, _ in outs[qh]], [b for _, b in outs[qh]], out=om[qh], lse=lm[qh])
+
+        ms, _ = _time_events(rank_fwd, reps)
+        st, bits = vlc.get_error(wsb)
+        if st != 0:
+            raise RuntimeError(f"context-parallel block: device error status {st} bits 0x{bits:x}")
+        rank_ms.append(ms)
+        del peers, outs, om, lm, qrl, krl, wsb
+    mean = sum(rank_ms) / cp
+    fl = 4.0 * d * H * L * (L + 1) / 2
+    return {"document_tokens": L, "cp": cp, "H": H, "head_dim": d, "whole_forward_ms": full_ms,
+            "whole_forward_eff_TFLOP/s": fl / (full_ms * 1e-3) / 1e12, "rank_forward_ms": rank_ms,
+            "balance_max_over_mean": max(rank_ms) / mean, "split_overhead": cp * mean / full_ms,
+            "note": "ranks run one after another on one GPU; communication not included"}
 
 
 def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
@@ -637,7 +745,7 @@ def e2e_measure(vlc, w, step, steps, world, dev, readback="result"):
     k+2's inputs arrive."""
     sets = [step, Step(vlc, w, *(torch.empty_like(t) if t is not None else None
                                  for t in (step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign)),
-                       fwd_only=step.fwd_only)]
+                       fwd_only=step.fwd_only, rope=step.rope)]
     host_in = [t.cpu().pin_memory() for t in (step.q, step.k, step.v, step.g, step.tokens, step.cu, step.ign)
                if t is not None]
 
@@ -763,6 +871,9 @@ def main():
     ap.add_argument("--workload", default="pt_bwd", choices=synth.WORKLOAD_NAMES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--rope", choices=("once", "fused"), default="once",
+                    help="once: the step rotates q, k by one pass and both directions run on q', k'; "
+                         "fused: the attention kernels rotate (forward tiles, backward prep pass)")
     ap.add_argument("--fwd-only", action="store_true",
                     help="step = positions/labels + forward only (for profiling the forward kernel)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
