@@ -345,7 +345,8 @@ struct Layout {
     static constexpr uint32_t V0 = K0 + kKStages * TILE;       // kVStages
     static constexpr uint32_t BAR0 = V0 + kVStages * TILE;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;      // tmem slot, abort flag, wait limit, unit ring
-    static constexpr uint32_t BYTES = MISC + 16 + 4 * kSlotInts * kRing;
+    static constexpr uint32_t RING = (MISC + 16 + 15) / 16 * 16;   // 16-byte aligned slots
+    static constexpr uint32_t BYTES = RING + 4 * kSlotInts * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     // TMEM: S at columns 0..127, dP at 128 (the packed bf16 dS of a step overwrites
     // the consumed dP columns), the dQ accumulator at 256, and the unit's Q' and dO
@@ -397,7 +398,7 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     auto bar = [&](int i) -> uint32_t { return sbase + LY::BAR0 + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);   // [abort flag, wait limit in us]
-    const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 16), bar(UNIT_FULL), bar(UNIT_EMPTY)};
+    const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::RING), bar(UNIT_FULL), bar(UNIT_EMPTY)};
     constexpr int kRingConsumers = 1 + 1 + 1 + 8;   // Q'/dO/K' and V producers, MMA warp, 8 math warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -819,7 +820,8 @@ struct Layout {
     static constexpr uint32_t LSED = DO0 + kQStages * TILE;    // kLsedSlots x (128 lse2 + 128 delta)
     static constexpr uint32_t BAR0 = LSED + kLsedSlots * 256 * 4;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;      // tmem slot, abort flag, wait limit, unit ring
-    static constexpr uint32_t BYTES = MISC + 16 + 4 * kSlotInts * kRing;
+    static constexpr uint32_t RING = (MISC + 16 + 15) / 16 * 16;   // 16-byte aligned slots
+    static constexpr uint32_t BYTES = RING + 4 * kSlotInts * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     // TMEM: S^T at 0, dP^T at 128 (the packed bf16 P^T / dS^T of a step overwrite the
     // consumed S^T / dP^T columns), dV and dK accumulators after them.
@@ -838,7 +840,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     auto bar = [&](int i) -> uint32_t { return sbase + LY::BAR0 + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);   // [abort flag, wait limit in us]
-    const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 16), bar(UNIT_FULL), bar(UNIT_EMPTY)};
+    const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::RING), bar(UNIT_FULL), bar(UNIT_EMPTY)};
     constexpr int kRingConsumers = 1 + 1 + 1 + 8 + 4;   // TMA producer, MMA warp, LSE/delta stager, 8 math warps,
                                                         // 4 epilogue warps
     float* lsed = reinterpret_cast<float*>(sgen + LY::LSED);

@@ -104,7 +104,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 // scheduler claims ahead of the slowest role (kRing - 1 units).  A unit index of
 // -1 ends the sequence.
 constexpr int kRing = 2;
-constexpr int kSlotInts = 12;   // unit index + the 10 fields of Unit, padded
+constexpr int kSlotInts = 12;   // unit index + the 10 fields of Unit, padded (16-byte aligned slots)
 
 struct Ring {
     volatile int* slot;     // kRing x kSlotInts ints in shared memory
@@ -123,16 +123,16 @@ __device__ __forceinline__ bool ring_put_warp(const Ring& rg, int n, int* counte
     if (lane == 0) u = atomicAdd(counter, 1);
     u = __shfl_sync(0xffffffffu, u, 0);
     if (u >= nunits) u = -1;
-    volatile int* d = rg.slot + s * kSlotInts;
-    if (u >= 0) {
-        const Unit w = decode(u);
-        if (lane == 0) {
-            d[1] = w.seg; d[2] = w.tile; d[3] = w.lo; d[4] = w.hi; d[5] = w.h;
-            d[6] = w.L; d[7] = w.row0; d[8] = w.Lk; d[9] = w.row0k; d[10] = w.off;
-        }
-    }
+    Unit w{};
+    if (u >= 0) w = decode(u);
     if (lane == 0) {
-        d[0] = u;
+        const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(const_cast<int*>(rg.slot + s * kSlotInts)));
+        const int v[12] = {u, w.seg, w.tile, w.lo, w.hi, w.h, w.L, w.row0, w.Lk, w.row0k, w.off, 0};
+#pragma unroll
+        for (int q = 0; q < 3; ++q)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a + 16u * q), "r"(v[4 * q]),
+                         "r"(v[4 * q + 1]), "r"(v[4 * q + 2]), "r"(v[4 * q + 3])
+                         : "memory");
         mbar_arrive(rg.full0 + 8u * s);   // release: waiters see the slot
     }
     __syncwarp();
@@ -141,9 +141,19 @@ __device__ __forceinline__ bool ring_put_warp(const Ring& rg, int n, int* counte
 }
 
 __device__ __forceinline__ void ring_read(const volatile int* d, int& u, Unit& w) {
-    u = d[0];
-    w.seg = d[1]; w.tile = d[2]; w.lo = d[3]; w.hi = d[4]; w.h = d[5];
-    w.L = d[6]; w.row0 = d[7]; w.Lk = d[8]; w.row0k = d[9]; w.off = d[10];
+    // three 16-byte loads: the slot is read while the tensor pipe's operand reads keep the
+    // shared memory busy, so every separate access costs a queueing delay
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(const_cast<int*>(d)));
+    int v[12];
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[4 * q]), "=r"(v[4 * q + 1]), "=r"(v[4 * q + 2]), "=r"(v[4 * q + 3])
+                     : "r"(a + 16u * q)
+                     : "memory");
+    u = v[0];
+    w.seg = v[1]; w.tile = v[2]; w.lo = v[3]; w.hi = v[4]; w.h = v[5];
+    w.L = v[6]; w.row0 = v[7]; w.Lk = v[8]; w.row0k = v[9]; w.off = v[10];
 }
 
 // One consumer thread (a TMA producer or the MMA issuer).

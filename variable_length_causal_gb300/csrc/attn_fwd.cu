@@ -89,7 +89,8 @@ struct Layout {
     static constexpr uint32_t V0 = K0 + 2 * TILE;      // 2 stages
     static constexpr uint32_t BAR0 = V0 + 2 * TILE;
     static constexpr uint32_t MISC = BAR0 + NUM_BARS * 8;   // tmem slot, abort flag, wait limit, unit ring
-    static constexpr uint32_t BYTES = MISC + 16 + 4 * kSlotInts * kRing;
+    static constexpr uint32_t RING = (MISC + 16 + 15) / 16 * 16;   // 16-byte aligned slots
+    static constexpr uint32_t BYTES = RING + 4 * kSlotInts * kRing;
     static constexpr uint32_t ALLOC = BYTES + 1024;
     __host__ __device__ static constexpr uint32_t S_COL(int t) { return 128u * t; }   // P_t shares these columns
     __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256u + 128u * t; }
@@ -148,7 +149,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     auto bar = [&](int i) -> uint32_t { return sbase + LY::BAR0 + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + LY::MISC);
     volatile int* abort = reinterpret_cast<volatile int*>(sgen + LY::MISC + 4);   // [abort flag, wait limit in us]
-    const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::MISC + 16), bar(UNIT_FULL), bar(UNIT_EMPTY)};
+    const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::RING), bar(UNIT_FULL), bar(UNIT_EMPTY)};
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int kRingConsumers = 1 + 1 + 1 + 8 + 4;   // Q/K and V producers, MMA warp, 8 softmax warps, 4 RoPE warps
