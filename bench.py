@@ -404,12 +404,15 @@ def gpu_arm(args, w, world, rank, local):
         "e2e": e2e,
     }
     if not args.no_extras and args.bins is None and world == 1:
-        line["extras"] = extra_measurements(vlc, w, dev, peaks, q, k, v, step)
-        line["extras"]["forward_configs"] = forward_configs(vlc, dev, peaks)
-        if not args.fwd_only:
+        which = EXTRAS if args.extras == "all" else tuple(args.extras.split(","))
+        line["extras"] = extra_measurements(vlc, w, dev, peaks, q, k, v, step, which)
+        if "forward_configs" in which:
+            line["extras"]["forward_configs"] = forward_configs(vlc, dev, peaks)
+        if "step_form" in which and not args.fwd_only:
             line["extras"]["step_other_rope_form"] = step_form_measurement(
                 vlc, w, q, k, v, g, tokens, cu, ign, "fused" if args.rope == "once" else "once")
-        line["extras"]["context_parallel"] = context_parallel_measurement(vlc, dev, peaks)
+        if "cp" in which:
+            line["extras"]["context_parallel"] = context_parallel_measurement(vlc, dev, peaks)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, q, k, v, g, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -584,14 +587,17 @@ def context_parallel_measurement(vlc, dev, peaks, L: int = 131072, cp: int = 4, 
             "note": "ranks run one after another on one GPU; communication not included"}
 
 
-def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
+EXTRAS = ("positions", "ce", "variants", "packer", "padded", "forward_configs", "step_form", "cp")
+
+
+def extra_measurements(vlc, w, dev, peaks, q, k, v, step, which=EXTRAS):
     """Positions/labels bandwidth on large packs with the workload's length mix, and (long-context
     workload) the padded comparator: every document padded to the buffer length costs one full
     causal run of that length, and the whole pack run as one causal segment ignores the boundaries."""
     out = {}
     sweep = {}
     lens = np.diff(w.cu).astype(np.int64)
-    for logT in (24, 26):
+    for logT in ((24, 26) if "positions" in which else ()):
         T = 1 << logT
         reps = -(-T // int(lens.sum()))
         L = np.tile(lens, reps)
@@ -608,8 +614,21 @@ def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
         gbs = 20.0 * T / (ms * 1e-3) / 1e9
         sweep[f"T=2^{logT}"] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
         del cu, tok, pos, lab
-    out["positions_labels_sweep"] = sweep
-    # shifted cross-entropy over this pack's labels with a 32000-token vocabulary (bf16 logits)
+    if sweep:
+        out["positions_labels_sweep"] = sweep
+    if "ce" in which:
+        out["shifted_cross_entropy"] = ce_measurement(vlc, w, dev, peaks, step)
+    if "variants" in which:
+        out["varlen_variants"] = variant_measurements(vlc, w, dev, peaks, step)
+    if "packer" in which:
+        out["host_packer"] = packer_measurement(vlc)
+    if w.name == "long" and "padded" in which:
+        out["padded_comparator"] = padded_comparator(vlc, w, dev, q, k, v, step)
+    return out
+
+
+def ce_measurement(vlc, w, dev, peaks, step):
+    """Shifted cross-entropy over this pack's labels with a 32000-token vocabulary (bf16 logits)."""
     V = 32000
     gen = torch.Generator(device=dev).manual_seed(4242)
     logits = (torch.randn((w.total, V), generator=gen, device=dev) * 2.0).to(torch.bfloat16)
@@ -619,33 +638,33 @@ def extra_measurements(vlc, w, dev, peaks, q, k, v, step):
                                                        check=False), 10)
     rows_read = int((step.lab != -100).sum().item())
     ce_bytes = rows_read * V * 2.0 + w.total * (8 + 4 + 1 + 4 + 1)
-    out["shifted_cross_entropy"] = {"vocab": V, "rows_read": rows_read, "ms": ms_ce,
-                                    "GB/s": ce_bytes / (ms_ce * 1e-3) / 1e9,
-                                    "frac_hbm": ce_bytes / (ms_ce * 1e-3) / 1e9 / peaks["hbm_gbs"]}
-    del logits, ws_ce
-    out["varlen_variants"] = variant_measurements(vlc, w, dev, peaks, step)
-    out["host_packer"] = packer_measurement(vlc)
-    if w.name == "long":
-        cu1 = torch.tensor([0, w.total], dtype=torch.int32, device=dev)
-        o1 = torch.empty_like(q)
-        lse1 = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
-        ws1 = vlc.new_workspace(1, w.total, w.H, w.d, w.total, False, dev)
-        ms1 = _time_ms(lambda: vlc.varlen_attn_fwd(q, k, v, cu1, w.total, out=o1, lse=lse1, workspace=ws1,
-                                                    check=False), 3)
-        docs = int((w.seg_ignore == 0).sum())
-        ms_packed = _time_ms(lambda: vlc.varlen_attn_fwd(q, k, v, step.cu, w.max_seqlen, out=step.o, lse=step.lse,
-                                                          workspace=step.ws_f, check=False), 5)
-        out["padded_comparator"] = {
-            "docs": docs,
-            "causal_run_ms": ms1,
-            "padded_forward_ms": ms1 * docs,
-            "whole_pack_causal_forward_ms": ms1,
-            "packed_forward_ms": ms_packed,
-            "speedup_packed_vs_padded": ms1 * docs / ms_packed,
-            "causal_run_tflops": 4.0 * w.d * w.H * (w.total * (w.total + 1) / 2) / (ms1 * 1e-3) / 1e12,
-        }
-        del o1, lse1, ws1
-    return out
+    return {"vocab": V, "rows_read": rows_read, "ms": ms_ce, "GB/s": ce_bytes / (ms_ce * 1e-3) / 1e9,
+            "frac_hbm": ce_bytes / (ms_ce * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+
+
+def padded_comparator(vlc, w, dev, q, k, v, step):
+    """Every document padded to the buffer length costs one full causal run of that length; the
+    whole pack run as one causal segment ignores the boundaries."""
+    cu1 = torch.tensor([0, w.total], dtype=torch.int32, device=dev)
+    o1 = torch.empty_like(q)
+    lse1 = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
+    ws1 = vlc.new_workspace(1, w.total, w.H, w.d, w.total, False, dev)
+    ms1 = _time_ms(lambda: vlc.varlen_attn_fwd(q, k, v, cu1, w.total, out=o1, lse=lse1, workspace=ws1,
+                                                check=False), 3)
+    docs = int((w.seg_ignore == 0).sum())
+    ms_packed = _time_ms(lambda: vlc.varlen_attn_fwd(q, k, v, step.cu, w.max_seqlen, out=step.o, lse=step.lse,
+                                                      workspace=step.ws_f, check=False), 5)
+    res = {
+        "docs": docs,
+        "causal_run_ms": ms1,
+        "padded_forward_ms": ms1 * docs,
+        "whole_pack_causal_forward_ms": ms1,
+        "packed_forward_ms": ms_packed,
+        "speedup_packed_vs_padded": ms1 * docs / ms_packed,
+        "causal_run_tflops": 4.0 * w.d * w.H * (w.total * (w.total + 1) / 2) / (ms1 * 1e-3) / 1e12,
+    }
+    del o1, lse1, ws1
+    return res
 
 
 def packer_measurement(vlc, n: int = 10_000_000, capacity: int = 4096, ranks: int = 8):
@@ -879,6 +898,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--e2e-readback", choices=("result", "all"), default="result",
                     help="end-to-end leg: read back the step's LSE only (result) or every output (all)")
+    ap.add_argument("--extras", default="all",
+                    help="comma-separated subset of " + ",".join(EXTRAS) + " (default: all)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the positions/labels sweep and the padded comparator")
     ap.add_argument("--bins", type=int, default=None,
