@@ -193,11 +193,12 @@ int vlc_attn_bwd_gqa(const void* dout, const void* q, const void* k, const void*
                                       rotates nothing and takes dq, dk back through R(p)^T
                                       (rope_theta and the pairing bit as for the rotation); the
                                       backward takes it for self-attention only */
-#define VLC_KEYS_ALL_VISIBLE 0x4u  /* vlc_attn_fwd_qkv only, with VLC_QK_ROTATED (or rope_theta
-                                      == 0): every key of a query's key segment is visible (a
-                                      block of keys that all precede the block of queries, as in
-                                      a context-parallel ring); the backward returns
-                                      VLC_ERR_UNSUPPORTED for it */
+#define VLC_KEYS_ALL_VISIBLE 0x4u  /* the _qkv calls only: every key of a query's key segment is
+                                      visible (a block of keys that all precede the block of
+                                      queries, as in a context-parallel ring).  The forward
+                                      needs VLC_QK_ROTATED (or rope_theta == 0); the backward
+                                      needs rope_theta == 0 and returns the gradients with
+                                      respect to the operands as given */
 
 /* vlc_attn_fwd_gqa / vlc_attn_bwd_gqa with a padded layout and an option word;
  * cu_padded == NULL and flags == 0 is exactly those calls.
@@ -292,7 +293,12 @@ int vlc_attn_bwd_qkv(const void* dout, const void* q, const void* k, const void*
  * same chunk: the causal square block, L == Lk), VLC_CP_BLOCK_NONE (nothing to
  * compute); -1 for invalid arguments.  A ring step hands every rank another
  * rank's two key/value halves; the partial results (O, LSE) of a query half over
- * the blocks it sees are combined with vlc_lse_merge. */
+ * the blocks it sees are combined with vlc_lse_merge.  The backward of a block is
+ * vlc_attn_bwd_qkv with the merged O and LSE of the query half, rope_theta == 0
+ * (gradients with respect to the rotated operands) and VLC_KEYS_ALL_VISIBLE where
+ * the forward had it; a query half's dq' and a key half's dk', dv are the sums
+ * (vlc_sum_parts) over the blocks they took part in, and vlc_rope_pos with
+ * VLC_ROPE_TRANSPOSE takes dq', dk' back to dq, dk. */
 #define VLC_CP_BLOCK_NONE 0
 #define VLC_CP_BLOCK_CAUSAL 1
 #define VLC_CP_BLOCK_ALL 2
@@ -308,9 +314,12 @@ int vlc_cp_block_mode(int32_t cp, int32_t q_rank, int32_t q_half, int32_t kv_ran
  *   x, out    bf16 [rows, H, d] (d = 64 or 128), 16-byte aligned, not overlapping
  *   pos       device int32 [rows], 0 <= pos[i] <= max_pos; a position outside
  *             sets VLC_DEVERR_POS in the workspace word and that row's out = 0
- *   flags     VLC_ROPE_INTERLEAVED selects the pairing; rope_theta > 0
+ *   flags     VLC_ROPE_INTERLEAVED selects the pairing; VLC_ROPE_TRANSPOSE applies
+ *             R(pos[i])^T instead (takes gradients with respect to rotated
+ *             operands back to the unrotated ones); rope_theta > 0
  *   ws        vlc_rope_pos_workspace_bytes(max_pos, d) bytes, 256-byte aligned
  *             (error word and cos/sin table); vlc_get_error reads it */
+#define VLC_ROPE_TRANSPOSE 0x8u
 size_t vlc_rope_pos_workspace_bytes(int32_t max_pos, int32_t d);
 int vlc_rope_pos(const void* x, const int32_t* pos, int32_t rows, int32_t H, int32_t d, int32_t max_pos,
                  float rope_theta, uint32_t flags, void* out, void* ws, size_t ws_bytes, void* stream);
@@ -327,6 +336,12 @@ int vlc_rope_pos(const void* x, const int32_t* pos, int32_t rows, int32_t H, int
 #define VLC_LSE_MERGE_MAX 16
 int vlc_lse_merge(const void* const* o_parts, const float* const* lse_parts, int32_t nparts, int32_t rows,
                   int32_t H, int32_t d, void* o, float* lse, void* stream);
+
+/* out = sum of nparts bf16 arrays of `elems` elements (a multiple of 8), accumulated
+ * in fp32 and rounded once: the partial gradients of a context-parallel ring's
+ * blocks.  parts: host array of device pointers, 16-byte aligned; out must not
+ * overlap them; 1 <= nparts <= VLC_LSE_MERGE_MAX. */
+int vlc_sum_parts(const void* const* parts, int32_t nparts, int64_t elems, void* out, void* stream);
 
 /* ---------------------------------------------------------------- host packing
  * The data step in front of the path; plain host functions (no device, no

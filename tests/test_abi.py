@@ -47,6 +47,12 @@ def test_host_side_queries(lib):
     assert lib.vlc_worklist_capacity(3, 9, 128) == 3 + 0 + 1
 
 
+def parts_one(ctypes, p):
+    arr = (ctypes.c_void_p * 1)()
+    arr[0] = p
+    return arr
+
+
 def test_host_argument_checks_need_no_gpu(lib):
     import ctypes
 
@@ -67,11 +73,14 @@ def test_host_argument_checks_need_no_gpu(lib):
                                dummy, dummy, dummy, 1 << 20, None) == 1
     assert lib.vlc_attn_fwd_qkv(dummy, dummy, dummy, dummy, dummy, 3, 9, 12, 2, 2, 128, 4, 6, 0.0, 1e4, 0x4,
                                 dummy, dummy, dummy, 1 << 20, None) == 1
-    # the backward takes pre-rotated operands for self-attention only, and no all-visible blocks
+    # the backward takes pre-rotated operands for self-attention only, and all-visible blocks only
+    # without RoPE (gradients with respect to the operands as given)
     assert lib.vlc_attn_bwd_qkv(dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 3, 9, 12, 2, 2, 128, 4,
                                 6, 0.0, 1e4, 0x2, dummy, dummy, dummy, dummy, 1 << 20, None) == 1
     assert lib.vlc_attn_bwd_qkv(dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 3, 9, 12, 2, 2, 128, 4,
-                                6, 0.0, 1e4, 0x4, dummy, dummy, dummy, dummy, 1 << 20, None) == 3
+                                6, 0.0, 1e4, 0x4, dummy, dummy, dummy, dummy, 1 << 20, None) == 1
+    assert lib.vlc_sum_parts(None, 1, 8, dummy, None) == 1
+    assert lib.vlc_sum_parts(parts_one(ctypes, dummy), 1, 12, dummy, None) == 1     # not a multiple of 8
     # context-parallel host calls and argument checks
     assert lib.vlc_cp_block_mode(2, 0, 1, 1, 0) == 2 and lib.vlc_cp_block_mode(2, 0, 2, 0, 0) == -1
     assert lib.vlc_rope_pos(dummy, dummy, 4, 2, 128, 9, 1e4, 0x2, dummy, dummy, 1 << 20, None) == 1

@@ -167,3 +167,80 @@ def test_context_parallel_ring_matches_full_attention(vlc, cp, lens, H, d):
         assert e.max() <= O_MAX and e.mean() <= O_MEAN
         gl = lse_loc[torch.from_numpy(heads).to(DEV), torch.from_numpy(pick).to(DEV)].cpu().numpy()
         assert np.abs(gl - l_ref).max() <= LSE_MAX
+
+
+def test_rope_pos_transpose_inverts(vlc):
+    x = _bf16((300, 2, 128), 5).to(DEV)
+    pos = torch.arange(300, dtype=torch.int32, device=DEV) * 7 % 1000
+    y = vlc.rope_pos(x, pos, 999)
+    back = vlc.rope_pos(y, pos, 999, transpose=True)
+    assert (back.float() - x.float()).abs().max().item() <= 2e-2    # two bf16 roundings
+    # the transpose is the rotation by -p: against the oracle's fp64 rotation
+    ref = oracle.rope_rows(x.float().cpu().numpy().reshape(-1, 128), -np.repeat(pos.cpu().numpy(), 2))
+    got = vlc.rope_pos(x, pos, 999, transpose=True).float().cpu().numpy().reshape(-1, 128)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.maximum(np.abs(ref), 1e-30) + 1e-6)
+
+
+def test_sum_parts(vlc):
+    parts = [_bf16((37, 3, 64), 60 + i).to(DEV) for i in range(5)]
+    out = vlc.sum_parts(parts)
+    ref = sum(p.double() for p in parts)
+    assert ((out.double() - ref).abs() <= 2.0 ** -8 * ref.abs() + 1e-6).all()
+
+
+@pytest.mark.parametrize("cp", [2, 4])
+def test_context_parallel_ring_backward_matches_full_gradients(vlc, cp):
+    """The ring's backward, all ranks one after another: every block's backward with the
+    merged O and LSE of its query half, block gradients summed per query half and per key
+    half, then taken back through R(pos)^T; against the oracle's full gradients."""
+    lens, H, d = [4096, 1024, 2560, 512, 64, 1000 - 1000 % (2 * cp)], 4, 64
+    w = synth.custom_workload(lens, H, d)
+    q, k, v, g = synth.make_tensors(w, seed=sum(lens) + 7 * cp, with_grad=True)
+    qd, kd, vd, gd = (t.to(DEV) for t in (q, k, v, g))
+    maxp = max(lens) - 1
+    loc = {}
+    for r in range(cp):
+        rows, pos, cu_chunk = vlc.cp_partition(w.cu, cp, r)
+        rd, pd = torch.from_numpy(rows).to(DEV), torch.from_numpy(pos).to(DEV)
+        loc[r] = dict(rows=rows, pos=pd, qr=vlc.rope_pos(qd[rd], pd, maxp), kr=vlc.rope_pos(kd[rd], pd, maxp),
+                      v=vd[rd].contiguous(), g=gd[rd].contiguous())
+    cuc = torch.from_numpy(cu_chunk).to(DEV)
+    mc = int(np.diff(cu_chunk).max())
+    half = len(loc[0]["rows"]) // 2
+    sl = lambda h: slice(h * half, (h + 1) * half)
+    blocks = {(r, qh): [(src, kh, vlc.cp_block_mode(cp, r, qh, src, kh)) for step in range(cp)
+                        for src in [(r - step) % cp] for kh in (0, 1)] for r in range(cp) for qh in (0, 1)}
+    blocks = {key: [b for b in val if b[2] != vlc.binding.CP_BLOCK_NONE] for key, val in blocks.items()}
+    # forward: merged O and LSE of every query half
+    om, lm = {}, {}
+    for (r, qh), bl in blocks.items():
+        parts = [vlc.varlen_attn_fwd(loc[r]["qr"][sl(qh)], loc[s]["kr"][sl(kh)], loc[s]["v"][sl(kh)], cuc, mc,
+                                     cu_seqlens_kv=cuc, max_seqlen_kv=mc, qk_rotated=True,
+                                     keys_all_visible=m == vlc.binding.CP_BLOCK_ALL) for s, kh, m in bl]
+        om[(r, qh)], lm[(r, qh)] = vlc.lse_merge([a for a, _ in parts], [b for _, b in parts])
+    # backward of every block; dq' collected per query half, dk', dv per key half
+    dq_p = {key: [] for key in blocks}
+    dk_p = {key: [] for key in blocks}
+    dv_p = {key: [] for key in blocks}
+    for (r, qh), bl in blocks.items():
+        for s, kh, m in bl:
+            gq, gk, gv = vlc.varlen_attn_bwd(loc[r]["g"][sl(qh)], loc[r]["qr"][sl(qh)], loc[s]["kr"][sl(kh)],
+                                             loc[s]["v"][sl(kh)], om[(r, qh)], lm[(r, qh)], cuc, mc, rope_theta=0.0,
+                                             cu_seqlens_kv=cuc, max_seqlen_kv=mc,
+                                             keys_all_visible=m == vlc.binding.CP_BLOCK_ALL)
+            dq_p[(r, qh)].append(gq)
+            dk_p[(s, kh)].append(gk)
+            dv_p[(s, kh)].append(gv)
+    dq = torch.zeros_like(qd)
+    dk = torch.zeros_like(kd)
+    dv = torch.zeros_like(vd)
+    for (r, h), parts in dq_p.items():
+        rows_d = torch.from_numpy(loc[r]["rows"][sl(h)]).to(DEV)
+        pos_h = loc[r]["pos"][sl(h)].contiguous()
+        dq[rows_d] = vlc.rope_pos(vlc.sum_parts(parts), pos_h, maxp, transpose=True)
+        dk[rows_d] = vlc.rope_pos(vlc.sum_parts(dk_p[(r, h)]), pos_h, maxp, transpose=True)
+        dv[rows_d] = vlc.sum_parts(dv_p[(r, h)])
+    ref = oracle.attn_bwd(g, q, k, v, w.cu)
+    for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        e = np.abs(a.float().cpu().numpy() - b)
+        assert np.isfinite(e).all() and e.max() <= 5e-2, (name, e.max())

@@ -26,6 +26,7 @@ from .binding import (  # noqa: F401
     set_wait_limit_us,
     shard_packs,
     shifted_cross_entropy,
+    sum_parts,
     varlen_attn_bwd,
     varlen_attn_fwd,
     workspace_bytes,

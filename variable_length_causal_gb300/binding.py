@@ -30,6 +30,7 @@ COST_KINDS = {"tokens": 0, "sumsq": 1}
 ROPE_INTERLEAVED = 0x1
 QK_ROTATED = 0x2
 KEYS_ALL_VISIBLE = 0x4
+ROPE_TRANSPOSE = 0x8
 DEVERR_POS = 0x80
 CP_BLOCK_NONE, CP_BLOCK_CAUSAL, CP_BLOCK_ALL = 0, 1, 2
 LSE_MERGE_MAX = 16
@@ -41,7 +42,7 @@ EXPORTED = [
     "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa", "vlc_attn_fwd_ex",
     "vlc_attn_bwd_ex", "vlc_workspace_bytes_qkv", "vlc_attn_fwd_qkv", "vlc_attn_bwd_qkv", "vlc_pack",
     "vlc_shard_packs", "vlc_rope_qk", "vlc_set_wait_limit_us", "vlc_cp_partition", "vlc_cp_block_mode",
-    "vlc_rope_pos_workspace_bytes", "vlc_rope_pos", "vlc_lse_merge",
+    "vlc_rope_pos_workspace_bytes", "vlc_rope_pos", "vlc_lse_merge", "vlc_sum_parts",
 ]
 
 _lock = threading.Lock()
@@ -86,6 +87,8 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_rope_pos.restype = cint
         lib.vlc_lse_merge.argtypes = [P, P, i32, i32, i32, i32, P, P, P]
         lib.vlc_lse_merge.restype = cint
+        lib.vlc_sum_parts.argtypes = [P, i32, i64, P, P]
+        lib.vlc_sum_parts.restype = cint
         lib.vlc_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, cint]
         lib.vlc_workspace_bytes.restype = sz
         lib.vlc_worklist_capacity.argtypes = [i32, i32, i32]
@@ -349,10 +352,12 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                     check: bool = True, rope_interleaved: bool = False,
                     cu_seqlens_padded: Optional[torch.Tensor] = None,
                     cu_seqlens_kv: Optional[torch.Tensor] = None, max_seqlen_kv: Optional[int] = None,
-                    qk_rotated: bool = False):
+                    qk_rotated: bool = False, keys_all_visible: bool = False):
     """Gradients (dQ, dK, dV) of sum(O * dO) for the forward above (dK, dV shaped like k, v;
     zero at padding rows).  qk_rotated: q and k are the rotated q', k' of ``rope_qk``; the
-    gradients returned are still with respect to the unrotated q and k."""
+    gradients returned are still with respect to the unrotated q and k.  keys_all_visible
+    (with cu_seqlens_kv and rope_theta=0): the backward of a block whose keys all precede its
+    queries, given the merged O and LSE of the whole attention (a context-parallel ring)."""
     lib = load_library()
     _require_cuda(dout, q, k, v, o, lse, cu_seqlens, cu_seqlens_padded, cu_seqlens_kv)
     qkv = cu_seqlens_kv is not None
@@ -376,7 +381,8 @@ def varlen_attn_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                            total_kv if qkv else None, max_seqlen_kv if qkv else None)
     else:
         ws = workspace
-    flags = (ROPE_INTERLEAVED if rope_interleaved else 0) | (QK_ROTATED if qk_rotated else 0)
+    flags = ((ROPE_INTERLEAVED if rope_interleaved else 0) | (QK_ROTATED if qk_rotated else 0)
+             | (KEYS_ALL_VISIBLE if keys_all_visible else 0))
     if qkv:
         st = lib.vlc_attn_bwd_qkv(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
                                   _ptr(cu_seqlens_kv), nseg, total, total_kv, H, H_kv, d, int(max_seqlen),
@@ -535,8 +541,9 @@ def cp_block_mode(cp: int, q_rank: int, q_half: int, kv_rank: int, kv_half: int)
 
 def rope_pos(x: torch.Tensor, pos: torch.Tensor, max_pos: int, rope_theta: float = 10000.0,
              rope_interleaved: bool = False, out: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None, check: bool = True) -> torch.Tensor:
-    """R(pos[i]) x[i] for every head of every row ([rows, H, d] bf16, pos int32 [rows])."""
+             workspace: Optional[torch.Tensor] = None, check: bool = True, transpose: bool = False) -> torch.Tensor:
+    """R(pos[i]) x[i] for every head of every row ([rows, H, d] bf16, pos int32 [rows]);
+    transpose applies R(pos[i])^T (gradients back through the rotation)."""
     lib = load_library()
     _require_cuda(x, pos)
     rows, H, d = x.shape
@@ -544,8 +551,8 @@ def rope_pos(x: torch.Tensor, pos: torch.Tensor, max_pos: int, rope_theta: float
     need = lib.vlc_rope_pos_workspace_bytes(int(max_pos), d)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device) if workspace is None else workspace
     st = lib.vlc_rope_pos(_ptr(x), _ptr(pos), rows, H, d, int(max_pos), float(rope_theta),
-                          ROPE_INTERLEAVED if rope_interleaved else 0, _ptr(out), _ptr(ws), ws.numel(),
-                          _stream(x.device))
+                          (ROPE_INTERLEAVED if rope_interleaved else 0) | (ROPE_TRANSPOSE if transpose else 0),
+                          _ptr(out), _ptr(ws), ws.numel(), _stream(x.device))
     _check(st, "vlc_rope_pos")
     if check:
         _raise_device_error(ws, "vlc_rope_pos")
@@ -572,3 +579,20 @@ def lse_merge(o_parts, lse_parts, out: Optional[torch.Tensor] = None, lse: Optio
     st = lib.vlc_lse_merge(optr, lptr, n, rows, H, d, _ptr(out), _ptr(lse), _stream(out.device))
     _check(st, "vlc_lse_merge")
     return out, lse
+
+
+def sum_parts(parts, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Sum of 1 to 16 bf16 tensors of one shape, accumulated in fp32 and rounded once."""
+    lib = load_library()
+    n = len(parts)
+    if not 1 <= n <= LSE_MERGE_MAX:
+        raise ValueError(f"1 to {LSE_MERGE_MAX} parts")
+    _require_cuda(*parts)
+    for t in parts:
+        if t.shape != parts[0].shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("parts must be contiguous bf16 tensors of one shape")
+    out = torch.empty_like(parts[0]) if out is None else out
+    ptrs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in parts])
+    st = lib.vlc_sum_parts(ptrs, n, parts[0].numel(), _ptr(out), _stream(out.device))
+    _check(st, "vlc_sum_parts")
+    return out

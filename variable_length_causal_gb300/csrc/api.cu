@@ -153,9 +153,10 @@ static int check_attn_args(const AttnArgs& a, int is_bwd) {
     if (is_bwd && (a.flags & VLC_QK_ROTATED) && a.cu_kv != nullptr) return VLC_ERR_ARG;
     if (a.flags & VLC_KEYS_ALL_VISIBLE) {
         // a block of keys that all precede the queries: separate key segments, and no
-        // in-kernel rotation (the positions are not implied by the lengths)
-        if (is_bwd) return VLC_ERR_UNSUPPORTED;
-        if (a.cu_kv == nullptr || !((a.flags & VLC_QK_ROTATED) || a.rope_theta == 0.f)) return VLC_ERR_ARG;
+        // in-kernel rotation (the positions are not implied by the lengths); the backward
+        // returns the gradients with respect to the operands as given (rope_theta == 0)
+        if (a.cu_kv == nullptr) return VLC_ERR_ARG;
+        if (is_bwd ? a.rope_theta != 0.f : !((a.flags & VLC_QK_ROTATED) || a.rope_theta == 0.f)) return VLC_ERR_ARG;
     }
     if (!(a.rope_theta >= 0.f) || !std::isfinite(a.rope_theta)) return VLC_ERR_ARG;
     if (a.d != 64 && a.d != 128) return VLC_ERR_UNSUPPORTED;
@@ -204,7 +205,7 @@ static int attn_fwd_impl(AttnArgs a) {
     {   // the work list and (with RoPE) the cos/sin table in one launch
         const WlSpec wl{a.cu, a.nseg, a.total, a.max_seqlen, kFwdQB, kFwdBN, VLC_WORKLIST_FWD, items,
                         L.item_cap, order, seg_base, &hdr->count, &hdr->err, a.cu_padded, a.cu_kv,
-                        a.total_kv, a.max_seqlen_kv};
+                        a.total_kv, a.max_seqlen_kv, (a.flags & VLC_KEYS_ALL_VISIBLE) ? 1 : 0};
         const TabSpec tab = rope_table_spec(table, L.table_rows, a.d, static_cast<double>(a.rope_theta));
         if (launch_meta(&wl, 1, mode != kRopeNone ? &tab : nullptr, s) != cudaSuccess) return VLC_ERR_CUDA;
     }
@@ -269,12 +270,13 @@ static int attn_bwd_impl(AttnArgs a) {
     const int mode = rope_mode(a.rope_theta, a.flags);
     float2* table2 = reinterpret_cast<float2*>(w + L.table2);
     {   // q-tile items (dQ pass), key-tile items (dK/dV pass) and the cos/sin tables in one launch
+        const int allv = (a.flags & VLC_KEYS_ALL_VISIBLE) ? 1 : 0;
         const WlSpec wl[2] = {
             {a.cu, a.nseg, a.total, a.max_seqlen, kFwdBM, kFwdBN, VLC_WORKLIST_FWD, items_q, L.item_cap, order,
-             seg_base_q, &hdr->count, &hdr->err, a.cu_padded, a.cu_kv, a.total_kv, a.max_seqlen_kv},
+             seg_base_q, &hdr->count, &hdr->err, a.cu_padded, a.cu_kv, a.total_kv, a.max_seqlen_kv, allv},
             {a.cu, a.nseg, a.total, a.max_seqlen, kBwdBM, kFwdBN, VLC_WORKLIST_BWD, items_k, L.item_cap,
              order + a.nseg, seg_base_k, &hdr->count2, &hdr->err, a.cu_padded, a.cu_kv, a.total_kv,
-             a.max_seqlen_kv}};
+             a.max_seqlen_kv, allv}};
         const TabSpec tab = rope_table_spec(table, L.table_rows, a.d, static_cast<double>(a.rope_theta), table2);
         if (launch_meta(wl, 2, mode != kRopeNone ? &tab : nullptr, s) != cudaSuccess) return VLC_ERR_CUDA;
     }
@@ -304,6 +306,7 @@ static int attn_bwd_impl(AttnArgs a) {
     p.use_rope = mode;
     p.operands_rotated = (a.flags & VLC_QK_ROTATED) ? 1 : 0;
     p.wait_limit_us = wait_limit_us();
+    p.keys_all_visible = (a.flags & VLC_KEYS_ALL_VISIBLE) ? 1 : 0;
     if (launch_attn_bwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
     return VLC_OK;
 }

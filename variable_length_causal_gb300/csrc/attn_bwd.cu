@@ -603,7 +603,9 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         // TMEM allocation): claims and decodes units ahead of the other roles
         {   // the whole warp: lane 0 claims and publishes, all lanes decode
             auto decode = [&](int u) {
-                return decode_unit_warp<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                Unit w = decode_unit_warp<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
+                if (KV && p.keys_all_visible) w.off = w.Lk;   // the diagonal past the last key: no mask
+                return w;
             };
             for (int n = 0;; ++n) {
                 int u;
@@ -1072,7 +1074,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         // TMEM allocation): claims and decodes units ahead of the other roles
         {   // the whole warp: lane 0 claims and publishes, all lanes decode
             auto decode = [&](int u) {
-                return decode_unit_warp<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+                Unit w = decode_unit_warp<KV>(p.items_k, p.seg_base_k, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.Hkv, u);
+                if (KV && p.keys_all_visible) w.off = w.Lk;   // the diagonal past the last key: no mask
+                return w;
             };
             for (int n = 0;; ++n) {
                 int u;
@@ -1286,7 +1290,7 @@ static cudaError_t launch_bwd_d(const BwdParams& p, int num_sms, cudaStream_t s)
         !make_tmap_thd(&k128, kop, p.total_kv, p.Hkv, D, 128) ||
         !make_tmap_thd(&v128, p.v, p.total_kv, p.Hkv, D, 128))
         return cudaErrorInvalidValue;
-    const bool kv = p.cu_kv != p.cu;
+    const bool kv = p.cu_kv != p.cu || p.keys_all_visible;   // the instance that reads the unit's offset
     {
         constexpr uint32_t smem = bwd::dq::Layout<D>::ALLOC;
         auto kernel = kv ? bwd::dq::dq_kernel<D, true> : bwd::dq::dq_kernel<D, false>;

@@ -1,8 +1,9 @@
 // cp_kernels.cu -- the device steps of the context-parallel split: RoPE by explicit
-// positions (a rank's rows keep the positions they had in the whole segment) and
-// the merge of partial attention results over disjoint key blocks.  Entry points
-// vlc_rope_pos, vlc_rope_pos_workspace_bytes and vlc_lse_merge (include/vlc.h);
-// the host partition is in cp.cpp.
+// positions (a rank's rows keep the positions they had in the whole segment; the
+// transposed rotation takes gradients back), the merge of partial attention results
+// over disjoint key blocks, and the sum of partial gradients.  Entry points
+// vlc_rope_pos, vlc_rope_pos_workspace_bytes, vlc_lse_merge and vlc_sum_parts
+// (include/vlc.h); the host partition is in cp.cpp.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -23,7 +24,7 @@ template <int D>
 __global__ void __launch_bounds__(256)
 rope_pos_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ pos, uint4* __restrict__ out,
                 int64_t rows, int32_t H, int32_t max_pos, const float2* __restrict__ table, int rope,
-                int32_t* err) {
+                bool transpose, int32_t* err) {
     constexpr int TPR = D / 16;
     constexpr int HALF = D / 16;
     const bool il = rope == kRopeInterleaved;
@@ -37,6 +38,10 @@ rope_pos_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ pos, ui
         if (!ok && c == 0) atomicOr(err, VLC_DEVERR_POS);
         float cs[8], sn[8];
         if (ok) load_angles<D>(table, p, il, c, cs, sn);
+        if (transpose) {   // R(p)^T = R(-p): the same cosines, negated sines
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sn[e] = -sn[e];
+        }
         for (int h = 0; h < H; ++h) {
             const int64_t lo = (row * H + h) * (2 * HALF) + c;
             rotate_chunks(x, out, lo, lo + HALF, cs, sn, ok, il);
@@ -99,6 +104,27 @@ lse_merge_kernel(const MergeParts parts, int64_t rows, int32_t H, uint4* __restr
     }
 }
 
+// out = sum of n bf16 arrays, accumulated in fp32 and rounded once (8 elements per thread).
+__global__ void __launch_bounds__(256)
+sum_parts_kernel(const MergeParts parts, int64_t n16, uint4* __restrict__ out) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int k = 0; k < parts.n; ++k) {
+            const uint4 v = __ldg(parts.o[k] + i);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[2 * e] += bf16_lo(wv[e]);
+                acc[2 * e + 1] += bf16_hi(wv[e]);
+            }
+        }
+        out[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                            pack_bf16x2(acc[6], acc[7]));
+    }
+}
+
 int grid_for(int64_t threads) {
     static int sms = 0;
     if (sms == 0) {
@@ -129,7 +155,7 @@ extern "C" int vlc_rope_pos(const void* x, const int32_t* pos, int32_t rows, int
                             float rope_theta, uint32_t flags, void* out, void* ws, size_t ws_bytes, void* stream) {
     using namespace vlc;
     if (x == nullptr || pos == nullptr || out == nullptr || rows < 1 || H < 1) return VLC_ERR_ARG;
-    if (flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED)) return VLC_ERR_ARG;
+    if (flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED | VLC_ROPE_TRANSPOSE)) return VLC_ERR_ARG;
     if (!(rope_theta > 0.f) || !std::isfinite(rope_theta)) return VLC_ERR_ARG;
     if (d != 64 && d != 128) return VLC_ERR_UNSUPPORTED;
     if (max_pos < 0 || max_pos >= VLC_MAX_SEQLEN) return VLC_ERR_UNSUPPORTED;
@@ -149,7 +175,24 @@ extern "C" int vlc_rope_pos(const void* x, const int32_t* pos, int32_t rows, int
     const int64_t threads = static_cast<int64_t>(rows) * (d / 16);
     auto kernel = d == 128 ? cp::rope_pos_kernel<128> : cp::rope_pos_kernel<64>;
     kernel<<<cp::grid_for(threads), 256, 0, s>>>(static_cast<const uint4*>(x), pos, static_cast<uint4*>(out), rows, H,
-                                                 max_pos, table, mode, err);
+                                                 max_pos, table, mode, (flags & VLC_ROPE_TRANSPOSE) != 0, err);
+    return cudaGetLastError() == cudaSuccess ? VLC_OK : VLC_ERR_CUDA;
+}
+
+extern "C" int vlc_sum_parts(const void* const* parts, int32_t nparts, int64_t elems, void* out, void* stream) {
+    using namespace vlc;
+    if (parts == nullptr || out == nullptr || nparts < 1 || nparts > VLC_LSE_MERGE_MAX || elems < 1 || elems % 8 != 0)
+        return VLC_ERR_ARG;
+    if (!cp::aligned(out, 16)) return VLC_ERR_ARG;
+    cp::MergeParts mp{};
+    mp.n = nparts;
+    for (int k = 0; k < nparts; ++k) {
+        if (parts[k] == nullptr || !cp::aligned(parts[k], 16)) return VLC_ERR_ARG;
+        mp.o[k] = static_cast<const uint4*>(parts[k]);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t n16 = elems / 8;
+    cp::sum_parts_kernel<<<cp::grid_for(n16), 256, 0, s>>>(mp, n16, static_cast<uint4*>(out));
     return cudaGetLastError() == cudaSuccess ? VLC_OK : VLC_ERR_CUDA;
 }
 

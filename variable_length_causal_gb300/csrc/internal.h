@@ -53,6 +53,7 @@ struct WlSpec {
     const int32_t* cu_padded;
     const int32_t* cu_kv;
     int32_t total_kv, max_seqlen_kv;
+    int all_visible;   // every key of a segment visible to every query (ranges as if the diagonal were past Lk)
 };
 struct TabSpec {
     float2* table;
@@ -174,6 +175,8 @@ struct BwdParams {
     int operands_rotated;      // 1: q and k already hold R(p) q, R(p) k; only the gradients are
                                // un-rotated (the prep pass computes D alone)
     uint32_t wait_limit_us;    // limit of one bounded wait in the kernels (kWaitLimitUs by default)
+    int keys_all_visible;      // 1: every key of a query's key segment is visible (no causal mask;
+                               // separate key segments, no RoPE)
 };
 
 // Limit of one bounded wait for the attention kernels launched from now on (the

@@ -208,7 +208,9 @@ __device__ __forceinline__ void worklist_body(const WlSpec& spec) {
         const int r = order[k];
         const int L = cu[r + 1] - cu[r];
         const int Lk = ck[r + 1] - ck[r];
-        const int off = Lk - L;   // queries are the last L of the Lk positions
+        // queries are the last L of the Lk positions; with every key visible the diagonal
+        // lies past the last key
+        const int off = spec.all_visible ? Lk : Lk - L;
         const int base = seg_base[k];
         const int n = seg_base[k + 1] - base;
         for (int j = 0; j < n; ++j) {
