@@ -23,6 +23,12 @@ no code with the CUDA path:
 * ``lse_merge``: results over disjoint key sets combined into the result over their
   union: with LSE_k = ln sum_{j in K_k} e^{s_j}, the union has LSE = ln sum_k e^{LSE_k}
   and O = sum_k e^{LSE_k - LSE} O_k (each O_k is a softmax-weighted mean over K_k).
+* ``block_attention_backward``: the standard softmax-attention derivatives restricted to
+  one block of keys, given the whole attention's LSE and D = rowsum(dO * O):
+  P = e^{S - LSE} on the block's visible entries, dV = P^T dO, dP = dO V^T,
+  dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q.  Every entry of the full
+  P, dS lies in exactly one block, so the blocks' dQ add up to the full dQ and each key
+  row's dK, dV come whole from the blocks that contain it.
 """
 from __future__ import annotations
 
@@ -87,3 +93,23 @@ def lse_merge(o_parts, lse_parts):
     wn = np.where(tot[None] > 0, w / np.where(tot > 0, tot, 1.0)[None], 0.0)  # [k, H, n]
     out_o = np.einsum("khn,knhd->nhd", wn, o)
     return out_o, out_lse
+
+
+def block_attention_backward(q, k, v, g, q_seg, q_pos, k_seg, k_pos, lse, delta, scale: float):
+    """q, g [n, H, d], k, v [m, H, d] (fp64, rotated), lse / delta [H, n] of the whole attention;
+    returns the block's (dq [n, H, d], dk [m, H, d], dv [m, H, d])."""
+    q, k, v, g = (np.asarray(x, np.float64) for x in (q, k, v, g))
+    n, H, d = q.shape
+    allow = (np.asarray(k_seg)[None, :] == np.asarray(q_seg)[:, None]) & \
+            (np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None])
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for h in range(H):
+        s = q[:, h, :] @ k[:, h, :].T * scale
+        fin = np.isfinite(lse[h])[:, None]
+        p = np.where(allow & fin, np.exp(np.where(allow, s, 0.0) - np.where(fin, lse[h][:, None], 0.0)), 0.0)
+        dp = g[:, h, :] @ v[:, h, :].T
+        ds = p * (dp - delta[h][:, None])
+        dv[:, h, :] = p.T @ g[:, h, :]
+        dq[:, h, :] = scale * ds @ k[:, h, :]
+        dk[:, h, :] = scale * ds.T @ q[:, h, :]
+    return dq, dk, dv

@@ -10,7 +10,9 @@ mathematics fix, independent of the oracle's own formulas:
 * block attention over all keys equals the already pinned oracle's segment-local causal
   forward (oracle.attn_fwd in exact mode) on the same rows, and merging it over any
   partition of the keys reproduces it; two identical partial results merge into the same O
-  with LSE + ln 2 (the union of two copies of a key set doubles the sum).
+  with LSE + ln 2 (the union of two copies of a key set doubles the sum);
+* the block backward over all keys equals the pinned oracle.attn_bwd (exact mode), and its
+  blocks over a partition of the keys add up to it.
 """
 import numpy as np
 import pytest
@@ -104,3 +106,31 @@ def test_merge_of_two_copies_adds_ln2():
     o_m, l_m = ocp.lse_merge([o, o], [lse, lse])
     assert np.abs(o_m - o).max() < 1e-12
     assert np.abs(l_m - (lse + np.log(2.0))).max() < 1e-12
+
+
+def test_block_backward_over_a_key_partition_adds_up_to_the_pinned_backward():
+    lengths = [24, 16, 40]
+    cp = 2
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T, H, d = int(cu[-1]), 2, 8
+    q, k, v, g = (_rand(T, H, d, 10 + i) for i in range(4))
+    seg = np.repeat(np.arange(len(lengths)), lengths)
+    pos = np.arange(T) - cu[seg]
+    scale = 1.0 / np.sqrt(d)
+    o, lse = ocp.block_attention(q, k, v, seg, pos, seg, pos, scale)
+    delta = np.einsum("nhd,nhd->hn", g, o)
+    ref = oracle.attn_bwd_f64(g, q, k, v, cu, theta=0.0)
+    whole = ocp.block_attention_backward(q, k, v, g, seg, pos, seg, pos, lse, delta, scale)
+    for a, b in zip(whole, ref):
+        assert np.abs(a - b).max() < 1e-10
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for rank in range(cp):
+        kr, kp, _ = ocp.partition(lengths, cp, rank)
+        bq, bk, bv = ocp.block_attention_backward(q, k[kr], v[kr], g, seg, pos, seg[kr], kp, lse, delta, scale)
+        dq += bq
+        dk[kr] += bk
+        dv[kr] += bv
+    for a, b in zip((dq, dk, dv), ref):
+        assert np.abs(a - b).max() < 1e-10
