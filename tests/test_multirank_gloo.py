@@ -101,12 +101,14 @@ def test_ranks_shard_packs_consistently_without_exchange():
 
 
 def _cp_worker(rank, world, port, out):
-    """One rank of a context-parallel ring over gloo: the product's host partition and block
-    rule decide what is held and computed; the oracle stands in for the device attention."""
+    """One rank of a context-parallel ring over gloo, forward and backward: the product's host
+    partition and block rule decide what is held and computed; the oracle stands in for the device
+    attention; the key halves' dk / dv are summed over the ranks with all_reduce."""
     os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
     import numpy as np
     import torch.distributed as dist
 
+    import oracle
     import variable_length_causal_gb300 as vlc
     from oracle import cp as ocp
 
@@ -148,7 +150,37 @@ def _cp_worker(rank, world, port, out):
                                          1.0 / np.sqrt(d))
     err_o = max(float(np.abs(outs[h][0] - o_full[h * half:(h + 1) * half]).max()) for h in (0, 1))
     err_l = max(float(np.abs(outs[h][1] - l_full[:, h * half:(h + 1) * half]).max()) for h in (0, 1))
-    out[rank] = (err_o, err_l, rows.tolist())
+
+    # backward: the same blocks with the merged O / LSE; dq stays with the queries, the
+    # dk / dv of a key half go back to the rank that holds it (summed over every rank)
+    dout = g.standard_normal((T, H, d))
+    scale = 1.0 / np.sqrt(d)
+    dq = np.zeros((len(rows), H, d))
+    dkv = torch.zeros((world, len(rows), 2 * H, d), dtype=torch.float64)   # per owner rank
+    for qh in (0, 1):
+        qs = slice(qh * half, (qh + 1) * half)
+        o_m, l_m = outs[qh]
+        delta = np.einsum("nhd,nhd->hn", dout[rows[qs]], o_m)
+        for step in range(world):
+            src = (rank - step) % world
+            kv = gathered[src].numpy()
+            k_rows, k_pos = metas[src][0].numpy(), metas[src][1].numpy()
+            for kh in (0, 1):
+                if vlc.cp_block_mode(world, rank, qh, src, kh) == vlc.binding.CP_BLOCK_NONE:
+                    continue
+                ks = slice(kh * half, (kh + 1) * half)
+                bq, bk, bv = ocp.block_attention_backward(q[rows[qs]], kv[ks, :H], kv[ks, H:], dout[rows[qs]],
+                                                          seg_all[rows[qs]], pos[qs], seg_all[k_rows[ks]],
+                                                          k_pos[ks], l_m, delta, scale)
+                dq[qs] += bq
+                dkv[src, ks, :H] += torch.from_numpy(bk)
+                dkv[src, ks, H:] += torch.from_numpy(bv)
+    dist.all_reduce(dkv)
+    dk_own, dv_own = dkv[rank, :, :H].numpy(), dkv[rank, :, H:].numpy()
+    dq_ref, dk_ref, dv_ref = oracle.attn_bwd_f64(dout, q, k, v, cu, theta=0.0)
+    err_g = max(float(np.abs(dq - dq_ref[rows]).max()), float(np.abs(dk_own - dk_ref[rows]).max()),
+                float(np.abs(dv_own - dv_ref[rows]).max()))
+    out[rank] = (err_o, err_l, rows.tolist(), err_g)
     dist.destroy_process_group()
 
 
@@ -160,4 +192,5 @@ def test_context_parallel_ring_over_two_gloo_ranks():
     mp.start_processes(_cp_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
     for r in range(world):
         assert out[r][0] < 1e-12 and out[r][1] < 1e-12
+        assert out[r][3] < 1e-10
     assert sorted(out[0][2] + out[1][2]) == list(range(160))
