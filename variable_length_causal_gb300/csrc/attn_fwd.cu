@@ -7,13 +7,13 @@
 // are q, k rotated by RoPE at the per-segment positions p = i - cu_r
 // (section "Positions are reset per segment").  LSE = ln sum exp(scores).
 //
-// Design: one persistent CTA per SM, 512 threads, warp-specialised.  A work
-// unit is (segment, head, block of 256 query rows) = two 128-row q tiles that
-// share every K/V tile; the work list holds only in-segment, at-or-below-
-// diagonal key tiles, and a q tile stops at its own diagonal key tile.  Units
-// are claimed dynamically (longest first) from a global counter by a scheduler
-// thread, which decodes each one and hands it to every role through a
-// shared-memory ring.
+// Design: one persistent CTA per SM, warp-specialised (640 threads; 512 in the
+// instance with RoPE warps).  A work unit is (segment, head, block of 256 query
+// rows) = two 128-row q tiles that share every K/V tile; the work list holds only
+// in-segment, at-or-below-diagonal key tiles, and a q tile stops at its own
+// diagonal key tile.  Units are claimed dynamically (longest first) from a global
+// counter by a scheduler warp, which decodes each one and hands it to every role
+// through a shared-memory ring.
 //   warp 0       TMA producer of q tiles (3-slot ring) and K tiles (2 stages),
 //                128-byte swizzle; warp 3 the same for V tiles (2 stages).
 //   warp 1       MMA issuer (one elected lane of the converged warp), tcgen05.mma
@@ -24,13 +24,17 @@
 //                other tile's MMAs.
 //   warp 2       TMEM allocator (512 columns: S/P 0, S/P 1, O 0, O 1), then the
 //                unit scheduler.
-//   warps 4-7    softmax + epilogue of q tile 0, one thread per query row:
-//   warps 8-11   the same for q tile 1.  Two passes over the S row in TMEM
-//                (row max, then exp2 and bf16 P written back over the consumed
-//                S columns); the causal / segment-tail mask only on a tile's
-//                last key tile; lazy O rescale when the row max grows by more
-//                than 2^8; epilogue O / l -> bf16 and LSE.
-//   warps 12-15  RoPE on the staged q and K tiles (segment-local positions).
+//   warps 4-11   softmax + epilogue of q tile 0; warps 12-19 the same for q tile 1.
+//                A query row (TMEM lane) belongs to two threads of one warp, 64 score
+//                columns each (the 16x32bx2 TMEM access shape), so a softmax step per
+//                thread is half a row: its maximum comes with the TMEM load (ld.red)
+//                and meets the other half's in one shuffle; exp2 and bf16 P written
+//                back over the consumed S columns; the causal / segment-tail mask only
+//                on a tile's last key tile; lazy O rescale when the row max grows by
+//                more than 2^8; epilogue O / l -> bf16 and LSE, half a row per thread.
+//   With RoPE in the kernel: warps 4-7 and 8-11 are the softmax of q tiles 0 and 1
+//                with one thread per row (128 scores each), and warps 12-15 rotate the
+//                staged q and K tiles (segment-local positions).
 // Every wait is bounded; on expiry the kernel sets VLC_DEVERR_TIMEOUT, drains
 // its own in-flight copies and MMAs, frees TMEM and returns.
 #include <type_traits>
@@ -50,26 +54,28 @@ constexpr int BQ = 128;                 // rows per q tile
 constexpr int QB = kFwdQB;              // rows per work unit (two q tiles)
 constexpr int BN = kFwdBN;              // rows per key tile
 static_assert(QB == 2 * BQ && BN == 128, "two 128-row q tiles per unit, 128-row key tiles");
-constexpr int kThreads = 512;
 constexpr int kQSlots = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr uint32_t kLaunchRegs = 65536 / kThreads;   // registers per thread at launch
-#ifndef VLC_FWD_CTRL_REGS
-#define VLC_FWD_CTRL_REGS 72
-#define VLC_FWD_ROPE_REGS 88
-#endif
-// per-thread registers of each warpgroup after the split: producer/MMA/TMEM,
-// RoPE, and the two softmax warpgroups
-constexpr uint32_t kCtrlRegs = VLC_FWD_CTRL_REGS, kRopeRegs = VLC_FWD_ROPE_REGS;
-constexpr uint32_t kSoftmaxRegs = (4 * kLaunchRegs - kCtrlRegs - kRopeRegs) / 2 / 8 * 8;
-static_assert(kCtrlRegs % 8 == 0 && kRopeRegs % 8 == 0, "register counts are multiples of 8");
-static_assert(kCtrlRegs + kRopeRegs + 2 * kSoftmaxRegs <= 4 * kLaunchRegs, "register split exceeds the pool");
-// Without RoPE in the kernel (no RoPE, or operands rotated beforehand) the RoPE warpgroup
-// idles at the minimum and the softmax warpgroups take its registers.
-constexpr uint32_t kIdleRegs = 24;
-constexpr uint32_t kSoftmaxRegsNR = (4 * kLaunchRegs - kCtrlRegs - kIdleRegs) / 2 / 8 * 8;
-static_assert(kCtrlRegs + kIdleRegs + 2 * kSoftmaxRegsNR <= 4 * kLaunchRegs, "register split exceeds the pool");
+// Threads: a control warpgroup (producers, MMA issuer, scheduler) and the softmax
+// warpgroups; the warpgroups re-split the launch's register pool with setmaxnreg.
+//   without RoPE warps: four softmax warpgroups, two per q tile (the two threads of a
+//     query row sit in one warp and take 64 score columns each);
+//   with RoPE warps: two softmax warpgroups, one thread per query row holding its
+//     128 scores, and a RoPE warpgroup (no register room for the split rows).
+template <bool ROPE>
+struct Cfg {
+    static constexpr int kSoftWarps = ROPE ? 8 : 16;
+    static constexpr int kThreads = 32 * (4 + kSoftWarps + (ROPE ? 4 : 0));   // 512 or 640
+    static constexpr uint32_t kLaunchRegs = 65536u / kThreads / 8u * 8u;      // registers per thread at launch
+    static constexpr uint32_t kCtrlRegs = ROPE ? 72u : 56u;
+    static constexpr uint32_t kRopeRegs = ROPE ? 88u : 0u;
+    static constexpr uint32_t kSoftRegs =
+        (kThreads * kLaunchRegs - 128u * kCtrlRegs - 128u * kRopeRegs) / (32u * kSoftWarps) / 8u * 8u;
+    static_assert(128u * kCtrlRegs + 128u * kRopeRegs + 32u * kSoftWarps * kSoftRegs <= kThreads * kLaunchRegs,
+                  "register split exceeds the pool");
+    static constexpr uint32_t kTileThreads = 32u * kSoftWarps / 2;   // softmax threads of one q tile
+};
 constexpr float kLn2 = 0.69314718055994530942f;
 
 enum : int {
@@ -136,13 +142,12 @@ __device__ __forceinline__ FUnit make_funit(const FwdParams& p, const Unit& w) {
 
 // KV: keys and values have segments of their own (bottom-right aligned queries).
 template <int D, bool KV, bool ROPE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<ROPE>::kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmKr,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using LY = Layout<D>;
-    constexpr uint32_t kSoft = ROPE ? kSoftmaxRegs : kSoftmaxRegsNR;
-    constexpr uint32_t kFourth = ROPE ? kRopeRegs : kIdleRegs;   // the RoPE warpgroup
+    using CF = Cfg<ROPE>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -152,8 +157,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const Ring rg{reinterpret_cast<volatile int*>(sgen + LY::RING), bar(UNIT_FULL), bar(UNIT_EMPTY)};
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr int kRingConsumers = 1 + 1 + 1 + 8 + 4;   // Q/K and V producers, MMA warp, 8 softmax warps, 4 RoPE warps
-                                                    // (the RoPE warps only when there is RoPE)
+    // Q/K and V producers, MMA warp, the softmax warps, and the 4 RoPE warps when they rotate
+    constexpr int kRingConsumers = 1 + 1 + 1 + CF::kSoftWarps + 4;
 
     __shared__ int s_skip, s_nunits;
     if (threadIdx.x == 0) {   // one read, so every thread takes the same branch
@@ -177,9 +182,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bar(V_FULL + i), 1);
             mbar_init(bar(V_EMPTY + i), 1);
             mbar_init(bar(S_FULL + i), 1);
-            mbar_init(bar(P_FULL + i), 128);
+            mbar_init(bar(P_FULL + i), CF::kTileThreads);   // the softmax threads of q tile i
             mbar_init(bar(O_FULL + i), 1);
-            mbar_init(bar(O_EMPTY + i), 128);
+            mbar_init(bar(O_EMPTY + i), CF::kTileThreads);
         }
         mbar_init(bar(DRAIN), 1);
         for (int i = 0; i < kRing; ++i) {
@@ -209,7 +214,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     // RoPE warpgroups give registers up for them (each role sets its budget first).
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        setmaxnreg_dec<kCtrlRegs>();
+        setmaxnreg_dec<CF::kCtrlRegs>();
         if (lane == 0) {
             const uint64_t pol_stream = make_l2_policy_evict_first();   // q: read once
             const uint64_t pol_keep = make_l2_policy_evict_last();      // K/V: read by many units
@@ -252,7 +257,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs this loop (so descriptors and addresses stay warp-uniform);
         // one elected lane issues every MMA and commit.
-        setmaxnreg_dec<kCtrlRegs>();
+        setmaxnreg_dec<CF::kCtrlRegs>();
         {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false);
             constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
@@ -345,143 +350,285 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_wait_limit(bar(DRAIN), 0, 200000000ull);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 12) {
-        // ------------------------------------------------------------ softmax + epilogue
-        setmaxnreg_inc<kSoft>();
-        const int t = (warp - 4) >> 2;             // q tile slot handled by this warpgroup
-        const int wq = warp & 3;                   // TMEM lane quadrant
-        const int r = wq * 32 + lane;              // query row in the tile = TMEM lane
-        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t sadr = tmem + lane_off + LY::S_COL(t);
-        const uint32_t oadr = tmem + lane_off + LY::O_COL(t);
-        const float sl2 = p.scale_log2;
-        const bool v8 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;   // 256-bit row stores
-        uint32_t cnt_s = 0, cnt_u = 0;
-        bool ok = true;
-        for (int un = 0; ok; ++un) {
-            int u;
-            Unit uw;
-            if (!(ok = ring_get_warp(rg, un, abort, u, uw)) || u < 0) break;
-            const FUnit f = make_funit<KV>(p, uw);
-            const int nt = t == 0 ? f.n0 : f.n1;
-            if (nt == 0) continue;
-            const int qpos = (f.q0 + t) * BQ + r;
-            float m_run = 0.f, l_run = 0.f;
-            for (int j = 0; j < nt; ++j) {
-                if (!(ok = wait_warp(bar(S_FULL + t), cnt_s & 1, abort))) break;
-                ++cnt_s;
-                tc_fence_after();
-                // allowed key columns of this tile: c <= lim.  Only the last tile is masked,
-                // or the last two when the diagonal is not tile-aligned (off % BN != 0)
-                const bool edge = (j == nt - 1) || (KV && j == nt - 2 && (f.w.off & (BN - 1)) != 0);
-                const int lim = edge ? min(qpos + f.w.off, f.w.Lk - 1) - j * BN : BN - 1;
-                // the thread's whole S row (BN fp32 columns) in registers: four loads, one wait
-                uint32_t s[BN];
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-                    tmem_ld32(sadr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(s + c * 32));
-                tmem_wait_ld();
-                if (edge) {   // masked scores -> -inf: they drop out of the max and exp2 gives 0
-#pragma unroll
-                    for (int e = 0; e < BN; ++e)
-                        if (e > lim) s[e] = 0xff800000u;
-                }
-                // row max of the raw scores: four independent 3-input max chains
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int e = 0; e < BN; e += 8) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        m4[q] = fmax3(m4[q], __uint_as_float(s[e + 2 * q]), __uint_as_float(s[e + 2 * q + 1]));
-                }
-                const float mt = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * sl2;
-                float m_use = m_run, alpha = 1.f;
-                bool rescale = false;
-                if (j == 0) {
-                    m_use = mt;
-                } else {
-                    rescale = __any_sync(0xffffffffu, mt > m_run + kRescaleThreshold);
-                    if (rescale) {
-                        m_use = fmaxf(m_run, mt);
-                        alpha = ex2_approx(m_run - m_use);
+    } else if (warp >= 4 && warp < 4 + CF::kSoftWarps) {
+        if constexpr (ROPE) {
+            // ------------------------------------------------------------ softmax + epilogue, one
+            // thread per query row (warps 4-7: q tile 0, 8-11: q tile 1; the RoPE warpgroup's
+            // registers leave no room for the split rows below)
+            setmaxnreg_inc<CF::kSoftRegs>();
+            const int t = (warp - 4) >> 2;             // q tile slot handled by this warpgroup
+            const int wq = warp & 3;                   // TMEM lane quadrant
+            const int r = wq * 32 + lane;              // query row in the tile = TMEM lane
+            const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+            const uint32_t sadr = tmem + lane_off + LY::S_COL(t);
+            const uint32_t oadr = tmem + lane_off + LY::O_COL(t);
+            const float sl2 = p.scale_log2;
+            const bool v8 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;   // 256-bit row stores
+            uint32_t cnt_s = 0, cnt_u = 0;
+            bool ok = true;
+            for (int un = 0; ok; ++un) {
+                int u;
+                Unit uw;
+                if (!(ok = ring_get_warp(rg, un, abort, u, uw)) || u < 0) break;
+                const FUnit f = make_funit<KV>(p, uw);
+                const int nt = t == 0 ? f.n0 : f.n1;
+                if (nt == 0) continue;
+                const int qpos = (f.q0 + t) * BQ + r;
+                float m_run = 0.f, l_run = 0.f;
+                for (int j = 0; j < nt; ++j) {
+                    if (!(ok = wait_warp(bar(S_FULL + t), cnt_s & 1, abort))) break;
+                    ++cnt_s;
+                    tc_fence_after();
+                    // allowed key columns of this tile: c <= lim.  Only the last tile is masked,
+                    // or the last two when the diagonal is not tile-aligned (off % BN != 0)
+                    const bool edge = (j == nt - 1) || (KV && j == nt - 2 && (f.w.off & (BN - 1)) != 0);
+                    const int lim = edge ? min(qpos + f.w.off, f.w.Lk - 1) - j * BN : BN - 1;
+                    // the thread's whole S row (BN fp32 columns) in registers: four loads, one wait
+                    uint32_t s[BN];
+    #pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+                        tmem_ld32(sadr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(s + c * 32));
+                    tmem_wait_ld();
+                    if (edge) {   // masked scores -> -inf: they drop out of the max and exp2 gives 0
+    #pragma unroll
+                        for (int e = 0; e < BN; ++e)
+                            if (e > lim) s[e] = 0xff800000u;
                     }
-                }
-                // P = exp2(s * scale_log2 - m) -> bf16 pairs written over the first BN/2
-                // S columns, each half as soon as it is packed
-                const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
-                float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-                for (int hlf = 0; hlf < 2; ++hlf) {
-                    uint32_t pk[BN / 4];
-#pragma unroll
-                    for (int e = 0; e < BN / 4; ++e) {
-                        const int c = hlf * (BN / 2) + 2 * e;
-                        const float2 x = fma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
-                        const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-                        rs2[e & 1] = add2(rs2[e & 1], make_float2(p0, p1));
-                        pk[e] = pack_bf16x2(p0, p1);
+                    // row max of the raw scores: four independent 3-input max chains
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    #pragma unroll
+                    for (int e = 0; e < BN; e += 8) {
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            m4[q] = fmax3(m4[q], __uint_as_float(s[e + 2 * q]), __uint_as_float(s[e + 2 * q + 1]));
                     }
-                    tmem_st32(sadr + hlf * (BN / 4), pk);
-                }
-                if (rescale) {   // O_t is stable: S_t(j) done implies P_t V(j-1) done
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t rr[32];
-                        tmem_ld32(oadr + c * 32, rr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-                        tmem_st32(oadr + c * 32, rr);
+                    const float mt = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * sl2;
+                    float m_use = m_run, alpha = 1.f;
+                    bool rescale = false;
+                    if (j == 0) {
+                        m_use = mt;
+                    } else {
+                        rescale = __any_sync(0xffffffffu, mt > m_run + kRescaleThreshold);
+                        if (rescale) {
+                            m_use = fmaxf(m_run, mt);
+                            alpha = ex2_approx(m_run - m_use);
+                        }
                     }
-                    l_run *= alpha;
-                }
-                tmem_wait_st();
-                l_run += (rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y);
-                m_run = m_use;
-                tc_fence_before();
-                mbar_arrive(bar(P_FULL + t));
-            }
-            if (!ok) break;
-            // ---- epilogue: O / l -> bf16, LSE
-            if (!(ok = wait_warp(bar(O_FULL + t), cnt_u & 1, abort))) break;
-            tc_fence_after();
-            const bool valid = qpos < f.w.L;
-            const int64_t tok = static_cast<int64_t>(f.w.row0) + qpos;
-            const float inv_l = 1.f / l_run;
-            uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                            ((valid ? tok : 0) * p.H + f.w.h) * static_cast<int64_t>(D) * 2;
-            // read O (two 32-column chunks at a time); the columns are released to the
-            // next unit as soon as the last chunk has landed, before packing and storing
-#pragma unroll
-            for (int c = 0; c < D / 32; c += 2) {
-                uint32_t ra[32], rb[32];
-                tmem_ld32(oadr + c * 32, ra);
-                tmem_ld32(oadr + c * 32 + 32, rb);
-                tmem_wait_ld();
-                if (c + 2 >= D / 32) {
+                    // P = exp2(s * scale_log2 - m) -> bf16 pairs written over the first BN/2
+                    // S columns, each half as soon as it is packed
+                    const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
+                    float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    #pragma unroll
+                    for (int hlf = 0; hlf < 2; ++hlf) {
+                        uint32_t pk[BN / 4];
+    #pragma unroll
+                        for (int e = 0; e < BN / 4; ++e) {
+                            const int c = hlf * (BN / 2) + 2 * e;
+                            const float2 x = fma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2);
+                            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                            rs2[e & 1] = add2(rs2[e & 1], make_float2(p0, p1));
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st32(sadr + hlf * (BN / 4), pk);
+                    }
+                    if (rescale) {   // O_t is stable: S_t(j) done implies P_t V(j-1) done
+    #pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t rr[32];
+                            tmem_ld32(oadr + c * 32, rr);
+                            tmem_wait_ld();
+    #pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                            tmem_st32(oadr + c * 32, rr);
+                        }
+                        l_run *= alpha;
+                    }
+                    tmem_wait_st();
+                    l_run += (rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y);
+                    m_run = m_use;
                     tc_fence_before();
-                    mbar_arrive(bar(O_EMPTY + t));
+                    mbar_arrive(bar(P_FULL + t));
                 }
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    pk[e] = pack_bf16x2(__uint_as_float(ra[2 * e]) * inv_l, __uint_as_float(ra[2 * e + 1]) * inv_l);
-                    pk[16 + e] = pack_bf16x2(__uint_as_float(rb[2 * e]) * inv_l, __uint_as_float(rb[2 * e + 1]) * inv_l);
+                if (!ok) break;
+                // ---- epilogue: O / l -> bf16, LSE
+                if (!(ok = wait_warp(bar(O_FULL + t), cnt_u & 1, abort))) break;
+                tc_fence_after();
+                const bool valid = qpos < f.w.L;
+                const int64_t tok = static_cast<int64_t>(f.w.row0) + qpos;
+                const float inv_l = 1.f / l_run;
+                uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                                ((valid ? tok : 0) * p.H + f.w.h) * static_cast<int64_t>(D) * 2;
+                // read O (two 32-column chunks at a time); the columns are released to the
+                // next unit as soon as the last chunk has landed, before packing and storing
+    #pragma unroll
+                for (int c = 0; c < D / 32; c += 2) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32(oadr + c * 32, ra);
+                    tmem_ld32(oadr + c * 32 + 32, rb);
+                    tmem_wait_ld();
+                    if (c + 2 >= D / 32) {
+                        tc_fence_before();
+                        mbar_arrive(bar(O_EMPTY + t));
+                    }
+                    uint32_t pk[32];
+    #pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        pk[e] = pack_bf16x2(__uint_as_float(ra[2 * e]) * inv_l, __uint_as_float(ra[2 * e + 1]) * inv_l);
+                        pk[16 + e] = pack_bf16x2(__uint_as_float(rb[2 * e]) * inv_l, __uint_as_float(rb[2 * e + 1]) * inv_l);
+                    }
+                    if (valid) {
+                        st_row64(orow + c * 64, pk, v8);
+                        st_row64(orow + c * 64 + 64, pk + 16, v8);
+                    }
                 }
-                if (valid) {
-                    st_row64(orow + c * 64, pk, v8);
-                    st_row64(orow + c * 64 + 64, pk + 16, v8);
-                }
+                if (valid)
+                    p.lse[static_cast<int64_t>(f.w.h) * p.total + tok] = (m_run + __log2f(l_run)) * kLn2;
+                ++cnt_u;
             }
-            if (valid)
-                p.lse[static_cast<int64_t>(f.w.h) * p.total + tok] = (m_run + __log2f(l_run)) * kLn2;
-            ++cnt_u;
+        } else {
+            // ------------------------------------------------------------ softmax + epilogue
+            // Two warpgroups per q tile.  A warp covers 16 query rows (TMEM lanes) of its
+            // quadrant; thread i < 16 takes score columns 0-63 of row i, thread i + 16 columns
+            // 64-127 of the same row (the 16x32bx2 access shape), so a row's maximum and sum
+            // meet in one shuffle.
+            setmaxnreg_inc<CF::kSoftRegs>();
+            const int t = (warp - 4) >> 3;             // q tile slot handled by this warp
+            const int wq = warp & 3;                   // TMEM lane quadrant (warp % 4)
+            const int sub = ((warp - 4) >> 2) & 1;     // which 16 lanes of the quadrant
+            const int hf = lane >> 4;                  // which half of the row's columns
+            const int r = wq * 32 + sub * 16 + (lane & 15);   // query row in the tile = TMEM lane
+            const uint32_t lane_off = static_cast<uint32_t>(wq * 32 + sub * 16) << 16;
+            const uint32_t sadr = tmem + lane_off + LY::S_COL(t);
+            const uint32_t oadr = tmem + lane_off + LY::O_COL(t);
+            constexpr int HC = BN / 2;                 // score columns per thread
+            constexpr int HD = D / 2;                  // output columns per thread
+            const float sl2 = p.scale_log2;
+            const bool v8 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;   // 256-bit row stores
+            uint32_t cnt_s = 0, cnt_u = 0;
+            bool ok = true;
+            for (int un = 0; ok; ++un) {
+                int u;
+                Unit uw;
+                if (!(ok = ring_get_warp(rg, un, abort, u, uw)) || u < 0) break;
+                const FUnit f = make_funit<KV>(p, uw);
+                const int nt = t == 0 ? f.n0 : f.n1;
+                if (nt == 0) continue;
+                const int qpos = (f.q0 + t) * BQ + r;
+                float m_run = 0.f, l_run = 0.f;   // l_run: this thread's half of the row sum
+                for (int j = 0; j < nt; ++j) {
+                    if (!(ok = wait_warp(bar(S_FULL + t), cnt_s & 1, abort))) break;
+                    ++cnt_s;
+                    tc_fence_after();
+                    // allowed key columns of this tile: c <= lim.  Only the last tile is masked,
+                    // or the last two when the diagonal is not tile-aligned (off % BN != 0)
+                    const bool edge = (j == nt - 1) || (KV && j == nt - 2 && (f.w.off & (BN - 1)) != 0);
+                    const int lim = (edge ? min(qpos + f.w.off, f.w.Lk - 1) - j * BN : BN - 1) - hf * HC;
+                    // the thread's 64 scores in registers (two loads, one wait); the loads also
+                    // return their maxima
+                    uint32_t s[HC];
+                    float mx0, mx1;
+                    tmem_ld32_pair_max<HC>(sadr, *reinterpret_cast<uint32_t(*)[32]>(s), mx0);
+                    tmem_ld32_pair_max<HC>(sadr + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32), mx1);
+                    tmem_wait_ld();
+                    float mloc = fmaxf(mx0, mx1);
+                    if (edge) {   // masked scores -> -inf: they drop out of the max and exp2 gives 0
+    #pragma unroll
+                        for (int e = 0; e < HC; ++e)
+                            if (e > lim) s[e] = 0xff800000u;
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    #pragma unroll
+                        for (int e = 0; e < HC; e += 8) {
+    #pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                m4[q] = fmax3(m4[q], __uint_as_float(s[e + 2 * q]), __uint_as_float(s[e + 2 * q + 1]));
+                        }
+                        mloc = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+                    }
+                    const float mt = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16)) * sl2;
+                    float m_use = m_run, alpha = 1.f;
+                    bool rescale = false;
+                    if (j == 0) {
+                        m_use = mt;
+                    } else {
+                        rescale = __any_sync(0xffffffffu, mt > m_run + kRescaleThreshold);
+                        if (rescale) {
+                            m_use = fmaxf(m_run, mt);
+                            alpha = ex2_approx(m_run - m_use);
+                        }
+                    }
+                    // P = exp2(s * scale_log2 - m) -> 32 bf16 pairs written over the row's
+                    // consumed S columns (thread i < 16: columns 0-31, i + 16: columns 32-63)
+                    const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
+                    float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    {
+                        uint32_t pk[HC / 2];
+    #pragma unroll
+                        for (int e = 0; e < HC / 2; ++e) {
+                            const float2 x = fma2(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nm2);
+                            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                            rs2[e & 1] = add2(rs2[e & 1], make_float2(p0, p1));
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st32_pair<HC / 2>(sadr, pk);
+                    }
+                    if (rescale) {   // O_t is stable: S_t(j) done implies P_t V(j-1) done
+    #pragma unroll 1
+                        for (int c = 0; c < HD / 32; ++c) {
+                            uint32_t rr[32];
+                            tmem_ld32_pair<HD>(oadr + c * 32, rr);
+                            tmem_wait_ld();
+    #pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                            tmem_st32_pair<HD>(oadr + c * 32, rr);
+                        }
+                        l_run *= alpha;
+                    }
+                    tmem_wait_st();
+                    l_run += (rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y);
+                    m_run = m_use;
+                    tc_fence_before();
+                    mbar_arrive(bar(P_FULL + t));
+                }
+                if (!ok) break;
+                // ---- epilogue: O / l -> bf16, LSE
+                if (!(ok = wait_warp(bar(O_FULL + t), cnt_u & 1, abort))) break;
+                tc_fence_after();
+                const bool valid = qpos < f.w.L;
+                const int64_t tok = static_cast<int64_t>(f.w.row0) + qpos;
+                const float l_row = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
+                const float inv_l = 1.f / l_row;
+                uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                                ((valid ? tok : 0) * p.H + f.w.h) * static_cast<int64_t>(D) * 2 + hf * HD * 2;
+                // the thread's half of the O row (columns hf * D/2 ...), all chunks then one wait;
+                // the columns go back to the next unit before packing and storing
+                uint32_t ro[HD];
+    #pragma unroll
+                for (int c = 0; c < HD / 32; ++c)
+                    tmem_ld32_pair<HD>(oadr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(ro + c * 32));
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(O_EMPTY + t));
+    #pragma unroll
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t pk[16];
+    #pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(ro[c * 32 + 2 * e]) * inv_l,
+                                            __uint_as_float(ro[c * 32 + 2 * e + 1]) * inv_l);
+                    if (valid) st_row64(orow + c * 64, pk, v8);
+                }
+                if (valid && hf == 0)
+                    p.lse[static_cast<int64_t>(f.w.h) * p.total + tok] = (m_run + __log2f(l_row)) * kLn2;
+                ++cnt_u;
+            }
         }
-    } else if (warp >= 12) {
+    } else if (warp >= 4 + CF::kSoftWarps) {
         // ------------------------------------------------------------ RoPE on staged q / K tiles
-        setmaxnreg_dec<kFourth>();
-        const int wr = warp - 12;
+        // (only in the instance with RoPE)
+        if constexpr (ROPE) setmaxnreg_dec<CF::kRopeRegs>();
+        const int wr = warp - 4 - CF::kSoftWarps;
         // one copy of the loop per pairing, so neither carries the other's state
         auto run = [&](auto il_tag) {
             constexpr bool IL = decltype(il_tag)::value;
@@ -521,7 +668,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }   // without RoPE these warps take no units
     } else if (warp == 3) {
         // ------------------------------------------------------------ TMA producer of V tiles
-        setmaxnreg_dec<kCtrlRegs>();
+        setmaxnreg_dec<CF::kCtrlRegs>();
         if (lane == 0) {
             const uint64_t pol_keep = make_l2_policy_evict_last();
             uint32_t vn = 0;
@@ -549,7 +696,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else {
         // ------------------------------------------------------------ warp 2: TMEM allocator, then
         // the unit scheduler (claims and decodes units ahead of the other roles)
-        setmaxnreg_dec<kCtrlRegs>();
+        setmaxnreg_dec<CF::kCtrlRegs>();
         {   // the whole warp: lane 0 claims and publishes, all lanes decode
             auto decode = [&](int u) {
                 Unit w = decode_unit_warp<KV>(p.items, p.seg_base, p.cu, p.rows, p.cu_kv, p.rows_kv, p.nseg, p.H, u);
@@ -607,23 +754,25 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
         !make_tmap_thd(&tkr, p.krot != nullptr ? p.krot : p.k, p.total_kv, p.Hkv, p.d, 128) ||
         !make_tmap_thd(&tv, p.v, p.total_kv, p.Hkv, p.d, 128))
         return cudaErrorInvalidValue;
-    const dim3 grid(num_sms), block(fwd::kThreads);
     const bool kv = p.cu_kv != p.cu || p.keys_all_visible;
-    // one instance with RoPE warps, one whose softmax warps take their registers
+    // one instance with RoPE warps, one without them
     const bool rope = p.use_rope != kRopeNone;
     auto kernel = p.d == 128
                       ? (kv ? (rope ? fwd::attn_fwd_kernel<128, true, true> : fwd::attn_fwd_kernel<128, true, false>)
                             : (rope ? fwd::attn_fwd_kernel<128, false, true> : fwd::attn_fwd_kernel<128, false, false>))
                       : (kv ? (rope ? fwd::attn_fwd_kernel<64, true, true> : fwd::attn_fwd_kernel<64, true, false>)
                             : (rope ? fwd::attn_fwd_kernel<64, false, true> : fwd::attn_fwd_kernel<64, false, false>));
+    const int threads = rope ? fwd::Cfg<true>::kThreads : fwd::Cfg<false>::kThreads;
+    const uint32_t regs = rope ? fwd::Cfg<true>::kLaunchRegs : fwd::Cfg<false>::kLaunchRegs;
+    const dim3 grid(num_sms), block(threads);
     const uint32_t smem = p.d == 128 ? fwd::Layout<128>::ALLOC : fwd::Layout<64>::ALLOC;
     // The warpgroups re-split the block's register pool at run time, which is only
-    // valid if every thread is launched with exactly kLaunchRegs registers.
+    // valid if every thread is launched with exactly the planned registers.
     {
         cudaFuncAttributes fa{};
         cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
         if (e != cudaSuccess) return e;
-        if (fa.numRegs != static_cast<int>(fwd::kLaunchRegs)) return cudaErrorInvalidConfiguration;
+        if (fa.numRegs != static_cast<int>(regs)) return cudaErrorInvalidConfiguration;
     }
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
