@@ -511,11 +511,15 @@ def context_parallel_measurement(vlc, dev, peaks, L: int = 131072, cp: int = 4, 
     holding chunks i and 2cp-1-i), the ranks' work run one after another on this GPU: every
     rank rotates its rows by their positions in the document, computes its blocks of the ring
     (the chunk's own causal block, and every earlier chunk with all keys visible) and merges
-    the partial results.  No communication is timed (one GPU).  Compared with the whole
-    document's causal forward on this GPU: balance = max rank time / mean rank time, and
-    split overhead = cp * mean rank time / whole-document time."""
+    the partial results.  The backward of a rank: every block's backward with the merged O and
+    LSE of its query half, its dq parts summed and taken back through R(pos)^T, and the dk / dv
+    parts of its own key halves summed (as many as the ring's blocks deliver; on one GPU the
+    parts summed are stand-ins of the right shape and count, the arithmetic is the same) and dk
+    taken back through R(pos)^T.  No communication is timed (one GPU).  Compared with the whole
+    document's causal forward / backward on this GPU: balance = max rank time / mean rank time,
+    and split overhead = cp * mean rank time / whole-document time."""
     w = synth.custom_workload([L], H, d)
-    q, k, v = synth.make_tensors(w, device=dev, seed=4321)
+    q, k, v, g = synth.make_tensors(w, device=dev, seed=4321, with_grad=True)
     cu = torch.from_numpy(w.cu).to(dev)
     qr, kr = vlc.rope_qk(q, k, cu, L)
     o1 = torch.empty_like(q)
@@ -523,24 +527,36 @@ def context_parallel_measurement(vlc, dev, peaks, L: int = 131072, cp: int = 4, 
     ws1 = vlc.new_workspace(1, L, H, d, L, False, dev)
     full_ms, _ = _time_events(lambda: vlc.varlen_attn_fwd(qr, kr, v, cu, L, out=o1, lse=l1, workspace=ws1,
                                                           check=False, qk_rotated=True), reps)
-    del o1, l1, ws1
+    wsb1 = vlc.new_workspace(1, L, H, d, L, True, dev)
+    gq1, gk1, gv1 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    full_bwd_ms, _ = _time_events(lambda: vlc.varlen_attn_bwd(g, qr, kr, v, o1, l1, cu, L, dq=gq1, dk=gk1, dv=gv1,
+                                                              workspace=wsb1, check=False, qk_rotated=True), reps)
+    del o1, l1, ws1, wsb1, gq1, gk1, gv1
     locs = {}
     for r in range(cp):
         rows, pos, cu_chunk = vlc.cp_partition(w.cu, cp, r)
         rows_d = torch.from_numpy(rows).to(dev)
         locs[r] = (rows_d, torch.from_numpy(pos).to(dev), torch.from_numpy(cu_chunk).to(dev), q[rows_d].contiguous(),
-                   k[rows_d].contiguous(), v[rows_d].contiguous())
+                   k[rows_d].contiguous(), v[rows_d].contiguous(), g[rows_d].contiguous())
     half = L // cp // 2
     m = L // (2 * cp)
-    rank_ms = []
+    # how many block gradients reach each key half (rank, half) in the ring
+    into = {(s2, kh): 0 for s2 in range(cp) for kh in (0, 1)}
+    for r2 in range(cp):
+        for qh in (0, 1):
+            for s2 in range(cp):
+                for kh in (0, 1):
+                    if vlc.cp_block_mode(cp, r2, qh, s2, kh) != vlc.binding.CP_BLOCK_NONE:
+                        into[(s2, kh)] += 1
+    rank_ms, rank_bwd_ms = [], []
     for r in range(cp):
-        rows_d, pos_d, cuc, ql, kl, vl = locs[r]
+        rows_d, pos_d, cuc, ql, kl, vl, gl = locs[r]
         qrl, krl = torch.empty_like(ql), torch.empty_like(kl)
         wsr = torch.empty(vlc.load_library().vlc_rope_pos_workspace_bytes(L - 1, d), dtype=torch.uint8, device=dev)
         # every other rank's rotated k/v halves, as the ring would deliver them
         peers = {}
         for s2 in range(cp):
-            _, p2, _, _, k2, v2 = locs[s2]
+            _, p2, _, _, k2, v2, _ = locs[s2]
             peers[s2] = (vlc.rope_pos(k2, p2, L - 1), v2)
         blocks = []
         for qh in (0, 1):
@@ -578,13 +594,55 @@ def context_parallel_measurement(vlc, dev, peaks, L: int = 131072, cp: int = 4, 
         if st != 0:
             raise RuntimeError(f"context-parallel block: device error status {st} bits 0x{bits:x}")
         rank_ms.append(ms)
-        del peers, outs, om, lm, qrl, krl, wsb
+        # backward: block gradients into preallocated parts, then the sums and R(pos)^T
+        wsbb = vlc.new_workspace(1, m, H, d, m, True, dev, total_kv=m, max_seqlen_kv=m)
+        nb = len(blocks)
+        gparts = [tuple(torch.empty((half, H, d), dtype=torch.bfloat16, device=dev) for _ in range(3))
+                  for _ in range(nb)]
+        recv = {kh: [torch.zeros((half, H, d), dtype=torch.bfloat16, device=dev) for _ in range(into[(r, kh)])]
+                for kh in (0, 1)}
+        dq_h = [torch.empty((half, H, d), dtype=torch.bfloat16, device=dev) for _ in (0, 1)]
+        dk_h = [torch.empty((half, H, d), dtype=torch.bfloat16, device=dev) for _ in (0, 1)]
+        dv_h = [torch.empty((half, H, d), dtype=torch.bfloat16, device=dev) for _ in (0, 1)]
+        gsum = torch.empty((half, H, d), dtype=torch.bfloat16, device=dev)
+
+        def rank_bwd():
+            for i, (qh, src, kh, mode) in enumerate(blocks):
+                kk, vv = peers[src]
+                gq, gk, gv = gparts[i]
+                vlc.varlen_attn_bwd(gl[qh * half:(qh + 1) * half], qrl[qh * half:(qh + 1) * half],
+                                    kk[kh * half:(kh + 1) * half], vv[kh * half:(kh + 1) * half], om[qh], lm[qh],
+                                    cuc, m, rope_theta=0.0, dq=gq, dk=gk, dv=gv, workspace=wsbb, check=False,
+                                    cu_seqlens_kv=cuc, max_seqlen_kv=m,
+                                    keys_all_visible=mode == vlc.binding.CP_BLOCK_ALL)
+            for qh in (0, 1):
+                vlc.sum_parts([gparts[i][0] for i, b in enumerate(blocks) if b[0] == qh], out=gsum)
+                vlc.rope_pos(gsum, pos_d[qh * half:(qh + 1) * half], L - 1, out=dq_h[qh], workspace=wsr,
+                             check=False, transpose=True)
+            for kh in (0, 1):
+                vlc.sum_parts(recv[kh], out=gsum)
+                vlc.rope_pos(gsum, pos_d[kh * half:(kh + 1) * half], L - 1, out=dk_h[kh], workspace=wsr,
+                             check=False, transpose=True)
+                vlc.sum_parts(recv[kh], out=dv_h[kh])
+
+        rank_fwd()
+        bms, _ = _time_events(rank_bwd, reps)
+        st, bits = vlc.get_error(wsbb)
+        if st != 0:
+            raise RuntimeError(f"context-parallel block backward: device error status {st} bits 0x{bits:x}")
+        rank_bwd_ms.append(bms)
+        del peers, outs, om, lm, qrl, krl, wsb, wsbb, gparts, recv, dq_h, dk_h, dv_h, gsum
     mean = sum(rank_ms) / cp
+    bmean = sum(rank_bwd_ms) / cp
     fl = 4.0 * d * H * L * (L + 1) / 2
     return {"document_tokens": L, "cp": cp, "H": H, "head_dim": d, "whole_forward_ms": full_ms,
             "whole_forward_eff_TFLOP/s": fl / (full_ms * 1e-3) / 1e12, "rank_forward_ms": rank_ms,
             "balance_max_over_mean": max(rank_ms) / mean, "split_overhead": cp * mean / full_ms,
-            "note": "ranks run one after another on one GPU; communication not included"}
+            "whole_backward_ms": full_bwd_ms, "whole_backward_eff_TFLOP/s": 2.5 * fl / (full_bwd_ms * 1e-3) / 1e12,
+            "rank_backward_ms": rank_bwd_ms, "backward_balance_max_over_mean": max(rank_bwd_ms) / bmean,
+            "backward_split_overhead": cp * bmean / full_bwd_ms,
+            "note": "ranks run one after another on one GPU; communication not included; the dk / dv sums of a "
+                    "rank's key halves take stand-in parts of the ring's count"}
 
 
 EXTRAS = ("positions", "ce", "variants", "packer", "padded", "forward_configs", "step_form", "cp")
