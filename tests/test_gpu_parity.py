@@ -389,10 +389,30 @@ def test_fwd_peaky_scores_rescale_paths(vlc):
     assert (el / np.maximum(1.0, np.abs(lse_ref))).max() <= LSE_MAX
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("il", [False, True])
+def test_fwd_rope_without_room_for_rotated_k(vlc, il, d):
+    # a workspace without the optional rotated-k region: the forward falls back to the
+    # instance whose RoPE warps rotate every staged q and K tile; with the full workspace
+    # k is rotated once beforehand and the softmax warps rotate the q tiles
+    lens = [2100, 5, 300, 129, 1]
+    w = synth.custom_workload(lens, 2, d)
+    q, k, v = (t.to(DEV) for t in synth.make_tensors(w, seed=78 + d))
+    full = vlc.workspace_bytes(w.nseg, w.total, w.H, d, w.max_seqlen, False)
+    krot_bytes = (w.total * w.H * d * 2 + 255) // 256 * 256
+    small = torch.empty(full - krot_bytes, dtype=torch.uint8, device=DEV)
+    o_ref, lse_ref = oracle.attn_fwd(*(t.cpu() for t in (q, k, v)), w.cu, interleaved=il)
+    for ws in (small, None):
+        o, lse = vlc.varlen_attn_fwd(q, k, v, _cu(w), w.max_seqlen, rope_interleaved=il, workspace=ws)
+        e = o.float().cpu().numpy() - o_ref
+        assert np.abs(e).max() <= 2e-2 and np.abs(e).mean() <= 2e-3
+        assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-3
+
+
 @pytest.mark.parametrize("il", [False, True])
 def test_fwd_bwd_with_prerotated_keys(vlc, il):
-    # a segment with at least 2048 keys takes the forward's rotated-k pass (its K tiles are
-    # not rotated in-kernel); its neighbours are short and keep the in-kernel rotation
+    # with room in the workspace every segment's k is rotated once before the forward (its
+    # K tiles are not rotated in-kernel; the q tiles are, by the softmax warps)
     lens = [2100, 5, 300, 2048]
     w = synth.custom_workload(lens, 2, 128)
     q, k, v, g = (t.to(DEV) for t in synth.make_tensors(w, seed=77, with_grad=True))

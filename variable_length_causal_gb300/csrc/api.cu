@@ -227,12 +227,13 @@ static int attn_fwd_impl(AttnArgs a) {
     p.use_rope = mode;
     p.wait_limit_us = wait_limit_us();
     p.keys_all_visible = (a.flags & VLC_KEYS_ALL_VISIBLE) ? 1 : 0;
-    // long segments: k rotated once into the workspace (if it has room), not once per unit
+    // k rotated once into the workspace (if it has room) for every segment: the kernel then
+    // rotates only the q tiles, in its softmax warps; without the room, its RoPE warps rotate
+    // every staged q and K tile
     p.krot = nullptr;
-    p.prerot_min = kPreRotMinKeys;
-    if (mode != kRopeNone && !qkv && a.ws_bytes >= L.total && a.max_seqlen >= kPreRotMinKeys) {
-        if (launch_krot(p, w + L.krot, order, kPreRotMinKeys, num_sms_cached(), s) != cudaSuccess)
-            return VLC_ERR_CUDA;
+    p.prerot_min = 0;
+    if (mode != kRopeNone && a.ws_bytes >= L.total) {
+        if (launch_krot(p, w + L.krot, order, 0, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
         p.krot = w + L.krot;
     }
     if (launch_attn_fwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;

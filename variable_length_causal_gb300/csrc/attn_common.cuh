@@ -250,15 +250,16 @@ __device__ __forceinline__ RopeStep<D> rope_step(const float2* __restrict__ tabl
 // Rotate a staged tile of ROWS rows (segment-local positions pos0 + row) in
 // place: x' = x cos - y sin, y' = y cos + x sin for each pair (x, y) of the
 // pairing IL, computed in fp32 (packed pairs) and rounded to bf16.  Executed
-// by 128 threads (4 warps, wr = 0..3); each 64-column block holds ROWS x 128 B.
+// by 128 threads (4 warps, wr = 0..3).
 // A thread reads the cos/sin of its first row from the table and advances the
 // angle by complex multiplication with its RopeStep (a few 1e-7 of drift over
 // a tile).
-template <int D, int ROWS, bool IL>
+// BLK: bytes between the tile's 64-column blocks (ROWS x 128 B for a whole tile; a slice of
+// a taller tile passes the taller tile's block size).
+template <int D, int ROWS, bool IL, uint32_t BLK = ROWS * 128u>
 __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2* __restrict__ table,
                                           const RopeStep<D>& step, int wr, int lane) {
     constexpr int half = D / 2;
-    constexpr uint32_t BLK = ROWS * 128u;
     constexpr int PAIRS_PER_ROW = half / 8;            // threads per row
     constexpr int ROWS_PER_IT = 32 / PAIRS_PER_ROW;
     constexpr int ROWS_PER_WARP = ROWS / 4;

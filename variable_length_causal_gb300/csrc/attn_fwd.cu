@@ -8,7 +8,7 @@
 // (section "Positions are reset per segment").  LSE = ln sum exp(scores).
 //
 // Design: one persistent CTA per SM, warp-specialised (640 threads; 512 in the
-// instance with RoPE warps).  A work unit is (segment, head, block of 256 query
+// fallback instance with RoPE warps).  A work unit is (segment, head, block of 256 query
 // rows) = two 128-row q tiles that share every K/V tile; the work list holds only
 // in-segment, at-or-below-diagonal key tiles, and a q tile stops at its own
 // diagonal key tile.  Units are claimed dynamically (longest first) from a global
@@ -32,9 +32,14 @@
 //                back over the consumed S columns; the causal / segment-tail mask only
 //                on a tile's last key tile; lazy O rescale when the row max grows by
 //                more than 2^8; epilogue O / l -> bf16 and LSE, half a row per thread.
-//   With RoPE in the kernel: warps 4-7 and 8-11 are the softmax of q tiles 0 and 1
-//                with one thread per row (128 scores each), and warps 12-15 rotate the
-//                staged q and K tiles (segment-local positions).
+//   RoPE (segment-local positions): k is rotated once beforehand into the workspace
+//                (krot_kernel, every segment) and the warps of q tile 0, which end each
+//                unit one key tile ahead of tile 1's, rotate the next unit's two staged q
+//                tiles in shared memory before their epilogue.  Without room in the
+//                workspace for the rotated k, a fallback instance rotates every staged q
+//                and K tile in a RoPE warpgroup (warps 12-15; its softmax warps 4-7 and
+//                8-11 hold one query row per thread, 128 scores each: there are no
+//                registers left for split rows).
 // Every wait is bounded; on expiry the kernel sets VLC_DEVERR_TIMEOUT, drains
 // its own in-flight copies and MMAs, frees TMEM and returns.
 #include <type_traits>
@@ -57,24 +62,36 @@ static_assert(QB == 2 * BQ && BN == 128, "two 128-row q tiles per unit, 128-row 
 constexpr int kQSlots = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// Kernel instances by where q and K tiles are rotated:
+//   kModePlain  no RoPE, or q, k rotated beforehand (vlc_rope_qk);
+//   kModeWarps  a RoPE warpgroup rotates every staged q and K tile (the fallback when the
+//               workspace has no room for a rotated copy of k);
+//   kModeQRot   k rotated once beforehand into the workspace for every segment, and the
+//               q tiles rotated in shared memory by the softmax warps of q tile 0 while
+//               they finish the unit before (they end it one key tile ahead of tile 1's).
+enum : int { kModePlain = 0, kModeWarps = 1, kModeQRot = 2 };
+
 // Threads: a control warpgroup (producers, MMA issuer, scheduler) and the softmax
 // warpgroups; the warpgroups re-split the launch's register pool with setmaxnreg.
 //   without RoPE warps: four softmax warpgroups, two per q tile (the two threads of a
 //     query row sit in one warp and take 64 score columns each);
 //   with RoPE warps: two softmax warpgroups, one thread per query row holding its
 //     128 scores, and a RoPE warpgroup (no register room for the split rows).
-template <bool ROPE>
+template <int MODE>
 struct Cfg {
-    static constexpr int kSoftWarps = ROPE ? 8 : 16;
-    static constexpr int kThreads = 32 * (4 + kSoftWarps + (ROPE ? 4 : 0));   // 512 or 640
-    static constexpr uint32_t kLaunchRegs = 65536u / kThreads / 8u * 8u;      // registers per thread at launch
-    static constexpr uint32_t kCtrlRegs = ROPE ? 72u : 56u;
-    static constexpr uint32_t kRopeRegs = ROPE ? 88u : 0u;
+    static constexpr bool kWarps = MODE == kModeWarps;
+    static constexpr int kSoftWarps = kWarps ? 8 : 16;
+    static constexpr int kThreads = 32 * (4 + kSoftWarps + (kWarps ? 4 : 0));   // 512 or 640
+    static constexpr uint32_t kLaunchRegs = 65536u / kThreads / 8u * 8u;        // registers per thread at launch
+    static constexpr uint32_t kCtrlRegs = kWarps ? 72u : 56u;
+    static constexpr uint32_t kRopeRegs = kWarps ? 88u : 0u;
     static constexpr uint32_t kSoftRegs =
         (kThreads * kLaunchRegs - 128u * kCtrlRegs - 128u * kRopeRegs) / (32u * kSoftWarps) / 8u * 8u;
     static_assert(128u * kCtrlRegs + 128u * kRopeRegs + 32u * kSoftWarps * kSoftRegs <= kThreads * kLaunchRegs,
                   "register split exceeds the pool");
     static constexpr uint32_t kTileThreads = 32u * kSoftWarps / 2;   // softmax threads of one q tile
+    // threads that rotate a staged q tile and arrive on its Q_READY barrier (a warpgroup)
+    static constexpr uint32_t kQReadyCount = 128u;
 };
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -141,13 +158,15 @@ __device__ __forceinline__ FUnit make_funit(const FwdParams& p, const Unit& w) {
 }
 
 // KV: keys and values have segments of their own (bottom-right aligned queries).
-template <int D, bool KV, bool ROPE>
-__global__ void __launch_bounds__(Cfg<ROPE>::kThreads, 1)
+template <int D, bool KV, int MODE>
+__global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmKr,
                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
     using LY = Layout<D>;
-    using CF = Cfg<ROPE>;
+    using CF = Cfg<MODE>;
+    constexpr bool ROPE = MODE == kModeWarps;     // the RoPE-warp instance (one thread per row)
+    constexpr bool ROTQ = MODE == kModeQRot;      // softmax warps rotate the q tiles
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
@@ -172,7 +191,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int i = 0; i < kQSlots; ++i) {
             mbar_init(bar(Q_FULL + i), 1);
-            mbar_init(bar(Q_READY + i), 128);
+            mbar_init(bar(Q_READY + i), CF::kQReadyCount);
             mbar_init(bar(Q_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -189,7 +208,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bar(DRAIN), 1);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(bar(UNIT_FULL + i), 1);
-            mbar_init(bar(UNIT_EMPTY + i), p.use_rope ? kRingConsumers : kRingConsumers - 4);
+            mbar_init(bar(UNIT_EMPTY + i), ROPE && p.use_rope ? kRingConsumers : kRingConsumers - 4);
         }
         abort[0] = 0;
         abort[1] = static_cast<int>(p.wait_limit_us);   // the waits' limit (ctl[1])
@@ -262,8 +281,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, false);
             constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);
             uint32_t qm = 0, kvn = 0, cnt_p[2] = {0, 0}, cnt_u[2] = {0, 0};
-            // without RoPE the staged tiles go straight from the TMA barriers to the MMAs
-            const int qrb = p.use_rope ? Q_READY : Q_FULL, krb = p.use_rope ? K_READY : K_FULL;
+            // without RoPE the staged tiles go straight from the TMA barriers to the MMAs; with
+            // the q rotation in the softmax warps the K tiles do (k was rotated beforehand)
+            const int qrb = p.use_rope ? Q_READY : Q_FULL, krb = ROPE && p.use_rope ? K_READY : K_FULL;
             bool ok = true;
             auto commit = [&](uint32_t b) {
                 if (elect_one()) mma_commit(b);
@@ -506,14 +526,46 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float sl2 = p.scale_log2;
             const bool v8 = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;   // 256-bit row stores
             uint32_t cnt_s = 0, cnt_u = 0;
-            bool ok = true;
-            for (int un = 0; ok; ++un) {
-                int u;
-                Unit uw;
-                if (!(ok = ring_get_warp(rg, un, abort, u, uw)) || u < 0) break;
+            // With kModeQRot the warps of q tile 0, which finish each unit one key tile before
+            // those of q tile 1, rotate the next unit's q tiles in shared memory (warpgroup sub
+            // takes tile sub) once they have landed and release them to the MMA warp; the next
+            // unit is read from the ring after this unit's last P, before the O wait.  qm counts
+            // the q slots of the units before the current one, as the producer and the MMA warp do.
+            uint32_t qm = 0;
+            auto rotate_q = [&](const FUnit& g, uint32_t qslots) -> bool {
+                if constexpr (ROTQ) {
+                    if (t != 0 || (sub == 1 && !g.has1)) return true;
+                    const uint32_t qs = qslots + sub;
+                    if (!wait_warp(bar(Q_FULL + qs % kQSlots), (qs / kQSlots) & 1, abort)) return false;
+                    const uint32_t tile = sbase + LY::Q0 + (qs % kQSlots) * LY::TILE;
+                    const int pos0 = (g.q0 + sub) * BQ + g.w.off;
+                    if (p.use_rope == kRopeInterleaved)
+                        rope_tile<D, 128, true>(tile, pos0, p.table, rope_step<D, true>(p.table, lane), wq, lane);
+                    else
+                        rope_tile<D, 128, false>(tile, pos0, p.table, rope_step<D, false>(p.table, lane), wq, lane);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(Q_READY + qs % kQSlots));
+                }
+                return true;
+            };
+            int u;
+            Unit uw;
+            bool ok = ring_get_warp(rg, 0, abort, u, uw);
+            if (ok && u >= 0) ok = rotate_q(make_funit<KV>(p, uw), 0);
+            for (int un = 0; ok && u >= 0; ++un) {
                 const FUnit f = make_funit<KV>(p, uw);
+                const uint32_t qm_next = qm + (f.has1 ? 2u : 1u);
                 const int nt = t == 0 ? f.n0 : f.n1;
-                if (nt == 0) continue;
+                int u_next;
+                Unit w_next;
+                if (nt == 0) {
+                    if (!(ok = ring_get_warp(rg, un + 1, abort, u_next, w_next))) break;
+                    if (u_next >= 0 && !(ok = rotate_q(make_funit<KV>(p, w_next), qm_next))) break;
+                    u = u_next;
+                    uw = w_next;
+                    qm = qm_next;
+                    continue;
+                }
                 const int qpos = (f.q0 + t) * BQ + r;
                 float m_run = 0.f, l_run = 0.f;   // l_run: this thread's half of the row sum
                 for (int j = 0; j < nt; ++j) {
@@ -592,6 +644,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     mbar_arrive(bar(P_FULL + t));
                 }
                 if (!ok) break;
+                if (!(ok = ring_get_warp(rg, un + 1, abort, u_next, w_next))) break;
+                if (u_next >= 0 && !(ok = rotate_q(make_funit<KV>(p, w_next), qm_next))) break;
                 // ---- epilogue: O / l -> bf16, LSE
                 if (!(ok = wait_warp(bar(O_FULL + t), cnt_u & 1, abort))) break;
                 tc_fence_after();
@@ -622,6 +676,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (valid && hf == 0)
                     p.lse[static_cast<int64_t>(f.w.h) * p.total + tok] = (m_run + __log2f(l_row)) * kLn2;
                 ++cnt_u;
+                u = u_next;
+                uw = w_next;
+                qm = qm_next;
             }
         }
     } else if (warp >= 4 + CF::kSoftWarps) {
@@ -755,15 +812,25 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
         !make_tmap_thd(&tv, p.v, p.total_kv, p.Hkv, p.d, 128))
         return cudaErrorInvalidValue;
     const bool kv = p.cu_kv != p.cu || p.keys_all_visible;
-    // one instance with RoPE warps, one without them
-    const bool rope = p.use_rope != kRopeNone;
-    auto kernel = p.d == 128
-                      ? (kv ? (rope ? fwd::attn_fwd_kernel<128, true, true> : fwd::attn_fwd_kernel<128, true, false>)
-                            : (rope ? fwd::attn_fwd_kernel<128, false, true> : fwd::attn_fwd_kernel<128, false, false>))
-                      : (kv ? (rope ? fwd::attn_fwd_kernel<64, true, true> : fwd::attn_fwd_kernel<64, true, false>)
-                            : (rope ? fwd::attn_fwd_kernel<64, false, true> : fwd::attn_fwd_kernel<64, false, false>));
-    const int threads = rope ? fwd::Cfg<true>::kThreads : fwd::Cfg<false>::kThreads;
-    const uint32_t regs = rope ? fwd::Cfg<true>::kLaunchRegs : fwd::Cfg<false>::kLaunchRegs;
+    // RoPE with k rotated beforehand into the workspace: the softmax warps rotate q; RoPE
+    // without that copy: the RoPE-warp instance; no RoPE (or operands rotated beforehand)
+    const int mode = p.use_rope == kRopeNone ? fwd::kModePlain
+                     : (p.krot != nullptr && p.prerot_min == 0 ? fwd::kModeQRot : fwd::kModeWarps);
+    using KFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams);
+    auto pick = [&](auto dtag, auto kvtag) -> KFn {
+        constexpr int D = decltype(dtag)::value;
+        constexpr bool KVI = decltype(kvtag)::value;
+        return mode == fwd::kModePlain  ? fwd::attn_fwd_kernel<D, KVI, fwd::kModePlain>
+               : mode == fwd::kModeQRot ? fwd::attn_fwd_kernel<D, KVI, fwd::kModeQRot>
+                                        : fwd::attn_fwd_kernel<D, KVI, fwd::kModeWarps>;
+    };
+    using D128 = std::integral_constant<int, 128>;
+    using D64 = std::integral_constant<int, 64>;
+    const KFn kernel = p.d == 128 ? (kv ? pick(D128{}, std::true_type{}) : pick(D128{}, std::false_type{}))
+                                  : (kv ? pick(D64{}, std::true_type{}) : pick(D64{}, std::false_type{}));
+    const int threads = mode == fwd::kModeWarps ? fwd::Cfg<fwd::kModeWarps>::kThreads : fwd::Cfg<fwd::kModePlain>::kThreads;
+    const uint32_t regs =
+        mode == fwd::kModeWarps ? fwd::Cfg<fwd::kModeWarps>::kLaunchRegs : fwd::Cfg<fwd::kModePlain>::kLaunchRegs;
     const dim3 grid(num_sms), block(threads);
     const uint32_t smem = p.d == 128 ? fwd::Layout<128>::ALLOC : fwd::Layout<64>::ALLOC;
     // The warpgroups re-split the block's register pool at run time, which is only
@@ -783,12 +850,12 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
 
 // ---------------------------------------------------------------- rotated k for long segments
 // One pass over the key rows of segments with at least min_keys keys: k' = R(p) k
-// (bf16, rounded once, the same rotation as the in-kernel tiles), so the forward
+// (bf16, rounded once, the rotation of the backward's prep pass), so the forward
 // kernel reads those K tiles ready-made instead of rotating each of them once per
-// work unit that reads it.  The work list's order puts the long segments first:
-// every block walks that order until the segments get short and takes a
-// grid-stride share of each long segment's rows (D/16 threads per row, as in the
-// backward's prep pass).
+// work unit that reads it.  cu: the key segments' offsets.  The work list's order
+// puts the long segments first: every block walks that order until the segments
+// get short and takes a grid-stride share of each segment's rows (D/16 threads per
+// row, as in the backward's prep pass).
 namespace fwd {
 template <int D>
 __global__ void __launch_bounds__(256)
@@ -825,7 +892,7 @@ krot_kernel(const uint4* __restrict__ k, uint4* __restrict__ krot, const int32_t
 cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, int32_t min_keys, int num_sms,
                         cudaStream_t s) {
     auto kernel = p.d == 128 ? fwd::krot_kernel<128> : fwd::krot_kernel<64>;
-    kernel<<<num_sms * 8, 256, 0, s>>>(static_cast<const uint4*>(p.k), static_cast<uint4*>(krot), p.cu, p.rows_kv,
+    kernel<<<num_sms * 8, 256, 0, s>>>(static_cast<const uint4*>(p.k), static_cast<uint4*>(krot), p.cu_kv, p.rows_kv,
                                        order, p.nseg, p.table, p.Hkv, p.use_rope, min_keys, p.err);
     return cudaGetLastError();
 }

@@ -106,7 +106,7 @@ struct FwdParams {
     int32_t* err;
     const float2* table;       // RoPE cos/sin [rows][d/2], null if no RoPE
     const void* krot;          // R(p) k for segments with at least prerot_min keys, or null
-    int32_t prerot_min;
+    int32_t prerot_min;        // 0 with krot: every key rotated beforehand (the q-rotating instance)
     int32_t nseg, total, H, d;
     int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
     int32_t total_kv;          // key/value rows (== total for self-attention)
@@ -119,16 +119,11 @@ struct FwdParams {
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s);
 
-// Segments with at least this many keys get their k rows rotated once, before the
-// forward kernel, instead of once per work unit inside it (a segment of T key
-// tiles is read by ~T/2 units; below ~16 tiles the extra HBM pass costs more than
-// the in-kernel rotations it saves).
-constexpr int32_t kPreRotMinKeys = 2048;
-
 // R(p) k into krot for the key rows of segments with at least min_keys keys
-// (other rows are not written).  order: the forward work list's segment order
-// (descending q-tile count, kFwdQB-row tiles), so the long segments come first;
-// self-attention only.  No-op if *err != 0.
+// (other rows are not written), keys at their own positions (0 .. Lk-1 of the key
+// segment, p.cu_kv).  order: the forward work list's segment order (descending
+// q-tile count, kFwdQB-row tiles), so the long segments come first.  No-op if
+// *err != 0.
 cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, int32_t min_keys, int num_sms,
                         cudaStream_t s);
 
