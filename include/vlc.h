@@ -416,8 +416,8 @@ int vlc_rope_qk(const void* q, const void* k, const int32_t* cu, const int32_t* 
  *            this call's VLC_DEVERR_* bits (0 when the call found no error).
  * Returns VLC_ERR_WORKSPACE, before enqueuing anything, when the forward
  * workspace without its optional rotated-k region exceeds the array; when the
- * whole workspace (vlc_workspace_bytes(..., 0)) fits, long segments take the
- * rotated-k pass as in vlc_attn_fwd.  Invalid or unsupported arguments give the
+ * whole workspace (vlc_workspace_bytes(..., 0)) fits, k is rotated once into it
+ * as in vlc_attn_fwd.  Invalid or unsupported arguments give the
  * status vlc_attn_fwd gives for them.
  * The first call on a device looks up the array's address (do it before any
  * stream capture begins).  All calls share the array: calls whose GPU work can

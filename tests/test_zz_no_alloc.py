@@ -5,8 +5,8 @@ is forbidden, or services whose device-memory budget is fixed at start-up) canno
 the library a workspace; this entry point keeps its scratch in a static device array.
 The tests call it through the C ABI twice in a row, on two different packs, and check
 each result against vlc_attn_fwd (which takes a workspace) with the parity tolerances;
-one pack has a segment of more than 2048 keys whose whole forward workspace fits in the
-static array, so the rotated-k pass runs inside it, and that result is also checked
+one pack (with a segment of more than 2048 keys) has a whole forward workspace that fits
+in the static array, so k is rotated once inside it, and that result is also checked
 against the fp64 oracle.  The file sits last in pytest's collection order.
 """
 import ctypes

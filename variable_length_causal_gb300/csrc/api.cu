@@ -58,7 +58,7 @@ WsLayout ws_layout(int32_t nseg, int32_t total, int32_t H, int32_t Hkv, int32_t 
         off = align256(off + static_cast<size_t>(total_kv) * Hkv * d * 2);
     }
     L.total_min = off;
-    if (!is_bwd) {   // the forward's rotated copy of k (long segments), used when the workspace has room
+    if (!is_bwd) {   // the forward's rotated copy of k, used when the workspace has room
         L.krot = off;
         off = align256(off + static_cast<size_t>(total_kv) * Hkv * d * 2);
     }

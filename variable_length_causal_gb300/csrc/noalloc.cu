@@ -13,11 +13,11 @@
 // Properties a caller must know:
 //  - The array holds kNoAllocScratchBytes (8 MiB) on every GPU that loads this
 //    library, for the lifetime of the process.  A problem is accepted when the
-//    forward's workspace without its optional region (the rotated copy of k for
-//    segments of at least 2048 keys) fits; larger ones are rejected with
-//    VLC_ERR_WORKSPACE before anything is enqueued.  When the whole workspace
-//    fits, long segments take the rotated-k pass exactly as vlc_attn_fwd does;
-//    otherwise their K tiles are rotated inside the attention kernel.
+//    forward's workspace without its optional region (the rotated copy of k)
+//    fits; larger ones are rejected with VLC_ERR_WORKSPACE before anything is
+//    enqueued.  When the whole workspace fits, k is rotated once into it exactly
+//    as vlc_attn_fwd does; otherwise the attention kernel's RoPE warps rotate
+//    every staged K tile.
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (with that device current) and caches it; make that
 //    first call before any stream capture begins.
@@ -80,8 +80,7 @@ extern "C" int vlc_attn_fwd_noalloc(const void* q, const void* k, const void* v,
     }
     // The scratch must hold the forward's work list, segment order, RoPE table and
     // error word.  If it also holds the optional rotated copy of k (the whole layout
-    // fits), the forward uses it for segments of at least 2048 keys; otherwise it
-    // rotates those K tiles inside the kernel.
+    // fits), the forward uses it; otherwise it rotates the K tiles inside the kernel.
     const size_t need = vlc::ws_layout(nseg, total, H, H, d, max_seqlen, 0).total_min;
     if (need > vlc::kNoAllocScratchBytes) return VLC_ERR_WORKSPACE;
     void* scratch = nullptr;
