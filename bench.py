@@ -226,11 +226,11 @@ class Step:
 
 # posl; rotation (worklist and table in one launch + q'/k'); forward (worklist + attention);
 # backward (2 worklists and table in one launch + delta + dq + dkdv).  With RoPE in the
-# kernels there is no rotation pass; the forward adds the rotated-k pass of long segments
-# when the pack has a segment of at least 2048 keys.
+# kernels there is no rotation pass; the forward adds its pass that rotates k once (the
+# attention kernel rotates the q tiles).
 def launches_per_step(w, fwd_only, rope):
     rot = 2 if rope == "once" else 0
-    krot = 1 if rope == "fused" and int(w.max_seqlen) >= 2048 else 0
+    krot = 1 if rope == "fused" else 0
     return 1 + rot + 2 + krot + (0 if fwd_only else 4)
 
 
@@ -373,7 +373,8 @@ def gpu_arm(args, w, world, rank, local):
                           "eff_TFLOP/s": fwd_tflops,
                           "kernels": ("rotation (meta_kernel: work list + RoPE table; rope_qk_kernel) + meta_kernel "
                                       "(work list) + attn_fwd_kernel" if args.rope == "once" else
-                                      "meta_kernel (work list + RoPE table) [+ krot_kernel] + attn_fwd_kernel")},
+                                      "meta_kernel (work list + RoPE table) + rope_qk_kernel (k only) + attn_fwd_kernel "
+                                      "(q rotated in the kernel)")},
         "attn_bwd_call": {"ms": t_bwd, "ms_median": statistics.median(per_bwd), "ms_min": min(per_bwd),
                           "eff_TFLOP/s": bwd_tflops,
                           "kernels": "meta_kernel (2 work lists + RoPE tables) + prep_kernel (delta) + dq_kernel + dkdv_kernel"},

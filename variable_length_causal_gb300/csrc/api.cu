@@ -231,9 +231,8 @@ static int attn_fwd_impl(AttnArgs a) {
     // rotates only the q tiles, in its softmax warps; without the room, its RoPE warps rotate
     // every staged q and K tile
     p.krot = nullptr;
-    p.prerot_min = 0;
     if (mode != kRopeNone && a.ws_bytes >= L.total) {
-        if (launch_krot(p, w + L.krot, order, 0, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
+        if (launch_rope_k(p, w + L.krot, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
         p.krot = w + L.krot;
     }
     if (launch_attn_fwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;

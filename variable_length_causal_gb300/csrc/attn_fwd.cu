@@ -33,7 +33,7 @@
 //                on a tile's last key tile; lazy O rescale when the row max grows by
 //                more than 2^8; epilogue O / l -> bf16 and LSE, half a row per thread.
 //   RoPE (segment-local positions): k is rotated once beforehand into the workspace
-//                (krot_kernel, every segment) and the warps of q tile 0, which end each
+//                (the k half of the rotation pass) and the warps of q tile 0, which end each
 //                unit one key tile ahead of tile 1's, rotate the next unit's two staged q
 //                tiles in shared memory before their epilogue.  Without room in the
 //                workspace for the rotated k, a fallback instance rotates every staged q
@@ -129,7 +129,7 @@ struct Layout {
 struct FUnit {
     Unit w;
     bool has1;
-    bool pre;   // K tiles come rotated from p.krot (long segments), not rotated in-kernel
+    bool pre;   // K tiles come rotated from p.krot, not rotated in-kernel
     int q0, n0, n1, nk;
     int hkv;   // key/value head of query head w.h
 };
@@ -152,7 +152,7 @@ __device__ __forceinline__ FUnit make_funit(const FwdParams& p, const Unit& w) {
         f.n1 = f.has1 ? f.q0 + 2 : 0;
     }
     f.nk = f.has1 ? f.n1 : f.n0;
-    f.pre = p.krot != nullptr && f.w.Lk >= p.prerot_min;
+    f.pre = p.krot != nullptr;
     f.hkv = p.Hkv == p.H ? f.w.h : f.w.h / (p.H / p.Hkv);
     return f;
 }
@@ -815,7 +815,7 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
     // RoPE with k rotated beforehand into the workspace: the softmax warps rotate q; RoPE
     // without that copy: the RoPE-warp instance; no RoPE (or operands rotated beforehand)
     const int mode = p.use_rope == kRopeNone ? fwd::kModePlain
-                     : (p.krot != nullptr && p.prerot_min == 0 ? fwd::kModeQRot : fwd::kModeWarps);
+                     : (p.krot != nullptr ? fwd::kModeQRot : fwd::kModeWarps);
     using KFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdParams);
     auto pick = [&](auto dtag, auto kvtag) -> KFn {
         constexpr int D = decltype(dtag)::value;
@@ -844,56 +844,6 @@ cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kernel<<<grid, block, smem, s>>>(tq, tk, tkr, tv, p);
-    return cudaGetLastError();
-}
-
-
-// ---------------------------------------------------------------- rotated k for long segments
-// One pass over the key rows of segments with at least min_keys keys: k' = R(p) k
-// (bf16, rounded once, the rotation of the backward's prep pass), so the forward
-// kernel reads those K tiles ready-made instead of rotating each of them once per
-// work unit that reads it.  cu: the key segments' offsets.  The work list's order
-// puts the long segments first: every block walks that order until the segments
-// get short and takes a grid-stride share of each segment's rows (D/16 threads per
-// row, as in the backward's prep pass).
-namespace fwd {
-template <int D>
-__global__ void __launch_bounds__(256)
-krot_kernel(const uint4* __restrict__ k, uint4* __restrict__ krot, const int32_t* __restrict__ cu,
-            const int32_t* __restrict__ rows, const int32_t* __restrict__ order, int32_t nseg,
-            const float2* __restrict__ table, int32_t Hkv, int rope, int32_t min_keys,
-            const int32_t* __restrict__ err) {
-    if (*err != 0) return;
-    constexpr int TPR = D / 16;
-    constexpr int HALF = D / 16;
-    const int min_tiles = (min_keys + kFwdQB - 1) / kFwdQB;
-    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int c = static_cast<int>(gtid % TPR);
-    const bool il = rope == kRopeInterleaved;
-    for (int i = 0; i < nseg; ++i) {
-        const int r = __ldg(order + i);
-        const int L = __ldg(cu + r + 1) - __ldg(cu + r);
-        if ((L + kFwdQB - 1) / kFwdQB < min_tiles) break;   // sorted: the rest are shorter
-        if (L < min_keys) continue;
-        const int64_t row0 = static_cast<int64_t>(__ldg(rows + r)) * Hkv;
-        const int64_t nrows = static_cast<int64_t>(L) * Hkv;
-        for (int64_t j = gtid / TPR; j < nrows; j += nthreads / TPR) {
-            const int64_t pos = j / Hkv;
-            float cs[8], sn[8];
-            load_angles<D>(table, pos, il, c, cs, sn);
-            const int64_t lo = (row0 + j) * (2 * HALF) + c;
-            rotate_chunks(k, krot, lo, lo + HALF, cs, sn, true, il);
-        }
-    }
-}
-}  // namespace fwd
-
-cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, int32_t min_keys, int num_sms,
-                        cudaStream_t s) {
-    auto kernel = p.d == 128 ? fwd::krot_kernel<128> : fwd::krot_kernel<64>;
-    kernel<<<num_sms * 8, 256, 0, s>>>(static_cast<const uint4*>(p.k), static_cast<uint4*>(krot), p.cu_kv, p.rows_kv,
-                                       order, p.nseg, p.table, p.Hkv, p.use_rope, min_keys, p.err);
     return cudaGetLastError();
 }
 
@@ -952,16 +902,27 @@ rope_qk_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k, uint4* 
 }
 }  // namespace fwd
 
-cudaError_t launch_rope_qk(const FwdParams& p, void* qrot, void* krot, int num_sms, cudaStream_t s) {
+static cudaError_t launch_rope_rows(const FwdParams& p, const void* q, const void* k, void* qrot, void* krot,
+                                    const int32_t* cu, const int32_t* rows, int32_t total, int32_t H, int num_sms,
+                                    cudaStream_t s) {
     const int tokb = 256 / (p.d / 16);   // tokens per block pass
-    int64_t blocks = (static_cast<int64_t>(p.total) + tokb - 1) / tokb;
+    int64_t blocks = (static_cast<int64_t>(total) + tokb - 1) / tokb;
     if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
     if (blocks < 1) blocks = 1;
     auto kernel = p.d == 128 ? fwd::rope_qk_kernel<128> : fwd::rope_qk_kernel<64>;
-    kernel<<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const uint4*>(p.q), static_cast<const uint4*>(p.k),
-                                                     static_cast<uint4*>(qrot), static_cast<uint4*>(krot), p.cu,
-                                                     p.rows, p.nseg, p.table, p.total, p.H, p.Hkv, p.use_rope, p.err);
+    kernel<<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const uint4*>(q), static_cast<const uint4*>(k),
+                                                     static_cast<uint4*>(qrot), static_cast<uint4*>(krot), cu, rows,
+                                                     p.nseg, p.table, total, H, p.Hkv, p.use_rope, p.err);
     return cudaGetLastError();
+}
+
+cudaError_t launch_rope_qk(const FwdParams& p, void* qrot, void* krot, int num_sms, cudaStream_t s) {
+    return launch_rope_rows(p, p.q, p.k, qrot, krot, p.cu, p.rows, p.total, p.H, num_sms, s);
+}
+
+// k alone (no query heads), over the key segments: the forward's rotated copy of k.
+cudaError_t launch_rope_k(const FwdParams& p, void* krot, int num_sms, cudaStream_t s) {
+    return launch_rope_rows(p, nullptr, p.k, nullptr, krot, p.cu_kv, p.rows_kv, p.total_kv, 0, num_sms, s);
 }
 
 }  // namespace vlc

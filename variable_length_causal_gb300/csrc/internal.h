@@ -105,8 +105,7 @@ struct FwdParams {
     int32_t* next;             // unit counter (zeroed before the launch)
     int32_t* err;
     const float2* table;       // RoPE cos/sin [rows][d/2], null if no RoPE
-    const void* krot;          // R(p) k for segments with at least prerot_min keys, or null
-    int32_t prerot_min;        // 0 with krot: every key rotated beforehand (the q-rotating instance)
+    const void* krot;          // R(p) k of every key row (rotated beforehand), or null
     int32_t nseg, total, H, d;
     int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
     int32_t total_kv;          // key/value rows (== total for self-attention)
@@ -119,13 +118,10 @@ struct FwdParams {
 
 cudaError_t launch_attn_fwd(const FwdParams& p, int num_sms, cudaStream_t s);
 
-// R(p) k into krot for the key rows of segments with at least min_keys keys
-// (other rows are not written), keys at their own positions (0 .. Lk-1 of the key
-// segment, p.cu_kv).  order: the forward work list's segment order (descending
-// q-tile count, kFwdQB-row tiles), so the long segments come first.  No-op if
-// *err != 0.
-cudaError_t launch_krot(const FwdParams& p, void* krot, const int32_t* order, int32_t min_keys, int num_sms,
-                        cudaStream_t s);
+// R(p) k into krot for every key row, keys at their own positions (0 .. Lk-1 of the key
+// segment, p.cu_kv / p.rows_kv; rows past a padded segment's length become zeros): the
+// pass of launch_rope_qk with no query heads.  No-op if *err != 0.
+cudaError_t launch_rope_k(const FwdParams& p, void* krot, int num_sms, cudaStream_t s);
 
 // R(p) q into qrot and R(p) k into krot for every row (self-attention; rows past
 // a segment's length in a padded layout become zeros).  Uses p.q, p.k, p.cu,
