@@ -2,8 +2,10 @@
 """Benchmark of the packed varlen causal attention path on GB300.
 
 One step = the whole hot path over one synthetic packed batch:
-  positions + labels  ->  forward attention (work list, RoPE table, tcgen05 kernel)
-  ->  backward attention (work lists, delta, dQ pass, dK/dV pass).
+  positions + labels  ->  forward attention (work list, RoPE table, k rotated once, tcgen05
+  kernel rotating the q tiles, which also returns q', k')  ->  backward attention on q', k'
+  (work lists, delta, dQ pass, dK/dV pass).  --rope once instead rotates q, k by one pass
+  before the forward.
 Metric: effective TFLOP/s counting only in-segment causal FLOPs of real (non-pad)
 segments, 4*d*H*pairs (forward) + 10*d*H*pairs (backward); packed real tokens/s
 is reported beside it.  Default workload: the pretraining-window forward+backward pack
@@ -179,7 +181,9 @@ class Step:
         self.o = torch.empty_like(q)
         self.lse = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
         self.fwd_only = fwd_only
-        self.rope = rope   # "once": q, k rotated by one pass for both directions; "fused": in the kernels
+        # "once": q, k rotated by one pass for both directions; "fused": RoPE in the forward kernel,
+        # which returns q', k' for the backward (forward-only: the plain forward with RoPE in the kernel)
+        self.rope = rope
         if fwd_only:
             self.dq = self.dk = self.dv = None
         else:
@@ -203,15 +207,21 @@ class Step:
         if once:
             vlc.rope_qk(self.q, self.k, self.cu, w.max_seqlen, rope_theta=w.theta, out=(self.qr, self.kr),
                         workspace=self.ws_f, check=False)
-        qa, ka = (self.qr, self.kr) if once else (self.q, self.k)
-        vlc.varlen_attn_fwd(qa, ka, self.v, self.cu, w.max_seqlen, rope_theta=w.theta, out=self.o,
-                            lse=self.lse, workspace=self.ws_f, check=False, qk_rotated=once)
+            vlc.varlen_attn_fwd(self.qr, self.kr, self.v, self.cu, w.max_seqlen, rope_theta=w.theta, out=self.o,
+                                lse=self.lse, workspace=self.ws_f, check=False, qk_rotated=True)
+        elif self.fwd_only:
+            vlc.varlen_attn_fwd(self.q, self.k, self.v, self.cu, w.max_seqlen, rope_theta=w.theta, out=self.o,
+                                lse=self.lse, workspace=self.ws_f, check=False)
+        else:   # RoPE in the forward kernel, which also returns q', k' for the backward
+            vlc.varlen_attn_fwd_rot(self.q, self.k, self.v, self.cu, w.max_seqlen, rope_theta=w.theta,
+                                    out=self.o, lse=self.lse, rotated_out=(self.qr, self.kr), workspace=self.ws_f,
+                                    check=False)
         if ev is not None:
             ev[2].record()
         if not self.fwd_only:
-            vlc.varlen_attn_bwd(self.g, qa, ka, self.v, self.o, self.lse, self.cu, w.max_seqlen,
+            vlc.varlen_attn_bwd(self.g, self.qr, self.kr, self.v, self.o, self.lse, self.cu, w.max_seqlen,
                                 rope_theta=w.theta, dq=self.dq, dk=self.dk, dv=self.dv, workspace=self.ws_b,
-                                check=False, qk_rotated=once)
+                                check=False, qk_rotated=True)
         if ev is not None:
             ev[3].record()
 
@@ -402,7 +412,9 @@ def gpu_arm(args, w, world, rank, local):
         "kernels": kernels, "roofline": roofline, "roofline_fwd": roofline_fwd,
         "gpu_launches": launches_per_step(w, args.fwd_only, args.rope) * args.steps,
         "rope": ("q, k rotated once per step (vlc_rope_qk), both passes on the rotated operands"
-                 if args.rope == "once" else "RoPE inside the attention kernels (forward tiles, backward prep)"),
+                 if args.rope == "once" else
+                 "RoPE in the forward kernel (k rotated by its k pass, q tiles inside the kernel), which returns "
+                 "q', k'; the backward runs on them"),
         "clocks": clk.summary(),
         "e2e": e2e,
     }
@@ -953,9 +965,10 @@ def main():
     ap.add_argument("--workload", default="pt_bwd", choices=synth.WORKLOAD_NAMES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--rope", choices=("once", "fused"), default="once",
-                    help="once: the step rotates q, k by one pass and both directions run on q', k'; "
-                         "fused: the attention kernels rotate (forward tiles, backward prep pass)")
+    ap.add_argument("--rope", choices=("once", "fused"), default="fused",
+                    help="fused: RoPE in the forward kernel (k rotated by its k pass, the q tiles inside the "
+                         "kernel), which returns q', k' for the backward; once: the step rotates q, k by one "
+                         "pass and both directions run on q', k'")
     ap.add_argument("--fwd-only", action="store_true",
                     help="step = positions/labels + forward only (for profiling the forward kernel)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")

@@ -403,6 +403,24 @@ int vlc_rope_qk(const void* q, const void* k, const int32_t* cu, const int32_t* 
                 int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen, float rope_theta,
                 uint32_t flags, void* qrot, void* krot, void* ws, size_t ws_bytes, void* stream);
 
+/* The forward with RoPE in the kernel ("Sequence packing and variable-length
+ * attention", charlestar, sections "EOS is content; isolation happens before
+ * softmax" and "Positions are reset per segment") that also returns the rotated
+ * operands it attended with: qrot = R(p_i) q ([total, H, d]) and krot = R(p_i) k
+ * ([total, H_kv, d]), bf16, per-segment positions.  A training step then runs
+ * vlc_attn_bwd_ex with VLC_QK_ROTATED on qrot, krot (its prep pass computes
+ * rowsum(dO * O) alone) and needs no separate rotation pass: k is rotated by the
+ * pass that prepares it for the kernel (written to krot), and the kernel writes
+ * each q tile's rows as it rotates them.  o, lse, the other arguments and the
+ * device error word as in vlc_attn_fwd_gqa; flags: VLC_ROPE_INTERLEAVED.
+ * Self-attention, no padded layout; rope_theta > 0 (else VLC_ERR_ARG); qrot and
+ * krot device pointers, 16-byte aligned, owned by the caller.  Workspace:
+ * vlc_workspace_bytes_gqa(..., 0) (its optional rotated-k region is not used). */
+int vlc_attn_fwd_rot(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                     int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                     float softmax_scale, float rope_theta, uint32_t flags, void* o, float* lse,
+                     void* qrot, void* krot, void* ws, size_t ws_bytes, void* stream);
+
 /* Forward attention for callers that cannot allocate device memory.  No
  * counterpart on the pages: it exists for callers that may not obtain memory
  * per call, such as code running inside another runtime's execution hook (a

@@ -92,6 +92,14 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.vlc_lse_merge(parts, parts, 17, 4, 2, 128, dummy, dummy, None) == 1
     assert lib.vlc_rope_qk(dummy, dummy, dummy, None, 3, 9, 2, 2, 128, 4, 1e4, 0x2, dummy, dummy, dummy,
                            1 << 20, None) == 1
+    # the forward that returns q', k': both outputs, RoPE on, only the interleaved bit
+    fwd_rot = lambda qr, kr, theta, flags, d=128: lib.vlc_attn_fwd_rot(
+        dummy, dummy, dummy, dummy, 3, 9, 2, 2, d, 4, 0.0, theta, flags, dummy, dummy, qr, kr, dummy, 1 << 20, None)
+    assert fwd_rot(None, dummy, 1e4, 0) == 1
+    assert fwd_rot(dummy, None, 1e4, 0) == 1
+    assert fwd_rot(dummy, dummy, 0.0, 0) == 1
+    assert fwd_rot(dummy, dummy, 1e4, 0x2) == 1
+    assert fwd_rot(dummy, dummy, 1e4, 0x1, d=96) == 3   # the interleaved bit passes; d = 96 is unsupported
     assert lib.vlc_attn_bwd_ex(dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 3, 9, 2, 2, 128,
                                4, 0.0, 1e4, 0x80000000, dummy, dummy, dummy, dummy, 1 << 20, None) == 1
     # the interleaved bit itself is accepted: the call proceeds to the shape checks

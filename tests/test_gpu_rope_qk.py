@@ -93,3 +93,29 @@ def test_rotated_padded_layout(vlc):
     ref = oracle.attn_bwd(g.cpu(), q.cpu(), k.cpu(), v.cpu(), cu, cu_padded=cp)
     for a, b in zip((dq, dk, dv), ref):
         assert np.abs(a.float().cpu().numpy() - b).max() <= G_MAX
+
+
+@pytest.mark.parametrize("il", [False, True])
+def test_fwd_rot_returns_the_rotated_operands_for_the_backward(vlc, il):
+    # the forward with RoPE in the kernel also writes q' (from the kernel's q-tile rotation) and
+    # k' (from its k pass); the backward on them with qk_rotated matches the oracle, and k' is
+    # the rotation pass's k' bit for bit
+    lens = [700, 1, 333, 129, 2300]
+    w = synth.custom_workload(lens, 4, 128)
+    q, k, v, g = synth.make_tensors(w, seed=91, with_grad=True)
+    qd, kd, vd, gd = (t.to(DEV) for t in (q, k, v, g))
+    cu = torch.from_numpy(w.cu).to(DEV)
+    o, lse, qr, kr = vlc.varlen_attn_fwd_rot(qd, kd, vd, cu, w.max_seqlen, rope_interleaved=il)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.cu, interleaved=il)
+    e = o.float().cpu().numpy() - o_ref
+    assert np.abs(e).max() <= 2e-2 and np.abs(e).mean() <= 2e-3
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-3
+    qr1, kr1 = vlc.rope_qk(qd, kd, cu, w.max_seqlen, rope_interleaved=il)
+    assert torch.equal(kr, kr1)
+    # q' from the in-kernel rotation: the same rotation up to the angle recurrence's last bits
+    assert torch.allclose(qr.float(), qr1.float(), rtol=2.0 ** -7, atol=1e-6)
+    grads = vlc.varlen_attn_bwd(gd, qr, kr, vd, o, lse, cu, w.max_seqlen, qk_rotated=True, rope_interleaved=il)
+    ref = oracle.attn_bwd(g, q, k, v, w.cu, interleaved=il)
+    for name, a, b in zip(("dq", "dk", "dv"), grads, ref):
+        err = np.abs(a.float().cpu().numpy() - b)
+        assert np.isfinite(err).all() and err.max() <= 5e-2, (name, err.max())

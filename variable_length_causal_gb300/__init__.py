@@ -8,6 +8,8 @@ pipeline: loss sum and target count over the pre-shifted labels; ``pack`` and
 ``shard_packs`` are the host step before it (windows by first-fit decreasing,
 windows to ranks by sum of squared lengths); ``cp_partition``, ``cp_block_mode``,
 ``rope_pos`` and ``lse_merge`` split long segments over a context-parallel group.
+``varlen_attn_fwd_rot`` is the forward with RoPE in the kernel that also returns the rotated
+q', k' for a training step's backward.
 """
 from .binding import (  # noqa: F401
     Packing,
@@ -29,5 +31,6 @@ from .binding import (  # noqa: F401
     sum_parts,
     varlen_attn_bwd,
     varlen_attn_fwd,
+    varlen_attn_fwd_rot,
     workspace_bytes,
 )

@@ -42,7 +42,7 @@ EXPORTED = [
     "vlc_workspace_bytes_gqa", "vlc_attn_fwd_gqa", "vlc_attn_bwd_gqa", "vlc_attn_fwd_ex",
     "vlc_attn_bwd_ex", "vlc_workspace_bytes_qkv", "vlc_attn_fwd_qkv", "vlc_attn_bwd_qkv", "vlc_pack",
     "vlc_shard_packs", "vlc_rope_qk", "vlc_set_wait_limit_us", "vlc_cp_partition", "vlc_cp_block_mode",
-    "vlc_rope_pos_workspace_bytes", "vlc_rope_pos", "vlc_lse_merge", "vlc_sum_parts",
+    "vlc_rope_pos_workspace_bytes", "vlc_rope_pos", "vlc_lse_merge", "vlc_sum_parts", "vlc_attn_fwd_rot",
 ]
 
 _lock = threading.Lock()
@@ -134,6 +134,9 @@ def load_library(path: str = LIB_PATH):
         lib.vlc_attn_bwd_qkv.restype = cint
         lib.vlc_rope_qk.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, f32, u32, P, P, P, sz, P]
         lib.vlc_rope_qk.restype = cint
+        lib.vlc_attn_fwd_rot.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32, u32, P, P, P, P,
+                                         P, sz, P]
+        lib.vlc_attn_fwd_rot.restype = cint
         lib.vlc_pack.argtypes = [P, i64, i32, i32, cint, P, P, P, P, P]
         lib.vlc_pack.restype = cint
         lib.vlc_shard_packs.argtypes = [P, P, P, i64, i32, cint, P, P]
@@ -448,6 +451,35 @@ def rope_qk(q: torch.Tensor, k: torch.Tensor, cu_seqlens: torch.Tensor, max_seql
     if check:
         _raise_device_error(ws, "vlc_rope_qk")
     return qrot, krot
+
+
+def varlen_attn_fwd_rot(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                        max_seqlen: int, softmax_scale: Optional[float] = None, rope_theta: float = 10000.0,
+                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                        rotated_out=None, workspace: Optional[torch.Tensor] = None, check: bool = True,
+                        rope_interleaved: bool = False):
+    """The forward with RoPE in the kernel that also returns the rotated operands it attended
+    with: (O, LSE, q', k').  A training step runs varlen_attn_bwd(..., qk_rotated=True) on q', k'
+    and needs no separate rotation pass.  Self-attention, no padded layout, rope_theta > 0."""
+    lib = load_library()
+    _require_cuda(q, k, v, cu_seqlens)
+    H_kv = _check_qkv([q] + ([] if out is None else [out]), [k, v])
+    total, H, d = q.shape
+    nseg = _cu_info(cu_seqlens)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    qrot, krot = (torch.empty_like(q), torch.empty_like(k)) if rotated_out is None else rotated_out
+    for t, ref in ((qrot, q), (krot, k)):
+        if t.shape != ref.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("rotated outputs must be contiguous bf16 tensors shaped like q and k")
+    ws = new_workspace(nseg, total, H, d, max_seqlen, False, q.device, H_kv) if workspace is None else workspace
+    st = lib.vlc_attn_fwd_rot(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), nseg, total, H, H_kv, d, int(max_seqlen),
+                              _scale(softmax_scale, d), float(rope_theta), ROPE_INTERLEAVED if rope_interleaved else 0,
+                              _ptr(out), _ptr(lse), _ptr(qrot), _ptr(krot), _ptr(ws), ws.numel(), _stream(q.device))
+    _check(st, "vlc_attn_fwd_rot")
+    if check:
+        _raise_device_error(ws, "vlc_attn_fwd_rot")
+    return out, lse, qrot, krot
 
 
 class Packing(NamedTuple):

@@ -141,6 +141,7 @@ struct AttnArgs {
     void* ws;
     size_t ws_bytes;
     void* stream;
+    void *qrot_out, *krot_out;   // forward: also return R(p) q and R(p) k (vlc_attn_fwd_rot)
 };
 
 static int check_attn_args(const AttnArgs& a, int is_bwd) {
@@ -231,9 +232,11 @@ static int attn_fwd_impl(AttnArgs a) {
     // rotates only the q tiles, in its softmax warps; without the room, its RoPE warps rotate
     // every staged q and K tile
     p.krot = nullptr;
-    if (mode != kRopeNone && a.ws_bytes >= L.total) {
-        if (launch_rope_k(p, w + L.krot, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
-        p.krot = w + L.krot;
+    p.qrot_out = a.qrot_out;
+    void* krot = a.krot_out != nullptr ? a.krot_out : (a.ws_bytes >= L.total ? w + L.krot : nullptr);
+    if (mode != kRopeNone && krot != nullptr) {
+        if (launch_rope_k(p, krot, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
+        p.krot = krot;
     }
     if (launch_attn_fwd(p, num_sms_cached(), s) != cudaSuccess) return VLC_ERR_CUDA;
     return VLC_OK;
@@ -419,6 +422,19 @@ int vlc_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* 
                     uint32_t flags, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
     return attn_fwd_impl(fwd_args(q, k, v, cu, cu_padded, nullptr, nseg, total, 0, H, H_kv, d, max_seqlen, 0,
                                   softmax_scale, rope_theta, flags, o, lse, ws, ws_bytes, stream));
+}
+
+int vlc_attn_fwd_rot(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,
+                     int32_t total, int32_t H, int32_t H_kv, int32_t d, int32_t max_seqlen,
+                     float softmax_scale, float rope_theta, uint32_t flags, void* o, float* lse,
+                     void* qrot, void* krot, void* ws, size_t ws_bytes, void* stream) {
+    if (qrot == nullptr || krot == nullptr || !aligned(qrot, 16) || !aligned(krot, 16)) return VLC_ERR_ARG;
+    if (!(rope_theta > 0.f) || (flags & ~static_cast<uint32_t>(VLC_ROPE_INTERLEAVED))) return VLC_ERR_ARG;
+    AttnArgs a = fwd_args(q, k, v, cu, nullptr, nullptr, nseg, total, 0, H, H_kv, d, max_seqlen, 0, softmax_scale,
+                          rope_theta, flags, o, lse, ws, ws_bytes, stream);
+    a.qrot_out = qrot;
+    a.krot_out = krot;
+    return attn_fwd_impl(a);
 }
 
 int vlc_attn_fwd_gqa(const void* q, const void* k, const void* v, const int32_t* cu, int32_t nseg,

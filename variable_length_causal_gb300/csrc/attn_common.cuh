@@ -255,10 +255,13 @@ __device__ __forceinline__ RopeStep<D> rope_step(const float2* __restrict__ tabl
 // angle by complex multiplication with its RopeStep (a few 1e-7 of drift over
 // a tile).
 // BLK: bytes between the tile's 64-column blocks (ROWS x 128 B for a whole tile; a slice of
-// a taller tile passes the taller tile's block size).
+// a taller tile passes the taller tile's block size).  gdst (optional): the rotated rows
+// r < nvalid are also written to global memory, row r at gdst + r * gstride (bf16, D columns).
 template <int D, int ROWS, bool IL, uint32_t BLK = ROWS * 128u>
 __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2* __restrict__ table,
-                                          const RopeStep<D>& step, int wr, int lane) {
+                                          const RopeStep<D>& step, int wr, int lane,
+                                          uint8_t* __restrict__ gdst = nullptr, int64_t gstride = 0,
+                                          int nvalid = 0) {
     constexpr int half = D / 2;
     constexpr int PAIRS_PER_ROW = half / 8;            // threads per row
     constexpr int ROWS_PER_IT = 32 / PAIRS_PER_ROW;
@@ -305,6 +308,11 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, int pos0, const float2*
                      ::"r"(lo_addr), "r"(na[0]), "r"(na[1]), "r"(na[2]), "r"(na[3]) : "memory");
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                      ::"r"(hi_addr), "r"(nb[0]), "r"(nb[1]), "r"(nb[2]), "r"(nb[3]) : "memory");
+        if (gdst != nullptr && r < nvalid) {   // the same 16-byte chunks of the row-major row
+            uint8_t* row = gdst + r * gstride;
+            *reinterpret_cast<uint4*>(row + 16 * ci) = make_uint4(na[0], na[1], na[2], na[3]);
+            *reinterpret_cast<uint4*>(row + (D == 128 ? 128 : 64) + 16 * ci) = make_uint4(nb[0], nb[1], nb[2], nb[3]);
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {   // advance the angle by ROWS_PER_IT rows
             const float2 c = cs[q], sv = sn[q];

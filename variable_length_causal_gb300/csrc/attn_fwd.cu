@@ -539,10 +539,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (!wait_warp(bar(Q_FULL + qs % kQSlots), (qs / kQSlots) & 1, abort)) return false;
                     const uint32_t tile = sbase + LY::Q0 + (qs % kQSlots) * LY::TILE;
                     const int pos0 = (g.q0 + sub) * BQ + g.w.off;
+                    // with qrot_out the rotated rows of the segment also go to global memory
+                    const int64_t gstride = static_cast<int64_t>(p.H) * D * 2;
+                    uint8_t* gdst = p.qrot_out == nullptr ? nullptr
+                                    : static_cast<uint8_t*>(p.qrot_out) +
+                                          (static_cast<int64_t>(g.w.row0) + (g.q0 + sub) * BQ) * gstride +
+                                          static_cast<int64_t>(g.w.h) * D * 2;
+                    const int nvalid = g.w.L - (g.q0 + sub) * BQ;
                     if (p.use_rope == kRopeInterleaved)
-                        rope_tile<D, 128, true>(tile, pos0, p.table, rope_step<D, true>(p.table, lane), wq, lane);
+                        rope_tile<D, 128, true>(tile, pos0, p.table, rope_step<D, true>(p.table, lane), wq, lane,
+                                                gdst, gstride, nvalid);
                     else
-                        rope_tile<D, 128, false>(tile, pos0, p.table, rope_step<D, false>(p.table, lane), wq, lane);
+                        rope_tile<D, 128, false>(tile, pos0, p.table, rope_step<D, false>(p.table, lane), wq, lane,
+                                                 gdst, gstride, nvalid);
                     fence_proxy_async_smem();
                     mbar_arrive(bar(Q_READY + qs % kQSlots));
                 }

@@ -106,6 +106,7 @@ struct FwdParams {
     int32_t* err;
     const float2* table;       // RoPE cos/sin [rows][d/2], null if no RoPE
     const void* krot;          // R(p) k of every key row (rotated beforehand), or null
+    void* qrot_out;            // with krot: the kernel also writes R(p) q here (bf16 [total, H, d]), or null
     int32_t nseg, total, H, d;
     int32_t Hkv;               // key/value heads; query head h reads head h / (H / Hkv)
     int32_t total_kv;          // key/value rows (== total for self-attention)
