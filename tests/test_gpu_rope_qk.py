@@ -95,13 +95,13 @@ def test_rotated_padded_layout(vlc):
         assert np.abs(a.float().cpu().numpy() - b).max() <= G_MAX
 
 
-@pytest.mark.parametrize("il,hkv", [(False, 4), (True, 4), (False, 2)])
-def test_fwd_rot_returns_the_rotated_operands_for_the_backward(vlc, il, hkv):
+@pytest.mark.parametrize("il,hkv,d", [(False, 4, 128), (True, 4, 128), (False, 2, 128), (True, 4, 64)])
+def test_fwd_rot_returns_the_rotated_operands_for_the_backward(vlc, il, hkv, d):
     # the forward with RoPE in the kernel also writes q' (from the kernel's q-tile rotation) and
     # k' (from its k pass); the backward on them with qk_rotated matches the oracle, and k' is
     # the rotation pass's k' bit for bit (hkv < 4: grouped key/value heads)
     lens = [700, 1, 333, 129, 2300]
-    w = synth.custom_workload(lens, 4, 128)
+    w = synth.custom_workload(lens, 4, d)
     q, k, v, g = synth.make_tensors(w, seed=91, with_grad=True)
     k, v = k[:, :hkv].contiguous(), v[:, :hkv].contiguous()
     qd, kd, vd, gd = (t.to(DEV) for t in (q, k, v, g))
