@@ -74,8 +74,10 @@ __device__ __forceinline__ Unit decode_unit_warp(const int4* __restrict__ items,
 
 // All 32 lanes poll; succeed together or give up together (ctl as in mbar_wait).
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* ctl) {
-    const uint32_t lim = static_cast<uint32_t>(ctl[1]);
+    // the common case first: a completed phase costs one probe and one vote (the limit is read
+    // from shared memory only on the slow path, so the probe does not queue behind that load)
     if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+    const uint32_t lim = static_cast<uint32_t>(ctl[1]);
     const bool sleep = lim >= kWaitLimitUs;
     uint64_t t0 = 0;
     const int lane = threadIdx.x & 31;

@@ -78,8 +78,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // (and raises ctl[0]) if it did not within the limit ctl[1], or if another role
 // already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* ctl) {
-    const uint32_t lim = static_cast<uint32_t>(ctl[1]);
     if (mbar_test_wait(bar, parity)) return true;
+    const uint32_t lim = static_cast<uint32_t>(ctl[1]);
     const bool sleep = lim >= kWaitLimitUs;
     if (sleep) {
 #pragma unroll 1
